@@ -1,0 +1,177 @@
+"""GAAC oracle: ctypes access to the scalar C statement of the codec and of
+fp64 decode attention (``gaac_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library and never imports it.
+
+Source: "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference on
+Personal Devices", sections 3.1-3.3 and Appendix D (see ``gaac_oracle.c``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gaac_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libgaac_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+KIND_K, KIND_V = 0, 1
+D, BLOCK, TILE = 128, 64, 8192
+OFF_CODE, OFF_TAG, OFF_ESC = 8192, 11264, 11520
+ESC_CAP = 512
+SLOT_BYTES = 12032
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (plain C11, -O2)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if force or not fresh:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i32, i64 = ctypes.c_int, ctypes.c_int64
+            L.gaac_ref_storage_index.argtypes = [i32, i32, i32]
+            L.gaac_ref_storage_index.restype = i32
+            L.gaac_ref_best_window.argtypes = [P, i32]
+            L.gaac_ref_best_window.restype = i32
+            L.gaac_ref_calibrate.argtypes = [P, i64, i64, i32, P, P]
+            L.gaac_ref_calibrate.restype = None
+            L.gaac_ref_encode_tile.argtypes = [P, i32, P, P, P, P, i32]
+            L.gaac_ref_encode_tile.restype = i32
+            L.gaac_ref_decode_tile.argtypes = [P, i32, P, P, i32, P]
+            L.gaac_ref_decode_tile.restype = i32
+            L.gaac_ref_mode_counts.argtypes = [P, P]
+            L.gaac_ref_mode_counts.restype = None
+            L.gaac_ref_raw_tile.argtypes = [P, i32, P]
+            L.gaac_ref_raw_tile.restype = None
+            L.gaac_ref_unraw_tile.argtypes = [P, i32, P]
+            L.gaac_ref_unraw_tile.restype = None
+            L.gaac_ref_escape_bytes_of_mode.argtypes = [i32]
+            L.gaac_ref_escape_bytes_of_mode.restype = i32
+            L.gaac_ref_attention.argtypes = [P, P, P, i64, i64, i32, i32, ctypes.c_double, P, P, P]
+            L.gaac_ref_attention.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _u16(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.uint16))
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.uint8))
+
+
+def storage_index(kind: int, t: int, c: int) -> int:
+    return lib().gaac_ref_storage_index(kind, t, c)
+
+
+def best_window(hist, width: int) -> int:
+    h = np.ascontiguousarray(np.asarray(hist, dtype=np.uint64))
+    assert h.shape == (256,)
+    return lib().gaac_ref_best_window(_ptr(h), width)
+
+
+def calibrate(x) -> tuple[np.ndarray, np.ndarray]:
+    """x: uint16 [n_tok][n_heads][128] BF16 bits -> (base3, base4) uint8 [n_heads][128]."""
+    x = _u16(x)
+    n_tok, n_heads, d = x.shape
+    assert d == D
+    b3 = np.zeros((n_heads, D), np.uint8)
+    b4 = np.zeros((n_heads, D), np.uint8)
+    lib().gaac_ref_calibrate(_ptr(x), n_tok, n_heads * D, n_heads, _ptr(b3), _ptr(b4))
+    return b3, b4
+
+
+def encode_tile(tile, kind: int, base3, base4, forced=None, esc_cap: int = ESC_CAP):
+    """Encode a [64][128] BF16 tile.  Returns (image uint8 [11520+esc_cap], esc_len);
+    esc_len is -1 when the escape stream would exceed esc_cap."""
+    tile = _u16(tile).reshape(BLOCK, D)
+    b3, b4 = _u8(base3).reshape(D), _u8(base4).reshape(D)
+    img = np.zeros(OFF_ESC + esc_cap, np.uint8)
+    fp = 0
+    if forced is not None:
+        forced = _u8(forced).reshape(1024)
+        fp = _ptr(forced)
+    esc = lib().gaac_ref_encode_tile(_ptr(tile), kind, _ptr(b3), _ptr(b4), fp, _ptr(img), esc_cap)
+    return img, esc
+
+
+def decode_tile(img, kind: int, base3, base4, esc_limit: int | None = None):
+    """Decode a slot image.  Returns (tile uint16 [64][128], status) where status is the
+    escape byte count consumed (>= 0) or a negative error."""
+    img = _u8(img)
+    if esc_limit is None:
+        esc_limit = img.size - OFF_ESC
+    b3, b4 = _u8(base3).reshape(D), _u8(base4).reshape(D)
+    out = np.zeros((BLOCK, D), np.uint16)
+    st = lib().gaac_ref_decode_tile(_ptr(img), kind, _ptr(b3), _ptr(b4), esc_limit, _ptr(out))
+    return out, st
+
+
+def mode_counts(img) -> np.ndarray:
+    img = _u8(img)
+    out = np.zeros(4, np.int64)
+    lib().gaac_ref_mode_counts(_ptr(img), _ptr(out))
+    return out
+
+
+def raw_tile(tile, kind: int) -> np.ndarray:
+    tile = _u16(tile).reshape(BLOCK, D)
+    out = np.zeros(TILE, np.uint16)
+    lib().gaac_ref_raw_tile(_ptr(tile), kind, _ptr(out))
+    return out
+
+
+def unraw_tile(raw, kind: int) -> np.ndarray:
+    raw = _u16(raw).reshape(TILE)
+    out = np.zeros((BLOCK, D), np.uint16)
+    lib().gaac_ref_unraw_tile(_ptr(raw), kind, _ptr(out))
+    return out
+
+
+def escape_bytes_of_mode(mode: int) -> int:
+    return lib().gaac_ref_escape_bytes_of_mode(mode)
+
+
+def attention(q, k, v, scale: float):
+    """fp64 decode attention of one sequence.
+    q: uint16 [Hq][128]; k, v: uint16 [T][Hkv][128] (BF16 bits).
+    Returns (out float64 [Hq][128], flags int32 [Hq])."""
+    q = _u16(q)
+    k = _u16(k)
+    v = _u16(v)
+    Hq = q.shape[0]
+    T, Hkv, d = k.shape
+    assert d == D and v.shape == k.shape and Hq % Hkv == 0
+    out = np.zeros((Hq, D), np.float64)
+    flags = np.zeros(Hq, np.int32)
+    scratch = np.zeros(max(T, 1), np.float64)
+    lib().gaac_ref_attention(_ptr(q), _ptr(k), _ptr(v), Hkv * D, T, Hq, Hkv, float(scale), _ptr(out), _ptr(flags),
+                             _ptr(scratch))
+    return out, flags

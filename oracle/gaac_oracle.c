@@ -1,0 +1,324 @@
+/*
+ * GAAC oracle: a plain, scalar, slow CPU statement of the GAAC codec and of
+ * decode attention in fp64.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this file's library.  It shares no
+ * code, header, table or constant generator with the CUDA library; every
+ * constant below is restated here from the format definition.
+ *
+ * Source of the method: "GAAC: Lossless KV Compression for Bandwidth-Efficient
+ * LLM Inference on Personal Devices" (Guo, George, Joshi), summary page:
+ *   - section 3.1 (Lossless KV Compression): per-head-channel calibrated
+ *     exponent windows of length 8 and 16; groups of eight values use a 3-bit,
+ *     4-bit or raw exponent mode depending on whether every offset fits; an
+ *     out-of-window value widens the whole group; sign and mantissa are kept
+ *     unchanged.
+ *   - section 3.2 (Attention with On-the-Fly Decompression): compressed blocks
+ *     and the raw tail share one softmax.
+ *   - section 3.3 and Figure 3 (Block-Wise Compression Scheduling):
+ *     fixed-capacity slots, oversized blocks stay BF16, BF16 tail filled and
+ *     then finalized.
+ *   - Appendix D, Table 9 (Storage): 3-bit exponent codes, 2-bit mode tags,
+ *     escape bytes, fixed-capacity escape slots.
+ * The page gives no bit layout.  This file fixes one, "GAAC tile format v1",
+ * summarised below and spelled out rule by rule at the step that follows it.
+ *
+ * Format v1 in brief (all multi-byte fields little-endian):
+ *   tile        64 tokens x 128 channels of one (sequence, block, kv-head, K|V)
+ *   storage     K tiles: element (t,c) at s = t*128 + c   (token-major)
+ *   order       V tiles: element (t,c) at s = c*64  + t   (channel-major)
+ *   group       8 consecutive elements in storage order, G = s / 8
+ *   slot image  [0,8192)      sign|mantissa byte per element, at s
+ *               [8192,11264)  code plane: 3 words per 32-element unit
+ *               [11264,11520) tag plane: 2 bits per group
+ *               [11520,12032) escape area, capacity 512 bytes, zero filled
+ *   raw tile    8192 BF16 words in storage order
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORC_D 128               /* head_dim */
+#define ORC_BLOCK 64            /* tokens per tile */
+#define ORC_TILE 8192           /* elements per tile */
+#define ORC_GROUPS 1024         /* groups of 8 per tile */
+#define ORC_UNITS 256           /* 32-element code units per tile */
+#define ORC_OFF_CODE 8192
+#define ORC_OFF_TAG 11264
+#define ORC_OFF_ESC 11520
+#define ORC_ESC_CAP 512
+#define ORC_SLOT 12032
+
+enum { ORC_KIND_K = 0, ORC_KIND_V = 1 };
+enum { ORC_M3BIT = 0, ORC_M4BIT = 1, ORC_MRAW = 2 };
+
+/* ---- BF16 fields (section 3.1: sign and mantissa verbatim, exponent coded) */
+static unsigned bf16_exponent(uint16_t x) { return (x >> 7) & 0xFFu; }
+static unsigned bf16_signmant(uint16_t x) { return ((x >> 8) & 0x80u) | (x & 0x7Fu); }
+static uint16_t bf16_join(unsigned signmant, unsigned exponent) {
+    return (uint16_t)(((signmant & 0x80u) << 8) | ((exponent & 0xFFu) << 7) | (signmant & 0x7Fu));
+}
+
+/* ---- storage order of a tile (format v1) */
+int gaac_ref_storage_index(int kind, int t, int c) {
+    return kind == ORC_KIND_K ? t * ORC_D + c : c * ORC_BLOCK + t;
+}
+static void storage_to_tc(int kind, int s, int* t, int* c) {
+    if (kind == ORC_KIND_K) { *t = s / ORC_D; *c = s % ORC_D; }
+    else { *c = s / ORC_BLOCK; *t = s % ORC_BLOCK; }
+}
+static int channel_of(int kind, int s) { int t, c; storage_to_tc(kind, s, &t, &c); return c; }
+
+/* ---- calibration (section 3.1 and 4.7.1: windows of 8 and 16 exponents per
+ * head-channel, chosen from calibration data).  Window with the largest count;
+ * ties go to the smallest base. */
+static int best_window(const uint64_t* hist, int width) {
+    uint64_t best = 0;
+    int arg = 0;
+    int have = 0;
+    for (int b = 0; b + width <= 256; ++b) {
+        uint64_t sum = 0;
+        for (int i = 0; i < width; ++i) sum += hist[b + i];
+        if (!have || sum > best) { best = sum; arg = b; have = 1; }
+    }
+    return arg;
+}
+
+int gaac_ref_best_window(const uint64_t* hist, int width) { return best_window(hist, width); }
+
+/* x[t*tok_stride + h*128 + c] for t < n_tok; writes base3[h*128+c], base4[h*128+c]. */
+void gaac_ref_calibrate(const uint16_t* x, int64_t n_tok, int64_t tok_stride, int n_heads,
+                        uint8_t* base3, uint8_t* base4) {
+    for (int h = 0; h < n_heads; ++h) {
+        for (int c = 0; c < ORC_D; ++c) {
+            uint64_t hist[256];
+            memset(hist, 0, sizeof hist);
+            for (int64_t t = 0; t < n_tok; ++t) hist[bf16_exponent(x[t * tok_stride + h * ORC_D + c])] += 1;
+            base3[h * ORC_D + c] = (uint8_t)best_window(hist, 8);
+            base4[h * ORC_D + c] = (uint8_t)best_window(hist, 16);
+        }
+    }
+}
+
+/* ---- code plane location of code bit `bit` (0..2) of element s (format v1).
+ * Unit u = s/32 owns words W0(u), W1(u), W2(u), word Wk(u) stored at byte
+ * offset 8192 + 4*(k*256 + u).  Within the unit, j = s%32, half h = j/16,
+ * jj = j%16, byte lane L = jj%4, quad q = jj/4:
+ *   q=0: code bits 0..2 -> Wh, lane L, bits 0..2
+ *   q=1: code bits 0..2 -> Wh, lane L, bits 3..5
+ *   q=2: code bits 0..2 -> W2, lane L, bits 3h..3h+2
+ *   q=3: code bits 0..1 -> Wh, lane L, bits 6..7; code bit 2 -> W2, lane L, bit 6+h
+ * Returns the byte offset inside the slot image; *bitpos is the bit inside it. */
+static int code_bit_location(int s, int bit, int* bitpos) {
+    int u = s / 32, j = s % 32, h = j / 16, jj = j % 16, lane = jj % 4, q = jj / 4;
+    int word, pos;
+    if (q == 0) { word = h; pos = bit; }
+    else if (q == 1) { word = h; pos = 3 + bit; }
+    else if (q == 2) { word = 2; pos = 3 * h + bit; }
+    else if (bit < 2) { word = h; pos = 6 + bit; }
+    else { word = 2; pos = 6 + h; }
+    *bitpos = pos;
+    return ORC_OFF_CODE + 4 * (word * ORC_UNITS + u) + lane;
+}
+
+static void put_code(uint8_t* img, int s, unsigned code) {
+    for (int b = 0; b < 3; ++b) {
+        int pos;
+        int at = code_bit_location(s, b, &pos);
+        if ((code >> b) & 1u) img[at] |= (uint8_t)(1u << pos);
+    }
+}
+
+static unsigned get_code(const uint8_t* img, int s) {
+    unsigned code = 0;
+    for (int b = 0; b < 3; ++b) {
+        int pos;
+        int at = code_bit_location(s, b, &pos);
+        code |= ((img[at] >> pos) & 1u) << b;
+    }
+    return code;
+}
+
+/* ---- tag plane: group G's 2-bit mode at byte 11264 + G/4, bits 2*(G%4). */
+static void put_tag(uint8_t* img, int G, unsigned mode) {
+    img[ORC_OFF_TAG + G / 4] |= (uint8_t)((mode & 3u) << (2 * (G % 4)));
+}
+static unsigned get_tag(const uint8_t* img, int G) { return (img[ORC_OFF_TAG + G / 4] >> (2 * (G % 4))) & 3u; }
+
+/* ---- mode rule (section 3.1): 3-bit if every offset from base3 is in [0,7],
+ * else 4-bit if every offset from base4 is in [0,15], else raw. */
+static unsigned choose_mode(const unsigned* e, const unsigned* b3, const unsigned* b4) {
+    int fits3 = 1, fits4 = 1;
+    for (int j = 0; j < 8; ++j) {
+        int o3 = (int)e[j] - (int)b3[j];
+        int o4 = (int)e[j] - (int)b4[j];
+        if (o3 < 0 || o3 > 7) fits3 = 0;
+        if (o4 < 0 || o4 > 15) fits4 = 0;
+    }
+    return fits3 ? ORC_M3BIT : (fits4 ? ORC_M4BIT : ORC_MRAW);
+}
+
+static int escape_bytes_of_mode(unsigned mode) { return mode == ORC_M3BIT ? 0 : (mode == ORC_M4BIT ? 1 : 5); }
+int gaac_ref_escape_bytes_of_mode(int mode) { return escape_bytes_of_mode((unsigned)mode); }
+
+/*
+ * Encode one full tile.  `tile` is the tile in logical order [64 tokens][128
+ * channels]; b3/b4 are the 128 per-channel bases of this (kv-head, K|V).
+ * `forced` (NULL or 1024 modes) overrides the mode rule, for tests only.
+ * `img` receives the slot image; it must hold 11520 + img_esc_cap bytes.
+ * Returns the escape length in bytes, or -1 if it exceeds img_esc_cap (the
+ * image is then incomplete).  Unused escape bytes stay zero.
+ */
+int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, const uint8_t* base4,
+                         const uint8_t* forced, uint8_t* img, int img_esc_cap) {
+    memset(img, 0, (size_t)(ORC_OFF_ESC + img_esc_cap));
+    uint16_t seq[ORC_TILE];
+    for (int t = 0; t < ORC_BLOCK; ++t)
+        for (int c = 0; c < ORC_D; ++c) seq[gaac_ref_storage_index(kind, t, c)] = tile[t * ORC_D + c];
+
+    for (int s = 0; s < ORC_TILE; ++s) img[s] = (uint8_t)bf16_signmant(seq[s]);
+
+    int esc = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned e[8], b3[8], b4[8];
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j;
+            e[j] = bf16_exponent(seq[s]);
+            b3[j] = base3[channel_of(kind, s)];
+            b4[j] = base4[channel_of(kind, s)];
+        }
+        unsigned mode = forced ? forced[G] : choose_mode(e, b3, b4);
+        put_tag(img, G, mode);
+        uint8_t escb[5] = {0, 0, 0, 0, 0};
+        for (int j = 0; j < 8; ++j) {
+            unsigned code;
+            if (mode == ORC_M3BIT) {
+                code = (e[j] - b3[j]) & 7u;
+            } else if (mode == ORC_M4BIT) {
+                unsigned off = (e[j] - b4[j]) & 0xFFu;
+                code = off & 7u;
+                escb[0] |= (uint8_t)(((off >> 3) & 1u) << j);
+            } else {
+                code = e[j] & 7u;
+                for (int k = 0; k < 5; ++k) escb[k] |= (uint8_t)(((e[j] >> (3 + k)) & 1u) << j);
+            }
+            put_code(img, 8 * G + j, code);
+        }
+        int nb = escape_bytes_of_mode(mode);
+        if (esc + nb > img_esc_cap) return -1;
+        for (int k = 0; k < nb; ++k) img[ORC_OFF_ESC + esc + k] = escb[k];
+        esc += nb;
+    }
+    return esc;
+}
+
+/*
+ * Decode one slot image into the logical tile [64][128].
+ * Returns the number of escape bytes consumed, or -1 on a reserved tag (3),
+ * or -2 if the escape stream would run past esc_limit bytes.
+ */
+int gaac_ref_decode_tile(const uint8_t* img, int kind, const uint8_t* base3, const uint8_t* base4,
+                         int esc_limit, uint16_t* tile) {
+    int off = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = get_tag(img, G);
+        if (mode == 3u) return -1;
+        int nb = escape_bytes_of_mode(mode);
+        if (off + nb > esc_limit) return -2;
+        const uint8_t* escb = img + ORC_OFF_ESC + off;
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j;
+            int c = channel_of(kind, s);
+            unsigned code = get_code(img, s), e;
+            if (mode == ORC_M3BIT) {
+                e = base3[c] + code;
+            } else if (mode == ORC_M4BIT) {
+                e = base4[c] + (code | (((escb[0] >> j) & 1u) << 3));
+            } else {
+                unsigned hi = 0;
+                for (int k = 0; k < 5; ++k) hi |= ((escb[k] >> j) & 1u) << k;
+                e = code | (hi << 3);
+            }
+            int t, cc;
+            storage_to_tc(kind, s, &t, &cc);
+            tile[t * ORC_D + cc] = bf16_join(img[s], e);
+        }
+        off += nb;
+    }
+    return off;
+}
+
+/* Per-mode group counts of an encoded tile (diagnostics of section 4.7.1). */
+void gaac_ref_mode_counts(const uint8_t* img, int64_t* counts4) {
+    for (int m = 0; m < 4; ++m) counts4[m] = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) counts4[get_tag(img, G)] += 1;
+}
+
+/* Raw fallback image (section 3.3): the BF16 words in storage order. */
+void gaac_ref_raw_tile(const uint16_t* tile, int kind, uint16_t* raw) {
+    for (int t = 0; t < ORC_BLOCK; ++t)
+        for (int c = 0; c < ORC_D; ++c) raw[gaac_ref_storage_index(kind, t, c)] = tile[t * ORC_D + c];
+}
+void gaac_ref_unraw_tile(const uint16_t* raw, int kind, uint16_t* tile) {
+    for (int t = 0; t < ORC_BLOCK; ++t)
+        for (int c = 0; c < ORC_D; ++c) tile[t * ORC_D + c] = raw[gaac_ref_storage_index(kind, t, c)];
+}
+
+/* ---- decode attention in fp64 (section 3.2; grouped-query heads share a
+ * kv-head, q head h reads kv-head h / (Hq/Hkv)).
+ * q[hq*128 + c]; k, v: element (t, hk, c) at t*tok_stride + hk*128 + c.
+ * out[hq*128 + c] = sum_t softmax_t(scale * q.k_t) v_t[c]; T == 0 gives zeros.
+ * flags (may be NULL), per q head: bit 0 set if some token's sum_c |q_c k_tc|
+ * reaches 2^130 (a dot product of q/16 and k, or its product with the scale,
+ * may then leave the fp32 range); bit 1 set if some channel's sum_t w_t |v_tc|
+ * (w_t = the unnormalised softmax weight, at most 1) exceeds the largest fp32
+ * value (an fp32 accumulator may then overflow).  Such rows are not
+ * comparable with an fp32 kernel and are reported apart. */
+static double bf16_to_double(uint16_t x) {
+    uint32_t u = (uint32_t)x << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+void gaac_ref_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t tok_stride, int64_t T,
+                        int Hq, int Hkv, double scale, double* out, int32_t* flags, double* logits_scratch) {
+    int r = Hq / Hkv;
+    for (int hq = 0; hq < Hq; ++hq) {
+        int hk = hq / r;
+        int32_t flag = 0;
+        for (int c = 0; c < ORC_D; ++c) out[hq * ORC_D + c] = 0.0;
+        if (T == 0) { if (flags) flags[hq] = 0; continue; }
+        double m = -INFINITY;
+        for (int64_t t = 0; t < T; ++t) {
+            double dot = 0.0, mag = 0.0;
+            for (int c = 0; c < ORC_D; ++c) {
+                double qc = bf16_to_double(q[hq * ORC_D + c]);
+                double kc = bf16_to_double(k[t * tok_stride + hk * ORC_D + c]);
+                dot += qc * kc;
+                mag += fabs(qc * kc);
+            }
+            if (mag >= ldexp(1.0, 130)) flag |= 1;
+            logits_scratch[t] = scale * dot;
+            if (logits_scratch[t] > m) m = logits_scratch[t];
+        }
+        double l = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            double w = exp(logits_scratch[t] - m);
+            logits_scratch[t] = w;
+            l += w;
+        }
+        for (int c = 0; c < ORC_D; ++c) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                double vc = bf16_to_double(v[t * tok_stride + hk * ORC_D + c]);
+                acc += logits_scratch[t] * vc;
+                mag += logits_scratch[t] * fabs(vc);
+            }
+            if (mag > 3.4028234663852886e38) flag |= 2;
+            out[hq * ORC_D + c] = acc / l;
+        }
+        if (flags) flags[hq] = flag;
+    }
+}
