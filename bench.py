@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Decode-step attention over a GAAC-compressed BF16 KV cache on GB300.
+
+One step = decode attention for all 36 layers of a Qwen3-8B-shaped model
+(32 query / 8 kv heads, head_dim 128, batch 1) at 65,536 cached tokens, read
+from the resident compressed cache (block 64, calibration on the first 512
+tokens), as in the GAAC page's section 4.4 setting (64K context, batch 1).
+
+Prints one JSON line (rank 0).  Default: N=1, 20 timed steps after 5 warm-up.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gaac|reference]
+--impl reference times the CPU oracle (scalar C decode + fp64 attention) on a
+bounded sample of the same workload, scaled to one step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & achieved HBM GB/s at 64K ctx; encode GB/s; ratio"
+UNIT = "us/step"
+WORKLOAD = "Qwen3-8B-shaped decode attention: 36 layers, batch 1, 32q/8kv, head_dim 128, T=65536, block 64"
+CONFIG_ID = 1
+
+
+# DRAM bytes (read + write) of one attn_split_kernel launch on this workload, from an
+# ncu capture, valid only for the kernel source it was taken on (see profiles/).
+NCU_TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+
+
+def kernel_sha() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("attention.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "lossless_compressed_kv_gaac_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="gaac", choices=["gaac", "reference"])
+    p.add_argument("--layers", type=int, default=36, help="layers per step (36 = the Qwen3-8B workload)")
+    p.add_argument("--cpu-units", type=int, default=6, help="(layer, kv-head) units in the CPU oracle sample")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ---------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ workload -----
+def build_layers(n_layers: int, device, raw: bool):
+    """Compressed (or all-raw) caches of n_layers layers, plus the per-layer queries."""
+    import torch
+
+    import gaac_workloads as W
+    from lossless_compressed_kv_gaac_gb300.cache import LayerCache
+
+    wl = W.WORKLOADS[CONFIG_ID]
+    T, H, Hq = wl.seq_len, wl.n_kv_heads, wl.n_q_heads
+    caches, qs = [], []
+    lens = torch.tensor([T], dtype=torch.int32, device=device)
+    for layer in range(n_layers):
+        k, v = W.make_kv(CONFIG_ID, layer, 1, T, H, device=device)
+        c = LayerCache(1, H, T // 64, device=device, n_slots=0 if raw else None, n_raw=T // 64 * H * 2 if raw else 256)
+        c.calibrate(k[0, :wl.n_calib], v[0, :wl.n_calib])
+        c.encode(k, v, lens, raw=raw)
+        caches.append(c)
+        qs.append(W.make_q(CONFIG_ID, layer, 1, Hq, device=device))
+        del k, v
+    torch.cuda.synchronize()
+    for c in caches:
+        assert int(c.status.item()) == 0, "encode reported an error"
+    return caches, qs
+
+
+def algorithmic_bytes(cache) -> int:
+    """Bytes the method must read for one attention launch over this layer: per slot tile the
+    planes (11,520 B) plus its escape bytes, per raw tile 16,384 B, plus 8 B per table entry and
+    the query (read) and output (written)."""
+    import torch
+
+    _, esc, mode, _ = cache.fields()
+    slot = mode == 0
+    raw = mode == 1
+    n = int(slot.sum().item()) * 11520 + int(esc[slot].sum().item()) + int(raw.sum().item()) * 16384
+    n += int((slot | raw).sum().item()) * 8
+    return n
+
+
+def time_graph(g, stream, steps: int):
+    """Replays the graph `steps` times on `stream`; CUDA-event time on that stream (ms)."""
+    import torch
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            g.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end)
+
+
+def run_gaac(args):
+    import torch
+
+    import gaac_workloads as W
+    import lossless_compressed_kv_gaac_gb300 as G
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    wl = W.WORKLOADS[CONFIG_ID]
+    L = args.layers
+    scale = wl.scale
+    stream = torch.cuda.Stream(device)
+
+    # ---- build the compressed cache of every layer (encode timed on layer 0)
+    caches, qs = build_layers(L, device, raw=False)
+    outs = [torch.empty((1, wl.n_q_heads, 128), dtype=torch.float32, device=device) for _ in range(L)]
+    c0 = caches[0]
+    k0, v0 = W.make_kv(CONFIG_ID, 0, 1, wl.seq_len, wl.n_kv_heads, device=device)
+    lens = torch.tensor([wl.seq_len], dtype=torch.int32, device=device)
+    enc_t = []
+    for i in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        c0.encode(k0, v0, lens)
+        e1.record()
+        e1.synchronize()
+        if i:
+            enc_t.append(e0.elapsed_time(e1))
+    raw_bytes_layer = 2 * wl.seq_len * wl.n_kv_heads * 128 * 2
+    encode_gbs = raw_bytes_layer / (min(enc_t) * 1e-3) / 1e9
+    dec_t = []
+    kd = torch.empty_like(k0)
+    vd = torch.empty_like(v0)
+    for i in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        G.decompress(c0.table, c0.seq_lens, c0.pools, c0.base3, c0.base4, kd, vd)
+        e1.record()
+        e1.synchronize()
+        if i:
+            dec_t.append(e0.elapsed_time(e1))
+    assert torch.equal(kd.view(torch.int16), k0.view(torch.int16)) and torch.equal(vd.view(torch.int16), v0.view(torch.int16))
+    decompress_gbs = raw_bytes_layer / (min(dec_t) * 1e-3) / 1e9
+    st = G.stats_dict(c0.stats)
+    del k0, v0, kd, vd
+    alg = [algorithmic_bytes(c) for c in caches]
+    alg_step = sum(alg)
+    raw_step = raw_bytes_layer * L
+    res = [c.resident_bytes() for c in caches]
+    resident_step = sum(r["slot_bytes"] + r["raw_bytes"] + r["table_bytes"] for r in res)
+    payload_ratio = raw_step / (alg_step - sum(r["table_bytes"] for r in res))
+    resident_ratio = raw_step / resident_step
+
+    # ---- one step: all layers, captured in a CUDA graph
+    def step():
+        for c, q, o in zip(caches, qs, outs):
+            c.attention(q, scale, out=o)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()  # first calls set kernel attributes outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(vis.split(",")[local] if vis else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    ms = time_graph(g, stream, args.steps)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    for c in caches:
+        assert int(c.status.item()) == 0
+    ms_per_step = ms / args.steps
+
+    # ---- per-launch duration of the attention call (split + combine), eager, same stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    per_launch = []
+    for rep in range(3):
+        with torch.cuda.stream(stream):
+            for (e0, e1), c, q, o in zip(ev, caches, qs, outs):
+                e0.record(stream)
+                c.attention(q, scale, out=o)
+                e1.record(stream)
+        stream.synchronize()
+        per_launch.append(sum(e0.elapsed_time(e1) for e0, e1 in ev) / L)
+    launch_ms = min(per_launch)
+    alg_launch = alg_step / L
+    achieved_gbs = alg_launch / (launch_ms * 1e-3) / 1e9
+
+    # ---- uncompressed BF16 baseline: the same kernel over an all-raw cache
+    bf16_ms = None
+    try:
+        raw_caches, _ = build_layers(L, device, raw=True)
+
+        def step_raw():
+            for c, q, o in zip(raw_caches, qs, outs):
+                c.attention(q, scale, out=o)
+
+        with torch.cuda.stream(stream):
+            step_raw()
+        torch.cuda.synchronize()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            step_raw()
+        bf16_ms = time_graph(g2, stream, args.steps) / args.steps
+        del raw_caches, g2
+    except torch.cuda.OutOfMemoryError:
+        bf16_ms = None
+    torch.cuda.empty_cache()
+
+    # ---- end to end through the public API: pinned host q in, host out back, every step
+    q_host = torch.stack([q for q in qs]).cpu().pin_memory()
+    out_host = torch.empty((L, 1, wl.n_q_heads, 128), dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(q_host, device=device)
+    out_dev = torch.empty((L, 1, wl.n_q_heads, 128), dtype=torch.float32, device=device)
+
+    def step_e2e():
+        q_dev.copy_(q_host, non_blocking=True)
+        for i, c in enumerate(caches):
+            c.attention(q_dev[i], scale, out=out_dev[i])
+        out_host.copy_(out_dev, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step_e2e()
+    torch.cuda.synchronize()
+    g3 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g3, stream=stream):
+        step_e2e()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g3.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            g3.replay()
+            stream.synchronize()  # the host reads the result every step
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["kernel_sha"] == kernel_sha() else None
+
+    result = {
+        "metric": METRIC,
+        "value": round(ms_per_step * 1e3 / world, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; lognormal channel scales, 4 x20 outlier key channels per head)",
+        "config": {"workload": WORKLOAD, "layers": L, "batch": 1, "seq_len": wl.seq_len, "q_heads": wl.n_q_heads,
+                   "kv_heads": wl.n_kv_heads, "head_dim": 128, "block": 64, "calibration_tokens": wl.n_calib,
+                   "l2": "inputs larger than L2 (%.2f GB compressed per step)" % (alg_step / 1e9),
+                   "replicas": "each rank runs the whole workload" if world > 1 else "single GPU"},
+        "hbm_gbs_compressed": round(alg_step / (ms_per_step * 1e-3) / 1e9, 1),
+        "equiv_uncompressed_gbs": round(raw_step / (ms_per_step * 1e-3) / 1e9, 1),
+        "bf16_cache_us_per_step": round(bf16_ms * 1e3, 2) if bf16_ms else None,
+        "speedup_vs_bf16_cache": round(bf16_ms / ms_per_step, 3) if bf16_ms else None,
+        "encode_gbs": round(encode_gbs, 1),
+        "decompress_gbs": round(decompress_gbs, 1),
+        "ratio": {"payload": round(payload_ratio, 4), "resident": round(resident_ratio, 4),
+                  "mode_shares": [round(st[f"groups{m}"] / max(1, 1024 * st["slot_tiles"]), 5) for m in range(3)]},
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved_gbs / peak, 4), "traffic": traffic,
+                     "kernel": "attn_split_kernel (+ attn_combine_kernel in the timed call)",
+                     "peak_source": peak_src, "launch_us": round(launch_ms * 1e3, 2),
+                     "algorithmic_bytes_per_launch": alg_launch},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_ms * 1e3 / world, 2), "unit": UNIT, "h2d_bytes_per_step": q_host.numel() * 2,
+                "d2h_bytes_per_step": out_host.numel() * 4},
+        "gpu_launches": 2 * L * args.steps,
+    }
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_units, L)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# --------------------------------------------------------------- oracle ----
+class OracleSample:
+    """The oracle as it stands, on the host cores: scalar C tile decode plus fp64
+    attention over one (layer, kv-head) unit of the workload (1,024 K and 1,024 V
+    tiles decoded, 4 query heads over 65,536 tokens).  The unit's tiles are
+    encoded by the oracle itself, untimed."""
+
+    def __init__(self, units: int):
+        import numpy as np
+
+        import gaac_workloads as W
+        import oracle as O
+
+        wl = W.WORKLOADS[CONFIG_ID]
+        self.T, self.H, self.r, self.scale = wl.seq_len, wl.n_kv_heads, wl.n_q_heads // wl.n_kv_heads, wl.scale
+        self.units = []
+        layer_data = {}
+        for u in range(units):
+            layer, h = u // self.H, u % self.H
+            if layer not in layer_data:
+                k, v = W.make_kv(CONFIG_ID, layer, 1, self.T, self.H)
+                kn = W.bits(k).numpy().view(np.uint16)[0]
+                vn = W.bits(v).numpy().view(np.uint16)[0]
+                q = W.bits(W.make_q(CONFIG_ID, layer, 1, wl.n_q_heads)).numpy().view(np.uint16)[0]
+                layer_data = {layer: (kn, vn, q, O.calibrate(kn[:512]), O.calibrate(vn[:512]))}
+            kn, vn, q, (b3k, b4k), (b3v, b4v) = layer_data[layer]
+            imgs = []
+            for blk in range(self.T // 64):
+                for kind, x, b3, b4 in ((0, kn, b3k, b4k), (1, vn, b3v, b4v)):
+                    img, e = O.encode_tile(x[blk * 64:(blk + 1) * 64, h], kind, b3[h], b4[h])
+                    imgs.append((kind, img, e, blk, b3[h].copy(), b4[h].copy()))
+            self.units.append((imgs, q[h * self.r:(h + 1) * self.r].copy()))
+
+    def run(self, u: int) -> float:
+        """Seconds for unit u: decode its tiles, then fp64 attention."""
+        import numpy as np
+
+        import oracle as O
+
+        imgs, q = self.units[u]
+        kd = np.zeros((self.T, 1, 128), np.uint16)
+        vd = np.zeros((self.T, 1, 128), np.uint16)
+        t0 = time.perf_counter()
+        for kind, img, e, blk, b3, b4 in imgs:
+            tile, _ = O.decode_tile(img, kind, b3, b4, e)
+            (kd if kind == 0 else vd)[blk * 64:(blk + 1) * 64, 0] = tile
+        O.attention(q, kd, vd, self.scale)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(units: int, n_layers: int) -> dict:
+    """Oracle time for `units` (layer, kv-head) units, scaled to n_layers x 8 kv-heads."""
+    smp = OracleSample(units)
+    total = sum(smp.run(u) for u in range(units))
+    step_us = total / units * n_layers * smp.H * 1e6
+    return {"value": round(step_us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{units} (layer, kv-head) units: decode 2x1024 tiles + fp64 attention for {smp.r} query heads "
+                      f"over {smp.T} tokens each, {total:.1f} s single-threaded, scaled x{n_layers * smp.H / units:.0f} "
+                      "to one step"}
+
+
+def run_reference(args):
+    """The oracle arm: each step times one (layer, kv-head) unit, scaled to a full step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    smp = OracleSample(1)
+    for _ in range(args.warmup):
+        smp.run(0)
+    steps_us = [smp.run(0) * args.layers * smp.H * 1e6 for _ in range(args.steps)]
+    v = statistics.median(steps_us)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": args.layers},
+        "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "1 (layer, kv-head) unit per step (decode 2x1024 tiles + fp64 attention, "
+                                   f"4 heads x 65536 tokens), scaled to {args.layers} layers x 8 kv-heads"},
+        "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gaac(args)
+
+
+if __name__ == "__main__":
+    main()

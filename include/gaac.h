@@ -1,0 +1,211 @@
+/*
+ * gaac.h — C ABI of the GAAC compressed-KV decode-attention library (GB300, sm_103a).
+ *
+ * Method: "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference on
+ * Personal Devices" (Guo, George, Joshi).  The cache keeps each BF16 value's sign
+ * and mantissa verbatim and codes its exponent as a calibrated per-channel base
+ * plus a 3-bit or 4-bit offset, or raw, chosen per group of eight (section 3.1);
+ * 64-token blocks are packed into fixed-capacity slots, oversized blocks and the
+ * open tail stay BF16 (section 3.3, Figure 3); attention rebuilds tiles on the fly
+ * instead of decompressing the cache (section 3.2).
+ *
+ * Conventions shared by every entry point
+ *  - All array arguments are DEVICE pointers owned by the caller, except where a
+ *    comment says host.  The library allocates no memory.
+ *  - Calls enqueue work on `stream` and return at once.  The return value reports
+ *    argument errors found on the host (GAAC_EINVAL) and launch failures
+ *    (GAAC_ECUDA); nothing is enqueued when it is not GAAC_OK.
+ *  - Errors found by kernels are written to `*d_status` (device int32, may be
+ *    NULL): the first nonzero code wins (atomic compare-and-swap from 0).  Kernels
+ *    never trap and never wait without a bound.  Read it after synchronising.
+ *  - BF16 values are passed as their uint16_t bit patterns.
+ *  - head_dim is 128 and the block is 64 tokens (format v1 below).
+ *
+ * Tile format v1 (identical in the CUDA library and in the test oracle):
+ *  tile        64 tokens x 128 channels of one (layer, sequence, block, kv-head, K|V)
+ *  order       K tiles token-major  (element (t,c) at s = t*128 + c),
+ *              V tiles channel-major (element (t,c) at s = c*64 + t)
+ *  group       8 consecutive elements in that order (G = s/8)
+ *  slot image  GAAC_SLOT_BYTES bytes:
+ *               [0,8192)      sign|mantissa byte of element s at byte s
+ *               [8192,11264)  3-bit codes: word k (0..2) of 32-element unit u at
+ *                             8192 + 4*(k*256 + u)
+ *               [11264,11520) 2-bit mode of group G at byte 11264 + G/4, bits 2*(G%4)
+ *               [11520,12032) escape bytes (mode 1: 1 byte, mode 2: 5 bytes per
+ *                             group, in group order), zero filled
+ *  raw tile    8192 BF16 words in the same storage order
+ */
+#ifndef GAAC_H
+#define GAAC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GAAC_API __attribute__((visibility("default")))
+#else
+#define GAAC_API
+#endif
+
+#define GAAC_HEAD_DIM 128
+#define GAAC_BLOCK 64
+#define GAAC_TILE_ELEMS 8192
+#define GAAC_SLOT_BYTES 12032
+#define GAAC_ESC_CAPACITY 512
+#define GAAC_RAW_TILE_BYTES 16384
+#define GAAC_MAX_GQA 8 /* query heads per kv-head supported by decode attention */
+
+/* Status codes (return values and *d_status). */
+enum {
+  GAAC_OK = 0,
+  GAAC_EINVAL = 1,   /* bad argument (host) or bad base / length (device) */
+  GAAC_EPOOL = 2,    /* raw-tile free list or slot index out of range */
+  GAAC_EFORMAT = 3,  /* reserved mode tag, bad table entry, escape past its length */
+  GAAC_ECUDA = 4,    /* a CUDA launch failed */
+  GAAC_ETIMEOUT = 5  /* a bounded wait inside a kernel gave up (data of that launch invalid) */
+};
+
+/* Table entry modes. */
+enum { GAAC_MODE_SLOT = 0, GAAC_MODE_RAW = 1, GAAC_MODE_NONE = 255 };
+
+/* Slot-table entry (section 3.3: a table keeps, per block, whether it is
+ * compressed or raw and where it lives).  One per (sequence, block, kv-head, K|V) of a layer, laid out
+ * table[batch][max_blocks][n_kv_heads][2]  (last index 0 = K, 1 = V). */
+typedef struct gaac_entry {
+  uint32_t index;   /* slot index (mode SLOT) or raw-tile index (mode RAW) */
+  uint16_t esc_len; /* escape bytes used in the slot (mode SLOT) */
+  uint8_t mode;     /* GAAC_MODE_* */
+  uint8_t n_tok;    /* tokens held: 64 for a sealed block, fewer for the open tail */
+} gaac_entry;
+
+/* Storage of one layer's compressed cache (all device pointers). */
+typedef struct gaac_pools {
+  uint8_t* slot_pool;       /* [n_slots][GAAC_SLOT_BYTES] */
+  int64_t n_slots;
+  uint16_t* raw_pool;       /* [n_raw][GAAC_TILE_ELEMS] */
+  int64_t n_raw;
+  const uint32_t* raw_free; /* free raw-tile indices, popped at raw_free[*raw_cursor]; NULL = identity list */
+  int64_t n_raw_free;       /* length of the free list (identity list: n_raw) */
+  uint32_t* raw_cursor;     /* device counter of popped entries */
+} gaac_pools;
+
+/* Optional encoder counters (device, accumulated with atomics). */
+typedef struct gaac_stats {
+  unsigned long long groups[4];     /* groups per mode tag 0..3 in encoded slots */
+  unsigned long long escape_bytes;  /* sum of esc_len over encoded slots */
+  unsigned long long slot_tiles;    /* tiles stored compressed */
+  unsigned long long raw_tiles;     /* full tiles that fell back to BF16 */
+  unsigned long long tail_tiles;    /* partial (open) tiles written as BF16 */
+} gaac_stats;
+
+/* Human-readable name of a status code (static string). */
+GAAC_API const char* gaac_strerror(int status);
+
+/* Library version of the tile format and of the ABI. */
+GAAC_API int gaac_format_version(void);
+
+/*
+ * Calibration (section 3.1: each head-channel gets a window of 8 and a window
+ * of 16 exponents, fixed from calibration data; section 4.7.1).  For each kv-head h and channel c, counts
+ * the exponents of x[t*tok_stride + h*128 + c] over t < n_tok and picks
+ *   base3[h*128+c] = argmax_{b in [0,248]} sum_{i<8}  count[b+i]
+ *   base4[h*128+c] = argmax_{b in [0,240]} sum_{i<16} count[b+i]
+ * (ties: smallest b).  Call once for K and once for V.
+ * x: BF16 bits, tok_stride in elements (>= n_kv_heads*128).  1 <= n_tok <= 65535.
+ */
+GAAC_API int gaac_calibrate(const uint16_t* x, int64_t n_tok, int64_t tok_stride, int n_kv_heads, uint8_t* base3,
+                   uint8_t* base4, int32_t* d_status, void* stream);
+
+/*
+ * Block encoder for prefill (section 3.3: at prefill the full blocks are
+ * compressed and the partial last block is kept as BF16).  For every sequence b
+ * with length seq_lens[b] and every kv-head and K|V:
+ *  - each complete block is encoded into slot slot_ids[((b*max_blocks+blk)*H+h)*2+kv]
+ *    (mode SLOT), or, if its escape stream exceeds GAAC_ESC_CAPACITY, copied as a
+ *    raw tile popped from the raw free list (mode RAW; that slot stays unused);
+ *  - the incomplete last block, if any, is copied into a raw tile popped from
+ *    the free list (mode RAW, n_tok = tokens held, the rest zero);
+ *  - table entries of blocks past the sequence are set to GAAC_MODE_NONE.
+ * slot_ids may be NULL: every block is then stored as a raw tile (an
+ * uncompressed BF16 cache in the same paged layout, read by the same attention
+ * kernel; used as the uncompressed baseline).
+ * k, v: BF16 bits, element (b, t, h, c) at b*seq_stride + t*tok_stride + h*128 + c.
+ * base3/base4: [2][n_kv_heads][128] bytes (index 0 = K, 1 = V), 16-byte aligned.
+ * k and v must be 16-byte aligned and both strides multiples of 8 elements.
+ * n_tok: tokens present per sequence in k and v.  Each seq_lens[b] must be
+ * <= min(n_tok, max_blocks*64); otherwise GAAC_EINVAL goes to *d_status and the
+ * sequence is left out (its entries become GAAC_MODE_NONE).
+ */
+GAAC_API int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t seq_stride, int64_t tok_stride,
+                       int64_t n_tok, const int32_t* seq_lens, int batch, int n_kv_heads, int max_blocks, const uint8_t* base3,
+                       const uint8_t* base4, gaac_entry* table, const uint32_t* slot_ids, const gaac_pools* pools,
+                       gaac_stats* stats, int32_t* d_status, void* stream);
+
+/*
+ * O(1) append of one decode token per sequence (section 3.3: decode tokens go
+ * to a BF16 tail block, which is compressed a single time once it is full).
+ * For each b, kv-head h, K|V: writes k_new/v_new[(b*n_kv_heads+h)*128 + c] at
+ * position p = seq_lens[b] % 64 of block blk = seq_lens[b] / 64, whose tile must
+ * be the open raw tail (a raw tile is popped from the free list when the block
+ * has none yet).  When the tile becomes full it is encoded into slot
+ * slot_ids[((b*max_blocks+blk)*n_kv_heads+h)*2+kv] (same layout as for
+ * gaac_encode_blocks); if it fits, the entry becomes SLOT and the raw tile is
+ * handed to block blk+1 as its tail; if not, the block stays RAW.  Finally
+ * seq_lens[b] += 1 (a second small kernel on the same stream).
+ * seq_lens[b] must be < max_blocks*64 (else GAAC_EINVAL in *d_status).
+ */
+GAAC_API int gaac_append(const uint16_t* k_new, const uint16_t* v_new, int32_t* seq_lens, int batch, int n_kv_heads,
+                int max_blocks, const uint8_t* base3, const uint8_t* base4, gaac_entry* table,
+                const uint32_t* slot_ids, const gaac_pools* pools, gaac_stats* stats, int32_t* d_status,
+                void* stream);
+
+/*
+ * Workspace bytes gaac_decode_attention needs for (batch, n_q_heads, n_splits).
+ * n_splits = 0 asks for the automatic choice (max_blocks must then be given).
+ */
+GAAC_API size_t gaac_attention_workspace(int batch, int n_kv_heads, int max_blocks, int n_splits);
+
+/* Number of splits gaac_decode_attention uses for n_splits = 0. */
+GAAC_API int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_blocks);
+
+/*
+ * Fused split-K GQA decode attention over the compressed cache (section 3.2:
+ * tiles are rebuilt inside the attention kernel, never decompressed to a full
+ * cache, and compressed blocks and the raw tail feed one softmax).
+ *   out[b][hq][c] = sum_{t < seq_lens[b]} softmax_t(scale * q[b][hq] . k[b][t][hk]) v[b][t][hk][c]
+ * with hk = hq / (n_q_heads / n_kv_heads), in fp32 (0 for an empty sequence).
+ * q: BF16 bits [batch][n_q_heads][128]; out: fp32 [batch][n_q_heads][128].
+ * n_q_heads / n_kv_heads must be an integer <= GAAC_MAX_GQA.
+ * workspace: at least gaac_attention_workspace(...) bytes, 16-byte aligned.
+ * pools: only slot_pool, n_slots, raw_pool and n_raw are read; both pools must be
+ * 16-byte aligned (tiles are fetched with bulk copies).  A table entry that is
+ * neither a valid slot nor a valid raw tile reports GAAC_EFORMAT and its block
+ * contributes nothing.
+ */
+GAAC_API int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
+                          const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
+                          const uint8_t* base3, const uint8_t* base4, float scale, int n_splits, float* out,
+                          void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream);
+
+/*
+ * Decompress a layer's cache back to BF16 (section 4.3 compares block decode
+ * latency; used for bit-exact checks).  Writes tokens t < seq_lens[b] of every
+ * (b, h) to k_out/v_out at b*seq_stride + t*tok_stride + h*128 + c; n_tok is the
+ * number of token rows the outputs hold (a longer sequence reports GAAC_EINVAL
+ * and only its first n_tok tokens are written).
+ * pools: slot_pool, n_slots, raw_pool, n_raw are read (16-byte aligned).  An
+ * invalid entry reports GAAC_EFORMAT and its tokens are left untouched.
+ */
+GAAC_API int gaac_decompress(const gaac_entry* table, const int32_t* seq_lens, int batch, int n_kv_heads, int max_blocks,
+                    const gaac_pools* pools, const uint8_t* base3, const uint8_t* base4, uint16_t* k_out,
+                    uint16_t* v_out, int64_t seq_stride, int64_t tok_stride, int64_t n_tok, int32_t* d_status,
+                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GAAC_H */

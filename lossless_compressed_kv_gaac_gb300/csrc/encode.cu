@@ -1,0 +1,444 @@
+// Block encoder (prefill), O(1) appender and seal of the GAAC cache.
+//
+// "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference on
+// Personal Devices":
+//  - section 3.1: per-channel base-plus-offset exponent codes; a group of eight
+//    takes the 3-bit mode if every offset from base3 fits [0,7], else the 4-bit
+//    mode if every offset from base4 fits [0,15], else the raw mode; sign and
+//    mantissa are stored unchanged;
+//  - section 3.3 / Figure 3: complete blocks are encoded once into
+//    fixed-capacity slots, oversized blocks stay BF16, the incomplete tail is a
+//    BF16 block that is encoded when it fills ("fill-then-finalize").
+//
+// One CTA of 256 threads encodes one tile; thread u owns the 32-element code
+// unit u (storage elements 32u..32u+31), i.e. exactly one tag byte and one
+// word of each code plane.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gaac {
+
+constexpr int kEncThreads = 256;
+
+struct EncShared {
+  alignas(16) uint16_t tile[kTile];  // tile in storage order
+  int warp_sums[kEncThreads / 32];
+  int mode_counts[4];
+  uint32_t raw_idx;
+  int ok;
+};
+
+// Channel of storage element s (format v1).
+__device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? (s & 127) : (s >> 6); }
+
+// Encodes the tile in sh->tile into `slot` (global, 16-byte aligned) unless its
+// escape stream exceeds the capacity.  Returns the escape length, or -1 when
+// the tile must stay raw (then nothing is written).  CTA-uniform result; all
+// 256 threads must call it.
+__device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restrict__ b3g,
+                               const uint8_t* __restrict__ b4g, uint8_t* __restrict__ slot,
+                               gaac_stats* stats) {
+  const int u = threadIdx.x;
+  const int lane = u & 31, warp = u >> 5;
+  uint32_t xw[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(sh->tile + 32 * u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 w = src[i];
+      xw[4 * i + 0] = w.x;
+      xw[4 * i + 1] = w.y;
+      xw[4 * i + 2] = w.z;
+      xw[4 * i + 3] = w.w;
+    }
+  }
+  if (u < 4) sh->mode_counts[u] = 0;
+
+  uint32_t code[32];
+  uint32_t smb[8];  // sign|mantissa bytes, 4 per word
+  uint32_t escw[5] = {0, 0, 0, 0, 0};  // up to 20 escape bytes, little-endian
+  int nesc = 0;
+  uint32_t tagbyte = 0;
+  int my_counts[3] = {0, 0, 0};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) smb[j] = 0;
+
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    int e[8], b3[8], b4[8];
+    bool fits3 = true, fits4 = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int el = 8 * gi + j;
+      const uint32_t x = (xw[el >> 1] >> (16 * (el & 1))) & 0xFFFFu;
+      e[j] = (x >> 7) & 0xFF;
+      const uint32_t sm = ((x >> 8) & 0x80u) | (x & 0x7Fu);
+      smb[el >> 2] |= sm << (8 * (el & 3));
+      const int c = channel_of(kind, 32 * u + el);
+      b3[j] = b3g[c];
+      b4[j] = b4g[c];
+      const int o3 = e[j] - b3[j], o4 = e[j] - b4[j];
+      fits3 = fits3 && (o3 >= 0) && (o3 <= 7);
+      fits4 = fits4 && (o4 >= 0) && (o4 <= 15);
+    }
+    const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
+    tagbyte |= mode << (2 * gi);
+    my_counts[mode] += 1;
+    uint32_t eb[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t cd;
+      if (mode == 0u) {
+        cd = static_cast<uint32_t>(e[j] - b3[j]) & 7u;
+      } else if (mode == 1u) {
+        const uint32_t off = static_cast<uint32_t>(e[j] - b4[j]) & 0xFFu;
+        cd = off & 7u;
+        eb[0] |= ((off >> 3) & 1u) << j;
+      } else {
+        cd = static_cast<uint32_t>(e[j]) & 7u;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) eb[k] |= ((static_cast<uint32_t>(e[j]) >> (3 + k)) & 1u) << j;
+      }
+      code[8 * gi + j] = cd;
+    }
+    const int nb = mode == 0u ? 0 : (mode == 1u ? 1 : 5);
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+      if (k < nb) {
+        const int at = nesc + k;  // < 20
+#pragma unroll
+        for (int w = 0; w < 5; ++w)
+          if ((at >> 2) == w) escw[w] |= eb[k] << (8 * (at & 3));
+      }
+    }
+    nesc += nb;
+  }
+
+  // Exclusive scan of the escape byte counts over the CTA (unit order = group order).
+  int incl = nesc;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) sh->warp_sums[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kEncThreads / 32; ++w) {
+    const int s = sh->warp_sums[w];
+    if (w < warp) before += s;
+    total += s;
+  }
+  const int off = before + incl - nesc;
+  if (total > kEscCap || slot == nullptr) return -1;
+
+  // Code plane words of this unit (format v1 placement).
+  uint32_t W[3] = {0, 0, 0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      const uint32_t c0 = code[16 * h + L], c1 = code[16 * h + 4 + L], c2 = code[16 * h + 8 + L],
+                     c3 = code[16 * h + 12 + L];
+      W[h] |= (c0 | (c1 << 3) | ((c3 & 3u) << 6)) << (8 * L);
+      W[2] |= ((c2 << (3 * h)) | (((c3 >> 2) & 1u) << (6 + h))) << (8 * L);
+    }
+  }
+  uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
+  smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
+  smdst[1] = make_uint4(smb[4], smb[5], smb[6], smb[7]);
+  uint32_t* cw = reinterpret_cast<uint32_t*>(slot + kOffCode);
+  cw[u] = W[0];
+  cw[256 + u] = W[1];
+  cw[512 + u] = W[2];
+  slot[kOffTag + u] = static_cast<uint8_t>(tagbyte);
+  for (int k = 0; k < nesc; ++k) slot[kOffEsc + off + k] = static_cast<uint8_t>(escw[k >> 2] >> (8 * (k & 3)));
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int at = 2 * u + i;  // 0..511
+    if (at >= total) slot[kOffEsc + at] = 0;
+  }
+  if (stats != nullptr) {
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+      if (my_counts[m]) atomicAdd(&sh->mode_counts[m], my_counts[m]);
+    __syncthreads();
+    if (u == 0) {
+#pragma unroll
+      for (int m = 0; m < 3; ++m)
+        atomicAdd(&stats->groups[m], static_cast<unsigned long long>(sh->mode_counts[m]));
+      atomicAdd(&stats->escape_bytes, static_cast<unsigned long long>(total));
+      atomicAdd(&stats->slot_tiles, 1ull);
+    }
+  }
+  return total;
+}
+
+__device__ __forceinline__ gaac_entry make_entry(uint32_t index, int esc, int mode, int n_tok) {
+  gaac_entry e;
+  e.index = index;
+  e.esc_len = static_cast<uint16_t>(esc);
+  e.mode = static_cast<uint8_t>(mode);
+  e.n_tok = static_cast<uint8_t>(n_tok);
+  return e;
+}
+
+// Pops one raw tile index from the free list; thread 0 only.  Returns false on exhaustion.
+__device__ __forceinline__ bool pop_raw(const gaac_pools& pools, uint32_t* idx, int32_t* status) {
+  const unsigned long long pos = atomicAdd(reinterpret_cast<unsigned int*>(pools.raw_cursor), 1u);
+  if (static_cast<long long>(pos) >= pools.n_raw_free) {
+    report(status, GAAC_EPOOL);
+    return false;
+  }
+  const uint32_t v = pools.raw_free != nullptr ? pools.raw_free[pos] : static_cast<uint32_t>(pos);
+  if (static_cast<long long>(v) >= pools.n_raw) {
+    report(status, GAAC_EPOOL);
+    return false;
+  }
+  *idx = v;
+  return true;
+}
+
+struct EncodeArgs {
+  const uint16_t* k;
+  const uint16_t* v;
+  int64_t seq_stride, tok_stride, n_tok;
+  const int32_t* seq_lens;
+  int n_kv_heads, max_blocks;
+  const uint8_t* base3;
+  const uint8_t* base4;
+  gaac_entry* table;
+  const uint32_t* slot_ids;
+  gaac_pools pools;
+  gaac_stats* stats;
+  int32_t* status;
+};
+
+// grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
+__global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a) {
+  __shared__ EncShared sh;
+  const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
+  const int blk = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const size_t eidx = ((static_cast<size_t>(b) * a.max_blocks + blk) * a.n_kv_heads + h) * 2 + kind;
+  const int len = a.seq_lens[b];
+  if (len < 0 || len > a.max_blocks * kBlock || len > a.n_tok) {
+    if (tid == 0) {
+      a.table[eidx] = make_entry(0, 0, GAAC_MODE_NONE, 0);
+      report(a.status, GAAC_EINVAL);
+    }
+    return;
+  }
+  if (blk * kBlock >= len) {
+    if (tid == 0) a.table[eidx] = make_entry(0, 0, GAAC_MODE_NONE, 0);
+    return;
+  }
+  const int nv = min(kBlock, len - blk * kBlock);
+  // Stage the tile in storage order; tokens past the sequence are zero.
+  {
+    const uint16_t* src = (kind == 0 ? a.k : a.v) + static_cast<int64_t>(b) * a.seq_stride +
+                          static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD;
+    const int t = tid >> 2, part = tid & 3;
+    uint4 w[4];
+    if (t < nv) {
+      const uint4* p = reinterpret_cast<const uint4*>(src + t * a.tok_stride + 32 * part);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = p[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (kind == 0) {
+      uint4* d = reinterpret_cast<uint4*>(sh.tile + t * kD + 32 * part);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[i] = w[i];
+    } else {
+      const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = 32 * part + 2 * i;
+        sh.tile[c * kBlock + t] = static_cast<uint16_t>(ws[i] & 0xFFFFu);
+        sh.tile[(c + 1) * kBlock + t] = static_cast<uint16_t>(ws[i] >> 16);
+      }
+    }
+  }
+  __syncthreads();
+  const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
+  const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
+  if (nv == kBlock && a.slot_ids != nullptr) {
+    const uint32_t slot_id = a.slot_ids[eidx];
+    uint8_t* slot = nullptr;
+    if (static_cast<int64_t>(slot_id) < a.pools.n_slots) {
+      slot = a.pools.slot_pool + static_cast<size_t>(slot_id) * kSlot;
+    } else if (tid == 0) {
+      report(a.status, GAAC_EPOOL);
+    }
+    const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, a.stats);
+    if (esc >= 0) {
+      if (tid == 0) a.table[eidx] = make_entry(slot_id, esc, GAAC_MODE_SLOT, kBlock);
+      return;
+    }
+  }
+  // Raw tile: overflow fallback of a full block, or the open tail.
+  if (tid == 0) {
+    uint32_t idx = 0;
+    sh.ok = pop_raw(a.pools, &idx, a.status) ? 1 : 0;
+    sh.raw_idx = idx;
+  }
+  __syncthreads();
+  if (!sh.ok) {
+    if (tid == 0) a.table[eidx] = make_entry(0, 0, GAAC_MODE_NONE, 0);
+    return;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.pools.raw_pool + static_cast<size_t>(sh.raw_idx) * kTile);
+  const uint4* s = reinterpret_cast<const uint4*>(sh.tile);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[tid + kEncThreads * i] = s[tid + kEncThreads * i];
+  if (tid == 0) {
+    a.table[eidx] = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, nv);
+    if (a.stats != nullptr && a.slot_ids != nullptr)
+      atomicAdd(nv == kBlock ? &a.stats->raw_tiles : &a.stats->tail_tiles, 1ull);
+  }
+}
+
+struct AppendArgs {
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* seq_lens;
+  int n_kv_heads, max_blocks;
+  const uint8_t* base3;
+  const uint8_t* base4;
+  gaac_entry* table;
+  const uint32_t* slot_ids;
+  gaac_pools pools;
+  gaac_stats* stats;
+  int32_t* status;
+};
+
+// grid (2*n_kv_heads, batch): x = h*2 + kind.
+__global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
+  __shared__ EncShared sh;
+  const int h = blockIdx.x >> 1, kind = blockIdx.x & 1, b = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int len = a.seq_lens[b];
+  if (len < 0 || len >= a.max_blocks * kBlock) {
+    if (tid == 0) report(a.status, GAAC_EINVAL);
+    return;
+  }
+  const int blk = len / kBlock, pos = len % kBlock;
+  gaac_entry* ep = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk) * a.n_kv_heads + h) * 2 + kind;
+  if (tid == 0) {
+    gaac_entry e = *ep;
+    int ok = 1;
+    if (e.mode != GAAC_MODE_RAW) {
+      if (pos != 0) {
+        report(a.status, GAAC_EFORMAT);
+        ok = 0;
+      } else {
+        uint32_t idx = 0;
+        ok = pop_raw(a.pools, &idx, a.status) ? 1 : 0;
+        e = make_entry(idx, 0, GAAC_MODE_RAW, 0);
+      }
+    } else if (e.n_tok != pos || static_cast<int64_t>(e.index) >= a.pools.n_raw) {
+      report(a.status, GAAC_EFORMAT);
+      ok = 0;
+    }
+    sh.raw_idx = e.index;
+    sh.ok = ok;
+  }
+  __syncthreads();
+  if (!sh.ok) return;
+  uint16_t* raw = a.pools.raw_pool + static_cast<size_t>(sh.raw_idx) * kTile;
+  if (tid < kD) {
+    const uint16_t x = (kind == 0 ? a.k_new : a.v_new)[(static_cast<size_t>(b) * a.n_kv_heads + h) * kD + tid];
+    raw[kind == 0 ? pos * kD + tid : tid * kBlock + pos] = x;
+  }
+  if (pos + 1 < kBlock) {
+    if (tid == 0) *ep = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, pos + 1);
+    return;
+  }
+  // The block is full: seal it (encode once; it is never re-encoded).
+  __syncthreads();
+  {
+    const uint4* s = reinterpret_cast<const uint4*>(raw);
+    uint4* d = reinterpret_cast<uint4*>(sh.tile);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[tid + kEncThreads * i] = s[tid + kEncThreads * i];
+  }
+  __syncthreads();
+  const uint32_t slot_id = a.slot_ids[((static_cast<size_t>(b) * a.max_blocks + blk) * a.n_kv_heads + h) * 2 + kind];
+  uint8_t* slot = nullptr;
+  if (static_cast<int64_t>(slot_id) < a.pools.n_slots) {
+    slot = a.pools.slot_pool + static_cast<size_t>(slot_id) * kSlot;
+  } else if (tid == 0) {
+    report(a.status, GAAC_EPOOL);
+  }
+  const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
+  const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
+  const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, a.stats);
+  if (tid == 0) {
+    if (esc >= 0) {
+      *ep = make_entry(slot_id, esc, GAAC_MODE_SLOT, kBlock);
+      if (blk + 1 < a.max_blocks) ep[static_cast<size_t>(a.n_kv_heads) * 2] = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, 0);
+    } else {
+      *ep = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, kBlock);
+      if (a.stats != nullptr) atomicAdd(&a.stats->raw_tiles, 1ull);
+    }
+  }
+}
+
+__global__ void bump_lens_kernel(int32_t* lens, int batch) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < batch) lens[i] += 1;
+}
+
+}  // namespace gaac
+
+using namespace gaac;
+
+static bool pools_ok(const gaac_pools* p) {
+  return p != nullptr && p->slot_pool != nullptr && p->raw_pool != nullptr && p->raw_cursor != nullptr &&
+         p->n_slots >= 0 && p->n_raw >= 0 && p->n_raw_free >= 0 &&
+         (reinterpret_cast<uintptr_t>(p->slot_pool) & 15u) == 0 && (reinterpret_cast<uintptr_t>(p->raw_pool) & 15u) == 0;
+}
+
+extern "C" int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t seq_stride, int64_t tok_stride,
+                                  int64_t n_tok, const int32_t* seq_lens, int batch, int n_kv_heads, int max_blocks,
+                                  const uint8_t* base3, const uint8_t* base4, gaac_entry* table,
+                                  const uint32_t* slot_ids, const gaac_pools* pools, gaac_stats* stats,
+                                  int32_t* d_status, void* stream) {
+  if (k == nullptr || v == nullptr || seq_lens == nullptr || base3 == nullptr || base4 == nullptr ||
+      table == nullptr || !pools_ok(pools))
+    return GAAC_EINVAL;
+  if (batch <= 0 || n_kv_heads <= 0 || max_blocks <= 0 || max_blocks > 65535 || batch > 65535 ||
+      n_kv_heads > 1024)
+    return GAAC_EINVAL;
+  if (tok_stride < static_cast<int64_t>(n_kv_heads) * kD || (tok_stride & 7) || (seq_stride & 7) ||
+      (reinterpret_cast<uintptr_t>(k) & 15u) || (reinterpret_cast<uintptr_t>(v) & 15u))
+    return GAAC_EINVAL;
+  if (n_tok < 0) return GAAC_EINVAL;
+  EncodeArgs a{k, v, seq_stride, tok_stride, n_tok, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids,
+               *pools, stats, d_status};
+  dim3 grid(2 * n_kv_heads, max_blocks, batch);
+  encode_blocks_kernel<<<grid, kEncThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
+
+extern "C" int gaac_append(const uint16_t* k_new, const uint16_t* v_new, int32_t* seq_lens, int batch,
+                           int n_kv_heads, int max_blocks, const uint8_t* base3, const uint8_t* base4,
+                           gaac_entry* table, const uint32_t* slot_ids, const gaac_pools* pools,
+                           gaac_stats* stats, int32_t* d_status, void* stream) {
+  if (k_new == nullptr || v_new == nullptr || seq_lens == nullptr || base3 == nullptr || base4 == nullptr ||
+      table == nullptr || slot_ids == nullptr || !pools_ok(pools))
+    return GAAC_EINVAL;
+  if (batch <= 0 || batch > 65535 || n_kv_heads <= 0 || n_kv_heads > 1024 || max_blocks <= 0) return GAAC_EINVAL;
+  AppendArgs a{k_new, v_new, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids, *pools,
+               stats, d_status};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  append_kernel<<<dim3(2 * n_kv_heads, batch), kEncThreads, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return GAAC_ECUDA;
+  bump_lens_kernel<<<(batch + 255) / 256, 256, 0, st>>>(seq_lens, batch);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}

@@ -1,0 +1,56 @@
+"""The C-ABI library loads on a machine without a GPU and exports every entry
+point include/gaac.h declares; host-side validation and the pure-host helpers
+answer without touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from lossless_compressed_kv_gaac_gb300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "gaac.h")).read()
+    names = re.findall(r"GAAC_API\s+[\w\s\*]+?\b(gaac_\w+)\s*\(", text)
+    assert len(names) >= 9
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_host_helpers(lib):
+    lib.gaac_strerror.restype = ctypes.c_char_p
+    assert lib.gaac_strerror(0) == b"ok"
+    assert lib.gaac_strerror(1) == b"invalid argument"
+    assert lib.gaac_format_version() == 1
+    lib.gaac_attention_workspace.restype = ctypes.c_size_t
+    # (16 m,l floats + 8 heads x 128 acc floats) x 4 bytes per (sequence, kv-head, split)
+    assert lib.gaac_attention_workspace(1, 8, 1024, 38) == 1 * 8 * 38 * (16 + 8 * 128) * 4
+    assert lib.gaac_attention_workspace(3, 4, 10, 5) == 3 * 4 * 5 * 1040 * 4
+
+
+def test_null_arguments_rejected_on_host(lib):
+    P = ctypes.c_void_p
+    EINVAL = 1
+    lib.gaac_decode_attention.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P,
+                                          ctypes.c_float, ctypes.c_int, P, P, ctypes.c_size_t, P, P]
+    assert lib.gaac_decode_attention(None, 1, 32, 8, 16, None, None, None, None, None, 0.1, 0, None, None, 0, None,
+                                     None) == EINVAL
+    lib.gaac_encode_blocks.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P]
+    assert lib.gaac_encode_blocks(None, None, 0, 1024, 0, None, 1, 8, 1, None, None, None, None, None, None, None,
+                                  None) == EINVAL
+    lib.gaac_calibrate.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P, P, P]
+    assert lib.gaac_calibrate(None, 10, 1024, 8, None, None, None, None) == EINVAL

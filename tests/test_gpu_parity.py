@@ -1,0 +1,249 @@
+"""CUDA path against the oracle, through the C ABI (marked gpu).
+
+Bit-exact: calibration bases, slot images (byte for byte, per logical tile of
+the table), raw tiles, decompression.  Attention: within 2e-3 max relative
+error (row-normwise) of the fp64 oracle; rows the oracle flags as outside the
+fp32 range are counted apart.
+
+Method: "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference
+on Personal Devices", sections 3.1 (codec), 3.2 (fused attention), 3.3 (slots,
+raw fallback, BF16 tail).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gaac_workloads as W
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import lossless_compressed_kv_gaac_gb300 as G
+    from lossless_compressed_kv_gaac_gb300.cache import LayerCache
+    from tests import gpu_util as U
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    G.lib()
+
+
+def _status(c):
+    torch.cuda.synchronize()
+    return int(c.status.item())
+
+
+def test_calibrate_bit_exact():
+    k, v = U.kv(0, 0, 1, 1024, 8)
+    c = U.build(k, v, U.lens_tensor([1024]))
+    b3, b4 = U.oracle_bases(k, v)
+    np.testing.assert_array_equal(c.base3.cpu().numpy(), b3)
+    np.testing.assert_array_equal(c.base4.cpu().numpy(), b4)
+    # a flat histogram region and random bits
+    rng = np.random.default_rng(0)
+    x = torch.from_numpy(rng.integers(0, 65536, (777, 3, 128)).astype(np.int64).astype(np.int16)).cuda()
+    g3 = torch.zeros(3, 128, dtype=torch.uint8, device="cuda")
+    g4 = torch.zeros_like(g3)
+    G.calibrate(x.view(torch.bfloat16), g3, g4)
+    r3, r4 = O.calibrate(U.u16(x))
+    np.testing.assert_array_equal(g3.cpu().numpy(), r3)
+    np.testing.assert_array_equal(g4.cpu().numpy(), r4)
+
+
+def test_config0_encode_decompress_attention():
+    """Config 0: 1 layer, batch 1, 16q/8kv, T=4096, calibrate on 512 tokens, scale 1/sqrt(128)."""
+    wl = W.WORKLOADS[0]
+    k, v = U.kv(0, 0, 1, wl.seq_len, wl.n_kv_heads)
+    lens = U.lens_tensor([wl.seq_len])
+    c = U.build(k, v, lens)
+    assert _status(c) == 0
+    n = U.check_tiles(c, k, v, lens)
+    assert n["slot"] > 0.95 * (64 * 8 * 2)
+    kd, vd = c.decompress(wl.seq_len)
+    assert torch.equal(kd.view(torch.int16), k.view(torch.int16))
+    assert torch.equal(vd.view(torch.int16), v.view(torch.int16))
+    q = W.make_q(0, 0, 1, wl.n_q_heads, device="cuda")
+    out = c.attention(q, wl.scale)
+    assert _status(c) == 0
+    worst, flagged = U.check_attention(out, q, k, v, lens, wl.scale)
+    assert flagged == 0
+    st = G.stats_dict(c.stats)
+    assert st["groups0"] + st["groups1"] + st["groups2"] == 1024 * st["slot_tiles"]
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 8), (64, 8), (12, 4)])
+def test_ragged_lengths_and_gqa(hq, hkv):
+    lens_v = [0, 1, 63, 64, 65, 700, 1024, 333]
+    B, T = len(lens_v), 1024
+    k, v = U.kv(0, 1, B, T, hkv)
+    lens = U.lens_tensor(lens_v)
+    c = U.build(k, v, lens, n_calib=512)
+    assert _status(c) == 0
+    U.check_tiles(c, k, v, lens)
+    kd, vd = c.decompress(T)
+    for b, L in enumerate(lens_v):
+        assert torch.equal(kd[b, :L].view(torch.int16), k[b, :L].view(torch.int16))
+        assert torch.equal(vd[b, :L].view(torch.int16), v[b, :L].view(torch.int16))
+    q = W.make_q(0, 1, B, hq, device="cuda")
+    for n_splits in (1, 3, 0):
+        out = c.attention(q, 1 / np.sqrt(128), n_splits=n_splits)
+        assert _status(c) == 0
+        U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128))
+    assert out[0].abs().max().item() == 0.0  # empty sequence -> zeros
+
+
+def test_all_raw_baseline_same_outputs():
+    """The uncompressed baseline: every block stored raw, read by the same kernel."""
+    k, v = U.kv(0, 2, 2, 2048, 8)
+    lens = U.lens_tensor([2048, 1500])
+    c = U.build(k, v, lens, raw=True)
+    assert _status(c) == 0
+    n = U.check_tiles(c, k, v, lens, raw_all=True)
+    assert n["slot"] == 0
+    q = W.make_q(0, 2, 2, 32, device="cuda")
+    out = c.attention(q, 1 / np.sqrt(128))
+    U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128))
+    cz = U.build(k, v, lens)
+    outz = cz.attention(q, 1 / np.sqrt(128))
+    torch.cuda.synchronize()
+    assert (out - outz).abs().max().item() < 1e-5
+
+
+def test_incremental_append_equals_one_shot():
+    """Config 3 shape, small: prefill then appends; sealed tiles equal a one-shot encode of the final cache."""
+    B, H, T0, steps = 3, 8, 200, 130
+    T = T0 + steps
+    k, v = U.kv(3, 0, B, T, H)
+    max_blocks = (T + 63) // 64 + 1
+    inc = LayerCache(B, H, max_blocks)
+    inc.calibrate(k[0, :T0], v[0, :T0])
+    inc.encode(k[:, :T0], v[:, :T0], U.lens_tensor([T0] * B))
+    q = W.make_q(3, 0, B, 16, device="cuda")
+    for s in range(steps):
+        inc.append(k[:, T0 + s].contiguous(), v[:, T0 + s].contiguous())
+        if s in (0, 55, 56, 57, steps - 1):
+            out = inc.attention(q, 1 / np.sqrt(128))
+            torch.cuda.synchronize()
+            L = T0 + s + 1
+            U.check_attention(out, q, k[:, :L], v[:, :L], U.lens_tensor([L] * B), 1 / np.sqrt(128))
+    assert _status(inc) == 0
+    assert inc.seq_lens.tolist() == [T] * B
+    one = LayerCache(B, H, max_blocks)
+    one.base3.copy_(inc.base3)
+    one.base4.copy_(inc.base4)
+    one.encode(k, v, U.lens_tensor([T] * B))
+    torch.cuda.synchronize()
+    b3, b4 = inc.base3.cpu().numpy(), inc.base4.cpu().numpy()
+    U.check_tiles(inc, k, v, inc.seq_lens, b3=b3, b4=b4)
+    U.check_tiles(one, k, v, one.seq_lens, b3=b3, b4=b4)
+    kd, vd = inc.decompress(T)
+    assert torch.equal(kd.view(torch.int16), k.view(torch.int16))
+    assert torch.equal(vd.view(torch.int16), v.view(torch.int16))
+
+
+def test_adversarial_small():
+    """Config 4 shape, small: 10% random-bit tokens after 512 clean ones."""
+    B, T, H = 2, 4096, 8
+    k, v = U.kv(4, 0, B, T, H, adversarial=0.1)
+    lens = U.lens_tensor([T, T - 100])
+    c = U.build(k, v, lens)
+    assert _status(c) == 0
+    n = U.check_tiles(c, k, v, lens)
+    assert n["raw"] > 0 and n["slot"] > 0
+    kd, vd = c.decompress(T)
+    assert torch.equal(kd[0].view(torch.int16), k[0].view(torch.int16))
+    q = W.make_q(4, 0, B, 32, device="cuda")
+    out = c.attention(q, 1 / np.sqrt(128))
+    U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128))
+
+
+def test_paged_scattered_slots():
+    """Config 2 shape, small: variable lengths, full blocks scattered over a shared slot pool."""
+    B, H, maxT = 8, 8, 2048
+    lens = W.make_lengths(2, B, 300, maxT, device="cuda")
+    k, v = U.kv(2, 0, B, maxT, H)
+    max_blocks = maxT // 64
+    positions = B * max_blocks * H * 2
+    pool = 2 * positions
+    perm = W.slot_permutation(2, 0, pool, device="cuda")[:positions].to(torch.int32)
+    slot_ids = perm.view(B, max_blocks, H, 2)
+    c = U.build(k, v, lens, slot_ids=slot_ids, n_slots=pool)
+    assert _status(c) == 0
+    U.check_tiles(c, k, v, lens)
+    q = W.make_q(2, 0, B, 16, device="cuda")
+    out = c.attention(q, 1 / np.sqrt(128))
+    U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128))
+
+
+def test_full_size_config1_layer():
+    """Config 1 sizes, one layer: T=65536, 32q/8kv, in the bench's launch configuration (auto splits)."""
+    T, H, Hq = 65536, 8, 32
+    k, v = U.kv(1, 0, 1, T, H)
+    lens = U.lens_tensor([T])
+    c = U.build(k, v, lens)
+    assert _status(c) == 0
+    rng = np.random.default_rng(1)
+    tiles = [(0, int(rng.integers(0, 1024)), int(rng.integers(0, H)), int(rng.integers(0, 2))) for _ in range(300)]
+    tiles += [(0, 1023, h, kind) for h in range(H) for kind in (0, 1)]
+    U.check_tiles(c, k, v, lens, tiles=tiles)
+    kd, vd = c.decompress(T)
+    assert torch.equal(kd.view(torch.int16), k.view(torch.int16))
+    assert torch.equal(vd.view(torch.int16), v.view(torch.int16))
+    q = W.make_q(1, 0, 1, Hq, device="cuda")
+    out = c.attention(q, 1 / np.sqrt(128))
+    assert _status(c) == 0
+    U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128))
+
+
+def test_full_size_config4():
+    """Config 4 sizes: batch 4, T=131072, 10% random-bit tokens; attention on every row."""
+    B, T, H, Hq = 4, 131072, 8, 32
+    k, v = U.kv(4, 0, B, T, H, adversarial=0.1)
+    lens = U.lens_tensor([T] * B)
+    c = U.build(k, v, lens)
+    assert _status(c) == 0
+    rng = np.random.default_rng(4)
+    tiles = [(int(rng.integers(0, B)), int(rng.integers(0, 2048)), int(rng.integers(0, H)), int(rng.integers(0, 2)))
+             for _ in range(300)]
+    n = U.check_tiles(c, k, v, lens, tiles=tiles)
+    assert n["raw"] > 0
+    kd, vd = c.decompress(T)
+    assert torch.equal(kd.view(torch.int16), k.view(torch.int16))
+    assert torch.equal(vd.view(torch.int16), v.view(torch.int16))
+    del kd, vd
+    q = W.make_q(4, 0, B, Hq, device="cuda")
+    out = c.attention(q, 1 / np.sqrt(128))
+    assert _status(c) == 0
+    U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128))
+
+
+def test_device_errors_are_reported_not_faulted():
+    k, v = U.kv(0, 3, 2, 512, 8)
+    lens = U.lens_tensor([512, 300])
+    c = U.build(k, v, lens)
+    assert _status(c) == 0
+    q = W.make_q(0, 3, 2, 16, device="cuda")
+    good = c.attention(q, 0.1).clone()
+    # a table entry with an unknown mode and one with an out-of-range index
+    c.table[0, 2, 1, 0] = (7 << 48)
+    c.table[1, 1, 3, 1] = (G.MODE_SLOT << 48) | (10 ** 9)
+    c.status.zero_()
+    out = c.attention(q, 0.1)
+    assert _status(c) == G.EFORMAT
+    assert torch.isfinite(out).all()
+    # entry (0,2,1,K) feeds q heads 2,3 of sequence 0; entry (1,1,3,V) q heads 6,7 of sequence 1
+    assert torch.equal(out[0, :2], good[0, :2]) and torch.equal(out[0, 4:], good[0, 4:])
+    assert torch.equal(out[1, :6], good[1, :6]) and torch.equal(out[1, 8:], good[1, 8:])
+    # raw pool exhaustion during encode
+    c2 = LayerCache(2, 8, 8, n_raw=3)
+    c2.calibrate(k[0], v[0])
+    c2.encode(k, v, lens)
+    assert _status(c2) == G.EPOOL
+    # host-side validation
+    with pytest.raises(G.GaacError):
+        G.decode_attention(q, c.seq_lens, c.table, c.pools, c.base3, c.base4, 0.1, out, c.workspace()[:8])
+    with pytest.raises(G.GaacError):
+        G.decode_attention(W.make_q(0, 3, 2, 80, device="cuda"), c.seq_lens, c.table, c.pools, c.base3, c.base4,
+                           0.1, torch.empty(2, 80, 128, device="cuda"), c.workspace())
