@@ -62,6 +62,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def reduce_max(x: float, device=None) -> float:
+    """Max of x over the ranks of the default process group (x itself when there is none)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ms_per_step_max: float, world: int) -> float:
+    """µs per step of the whole job: N replicas each finish one step per ms_per_step_max."""
+    return ms_per_step_max * 1e3 / world
+
+
 # ---------------------------------------------------------------- clocks ----
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
@@ -250,10 +267,8 @@ def run_gaac(args):
     time.sleep(0.3)
     ms = time_graph(g, stream, args.steps)
     clk = clocks.stop()
+    ms = reduce_max(ms, device)
     if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
     for c in caches:
         assert int(c.status.item()) == 0
@@ -322,10 +337,7 @@ def run_gaac(args):
             g3.replay()
             stream.synchronize()  # the host reads the result every step
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, device)
 
     peaks = {}
     try:
@@ -339,7 +351,7 @@ def run_gaac(args):
 
     result = {
         "metric": METRIC,
-        "value": round(ms_per_step * 1e3 / world, 2),
+        "value": round(job_value(ms_per_step, world), 2),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -368,7 +380,7 @@ def run_gaac(args):
                      "peak_source": peak_src, "launch_us": round(launch_ms * 1e3, 2),
                      "algorithmic_bytes_per_launch": alg_launch},
         "clocks": clk,
-        "e2e": {"value": round(e2e_ms * 1e3 / world, 2), "unit": UNIT, "h2d_bytes_per_step": q_host.numel() * 2,
+        "e2e": {"value": round(job_value(e2e_ms, world), 2), "unit": UNIT, "h2d_bytes_per_step": q_host.numel() * 2,
                 "d2h_bytes_per_step": out_host.numel() * 4},
         "gpu_launches": 2 * L * args.steps,
     }

@@ -151,7 +151,7 @@ GAAC_API int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t se
  * For each b, kv-head h, K|V: writes k_new/v_new[(b*n_kv_heads+h)*128 + c] at
  * position p = seq_lens[b] % 64 of block blk = seq_lens[b] / 64, whose tile must
  * be the open raw tail (a raw tile is popped from the free list when the block
- * has none yet).  When the tile becomes full it is encoded into slot
+ * has none yet; a new tail tile is cleared to zero first).  When the tile becomes full it is encoded into slot
  * slot_ids[((b*max_blocks+blk)*n_kv_heads+h)*2+kv] (same layout as for
  * gaac_encode_blocks); if it fits, the entry becomes SLOT and the raw tile is
  * handed to block blk+1 as its tail; if not, the block stays RAW.  Finally

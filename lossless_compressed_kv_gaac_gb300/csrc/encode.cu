@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
         ok = 0;
       } else {
         uint32_t idx = 0;
-        ok = pop_raw(a.pools, &idx, a.status) ? 1 : 0;
+        ok = pop_raw(a.pools, &idx, a.status) ? 2 : 0;  // 2: a fresh tile, cleared below
         e = make_entry(idx, 0, GAAC_MODE_RAW, 0);
       }
     } else if (e.n_tok != pos || static_cast<int64_t>(e.index) >= a.pools.n_raw) {
@@ -351,6 +351,12 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   __syncthreads();
   if (!sh.ok) return;
   uint16_t* raw = a.pools.raw_pool + static_cast<size_t>(sh.raw_idx) * kTile;
+  if (sh.ok == 2) {
+    uint4* d = reinterpret_cast<uint4*>(raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[tid + kEncThreads * i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+  }
   if (tid < kD) {
     const uint16_t x = (kind == 0 ? a.k_new : a.v_new)[(static_cast<size_t>(b) * a.n_kv_heads + h) * kD + tid];
     raw[kind == 0 ? pos * kD + tid : tid * kBlock + pos] = x;
@@ -378,6 +384,13 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
   const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
   const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, a.stats);
+  if (esc >= 0 && blk + 1 < a.max_blocks) {
+    // The raw tile becomes the next block's empty tail: clear it so that a tail
+    // always holds zeros past its last token.
+    uint4* d = reinterpret_cast<uint4*>(raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[tid + kEncThreads * i] = make_uint4(0, 0, 0, 0);
+  }
   if (tid == 0) {
     if (esc >= 0) {
       *ep = make_entry(slot_id, esc, GAAC_MODE_SLOT, kBlock);
