@@ -192,6 +192,35 @@ GAAC_API int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, 
                           void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream);
 
 /*
+ * Allocation-free decode attention.  The GAAC page has no counterpart; this is a
+ * convenience of this library for callers that cannot allocate device memory
+ * when they call it, such as a serving loop whose memory plan is fixed after
+ * start-up, a plugin whose host owns all device allocations, or any code that
+ * must not enter an allocator on the decode path.
+ *
+ * Same arguments, result and errors as gaac_decode_attention, without the
+ * workspace: the split partials go to a scratch array of
+ * GAAC_STATIC_SCRATCH_BYTES bytes that the library itself holds in device
+ * memory on every GPU that loads it, until the process exits.  A call whose
+ * partials would not fit (gaac_attention_workspace(batch, n_kv_heads,
+ * max_blocks, n_splits) > GAAC_STATIC_SCRATCH_BYTES) returns GAAC_EINVAL and
+ * enqueues nothing.  It calls no allocator (no cudaMalloc, no cudaFree).
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array.  Calls whose kernels overlap on the GPU
+ *    (other streams, other threads) race on it and give wrong results; issue
+ *    them in one stream or order them.  The array keeps the last call's
+ *    partials; nothing in it needs to start at zero, every call rewrites what it
+ *    reads.
+ */
+#define GAAC_STATIC_SCRATCH_BYTES (4u << 20)
+GAAC_API int gaac_decode_attention_noalloc(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads,
+                                           int max_blocks, const int32_t* seq_lens, const gaac_entry* table,
+                                           const gaac_pools* pools, const uint8_t* base3, const uint8_t* base4,
+                                           float scale, int n_splits, float* out, int32_t* d_status, void* stream);
+
+/*
  * Decompress a layer's cache back to BF16 (section 4.3 compares block decode
  * latency; used for bit-exact checks).  Writes tokens t < seq_lens[b] of every
  * (b, h) to k_out/v_out at b*seq_stride + t*tok_stride + h*128 + c; n_tok is the

@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
                                                 P, P]
             L.gaac_decode_attention.restype = i32
             L.gaac_decompress.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, i64, i64, i64, P, P]
+            L.gaac_decode_attention_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, ctypes.c_float, i32, P,
+                                                        P, P]
+            L.gaac_decode_attention_noalloc.restype = i32
             L.gaac_decompress.restype = i32
             _lib = L
     return _lib
@@ -235,3 +238,19 @@ def decompress(table, seq_lens, pools: Pools, base3, base4, k_out, v_out, status
         table.data_ptr(), seq_lens.data_ptr(), table.shape[0], table.shape[2], table.shape[1], ctypes.byref(pc),
         base3.data_ptr(), base4.data_ptr(), k_out.data_ptr(), v_out.data_ptr(), ss, ts,
         min(k_out.shape[1], v_out.shape[1]), _ptr(status), _stream(stream)))
+
+
+STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def decode_attention_noalloc(q, seq_lens, table, pools: Pools, base3, base4, scale: float, out, n_splits: int = 0,
+                             status=None, stream=None) -> None:
+    """decode_attention without a workspace: for callers that cannot allocate device memory at call time.
+    The split partials use the library's own fixed scratch array (STATIC_SCRATCH_BYTES per device), so
+    calls must not overlap on the GPU, and the first call on a device must come before any stream capture."""
+    batch, hq = q.shape[0], q.shape[1]
+    max_blocks, hkv = table.shape[1], table.shape[2]
+    pc = pools.c()
+    _check("gaac_decode_attention_noalloc", lib().gaac_decode_attention_noalloc(
+        q.data_ptr(), batch, hq, hkv, max_blocks, seq_lens.data_ptr(), table.data_ptr(), ctypes.byref(pc),
+        base3.data_ptr(), base4.data_ptr(), float(scale), n_splits, out.data_ptr(), _ptr(status), _stream(stream)))

@@ -547,3 +547,42 @@ extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads
   attn_combine_kernel<<<dim3(n_q_heads, batch), kD, 0, st>>>(a.part, n_q_heads, n_kv_heads, a.r, n_splits, out);
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
+
+// ------------------------------------------------------------------------
+// Allocation-free variant.  Some callers cannot hand the library a workspace
+// allocated at call time: a serving loop that has frozen its device memory
+// plan, a plugin whose host owns every allocation, or code that must not call
+// into an allocator on the decode path.  This entry point runs the same two
+// kernels with their split partials in a fixed scratch array that lives in the
+// library itself.
+constexpr size_t kStaticScratchBytes = GAAC_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];
+
+// Device address of g_attn_scratch on the current device, looked up once per
+// device (the host-side name is only a stand-in and must not reach a kernel).
+static void* static_scratch_address() {
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+extern "C" int gaac_decode_attention_noalloc(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads,
+                                             int max_blocks, const int32_t* seq_lens, const gaac_entry* table,
+                                             const gaac_pools* pools, const uint8_t* base3, const uint8_t* base4,
+                                             float scale, int n_splits, float* out, int32_t* d_status,
+                                             void* stream) {
+  if (batch <= 0 || n_kv_heads <= 0 || max_blocks <= 0) return GAAC_EINVAL;
+  int ns = n_splits <= 0 ? gaac_attention_auto_splits(batch, n_kv_heads, max_blocks) : n_splits;
+  if (ns > max_blocks) ns = max_blocks;
+  if (gaac_attention_workspace(batch, n_kv_heads, max_blocks, ns) > kStaticScratchBytes) return GAAC_EINVAL;
+  void* scratch = static_scratch_address();
+  if (scratch == nullptr) return GAAC_ECUDA;
+  return gaac_decode_attention(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, base3, base4,
+                               scale, ns, out, scratch, kStaticScratchBytes, d_status, stream);
+}
