@@ -17,6 +17,9 @@
 //    each thread's 32 channels are contiguous), PV^T with 32 channels x 8 heads
 //    per warp (V channel-major, each thread's 16 tokens contiguous).  No
 //    decompressed tile is ever written back to shared memory.
+//  * The producer warp also checks each slot image's tag plane and gathers the
+//    escape bytes of 4-bit-mode groups per 32-element unit (into the unused
+//    tail of the stage region), so consumers decode without per-lane branches.
 //  * Online softmax in the log2 domain, shared by the CTA through a small score
 //    buffer and one named barrier per block; P enters the PV product as a
 //    bf16 hi + lo pair so its rounding stays near 2^-17.
@@ -32,12 +35,19 @@
 
 namespace gaac {
 
-constexpr int kAttWarps = 4;
+constexpr int kAttWarps = 4;                // consumer warps
 constexpr int kAttThreads = (kAttWarps + 1) * 32;
-constexpr int kStages = 3;
+#ifndef GAAC_ATT_STAGES
+#define GAAC_ATT_STAGES 2
+#endif
+#ifndef GAAC_ATT_CTAS_PER_SM
+#define GAAC_ATT_CTAS_PER_SM 3
+#endif
+constexpr int kStages = GAAC_ATT_STAGES;
+constexpr int kCtasPerSm = GAAC_ATT_CTAS_PER_SM;
 constexpr int kStageBytes = 2 * kRawBytes;  // K region + V region
-constexpr int kSStride = 68;                // floats per head row of the score buffer
 constexpr int kRPad = 8;                    // query heads per kv-head in the MMA N dimension
+constexpr int kPStride = 72;                // bf16 per head row of the probability buffer (64 + pad)
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
 
 struct StageMeta {
@@ -46,10 +56,13 @@ struct StageMeta {
 
 struct AttSmem {
   alignas(128) uint8_t stage[kStages][kStageBytes];
-  alignas(16) float S[2][kRPad][kSStride];
+  alignas(16) uint16_t P[2][2][kRPad][kPStride];  // [block parity][hi, lo][head][token] bf16 probabilities
+  alignas(16) float wmax[2][kRPad][kAttWarps];     // [parity][head][warp] max of the warp's 16 scores
+  alignas(16) float wsum[2][kRPad][kAttWarps];     // [parity][head][warp] sum of the warp's 16 probabilities
+  uint2 lut[256];                                  // escape byte -> spread bits of a 4-bit group
   StageMeta meta[kStages];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kStages];   // bulk copies landed
+  uint64_t empty[kStages];  // consumers done with the stage
 };
 
 struct AttnArgs {
@@ -75,105 +88,112 @@ __device__ __forceinline__ uint32_t bf16x2_div16(uint32_t w) {
   return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
   return r;
 }
 
-// Exclusive prefix of escape bytes over the 64 tag words of a slot image:
-// lane l returns the prefixes of words l and l+32.
-__device__ __forceinline__ void tag_word_prefix(const uint8_t* tile, int lane, int& pre_lo, int& pre_hi) {
-  const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile + kOffTag);
-  const int c0 = esc_count(tw[lane]), c1 = esc_count(tw[lane + 32]);
-  int i0 = c0, i1 = c1;
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ int warp_sum(int x) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, d);
+  return x;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int x, int lane) {
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int v0 = __shfl_up_sync(0xFFFFFFFFu, i0, d), v1 = __shfl_up_sync(0xFFFFFFFFu, i1, d);
-    if (lane >= d) {
-      i0 += v0;
-      i1 += v1;
+    const int v = __shfl_up_sync(0xFFFFFFFFu, x, d);
+    if (lane >= d) x += v;
+  }
+  return x;
+}
+
+// Per consumer warp and slot image.  Warp w decodes exactly the 32-element
+// units [64w, 64w+64) of the tile (K: its 16 tokens, V: its 32 channels), whose
+// tags are tag words [16w, 16w+16).  Returns the escape bytes before that range
+// and checks the whole tag plane (no reserved tag; escape bytes add up to
+// esc_len), a decision every warp takes identically.
+__device__ __forceinline__ bool range_escape_base(const uint8_t* tile, int esc_len, int warp, int lane,
+                                                  int& before) {
+  const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile + kOffTag);
+  const uint32_t wa = tw[lane], wb = tw[lane + 32];
+  const int ca = esc_count(wa), cb = esc_count(wb);
+  const bool reserved = ((wa & (wa >> 1)) | (wb & (wb >> 1))) & 0x55555555u;
+  const int bnd = 16 * warp;
+  const int red = warp_sum(((lane < bnd ? ca : 0) + (lane + 32 < bnd ? cb : 0)) | ((ca + cb) << 16));
+  before = red & 0xFFFF;
+  return !__any_sync(0xFFFFFFFFu, reserved) && (red >> 16) == esc_len;
+}
+
+// Escape bytes of the 4-bit-mode groups among the groups of tag byte/nibble
+// `tags` (ngroups groups, escape offset of the first at `off`), gathered as
+// byte j for group j (0 for the other groups).
+template <int NG>
+__device__ __forceinline__ uint32_t gather_groups(const uint8_t* esc, uint32_t tags, int off) {
+  uint32_t x = 0;
+#pragma unroll
+  for (int j = 0; j < NG; ++j) {
+    const uint32_t m = (tags >> (2 * j)) & 3u;
+    if (m == 1u) x |= static_cast<uint32_t>(esc[off]) << (8 * j);
+    off += esc_of_tag(m);
+  }
+  return x;
+}
+
+// Exponents of one half-unit (16 elements) into 8 bf16x2 words.  xw16: the two
+// groups' gathered 4-bit escape bytes; off: escape offset of its first group
+// (used only for raw-mode groups).
+__device__ __forceinline__ void decode_half(const uint8_t* tile, uint32_t Wh, uint32_t W2, int hh, uint32_t tagnib,
+                                            uint32_t xw16, int off, const uint4 sm, const uint32_t b3[4],
+                                            const uint32_t b4[4], const uint2* lut, uint32_t out[8]) {
+  uint32_t c[4];
+  extract_codes(Wh, W2, hh, c);
+  const uint2 s0 = lut[xw16 & 0xFFu], s1 = lut[(xw16 >> 8) & 0xFFu];
+  const bool g0 = (tagnib & 3u) != 0u, g1 = (tagnib & 12u) != 0u;
+  uint32_t e[4];
+  e[0] = (g0 ? b4[0] : b3[0]) + c[0] + s0.x;
+  e[1] = (g0 ? b4[1] : b3[1]) + c[1] + s0.y;
+  e[2] = (g1 ? b4[2] : b3[2]) + c[2] + s1.x;
+  e[3] = (g1 ? b4[3] : b3[3]) + c[3] + s1.y;
+  if (tagnib & 0xAu) {  // a raw-mode group in this half (rare): five escape bit planes
+    const uint8_t* esc = tile + kOffEsc;
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const uint32_t m = (tagnib >> (2 * gi)) & 3u;
+      if (m == 2u) {
+        const int o = off + (gi == 0 ? 0 : esc_of_tag(tagnib & 3u));
+        uint32_t hi0 = 0, hi1 = 0;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+          const uint32_t x = esc[o + k];
+          hi0 |= spread4(x & 15u) << (3 + k);
+          hi1 |= spread4(x >> 4) << (3 + k);
+        }
+        e[2 * gi] = c[2 * gi] | hi0;
+        e[2 * gi + 1] = c[2 * gi + 1] | hi1;
+      }
     }
   }
-  const int tot0 = __shfl_sync(0xFFFFFFFFu, i0, 31);
-  pre_lo = i0 - c0;
-  pre_hi = tot0 + i1 - c1;
+  join_bf16x4(sm.x, e[0], out[0], out[1]);
+  join_bf16x4(sm.y, e[1], out[2], out[3]);
+  join_bf16x4(sm.z, e[2], out[4], out[5]);
+  join_bf16x4(sm.w, e[3], out[6], out[7]);
 }
 
-// K token t, channels 32tq..32tq+31 -> 16 bf16x2 words (channel pairs 32tq+2m, +1).
-__device__ __forceinline__ void k_raw(const uint8_t* tile, int t, int tq, uint32_t out[16]) {
-  const uint4* p = reinterpret_cast<const uint4*>(tile + 256 * t + 64 * tq);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 w = p[i];
-    out[4 * i] = w.x;
-    out[4 * i + 1] = w.y;
-    out[4 * i + 2] = w.z;
-    out[4 * i + 3] = w.w;
-  }
+__device__ __forceinline__ void load8(const uint8_t* p, uint32_t out[8]) {
+  const uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
+  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
 }
 
-__device__ __forceinline__ void k_slot(const uint8_t* tile, int t, int tq, const uint32_t k3[8],
-                                       const uint32_t k4[8], int word_pre, int esc_len, uint32_t out[16],
-                                       bool* bad) {
-  const int u = 4 * t + tq;
-  const uint32_t* cw = reinterpret_cast<const uint32_t*>(tile + kOffCode);
-  const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
-  const uint32_t tagbyte = tile[kOffTag + u];
-  const uint4* sp = reinterpret_cast<const uint4*>(tile + 128 * t + 32 * tq);
-  const uint4 s0 = sp[0], s1 = sp[1];
-  const uint32_t smw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  int esc0 = 0, esc1 = 0;
-  if (tagbyte != 0u) {
-    const uint32_t tword = *reinterpret_cast<const uint32_t*>(tile + kOffTag + 4 * t);
-    esc0 = word_pre + esc_count(tword & ((1u << (8 * tq)) - 1u));
-    esc1 = esc0 + esc_count(tagbyte & 15u);
-  }
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    uint32_t e[4];
-    half_exponents(hh == 0 ? W0 : W1, W2, hh, (tagbyte >> (4 * hh)) & 15u, k3 + 4 * hh, k4 + 4 * hh,
-                   tile + kOffEsc, hh == 0 ? esc0 : esc1, esc_len, e, bad);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) join_bf16x4(smw[4 * hh + q], e[q], out[8 * hh + 2 * q], out[8 * hh + 2 * q + 1]);
-  }
-}
-
-// V channel c, tokens 16tq..16tq+15 -> 8 bf16x2 words (token pairs 16tq+2m, +1).
-__device__ __forceinline__ void v_raw(const uint8_t* tile, int c, int tq, uint32_t out[8]) {
-  const uint4* p = reinterpret_cast<const uint4*>(tile + 128 * c + 32 * tq);
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint4 w = p[i];
-    out[4 * i] = w.x;
-    out[4 * i + 1] = w.y;
-    out[4 * i + 2] = w.z;
-    out[4 * i + 3] = w.w;
-  }
-}
-
-__device__ __forceinline__ void v_slot(const uint8_t* tile, int c, int tq, uint32_t b3w, uint32_t b4w, int word_pre,
-                                       int esc_len, uint32_t out[8], bool* bad) {
-  const int u = 2 * c + (tq >> 1), hh = tq & 1;
-  const uint32_t* cw = reinterpret_cast<const uint32_t*>(tile + kOffCode);
-  const uint32_t Wh = cw[256 * hh + u], W2 = cw[512 + u];
-  const uint32_t tagnib = (static_cast<uint32_t>(tile[kOffTag + u]) >> (4 * hh)) & 15u;
-  const uint4 s = *reinterpret_cast<const uint4*>(tile + 64 * c + 16 * tq);
-  int esc0 = 0;
-  if (tagnib != 0u) {
-    const uint32_t tword = *reinterpret_cast<const uint32_t*>(tile + kOffTag + 4 * (c >> 1));
-    esc0 = word_pre + esc_count(tword & ((1u << (16 * (c & 1) + 4 * tq)) - 1u));
-  }
-  const uint32_t b3[4] = {b3w, b3w, b3w, b3w}, b4[4] = {b4w, b4w, b4w, b4w};
-  uint32_t e[4];
-  half_exponents(Wh, W2, hh, tagnib, b3, b4, tile + kOffEsc, esc0, esc_len, e, bad);
-  join_bf16x4(s.x, e[0], out[0], out[1]);
-  join_bf16x4(s.y, e[1], out[2], out[3]);
-  join_bf16x4(s.z, e[2], out[4], out[5]);
-  join_bf16x4(s.w, e[3], out[6], out[7]);
-}
-
-__global__ void __launch_bounds__(kAttThreads, 2) attn_split_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   AttSmem& sm = *reinterpret_cast<AttSmem*>(smem_raw);
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -188,6 +208,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) attn_split_kernel(AttnArgs a) 
   const int blk0 = split * per;
   const int n_my = max(0, min(nblk, blk0 + per) - blk0);
 
+  for (int x = tid; x < 256; x += kAttThreads) sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
@@ -198,31 +219,43 @@ __global__ void __launch_bounds__(kAttThreads, 2) attn_split_kernel(AttnArgs a) 
   }
   __syncthreads();
 
-  if (warp == kAttWarps) {  // ------------------------------------ producer
-    if (lane == 0) {
-      for (int i = 0; i < n_my; ++i) {
+  if (warp == kAttWarps) {  // ------------------------------------------------ producer warp
+    // Table entries of 32 blocks at a time, one block per lane.
+    const gaac_entry* tab = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk0) * a.Hkv + h) * 2;
+    const size_t blk_stride = static_cast<size_t>(a.Hkv) * 2;
+    uint2 ek = make_uint2(0, GAAC_MODE_NONE << 16), ev = ek;
+    for (int i = 0; i < n_my; ++i) {
+      if ((i & 31) == 0) {
+        const int j = i + lane;
+        if (j < n_my) {
+          ek = *reinterpret_cast<const uint2*>(tab + j * blk_stride);
+          ev = *reinterpret_cast<const uint2*>(tab + j * blk_stride + 1);
+        }
+      }
+      const uint32_t k0 = __shfl_sync(0xFFFFFFFFu, ek.x, i & 31), k1 = __shfl_sync(0xFFFFFFFFu, ek.y, i & 31);
+      const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, ev.x, i & 31), v1 = __shfl_sync(0xFFFFFFFFu, ev.y, i & 31);
+      if (lane == 0) {
         const int st = i % kStages;
         if (i >= kStages) mbar_wait(&sm.empty[st], ((i / kStages) & 1) ^ 1, a.status);
-        const gaac_entry* ep =
-            a.table + ((static_cast<size_t>(b) * a.max_blocks + blk0 + i) * a.Hkv + h) * 2;
         uint32_t bytes[2];
         const void* src[2];
         int mode[2], esc[2];
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
-          const gaac_entry e = ep[kv];
+          const uint32_t index = kv ? v0 : k0, w1 = kv ? v1 : k1;
+          const uint32_t esc_len = w1 & 0xFFFFu, emode = (w1 >> 16) & 0xFFu;
           bytes[kv] = 0;
           src[kv] = nullptr;
           esc[kv] = 0;
-          if (e.mode == GAAC_MODE_SLOT && static_cast<int64_t>(e.index) < a.n_slots && e.esc_len <= kEscCap) {
+          if (emode == GAAC_MODE_SLOT && static_cast<int64_t>(index) < a.n_slots && esc_len <= kEscCap) {
             mode[kv] = GAAC_MODE_SLOT;
-            esc[kv] = e.esc_len;
-            bytes[kv] = kOffEsc + ((e.esc_len + 15) & ~15);
-            src[kv] = a.slot_pool + static_cast<size_t>(e.index) * kSlot;
-          } else if (e.mode == GAAC_MODE_RAW && static_cast<int64_t>(e.index) < a.n_raw) {
+            esc[kv] = static_cast<int>(esc_len);
+            bytes[kv] = kOffEsc + ((esc_len + 15u) & ~15u);
+            src[kv] = a.slot_pool + static_cast<size_t>(index) * kSlot;
+          } else if (emode == GAAC_MODE_RAW && static_cast<int64_t>(index) < a.n_raw) {
             mode[kv] = GAAC_MODE_RAW;
             bytes[kv] = kRawBytes;
-            src[kv] = a.raw_pool + static_cast<size_t>(e.index) * kTile;
+            src[kv] = a.raw_pool + static_cast<size_t>(index) * kTile;
           } else {
             mode[kv] = GAAC_MODE_NONE;
             report(a.status, GAAC_EFORMAT);
@@ -233,11 +266,12 @@ __global__ void __launch_bounds__(kAttThreads, 2) attn_split_kernel(AttnArgs a) 
         if (bytes[0]) bulk_g2s(sm.stage[st], src[0], bytes[0], &sm.full[st]);
         if (bytes[1]) bulk_g2s(sm.stage[st] + kRawBytes, src[1], bytes[1], &sm.full[st]);
       }
+      __syncwarp();
     }
     return;
   }
 
-  // ---------------------------------------------------------------- consumers
+  // ------------------------------------------------------------------------- consumers
   const int g = lane >> 2, tq = lane & 3;
   const int r = a.r;
   uint32_t qf[16];
@@ -265,7 +299,7 @@ __global__ void __launch_bounds__(kAttThreads, 2) attn_split_kernel(AttnArgs a) 
     k4[0] = y0.x; k4[1] = y0.y; k4[2] = y0.z; k4[3] = y0.w;
     k4[4] = y1.x; k4[5] = y1.y; k4[6] = y1.z; k4[7] = y1.w;
   }
-  uint32_t v3[4], v4[4];  // [mi*2 + (0: channel g, 1: channel g+8)]
+  uint32_t v3[4], v4[4];  // [mi*2 + hb]: channel 32warp + 16mi + g + 8hb, byte replicated
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi) {
 #pragma unroll
@@ -275,163 +309,242 @@ __global__ void __launch_bounds__(kAttThreads, 2) attn_split_kernel(AttnArgs a) 
       v4[2 * mi + hb] = 0x01010101u * a.base4[(a.Hkv + h) * kD + c];
     }
   }
-  float acc[2][4];
+  float accH[2][4], accL[2][4];
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[mi][j] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-  bool bad = false;
+    for (int j = 0; j < 4; ++j) accH[mi][j] = accL[mi][j] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads 2tq, 2tq+1 (log2 domain)
+  float lg = 0.f;                        // running sum of head g
   const int t0 = 16 * warp + g, t1 = t0 + 8;
 
   for (int i = 0; i < n_my; ++i) {
-    const int st = i % kStages;
+    const int st = i % kStages, par = i & 1;
     mbar_wait(&sm.full[st], (i / kStages) & 1, a.status);
     const StageMeta md = sm.meta[st];
     const int nv = min(kBlock, len - (blk0 + i) * kBlock);
     const uint8_t* tK = sm.stage[st];
     const uint8_t* tV = tK + kRawBytes;
 
-    // ---- S = (q/16) K^T for tokens t0, t1 of this warp's 16-token slice
-    uint32_t ka[16], kb[16];
-    if (md.modeK == GAAC_MODE_SLOT) {
-      int pre_lo = 0, pre_hi = 0;
-      if (md.escK > 0) tag_word_prefix(tK, lane, pre_lo, pre_hi);
-      const int src = warp < 2 ? pre_lo : pre_hi;
-      const int wp0 = __shfl_sync(0xFFFFFFFFu, src, t0 & 31);
-      const int wp1 = __shfl_sync(0xFFFFFFFFu, src, t1 & 31);
-      k_slot(tK, t0, tq, k3, k4, wp0, md.escK, ka, &bad);
-      k_slot(tK, t1, tq, k3, k4, wp1, md.escK, kb, &bad);
-    } else if (md.modeK == GAAC_MODE_RAW) {
-      k_raw(tK, t0, tq, ka);
-      k_raw(tK, t1, tq, kb);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) ka[j] = kb[j] = 0u;
-    }
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) mma_bf16(s, ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1], qf[2 * ks], qf[2 * ks + 1]);
-    const bool ok0 = t0 < nv && md.modeK != GAAC_MODE_NONE, ok1 = t1 < nv && md.modeK != GAAC_MODE_NONE;
-    float* Sb = &sm.S[i & 1][0][0];
-    Sb[(2 * tq) * kSStride + t0] = ok0 ? s[0] * a.scale_log2 : -INFINITY;
-    Sb[(2 * tq + 1) * kSStride + t0] = ok0 ? s[1] * a.scale_log2 : -INFINITY;
-    Sb[(2 * tq) * kSStride + t1] = ok1 ? s[2] * a.scale_log2 : -INFINITY;
-    Sb[(2 * tq + 1) * kSStride + t1] = ok1 ? s[3] * a.scale_log2 : -INFINITY;
-    named_bar_sync(1, kAttWarps * 32);
-
-    // ---- online softmax for head g over this thread's tokens 16tq..16tq+15
-    float p[16];
-    {
-      const float4* sr = reinterpret_cast<const float4*>(Sb + g * kSStride + 16 * tq);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v = sr[j];
-        p[4 * j] = v.x;
-        p[4 * j + 1] = v.y;
-        p[4 * j + 2] = v.z;
-        p[4 * j + 3] = v.w;
-      }
-    }
-    float mx = p[0];
-#pragma unroll
-    for (int j = 1; j < 16; ++j) mx = fmaxf(mx, p[j]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    float alpha;
-    if (m_new == -INFINITY) {
-      alpha = 1.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) p[j] = 0.f;
-    } else {
-      alpha = exp2f(m_run - m_new);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) p[j] = exp2f(p[j] - m_new);
-    }
-    float ls = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) ls += p[j];
-    ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 1);
-    ls += __shfl_xor_sync(0xFFFFFFFFu, ls, 2);
-    l_run = l_run * alpha + ls;
-    m_run = m_new;
-    uint32_t ph[8], pl[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      ph[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
-      const float h0 = __uint_as_float(ph[j] << 16), h1 = __uint_as_float(ph[j] & 0xFFFF0000u);
-      pl[j] = pack_bf16x2(p[2 * j] - h0, p[2 * j + 1] - h1);
-    }
-    const float al0 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * tq);
-    const float al1 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * tq + 4);
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      acc[mi][0] *= al0;
-      acc[mi][1] *= al1;
-      acc[mi][2] *= al0;
-      acc[mi][3] *= al1;
-    }
-
-    // ---- O^T += V^T P^T for channels 32warp + 16mi + {g, g+8}
-    int vpre_lo = 0, vpre_hi = 0;
-    if (md.modeV == GAAC_MODE_SLOT && md.escV > 0) tag_word_prefix(tV, lane, vpre_lo, vpre_hi);
-    const int vsrc = warp < 2 ? vpre_lo : vpre_hi;
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      const int cA = 32 * warp + 16 * mi + g, cB = cA + 8;
-      uint32_t va[8], vb[8];
-      const int wpA = __shfl_sync(0xFFFFFFFFu, vsrc, (cA >> 1) & 31);
-      const int wpB = __shfl_sync(0xFFFFFFFFu, vsrc, (cB >> 1) & 31);
-      if (md.modeV == GAAC_MODE_SLOT) {
-        v_slot(tV, cA, tq, v3[2 * mi], v4[2 * mi], wpA, md.escV, va, &bad);
-        v_slot(tV, cB, tq, v3[2 * mi + 1], v4[2 * mi + 1], wpB, md.escV, vb, &bad);
-      } else if (md.modeV == GAAC_MODE_RAW) {
-        v_raw(tV, cA, tq, va);
-        v_raw(tV, cB, tq, vb);
+    // ---------------- K: S = (q/16) K^T for tokens t0, t1
+    int modeK = md.modeK;
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    if (modeK == GAAC_MODE_SLOT) {
+      int before;
+      if (!range_escape_base(tK, md.escK, warp, lane, before)) {
+        modeK = GAAC_MODE_NONE;
+        if (warp == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
       } else {
+        // this lane's units: uA = 4*t0 + tq = 64w + lane, uB = uA + 32 (range positions lane, lane + 32)
+        const uint32_t tbA = tK[kOffTag + 64 * warp + lane], tbB = tK[kOffTag + 64 * warp + 32 + lane];
+        const int cA = esc_count(tbA), cB = esc_count(tbB);
+        const int sc = warp_incl_scan(cA | (cB << 16), lane);
+        const int totA = __shfl_sync(0xFFFFFFFFu, sc, 31) & 0xFFFF;
+        const int offA = before + (sc & 0xFFFF) - cA;
+        const int offB = before + totA + (sc >> 16) - cB;
+        const uint32_t xA = gather_groups<4>(tK + kOffEsc, tbA, offA);
+        const uint32_t xB = gather_groups<4>(tK + kOffEsc, tbB, offB);
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(tK + kOffCode);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) va[j] = vb[j] = 0u;
-      }
-      if (nv < kBlock) {
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t ka[8], kb[8];
+          const int uA = 4 * t0 + tq, uB = 4 * t1 + tq;
+          const uint32_t nibA = (tbA >> (4 * hh)) & 15u, nibB = (tbB >> (4 * hh)) & 15u;
+          const int hoA = offA + (hh ? esc_count(tbA & 15u) : 0), hoB = offB + (hh ? esc_count(tbB & 15u) : 0);
+          decode_half(tK, cw[256 * hh + uA], cw[512 + uA], hh, nibA, xA >> (16 * hh), hoA,
+                      *reinterpret_cast<const uint4*>(tK + 128 * t0 + 32 * tq + 16 * hh), k3 + 4 * hh, k4 + 4 * hh,
+                      sm.lut, ka);
+          decode_half(tK, cw[256 * hh + uB], cw[512 + uB], hh, nibB, xB >> (16 * hh), hoB,
+                      *reinterpret_cast<const uint4*>(tK + 128 * t1 + 32 * tq + 16 * hh), k3 + 4 * hh, k4 + 4 * hh,
+                      sm.lut, kb);
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int tt = 16 * tq + 2 * m;
-          const uint32_t keep = (tt < nv ? 0x0000FFFFu : 0u) | (tt + 1 < nv ? 0xFFFF0000u : 0u);
-          va[m] &= keep;
-          vb[m] &= keep;
+          for (int j = 0; j < 4; ++j) {
+            const int ks = 4 * hh + j;
+            mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks], qf[2 * ks + 1]);
+          }
         }
       }
+    } else if (modeK == GAAC_MODE_RAW) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t ka[8], kb[8];
+        load8(tK + 256 * t0 + 64 * tq + 32 * hh, ka);
+        load8(tK + 256 * t1 + 64 * tq + 32 * hh, kb);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ks = 4 * hh + j;
+          mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks], qf[2 * ks + 1]);
+        }
+      }
+    }
+    const bool ok0 = t0 < nv && modeK != GAAC_MODE_NONE, ok1 = t1 < nv && modeK != GAAC_MODE_NONE;
+    // s[0]: (t0, head 2tq), s[1]: (t0, 2tq+1), s[2]: (t1, 2tq), s[3]: (t1, 2tq+1)
+    const float s0 = ok0 ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
+    const float s1 = ok0 ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
+    const float s2 = ok1 ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
+    const float s3 = ok1 ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
+
+    // ---------------- softmax: block max over the 4 warps' slices
+    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int d = 4; d < 32; d <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, d));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, d));
+    }
+    if (g == 0) {
+      sm.wmax[par][2 * tq][warp] = x0;
+      sm.wmax[par][2 * tq + 1][warp] = x1;
+    }
+    named_bar_sync(1, kAttWarps * 32);
+    const float4 wa = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq][0]);
+    const float4 wb = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq + 1][0]);
+    const float n0 = fmaxf(m0, fmaxf(fmaxf(wa.x, wa.y), fmaxf(wa.z, wa.w)));
+    const float n1 = fmaxf(m1, fmaxf(fmaxf(wb.x, wb.y), fmaxf(wb.z, wb.w)));
+    const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
+    const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
+    const float p0 = n0 == -INFINITY ? 0.f : fast_exp2(s0 - n0);
+    const float p2 = n0 == -INFINITY ? 0.f : fast_exp2(s2 - n0);
+    const float p1 = n1 == -INFINITY ? 0.f : fast_exp2(s1 - n1);
+    const float p3 = n1 == -INFINITY ? 0.f : fast_exp2(s3 - n1);
+    m0 = n0;
+    m1 = n1;
+    float y0 = p0 + p2, y1 = p1 + p3;
+#pragma unroll
+    for (int d = 4; d < 32; d <<= 1) {
+      y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, d);
+      y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, d);
+    }
+    if (g == 0) {
+      sm.wsum[par][2 * tq][warp] = y0;
+      sm.wsum[par][2 * tq + 1][warp] = y1;
+    }
+    {
+      uint16_t* Ph = &sm.P[par][0][0][0];
+      uint16_t* Pl = &sm.P[par][1][0][0];
+      const float pv[4] = {p0, p1, p2, p3};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int head = 2 * tq + (j & 1), tok = j < 2 ? t0 : t1;
+        const uint16_t hb = to_bf16(pv[j]);
+        Ph[head * kPStride + tok] = hb;
+        Pl[head * kPStride + tok] = to_bf16(pv[j] - __uint_as_float(static_cast<uint32_t>(hb) << 16));
+      }
+    }
+    named_bar_sync(1, kAttWarps * 32);
+
+    // ---------------- PV: O^T += V^T P^T for channels 32warp + 16mi + {g, g+8}
+    uint32_t ph[8], pl[8];
+    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][0][g][16 * tq]), ph);
+    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][1][g][16 * tq]), pl);
+    {
+      const float4 ws = *reinterpret_cast<const float4*>(&sm.wsum[par][g][0]);
+      const float a0s = __shfl_sync(0xFFFFFFFFu, al0, g >> 1), a1s = __shfl_sync(0xFFFFFFFFu, al1, g >> 1);
+      lg = lg * ((g & 1) ? a1s : a0s) + ((ws.x + ws.y) + (ws.z + ws.w));
+    }
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      accH[mi][0] *= al0; accH[mi][1] *= al1; accH[mi][2] *= al0; accH[mi][3] *= al1;
+      accL[mi][0] *= al0; accL[mi][1] *= al1; accL[mi][2] *= al0; accL[mi][3] *= al1;
+    }
+    int modeV = md.modeV;
+    uint32_t va[2][8], vb[2][8];
+    if (modeV == GAAC_MODE_SLOT) {
+      int before;
+      if (!range_escape_base(tV, md.escV, warp, lane, before)) {
+        modeV = GAAC_MODE_NONE;
+        if (warp == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
+      } else {
+        // half-unit k = 2*mi + hb: channel c, unit u = 2c + tq/2, half tq%2; its range position
+        // (in half-units) is 64*mi + 32*hb + lane, so each k is a lane-ordered segment of 32.
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(tV + kOffCode);
+        const int hh = tq & 1;
+        uint32_t nib[4];
+        int cnt[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int u = 64 * warp + 32 * (k >> 1) + 16 * (k & 1) + 2 * g + (tq >> 1);
+          nib[k] = (static_cast<uint32_t>(tV[kOffTag + u]) >> (4 * hh)) & 15u;
+          cnt[k] = esc_count(nib[k]);
+        }
+        const int s01 = warp_incl_scan(cnt[0] | (cnt[1] << 16), lane);
+        const int s23 = warp_incl_scan(cnt[2] | (cnt[3] << 16), lane);
+        const int t01 = __shfl_sync(0xFFFFFFFFu, s01, 31), t23 = __shfl_sync(0xFFFFFFFFu, s23, 31);
+        int ho[4];
+        ho[0] = before + (s01 & 0xFFFF) - cnt[0];
+        ho[1] = before + (t01 & 0xFFFF) + (s01 >> 16) - cnt[1];
+        ho[2] = before + (t01 & 0xFFFF) + (t01 >> 16) + (s23 & 0xFFFF) - cnt[2];
+        ho[3] = before + (t01 & 0xFFFF) + (t01 >> 16) + (t23 & 0xFFFF) + (s23 >> 16) - cnt[3];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = 32 * warp + 16 * (k >> 1) + g + 8 * (k & 1);
+          const int u = 2 * c + (tq >> 1);
+          const uint32_t xw = gather_groups<2>(tV + kOffEsc, nib[k], ho[k]);
+          const uint32_t b3[4] = {v3[k], v3[k], v3[k], v3[k]}, b4[4] = {v4[k], v4[k], v4[k], v4[k]};
+          decode_half(tV, cw[256 * hh + u], cw[512 + u], hh, nib[k], xw, ho[k],
+                      *reinterpret_cast<const uint4*>(tV + 64 * c + 16 * tq), b3, b4, sm.lut,
+                      (k & 1) ? vb[k >> 1] : va[k >> 1]);
+        }
+      }
+    }
+    if (modeV == GAAC_MODE_RAW) {
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const int cA = 32 * warp + 16 * mi + g;
+        load8(tV + 128 * cA + 32 * tq, va[mi]);
+        load8(tV + 128 * (cA + 8) + 32 * tq, vb[mi]);
+      }
+    } else if (modeV == GAAC_MODE_NONE) {
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) va[mi][j] = vb[mi][j] = 0u;
+    }
+    if (nv < kBlock) {  // the open tail: tokens past the sequence must not reach the product
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int tt = 16 * tq + 2 * m;
+        const uint32_t keep = (tt < nv ? 0x0000FFFFu : 0u) | (tt + 1 < nv ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+          va[mi][m] &= keep;
+          vb[mi][m] &= keep;
+        }
+      }
+    }
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(acc[mi], va[2 * ks], vb[2 * ks], va[2 * ks + 1], vb[2 * ks + 1], ph[2 * ks], ph[2 * ks + 1]);
-        mma_bf16(acc[mi], va[2 * ks], vb[2 * ks], va[2 * ks + 1], vb[2 * ks + 1], pl[2 * ks], pl[2 * ks + 1]);
+        mma_bf16(accH[mi], va[mi][2 * ks], vb[mi][2 * ks], va[mi][2 * ks + 1], vb[mi][2 * ks + 1], ph[2 * ks],
+                 ph[2 * ks + 1]);
+        mma_bf16(accL[mi], va[mi][2 * ks], vb[mi][2 * ks], va[mi][2 * ks + 1], vb[mi][2 * ks + 1], pl[2 * ks],
+                 pl[2 * ks + 1]);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[st]);
   }
-  if (bad) report(a.status, GAAC_EFORMAT);
-  // Every issued copy was awaited above; after a timed-out wait, wait once
-  // more (bounded) so that no copy is still landing when the CTA exits.
+  // Every issued copy was awaited above; after a timed-out wait, wait once more
+  // (bounded) so that no copy is still landing when the CTA exits.
   if (warp == 0 && lane == 0) {
     for (int i = max(0, n_my - kStages); i < n_my; ++i)
       mbar_wait(&sm.full[i % kStages], (i / kStages) & 1, a.status, 1u << 20);
   }
 
   float* part = a.part + ((static_cast<size_t>(b) * a.Hkv + h) * a.n_splits + split) * kPartFloats;
+  const float mg0 = __shfl_sync(0xFFFFFFFFu, m0, g >> 1), mg1 = __shfl_sync(0xFFFFFFFFu, m1, g >> 1);
   if (warp == 0 && tq == 0) {
-    part[2 * g] = m_run;
-    part[2 * g + 1] = l_run;
+    part[2 * g] = (g & 1) ? mg1 : mg0;
+    part[2 * g + 1] = lg;
   }
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi) {
     const int cA = 32 * warp + 16 * mi + g, cB = cA + 8;
     float* pa = part + 2 * kRPad;
-    pa[(2 * tq) * kD + cA] = acc[mi][0];
-    pa[(2 * tq + 1) * kD + cA] = acc[mi][1];
-    pa[(2 * tq) * kD + cB] = acc[mi][2];
-    pa[(2 * tq + 1) * kD + cB] = acc[mi][3];
+    pa[(2 * tq) * kD + cA] = accH[mi][0] + accL[mi][0];
+    pa[(2 * tq + 1) * kD + cA] = accH[mi][1] + accL[mi][1];
+    pa[(2 * tq) * kD + cB] = accH[mi][2] + accL[mi][2];
+    pa[(2 * tq + 1) * kD + cB] = accH[mi][3] + accL[mi][3];
   }
 }
 
@@ -488,7 +601,7 @@ using namespace gaac;
 
 extern "C" int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_blocks) {
   if (batch <= 0 || n_kv_heads <= 0 || max_blocks <= 0) return 1;
-  const long long target = 2LL * device_sms();  // two CTAs per SM
+  const long long target = static_cast<long long>(kCtasPerSm) * device_sms();  // one wave of resident CTAs
   const long long pairs = static_cast<long long>(batch) * n_kv_heads;
   long long s = (target + pairs - 1) / pairs;
   if (s > max_blocks) s = max_blocks;

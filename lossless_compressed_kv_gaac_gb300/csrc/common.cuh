@@ -101,6 +101,97 @@ __device__ __forceinline__ void half_exponents(uint32_t wh, uint32_t w2, int h, 
   }
 }
 
+// Table entry x: the escape byte x of a 4-bit group spread over two exponent
+// words, bit j of x becoming bit 3 of byte lane j%4 of word j/4.
+__device__ __forceinline__ uint2 spread_entry(uint32_t x) {
+  return make_uint2(spread4(x & 15u) << 3, spread4(x >> 4) << 3);
+}
+
+// Escape bytes of a group with tag m (0: 0, 1: 1, 2: 5; tag 3 counts 6 and is
+// rejected by the caller).
+__device__ __forceinline__ int esc_of_tag(uint32_t m) { return static_cast<int>((m & 1u) + 5u * (m >> 1)); }
+
+// Exponent bytes of one half-unit (two groups of eight), without per-lane
+// branches for the 3-bit and 4-bit modes.  tagnib: the two groups' tags (bits
+// 0-1 first group); b3/b4: base bytes laid out like the codes; esc: escape area
+// of the slot image (esc_len bytes valid); off: escape offset of the first
+// group; lut: 256 spread_entry values.  Raw-mode groups take a rare branch.
+// Sets *bad on a reserved tag or an escape read past esc_len (such bytes read as 0).
+__device__ __forceinline__ void half_exponents_fast(uint32_t wh, uint32_t w2, int h, uint32_t tagnib,
+                                                    const uint32_t b3[4], const uint32_t b4[4],
+                                                    const uint8_t* esc, int off, int esc_len, const uint2* lut,
+                                                    uint32_t e[4], bool* bad) {
+  uint32_t c[4];
+  extract_codes(wh, w2, h, c);
+  const uint32_t m0 = tagnib & 3u, m1 = (tagnib >> 2) & 3u;
+  const int off1 = off + esc_of_tag(m0);
+  const uint32_t x0 = (m0 == 1u && off < esc_len) ? esc[off] : 0u;
+  const uint32_t x1 = (m1 == 1u && off1 < esc_len) ? esc[off1] : 0u;
+  const uint2 s0 = lut[x0], s1 = lut[x1];
+  e[0] = (m0 != 0u ? b4[0] : b3[0]) + c[0] + s0.x;
+  e[1] = (m0 != 0u ? b4[1] : b3[1]) + c[1] + s0.y;
+  e[2] = (m1 != 0u ? b4[2] : b3[2]) + c[2] + s1.x;
+  e[3] = (m1 != 0u ? b4[3] : b3[3]) + c[3] + s1.y;
+  if ((m0 == 1u && off >= esc_len) || (m1 == 1u && off1 >= esc_len)) *bad = true;
+  if (tagnib & 0xAu) {  // a raw-mode (or reserved) group: five escape bit planes
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const uint32_t m = gi == 0 ? m0 : m1;
+      if (m >= 2u) {
+        const int o = gi == 0 ? off : off1;
+        const bool in = m == 2u && o + 5 <= esc_len;
+        if (!in) *bad = true;
+        uint32_t hi0 = 0, hi1 = 0;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+          const uint32_t x = in ? esc[o + k] : 0u;
+          hi0 |= spread4(x & 15u) << (3 + k);
+          hi1 |= spread4(x >> 4) << (3 + k);
+        }
+        e[2 * gi] = c[2 * gi] | hi0;
+        e[2 * gi + 1] = c[2 * gi + 1] | hi1;
+      }
+    }
+  }
+}
+
+// Exponent bytes of one half-unit when the 4-bit-mode escape bytes of its unit
+// have been gathered in advance: xw holds, in byte j, the escape byte of group j
+// of the unit (0 unless that group is in 4-bit mode).  tb: the unit's tag byte;
+// hh: which half.  Raw-mode groups are left for the caller (their words come out
+// as base4 + code).  The tile must have been validated (no reserved tags).
+__device__ __forceinline__ void half_exponents_gathered(uint32_t wh, uint32_t w2, int hh, uint32_t tb, uint32_t xw,
+                                                        const uint32_t b3[4], const uint32_t b4[4],
+                                                        const uint2* lut, uint32_t e[4]) {
+  uint32_t c[4];
+  extract_codes(wh, w2, hh, c);
+  const uint32_t tagnib = (tb >> (4 * hh)) & 15u;
+  const uint32_t xs = xw >> (16 * hh);
+  const uint2 s0 = lut[xs & 0xFFu], s1 = lut[(xs >> 8) & 0xFFu];
+  const bool w0 = (tagnib & 3u) != 0u, w1 = (tagnib & 12u) != 0u;
+  e[0] = (w0 ? b4[0] : b3[0]) + c[0] + s0.x;
+  e[1] = (w0 ? b4[1] : b3[1]) + c[1] + s0.y;
+  e[2] = (w1 ? b4[2] : b3[2]) + c[2] + s1.x;
+  e[3] = (w1 ? b4[3] : b3[3]) + c[3] + s1.y;
+}
+
+// Raw-mode group gi (0/1) of a half-unit: exponent words from the group's five
+// escape bit planes at `esc` (already offset to the group).
+__device__ __forceinline__ void raw_group_exponents(uint32_t wh, uint32_t w2, int hh, int gi, const uint8_t* esc,
+                                                    uint32_t e[4]) {
+  uint32_t c[4];
+  extract_codes(wh, w2, hh, c);
+  uint32_t hi0 = 0, hi1 = 0;
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const uint32_t x = esc[k];
+    hi0 |= spread4(x & 15u) << (3 + k);
+    hi1 |= spread4(x >> 4) << (3 + k);
+  }
+  e[2 * gi] = c[2 * gi] | hi0;
+  e[2 * gi + 1] = c[2 * gi + 1] | hi1;
+}
+
 // Four BF16 values from their sign|mantissa bytes and exponent bytes (byte
 // lane L = element L), returned as two bf16x2 words: p01 = elements {0,1},
 // p23 = elements {2,3} (lower element in the low half).
@@ -134,20 +225,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// One poll; the thread may sleep up to ~20 us inside it (woken early when the
+// phase completes), so a waiting warp takes few issue slots from working warps.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(20000)
       : "memory");
   return ok != 0u;
 }
 
-// Bounded wait: gives up after `limit` polls (each poll may suspend the thread
-// for a short, hardware-chosen time) and reports GAAC_ETIMEOUT.
+// Bounded wait: gives up after `limit` polls and reports GAAC_ETIMEOUT.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
-                                          uint32_t limit = (1u << 20)) {
+                                          uint32_t limit = (1u << 17)) {
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   report(status, GAAC_ETIMEOUT);
