@@ -35,34 +35,42 @@
 
 namespace gaac {
 
-constexpr int kAttWarps = 4;                // consumer warps
-constexpr int kAttThreads = (kAttWarps + 1) * 32;
+// Warp roles: warps 0-3 take K (decode, QK^T, softmax), warps 4-7 take V
+// (decode, PV), warp 8 streams tiles.  K warps run up to two blocks ahead of V
+// warps; P crosses over through a double-buffered shared-memory buffer.
+constexpr int kKWarps = 4, kVWarps = 4;
+constexpr int kProducerWarp = kKWarps + kVWarps;
+constexpr int kAttThreads = (kProducerWarp + 1) * 32;
 #ifndef GAAC_ATT_STAGES
-#define GAAC_ATT_STAGES 2
+#define GAAC_ATT_STAGES 3
 #endif
 #ifndef GAAC_ATT_CTAS_PER_SM
-#define GAAC_ATT_CTAS_PER_SM 3
+#define GAAC_ATT_CTAS_PER_SM 2
 #endif
 constexpr int kStages = GAAC_ATT_STAGES;
 constexpr int kCtasPerSm = GAAC_ATT_CTAS_PER_SM;
-constexpr int kStageBytes = 2 * kRawBytes;  // K region + V region
-constexpr int kRPad = 8;                    // query heads per kv-head in the MMA N dimension
-constexpr int kPStride = 72;                // bf16 per head row of the probability buffer (64 + pad)
+constexpr int kRPad = 8;     // query heads per kv-head in the MMA N dimension
+constexpr int kPStride = 72;  // bf16 per head row of the probability buffer (64 + pad)
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
+// named barriers (0 is __syncthreads)
+constexpr int kBarK = 1;           // the 4 K warps
+constexpr int kBarPFull = 2;       // + parity: P of a block written (K arrive, V sync)
+constexpr int kBarPEmpty = 4;      // + parity: P of a block read (V arrive, K sync)
 
-struct StageMeta {
-  int modeK, modeV, escK, escV;
+struct TileMeta {
+  int mode, esc;
 };
 
 struct AttSmem {
-  alignas(128) uint8_t stage[kStages][kStageBytes];
+  alignas(128) uint8_t ringK[kStages][kRawBytes];
+  alignas(128) uint8_t ringV[kStages][kRawBytes];
   alignas(16) uint16_t P[2][2][kRPad][kPStride];  // [block parity][hi, lo][head][token] bf16 probabilities
-  alignas(16) float wmax[2][kRPad][kAttWarps];     // [parity][head][warp] max of the warp's 16 scores
-  alignas(16) float wsum[2][kRPad][kAttWarps];     // [parity][head][warp] sum of the warp's 16 probabilities
+  alignas(16) float wmax[2][kRPad][kKWarps];       // [parity][head][K warp] max over the warp's 16 scores
+  alignas(16) float wsum[2][kRPad][kKWarps];       // [parity][head][K warp] sum of the warp's 16 probabilities
+  alignas(16) float alpha[2][kRPad];               // [parity][head] rescale factor of the running sums
   uint2 lut[256];                                  // escape byte -> spread bits of a 4-bit group
-  StageMeta meta[kStages];
-  uint64_t full[kStages];   // bulk copies landed
-  uint64_t empty[kStages];  // consumers done with the stage
+  TileMeta metaK[kStages], metaV[kStages];
+  uint64_t fullK[kStages], emptyK[kStages], fullV[kStages], emptyV[kStages];
 };
 
 struct AttnArgs {
@@ -193,6 +201,49 @@ __device__ __forceinline__ void load8(const uint8_t* p, uint32_t out[8]) {
   out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
 }
 
+__device__ __forceinline__ void named_bar_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Producer lane for one tile kind (kv 0 = K, 1 = V): streams the tile of every
+// block of the split into its ring, prefetching the next table entry while it
+// waits for a free slot.
+__device__ __forceinline__ void stream_tiles(const AttnArgs& a, AttSmem& sm, int kv, int b, int h, int blk0, int n_my) {
+  const gaac_entry* tab = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk0) * a.Hkv + h) * 2 + kv;
+  const size_t stride = static_cast<size_t>(a.Hkv) * 2;
+  uint8_t(*ring)[kRawBytes] = kv ? sm.ringV : sm.ringK;
+  TileMeta* meta = kv ? sm.metaV : sm.metaK;
+  uint64_t* full = kv ? sm.fullV : sm.fullK;
+  uint64_t* empty = kv ? sm.emptyV : sm.emptyK;
+  uint2 cur = make_uint2(0u, 0u);
+  if (n_my > 0) cur = *reinterpret_cast<const uint2*>(tab);
+  for (int j = 0; j < n_my; ++j) {
+    uint2 nxt = cur;
+    if (j + 1 < n_my) nxt = *reinterpret_cast<const uint2*>(tab + (j + 1) * stride);
+    const int st = j % kStages;
+    if (j >= kStages) mbar_wait(&empty[st], ((j / kStages) & 1) ^ 1, a.status);
+    const uint32_t index = cur.x, esc_len = cur.y & 0xFFFFu, emode = (cur.y >> 16) & 0xFFu;
+    uint32_t bytes = 0;
+    const void* src = nullptr;
+    TileMeta tm{GAAC_MODE_NONE, 0};
+    if (emode == GAAC_MODE_SLOT && static_cast<int64_t>(index) < a.n_slots && esc_len <= kEscCap) {
+      tm = TileMeta{GAAC_MODE_SLOT, static_cast<int>(esc_len)};
+      bytes = kOffEsc + ((esc_len + 15u) & ~15u);
+      src = a.slot_pool + static_cast<size_t>(index) * kSlot;
+    } else if (emode == GAAC_MODE_RAW && static_cast<int64_t>(index) < a.n_raw) {
+      tm = TileMeta{GAAC_MODE_RAW, 0};
+      bytes = kRawBytes;
+      src = a.raw_pool + static_cast<size_t>(index) * kTile;
+    } else {
+      report(a.status, GAAC_EFORMAT);
+    }
+    meta[st] = tm;
+    mbar_arrive_expect_tx(&full[st], bytes);
+    if (bytes) bulk_g2s(ring[st], src, bytes, &full[st]);
+    cur = nxt;
+  }
+}
+
 __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   AttSmem& sm = *reinterpret_cast<AttSmem*>(smem_raw);
@@ -212,99 +263,186 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kAttWarps);
+      mbar_init(&sm.fullK[s], 1);
+      mbar_init(&sm.fullV[s], 1);
+      mbar_init(&sm.emptyK[s], kKWarps);
+      mbar_init(&sm.emptyV[s], kVWarps);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kAttWarps) {  // ------------------------------------------------ producer warp
-    // Table entries of 32 blocks at a time, one block per lane.
-    const gaac_entry* tab = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk0) * a.Hkv + h) * 2;
-    const size_t blk_stride = static_cast<size_t>(a.Hkv) * 2;
-    uint2 ek = make_uint2(0, GAAC_MODE_NONE << 16), ev = ek;
-    for (int i = 0; i < n_my; ++i) {
-      if ((i & 31) == 0) {
-        const int j = i + lane;
-        if (j < n_my) {
-          ek = *reinterpret_cast<const uint2*>(tab + j * blk_stride);
-          ev = *reinterpret_cast<const uint2*>(tab + j * blk_stride + 1);
-        }
-      }
-      const uint32_t k0 = __shfl_sync(0xFFFFFFFFu, ek.x, i & 31), k1 = __shfl_sync(0xFFFFFFFFu, ek.y, i & 31);
-      const uint32_t v0 = __shfl_sync(0xFFFFFFFFu, ev.x, i & 31), v1 = __shfl_sync(0xFFFFFFFFu, ev.y, i & 31);
-      if (lane == 0) {
-        const int st = i % kStages;
-        if (i >= kStages) mbar_wait(&sm.empty[st], ((i / kStages) & 1) ^ 1, a.status);
-        uint32_t bytes[2];
-        const void* src[2];
-        int mode[2], esc[2];
+  const int g = lane >> 2, tq = lane & 3;
+  const int r = a.r;
+  float* part = a.part + ((static_cast<size_t>(b) * a.Hkv + h) * a.n_splits + split) * kPartFloats;
+
+  if (warp == kProducerWarp) {  // ------------------------------------------------ producer
+    if (lane < 2) stream_tiles(a, sm, lane, b, h, blk0, n_my);
+    return;
+  }
+
+  if (warp < kKWarps) {  // ------------------------------------------------------- K warps
+    const int kw = warp;
+    uint32_t qf[16];
+    if (g < r) {
+      const uint4* qp =
+          reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + h * r + g) * kD + 32 * tq);
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t index = kv ? v0 : k0, w1 = kv ? v1 : k1;
-          const uint32_t esc_len = w1 & 0xFFFFu, emode = (w1 >> 16) & 0xFFu;
-          bytes[kv] = 0;
-          src[kv] = nullptr;
-          esc[kv] = 0;
-          if (emode == GAAC_MODE_SLOT && static_cast<int64_t>(index) < a.n_slots && esc_len <= kEscCap) {
-            mode[kv] = GAAC_MODE_SLOT;
-            esc[kv] = static_cast<int>(esc_len);
-            bytes[kv] = kOffEsc + ((esc_len + 15u) & ~15u);
-            src[kv] = a.slot_pool + static_cast<size_t>(index) * kSlot;
-          } else if (emode == GAAC_MODE_RAW && static_cast<int64_t>(index) < a.n_raw) {
-            mode[kv] = GAAC_MODE_RAW;
-            bytes[kv] = kRawBytes;
-            src[kv] = a.raw_pool + static_cast<size_t>(index) * kTile;
-          } else {
-            mode[kv] = GAAC_MODE_NONE;
-            report(a.status, GAAC_EFORMAT);
+      for (int i = 0; i < 4; ++i) {
+        const uint4 w = qp[i];
+        qf[4 * i] = bf16x2_div16(w.x);
+        qf[4 * i + 1] = bf16x2_div16(w.y);
+        qf[4 * i + 2] = bf16x2_div16(w.z);
+        qf[4 * i + 3] = bf16x2_div16(w.w);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) qf[i] = 0u;
+    }
+    uint32_t k3[8], k4[8];
+    {
+      const uint4* p3 = reinterpret_cast<const uint4*>(a.base3 + h * kD + 32 * tq);
+      const uint4* p4 = reinterpret_cast<const uint4*>(a.base4 + h * kD + 32 * tq);
+      const uint4 x0 = p3[0], x1 = p3[1], y0 = p4[0], y1 = p4[1];
+      k3[0] = x0.x; k3[1] = x0.y; k3[2] = x0.z; k3[3] = x0.w;
+      k3[4] = x1.x; k3[5] = x1.y; k3[6] = x1.z; k3[7] = x1.w;
+      k4[0] = y0.x; k4[1] = y0.y; k4[2] = y0.z; k4[3] = y0.w;
+      k4[4] = y1.x; k4[5] = y1.y; k4[6] = y1.z; k4[7] = y1.w;
+    }
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads 2tq, 2tq+1 (log2 domain)
+    const int t0 = 16 * kw + g, t1 = t0 + 8;
+    for (int i = 0; i < n_my; ++i) {
+      const int st = i % kStages, par = i & 1;
+      mbar_wait(&sm.fullK[st], (i / kStages) & 1, a.status);
+      const TileMeta md = sm.metaK[st];
+      const int nv = min(kBlock, len - (blk0 + i) * kBlock);
+      const uint8_t* tK = sm.ringK[st];
+      int modeK = md.mode;
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      if (modeK == GAAC_MODE_SLOT) {
+        int before;
+        if (!range_escape_base(tK, md.esc, kw, lane, before)) {
+          modeK = GAAC_MODE_NONE;
+          if (kw == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
+        } else {
+          // this lane's units: uA = 4*t0 + tq = 64kw + lane, uB = uA + 32 (range positions lane, lane + 32)
+          const uint32_t tbA = tK[kOffTag + 64 * kw + lane], tbB = tK[kOffTag + 64 * kw + 32 + lane];
+          const int cA = esc_count(tbA), cB = esc_count(tbB);
+          const int sc = warp_incl_scan(cA | (cB << 16), lane);
+          const int totA = __shfl_sync(0xFFFFFFFFu, sc, 31) & 0xFFFF;
+          const int offA = before + (sc & 0xFFFF) - cA;
+          const int offB = before + totA + (sc >> 16) - cB;
+          const uint32_t xA = gather_groups<4>(tK + kOffEsc, tbA, offA);
+          const uint32_t xB = gather_groups<4>(tK + kOffEsc, tbB, offB);
+          const uint32_t* cw = reinterpret_cast<const uint32_t*>(tK + kOffCode);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t ka[8], kb[8];
+            const int uA = 4 * t0 + tq, uB = 4 * t1 + tq;
+            const uint32_t nibA = (tbA >> (4 * hh)) & 15u, nibB = (tbB >> (4 * hh)) & 15u;
+            const int hoA = offA + (hh ? esc_count(tbA & 15u) : 0), hoB = offB + (hh ? esc_count(tbB & 15u) : 0);
+            decode_half(tK, cw[256 * hh + uA], cw[512 + uA], hh, nibA, xA >> (16 * hh), hoA,
+                        *reinterpret_cast<const uint4*>(tK + 128 * t0 + 32 * tq + 16 * hh), k3 + 4 * hh,
+                        k4 + 4 * hh, sm.lut, ka);
+            decode_half(tK, cw[256 * hh + uB], cw[512 + uB], hh, nibB, xB >> (16 * hh), hoB,
+                        *reinterpret_cast<const uint4*>(tK + 128 * t1 + 32 * tq + 16 * hh), k3 + 4 * hh,
+                        k4 + 4 * hh, sm.lut, kb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int ks = 4 * hh + j;
+              mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks],
+                       qf[2 * ks + 1]);
+            }
           }
         }
-        sm.meta[st] = StageMeta{mode[0], mode[1], esc[0], esc[1]};
-        mbar_arrive_expect_tx(&sm.full[st], bytes[0] + bytes[1]);
-        if (bytes[0]) bulk_g2s(sm.stage[st], src[0], bytes[0], &sm.full[st]);
-        if (bytes[1]) bulk_g2s(sm.stage[st] + kRawBytes, src[1], bytes[1], &sm.full[st]);
+      } else if (modeK == GAAC_MODE_RAW) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t ka[8], kb[8];
+          load8(tK + 256 * t0 + 64 * tq + 32 * hh, ka);
+          load8(tK + 256 * t1 + 64 * tq + 32 * hh, kb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ks = 4 * hh + j;
+            mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks], qf[2 * ks + 1]);
+          }
+        }
       }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.emptyK[st]);  // the K tile is no longer read
+      const bool ok0 = t0 < nv && modeK != GAAC_MODE_NONE, ok1 = t1 < nv && modeK != GAAC_MODE_NONE;
+      // scores: (t0, head 2tq), (t0, 2tq+1), (t1, 2tq), (t1, 2tq+1)
+      const float s0 = ok0 ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
+      const float s1 = ok0 ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
+      const float s2 = ok1 ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
+      const float s3 = ok1 ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
+      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int d = 4; d < 32; d <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, d));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, d));
+      }
+      if (g == 0) {
+        sm.wmax[par][2 * tq][kw] = x0;
+        sm.wmax[par][2 * tq + 1][kw] = x1;
+      }
+      named_bar_sync(kBarK, kKWarps * 32);
+      const float4 wa = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq][0]);
+      const float4 wb = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq + 1][0]);
+      const float n0 = fmaxf(m0, fmaxf(fmaxf(wa.x, wa.y), fmaxf(wa.z, wa.w)));
+      const float n1 = fmaxf(m1, fmaxf(fmaxf(wb.x, wb.y), fmaxf(wb.z, wb.w)));
+      const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
+      const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
+      const float p0 = n0 == -INFINITY ? 0.f : fast_exp2(s0 - n0);
+      const float p2 = n0 == -INFINITY ? 0.f : fast_exp2(s2 - n0);
+      const float p1 = n1 == -INFINITY ? 0.f : fast_exp2(s1 - n1);
+      const float p3 = n1 == -INFINITY ? 0.f : fast_exp2(s3 - n1);
+      m0 = n0;
+      m1 = n1;
+      float y0 = p0 + p2, y1 = p1 + p3;
+#pragma unroll
+      for (int d = 4; d < 32; d <<= 1) {
+        y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, d);
+        y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, d);
+      }
+      if (i >= 2) named_bar_sync(kBarPEmpty + par, (kKWarps + kVWarps) * 32);  // V warps are done with P[par]
+      if (g == 0) {
+        sm.wsum[par][2 * tq][kw] = y0;
+        sm.wsum[par][2 * tq + 1][kw] = y1;
+        if (kw == 0) {
+          sm.alpha[par][2 * tq] = al0;
+          sm.alpha[par][2 * tq + 1] = al1;
+        }
+      }
+      {
+        uint16_t* Ph = &sm.P[par][0][0][0];
+        uint16_t* Pl = &sm.P[par][1][0][0];
+        const float pv[4] = {p0, p1, p2, p3};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int head = 2 * tq + (j & 1), tok = j < 2 ? t0 : t1;
+          const uint16_t hb = to_bf16(pv[j]);
+          Ph[head * kPStride + tok] = hb;
+          Pl[head * kPStride + tok] = to_bf16(pv[j] - __uint_as_float(static_cast<uint32_t>(hb) << 16));
+        }
+      }
+      named_bar_arrive(kBarPFull + par, (kKWarps + kVWarps) * 32);
+    }
+    if (kw == 0 && g == 0) {
+      part[4 * tq] = m0;      // head 2tq
+      part[4 * tq + 2] = m1;  // head 2tq + 1
     }
     return;
   }
 
-  // ------------------------------------------------------------------------- consumers
-  const int g = lane >> 2, tq = lane & 3;
-  const int r = a.r;
-  uint32_t qf[16];
-  if (g < r) {
-    const uint4* qp = reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + h * r + g) * kD + 32 * tq);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 w = qp[i];
-      qf[4 * i] = bf16x2_div16(w.x);
-      qf[4 * i + 1] = bf16x2_div16(w.y);
-      qf[4 * i + 2] = bf16x2_div16(w.z);
-      qf[4 * i + 3] = bf16x2_div16(w.w);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) qf[i] = 0u;
-  }
-  uint32_t k3[8], k4[8];
-  {
-    const uint4* p3 = reinterpret_cast<const uint4*>(a.base3 + h * kD + 32 * tq);
-    const uint4* p4 = reinterpret_cast<const uint4*>(a.base4 + h * kD + 32 * tq);
-    const uint4 x0 = p3[0], x1 = p3[1], y0 = p4[0], y1 = p4[1];
-    k3[0] = x0.x; k3[1] = x0.y; k3[2] = x0.z; k3[3] = x0.w;
-    k3[4] = x1.x; k3[5] = x1.y; k3[6] = x1.z; k3[7] = x1.w;
-    k4[0] = y0.x; k4[1] = y0.y; k4[2] = y0.z; k4[3] = y0.w;
-    k4[4] = y1.x; k4[5] = y1.y; k4[6] = y1.z; k4[7] = y1.w;
-  }
-  uint32_t v3[4], v4[4];  // [mi*2 + hb]: channel 32warp + 16mi + g + 8hb, byte replicated
+  // ------------------------------------------------------------------------------------ V warps
+  const int vw = warp - kKWarps;
+  uint32_t v3[4], v4[4];  // [mi*2 + hb]: channel 32vw + 16mi + g + 8hb, byte replicated
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi) {
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
-      const int c = 32 * warp + 16 * mi + g + 8 * hb;
+      const int c = 32 * vw + 16 * mi + g + 8 * hb;
       v3[2 * mi + hb] = 0x01010101u * a.base3[(a.Hkv + h) * kD + c];
       v4[2 * mi + hb] = 0x01010101u * a.base4[(a.Hkv + h) * kD + c];
     }
@@ -314,145 +452,20 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
     for (int j = 0; j < 4; ++j) accH[mi][j] = accL[mi][j] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads 2tq, 2tq+1 (log2 domain)
-  float lg = 0.f;                        // running sum of head g
-  const int t0 = 16 * warp + g, t1 = t0 + 8;
-
+  float lg = 0.f;  // running sum of head g
   for (int i = 0; i < n_my; ++i) {
     const int st = i % kStages, par = i & 1;
-    mbar_wait(&sm.full[st], (i / kStages) & 1, a.status);
-    const StageMeta md = sm.meta[st];
+    mbar_wait(&sm.fullV[st], (i / kStages) & 1, a.status);
+    const TileMeta md = sm.metaV[st];
     const int nv = min(kBlock, len - (blk0 + i) * kBlock);
-    const uint8_t* tK = sm.stage[st];
-    const uint8_t* tV = tK + kRawBytes;
-
-    // ---------------- K: S = (q/16) K^T for tokens t0, t1
-    int modeK = md.modeK;
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    if (modeK == GAAC_MODE_SLOT) {
-      int before;
-      if (!range_escape_base(tK, md.escK, warp, lane, before)) {
-        modeK = GAAC_MODE_NONE;
-        if (warp == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
-      } else {
-        // this lane's units: uA = 4*t0 + tq = 64w + lane, uB = uA + 32 (range positions lane, lane + 32)
-        const uint32_t tbA = tK[kOffTag + 64 * warp + lane], tbB = tK[kOffTag + 64 * warp + 32 + lane];
-        const int cA = esc_count(tbA), cB = esc_count(tbB);
-        const int sc = warp_incl_scan(cA | (cB << 16), lane);
-        const int totA = __shfl_sync(0xFFFFFFFFu, sc, 31) & 0xFFFF;
-        const int offA = before + (sc & 0xFFFF) - cA;
-        const int offB = before + totA + (sc >> 16) - cB;
-        const uint32_t xA = gather_groups<4>(tK + kOffEsc, tbA, offA);
-        const uint32_t xB = gather_groups<4>(tK + kOffEsc, tbB, offB);
-        const uint32_t* cw = reinterpret_cast<const uint32_t*>(tK + kOffCode);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t ka[8], kb[8];
-          const int uA = 4 * t0 + tq, uB = 4 * t1 + tq;
-          const uint32_t nibA = (tbA >> (4 * hh)) & 15u, nibB = (tbB >> (4 * hh)) & 15u;
-          const int hoA = offA + (hh ? esc_count(tbA & 15u) : 0), hoB = offB + (hh ? esc_count(tbB & 15u) : 0);
-          decode_half(tK, cw[256 * hh + uA], cw[512 + uA], hh, nibA, xA >> (16 * hh), hoA,
-                      *reinterpret_cast<const uint4*>(tK + 128 * t0 + 32 * tq + 16 * hh), k3 + 4 * hh, k4 + 4 * hh,
-                      sm.lut, ka);
-          decode_half(tK, cw[256 * hh + uB], cw[512 + uB], hh, nibB, xB >> (16 * hh), hoB,
-                      *reinterpret_cast<const uint4*>(tK + 128 * t1 + 32 * tq + 16 * hh), k3 + 4 * hh, k4 + 4 * hh,
-                      sm.lut, kb);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int ks = 4 * hh + j;
-            mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks], qf[2 * ks + 1]);
-          }
-        }
-      }
-    } else if (modeK == GAAC_MODE_RAW) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t ka[8], kb[8];
-        load8(tK + 256 * t0 + 64 * tq + 32 * hh, ka);
-        load8(tK + 256 * t1 + 64 * tq + 32 * hh, kb);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ks = 4 * hh + j;
-          mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks], qf[2 * ks + 1]);
-        }
-      }
-    }
-    const bool ok0 = t0 < nv && modeK != GAAC_MODE_NONE, ok1 = t1 < nv && modeK != GAAC_MODE_NONE;
-    // s[0]: (t0, head 2tq), s[1]: (t0, 2tq+1), s[2]: (t1, 2tq), s[3]: (t1, 2tq+1)
-    const float s0 = ok0 ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
-    const float s1 = ok0 ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
-    const float s2 = ok1 ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
-    const float s3 = ok1 ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
-
-    // ---------------- softmax: block max over the 4 warps' slices
-    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
-#pragma unroll
-    for (int d = 4; d < 32; d <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, d));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, d));
-    }
-    if (g == 0) {
-      sm.wmax[par][2 * tq][warp] = x0;
-      sm.wmax[par][2 * tq + 1][warp] = x1;
-    }
-    named_bar_sync(1, kAttWarps * 32);
-    const float4 wa = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq][0]);
-    const float4 wb = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq + 1][0]);
-    const float n0 = fmaxf(m0, fmaxf(fmaxf(wa.x, wa.y), fmaxf(wa.z, wa.w)));
-    const float n1 = fmaxf(m1, fmaxf(fmaxf(wb.x, wb.y), fmaxf(wb.z, wb.w)));
-    const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
-    const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
-    const float p0 = n0 == -INFINITY ? 0.f : fast_exp2(s0 - n0);
-    const float p2 = n0 == -INFINITY ? 0.f : fast_exp2(s2 - n0);
-    const float p1 = n1 == -INFINITY ? 0.f : fast_exp2(s1 - n1);
-    const float p3 = n1 == -INFINITY ? 0.f : fast_exp2(s3 - n1);
-    m0 = n0;
-    m1 = n1;
-    float y0 = p0 + p2, y1 = p1 + p3;
-#pragma unroll
-    for (int d = 4; d < 32; d <<= 1) {
-      y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, d);
-      y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, d);
-    }
-    if (g == 0) {
-      sm.wsum[par][2 * tq][warp] = y0;
-      sm.wsum[par][2 * tq + 1][warp] = y1;
-    }
-    {
-      uint16_t* Ph = &sm.P[par][0][0][0];
-      uint16_t* Pl = &sm.P[par][1][0][0];
-      const float pv[4] = {p0, p1, p2, p3};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int head = 2 * tq + (j & 1), tok = j < 2 ? t0 : t1;
-        const uint16_t hb = to_bf16(pv[j]);
-        Ph[head * kPStride + tok] = hb;
-        Pl[head * kPStride + tok] = to_bf16(pv[j] - __uint_as_float(static_cast<uint32_t>(hb) << 16));
-      }
-    }
-    named_bar_sync(1, kAttWarps * 32);
-
-    // ---------------- PV: O^T += V^T P^T for channels 32warp + 16mi + {g, g+8}
-    uint32_t ph[8], pl[8];
-    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][0][g][16 * tq]), ph);
-    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][1][g][16 * tq]), pl);
-    {
-      const float4 ws = *reinterpret_cast<const float4*>(&sm.wsum[par][g][0]);
-      const float a0s = __shfl_sync(0xFFFFFFFFu, al0, g >> 1), a1s = __shfl_sync(0xFFFFFFFFu, al1, g >> 1);
-      lg = lg * ((g & 1) ? a1s : a0s) + ((ws.x + ws.y) + (ws.z + ws.w));
-    }
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      accH[mi][0] *= al0; accH[mi][1] *= al1; accH[mi][2] *= al0; accH[mi][3] *= al1;
-      accL[mi][0] *= al0; accL[mi][1] *= al1; accL[mi][2] *= al0; accL[mi][3] *= al1;
-    }
-    int modeV = md.modeV;
+    const uint8_t* tV = sm.ringV[st];
+    int modeV = md.mode;
     uint32_t va[2][8], vb[2][8];
     if (modeV == GAAC_MODE_SLOT) {
       int before;
-      if (!range_escape_base(tV, md.escV, warp, lane, before)) {
+      if (!range_escape_base(tV, md.esc, vw, lane, before)) {
         modeV = GAAC_MODE_NONE;
-        if (warp == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
+        if (vw == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
       } else {
         // half-unit k = 2*mi + hb: channel c, unit u = 2c + tq/2, half tq%2; its range position
         // (in half-units) is 64*mi + 32*hb + lane, so each k is a lane-ordered segment of 32.
@@ -462,7 +475,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
         int cnt[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int u = 64 * warp + 32 * (k >> 1) + 16 * (k & 1) + 2 * g + (tq >> 1);
+          const int u = 64 * vw + 32 * (k >> 1) + 16 * (k & 1) + 2 * g + (tq >> 1);
           nib[k] = (static_cast<uint32_t>(tV[kOffTag + u]) >> (4 * hh)) & 15u;
           cnt[k] = esc_count(nib[k]);
         }
@@ -476,7 +489,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
         ho[3] = before + (t01 & 0xFFFF) + (t01 >> 16) + (t23 & 0xFFFF) + (s23 >> 16) - cnt[3];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int c = 32 * warp + 16 * (k >> 1) + g + 8 * (k & 1);
+          const int c = 32 * vw + 16 * (k >> 1) + g + 8 * (k & 1);
           const int u = 2 * c + (tq >> 1);
           const uint32_t xw = gather_groups<2>(tV + kOffEsc, nib[k], ho[k]);
           const uint32_t b3[4] = {v3[k], v3[k], v3[k], v3[k]}, b4[4] = {v4[k], v4[k], v4[k], v4[k]};
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     if (modeV == GAAC_MODE_RAW) {
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi) {
-        const int cA = 32 * warp + 16 * mi + g;
+        const int cA = 32 * vw + 16 * mi + g;
         load8(tV + 128 * cA + 32 * tq, va[mi]);
         load8(tV + 128 * (cA + 8) + 32 * tq, vb[mi]);
       }
@@ -499,6 +512,8 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
 #pragma unroll
         for (int j = 0; j < 8; ++j) va[mi][j] = vb[mi][j] = 0u;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.emptyV[st]);  // the V tile is no longer read
     if (nv < kBlock) {  // the open tail: tokens past the sequence must not reach the product
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -511,8 +526,18 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
         }
       }
     }
+    named_bar_sync(kBarPFull + par, (kKWarps + kVWarps) * 32);  // P of block i is written
+    uint32_t ph[8], pl[8];
+    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][0][g][16 * tq]), ph);
+    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][1][g][16 * tq]), pl);
+    const float4 ws = *reinterpret_cast<const float4*>(&sm.wsum[par][g][0]);
+    const float alg = sm.alpha[par][g], al0 = sm.alpha[par][2 * tq], al1 = sm.alpha[par][2 * tq + 1];
+    if (i + 2 < n_my) named_bar_arrive(kBarPEmpty + par, (kKWarps + kVWarps) * 32);
+    lg = lg * alg + ((ws.x + ws.y) + (ws.z + ws.w));
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi) {
+      accH[mi][0] *= al0; accH[mi][1] *= al1; accH[mi][2] *= al0; accH[mi][3] *= al1;
+      accL[mi][0] *= al0; accL[mi][1] *= al1; accL[mi][2] *= al0; accL[mi][3] *= al1;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma_bf16(accH[mi], va[mi][2 * ks], vb[mi][2 * ks], va[mi][2 * ks + 1], vb[mi][2 * ks + 1], ph[2 * ks],
@@ -521,25 +546,20 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
                  pl[2 * ks + 1]);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[st]);
   }
-  // Every issued copy was awaited above; after a timed-out wait, wait once more
-  // (bounded) so that no copy is still landing when the CTA exits.
-  if (warp == 0 && lane == 0) {
-    for (int i = max(0, n_my - kStages); i < n_my; ++i)
-      mbar_wait(&sm.full[i % kStages], (i / kStages) & 1, a.status, 1u << 20);
+  // Every issued copy was awaited (K warps and V warps consumed every stage);
+  // after a timed-out wait, wait once more (bounded) so that no copy is still
+  // landing when the CTA exits.
+  if (vw == 0 && lane == 0) {
+    for (int i = max(0, n_my - kStages); i < n_my; ++i) {
+      mbar_wait(&sm.fullK[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
+      mbar_wait(&sm.fullV[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
+    }
   }
-
-  float* part = a.part + ((static_cast<size_t>(b) * a.Hkv + h) * a.n_splits + split) * kPartFloats;
-  const float mg0 = __shfl_sync(0xFFFFFFFFu, m0, g >> 1), mg1 = __shfl_sync(0xFFFFFFFFu, m1, g >> 1);
-  if (warp == 0 && tq == 0) {
-    part[2 * g] = (g & 1) ? mg1 : mg0;
-    part[2 * g + 1] = lg;
-  }
+  if (vw == 0 && tq == 0) part[2 * g + 1] = lg;
 #pragma unroll
   for (int mi = 0; mi < 2; ++mi) {
-    const int cA = 32 * warp + 16 * mi + g, cB = cA + 8;
+    const int cA = 32 * vw + 16 * mi + g, cB = cA + 8;
     float* pa = part + 2 * kRPad;
     pa[(2 * tq) * kD + cA] = accH[mi][0] + accL[mi][0];
     pa[(2 * tq + 1) * kD + cA] = accH[mi][1] + accL[mi][1];
