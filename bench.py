@@ -34,7 +34,7 @@ CONFIG_ID = 1
 
 # DRAM bytes (read + write) of one attn_split_kernel launch on this workload, from an
 # ncu capture, valid only for the kernel source it was taken on (see profiles/).
-NCU_TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+NCU_TRAFFIC = {"kernel_sha": "9d964ca8c61069b1", "bytes_per_launch": 194483712}
 
 
 def kernel_sha() -> str:
@@ -53,7 +53,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="gaac", choices=["gaac", "reference"])
     p.add_argument("--layers", type=int, default=36, help="layers per step (36 = the Qwen3-8B workload)")
-    p.add_argument("--cpu-units", type=int, default=6, help="(layer, kv-head) units in the CPU oracle sample")
+    p.add_argument("--cpu-units", type=int, default=48, help="(layer, kv-head) units in the CPU oracle sample")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return p.parse_args()
 

@@ -247,3 +247,75 @@ def test_device_errors_are_reported_not_faulted():
     with pytest.raises(G.GaacError):
         G.decode_attention(W.make_q(0, 3, 2, 80, device="cuda"), c.seq_lens, c.table, c.pools, c.base3, c.base4,
                            0.1, torch.empty(2, 80, 128, device="cuda"), c.workspace())
+
+
+def test_full_size_config2_paged():
+    """Config 2 sizes, one layer: batch 32, lengths uniform in [4096, 32768], 16q/8kv, full blocks
+    scattered over a shared slot pool by a seeded permutation."""
+    B, H, Hq, maxT = 32, 8, 16, 32768
+    lens = W.make_lengths(2, B, 4096, maxT, device="cuda")
+    k, v = U.kv(2, 0, B, maxT, H)
+    max_blocks = maxT // 64
+    positions = B * max_blocks * H * 2
+    perm = W.slot_permutation(2, 0, positions, device="cuda").to(torch.int32)
+    c = U.build(k, v, lens, slot_ids=perm.view(B, max_blocks, H, 2), n_slots=positions)
+    assert _status(c) == 0
+    rng = np.random.default_rng(2)
+    lens_np = lens.cpu().numpy()
+    tiles = []
+    for _ in range(300):
+        b = int(rng.integers(0, B))
+        tiles.append((b, int(rng.integers(0, (lens_np[b] + 63) // 64)), int(rng.integers(0, H)), int(rng.integers(0, 2))))
+    U.check_tiles(c, k, v, lens, tiles=tiles)
+    kd, vd = c.decompress(maxT)
+    for b in range(B):
+        L = int(lens_np[b])
+        assert torch.equal(kd[b, :L].view(torch.int16), k[b, :L].view(torch.int16))
+        assert torch.equal(vd[b, :L].view(torch.int16), v[b, :L].view(torch.int16))
+    del kd, vd
+    q = W.make_q(2, 0, B, Hq, device="cuda")
+    out = c.attention(q, 1 / np.sqrt(128))
+    assert _status(c) == 0
+    U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128), seqs=[0, 7, 19, 31])
+
+
+def test_full_size_config3_incremental():
+    """Config 3 sizes, one layer: batch 8, prefill 32768 tokens, then 256 decode steps that each append
+    one token per sequence and attend; the final compressed bytes equal a one-shot encode of the cache."""
+    B, H, Hq, T0, steps = 8, 8, 16, 32768, 256
+    T = T0 + steps
+    k, v = U.kv(3, 0, B, T, H)
+    max_blocks = T // 64
+    inc = LayerCache(B, H, max_blocks)
+    inc.calibrate(k[0, :512], v[0, :512])
+    inc.encode(k[:, :T0], v[:, :T0], U.lens_tensor([T0] * B))
+    q = W.make_q(3, 0, B, Hq, device="cuda")
+    for s in range(steps):
+        inc.append(k[:, T0 + s].contiguous(), v[:, T0 + s].contiguous())
+        out = inc.attention(q, 1 / np.sqrt(128))
+        if s in (0, 63, 255):
+            torch.cuda.synchronize()
+            L = T0 + s + 1
+            U.check_attention(out, q, k[:, :L], v[:, :L], U.lens_tensor([L] * B), 1 / np.sqrt(128), seqs=[0, 5])
+    assert _status(inc) == 0
+    assert inc.seq_lens.tolist() == [T] * B
+    one = LayerCache(B, H, max_blocks)
+    one.base3.copy_(inc.base3)
+    one.base4.copy_(inc.base4)
+    one.encode(k, v, U.lens_tensor([T] * B))
+    torch.cuda.synchronize()
+    assert _status(one) == 0
+    # compare every logical tile: same mode and escape length, same slot or raw bytes
+    ia, ea, ma, na = inc.fields()
+    ib, eb, mb, nb = one.fields()
+    assert torch.equal(ma, mb) and torch.equal(ea, eb) and torch.equal(na, nb)
+    slot = ma == G.MODE_SLOT
+    assert bool(slot.all()), "every block of the final cache is full and compressible"
+    sa = inc.pools.slot_pool[ia[slot].long()]
+    sb = one.pools.slot_pool[ib[slot].long()]
+    assert torch.equal(sa, sb)
+    b3, b4 = inc.base3.cpu().numpy(), inc.base4.cpu().numpy()
+    rng = np.random.default_rng(3)
+    tiles = [(int(rng.integers(0, B)), int(rng.integers(0, max_blocks)), int(rng.integers(0, H)),
+              int(rng.integers(0, 2))) for _ in range(100)]
+    U.check_tiles(inc, k, v, inc.seq_lens, tiles=tiles, b3=b3, b4=b4)
