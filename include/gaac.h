@@ -180,7 +180,10 @@ GAAC_API int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_block
  * with hk = hq / (n_q_heads / n_kv_heads), in fp32 (0 for an empty sequence).
  * q: BF16 bits [batch][n_q_heads][128]; out: fp32 [batch][n_q_heads][128].
  * n_q_heads / n_kv_heads must be an integer <= GAAC_MAX_GQA.
- * workspace: at least gaac_attention_workspace(...) bytes, 16-byte aligned.
+ * workspace: at least gaac_attention_workspace(...) bytes, 16-byte aligned.  It holds
+ * the split partials and, at its end, one counter per (sequence, kv-head) that
+ * must be zero before the first call; every call leaves them at zero again.
+ * After a call that reported an error, zero the workspace before reusing it.
  * pools: only slot_pool, n_slots, raw_pool and n_raw are read; both pools must be
  * 16-byte aligned (tiles are fetched with bulk copies).  A table entry that is
  * neither a valid slot nor a valid raw tile reports GAAC_EFORMAT and its block
@@ -211,8 +214,8 @@ GAAC_API int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, 
  *  - Every call shares the one array.  Calls whose kernels overlap on the GPU
  *    (other streams, other threads) race on it and give wrong results; issue
  *    them in one stream or order them.  The array keeps the last call's
- *    partials; nothing in it needs to start at zero, every call rewrites what it
- *    reads.
+ *    partials; each call first clears the merge counters it uses (a small
+ *    memset on the same stream) and rewrites everything else it reads.
  */
 #define GAAC_STATIC_SCRATCH_BYTES (4u << 20)
 GAAC_API int gaac_decode_attention_noalloc(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads,

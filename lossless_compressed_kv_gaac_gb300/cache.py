@@ -64,7 +64,7 @@ class LayerCache:
     def workspace(self, n_splits: int = 0) -> torch.Tensor:
         need = attention_workspace(self.batch, self.n_kv_heads, self.max_blocks, n_splits)
         if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
+            self._ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=self.device)
         return self._ws
 
     def attention(self, q: torch.Tensor, scale: float, out: torch.Tensor | None = None, n_splits: int = 0,

@@ -25,8 +25,9 @@
 //    bf16 hi + lo pair so its rounding stays near 2^-17.
 //  * q is pre-scaled by 2^-4 (exact for normal values) to keep q.k inside the
 //    fp32 range for extreme keys; the factor is folded into the softmax scale.
-//  * Partials (m, l, acc) per split go to the workspace; a combine kernel merges
-//    them with a log-sum-exp.
+//  * Partials (m, l, acc) per split go to the workspace; the last CTA of each
+//    (sequence, kv-head) to finish, found with a device counter, merges them with
+//    a log-sum-exp (the final split reduction) and resets the counter.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -71,6 +72,9 @@ struct AttSmem {
   uint2 lut[256];                                  // escape byte -> spread bits of a 4-bit group
   TileMeta metaK[kStages], metaV[kStages];
   uint64_t fullK[kStages], emptyK[kStages], fullV[kStages], emptyV[kStages];
+  float wmerge[32][kRPad];  // merge: split weights of one chunk of 32 splits
+  float mmax[kRPad], den[kRPad];
+  int last;
 };
 
 struct AttnArgs {
@@ -86,6 +90,8 @@ struct AttnArgs {
   float scale_log2;  // scale * 16 * log2(e)
   int Hq, Hkv, r, max_blocks, n_splits;
   float* part;
+  unsigned int* counters;  // [batch][Hkv] splits finished; zero between launches
+  float* out;
   int32_t* status;
 };
 
@@ -278,10 +284,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
 
   if (warp == kProducerWarp) {  // ------------------------------------------------ producer
     if (lane < 2) stream_tiles(a, sm, lane, b, h, blk0, n_my);
-    return;
-  }
-
-  if (warp < kKWarps) {  // ------------------------------------------------------- K warps
+  } else if (warp < kKWarps) {  // ------------------------------------------------ K warps
     const int kw = warp;
     uint32_t qf[16];
     if (g < r) {
@@ -432,10 +435,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
       part[4 * tq] = m0;      // head 2tq
       part[4 * tq + 2] = m1;  // head 2tq + 1
     }
-    return;
-  }
-
-  // ------------------------------------------------------------------------------------ V warps
+  } else {  // ---------------------------------------------------------------------- V warps
   const int vw = warp - kKWarps;
   uint32_t v3[4], v4[4];  // [mi*2 + hb]: channel 32vw + 16mi + g + 8hb, byte replicated
 #pragma unroll
@@ -566,28 +566,65 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     pa[(2 * tq) * kD + cB] = accH[mi][2] + accL[mi][2];
     pa[(2 * tq + 1) * kD + cB] = accH[mi][3] + accL[mi][3];
   }
-}
-
-// grid (Hq, batch), 128 threads: log-sum-exp merge of the split partials.
-__global__ void __launch_bounds__(kD) attn_combine_kernel(const float* __restrict__ part, int Hq, int Hkv, int r,
-                                                          int n_splits, float* __restrict__ out) {
-  const int hq = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-  const int h = hq / r, n = hq % r;
-  const float* base = part + (static_cast<size_t>(b) * Hkv + h) * n_splits * kPartFloats;
-  float m = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) m = fmaxf(m, base[static_cast<size_t>(s) * kPartFloats + 2 * n]);
-  float num = 0.f, den = 0.f;
-  if (m != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const float* ps = base + static_cast<size_t>(s) * kPartFloats;
-      const float ms = ps[2 * n];
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - m);
-      den += ps[2 * n + 1] * w;
-      num += ps[2 * kRPad + n * kD + c] * w;
-    }
   }
-  out[(static_cast<size_t>(b) * Hq + hq) * kD + c] = den > 0.f ? num / den : 0.f;
+
+  // ---------------------------------------------------------------- split merge (final reduction)
+  // The last CTA of a (sequence, kv-head) to finish merges the partials of all
+  // its splits with a log-sum-exp; the counter goes back to zero for the next
+  // launch.  No CTA ever waits for another.
+  __threadfence();
+  __syncthreads();
+  unsigned int* counter = a.counters + static_cast<size_t>(b) * a.Hkv + h;
+  if (tid == 0) sm.last = atomicAdd(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  const int ns = a.n_splits;
+  const float* base = a.part + static_cast<size_t>(b) * a.Hkv * ns * kPartFloats + static_cast<size_t>(h) * ns * kPartFloats;
+  if (warp < r) {  // warp n: the largest running max of head n over the splits
+    float mx = -INFINITY;
+    for (int sp = lane; sp < ns; sp += 32) mx = fmaxf(mx, base[static_cast<size_t>(sp) * kPartFloats + 2 * warp]);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, d));
+    if (lane == 0) sm.mmax[warp] = mx;
+  }
+  __syncthreads();
+  constexpr int kOutPerThread = (kRPad * kD + kAttThreads - 1) / kAttThreads;
+  float num[kOutPerThread], dsum[kOutPerThread];
+#pragma unroll
+  for (int k = 0; k < kOutPerThread; ++k) num[k] = dsum[k] = 0.f;
+  for (int cs = 0; cs < ns; cs += 32) {
+    for (int idx = tid; idx < 32 * kRPad; idx += kAttThreads) {
+      const int sp = cs + idx / kRPad, n = idx % kRPad;
+      float w = 0.f;
+      if (sp < ns && n < r) {
+        const float ms = base[static_cast<size_t>(sp) * kPartFloats + 2 * n];
+        if (ms != -INFINITY) w = fast_exp2(ms - sm.mmax[n]);
+      }
+      sm.wmerge[idx / kRPad][n] = w;
+    }
+    __syncthreads();
+    const int cn = min(32, ns - cs);
+#pragma unroll
+    for (int k = 0; k < kOutPerThread; ++k) {
+      const int o = tid + k * kAttThreads, n = o / kD, c = o % kD;
+      if (n < r) {
+        for (int j = 0; j < cn; ++j) {
+          const float w = sm.wmerge[j][n];
+          const float* ps = base + static_cast<size_t>(cs + j) * kPartFloats;
+          num[k] += w * ps[2 * kRPad + n * kD + c];
+          dsum[k] += w * ps[2 * n + 1];
+        }
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < kOutPerThread; ++k) {
+    const int o = tid + k * kAttThreads, n = o / kD, c = o % kD;
+    if (n < r) a.out[(static_cast<size_t>(b) * a.Hq + h * r + n) * kD + c] = dsum[k] > 0.f ? num[k] / dsum[k] : 0.f;
+  }
+  if (tid == 0) *counter = 0u;
 }
 
 static int device_sms() {
@@ -628,10 +665,15 @@ extern "C" int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_blo
   return static_cast<int>(s < 1 ? 1 : s);
 }
 
+static size_t partials_bytes(int batch, int n_kv_heads, int n_splits) {
+  return static_cast<size_t>(batch) * n_kv_heads * n_splits * kPartFloats * sizeof(float);
+}
+
 extern "C" size_t gaac_attention_workspace(int batch, int n_kv_heads, int max_blocks, int n_splits) {
   if (n_splits <= 0) n_splits = gaac_attention_auto_splits(batch, n_kv_heads, max_blocks);
   if (batch <= 0 || n_kv_heads <= 0) return 0;
-  return static_cast<size_t>(batch) * n_kv_heads * n_splits * kPartFloats * sizeof(float);
+  const size_t counters = (static_cast<size_t>(batch) * n_kv_heads * sizeof(unsigned int) + 15) & ~static_cast<size_t>(15);
+  return partials_bytes(batch, n_kv_heads, n_splits) + counters;
 }
 
 extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
@@ -673,11 +715,11 @@ extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads
   a.max_blocks = max_blocks;
   a.n_splits = n_splits;
   a.part = static_cast<float*>(workspace);
+  a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + partials_bytes(batch, n_kv_heads, n_splits));
+  a.out = out;
   a.status = d_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   attn_split_kernel<<<dim3(n_splits, n_kv_heads, batch), kAttThreads, sizeof(AttSmem), st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return GAAC_ECUDA;
-  attn_combine_kernel<<<dim3(n_q_heads, batch), kD, 0, st>>>(a.part, n_q_heads, n_kv_heads, a.r, n_splits, out);
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
 
@@ -716,6 +758,12 @@ extern "C" int gaac_decode_attention_noalloc(const uint16_t* q, int batch, int n
   if (gaac_attention_workspace(batch, n_kv_heads, max_blocks, ns) > kStaticScratchBytes) return GAAC_EINVAL;
   void* scratch = static_scratch_address();
   if (scratch == nullptr) return GAAC_ECUDA;
+  // The merge counters must start at zero; clear them on every call so that a
+  // call never depends on how an earlier one ended.
+  const size_t cbytes = static_cast<size_t>(batch) * n_kv_heads * sizeof(unsigned int);
+  if (cudaMemsetAsync(static_cast<char*>(scratch) + partials_bytes(batch, n_kv_heads, ns), 0, cbytes,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GAAC_ECUDA;
   return gaac_decode_attention(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, base3, base4,
                                scale, ns, out, scratch, kStaticScratchBytes, d_status, stream);
 }

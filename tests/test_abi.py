@@ -36,9 +36,10 @@ def test_host_helpers(lib):
     assert lib.gaac_strerror(1) == b"invalid argument"
     assert lib.gaac_format_version() == 1
     lib.gaac_attention_workspace.restype = ctypes.c_size_t
-    # (16 m,l floats + 8 heads x 128 acc floats) x 4 bytes per (sequence, kv-head, split)
-    assert lib.gaac_attention_workspace(1, 8, 1024, 38) == 1 * 8 * 38 * (16 + 8 * 128) * 4
-    assert lib.gaac_attention_workspace(3, 4, 10, 5) == 3 * 4 * 5 * 1040 * 4
+    # (16 m,l floats + 8 heads x 128 acc floats) x 4 bytes per (sequence, kv-head, split),
+    # then one 4-byte merge counter per (sequence, kv-head), rounded up to 16 bytes
+    assert lib.gaac_attention_workspace(1, 8, 1024, 38) == 1 * 8 * 38 * (16 + 8 * 128) * 4 + 32
+    assert lib.gaac_attention_workspace(3, 4, 10, 5) == 3 * 4 * 5 * 1040 * 4 + 48
 
 
 def test_null_arguments_rejected_on_host(lib):
