@@ -72,8 +72,6 @@ struct AttSmem {
   uint2 lut[256];                                  // escape byte -> spread bits of a 4-bit group
   TileMeta metaK[kStages], metaV[kStages];
   uint64_t fullK[kStages], emptyK[kStages], fullV[kStages], emptyV[kStages];
-  float wmerge[32][kRPad];  // merge: split weights of one chunk of 32 splits
-  float mmax[kRPad], den[kRPad];
   int last;
 };
 
@@ -207,6 +205,12 @@ __device__ __forceinline__ void load8(const uint8_t* p, uint32_t out[8]) {
   out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
 }
 
+__device__ __forceinline__ unsigned int atomic_add_acq_rel(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void named_bar_arrive(int id, int threads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -247,6 +251,100 @@ __device__ __forceinline__ void stream_tiles(const AttnArgs& a, AttSmem& sm, int
     mbar_arrive_expect_tx(&full[st], bytes);
     if (bytes) bulk_g2s(ring[st], src, bytes, &full[st]);
     cur = nxt;
+  }
+}
+
+// Log-sum-exp merge of the n_splits partials (m, l, acc) of one (sequence,
+// kv-head) into out[b, h*r + n, :] = sum_s w_s acc_s / sum_s w_s l_s with
+// w_s = 2^(m_s - max_s m_s) per head n (the final split reduction).  Runs on
+// the CTA that finished last, so it is a tail on the critical path: each
+// thread owns one float4 column of the output and a subset of the splits,
+// issues that subset's loads ten at a time and folds them in with its own
+// running maximum; the subsets are then combined the same way in shared
+// memory.  The ring buffers are free by then and hold that exchange.
+// base: the first partial of the pair; out: its first output row.
+__device__ __noinline__ void merge_splits(const float* base, int ns, int r, float* out, AttSmem& sm, int tid) {
+  constexpr int kBatch = 10;
+  const int o4n = r * (kD / 4);  // float4 columns of the r x 128 output
+  const int groups = kAttThreads / o4n;
+  const int o4 = tid % o4n, grp = tid / o4n;
+  const int n = o4 / (kD / 4), c4 = o4 % (kD / 4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f, mt = -INFINITY;
+  if (grp < groups) {
+    const float* pcol = base + 2 * kRPad + n * kD + 4 * c4;
+    for (int sp0 = grp; sp0 < ns; sp0 += kBatch * groups) {
+      float2 ml[kBatch];
+      float4 v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int sp = sp0 + u * groups;
+        if (sp < ns) {
+          ml[u] = __ldcg(reinterpret_cast<const float2*>(base + static_cast<size_t>(sp) * kPartFloats + 2 * n));
+          v[u] = __ldcg(reinterpret_cast<const float4*>(pcol + static_cast<size_t>(sp) * kPartFloats));
+        } else {
+          ml[u] = make_float2(-INFINITY, 0.f);
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float mb = mt;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, ml[u].x);
+      if (mb != -INFINITY) {
+        const float al = mt == -INFINITY ? 0.f : fast_exp2(mt - mb);
+        acc.x *= al;
+        acc.y *= al;
+        acc.z *= al;
+        acc.w *= al;
+        den *= al;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const float w = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - mb);
+          acc.x += w * v[u].x;
+          acc.y += w * v[u].y;
+          acc.z += w * v[u].z;
+          acc.w += w * v[u].w;
+          den += w * ml[u].y;
+        }
+        mt = mb;
+      }
+    }
+  }
+  float4* xa = reinterpret_cast<float4*>(sm.ringK);  // [groups][o4n] accumulators
+  float2* xm = reinterpret_cast<float2*>(sm.ringV);  // [groups][o4n] (running max, denominator)
+  if (grp < groups && groups > 1) {
+    xa[grp * o4n + o4] = acc;
+    xm[grp * o4n + o4] = make_float2(mt, den);
+  }
+  __syncthreads();
+  if (tid < o4n) {
+    float mx = mt;
+    for (int gi = 1; gi < groups; ++gi) mx = fmaxf(mx, xm[gi * o4n + o4].x);
+    if (mx != -INFINITY) {
+      const float al = mt == -INFINITY ? 0.f : fast_exp2(mt - mx);
+      acc.x *= al;
+      acc.y *= al;
+      acc.z *= al;
+      acc.w *= al;
+      den *= al;
+      for (int gi = 1; gi < groups; ++gi) {
+        const float2 md = xm[gi * o4n + o4];
+        if (md.x == -INFINITY) continue;
+        const float w = fast_exp2(md.x - mx);
+        const float4 x = xa[gi * o4n + o4];
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+        den += w * md.y;
+      }
+    }
+    float* o = out + n * kD + 4 * c4;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    o[0] = acc.x * inv;
+    o[1] = acc.y * inv;
+    o[2] = acc.z * inv;
+    o[3] = acc.w * inv;
   }
 }
 
@@ -571,59 +669,20 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   // ---------------------------------------------------------------- split merge (final reduction)
   // The last CTA of a (sequence, kv-head) to finish merges the partials of all
   // its splits with a log-sum-exp; the counter goes back to zero for the next
-  // launch.  No CTA ever waits for another.
-  __threadfence();
+  // launch.  No CTA ever waits for another.  The merge is a short tail on the
+  // critical path, so it keeps many independent L2 loads in flight: one round
+  // for the per-head maxima, then every thread streams its share of the splits'
+  // accumulators (eight at a time) and the CTA adds the shares up in shared memory.
+  // Release/acquire through the counter: the barrier orders every thread's
+  // partial stores before thread 0's acq_rel add, and the add orders the other
+  // splits' stores before this CTA's loads (the barrier passes that on).
   __syncthreads();
   unsigned int* counter = a.counters + static_cast<size_t>(b) * a.Hkv + h;
-  if (tid == 0) sm.last = atomicAdd(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
+  if (tid == 0) sm.last = atomic_add_acq_rel(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
   __syncthreads();
   if (!sm.last) return;
-  __threadfence();
-  const int ns = a.n_splits;
-  const float* base = a.part + static_cast<size_t>(b) * a.Hkv * ns * kPartFloats + static_cast<size_t>(h) * ns * kPartFloats;
-  if (warp < r) {  // warp n: the largest running max of head n over the splits
-    float mx = -INFINITY;
-    for (int sp = lane; sp < ns; sp += 32) mx = fmaxf(mx, base[static_cast<size_t>(sp) * kPartFloats + 2 * warp]);
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, d));
-    if (lane == 0) sm.mmax[warp] = mx;
-  }
-  __syncthreads();
-  constexpr int kOutPerThread = (kRPad * kD + kAttThreads - 1) / kAttThreads;
-  float num[kOutPerThread], dsum[kOutPerThread];
-#pragma unroll
-  for (int k = 0; k < kOutPerThread; ++k) num[k] = dsum[k] = 0.f;
-  for (int cs = 0; cs < ns; cs += 32) {
-    for (int idx = tid; idx < 32 * kRPad; idx += kAttThreads) {
-      const int sp = cs + idx / kRPad, n = idx % kRPad;
-      float w = 0.f;
-      if (sp < ns && n < r) {
-        const float ms = base[static_cast<size_t>(sp) * kPartFloats + 2 * n];
-        if (ms != -INFINITY) w = fast_exp2(ms - sm.mmax[n]);
-      }
-      sm.wmerge[idx / kRPad][n] = w;
-    }
-    __syncthreads();
-    const int cn = min(32, ns - cs);
-#pragma unroll
-    for (int k = 0; k < kOutPerThread; ++k) {
-      const int o = tid + k * kAttThreads, n = o / kD, c = o % kD;
-      if (n < r) {
-        for (int j = 0; j < cn; ++j) {
-          const float w = sm.wmerge[j][n];
-          const float* ps = base + static_cast<size_t>(cs + j) * kPartFloats;
-          num[k] += w * ps[2 * kRPad + n * kD + c];
-          dsum[k] += w * ps[2 * n + 1];
-        }
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int k = 0; k < kOutPerThread; ++k) {
-    const int o = tid + k * kAttThreads, n = o / kD, c = o % kD;
-    if (n < r) a.out[(static_cast<size_t>(b) * a.Hq + h * r + n) * kD + c] = dsum[k] > 0.f ? num[k] / dsum[k] : 0.f;
-  }
+  merge_splits(a.part + (static_cast<size_t>(b) * a.Hkv + h) * a.n_splits * kPartFloats, a.n_splits, r,
+               a.out + (static_cast<size_t>(b) * a.Hq + h * r) * kD, sm, tid);
   if (tid == 0) *counter = 0u;
 }
 
