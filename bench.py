@@ -157,14 +157,14 @@ def build_layers(n_layers: int, device, raw: bool):
 
 def algorithmic_bytes(cache) -> int:
     """Bytes the method must read for one attention launch over this layer: per slot tile the
-    planes (11,520 B) plus its escape bytes, per raw tile 16,384 B, plus 8 B per table entry and
-    the query (read) and output (written)."""
+    planes and the escape directory (11,536 B) plus its escape bytes, per raw tile 16,384 B,
+    plus 8 B per table entry."""
     import torch
 
     _, esc, mode, _ = cache.fields()
     slot = mode == 0
     raw = mode == 1
-    n = int(slot.sum().item()) * 11520 + int(esc[slot].sum().item()) + int(raw.sum().item()) * 16384
+    n = int(slot.sum().item()) * 11536 + int(esc[slot].sum().item()) + int(raw.sum().item()) * 16384
     n += int((slot | raw).sum().item()) * 8
     return n
 

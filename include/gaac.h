@@ -19,20 +19,24 @@
  *    NULL): the first nonzero code wins (atomic compare-and-swap from 0).  Kernels
  *    never trap and never wait without a bound.  Read it after synchronising.
  *  - BF16 values are passed as their uint16_t bit patterns.
- *  - head_dim is 128 and the block is 64 tokens (format v1 below).
+ *  - head_dim is 128 and the block is 64 tokens (format v2 below).
  *
- * Tile format v1 (identical in the CUDA library and in the test oracle):
+ * Tile format v2 (identical in the CUDA library and in the test oracle):
  *  tile        64 tokens x 128 channels of one (layer, sequence, block, kv-head, K|V)
  *  order       K tiles token-major  (element (t,c) at s = t*128 + c),
  *              V tiles channel-major (element (t,c) at s = c*64 + t)
  *  group       8 consecutive elements in that order (G = s/8)
  *  slot image  GAAC_SLOT_BYTES bytes:
- *               [0,8192)      sign|mantissa byte of element s at byte s
+ *               [0,8192)      byte s: mantissa of element s in bits 0-6; bit 7 is
+ *                             the sign of element 4*(s/4) + (s+3)%4 (the signs of
+ *                             each aligned group of four rotated by one byte)
  *               [8192,11264)  3-bit codes: word k (0..2) of 32-element unit u at
  *                             8192 + 4*(k*256 + u)
  *               [11264,11520) 2-bit mode of group G at byte 11264 + G/4, bits 2*(G%4)
- *               [11520,12032) escape bytes (mode 1: 1 byte, mode 2: 5 bytes per
- *                             group, in group order), zero filled
+ *               [11520,11536) escape directory: 8 little-endian u16; entry w is
+ *                             the number of escape bytes of groups [0, 128*(w+1))
+ *               [11536,12032) escape bytes (mode 1: 1 byte, mode 2: 5 bytes per
+ *                             group, in group order), zero filled; capacity 496
  *  raw tile    8192 BF16 words in the same storage order
  */
 #ifndef GAAC_H
@@ -55,7 +59,7 @@ extern "C" {
 #define GAAC_BLOCK 64
 #define GAAC_TILE_ELEMS 8192
 #define GAAC_SLOT_BYTES 12032
-#define GAAC_ESC_CAPACITY 512
+#define GAAC_ESC_CAPACITY 496
 #define GAAC_RAW_TILE_BYTES 16384
 #define GAAC_MAX_GQA 8 /* query heads per kv-head supported by decode attention */
 
@@ -77,7 +81,7 @@ enum { GAAC_MODE_SLOT = 0, GAAC_MODE_RAW = 1, GAAC_MODE_NONE = 255 };
  * table[batch][max_blocks][n_kv_heads][2]  (last index 0 = K, 1 = V). */
 typedef struct gaac_entry {
   uint32_t index;   /* slot index (mode SLOT) or raw-tile index (mode RAW) */
-  uint16_t esc_len; /* escape bytes used in the slot (mode SLOT) */
+  uint16_t esc_len; /* escape bytes used in the slot, directory not counted (mode SLOT) */
   uint8_t mode;     /* GAAC_MODE_* */
   uint8_t n_tok;    /* tokens held: 64 for a sealed block, fewer for the open tail */
 } gaac_entry;

@@ -7,7 +7,7 @@ library's CUDA kernels; there is no CPU fallback.  If ``libgaac.so`` has not bee
 built, the first call raises.
 
 Method: "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference on
-Personal Devices" (sections 3.1-3.3).  Tile format v1 is described in gaac.h.
+Personal Devices" (sections 3.1-3.3).  Tile format v2 is described in gaac.h.
 """
 from __future__ import annotations
 
@@ -21,7 +21,7 @@ HEAD_DIM = 128
 BLOCK = 64
 TILE_ELEMS = 8192
 SLOT_BYTES = 12032
-ESC_CAPACITY = 512
+ESC_CAPACITY = 496
 RAW_TILE_BYTES = 16384
 MAX_GQA = 8
 

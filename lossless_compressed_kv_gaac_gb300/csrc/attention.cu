@@ -2,32 +2,40 @@
 //
 // "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference on
 // Personal Devices", section 3.2: attention reads the compressed tiles and
-// rebuilds the values it needs on the fly (no decompressed copy of the cache);
-// compressed blocks and the raw tail go through one softmax.  Section 3.3: the
-// block table says per block whether it is a slot or a raw tile.
+// rebuilds the values it needs on the fly (no decompressed copy of the cache
+// in global memory); compressed blocks and the raw tail go through one
+// softmax.  Section 3.3: the block table says per block whether it is a slot
+// or a raw tile.
 //
-// GB300 design
-//  * grid (split, kv-head, sequence); 160 threads: warp 4 is a producer that
-//    streams each 64-token block's K and V tile bytes (only the bytes the slot
-//    uses) into a 3-stage shared-memory ring with 1-D bulk copies tracked by
-//    mbarriers; warps 0-3 consume.
-//  * The exponent decoder works on four elements per 32-bit operation and
-//    writes BF16 pairs straight into mma.sync m16n8k16 fragments: QK^T with
-//    16 tokens x 8 query heads per warp (K token-major, channels permuted so
-//    each thread's 32 channels are contiguous), PV^T with 32 channels x 8 heads
-//    per warp (V channel-major, each thread's 16 tokens contiguous).  No
-//    decompressed tile is ever written back to shared memory.
-//  * The producer warp also checks each slot image's tag plane and gathers the
-//    escape bytes of 4-bit-mode groups per 32-element unit (into the unused
-//    tail of the stage region), so consumers decode without per-lane branches.
-//  * Online softmax in the log2 domain, shared by the CTA through a small score
-//    buffer and one named barrier per block; P enters the PV product as a
-//    bf16 hi + lo pair so its rounding stays near 2^-17.
+// GB300 design: one CTA of 352 threads per SM, grid (split, kv-head, sequence).
+//  * Warp 10 (producer): one lane streams each 64-token block's K and V tile
+//    images (only the bytes a slot uses) into a 3-stage shared-memory ring
+//    with 1-D bulk copies tracked by mbarriers.
+//  * Warps 0-7 (decoders): warp w rebuilds quarter w%4 (code units
+//    [64q, 64q+64)) of the K (w < 4) or V tile into BF16 in a swizzled
+//    shared-memory tile.  A lane owns two 32-element units.  The escape
+//    directory gives the quarter's first escape byte, a packed warp scan each
+//    unit's, and one byte permute gathers a unit's 4-bit escape bytes.
+//    Exponents are rebuilt four at a time in 32-bit words (the bytes cannot
+//    carry) and joined with the sign|mantissa word by two bit selects and a
+//    byte rotation per four values.  Raw-mode groups are rare and patched
+//    afterwards by the lane that owns them.
+//  * Warps 8-9 (tensor-core warps) take alternate blocks: QK^T and PV^T with
+//    ldmatrix + mma.sync m16n8k16 (bf16 in, fp32 accumulate), an online
+//    softmax in the log2 domain that rescales only when a running maximum
+//    rises, and P stored transposed (stmatrix) as a bf16 hi + lo pair so its
+//    rounding stays near 2^-17.  Each warp keeps (m, l, acc) for its own
+//    blocks; the two are merged when the split ends.
+//  * The decoded tiles hold each group of four values in the order {0,2,1,3}
+//    (the join's output order).  The QK^T contraction runs over channels in
+//    that order (q's fragment follows it); the PV^T contraction runs over
+//    tokens in that order (QK^T rows are permuted the same way, so P^T comes
+//    out in it).
 //  * q is pre-scaled by 2^-4 (exact for normal values) to keep q.k inside the
 //    fp32 range for extreme keys; the factor is folded into the softmax scale.
 //  * Partials (m, l, acc) per split go to the workspace; the last CTA of each
-//    (sequence, kv-head) to finish, found with a device counter, merges them with
-//    a log-sum-exp (the final split reduction) and resets the counter.
+//    (sequence, kv-head) to finish, found with a device counter, merges them
+//    with a log-sum-exp (the final split reduction) and resets the counter.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -36,42 +44,41 @@
 
 namespace gaac {
 
-// Warp roles: warps 0-3 take K (decode, QK^T, softmax), warps 4-7 take V
-// (decode, PV), warp 8 streams tiles.  K warps run up to two blocks ahead of V
-// warps; P crosses over through a double-buffered shared-memory buffer.
-constexpr int kKWarps = 4, kVWarps = 4;
-constexpr int kProducerWarp = kKWarps + kVWarps;
+constexpr int kDWarps = 16;                      // decoders: 0-7 K eighths, 8-15 V eighths
+constexpr int kMWarps = 2;                       // tensor-core warps (alternate blocks)
+constexpr int kMWarp0 = kDWarps;
+constexpr int kProducerWarp = kDWarps + kMWarps;
 constexpr int kAttThreads = (kProducerWarp + 1) * 32;
-#ifndef GAAC_ATT_STAGES
-#define GAAC_ATT_STAGES 3
-#endif
-#ifndef GAAC_ATT_CTAS_PER_SM
-#define GAAC_ATT_CTAS_PER_SM 2
-#endif
-constexpr int kStages = GAAC_ATT_STAGES;
-constexpr int kCtasPerSm = GAAC_ATT_CTAS_PER_SM;
-constexpr int kRPad = 8;     // query heads per kv-head in the MMA N dimension
-constexpr int kPStride = 72;  // bf16 per head row of the probability buffer (64 + pad)
+constexpr int kStages = 3;                       // staging ring of K+V tile images
+constexpr int kDecBufs = 3;                      // decoded BF16 K+V tiles
+constexpr int kCtasPerSm = 1;
+constexpr int kRPad = 8;                         // query heads per kv-head in the MMA N dimension
+constexpr int kPtStride = 72;                    // bf16 per head row of P^T (64 tokens + pad): 144 B
+constexpr int kQStride = 136;                    // bf16 per head row of q (128 channels + pad): 272 B
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
-// named barriers (0 is __syncthreads)
-constexpr int kBarK = 1;           // the 4 K warps
-constexpr int kBarPFull = 2;       // + parity: P of a block written (K arrive, V sync)
-constexpr int kBarPEmpty = 4;      // + parity: P of a block read (V arrive, K sync)
+constexpr int kBarM = 1;                         // named barrier of the two tensor-core warps
+constexpr uint32_t kJoinMask = 0x807F807Fu;      // sign and mantissa bits of a bf16x2 word
+constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-struct TileMeta {
-  int mode, esc;
+struct StageMeta {
+  int mode[2], esc[2];  // [K, V]
 };
 
 struct AttSmem {
-  alignas(128) uint8_t ringK[kStages][kRawBytes];
-  alignas(128) uint8_t ringV[kStages][kRawBytes];
-  alignas(16) uint16_t P[2][2][kRPad][kPStride];  // [block parity][hi, lo][head][token] bf16 probabilities
-  alignas(16) float wmax[2][kRPad][kKWarps];       // [parity][head][K warp] max over the warp's 16 scores
-  alignas(16) float wsum[2][kRPad][kKWarps];       // [parity][head][K warp] sum of the warp's 16 probabilities
-  alignas(16) float alpha[2][kRPad];               // [parity][head] rescale factor of the running sums
-  uint2 lut[256];                                  // escape byte -> spread bits of a 4-bit group
-  TileMeta metaK[kStages], metaV[kStages];
-  uint64_t fullK[kStages], emptyK[kStages], fullV[kStages], emptyV[kStages];
+  alignas(128) uint8_t stage[kStages][2][kRawBytes];  // K, V tile images
+  alignas(128) uint8_t decK[kDecBufs][kTile * 2];      // BF16 K, rows = tokens (256 B), swizzled
+  alignas(128) uint8_t decV[kDecBufs][kTile * 2];      // BF16 V, rows = channels (128 B), swizzled
+  alignas(16) uint16_t pt[kMWarps][2][kRPad][kPtStride];  // P^T hi, lo of each tensor-core warp
+  alignas(16) uint16_t qs[kRPad][kQStride];               // q * 2^-4, channels in decoded order
+  alignas(16) float xacc[kRPad][kD];                      // tensor-core warp 1's acc at the end
+  float xm[kRPad], xl[kRPad];
+  uint2 lut[256];       // escape byte -> bit 3 spread into the byte lanes of two exponent words
+  uint32_t sel[256];    // tag byte -> byte permute that gathers a unit's 4-bit escape bytes
+  StageMeta smeta[kStages];
+  int dec_nv[kDecBufs];                   // tokens of the block in decoded buffer d
+  alignas(8) uint8_t dec_bad[kDecBufs][8];  // K eighth failed its checks
+  uint64_t stFull[kStages], stEmpty[kStages];
+  uint64_t dkFull[kDecBufs], dvFull[kDecBufs], dkEmpty[kDecBufs], dvEmpty[kDecBufs];
   int last;
 };
 
@@ -93,6 +100,8 @@ struct AttnArgs {
   int32_t* status;
 };
 
+// ------------------------------------------------------------------ helpers
+
 // bf16x2 times 2^-4; exact whenever the result is a normal number.
 __device__ __forceinline__ uint32_t bf16x2_div16(uint32_t w) {
   const float lo = __uint_as_float(w << 16) * 0.0625f;
@@ -100,9 +109,9 @@ __device__ __forceinline__ uint32_t bf16x2_div16(uint32_t w) {
   return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
 }
 
-__device__ __forceinline__ uint16_t to_bf16(float x) {
-  uint16_t r;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(x));
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
@@ -112,97 +121,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ int warp_sum(int x) {
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, d);
-  return x;
-}
-
 __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, x, d);
+    const int v = __shfl_up_sync(kFull, x, d);
     if (lane >= d) x += v;
   }
   return x;
-}
-
-// Per consumer warp and slot image.  Warp w decodes exactly the 32-element
-// units [64w, 64w+64) of the tile (K: its 16 tokens, V: its 32 channels), whose
-// tags are tag words [16w, 16w+16).  Returns the escape bytes before that range
-// and checks the whole tag plane (no reserved tag; escape bytes add up to
-// esc_len), a decision every warp takes identically.
-__device__ __forceinline__ bool range_escape_base(const uint8_t* tile, int esc_len, int warp, int lane,
-                                                  int& before) {
-  const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile + kOffTag);
-  const uint32_t wa = tw[lane], wb = tw[lane + 32];
-  const int ca = esc_count(wa), cb = esc_count(wb);
-  const bool reserved = ((wa & (wa >> 1)) | (wb & (wb >> 1))) & 0x55555555u;
-  const int bnd = 16 * warp;
-  const int red = warp_sum(((lane < bnd ? ca : 0) + (lane + 32 < bnd ? cb : 0)) | ((ca + cb) << 16));
-  before = red & 0xFFFF;
-  return !__any_sync(0xFFFFFFFFu, reserved) && (red >> 16) == esc_len;
-}
-
-// Escape bytes of the 4-bit-mode groups among the groups of tag byte/nibble
-// `tags` (ngroups groups, escape offset of the first at `off`), gathered as
-// byte j for group j (0 for the other groups).
-template <int NG>
-__device__ __forceinline__ uint32_t gather_groups(const uint8_t* esc, uint32_t tags, int off) {
-  uint32_t x = 0;
-#pragma unroll
-  for (int j = 0; j < NG; ++j) {
-    const uint32_t m = (tags >> (2 * j)) & 3u;
-    if (m == 1u) x |= static_cast<uint32_t>(esc[off]) << (8 * j);
-    off += esc_of_tag(m);
-  }
-  return x;
-}
-
-// Exponents of one half-unit (16 elements) into 8 bf16x2 words.  xw16: the two
-// groups' gathered 4-bit escape bytes; off: escape offset of its first group
-// (used only for raw-mode groups).
-__device__ __forceinline__ void decode_half(const uint8_t* tile, uint32_t Wh, uint32_t W2, int hh, uint32_t tagnib,
-                                            uint32_t xw16, int off, const uint4 sm, const uint32_t b3[4],
-                                            const uint32_t b4[4], const uint2* lut, uint32_t out[8]) {
-  uint32_t c[4];
-  extract_codes(Wh, W2, hh, c);
-  const uint2 s0 = lut[xw16 & 0xFFu], s1 = lut[(xw16 >> 8) & 0xFFu];
-  const bool g0 = (tagnib & 3u) != 0u, g1 = (tagnib & 12u) != 0u;
-  uint32_t e[4];
-  e[0] = (g0 ? b4[0] : b3[0]) + c[0] + s0.x;
-  e[1] = (g0 ? b4[1] : b3[1]) + c[1] + s0.y;
-  e[2] = (g1 ? b4[2] : b3[2]) + c[2] + s1.x;
-  e[3] = (g1 ? b4[3] : b3[3]) + c[3] + s1.y;
-  if (tagnib & 0xAu) {  // a raw-mode group in this half (rare): five escape bit planes
-    const uint8_t* esc = tile + kOffEsc;
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      const uint32_t m = (tagnib >> (2 * gi)) & 3u;
-      if (m == 2u) {
-        const int o = off + (gi == 0 ? 0 : esc_of_tag(tagnib & 3u));
-        uint32_t hi0 = 0, hi1 = 0;
-#pragma unroll
-        for (int k = 0; k < 5; ++k) {
-          const uint32_t x = esc[o + k];
-          hi0 |= spread4(x & 15u) << (3 + k);
-          hi1 |= spread4(x >> 4) << (3 + k);
-        }
-        e[2 * gi] = c[2 * gi] | hi0;
-        e[2 * gi + 1] = c[2 * gi + 1] | hi1;
-      }
-    }
-  }
-  join_bf16x4(sm.x, e[0], out[0], out[1]);
-  join_bf16x4(sm.y, e[1], out[2], out[3]);
-  join_bf16x4(sm.z, e[2], out[4], out[5]);
-  join_bf16x4(sm.w, e[3], out[6], out[7]);
-}
-
-__device__ __forceinline__ void load8(const uint8_t* p, uint32_t out[8]) {
-  const uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
-  out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
-  out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
 }
 
 __device__ __forceinline__ unsigned int atomic_add_acq_rel(unsigned int* p, unsigned int v) {
@@ -211,46 +136,512 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel(unsigned int* p, unsi
   return old;
 }
 
-__device__ __forceinline__ void named_bar_arrive(int id, int threads) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
 }
 
-// Producer lane for one tile kind (kv 0 = K, 1 = V): streams the tile of every
-// block of the split into its ring, prefetching the next table entry while it
-// waits for a free slot.
-__device__ __forceinline__ void stream_tiles(const AttnArgs& a, AttSmem& sm, int kv, int b, int h, int blk0, int n_my) {
-  const gaac_entry* tab = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk0) * a.Hkv + h) * 2 + kv;
-  const size_t stride = static_cast<size_t>(a.Hkv) * 2;
-  uint8_t(*ring)[kRawBytes] = kv ? sm.ringV : sm.ringK;
-  TileMeta* meta = kv ? sm.metaV : sm.metaK;
-  uint64_t* full = kv ? sm.fullV : sm.fullK;
-  uint64_t* empty = kv ? sm.emptyV : sm.emptyK;
-  uint2 cur = make_uint2(0u, 0u);
-  if (n_my > 0) cur = *reinterpret_cast<const uint2*>(tab);
-  for (int j = 0; j < n_my; ++j) {
-    uint2 nxt = cur;
-    if (j + 1 < n_my) nxt = *reinterpret_cast<const uint2*>(tab + (j + 1) * stride);
-    const int st = j % kStages;
-    if (j >= kStages) mbar_wait(&empty[st], ((j / kStages) & 1) ^ 1, a.status);
-    const uint32_t index = cur.x, esc_len = cur.y & 0xFFFFu, emode = (cur.y >> 16) & 0xFFu;
-    uint32_t bytes = 0;
-    const void* src = nullptr;
-    TileMeta tm{GAAC_MODE_NONE, 0};
-    if (emode == GAAC_MODE_SLOT && static_cast<int64_t>(index) < a.n_slots && esc_len <= kEscCap) {
-      tm = TileMeta{GAAC_MODE_SLOT, static_cast<int>(esc_len)};
-      bytes = kOffEsc + ((esc_len + 15u) & ~15u);
-      src = a.slot_pool + static_cast<size_t>(index) * kSlot;
-    } else if (emode == GAAC_MODE_RAW && static_cast<int64_t>(index) < a.n_raw) {
-      tm = TileMeta{GAAC_MODE_RAW, 0};
-      bytes = kRawBytes;
-      src = a.raw_pool + static_cast<size_t>(index) * kTile;
-    } else {
-      report(a.status, GAAC_EFORMAT);
+__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+
+// Position p of a decoded row holds element quad_perm(p): each aligned group
+// of four is stored {0,2,1,3}.  The map is its own inverse.
+__device__ __forceinline__ int quad_perm(int p) { return (p & ~3) | ((p & 1) << 1) | ((p >> 1) & 1); }
+
+// Byte offset of 16-byte chunk c (0..15) of token row t in a decoded K tile.
+// The chunk's low three bits are XORed with the row (and bit 1 flipped in the
+// upper half-row) so that ldmatrix over 8 rows and the decoders' 16-byte
+// stores both touch 8 different bank groups.
+__device__ __forceinline__ uint32_t kswz(int t, int c) {
+  return static_cast<uint32_t>(t * 256 + 16 * ((c & 8) | ((c ^ t ^ ((c >> 3) << 1)) & 7)));
+}
+// Byte offset of 16-byte chunk c (0..7) of channel row ch in a decoded V tile.
+__device__ __forceinline__ uint32_t vswz(int ch, int c) { return static_cast<uint32_t>(ch * 128 + 16 * ((c ^ ch) & 7)); }
+
+// Four BF16 values from one sign|mantissa word of format v2 (byte L: mantissa
+// of element L, sign of element (L+3)%4) and their exponent word (byte L =
+// exponent of element L): p02 = elements {0, 2}, p13 = elements {1, 3}.
+// Rotating the exponents left by 7 puts elements 0 and 2 in their bf16 fields
+// and elements 1 and 3 in the fields of the same word rotated by one byte.
+__device__ __forceinline__ void join_v2(uint32_t w, uint32_t e, uint32_t& p02, uint32_t& p13) {
+  const uint32_t r = __funnelshift_l(e, e, 7);
+  p02 = (w & kJoinMask) | (r & ~kJoinMask);
+  const uint32_t t = (w & ~kJoinMask) | (r & kJoinMask);
+  p13 = __byte_perm(t, t, 0x0321);
+}
+
+// Byte permute selector that gathers the escape bytes of a unit's 4-bit
+// groups from the four escape bytes at the unit's offset: byte j of the result
+// is group j's escape byte if group j is 4-bit and no raw group precedes it in
+// the unit, else 0 (those groups are patched separately).
+__device__ __forceinline__ uint32_t gather_selector(uint32_t tb) {
+  uint32_t s = 0, rank = 0;
+  bool raw = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t t = (tb >> (2 * j)) & 3u;
+    if (t >= 2u) raw = true;
+    const uint32_t nib = (t == 1u && !raw) ? rank : 4u;  // 4: a zero byte of the second operand
+    if (t == 1u) ++rank;
+    s |= nib << (4 * j);
+  }
+  return s;
+}
+
+// The four escape bytes starting at escape offset `off` of a slot image.
+__device__ __forceinline__ uint32_t escape_window(const uint8_t* img, int off) {
+  const uint32_t* ew = reinterpret_cast<const uint32_t*>(img + kOffEsc);
+  const uint32_t w0 = ew[off >> 2], w1 = ew[(off >> 2) + 1];
+  return __funnelshift_r(w0, w1, 8 * (off & 3));
+}
+
+// Rebuilds 32-element unit u of a slot image into 16 bf16x2 words, in decoded
+// order: word 2q+i of half h holds elements 16h+4q + {0,2} (i=0) / {1,3} (i=1).
+// x: the unit's gathered 4-bit escape bytes (byte j = group j); b3/d43: the
+// unit's base3 words and base4 - base3 (32-bit, modular: e stays exact), word
+// i covering elements 4i..4i+3.  Raw groups and 4-bit groups after them come
+// out wrong and are patched by patch_unit.
+__device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t tb, uint32_t x, const uint32_t b3[8],
+                                            const uint32_t d43[8], const uint2* lut, uint32_t o[16]) {
+  const uint32_t* cw = reinterpret_cast<const uint32_t*>(img + kOffCode);
+  const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
+  const uint4 s0 = *reinterpret_cast<const uint4*>(img + 32 * u);
+  const uint4 s1 = *reinterpret_cast<const uint4*>(img + 32 * u + 16);
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t c[4];
+    extract_codes(hh ? W1 : W0, W2, hh, c);
+    const uint2 sa = lut[(x >> (16 * hh)) & 0xFFu], sb = lut[(x >> (16 * hh + 8)) & 0xFFu];
+    const uint32_t fa = (tb >> (4 * hh)) & 1u, fb = (tb >> (4 * hh + 2)) & 1u;  // 4-bit flags of the two groups
+    uint32_t e[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t f = q < 2 ? fa : fb;
+      const uint32_t s = q == 0 ? sa.x : (q == 1 ? sa.y : (q == 2 ? sb.x : sb.y));
+      e[q] = (b3[4 * hh + q] + c[q] + s) + f * d43[4 * hh + q];
     }
-    meta[st] = tm;
-    mbar_arrive_expect_tx(&full[st], bytes);
-    if (bytes) bulk_g2s(ring[st], src, bytes, &full[st]);
-    cur = nxt;
+    const uint4 sm = hh ? s1 : s0;
+    join_v2(sm.x, e[0], o[8 * hh + 0], o[8 * hh + 1]);
+    join_v2(sm.y, e[1], o[8 * hh + 2], o[8 * hh + 3]);
+    join_v2(sm.z, e[2], o[8 * hh + 4], o[8 * hh + 5]);
+    join_v2(sm.w, e[3], o[8 * hh + 6], o[8 * hh + 7]);
+  }
+}
+
+// Decoded chunk j (0..3) of unit u of a K (kind 0) or V tile: byte offset.
+__device__ __forceinline__ uint32_t unit_chunk(int kind, int u, int j) {
+  return kind == 0 ? kswz(u >> 2, 4 * (u & 3) + j) : vswz(u >> 1, 4 * (u & 1) + j);
+}
+
+__device__ __forceinline__ void store_unit(uint8_t* dec, uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                           const uint32_t o[16]) {
+  *reinterpret_cast<uint4*>(dec + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(dec + c1) = make_uint4(o[4], o[5], o[6], o[7]);
+  *reinterpret_cast<uint4*>(dec + c2) = make_uint4(o[8], o[9], o[10], o[11]);
+  *reinterpret_cast<uint4*>(dec + c3) = make_uint4(o[12], o[13], o[14], o[15]);
+}
+
+// V tail (the open block): zero the decoded values of tokens >= nv in V unit
+// u, whose tokens are 32(u%2)..+31, so that no stale value meets a zero
+// probability.  Runs for one block per split at most.
+__device__ __noinline__ void clear_tail(uint8_t* dec, int u, int nv) {
+#pragma unroll 1
+  for (int j = 0; j < 4; ++j) {
+    const int t0 = 32 * (u & 1) + 8 * j;  // chunk j: tokens t0..t0+7 stored {0,2,1,3,4,6,5,7}
+    if (t0 + 8 <= nv) continue;
+    uint4* p = reinterpret_cast<uint4*>(dec + vswz(u >> 1, 4 * (u & 1) + j));
+    uint4 w = *p;
+    w.x &= (t0 < nv ? 0x0000FFFFu : 0u) | (t0 + 2 < nv ? 0xFFFF0000u : 0u);
+    w.y &= (t0 + 1 < nv ? 0x0000FFFFu : 0u) | (t0 + 3 < nv ? 0xFFFF0000u : 0u);
+    w.z &= (t0 + 4 < nv ? 0x0000FFFFu : 0u) | (t0 + 6 < nv ? 0xFFFF0000u : 0u);
+    w.w &= (t0 + 5 < nv ? 0x0000FFFFu : 0u) | (t0 + 7 < nv ? 0xFFFF0000u : 0u);
+    *p = w;
+  }
+}
+
+// Re-decodes the groups of unit u that decode_unit cannot: raw groups (their
+// exponent bits 3..7 are five escape bit planes) and 4-bit groups placed after
+// a raw group.  off: the unit's first escape byte.  Rewrites those groups'
+// 16-byte chunks in the decoded tile.
+__device__ __noinline__ void patch_unit(const uint8_t* img, int kind, int u, uint32_t tb, int off, const uint8_t* b4g,
+                                        const uint2* lut, uint8_t* dec) {
+  uint32_t fix = 0;
+  bool raw = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t t = (tb >> (2 * j)) & 3u;
+    if (t == 2u || (t == 1u && raw)) fix |= 1u << j;
+    if (t == 2u) raw = true;
+  }
+  const uint32_t* cw = reinterpret_cast<const uint32_t*>(img + kOffCode);
+  const uint8_t* esc = img + kOffEsc;
+#pragma unroll 1
+  while (fix) {
+    const int j = __ffs(fix) - 1;
+    fix &= fix - 1;
+    const uint32_t t = (tb >> (2 * j)) & 3u;
+    const int o = off + esc_count(tb & ((1u << (2 * j)) - 1u));
+    const int hh = j >> 1;
+    uint32_t c[4];
+    extract_codes(hh ? cw[256 + u] : cw[u], cw[512 + u], hh, c);
+    const uint32_t ca = (j & 1) ? c[2] : c[0], cb = (j & 1) ? c[3] : c[1];
+    const uint2 smw = *reinterpret_cast<const uint2*>(img + 32 * u + 8 * j);
+    uint32_t ea, eb;
+    if (t == 1u) {
+      uint32_t ba, bb;
+      if (kind == 0) {
+        const int ch = 32 * (u & 3) + 8 * j;
+        ba = *reinterpret_cast<const uint32_t*>(b4g + ch);
+        bb = *reinterpret_cast<const uint32_t*>(b4g + ch + 4);
+      } else {
+        ba = bb = 0x01010101u * b4g[u >> 1];
+      }
+      const uint2 s = lut[esc[o]];
+      ea = ba + ca + s.x;
+      eb = bb + cb + s.y;
+    } else {
+      uint32_t h0 = 0, h1 = 0;
+#pragma unroll
+      for (int k = 0; k < 5; ++k) {
+        const uint2 s = lut[esc[o + k]];  // bit plane 3+k: spread to bit 3, shifted up by k
+        h0 |= s.x << k;
+        h1 |= s.y << k;
+      }
+      ea = ca | h0;
+      eb = cb | h1;
+    }
+    uint32_t w[4];
+    join_v2(smw.x, ea, w[0], w[1]);
+    join_v2(smw.y, eb, w[2], w[3]);
+    *reinterpret_cast<uint4*>(dec + unit_chunk(kind, u, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Raw tile (BF16 in storage order) unit u into decoded order.
+__device__ __forceinline__ void raw_unit(const uint8_t* img, int u, uint32_t o[16]) {
+  const uint4* src = reinterpret_cast<const uint4*>(img + 64 * u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 w = src[i];
+    o[4 * i + 0] = __byte_perm(w.x, w.y, 0x5410);  // elements {0, 2} of the quad
+    o[4 * i + 1] = __byte_perm(w.x, w.y, 0x7632);  // elements {1, 3}
+    o[4 * i + 2] = __byte_perm(w.z, w.w, 0x5410);
+    o[4 * i + 3] = __byte_perm(w.z, w.w, 0x7632);
+  }
+}
+
+// ------------------------------------------------------------------ decoders
+
+// One decoder warp: eighth e8 (code units [32 e8, 32 e8 + 32)) of every
+// block's K (kind 0) or V (kind 1) tile; lane l owns unit 32 e8 + l.  A K unit
+// is one token's channel block l%4, a V unit one half of channel 16 e8 + l/2,
+// so a lane's window bases never change.  Both kinds run this one code path.
+__device__ __forceinline__ void decoder_warp(const AttnArgs& a, AttSmem& sm, int h, int blk0, int n_my, int len,
+                                             int kind, int e8, int lane) {
+  const uint8_t* b3g = a.base3 + (kind * a.Hkv + h) * kD;
+  const uint8_t* b4g = a.base4 + (kind * a.Hkv + h) * kD;
+  const int u = kDirUnits * e8 + lane;
+  uint32_t b3[8], d43[8];
+  if (kind == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      b3[i] = *reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 4 * i);
+      d43[i] = *reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 4 * i) - b3[i];
+    }
+  } else {
+    const uint32_t x3 = 0x01010101u * b3g[u >> 1], x4 = 0x01010101u * b4g[u >> 1];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      b3[i] = x3;
+      d43[i] = x4 - x3;
+    }
+  }
+  const uint32_t c0 = unit_chunk(kind, u, 0), c1 = unit_chunk(kind, u, 1), c2 = unit_chunk(kind, u, 2),
+                 c3 = unit_chunk(kind, u, 3);
+  uint64_t* dec_full = kind ? sm.dvFull : sm.dkFull;
+  uint64_t* dec_empty = kind ? sm.dvEmpty : sm.dkEmpty;
+#pragma unroll 1
+  for (int j = 0; j < n_my; ++j) {
+    const int st = j % kStages, db = j % kDecBufs;
+    mbar_wait(&sm.stFull[st], (j / kStages) & 1, a.status);
+    if (j >= kDecBufs) mbar_wait(&dec_empty[db], ((j / kDecBufs) & 1) ^ 1, a.status);
+    const int mode = sm.smeta[st].mode[kind], esc_len = sm.smeta[st].esc[kind];
+    const int nv = min(kBlock, len - (blk0 + j) * kBlock);
+    const uint8_t* img = sm.stage[st][kind];
+    uint8_t* dec = kind ? sm.decV[db] : sm.decK[db];
+    const bool slot = mode == GAAC_MODE_SLOT;
+    bool bad = !slot && mode != GAAC_MODE_RAW;
+    uint32_t tb = 0;
+    int off = 0;
+    if (slot) {
+      const uint16_t* dir = reinterpret_cast<const uint16_t*>(img + kOffDir);
+      const int start = e8 ? dir[e8 - 1] : 0, end = dir[e8];
+      tb = img[kOffTag + u];
+      const int cnt = esc_count(tb);
+      const int incl = warp_incl_scan(cnt, lane);
+      off = start + incl - cnt;  // escape bytes are in unit order
+      bad = __any_sync(kFull, ((tb & (tb >> 1)) & 0x55u) != 0u) || start > end || end > esc_len ||
+            start + __shfl_sync(kFull, incl, 31) != end;
+      if (bad && lane == 0) report(a.status, GAAC_EFORMAT);
+    }
+    // Every escape offset used below lies inside [start, end) and end <= 496.
+    uint32_t o[16];
+    if (bad) {  // no valid data: zeros (K blocks are also masked by the tensor-core warp)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = 0u;
+    } else if (slot) {
+      decode_unit(img, u, tb, __byte_perm(escape_window(img, off), 0u, sm.sel[tb]), b3, d43, sm.lut, o);
+    } else {
+      raw_unit(img, u, o);
+    }
+    store_unit(dec, c0, c1, c2, c3, o);
+    if (slot && !bad && (tb & 0xAAu)) patch_unit(img, kind, u, tb, off, b4g, sm.lut, dec);
+    if (kind == 1 && nv < kBlock) clear_tail(dec, u, nv);
+    if (kind == 0 && lane == 0) {
+      sm.dec_bad[db][e8] = bad ? 1 : 0;
+      if (e8 == 0) sm.dec_nv[db] = nv;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&sm.stEmpty[st]);
+      mbar_arrive(&dec_full[db]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ producer
+
+__device__ __forceinline__ void producer_lane(const AttnArgs& a, AttSmem& sm, int b, int h, int blk0, int n_my) {
+  const gaac_entry* tab = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk0) * a.Hkv + h) * 2;
+  const size_t stride = static_cast<size_t>(a.Hkv) * 2;
+  uint2 curK = make_uint2(0u, 0u), curV = make_uint2(0u, 0u);
+  if (n_my > 0) {
+    curK = *reinterpret_cast<const uint2*>(tab);
+    curV = *reinterpret_cast<const uint2*>(tab + 1);
+  }
+#pragma unroll 1
+  for (int j = 0; j < n_my; ++j) {
+    uint2 nxtK = curK, nxtV = curV;
+    if (j + 1 < n_my) {
+      nxtK = *reinterpret_cast<const uint2*>(tab + (j + 1) * stride);
+      nxtV = *reinterpret_cast<const uint2*>(tab + (j + 1) * stride + 1);
+    }
+    const int st = j % kStages;
+    if (j >= kStages) mbar_wait(&sm.stEmpty[st], ((j / kStages) & 1) ^ 1, a.status);
+    StageMeta m;
+    uint32_t bytes[2];
+    const void* src[2];
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint2 cur = kv ? curV : curK;
+      const uint32_t index = cur.x, esc_len = cur.y & 0xFFFFu, emode = (cur.y >> 16) & 0xFFu;
+      bytes[kv] = 0;
+      src[kv] = nullptr;
+      m.mode[kv] = GAAC_MODE_NONE;
+      m.esc[kv] = 0;
+      if (emode == GAAC_MODE_SLOT && static_cast<int64_t>(index) < a.n_slots && esc_len <= kEscCap) {
+        m.mode[kv] = GAAC_MODE_SLOT;
+        m.esc[kv] = static_cast<int>(esc_len);
+        bytes[kv] = (kOffEsc + esc_len + 15u) & ~15u;
+        src[kv] = a.slot_pool + static_cast<size_t>(index) * kSlot;
+      } else if (emode == GAAC_MODE_RAW && static_cast<int64_t>(index) < a.n_raw) {
+        m.mode[kv] = GAAC_MODE_RAW;
+        bytes[kv] = kRawBytes;
+        src[kv] = a.raw_pool + static_cast<size_t>(index) * kTile;
+      } else {
+        report(a.status, GAAC_EFORMAT);
+      }
+    }
+    sm.smeta[st] = m;
+    mbar_arrive_expect_tx(&sm.stFull[st], bytes[0] + bytes[1]);
+    if (bytes[0]) bulk_g2s(sm.stage[st][0], src[0], bytes[0], &sm.stFull[st]);
+    if (bytes[1]) bulk_g2s(sm.stage[st][1], src[1], bytes[1], &sm.stFull[st]);
+    curK = nxtK;
+    curV = nxtV;
+  }
+  // Every issued copy was consumed by the decoders; after a timed-out wait,
+  // wait once more (bounded) so that no copy is still landing at exit.
+#pragma unroll 1
+  for (int i = max(0, n_my - kStages); i < n_my; ++i)
+    mbar_wait(&sm.stFull[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
+}
+
+// ------------------------------------------------------------- tensor cores
+
+__device__ __forceinline__ void tensor_warp(const AttnArgs& a, AttSmem& sm, int n_my, float* part, int mw, int lane) {
+  const int g = lane >> 2, tq = lane & 3;
+  // ldmatrix row of this lane inside a 16-row tile: matrix m = lane/8 covers rows 8(m%2).., columns 8(m/2)..
+  const int lrow = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int lcol = lane >> 4;
+  const int ktok = quad_perm(lrow);  // QK^T rows follow the decoded token order of V
+  float acc[8][4];
+#pragma unroll
+  for (int ct = 0; ct < 8; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2tq, 2tq+1 (log2 domain)
+  const uint32_t pth = smem_addr(&sm.pt[mw][0][0][0]), ptl = smem_addr(&sm.pt[mw][1][0][0]);
+  const uint32_t qsa = smem_addr(&sm.qs[lane & 7][0]) + 16u * (lane >> 3);  // q rows as B: chunk lane/8
+  const int prow = lane & 7, pm = lane >> 3;
+  // P^T as B: matrices (hi k0-7, hi k8-15, lo k0-7, lo k8-15) of one k-step
+  const uint32_t pba = ((lane >> 4) ? ptl : pth) + static_cast<uint32_t>(prow * kPtStride * 2 + 16 * ((lane >> 3) & 1));
+
+#pragma unroll 1
+  for (int j = mw; j < n_my; j += kMWarps) {
+    const int db = j % kDecBufs;
+    const uint32_t par = (j / kDecBufs) & 1;
+    mbar_wait(&sm.dkFull[db], par, a.status);
+    const int nv = sm.dec_nv[db];
+    const uint2 badw = *reinterpret_cast<const uint2*>(sm.dec_bad[db]);
+    const bool kbad = (badw.x | badw.y) != 0u;
+    // ---- S = K q^T: 4 row tiles of 16 tokens, 8 k-steps of 16 channels
+    float s[4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+    const uint32_t kb = smem_addr(sm.decK[db]);
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {  // two k-steps per q load
+      uint32_t q0, q1, q2, q3;
+      ldsm_x4(qsa + 64u * k2, q0, q1, q2, q3);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int ks = 2 * k2 + kk;
+        const uint32_t ka = kb + kswz(ktok, 2 * ks + lcol);  // row 16mt + ktok keeps the row's swizzle
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(ka + 4096u * mt, a0, a1, a2, a3);
+          mma_bf16(s[mt], a0, a1, a2, a3, kk ? q2 : q0, kk ? q3 : q1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.dkEmpty[db]);
+    // ---- online softmax (rows g and g+8 of each tile: tokens 16mt + quad_perm(g) (+8))
+    const int tg = quad_perm(g);
+    float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const bool ok0 = !kbad && 16 * mt + tg < nv, ok1 = !kbad && 16 * mt + 8 + tg < nv;
+      s[mt][0] = ok0 ? s[mt][0] * a.scale_log2 : -INFINITY;
+      s[mt][1] = ok0 ? s[mt][1] * a.scale_log2 : -INFINITY;
+      s[mt][2] = ok1 ? s[mt][2] * a.scale_log2 : -INFINITY;
+      s[mt][3] = ok1 ? s[mt][3] * a.scale_log2 : -INFINITY;
+      x0 = fmaxf(x0, fmaxf(s[mt][0], s[mt][2]));
+      x1 = fmaxf(x1, fmaxf(s[mt][1], s[mt][3]));
+    }
+    if (__any_sync(kFull, x0 > m0 || x1 > m1)) {  // a running maximum rises: rescale (rare after the first blocks)
+#pragma unroll
+      for (int d = 4; d < 32; d <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, d));
+        x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, d));
+      }
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
+      const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int ct = 0; ct < 8; ++ct) {
+        acc[ct][0] *= al0;
+        acc[ct][1] *= al1;
+        acc[ct][2] *= al0;
+        acc[ct][3] *= al1;
+      }
+      m0 = n0;
+      m1 = n1;
+    }
+    uint32_t ph[4][2], pl[4][2];  // [tile][row half]: bf16x2 of heads (2tq, 2tq+1)
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float p0 = m0 == -INFINITY ? 0.f : fast_exp2(s[mt][2 * hf] - m0);
+        const float p1 = m1 == -INFINITY ? 0.f : fast_exp2(s[mt][2 * hf + 1] - m1);
+        l0 += p0;
+        l1 += p1;
+        const uint32_t hi = pack_bf16x2(p0, p1);
+        ph[mt][hf] = hi;
+        pl[mt][hf] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+      }
+    }
+    // P^T[head][position]: matrix k of a store covers positions 8(4i + k)..+7 (tile 2i + k/2, row half k%2)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t off = static_cast<uint32_t>(prow * kPtStride * 2 + (4 * i + pm) * 16);
+      stsm_x4_trans(pth + off, ph[2 * i][0], ph[2 * i][1], ph[2 * i + 1][0], ph[2 * i + 1][1]);
+      stsm_x4_trans(ptl + off, pl[2 * i][0], pl[2 * i][1], pl[2 * i + 1][0], pl[2 * i + 1][1]);
+    }
+    __syncwarp();
+    // ---- acc += V^T P: 8 row tiles of 16 channels, 4 k-steps of 16 tokens
+    mbar_wait(&sm.dvFull[db], par, a.status);
+    const uint32_t vb = smem_addr(sm.decV[db]);
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt) {
+      uint32_t bh0, bh1, bl0, bl1;
+      ldsm_x4(pba + 32u * kt, bh0, bh1, bl0, bl1);
+      const uint32_t va = vb + vswz(lrow, 2 * kt + lcol);  // row 16ct + lrow keeps the row's swizzle
+#pragma unroll
+      for (int ct = 0; ct < 8; ++ct) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(va + 2048u * ct, a0, a1, a2, a3);
+        mma_bf16(acc[ct], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16(acc[ct], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.dvEmpty[db]);
+  }
+  // ---- row sums over the 8 lanes of each head pair, then merge the two warps
+#pragma unroll
+  for (int d = 4; d < 32; d <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, d);
+    l1 += __shfl_xor_sync(kFull, l1, d);
+  }
+  if (mw == 1) {
+    if (g == 0) {
+      sm.xm[2 * tq] = m0;
+      sm.xm[2 * tq + 1] = m1;
+      sm.xl[2 * tq] = l0;
+      sm.xl[2 * tq + 1] = l1;
+    }
+#pragma unroll
+    for (int ct = 0; ct < 8; ++ct) {
+      sm.xacc[2 * tq][16 * ct + g] = acc[ct][0];
+      sm.xacc[2 * tq + 1][16 * ct + g] = acc[ct][1];
+      sm.xacc[2 * tq][16 * ct + g + 8] = acc[ct][2];
+      sm.xacc[2 * tq + 1][16 * ct + g + 8] = acc[ct][3];
+    }
+  }
+  named_bar_sync(kBarM, kMWarps * 32);
+  if (mw == 0) {
+    float w[2][2], mm[2];  // [head i][own, other]
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float mo = i ? m1 : m0, mx = sm.xm[2 * tq + i];
+      const float M = fmaxf(mo, mx);
+      mm[i] = M;
+      w[i][0] = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
+      w[i][1] = mx == -INFINITY ? 0.f : fast_exp2(mx - M);
+    }
+    if (g == 0) {
+      part[4 * tq + 0] = mm[0];
+      part[4 * tq + 1] = w[0][0] * l0 + w[0][1] * sm.xl[2 * tq];
+      part[4 * tq + 2] = mm[1];
+      part[4 * tq + 3] = w[1][0] * l1 + w[1][1] * sm.xl[2 * tq + 1];
+    }
+    float* pa = part + 2 * kRPad;
+#pragma unroll
+    for (int ct = 0; ct < 8; ++ct) {
+      const int cA = 16 * ct + g, cB = cA + 8;
+      pa[(2 * tq) * kD + cA] = w[0][0] * acc[ct][0] + w[0][1] * sm.xacc[2 * tq][cA];
+      pa[(2 * tq + 1) * kD + cA] = w[1][0] * acc[ct][1] + w[1][1] * sm.xacc[2 * tq + 1][cA];
+      pa[(2 * tq) * kD + cB] = w[0][0] * acc[ct][2] + w[0][1] * sm.xacc[2 * tq][cB];
+      pa[(2 * tq + 1) * kD + cB] = w[1][0] * acc[ct][3] + w[1][1] * sm.xacc[2 * tq + 1][cB];
+    }
   }
 }
 
@@ -261,7 +652,7 @@ __device__ __forceinline__ void stream_tiles(const AttnArgs& a, AttSmem& sm, int
 // thread owns one float4 column of the output and a subset of the splits,
 // issues that subset's loads ten at a time and folds them in with its own
 // running maximum; the subsets are then combined the same way in shared
-// memory.  The ring buffers are free by then and hold that exchange.
+// memory.  The staging ring is free by then and holds that exchange.
 // base: the first partial of the pair; out: its first output row.
 __device__ __noinline__ void merge_splits(const float* base, int ns, int r, float* out, AttSmem& sm, int tid) {
   constexpr int kBatch = 10;
@@ -310,8 +701,8 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
       }
     }
   }
-  float4* xa = reinterpret_cast<float4*>(sm.ringK);  // [groups][o4n] accumulators
-  float2* xm = reinterpret_cast<float2*>(sm.ringV);  // [groups][o4n] (running max, denominator)
+  float4* xa = reinterpret_cast<float4*>(sm.stage[0][0]);  // [groups][o4n] accumulators
+  float2* xm = reinterpret_cast<float2*>(sm.stage[1][0]);  // [groups][o4n] (running max, denominator)
   if (grp < groups && groups > 1) {
     xa[grp * o4n + o4] = acc;
     xm[grp * o4n + o4] = make_float2(mt, den);
@@ -348,6 +739,7 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
   }
 }
 
+
 __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   AttSmem& sm = *reinterpret_cast<AttSmem*>(smem_raw);
@@ -358,321 +750,57 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     if (tid == 0) report(a.status, GAAC_EINVAL);
     len = 0;
   }
+  // This split's blocks of the sequence: an even share of its blocks.
   const int nblk = (len + kBlock - 1) / kBlock;
-  const int per = (a.max_blocks + a.n_splits - 1) / a.n_splits;
+  const int per = (nblk + a.n_splits - 1) / a.n_splits;
   const int blk0 = split * per;
   const int n_my = max(0, min(nblk, blk0 + per) - blk0);
 
-  for (int x = tid; x < 256; x += kAttThreads) sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
+  for (int x = tid; x < 256; x += kAttThreads) {
+    sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
+    sm.sel[x] = gather_selector(static_cast<uint32_t>(x));
+  }
+  // q of the kv-head's query heads, times 2^-4, channels in decoded order (the B operand of QK^T)
+  for (int x = tid; x < kRPad * kD / 2; x += kAttThreads) {
+    const int n = x / (kD / 2), p = 2 * (x % (kD / 2));  // positions p, p+1 hold channels quad_perm(p), quad_perm(p+1)
+    uint32_t w = 0u;
+    if (n < a.r) {
+      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + h * a.r + n) * kD;
+      w = bf16x2_div16(static_cast<uint32_t>(qrow[quad_perm(p)]) | (static_cast<uint32_t>(qrow[quad_perm(p + 1)]) << 16));
+    }
+    *reinterpret_cast<uint32_t*>(&sm.qs[n][p]) = w;
+  }
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.fullK[s], 1);
-      mbar_init(&sm.fullV[s], 1);
-      mbar_init(&sm.emptyK[s], kKWarps);
-      mbar_init(&sm.emptyV[s], kVWarps);
+      mbar_init(&sm.stFull[s], 1);
+      mbar_init(&sm.stEmpty[s], kDWarps);
+    }
+#pragma unroll
+    for (int d = 0; d < kDecBufs; ++d) {
+      mbar_init(&sm.dkFull[d], kDWarps / 2);
+      mbar_init(&sm.dvFull[d], kDWarps / 2);
+      mbar_init(&sm.dkEmpty[d], 1);
+      mbar_init(&sm.dvEmpty[d], 1);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  const int g = lane >> 2, tq = lane & 3;
   const int r = a.r;
   float* part = a.part + ((static_cast<size_t>(b) * a.Hkv + h) * a.n_splits + split) * kPartFloats;
-
-  if (warp == kProducerWarp) {  // ------------------------------------------------ producer
-    if (lane < 2) stream_tiles(a, sm, lane, b, h, blk0, n_my);
-  } else if (warp < kKWarps) {  // ------------------------------------------------ K warps
-    const int kw = warp;
-    uint32_t qf[16];
-    if (g < r) {
-      const uint4* qp =
-          reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + h * r + g) * kD + 32 * tq);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 w = qp[i];
-        qf[4 * i] = bf16x2_div16(w.x);
-        qf[4 * i + 1] = bf16x2_div16(w.y);
-        qf[4 * i + 2] = bf16x2_div16(w.z);
-        qf[4 * i + 3] = bf16x2_div16(w.w);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) qf[i] = 0u;
-    }
-    uint32_t k3[8], k4[8];
-    {
-      const uint4* p3 = reinterpret_cast<const uint4*>(a.base3 + h * kD + 32 * tq);
-      const uint4* p4 = reinterpret_cast<const uint4*>(a.base4 + h * kD + 32 * tq);
-      const uint4 x0 = p3[0], x1 = p3[1], y0 = p4[0], y1 = p4[1];
-      k3[0] = x0.x; k3[1] = x0.y; k3[2] = x0.z; k3[3] = x0.w;
-      k3[4] = x1.x; k3[5] = x1.y; k3[6] = x1.z; k3[7] = x1.w;
-      k4[0] = y0.x; k4[1] = y0.y; k4[2] = y0.z; k4[3] = y0.w;
-      k4[4] = y1.x; k4[5] = y1.y; k4[6] = y1.z; k4[7] = y1.w;
-    }
-    float m0 = -INFINITY, m1 = -INFINITY;  // running max of heads 2tq, 2tq+1 (log2 domain)
-    const int t0 = 16 * kw + g, t1 = t0 + 8;
-    for (int i = 0; i < n_my; ++i) {
-      const int st = i % kStages, par = i & 1;
-      mbar_wait(&sm.fullK[st], (i / kStages) & 1, a.status);
-      const TileMeta md = sm.metaK[st];
-      const int nv = min(kBlock, len - (blk0 + i) * kBlock);
-      const uint8_t* tK = sm.ringK[st];
-      int modeK = md.mode;
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-      if (modeK == GAAC_MODE_SLOT) {
-        int before;
-        if (!range_escape_base(tK, md.esc, kw, lane, before)) {
-          modeK = GAAC_MODE_NONE;
-          if (kw == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
-        } else {
-          // this lane's units: uA = 4*t0 + tq = 64kw + lane, uB = uA + 32 (range positions lane, lane + 32)
-          const uint32_t tbA = tK[kOffTag + 64 * kw + lane], tbB = tK[kOffTag + 64 * kw + 32 + lane];
-          const int cA = esc_count(tbA), cB = esc_count(tbB);
-          const int sc = warp_incl_scan(cA | (cB << 16), lane);
-          const int totA = __shfl_sync(0xFFFFFFFFu, sc, 31) & 0xFFFF;
-          const int offA = before + (sc & 0xFFFF) - cA;
-          const int offB = before + totA + (sc >> 16) - cB;
-          const uint32_t xA = gather_groups<4>(tK + kOffEsc, tbA, offA);
-          const uint32_t xB = gather_groups<4>(tK + kOffEsc, tbB, offB);
-          const uint32_t* cw = reinterpret_cast<const uint32_t*>(tK + kOffCode);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t ka[8], kb[8];
-            const int uA = 4 * t0 + tq, uB = 4 * t1 + tq;
-            const uint32_t nibA = (tbA >> (4 * hh)) & 15u, nibB = (tbB >> (4 * hh)) & 15u;
-            const int hoA = offA + (hh ? esc_count(tbA & 15u) : 0), hoB = offB + (hh ? esc_count(tbB & 15u) : 0);
-            decode_half(tK, cw[256 * hh + uA], cw[512 + uA], hh, nibA, xA >> (16 * hh), hoA,
-                        *reinterpret_cast<const uint4*>(tK + 128 * t0 + 32 * tq + 16 * hh), k3 + 4 * hh,
-                        k4 + 4 * hh, sm.lut, ka);
-            decode_half(tK, cw[256 * hh + uB], cw[512 + uB], hh, nibB, xB >> (16 * hh), hoB,
-                        *reinterpret_cast<const uint4*>(tK + 128 * t1 + 32 * tq + 16 * hh), k3 + 4 * hh,
-                        k4 + 4 * hh, sm.lut, kb);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int ks = 4 * hh + j;
-              mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks],
-                       qf[2 * ks + 1]);
-            }
-          }
-        }
-      } else if (modeK == GAAC_MODE_RAW) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t ka[8], kb[8];
-          load8(tK + 256 * t0 + 64 * tq + 32 * hh, ka);
-          load8(tK + 256 * t1 + 64 * tq + 32 * hh, kb);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int ks = 4 * hh + j;
-            mma_bf16(j & 1 ? sb : sa, ka[2 * j], kb[2 * j], ka[2 * j + 1], kb[2 * j + 1], qf[2 * ks], qf[2 * ks + 1]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.emptyK[st]);  // the K tile is no longer read
-      const bool ok0 = t0 < nv && modeK != GAAC_MODE_NONE, ok1 = t1 < nv && modeK != GAAC_MODE_NONE;
-      // scores: (t0, head 2tq), (t0, 2tq+1), (t1, 2tq), (t1, 2tq+1)
-      const float s0 = ok0 ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
-      const float s1 = ok0 ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
-      const float s2 = ok1 ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
-      const float s3 = ok1 ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
-      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
-#pragma unroll
-      for (int d = 4; d < 32; d <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(0xFFFFFFFFu, x0, d));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xFFFFFFFFu, x1, d));
-      }
-      if (g == 0) {
-        sm.wmax[par][2 * tq][kw] = x0;
-        sm.wmax[par][2 * tq + 1][kw] = x1;
-      }
-      named_bar_sync(kBarK, kKWarps * 32);
-      const float4 wa = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq][0]);
-      const float4 wb = *reinterpret_cast<const float4*>(&sm.wmax[par][2 * tq + 1][0]);
-      const float n0 = fmaxf(m0, fmaxf(fmaxf(wa.x, wa.y), fmaxf(wa.z, wa.w)));
-      const float n1 = fmaxf(m1, fmaxf(fmaxf(wb.x, wb.y), fmaxf(wb.z, wb.w)));
-      const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
-      const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
-      const float p0 = n0 == -INFINITY ? 0.f : fast_exp2(s0 - n0);
-      const float p2 = n0 == -INFINITY ? 0.f : fast_exp2(s2 - n0);
-      const float p1 = n1 == -INFINITY ? 0.f : fast_exp2(s1 - n1);
-      const float p3 = n1 == -INFINITY ? 0.f : fast_exp2(s3 - n1);
-      m0 = n0;
-      m1 = n1;
-      float y0 = p0 + p2, y1 = p1 + p3;
-#pragma unroll
-      for (int d = 4; d < 32; d <<= 1) {
-        y0 += __shfl_xor_sync(0xFFFFFFFFu, y0, d);
-        y1 += __shfl_xor_sync(0xFFFFFFFFu, y1, d);
-      }
-      if (i >= 2) named_bar_sync(kBarPEmpty + par, (kKWarps + kVWarps) * 32);  // V warps are done with P[par]
-      if (g == 0) {
-        sm.wsum[par][2 * tq][kw] = y0;
-        sm.wsum[par][2 * tq + 1][kw] = y1;
-        if (kw == 0) {
-          sm.alpha[par][2 * tq] = al0;
-          sm.alpha[par][2 * tq + 1] = al1;
-        }
-      }
-      {
-        uint16_t* Ph = &sm.P[par][0][0][0];
-        uint16_t* Pl = &sm.P[par][1][0][0];
-        const float pv[4] = {p0, p1, p2, p3};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int head = 2 * tq + (j & 1), tok = j < 2 ? t0 : t1;
-          const uint16_t hb = to_bf16(pv[j]);
-          Ph[head * kPStride + tok] = hb;
-          Pl[head * kPStride + tok] = to_bf16(pv[j] - __uint_as_float(static_cast<uint32_t>(hb) << 16));
-        }
-      }
-      named_bar_arrive(kBarPFull + par, (kKWarps + kVWarps) * 32);
-    }
-    if (kw == 0 && g == 0) {
-      part[4 * tq] = m0;      // head 2tq
-      part[4 * tq + 2] = m1;  // head 2tq + 1
-    }
-  } else {  // ---------------------------------------------------------------------- V warps
-  const int vw = warp - kKWarps;
-  uint32_t v3[4], v4[4];  // [mi*2 + hb]: channel 32vw + 16mi + g + 8hb, byte replicated
-#pragma unroll
-  for (int mi = 0; mi < 2; ++mi) {
-#pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      const int c = 32 * vw + 16 * mi + g + 8 * hb;
-      v3[2 * mi + hb] = 0x01010101u * a.base3[(a.Hkv + h) * kD + c];
-      v4[2 * mi + hb] = 0x01010101u * a.base4[(a.Hkv + h) * kD + c];
-    }
-  }
-  float accH[2][4], accL[2][4];
-#pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) accH[mi][j] = accL[mi][j] = 0.f;
-  float lg = 0.f;  // running sum of head g
-  for (int i = 0; i < n_my; ++i) {
-    const int st = i % kStages, par = i & 1;
-    mbar_wait(&sm.fullV[st], (i / kStages) & 1, a.status);
-    const TileMeta md = sm.metaV[st];
-    const int nv = min(kBlock, len - (blk0 + i) * kBlock);
-    const uint8_t* tV = sm.ringV[st];
-    int modeV = md.mode;
-    uint32_t va[2][8], vb[2][8];
-    if (modeV == GAAC_MODE_SLOT) {
-      int before;
-      if (!range_escape_base(tV, md.esc, vw, lane, before)) {
-        modeV = GAAC_MODE_NONE;
-        if (vw == 0 && lane == 0) report(a.status, GAAC_EFORMAT);
-      } else {
-        // half-unit k = 2*mi + hb: channel c, unit u = 2c + tq/2, half tq%2; its range position
-        // (in half-units) is 64*mi + 32*hb + lane, so each k is a lane-ordered segment of 32.
-        const uint32_t* cw = reinterpret_cast<const uint32_t*>(tV + kOffCode);
-        const int hh = tq & 1;
-        uint32_t nib[4];
-        int cnt[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int u = 64 * vw + 32 * (k >> 1) + 16 * (k & 1) + 2 * g + (tq >> 1);
-          nib[k] = (static_cast<uint32_t>(tV[kOffTag + u]) >> (4 * hh)) & 15u;
-          cnt[k] = esc_count(nib[k]);
-        }
-        const int s01 = warp_incl_scan(cnt[0] | (cnt[1] << 16), lane);
-        const int s23 = warp_incl_scan(cnt[2] | (cnt[3] << 16), lane);
-        const int t01 = __shfl_sync(0xFFFFFFFFu, s01, 31), t23 = __shfl_sync(0xFFFFFFFFu, s23, 31);
-        int ho[4];
-        ho[0] = before + (s01 & 0xFFFF) - cnt[0];
-        ho[1] = before + (t01 & 0xFFFF) + (s01 >> 16) - cnt[1];
-        ho[2] = before + (t01 & 0xFFFF) + (t01 >> 16) + (s23 & 0xFFFF) - cnt[2];
-        ho[3] = before + (t01 & 0xFFFF) + (t01 >> 16) + (t23 & 0xFFFF) + (s23 >> 16) - cnt[3];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = 32 * vw + 16 * (k >> 1) + g + 8 * (k & 1);
-          const int u = 2 * c + (tq >> 1);
-          const uint32_t xw = gather_groups<2>(tV + kOffEsc, nib[k], ho[k]);
-          const uint32_t b3[4] = {v3[k], v3[k], v3[k], v3[k]}, b4[4] = {v4[k], v4[k], v4[k], v4[k]};
-          decode_half(tV, cw[256 * hh + u], cw[512 + u], hh, nib[k], xw, ho[k],
-                      *reinterpret_cast<const uint4*>(tV + 64 * c + 16 * tq), b3, b4, sm.lut,
-                      (k & 1) ? vb[k >> 1] : va[k >> 1]);
-        }
-      }
-    }
-    if (modeV == GAAC_MODE_RAW) {
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        const int cA = 32 * vw + 16 * mi + g;
-        load8(tV + 128 * cA + 32 * tq, va[mi]);
-        load8(tV + 128 * (cA + 8) + 32 * tq, vb[mi]);
-      }
-    } else if (modeV == GAAC_MODE_NONE) {
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) va[mi][j] = vb[mi][j] = 0u;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.emptyV[st]);  // the V tile is no longer read
-    if (nv < kBlock) {  // the open tail: tokens past the sequence must not reach the product
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int tt = 16 * tq + 2 * m;
-        const uint32_t keep = (tt < nv ? 0x0000FFFFu : 0u) | (tt + 1 < nv ? 0xFFFF0000u : 0u);
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-          va[mi][m] &= keep;
-          vb[mi][m] &= keep;
-        }
-      }
-    }
-    named_bar_sync(kBarPFull + par, (kKWarps + kVWarps) * 32);  // P of block i is written
-    uint32_t ph[8], pl[8];
-    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][0][g][16 * tq]), ph);
-    load8(reinterpret_cast<const uint8_t*>(&sm.P[par][1][g][16 * tq]), pl);
-    const float4 ws = *reinterpret_cast<const float4*>(&sm.wsum[par][g][0]);
-    const float alg = sm.alpha[par][g], al0 = sm.alpha[par][2 * tq], al1 = sm.alpha[par][2 * tq + 1];
-    if (i + 2 < n_my) named_bar_arrive(kBarPEmpty + par, (kKWarps + kVWarps) * 32);
-    lg = lg * alg + ((ws.x + ws.y) + (ws.z + ws.w));
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      accH[mi][0] *= al0; accH[mi][1] *= al1; accH[mi][2] *= al0; accH[mi][3] *= al1;
-      accL[mi][0] *= al0; accL[mi][1] *= al1; accL[mi][2] *= al0; accL[mi][3] *= al1;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_bf16(accH[mi], va[mi][2 * ks], vb[mi][2 * ks], va[mi][2 * ks + 1], vb[mi][2 * ks + 1], ph[2 * ks],
-                 ph[2 * ks + 1]);
-        mma_bf16(accL[mi], va[mi][2 * ks], vb[mi][2 * ks], va[mi][2 * ks + 1], vb[mi][2 * ks + 1], pl[2 * ks],
-                 pl[2 * ks + 1]);
-      }
-    }
-  }
-  // Every issued copy was awaited (K warps and V warps consumed every stage);
-  // after a timed-out wait, wait once more (bounded) so that no copy is still
-  // landing when the CTA exits.
-  if (vw == 0 && lane == 0) {
-    for (int i = max(0, n_my - kStages); i < n_my; ++i) {
-      mbar_wait(&sm.fullK[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
-      mbar_wait(&sm.fullV[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
-    }
-  }
-  if (vw == 0 && tq == 0) part[2 * g + 1] = lg;
-#pragma unroll
-  for (int mi = 0; mi < 2; ++mi) {
-    const int cA = 32 * vw + 16 * mi + g, cB = cA + 8;
-    float* pa = part + 2 * kRPad;
-    pa[(2 * tq) * kD + cA] = accH[mi][0] + accL[mi][0];
-    pa[(2 * tq + 1) * kD + cA] = accH[mi][1] + accL[mi][1];
-    pa[(2 * tq) * kD + cB] = accH[mi][2] + accL[mi][2];
-    pa[(2 * tq + 1) * kD + cB] = accH[mi][3] + accL[mi][3];
-  }
+  if (warp < kDWarps) {
+    decoder_warp(a, sm, h, blk0, n_my, len, warp / (kDWarps / 2), warp % (kDWarps / 2), lane);
+  } else if (warp < kProducerWarp) {
+    tensor_warp(a, sm, n_my, part, warp - kMWarp0, lane);
+  } else if (lane == 0) {
+    producer_lane(a, sm, b, h, blk0, n_my);
   }
 
   // ---------------------------------------------------------------- split merge (final reduction)
   // The last CTA of a (sequence, kv-head) to finish merges the partials of all
   // its splits with a log-sum-exp; the counter goes back to zero for the next
-  // launch.  No CTA ever waits for another.  The merge is a short tail on the
-  // critical path, so it keeps many independent L2 loads in flight: one round
-  // for the per-head maxima, then every thread streams its share of the splits'
-  // accumulators (eight at a time) and the CTA adds the shares up in shared memory.
+  // launch.  No CTA ever waits for another.
   // Release/acquire through the counter: the barrier orders every thread's
   // partial stores before thread 0's acq_rel add, and the add orders the other
   // splits' stores before this CTA's loads (the barrier passes that on).
@@ -786,8 +914,8 @@ extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads
 // Allocation-free variant.  Some callers cannot hand the library a workspace
 // allocated at call time: a serving loop that has frozen its device memory
 // plan, a plugin whose host owns every allocation, or code that must not call
-// into an allocator on the decode path.  This entry point runs the same two
-// kernels with their split partials in a fixed scratch array that lives in the
+// into an allocator on the decode path.  This entry point runs the same kernel with
+// its split partials in a fixed scratch array that lives in the
 // library itself.
 constexpr size_t kStaticScratchBytes = GAAC_STATIC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_attn_scratch[kStaticScratchBytes];

@@ -1,10 +1,10 @@
-// Device-side building blocks of the GAAC library: tile format v1 constants,
+// Device-side building blocks of the GAAC library: tile format v2 constants,
 // the packed exponent decoder, status reporting, mbarrier and bulk-copy PTX.
 //
 // Method: "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference
 // on Personal Devices", section 3.1 (base-plus-offset exponent codes, 3-bit /
 // 4-bit / raw groups of eight, sign and mantissa verbatim) and Appendix D
-// (3-bit code plane, 2-bit tags, escape bytes).  The bit layout is format v1 as
+// (3-bit code plane, 2-bit tags, escape bytes).  The bit layout is format v2 as
 // declared in gaac.h.
 #pragma once
 
@@ -20,8 +20,10 @@ constexpr int kTile = 8192;
 constexpr int kOffCode = 8192;
 constexpr int kPlaneBytes = 1024;  // one code plane: 256 words
 constexpr int kOffTag = 11264;
-constexpr int kOffEsc = 11520;
-constexpr int kEscCap = 512;
+constexpr int kOffDir = 11520;  // escape directory: 8 x u16, entry w = escape bytes of eighths 0..w
+constexpr int kOffEsc = 11536;  // escape bytes
+constexpr int kEscCap = 496;
+constexpr int kDirUnits = 32;   // units per directory entry: an eighth = 128 groups = 1024 elements
 constexpr int kSlot = 12032;
 constexpr int kRawBytes = 16384;
 
@@ -240,6 +242,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait: gives up after `limit` polls and reports GAAC_ETIMEOUT.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
                                           uint32_t limit = (1u << 17)) {
+#pragma unroll 1
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   report(status, GAAC_ETIMEOUT);

@@ -88,12 +88,24 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
     const uint32_t tagbyte = slot[kOffTag + u];
     const uint32_t tword = tagw[u >> 2];
     const int esc_unit = word_prefix[u >> 2] + esc_count(tword & ((1u << (8 * (u & 3))) - 1u));
+    // The escape directory must hold the prefix at each quarter boundary and the total.
+    const uint16_t* dir = reinterpret_cast<const uint16_t*>(slot + kOffDir);
+    bool bad = false;
+    if ((u & (kDirUnits - 1)) == 0 && u > 0 && dir[u / kDirUnits - 1] != esc_unit) bad = true;
+    if (u == 255) {
+      const int total = esc_unit + esc_count(tagbyte);
+      if (dir[7] != total || total != ent.esc_len) bad = true;
+    }
     const uint4* smp = reinterpret_cast<const uint4*>(slot + 32 * u);
     const uint4 s0 = smp[0], s1 = smp[1];
-    const uint32_t smw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t smw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // signs back to their own bytes (stored one byte up, cyclically)
+      const uint32_t sg = smw[j] & 0x80808080u;
+      smw[j] = (smw[j] & 0x7F7F7F7Fu) | ((sg >> 8) | (sg << 24));
+    }
     const uint8_t* b3g = a.base3 + (kind * a.n_kv_heads + h) * kD;
     const uint8_t* b4g = a.base4 + (kind * a.n_kv_heads + h) * kD;
-    bool bad = false;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       uint32_t b3[4], b4[4];

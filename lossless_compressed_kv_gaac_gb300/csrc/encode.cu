@@ -29,7 +29,7 @@ struct EncShared {
   int ok;
 };
 
-// Channel of storage element s (format v1).
+// Channel of storage element s (format v2).
 __device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? (s & 127) : (s >> 6); }
 
 // Encodes the tile in sh->tile into `slot` (global, 16-byte aligned) unless its
@@ -134,7 +134,7 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
   const int off = before + incl - nesc;
   if (total > kEscCap || slot == nullptr) return -1;
 
-  // Code plane words of this unit (format v1 placement).
+  // Code plane words of this unit (format v2 placement).
   uint32_t W[3] = {0, 0, 0};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -145,6 +145,13 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
       W[h] |= (c0 | (c1 << 3) | ((c3 & 3u) << 6)) << (8 * L);
       W[2] |= ((c2 << (3 * h)) | (((c3 >> 2) & 1u) << (6 + h))) << (8 * L);
     }
+  }
+  // Sign|mantissa plane: each byte keeps its mantissa and takes the sign of the
+  // previous element of its aligned group of four (cyclically).
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t sg = smb[j] & 0x80808080u;
+    smb[j] = (smb[j] & 0x7F7F7F7Fu) | ((sg << 8) | (sg >> 24));
   }
   uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
   smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
@@ -158,7 +165,12 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int at = 2 * u + i;  // 0..511
-    if (at >= total) slot[kOffEsc + at] = 0;
+    if (at >= total && at < kEscCap) slot[kOffEsc + at] = 0;
+  }
+  if ((u & (kDirUnits - 1)) == kDirUnits - 1) {  // directory entry of eighth u / 32
+    const int w = u / kDirUnits, end = off + nesc;
+    slot[kOffDir + 2 * w] = static_cast<uint8_t>(end & 0xFF);
+    slot[kOffDir + 2 * w + 1] = static_cast<uint8_t>(end >> 8);
   }
   if (stats != nullptr) {
 #pragma unroll

@@ -26,8 +26,8 @@ _lib = None
 
 KIND_K, KIND_V = 0, 1
 D, BLOCK, TILE = 128, 64, 8192
-OFF_CODE, OFF_TAG, OFF_ESC = 8192, 11264, 11520
-ESC_CAP = 512
+OFF_CODE, OFF_TAG, OFF_DIR, OFF_ESC = 8192, 11264, 11520, 11536
+ESC_CAP = 496
 SLOT_BYTES = 12032
 
 
@@ -109,8 +109,9 @@ def calibrate(x) -> tuple[np.ndarray, np.ndarray]:
 
 
 def encode_tile(tile, kind: int, base3, base4, forced=None, esc_cap: int = ESC_CAP):
-    """Encode a [64][128] BF16 tile.  Returns (image uint8 [11520+esc_cap], esc_len);
-    esc_len is -1 when the escape stream would exceed esc_cap."""
+    """Encode a [64][128] BF16 tile.  Returns (image uint8 [11536+esc_cap], esc_len);
+    esc_len (escape bytes, the directory not counted) is -1 when the escape
+    stream would exceed esc_cap."""
     tile = _u16(tile).reshape(BLOCK, D)
     b3, b4 = _u8(base3).reshape(D), _u8(base4).reshape(D)
     img = np.zeros(OFF_ESC + esc_cap, np.uint8)

@@ -21,18 +21,24 @@
  *     then finalized.
  *   - Appendix D, Table 9 (Storage): 3-bit exponent codes, 2-bit mode tags,
  *     escape bytes, fixed-capacity escape slots.
- * The page gives no bit layout.  This file fixes one, "GAAC tile format v1",
+ * The page gives no bit layout.  This file fixes one, "GAAC tile format v2",
  * summarised below and spelled out rule by rule at the step that follows it.
  *
- * Format v1 in brief (all multi-byte fields little-endian):
+ * Format v2 in brief (all multi-byte fields little-endian):
  *   tile        64 tokens x 128 channels of one (sequence, block, kv-head, K|V)
  *   storage     K tiles: element (t,c) at s = t*128 + c   (token-major)
  *   order       V tiles: element (t,c) at s = c*64  + t   (channel-major)
  *   group       8 consecutive elements in storage order, G = s / 8
- *   slot image  [0,8192)      sign|mantissa byte per element, at s
+ *   eighth      128 consecutive groups (1024 elements), w = G / 128
+ *   slot image  [0,8192)      mantissa of element s in bits 0-6 of byte s; bit 7
+ *                             of byte s holds the sign of element
+ *                             4*(s/4) + (s+3)%4 (signs rotated by one byte
+ *                             inside each aligned group of four)
  *               [8192,11264)  code plane: 3 words per 32-element unit
  *               [11264,11520) tag plane: 2 bits per group
- *               [11520,12032) escape area, capacity 512 bytes, zero filled
+ *               [11520,11536) escape directory: 8 u16, entry w = escape bytes
+ *                             of eighths 0..w
+ *               [11536,12032) escape bytes, capacity 496, zero filled
  *   raw tile    8192 BF16 words in storage order
  */
 #include <math.h>
@@ -46,8 +52,10 @@
 #define ORC_UNITS 256           /* 32-element code units per tile */
 #define ORC_OFF_CODE 8192
 #define ORC_OFF_TAG 11264
-#define ORC_OFF_ESC 11520
-#define ORC_ESC_CAP 512
+#define ORC_OFF_DIR 11520          /* escape directory: 8 x u16 */
+#define ORC_OFF_ESC 11536          /* escape bytes */
+#define ORC_ESC_CAP 496
+#define ORC_DIR_GROUPS 128         /* groups per directory entry (an eighth of the tile) */
 #define ORC_SLOT 12032
 
 enum { ORC_KIND_K = 0, ORC_KIND_V = 1 };
@@ -59,6 +67,12 @@ static unsigned bf16_signmant(uint16_t x) { return ((x >> 8) & 0x80u) | (x & 0x7
 static uint16_t bf16_join(unsigned signmant, unsigned exponent) {
     return (uint16_t)(((signmant & 0x80u) << 8) | ((exponent & 0xFFu) << 7) | (signmant & 0x7Fu));
 }
+
+/* ---- sign|mantissa plane (format v2): byte s keeps the mantissa of element s
+ * and the sign of element sign_source(s), the previous element of the same
+ * aligned group of four, cyclically (byte 4i holds the sign of 4i+3). */
+static int sign_source(int s) { return 4 * (s / 4) + (s + 3) % 4; }
+static int sign_holder(int s) { return 4 * (s / 4) + (s + 1) % 4; }
 
 /* ---- storage order of a tile (format v1) */
 int gaac_ref_storage_index(int kind, int t, int c) {
@@ -166,9 +180,10 @@ int gaac_ref_escape_bytes_of_mode(int mode) { return escape_bytes_of_mode((unsig
  * Encode one full tile.  `tile` is the tile in logical order [64 tokens][128
  * channels]; b3/b4 are the 128 per-channel bases of this (kv-head, K|V).
  * `forced` (NULL or 1024 modes) overrides the mode rule, for tests only.
- * `img` receives the slot image; it must hold 11520 + img_esc_cap bytes.
- * Returns the escape length in bytes, or -1 if it exceeds img_esc_cap (the
- * image is then incomplete).  Unused escape bytes stay zero.
+ * `img` receives the slot image; it must hold 11536 + img_esc_cap bytes.
+ * Returns the escape length in bytes (escape bytes only, the directory not
+ * counted), or -1 if it exceeds img_esc_cap (the image is then incomplete).
+ * Unused escape bytes stay zero.
  */
 int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, const uint8_t* base4,
                          const uint8_t* forced, uint8_t* img, int img_esc_cap) {
@@ -177,7 +192,8 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
     for (int t = 0; t < ORC_BLOCK; ++t)
         for (int c = 0; c < ORC_D; ++c) seq[gaac_ref_storage_index(kind, t, c)] = tile[t * ORC_D + c];
 
-    for (int s = 0; s < ORC_TILE; ++s) img[s] = (uint8_t)bf16_signmant(seq[s]);
+    for (int s = 0; s < ORC_TILE; ++s)
+        img[s] = (uint8_t)((bf16_signmant(seq[s]) & 0x7Fu) | (bf16_signmant(seq[sign_source(s)]) & 0x80u));
 
     int esc = 0;
     for (int G = 0; G < ORC_GROUPS; ++G) {
@@ -209,6 +225,11 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
         if (esc + nb > img_esc_cap) return -1;
         for (int k = 0; k < nb; ++k) img[ORC_OFF_ESC + esc + k] = escb[k];
         esc += nb;
+        if ((G + 1) % ORC_DIR_GROUPS == 0) {  /* directory entry: escape bytes so far */
+            int w = G / ORC_DIR_GROUPS;
+            img[ORC_OFF_DIR + 2 * w] = (uint8_t)(esc & 0xFF);
+            img[ORC_OFF_DIR + 2 * w + 1] = (uint8_t)(esc >> 8);
+        }
     }
     return esc;
 }
@@ -216,7 +237,8 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
 /*
  * Decode one slot image into the logical tile [64][128].
  * Returns the number of escape bytes consumed, or -1 on a reserved tag (3),
- * or -2 if the escape stream would run past esc_limit bytes.
+ * -2 if the escape stream would run past esc_limit bytes, or -3 if a
+ * directory entry differs from the escape bytes of the eighths it covers.
  */
 int gaac_ref_decode_tile(const uint8_t* img, int kind, const uint8_t* base3, const uint8_t* base4,
                          int esc_limit, uint16_t* tile) {
@@ -242,9 +264,15 @@ int gaac_ref_decode_tile(const uint8_t* img, int kind, const uint8_t* base3, con
             }
             int t, cc;
             storage_to_tc(kind, s, &t, &cc);
-            tile[t * ORC_D + cc] = bf16_join(img[s], e);
+            unsigned sm = (img[s] & 0x7Fu) | (img[sign_holder(s)] & 0x80u);
+            tile[t * ORC_D + cc] = bf16_join(sm, e);
         }
         off += nb;
+        if ((G + 1) % ORC_DIR_GROUPS == 0) {
+            int w = G / ORC_DIR_GROUPS;
+            int dir = img[ORC_OFF_DIR + 2 * w] | (img[ORC_OFF_DIR + 2 * w + 1] << 8);
+            if (dir != off) return -3;
+        }
     }
     return off;
 }

@@ -64,7 +64,7 @@ def _golden_tile(case):
 
 
 def test_golden_format_examples(orc):
-    cases = json.load(open(os.path.join(HERE, "golden", "format_v1_examples.json")))["cases"]
+    cases = json.load(open(os.path.join(HERE, "golden", "format_v2_examples.json")))["cases"]
     for case in cases:
         tile = _golden_tile(case)
         b3 = np.full(128, case["base3"], np.uint8)
@@ -82,7 +82,7 @@ def test_golden_format_examples(orc):
 
 
 def test_storage_order_pins(orc):
-    """K tiles are token-major, V tiles channel-major (format v1)."""
+    """K tiles are token-major, V tiles channel-major (format v2)."""
     assert orc.storage_index(0, 5, 3) == 5 * 128 + 3
     assert orc.storage_index(1, 5, 3) == 3 * 64 + 5
     tile = np.arange(8192, dtype=np.uint16).reshape(64, 128)
@@ -146,7 +146,7 @@ def test_mode_minimality_brute_force(orc, kind):
 
 
 def test_capacity_overflow_reported(orc):
-    """A tile whose escape stream exceeds the 512-byte area is reported (-1): it must stay BF16."""
+    """A tile whose escape stream exceeds the 496-byte area is reported (-1): it must stay BF16."""
     rng = np.random.default_rng(5)
     tile = rng.integers(0, 65536, (64, 128)).astype(np.uint16)
     b3 = np.full(128, 124, np.uint8)
@@ -154,7 +154,78 @@ def test_capacity_overflow_reported(orc):
     img, esc = orc.encode_tile(tile, 0, b3, b4)
     assert esc == -1
     img, esc = orc.encode_tile(tile, 0, b3, b4, esc_cap=FULL_CAP)
-    assert esc > 512
+    assert esc > 496
+
+
+def test_capacity_edge(orc):
+    """496 escape bytes fit, 497 do not: 496 4-bit groups fill the area exactly."""
+    b3 = np.full(128, 124, np.uint8)
+    b4 = np.full(128, 120, np.uint8)
+    tile = np.full((64, 128), 16256, np.uint16)  # 1.0: exponent 127, 3-bit mode
+    flat = tile.reshape(-1)  # K storage order is token-major = logical order
+    for n_wide, expect in ((496, 496), (497, -1)):
+        t = flat.copy()
+        t[8 * np.arange(n_wide)] = 135 << 7  # exponent 135: outside [124,131], inside [120,135]
+        img, esc = orc.encode_tile(t.reshape(64, 128), 0, b3, b4)
+        assert esc == expect
+
+
+def _tags(img):
+    return np.array([(int(img[11264 + g // 4]) >> (2 * (g % 4))) & 3 for g in range(1024)])
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_escape_directory_is_the_eighth_prefix(orc, kind):
+    """Directory entry w = escape bytes of groups [0, 128(w+1)), read back from the tag plane
+    with the stream-size rule (0, 1, 5 bytes per mode); the escape bytes start at 11536."""
+    rng = np.random.default_rng(77 + kind)
+    for trial in range(6):
+        b3 = rng.integers(100, 130, 128).astype(np.uint8)
+        b4 = (b3.astype(int) - rng.integers(0, 8, 128)).clip(0, 240).astype(np.uint8)
+        e = b3[None, :].astype(int) + rng.integers(-3, 12, (64, 128))
+        e = np.where(rng.random((64, 128)) < 0.002, rng.integers(0, 255, (64, 128)), e).clip(0, 254)
+        tile = ((rng.integers(0, 2, (64, 128)) << 15) | (e << 7) | rng.integers(0, 128, (64, 128))).astype(np.uint16)
+        img, esc = orc.encode_tile(tile, kind, b3, b4, esc_cap=FULL_CAP)
+        assert esc >= 0
+        per = np.array([0, 1, 5, 0])[_tags(img)]
+        want = np.cumsum(per.reshape(8, 128).sum(axis=1))
+        got = img[11520:11536].view("<u2")
+        np.testing.assert_array_equal(got, want)
+        assert want[7] == esc
+        dec, st = orc.decode_tile(img, kind, b3, b4, esc_limit=esc)
+        assert st == esc
+        np.testing.assert_array_equal(dec, tile)
+
+
+def test_corrupt_directory_rejected(orc):
+    tile = np.full((64, 128), 16256, np.uint16)
+    tile[20, 0] = 135 << 7  # one 4-bit group in eighth 2 (tokens 16-23)
+    b3 = np.full(128, 124, np.uint8)
+    b4 = np.full(128, 120, np.uint8)
+    img, esc = orc.encode_tile(tile, 0, b3, b4)
+    assert esc == 1
+    assert list(img[11520:11536]) == [0, 0, 0, 0, 1, 0, 1, 0, 1, 0, 1, 0, 1, 0, 1, 0]
+    bad = img.copy()
+    bad[11520] = 1  # claims eighth 0 holds one escape byte
+    _, st = orc.decode_tile(bad, 0, b3, b4, esc)
+    assert st == -3
+
+
+def test_sign_rotation_pins(orc):
+    """Byte s of the sign|mantissa plane carries the mantissa of element s and the sign of
+    element 4(s/4) + (s+3)%4: a single negative element at s sets bit 7 of byte 4(s/4) + (s+1)%4."""
+    b = np.full(128, 124, np.uint8)
+    for kind in (0, 1):
+        for s in (0, 1, 2, 3, 4101, 8191):
+            tile = np.full((64, 128), 16256, np.uint16)
+            t, c = (s // 128, s % 128) if kind == 0 else (s % 64, s // 64)
+            tile[t, c] = 0xBF80 | 0x2D  # -1.0 with mantissa 0x2D
+            img, esc = orc.encode_tile(tile, kind, b, b)
+            holder = 4 * (s // 4) + (s + 1) % 4
+            expect = np.zeros(8192, np.uint8)
+            expect[s] |= 0x2D
+            expect[holder] |= 0x80
+            np.testing.assert_array_equal(img[:8192], expect)
 
 
 def test_reserved_tag_rejected(orc):
