@@ -45,7 +45,9 @@
 namespace gaac {
 
 constexpr int kDWarps = 16;                      // decoders: 0-7 K eighths, 8-15 V eighths
-constexpr int kMWarps = 2;                       // tensor-core warps (alternate blocks)
+constexpr int kMGroupWarps = 4;                  // a tensor-core group: one 16-token / 32-channel share per warp
+constexpr int kMGroups = 1;                      // groups take alternate blocks
+constexpr int kMWarps = kMGroupWarps * kMGroups;
 constexpr int kMWarp0 = kDWarps;
 constexpr int kProducerWarp = kDWarps + kMWarps;
 constexpr int kAttThreads = (kProducerWarp + 1) * 32;
@@ -56,7 +58,8 @@ constexpr int kRPad = 8;                         // query heads per kv-head in t
 constexpr int kPtStride = 72;                    // bf16 per head row of P^T (64 tokens + pad): 144 B
 constexpr int kQStride = 136;                    // bf16 per head row of q (128 channels + pad): 272 B
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
-constexpr int kBarM = 1;                         // named barrier of the two tensor-core warps
+constexpr int kBarM = 1;                         // named barriers 1, 2: one per tensor-core group
+constexpr int kBarMAll = kBarM + kMGroups;       // all tensor-core warps (end of the split)
 constexpr uint32_t kJoinMask = 0x807F807Fu;      // sign and mantissa bits of a bf16x2 word
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -68,12 +71,14 @@ struct AttSmem {
   alignas(128) uint8_t stage[kStages][2][kRawBytes];  // K, V tile images
   alignas(128) uint8_t decK[kDecBufs][kTile * 2];      // BF16 K, rows = tokens (256 B), swizzled
   alignas(128) uint8_t decV[kDecBufs][kTile * 2];      // BF16 V, rows = channels (128 B), swizzled
-  alignas(16) uint16_t pt[kMWarps][2][kRPad][kPtStride];  // P^T hi, lo of each tensor-core warp
-  alignas(16) uint16_t qs[kRPad][kQStride];               // q * 2^-4, channels in decoded order
-  alignas(16) float xacc[kRPad][kD];                      // tensor-core warp 1's acc at the end
-  float xm[kRPad], xl[kRPad];
+  alignas(16) uint16_t pt[kMGroups][2][kRPad][kPtStride];  // per group: P^T hi, lo of its current block
+  alignas(16) uint16_t qs[kRPad][kQStride];                 // q * 2^-4, channels in decoded order
+  alignas(16) float wmax[kMGroups][kRPad][kMGroupWarps];    // per head: max of each warp's 16 scores
+  alignas(16) float wl[kMGroups][kRPad][kMGroupWarps];      // per head: row sums of each warp (at the end)
+  alignas(16) float xacc[kRPad][kD];                        // group 1's accumulators (at the end)
+  float xm[kRPad];                                          // group 1's running maxima (at the end)
   uint2 lut[256];       // escape byte -> bit 3 spread into the byte lanes of two exponent words
-  uint32_t sel[256];    // tag byte -> byte permute that gathers a unit's 4-bit escape bytes
+  uint32_t tagl[256];   // tag byte -> gather selector (bits 0-15), escape bytes (16-23), needs a patch (24)
   StageMeta smeta[kStages];
   int dec_nv[kDecBufs];                   // tokens of the block in decoded buffer d
   alignas(8) uint8_t dec_bad[kDecBufs][8];  // K eighth failed its checks
@@ -169,28 +174,36 @@ __device__ __forceinline__ uint32_t vswz(int ch, int c) { return static_cast<uin
 // Rotating the exponents left by 7 puts elements 0 and 2 in their bf16 fields
 // and elements 1 and 3 in the fields of the same word rotated by one byte.
 __device__ __forceinline__ void join_v2(uint32_t w, uint32_t e, uint32_t& p02, uint32_t& p13) {
-  const uint32_t r = __funnelshift_l(e, e, 7);
-  p02 = (w & kJoinMask) | (r & ~kJoinMask);
-  const uint32_t t = (w & ~kJoinMask) | (r & kJoinMask);
+  uint32_t r, t;
+  asm("shf.l.wrap.b32 %0, %1, %1, 7;" : "=r"(r) : "r"(e));
+  // lop3 0xE4: c ? a : b per bit, with c = kJoinMask (the sign and mantissa bits of a bf16x2 word)
+  asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(p02) : "r"(w), "r"(r), "n"(kJoinMask));  // sign|mantissa from w
+  asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(t) : "r"(r), "r"(w), "n"(kJoinMask));    // rotated frame
   p13 = __byte_perm(t, t, 0x0321);
 }
 
-// Byte permute selector that gathers the escape bytes of a unit's 4-bit
-// groups from the four escape bytes at the unit's offset: byte j of the result
-// is group j's escape byte if group j is 4-bit and no raw group precedes it in
-// the unit, else 0 (those groups are patched separately).
-__device__ __forceinline__ uint32_t gather_selector(uint32_t tb) {
-  uint32_t s = 0, rank = 0;
-  bool raw = false;
+// Everything the decoders need from a unit's tag byte (4 groups x 2 bits):
+//  bits 0-15: byte permute selector that gathers the escape bytes of the
+//    unit's 4-bit groups from the four escape bytes at the unit's offset (byte
+//    j = group j's escape byte if group j is 4-bit and no raw group precedes it
+//    in the unit, else a zero byte; the others are patched separately);
+//  bits 16-23: the unit's escape bytes (1 per 4-bit group, 5 per raw group),
+//    255 if a group has the reserved tag 3 (the quarter's total check fails);
+//  bit 24: the unit has a raw group (patch_unit must run).
+__device__ __forceinline__ uint32_t tag_entry(uint32_t tb) {
+  uint32_t s = 0, rank = 0, bytes = 0;
+  bool raw = false, reserved = false;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t t = (tb >> (2 * j)) & 3u;
+    if (t == 3u) reserved = true;
     if (t >= 2u) raw = true;
     const uint32_t nib = (t == 1u && !raw) ? rank : 4u;  // 4: a zero byte of the second operand
     if (t == 1u) ++rank;
+    bytes += t == 1u ? 1u : (t == 2u ? 5u : 0u);
     s |= nib << (4 * j);
   }
-  return s;
+  return s | ((reserved ? 255u : bytes) << 16) | (raw ? (1u << 24) : 0u);
 }
 
 // The four escape bytes starting at escape offset `off` of a slot image.
@@ -268,8 +281,8 @@ __device__ __noinline__ void clear_tail(uint8_t* dec, int u, int nv) {
 // exponent bits 3..7 are five escape bit planes) and 4-bit groups placed after
 // a raw group.  off: the unit's first escape byte.  Rewrites those groups'
 // 16-byte chunks in the decoded tile.
-__device__ __noinline__ void patch_unit(const uint8_t* img, int kind, int u, uint32_t tb, int off, const uint8_t* b4g,
-                                        const uint2* lut, uint8_t* dec) {
+__device__ __forceinline__ void patch_unit(const uint8_t* img, int kind, int u, uint32_t tb, int off,
+                                           const uint8_t* b4g, const uint2* lut, uint8_t* dec) {
   uint32_t fix = 0;
   bool raw = false;
 #pragma unroll
@@ -376,31 +389,31 @@ __device__ __forceinline__ void decoder_warp(const AttnArgs& a, AttSmem& sm, int
     uint8_t* dec = kind ? sm.decV[db] : sm.decK[db];
     const bool slot = mode == GAAC_MODE_SLOT;
     bool bad = !slot && mode != GAAC_MODE_RAW;
-    uint32_t tb = 0;
+    uint32_t tb = 0, te = 0;  // tag byte and its tag_entry word
     int off = 0;
     if (slot) {
       const uint16_t* dir = reinterpret_cast<const uint16_t*>(img + kOffDir);
       const int start = e8 ? dir[e8 - 1] : 0, end = dir[e8];
       tb = img[kOffTag + u];
-      const int cnt = esc_count(tb);
+      te = sm.tagl[tb];
+      const int cnt = (te >> 16) & 0xFF;
       const int incl = warp_incl_scan(cnt, lane);
       off = start + incl - cnt;  // escape bytes are in unit order
-      bad = __any_sync(kFull, ((tb & (tb >> 1)) & 0x55u) != 0u) || start > end || end > esc_len ||
-            start + __shfl_sync(kFull, incl, 31) != end;
+      bad = start > end || end > esc_len || start + __shfl_sync(kFull, incl, 31) != end;
       if (bad && lane == 0) report(a.status, GAAC_EFORMAT);
     }
     // Every escape offset used below lies inside [start, end) and end <= 496.
     uint32_t o[16];
-    if (bad) {  // no valid data: zeros (K blocks are also masked by the tensor-core warp)
+    if (bad) {  // no valid data: zeros (K blocks are also masked by the tensor-core warps)
 #pragma unroll
       for (int i = 0; i < 16; ++i) o[i] = 0u;
     } else if (slot) {
-      decode_unit(img, u, tb, __byte_perm(escape_window(img, off), 0u, sm.sel[tb]), b3, d43, sm.lut, o);
+      decode_unit(img, u, tb, __byte_perm(escape_window(img, off), 0u, te & 0xFFFFu), b3, d43, sm.lut, o);
     } else {
       raw_unit(img, u, o);
     }
     store_unit(dec, c0, c1, c2, c3, o);
-    if (slot && !bad && (tb & 0xAAu)) patch_unit(img, kind, u, tb, off, b4g, sm.lut, dec);
+    if (slot && !bad && (te >> 24)) patch_unit(img, kind, u, tb, off, b4g, sm.lut, dec);  // raw groups: rare
     if (kind == 1 && nv < kBlock) clear_tail(dec, u, nv);
     if (kind == 0 && lane == 0) {
       sm.dec_bad[db][e8] = bad ? 1 : 0;
@@ -473,79 +486,90 @@ __device__ __forceinline__ void producer_lane(const AttnArgs& a, AttSmem& sm, in
 
 // ------------------------------------------------------------- tensor cores
 
-__device__ __forceinline__ void tensor_warp(const AttnArgs& a, AttSmem& sm, int n_my, float* part, int mw, int lane) {
+// A tensor-core group of four warps shares each of its blocks (group gr takes
+// blocks gr, gr+2, ...): warp w scores tokens [16w, 16w+16) (QK^T) and
+// accumulates channels [32w, 32w+32) (PV^T).  The block maximum per head goes
+// through shared memory, so the group's warps keep the same running maximum;
+// the two groups' partials are merged when the split ends.
+__device__ __forceinline__ void tensor_warp(const AttnArgs& a, AttSmem& sm, int n_my, float* part, int gr, int w,
+                                            int lane) {
   const int g = lane >> 2, tq = lane & 3;
   // ldmatrix row of this lane inside a 16-row tile: matrix m = lane/8 covers rows 8(m%2).., columns 8(m/2)..
   const int lrow = ((lane >> 3) & 1) * 8 + (lane & 7);
   const int lcol = lane >> 4;
-  const int ktok = quad_perm(lrow);  // QK^T rows follow the decoded token order of V
-  float acc[8][4];
+  const int tg = quad_perm(g);
+  float acc[2][4];  // channel tiles 2w, 2w+1
 #pragma unroll
-  for (int ct = 0; ct < 8; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
+  for (int ct = 0; ct < 2; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2tq, 2tq+1 (log2 domain)
-  const uint32_t pth = smem_addr(&sm.pt[mw][0][0][0]), ptl = smem_addr(&sm.pt[mw][1][0][0]);
-  const uint32_t qsa = smem_addr(&sm.qs[lane & 7][0]) + 16u * (lane >> 3);  // q rows as B: chunk lane/8
-  const int prow = lane & 7, pm = lane >> 3;
-  // P^T as B: matrices (hi k0-7, hi k8-15, lo k0-7, lo k8-15) of one k-step
-  const uint32_t pba = ((lane >> 4) ? ptl : pth) + static_cast<uint32_t>(prow * kPtStride * 2 + 16 * ((lane >> 3) & 1));
+  // q as the B operand of QK^T: two k-steps per ldmatrix (chunk lane/8 of the head row lane%8)
+  uint32_t qf[16];
+  {
+    const uint32_t qsa = smem_addr(&sm.qs[lane & 7][0]) + 16u * (lane >> 3);
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) ldsm_x4(qsa + 64u * k2, qf[4 * k2], qf[4 * k2 + 1], qf[4 * k2 + 2], qf[4 * k2 + 3]);
+  }
+  const uint32_t pth = smem_addr(&sm.pt[gr][0][0][0]);
+  // P^T store: matrices (hi rows 0-7, hi rows 8-15, lo rows 0-7, lo rows 8-15) of this warp's 16 positions
+  const uint32_t pst = pth + static_cast<uint32_t>((lane >> 4) * kRPad * kPtStride * 2 + (lane & 7) * kPtStride * 2 +
+                                                   (2 * w + ((lane >> 3) & 1)) * 16);
+  // P^T as B of one k-step: matrices (hi k0-7, hi k8-15, lo k0-7, lo k8-15)
+  const uint32_t pba = pth + static_cast<uint32_t>((lane >> 4) * kRPad * kPtStride * 2 + (lane & 7) * kPtStride * 2 +
+                                                   16 * ((lane >> 3) & 1));
+  uint32_t koff[8], voff[8];  // swizzled ldmatrix offsets: K row 16w + quad_perm(lrow) per k-step; V rows per (k-step, tile)
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) koff[ks] = kswz(16 * w + quad_perm(lrow), 2 * ks + lcol);  // rows follow V's token order
+#pragma unroll
+  for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) voff[2 * kt + ct] = vswz(32 * w + 16 * ct + lrow, 2 * kt + lcol);
 
 #pragma unroll 1
-  for (int j = mw; j < n_my; j += kMWarps) {
+  for (int j = gr; j < n_my; j += kMGroups) {
     const int db = j % kDecBufs;
     const uint32_t par = (j / kDecBufs) & 1;
     mbar_wait(&sm.dkFull[db], par, a.status);
     const int nv = sm.dec_nv[db];
-    const uint2 badw = *reinterpret_cast<const uint2*>(sm.dec_bad[db]);
+    const uint2 badw = *reinterpret_cast<const uint2*>(sm.dec_bad[db]);  // one byte per K eighth
     const bool kbad = (badw.x | badw.y) != 0u;
-    // ---- S = K q^T: 4 row tiles of 16 tokens, 8 k-steps of 16 channels
-    float s[4][4];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+    // ---- S = K q^T for tokens 16w..16w+15: 8 k-steps in two accumulation chains
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t kb = smem_addr(sm.decK[db]);
 #pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {  // two k-steps per q load
-      uint32_t q0, q1, q2, q3;
-      ldsm_x4(qsa + 64u * k2, q0, q1, q2, q3);
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int ks = 2 * k2 + kk;
-        const uint32_t ka = kb + kswz(ktok, 2 * ks + lcol);  // row 16mt + ktok keeps the row's swizzle
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(ka + 4096u * mt, a0, a1, a2, a3);
-          mma_bf16(s[mt], a0, a1, a2, a3, kk ? q2 : q0, kk ? q3 : q1);
-        }
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kb + koff[ks], a0, a1, a2, a3);
+      mma_bf16(ks & 1 ? sb : sa, a0, a1, a2, a3, qf[2 * ks], qf[2 * ks + 1]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.dkEmpty[db]);
-    // ---- online softmax (rows g and g+8 of each tile: tokens 16mt + quad_perm(g) (+8))
-    const int tg = quad_perm(g);
-    float x0 = -INFINITY, x1 = -INFINITY;
+    const bool ok0 = !kbad && 16 * w + tg < nv, ok1 = !kbad && 16 * w + 8 + tg < nv;
+    float s0 = ok0 ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
+    float s1 = ok0 ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
+    float s2 = ok1 ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
+    float s3 = ok1 ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
+    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const bool ok0 = !kbad && 16 * mt + tg < nv, ok1 = !kbad && 16 * mt + 8 + tg < nv;
-      s[mt][0] = ok0 ? s[mt][0] * a.scale_log2 : -INFINITY;
-      s[mt][1] = ok0 ? s[mt][1] * a.scale_log2 : -INFINITY;
-      s[mt][2] = ok1 ? s[mt][2] * a.scale_log2 : -INFINITY;
-      s[mt][3] = ok1 ? s[mt][3] * a.scale_log2 : -INFINITY;
-      x0 = fmaxf(x0, fmaxf(s[mt][0], s[mt][2]));
-      x1 = fmaxf(x1, fmaxf(s[mt][1], s[mt][3]));
+    for (int d = 4; d < 32; d <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, d));
+      x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, d));
     }
-    if (__any_sync(kFull, x0 > m0 || x1 > m1)) {  // a running maximum rises: rescale (rare after the first blocks)
-#pragma unroll
-      for (int d = 4; d < 32; d <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, d));
-        x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, d));
-      }
-      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    if (g == 0) {
+      sm.wmax[gr][2 * tq][w] = x0;
+      sm.wmax[gr][2 * tq + 1][w] = x1;
+    }
+    named_bar_sync(kBarM + gr, kMGroupWarps * 32);  // block maxima of the group's warps written
+    const float4 ma = *reinterpret_cast<const float4*>(&sm.wmax[gr][2 * tq][0]);
+    const float4 mb = *reinterpret_cast<const float4*>(&sm.wmax[gr][2 * tq + 1][0]);
+    const float n0 = fmaxf(m0, fmaxf(fmaxf(ma.x, ma.y), fmaxf(ma.z, ma.w)));
+    const float n1 = fmaxf(m1, fmaxf(fmaxf(mb.x, mb.y), fmaxf(mb.z, mb.w)));
+    if (n0 != m0 || n1 != m1) {  // a running maximum rises: rescale (rare after the first blocks)
       const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
       const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
       l0 *= al0;
       l1 *= al1;
 #pragma unroll
-      for (int ct = 0; ct < 8; ++ct) {
+      for (int ct = 0; ct < 2; ++ct) {
         acc[ct][0] *= al0;
         acc[ct][1] *= al1;
         acc[ct][2] *= al0;
@@ -554,40 +578,28 @@ __device__ __forceinline__ void tensor_warp(const AttnArgs& a, AttSmem& sm, int 
       m0 = n0;
       m1 = n1;
     }
-    uint32_t ph[4][2], pl[4][2];  // [tile][row half]: bf16x2 of heads (2tq, 2tq+1)
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const float p0 = m0 == -INFINITY ? 0.f : fast_exp2(s[mt][2 * hf] - m0);
-        const float p1 = m1 == -INFINITY ? 0.f : fast_exp2(s[mt][2 * hf + 1] - m1);
-        l0 += p0;
-        l1 += p1;
-        const uint32_t hi = pack_bf16x2(p0, p1);
-        ph[mt][hf] = hi;
-        pl[mt][hf] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
-      }
-    }
-    // P^T[head][position]: matrix k of a store covers positions 8(4i + k)..+7 (tile 2i + k/2, row half k%2)
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t off = static_cast<uint32_t>(prow * kPtStride * 2 + (4 * i + pm) * 16);
-      stsm_x4_trans(pth + off, ph[2 * i][0], ph[2 * i][1], ph[2 * i + 1][0], ph[2 * i + 1][1]);
-      stsm_x4_trans(ptl + off, pl[2 * i][0], pl[2 * i][1], pl[2 * i + 1][0], pl[2 * i + 1][1]);
-    }
-    __syncwarp();
-    // ---- acc += V^T P: 8 row tiles of 16 channels, 4 k-steps of 16 tokens
+    const float p0 = m0 == -INFINITY ? 0.f : fast_exp2(s0 - m0);
+    const float p1 = m1 == -INFINITY ? 0.f : fast_exp2(s1 - m1);
+    const float p2 = m0 == -INFINITY ? 0.f : fast_exp2(s2 - m0);
+    const float p3 = m1 == -INFINITY ? 0.f : fast_exp2(s3 - m1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+    const uint32_t r01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
+    const uint32_t r23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
+    stsm_x4_trans(pst, h01, h23, r01, r23);  // P^T[head][16w + row]
+    named_bar_sync(kBarM + gr, kMGroupWarps * 32);  // P^T of the block complete
+    // ---- acc += V^T P for channels 32w..32w+31: 4 k-steps of 16 tokens
     mbar_wait(&sm.dvFull[db], par, a.status);
     const uint32_t vb = smem_addr(sm.decV[db]);
 #pragma unroll
     for (int kt = 0; kt < 4; ++kt) {
       uint32_t bh0, bh1, bl0, bl1;
       ldsm_x4(pba + 32u * kt, bh0, bh1, bl0, bl1);
-      const uint32_t va = vb + vswz(lrow, 2 * kt + lcol);  // row 16ct + lrow keeps the row's swizzle
 #pragma unroll
-      for (int ct = 0; ct < 8; ++ct) {
+      for (int ct = 0; ct < 2; ++ct) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(va + 2048u * ct, a0, a1, a2, a3);
+        ldsm_x4(vb + voff[2 * kt + ct], a0, a1, a2, a3);
         mma_bf16(acc[ct], a0, a1, a2, a3, bh0, bh1);
         mma_bf16(acc[ct], a0, a1, a2, a3, bl0, bl1);
       }
@@ -595,52 +607,75 @@ __device__ __forceinline__ void tensor_warp(const AttnArgs& a, AttSmem& sm, int 
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.dvEmpty[db]);
   }
-  // ---- row sums over the 8 lanes of each head pair, then merge the two warps
+  // ---- the split's partial: l summed over lanes and warps; group 1 hands (m, l, acc) to group 0, which
+  // merges the two with a log-sum-exp and writes the partial
 #pragma unroll
   for (int d = 4; d < 32; d <<= 1) {
     l0 += __shfl_xor_sync(kFull, l0, d);
     l1 += __shfl_xor_sync(kFull, l1, d);
   }
-  if (mw == 1) {
-    if (g == 0) {
+  if (g == 0) {
+    sm.wl[gr][2 * tq][w] = l0;
+    sm.wl[gr][2 * tq + 1][w] = l1;
+  }
+  if (gr == kMGroups - 1 && gr > 0) {
+    if (w == 0 && g == 0) {
       sm.xm[2 * tq] = m0;
       sm.xm[2 * tq + 1] = m1;
-      sm.xl[2 * tq] = l0;
-      sm.xl[2 * tq + 1] = l1;
     }
 #pragma unroll
-    for (int ct = 0; ct < 8; ++ct) {
-      sm.xacc[2 * tq][16 * ct + g] = acc[ct][0];
-      sm.xacc[2 * tq + 1][16 * ct + g] = acc[ct][1];
-      sm.xacc[2 * tq][16 * ct + g + 8] = acc[ct][2];
-      sm.xacc[2 * tq + 1][16 * ct + g + 8] = acc[ct][3];
+    for (int ct = 0; ct < 2; ++ct) {
+      const int cA = 32 * w + 16 * ct + g, cB = cA + 8;
+      sm.xacc[2 * tq][cA] = acc[ct][0];
+      sm.xacc[2 * tq + 1][cA] = acc[ct][1];
+      sm.xacc[2 * tq][cB] = acc[ct][2];
+      sm.xacc[2 * tq + 1][cB] = acc[ct][3];
     }
   }
-  named_bar_sync(kBarM, kMWarps * 32);
-  if (mw == 0) {
-    float w[2][2], mm[2];  // [head i][own, other]
+  named_bar_sync(kBarMAll, kMWarps * 32);
+  if (gr != 0) return;
+  float wt[2][2];  // [head 2tq + i][own group, group 1]
+  float mm[2], ll[2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float mo = i ? m1 : m0, mx = sm.xm[2 * tq + i];
+  for (int i = 0; i < 2; ++i) {
+    const float4 la = *reinterpret_cast<const float4*>(&sm.wl[0][2 * tq + i][0]);
+    const float lown = (la.x + la.y) + (la.z + la.w);
+    const float mo = i ? m1 : m0;
+    if (kMGroups > 1) {
+      const float mx = sm.xm[2 * tq + i];
       const float M = fmaxf(mo, mx);
       mm[i] = M;
-      w[i][0] = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
-      w[i][1] = mx == -INFINITY ? 0.f : fast_exp2(mx - M);
+      wt[i][0] = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
+      wt[i][1] = mx == -INFINITY ? 0.f : fast_exp2(mx - M);
+      const float4 lb = *reinterpret_cast<const float4*>(&sm.wl[kMGroups - 1][2 * tq + i][0]);
+      ll[i] = wt[i][0] * lown + wt[i][1] * ((lb.x + lb.y) + (lb.z + lb.w));
+    } else {
+      mm[i] = mo;
+      wt[i][0] = 1.f;
+      wt[i][1] = 0.f;
+      ll[i] = lown;
     }
-    if (g == 0) {
-      part[4 * tq + 0] = mm[0];
-      part[4 * tq + 1] = w[0][0] * l0 + w[0][1] * sm.xl[2 * tq];
-      part[4 * tq + 2] = mm[1];
-      part[4 * tq + 3] = w[1][0] * l1 + w[1][1] * sm.xl[2 * tq + 1];
-    }
-    float* pa = part + 2 * kRPad;
+  }
+  if (w == 0 && g == 0) {
+    part[4 * tq + 0] = mm[0];
+    part[4 * tq + 1] = ll[0];
+    part[4 * tq + 2] = mm[1];
+    part[4 * tq + 3] = ll[1];
+  }
+  float* pa = part + 2 * kRPad;
 #pragma unroll
-    for (int ct = 0; ct < 8; ++ct) {
-      const int cA = 16 * ct + g, cB = cA + 8;
-      pa[(2 * tq) * kD + cA] = w[0][0] * acc[ct][0] + w[0][1] * sm.xacc[2 * tq][cA];
-      pa[(2 * tq + 1) * kD + cA] = w[1][0] * acc[ct][1] + w[1][1] * sm.xacc[2 * tq + 1][cA];
-      pa[(2 * tq) * kD + cB] = w[0][0] * acc[ct][2] + w[0][1] * sm.xacc[2 * tq][cB];
-      pa[(2 * tq + 1) * kD + cB] = w[1][0] * acc[ct][3] + w[1][1] * sm.xacc[2 * tq + 1][cB];
+  for (int ct = 0; ct < 2; ++ct) {
+    const int cA = 32 * w + 16 * ct + g, cB = cA + 8;
+    if (kMGroups > 1) {
+      pa[(2 * tq) * kD + cA] = wt[0][0] * acc[ct][0] + wt[0][1] * sm.xacc[2 * tq][cA];
+      pa[(2 * tq + 1) * kD + cA] = wt[1][0] * acc[ct][1] + wt[1][1] * sm.xacc[2 * tq + 1][cA];
+      pa[(2 * tq) * kD + cB] = wt[0][0] * acc[ct][2] + wt[0][1] * sm.xacc[2 * tq][cB];
+      pa[(2 * tq + 1) * kD + cB] = wt[1][0] * acc[ct][3] + wt[1][1] * sm.xacc[2 * tq + 1][cB];
+    } else {
+      pa[(2 * tq) * kD + cA] = acc[ct][0];
+      pa[(2 * tq + 1) * kD + cA] = acc[ct][1];
+      pa[(2 * tq) * kD + cB] = acc[ct][2];
+      pa[(2 * tq + 1) * kD + cB] = acc[ct][3];
     }
   }
 }
@@ -758,7 +793,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
 
   for (int x = tid; x < 256; x += kAttThreads) {
     sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
-    sm.sel[x] = gather_selector(static_cast<uint32_t>(x));
+    sm.tagl[x] = tag_entry(static_cast<uint32_t>(x));
   }
   // q of the kv-head's query heads, times 2^-4, channels in decoded order (the B operand of QK^T)
   for (int x = tid; x < kRPad * kD / 2; x += kAttThreads) {
@@ -780,8 +815,8 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     for (int d = 0; d < kDecBufs; ++d) {
       mbar_init(&sm.dkFull[d], kDWarps / 2);
       mbar_init(&sm.dvFull[d], kDWarps / 2);
-      mbar_init(&sm.dkEmpty[d], 1);
-      mbar_init(&sm.dvEmpty[d], 1);
+      mbar_init(&sm.dkEmpty[d], kMGroupWarps);
+      mbar_init(&sm.dvEmpty[d], kMGroupWarps);
     }
     fence_mbar_init();
   }
@@ -792,7 +827,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   if (warp < kDWarps) {
     decoder_warp(a, sm, h, blk0, n_my, len, warp / (kDWarps / 2), warp % (kDWarps / 2), lane);
   } else if (warp < kProducerWarp) {
-    tensor_warp(a, sm, n_my, part, warp - kMWarp0, lane);
+    tensor_warp(a, sm, n_my, part, (warp - kMWarp0) / kMGroupWarps, (warp - kMWarp0) % kMGroupWarps, lane);
   } else if (lane == 0) {
     producer_lane(a, sm, b, h, blk0, n_my);
   }
