@@ -236,7 +236,7 @@ __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t 
     for (int q = 0; q < 4; ++q) {
       const uint32_t f = q < 2 ? fa : fb;
       const uint32_t s = q == 0 ? sa.x : (q == 1 ? sa.y : (q == 2 ? sb.x : sb.y));
-      e[q] = (b3[4 * hh + q] + c[q] + s) + f * d43[4 * hh + q];
+      e[q] = (f ? b3[4 * hh + q] + d43[4 * hh + q] : b3[4 * hh + q]) + c[q] + s;  // base4 = base3 + d43
     }
     const uint4 sm = hh ? s1 : s0;
     join_v2(sm.x, e[0], o[8 * hh + 0], o[8 * hh + 1]);
