@@ -378,41 +378,47 @@ __device__ __forceinline__ void decoder_warp(const AttnArgs& a, AttSmem& sm, int
                  c3 = unit_chunk(kind, u, 3);
   uint64_t* dec_full = kind ? sm.dvFull : sm.dkFull;
   uint64_t* dec_empty = kind ? sm.dvEmpty : sm.dkEmpty;
+  int st = 0, db = 0;
+  uint32_t sph = 0u, dph = 0u;  // parity of the current lap of the staging ring / decoded buffers
 #pragma unroll 1
   for (int j = 0; j < n_my; ++j) {
-    const int st = j % kStages, db = j % kDecBufs;
-    mbar_wait(&sm.stFull[st], (j / kStages) & 1, a.status);
-    if (j >= kDecBufs) mbar_wait(&dec_empty[db], ((j / kDecBufs) & 1) ^ 1, a.status);
+    mbar_wait(&sm.stFull[st], sph, a.status);
+    // the decoded buffer is needed only at the stores: poll it now, wait there if it was not free
+    const bool dfree = j < kDecBufs || mbar_test_wait(&dec_empty[db], dph ^ 1u);
     const int mode = sm.smeta[st].mode[kind], esc_len = sm.smeta[st].esc[kind];
     const int nv = min(kBlock, len - (blk0 + j) * kBlock);
     const uint8_t* img = sm.stage[st][kind];
     uint8_t* dec = kind ? sm.decV[db] : sm.decK[db];
     const bool slot = mode == GAAC_MODE_SLOT;
-    bool bad = !slot && mode != GAAC_MODE_RAW;
-    uint32_t tb = 0, te = 0;  // tag byte and its tag_entry word
-    int off = 0;
-    if (slot) {
-      const uint16_t* dir = reinterpret_cast<const uint16_t*>(img + kOffDir);
-      const int start = e8 ? dir[e8 - 1] : 0, end = dir[e8];
-      tb = img[kOffTag + u];
-      te = sm.tagl[tb];
-      const int cnt = (te >> 16) & 0xFF;
-      const int incl = warp_incl_scan(cnt, lane);
-      off = start + incl - cnt;  // escape bytes are in unit order
-      bad = start > end || end > esc_len || start + __shfl_sync(kFull, incl, 31) != end;
-      if (bad && lane == 0) report(a.status, GAAC_EFORMAT);
-    }
-    // Every escape offset used below lies inside [start, end) and end <= 496.
+    // Slot bookkeeping, read without waiting for the mode (the bytes are harmless for other modes):
+    // the escape directory gives the eighth's first escape byte, a warp scan of the units' counts each
+    // unit's (escape bytes are in unit order); the eighth's total must match the directory.
+    const uint16_t* dir = reinterpret_cast<const uint16_t*>(img + kOffDir);
+    const int start = e8 ? dir[e8 - 1] : 0, end = dir[e8];
+    const uint32_t tb = img[kOffTag + u];
+    const uint32_t te = sm.tagl[tb];
+    const int cnt = (te >> 16) & 0xFF;
+    const int incl = warp_incl_scan(cnt, lane);
+    const int off = min(max(start + incl - cnt, 0), kEscCap);  // clamped: reads stay in the image
+    const int total = __shfl_sync(kFull, incl, 31);
     uint32_t o[16];
-    if (bad) {  // no valid data: zeros (K blocks are also masked by the tensor-core warps)
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = 0u;
-    } else if (slot) {
+    if (slot) {
       decode_unit(img, u, tb, __byte_perm(escape_window(img, off), 0u, te & 0xFFFFu), b3, d43, sm.lut, o);
     } else {
       raw_unit(img, u, o);
     }
+    bool bad = !slot && mode != GAAC_MODE_RAW;
+    if (slot) {
+      bad = start > end || end > esc_len || start + total != end;
+      if (bad && lane == 0) report(a.status, GAAC_EFORMAT);
+    }
+    if (bad) {  // no valid data: zeros (K blocks are also masked by the tensor-core warps)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = 0u;
+    }
+    if (!dfree) mbar_wait(&dec_empty[db], dph ^ 1u, a.status);
     store_unit(dec, c0, c1, c2, c3, o);
+    // Every escape offset used below lies inside [start, end) and end <= 496.
     if (slot && !bad && (te >> 24)) patch_unit(img, kind, u, tb, off, b4g, sm.lut, dec);  // raw groups: rare
     if (kind == 1 && nv < kBlock) clear_tail(dec, u, nv);
     if (kind == 0 && lane == 0) {
@@ -423,6 +429,14 @@ __device__ __forceinline__ void decoder_warp(const AttnArgs& a, AttSmem& sm, int
     if (lane == 0) {
       mbar_arrive(&sm.stEmpty[st]);
       mbar_arrive(&dec_full[db]);
+    }
+    if (++st == kStages) {
+      st = 0;
+      sph ^= 1u;
+    }
+    if (++db == kDecBufs) {
+      db = 0;
+      dph ^= 1u;
     }
   }
 }
