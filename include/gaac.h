@@ -19,24 +19,31 @@
  *    NULL): the first nonzero code wins (atomic compare-and-swap from 0).  Kernels
  *    never trap and never wait without a bound.  Read it after synchronising.
  *  - BF16 values are passed as their uint16_t bit patterns.
- *  - head_dim is 128 and the block is 64 tokens (format v2 below).
+ *  - head_dim is 128 and the block is 64 tokens (format v3 below).
  *
- * Tile format v2 (identical in the CUDA library and in the test oracle):
+ * Tile format v3 (identical in the CUDA library and in the test oracle):
  *  tile        64 tokens x 128 channels of one (layer, sequence, block, kv-head, K|V)
- *  order       K tiles token-major  (element (t,c) at s = t*128 + c),
- *              V tiles channel-major (element (t,c) at s = c*64 + t)
+ *  order       K tiles token-major  (element (t,c) at s = t*128 + c);
+ *              V tiles in tensor-core operand order:
+ *                s = 1024*(2*(t/16) + c/64) + 32*(4*(c%8) + (t%8)/2) + 8*((c/16)%4)
+ *                    + (c%16)/8 + 2*(t%2) + 4*((t%16)/8)
+ *              (32-element unit 32*(2w+h) + 4g + q holds channels 16m+g and
+ *              16m+g+8, m = 4h..4h+3, at tokens 16w + 2q + {0,1,8,9})
  *  group       8 consecutive elements in that order (G = s/8)
  *  slot image  GAAC_SLOT_BYTES bytes:
  *               [0,8192)      byte s: mantissa of element s in bits 0-6; bit 7 is
  *                             the sign of element 4*(s/4) + (s+3)%4 (the signs of
  *                             each aligned group of four rotated by one byte)
  *               [8192,11264)  3-bit codes: word k (0..2) of 32-element unit u at
- *                             8192 + 4*(k*256 + u)
+ *                             8192 + 4*(k*256 + u); raw groups have code 0
  *               [11264,11520) 2-bit mode of group G at byte 11264 + G/4, bits 2*(G%4)
  *               [11520,11536) escape directory: 8 little-endian u16; entry w is
- *                             the number of escape bytes of groups [0, 128*(w+1))
- *               [11536,12032) escape bytes (mode 1: 1 byte, mode 2: 5 bytes per
- *                             group, in group order), zero filled; capacity 496
+ *                             (4-bit groups in [0, 128*(w+1))) mod 512
+ *                             + 512 * ((raw groups there) mod 128)
+ *               [11536,12032) escape area, zero filled, capacity 496: one byte per
+ *                             4-bit group (bit j = bit 3 of element j's offset), in
+ *                             group order; then eight bytes per raw group (its
+ *                             exponents), in group order
  *  raw tile    8192 BF16 words in the same storage order
  */
 #ifndef GAAC_H
@@ -81,7 +88,7 @@ enum { GAAC_MODE_SLOT = 0, GAAC_MODE_RAW = 1, GAAC_MODE_NONE = 255 };
  * table[batch][max_blocks][n_kv_heads][2]  (last index 0 = K, 1 = V). */
 typedef struct gaac_entry {
   uint32_t index;   /* slot index (mode SLOT) or raw-tile index (mode RAW) */
-  uint16_t esc_len; /* escape bytes used in the slot, directory not counted (mode SLOT) */
+  uint16_t esc_len; /* bytes of the escape area used: 4-bit bytes + 8 per raw group (mode SLOT) */
   uint8_t mode;     /* GAAC_MODE_* */
   uint8_t n_tok;    /* tokens held: 64 for a sealed block, fewer for the open tail */
 } gaac_entry;

@@ -7,7 +7,7 @@ library's CUDA kernels; there is no CPU fallback.  If ``libgaac.so`` has not bee
 built, the first call raises.
 
 Method: "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference on
-Personal Devices" (sections 3.1-3.3).  Tile format v2 is described in gaac.h.
+Personal Devices" (sections 3.1-3.3).  Tile format v3 is described in gaac.h.
 """
 from __future__ import annotations
 

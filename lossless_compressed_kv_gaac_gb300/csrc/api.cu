@@ -13,4 +13,4 @@ extern "C" const char* gaac_strerror(int status) {
   }
 }
 
-extern "C" int gaac_format_version(void) { return 2; }
+extern "C" int gaac_format_version(void) { return 3; }

@@ -7,30 +7,36 @@
 // softmax.  Section 3.3: the block table says per block whether it is a slot
 // or a raw tile.
 //
-// GB300 design: one CTA of 352 threads per SM, grid (split, kv-head, sequence).
-//  * Warp 10 (producer): one lane streams each 64-token block's K and V tile
-//    images (only the bytes a slot uses) into a 3-stage shared-memory ring
+// GB300 design: one CTA of 416 threads per SM, grid (split, kv-head, sequence).
+//  * Warp 12 (producer): one lane streams each 64-token block's K and V tile
+//    images (only the bytes a slot uses) into a 6-stage shared-memory ring
 //    with 1-D bulk copies tracked by mbarriers.
-//  * Warps 0-7 (decoders): warp w rebuilds quarter w%4 (code units
-//    [64q, 64q+64)) of the K (w < 4) or V tile into BF16 in a swizzled
-//    shared-memory tile.  A lane owns two 32-element units.  The escape
-//    directory gives the quarter's first escape byte, a packed warp scan each
-//    unit's, and one byte permute gathers a unit's 4-bit escape bytes.
-//    Exponents are rebuilt four at a time in 32-bit words (the bytes cannot
-//    carry) and joined with the sign|mantissa word by two bit selects and a
-//    byte rotation per four values.  Raw-mode groups are rare and patched
-//    afterwards by the lane that owns them.
-//  * Warps 8-9 (tensor-core warps) take alternate blocks: QK^T and PV^T with
-//    ldmatrix + mma.sync m16n8k16 (bf16 in, fp32 accumulate), an online
-//    softmax in the log2 domain that rescales only when a running maximum
-//    rises, and P stored transposed (stmatrix) as a bf16 hi + lo pair so its
-//    rounding stays near 2^-17.  Each warp keeps (m, l, acc) for its own
-//    blocks; the two are merged when the split ends.
-//  * The decoded tiles hold each group of four values in the order {0,2,1,3}
-//    (the join's output order).  The QK^T contraction runs over channels in
-//    that order (q's fragment follows it); the PV^T contraction runs over
-//    tokens in that order (QK^T rows are permuted the same way, so P^T comes
-//    out in it).
+//  * Warps 0-11 form three groups of four; group gr takes blocks gr, gr+3, ...
+//    of the split, and warp w of a group takes tokens [16w, 16w+16) of each.
+//    Each warp keeps its own online-softmax state (m, l, acc) over its tokens;
+//    the twelve states are merged with a log-sum-exp when the split ends.
+//  * Per block a lane rebuilds two K units and two V units (32 elements each)
+//    straight into tensor-core operand registers, with no shared-memory copy
+//    of the decoded tile:
+//      - K units 64w + lane and 64w + 32 + lane are tokens 16w + g and
+//        16w + 8 + g (g = lane/4), channel block lane%4: exactly the B operand
+//        of S^T = q K^T over eight tokens (mma.sync m16n8k16, q as A with the
+//        8 query heads in rows 0-7 and channels in the order the decoder
+//        emits them);
+//      - the S^T accumulators of the two token octets are, lane for lane, the
+//        B operand (P^T) of O^T += V^T P^T, so softmax needs no data movement;
+//      - V tiles are stored in operand order (format v3), so V units 64w +
+//        lane and 64w + 32 + lane are the A operands of four 16-channel tiles
+//        each for this warp's 16 tokens.
+//  * Decode of a unit: the escape directory gives the eighth's first 4-bit
+//    escape byte and raw group; one warp scan of four packed counts gives each
+//    unit's; one byte permute gathers a unit's 4-bit escape bytes.  Exponents
+//    are rebuilt four at a time in 32-bit words and joined with the
+//    sign|mantissa word by two bit selects and a byte rotation per four
+//    values.  Raw groups (their eight exponents in the escape area) are
+//    re-joined by the lanes that own them.
+//  * Softmax in the log2 domain; rescales only when a running maximum rises;
+//    P goes to the tensor cores as a bf16 hi + lo pair (rounding near 2^-17).
 //  * q is pre-scaled by 2^-4 (exact for normal values) to keep q.k inside the
 //    fp32 range for extreme keys; the factor is folded into the softmax scale.
 //  * Partials (m, l, acc) per split go to the workspace; the last CTA of each
@@ -44,24 +50,17 @@
 
 namespace gaac {
 
-constexpr int kDWarps = 16;                      // decoders: 0-7 K eighths, 8-15 V eighths
-constexpr int kMGroupWarps = 4;                  // a tensor-core group: one 16-token / 32-channel share per warp
-constexpr int kMGroups = 1;                      // groups take alternate blocks
-constexpr int kMWarps = kMGroupWarps * kMGroups;
-constexpr int kMWarp0 = kDWarps;
-constexpr int kProducerWarp = kDWarps + kMWarps;
-constexpr int kAttThreads = (kProducerWarp + 1) * 32;
-constexpr int kStages = 3;                       // staging ring of K+V tile images
-constexpr int kDecBufs = 3;                      // decoded BF16 K+V tiles
+constexpr int kGroupWarps = 4;                    // token quarters of a block
+constexpr int kGroups = 3;                        // warp groups, alternate blocks
+constexpr int kCWarps = kGroupWarps * kGroups;    // compute warps
+constexpr int kAttThreads = kCWarps * 32;
+constexpr int kStages = 6;                        // staging ring of K+V tile images (a multiple of kGroups)
 constexpr int kCtasPerSm = 1;
-constexpr int kRPad = 8;                         // query heads per kv-head in the MMA N dimension
-constexpr int kPtStride = 72;                    // bf16 per head row of P^T (64 tokens + pad): 144 B
-constexpr int kQStride = 136;                    // bf16 per head row of q (128 channels + pad): 272 B
+constexpr int kRPad = 8;                          // query heads per kv-head in the MMA rows
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
-constexpr int kBarM = 1;                         // named barriers 1, 2: one per tensor-core group
-constexpr int kBarMAll = kBarM + kMGroups;       // all tensor-core warps (end of the split)
-constexpr uint32_t kJoinMask = 0x807F807Fu;      // sign and mantissa bits of a bf16x2 word
+constexpr uint32_t kJoinMask = 0x807F807Fu;       // sign and mantissa bits of a bf16x2 word
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+static_assert(kStages % kGroups == 0, "a stage must always feed the same group");
 
 struct StageMeta {
   int mode[2], esc[2];  // [K, V]
@@ -69,21 +68,17 @@ struct StageMeta {
 
 struct AttSmem {
   alignas(128) uint8_t stage[kStages][2][kRawBytes];  // K, V tile images
-  alignas(128) uint8_t decK[kDecBufs][kTile * 2];      // BF16 K, rows = tokens (256 B), swizzled
-  alignas(128) uint8_t decV[kDecBufs][kTile * 2];      // BF16 V, rows = channels (128 B), swizzled
-  alignas(16) uint16_t pt[kMGroups][2][kRPad][kPtStride];  // per group: P^T hi, lo of its current block
-  alignas(16) uint16_t qs[kRPad][kQStride];                 // q * 2^-4, channels in decoded order
-  alignas(16) float wmax[kMGroups][kRPad][kMGroupWarps];    // per head: max of each warp's 16 scores
-  alignas(16) float wl[kMGroups][kRPad][kMGroupWarps];      // per head: row sums of each warp (at the end)
-  alignas(16) float xacc[kRPad][kD];                        // group 1's accumulators (at the end)
-  float xm[kRPad];                                          // group 1's running maxima (at the end)
-  uint2 lut[256];       // escape byte -> bit 3 spread into the byte lanes of two exponent words
-  uint32_t tagl[256];   // tag byte -> gather selector (bits 0-15), escape bytes (16-23), needs a patch (24)
+  uint2 lut[256];                 // escape byte -> bit 3 spread into the byte lanes of two exponent words
+  uint32_t tagl[256];             // tag byte -> gather selector, counts, raw groups (tag_entry)
+  alignas(16) uint8_t bases[2][2][kD];  // [K|V][base3|base4][channel] of the CTA's kv-head
   StageMeta smeta[kStages];
-  int dec_nv[kDecBufs];                   // tokens of the block in decoded buffer d
-  alignas(8) uint8_t dec_bad[kDecBufs][8];  // K eighth failed its checks
-  uint64_t stFull[kStages], stEmpty[kStages];
-  uint64_t dkFull[kDecBufs], dvFull[kDecBufs], dkEmpty[kDecBufs], dvEmpty[kDecBufs];
+  alignas(16) uint32_t qf[kRPad][4][16];  // q A-operand words per (head g, lane tq): qa0[0..7], qa2[0..7]
+  alignas(16) uint32_t vbw[32][2][8];     // V base words per lane and unit: base3 of groups 0-3, base4 - base3
+  unsigned int stDone[kStages];           // warps of the group done reading the stage's current block
+  float wm[kCWarps][kRPad];       // per warp and head: running maximum (end of split)
+  float wl[kCWarps][kRPad];       // per warp and head: denominator (end of split)
+  float ww[kCWarps][kRPad];       // per warp and head: merge weight (end of split)
+  uint64_t stFull[kStages];
   int last;
 };
 
@@ -126,10 +121,10 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ int warp_incl_scan(int x, int lane) {
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(kFull, x, d);
+    const uint32_t v = __shfl_up_sync(kFull, x, d);
     if (lane >= d) x += v;
   }
   return x;
@@ -137,38 +132,11 @@ __device__ __forceinline__ int warp_incl_scan(int x, int lane) {
 
 __device__ __forceinline__ unsigned int atomic_add_acq_rel(unsigned int* p, unsigned int v) {
   unsigned int old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r0), "r"(r1),
-               "r"(r2), "r"(r3)
-               : "memory");
-}
-
-// Position p of a decoded row holds element quad_perm(p): each aligned group
-// of four is stored {0,2,1,3}.  The map is its own inverse.
-__device__ __forceinline__ int quad_perm(int p) { return (p & ~3) | ((p & 1) << 1) | ((p >> 1) & 1); }
-
-// Byte offset of 16-byte chunk c (0..15) of token row t in a decoded K tile.
-// The chunk's low three bits are XORed with the row (and bit 1 flipped in the
-// upper half-row) so that ldmatrix over 8 rows and the decoders' 16-byte
-// stores both touch 8 different bank groups.
-__device__ __forceinline__ uint32_t kswz(int t, int c) {
-  return static_cast<uint32_t>(t * 256 + 16 * ((c & 8) | ((c ^ t ^ ((c >> 3) << 1)) & 7)));
-}
-// Byte offset of 16-byte chunk c (0..7) of channel row ch in a decoded V tile.
-__device__ __forceinline__ uint32_t vswz(int ch, int c) { return static_cast<uint32_t>(ch * 128 + 16 * ((c ^ ch) & 7)); }
-
-// Four BF16 values from one sign|mantissa word of format v2 (byte L: mantissa
+// Four BF16 values from one sign|mantissa word of format v3 (byte L: mantissa
 // of element L, sign of element (L+3)%4) and their exponent word (byte L =
 // exponent of element L): p02 = elements {0, 2}, p13 = elements {1, 3}.
 // Rotating the exponents left by 7 puts elements 0 and 2 in their bf16 fields
@@ -183,42 +151,40 @@ __device__ __forceinline__ void join_v2(uint32_t w, uint32_t e, uint32_t& p02, u
 }
 
 // Everything the decoders need from a unit's tag byte (4 groups x 2 bits):
-//  bits 0-15: byte permute selector that gathers the escape bytes of the
-//    unit's 4-bit groups from the four escape bytes at the unit's offset (byte
-//    j = group j's escape byte if group j is 4-bit and no raw group precedes it
-//    in the unit, else a zero byte; the others are patched separately);
-//  bits 16-23: the unit's escape bytes (1 per 4-bit group, 5 per raw group),
-//    255 if a group has the reserved tag 3 (the quarter's total check fails);
-//  bit 24: the unit has a raw group (patch_unit must run).
+//  bits 0-15: byte permute selector that gathers the unit's 4-bit escape
+//    bytes from the four escape bytes at the unit's offset (byte j = group j's
+//    escape byte if group j is 4-bit, else a zero byte);
+//  bits 16-18: 4-bit groups; bits 19-21: raw groups; bit 22: a reserved tag;
+//  bits 24-27: which groups are raw.
 __device__ __forceinline__ uint32_t tag_entry(uint32_t tb) {
-  uint32_t s = 0, rank = 0, bytes = 0;
-  bool raw = false, reserved = false;
+  uint32_t sel = 0, n4 = 0, nr = 0, rsv = 0, raw = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t t = (tb >> (2 * j)) & 3u;
-    if (t == 3u) reserved = true;
-    if (t >= 2u) raw = true;
-    const uint32_t nib = (t == 1u && !raw) ? rank : 4u;  // 4: a zero byte of the second operand
-    if (t == 1u) ++rank;
-    bytes += t == 1u ? 1u : (t == 2u ? 5u : 0u);
-    s |= nib << (4 * j);
+    sel |= (t == 1u ? n4 : 4u) << (4 * j);  // 4: a zero byte of the second operand
+    if (t == 1u) ++n4;
+    if (t == 2u) {
+      ++nr;
+      raw |= 1u << j;
+    }
+    if (t == 3u) rsv = 1u;
   }
-  return s | ((reserved ? 255u : bytes) << 16) | (raw ? (1u << 24) : 0u);
+  return sel | (n4 << 16) | (nr << 19) | (rsv << 22) | (raw << 24);
 }
 
-// The four escape bytes starting at escape offset `off` of a slot image.
+// The four escape bytes starting at escape offset `off` (clamped into the escape area).
 __device__ __forceinline__ uint32_t escape_window(const uint8_t* img, int off) {
+  off = min(off, kEscCap);
   const uint32_t* ew = reinterpret_cast<const uint32_t*>(img + kOffEsc);
   const uint32_t w0 = ew[off >> 2], w1 = ew[(off >> 2) + 1];
   return __funnelshift_r(w0, w1, 8 * (off & 3));
 }
 
-// Rebuilds 32-element unit u of a slot image into 16 bf16x2 words, in decoded
-// order: word 2q+i of half h holds elements 16h+4q + {0,2} (i=0) / {1,3} (i=1).
-// x: the unit's gathered 4-bit escape bytes (byte j = group j); b3/d43: the
-// unit's base3 words and base4 - base3 (32-bit, modular: e stays exact), word
-// i covering elements 4i..4i+3.  Raw groups and 4-bit groups after them come
-// out wrong and are patched by patch_unit.
+// Rebuilds 32-element unit u of a slot image into 16 bf16x2 words: word 2m+i
+// holds elements 4m + {0,2} (i=0) / {1,3} (i=1).  x: the unit's gathered 4-bit
+// escape bytes (byte j = group j); b3/d43: the unit's base3 words and base4 -
+// base3 (32-bit, modular: e stays exact), word 2i and 2i+1 covering group i.
+// Raw groups come out wrong and are re-joined by fix_raw.
 __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t tb, uint32_t x, const uint32_t b3[8],
                                             const uint32_t d43[8], const uint2* lut, uint32_t o[16]) {
   const uint32_t* cw = reinterpret_cast<const uint32_t*>(img + kOffCode);
@@ -235,8 +201,8 @@ __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t 
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint32_t f = q < 2 ? fa : fb;
-      const uint32_t s = q == 0 ? sa.x : (q == 1 ? sa.y : (q == 2 ? sb.x : sb.y));
-      e[q] = (f ? b3[4 * hh + q] + d43[4 * hh + q] : b3[4 * hh + q]) + c[q] + s;  // base4 = base3 + d43
+      const uint32_t sp = q == 0 ? sa.x : (q == 1 ? sa.y : (q == 2 ? sb.x : sb.y));
+      e[q] = (f ? b3[4 * hh + q] + d43[4 * hh + q] : b3[4 * hh + q]) + c[q] + sp;  // base4 = base3 + d43
     }
     const uint4 sm = hh ? s1 : s0;
     join_v2(sm.x, e[0], o[8 * hh + 0], o[8 * hh + 1]);
@@ -246,96 +212,23 @@ __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t 
   }
 }
 
-// Decoded chunk j (0..3) of unit u of a K (kind 0) or V tile: byte offset.
-__device__ __forceinline__ uint32_t unit_chunk(int kind, int u, int j) {
-  return kind == 0 ? kswz(u >> 2, 4 * (u & 3) + j) : vswz(u >> 1, 4 * (u & 1) + j);
-}
-
-__device__ __forceinline__ void store_unit(uint8_t* dec, uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                           const uint32_t o[16]) {
-  *reinterpret_cast<uint4*>(dec + c0) = make_uint4(o[0], o[1], o[2], o[3]);
-  *reinterpret_cast<uint4*>(dec + c1) = make_uint4(o[4], o[5], o[6], o[7]);
-  *reinterpret_cast<uint4*>(dec + c2) = make_uint4(o[8], o[9], o[10], o[11]);
-  *reinterpret_cast<uint4*>(dec + c3) = make_uint4(o[12], o[13], o[14], o[15]);
-}
-
-// V tail (the open block): zero the decoded values of tokens >= nv in V unit
-// u, whose tokens are 32(u%2)..+31, so that no stale value meets a zero
-// probability.  Runs for one block per split at most.
-__device__ __noinline__ void clear_tail(uint8_t* dec, int u, int nv) {
-#pragma unroll 1
-  for (int j = 0; j < 4; ++j) {
-    const int t0 = 32 * (u & 1) + 8 * j;  // chunk j: tokens t0..t0+7 stored {0,2,1,3,4,6,5,7}
-    if (t0 + 8 <= nv) continue;
-    uint4* p = reinterpret_cast<uint4*>(dec + vswz(u >> 1, 4 * (u & 1) + j));
-    uint4 w = *p;
-    w.x &= (t0 < nv ? 0x0000FFFFu : 0u) | (t0 + 2 < nv ? 0xFFFF0000u : 0u);
-    w.y &= (t0 + 1 < nv ? 0x0000FFFFu : 0u) | (t0 + 3 < nv ? 0xFFFF0000u : 0u);
-    w.z &= (t0 + 4 < nv ? 0x0000FFFFu : 0u) | (t0 + 6 < nv ? 0xFFFF0000u : 0u);
-    w.w &= (t0 + 5 < nv ? 0x0000FFFFu : 0u) | (t0 + 7 < nv ? 0xFFFF0000u : 0u);
-    *p = w;
-  }
-}
-
-// Re-decodes the groups of unit u that decode_unit cannot: raw groups (their
-// exponent bits 3..7 are five escape bit planes) and 4-bit groups placed after
-// a raw group.  off: the unit's first escape byte.  Rewrites those groups'
-// 16-byte chunks in the decoded tile.
-__device__ __forceinline__ void patch_unit(const uint8_t* img, int kind, int u, uint32_t tb, int off,
-                                           const uint8_t* b4g, const uint2* lut, uint8_t* dec) {
-  uint32_t fix = 0;
-  bool raw = false;
+// Re-joins the raw groups of unit u: their exponents are eight escape bytes
+// each, the unit's first at escape offset `oraw` (clamped into the area).
+__device__ __forceinline__ void fix_raw(const uint8_t* img, int u, uint32_t tb, int oraw, uint32_t o[16]) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t t = (tb >> (2 * j)) & 3u;
-    if (t == 2u || (t == 1u && raw)) fix |= 1u << j;
-    if (t == 2u) raw = true;
-  }
-  const uint32_t* cw = reinterpret_cast<const uint32_t*>(img + kOffCode);
-  const uint8_t* esc = img + kOffEsc;
-#pragma unroll 1
-  while (fix) {
-    const int j = __ffs(fix) - 1;
-    fix &= fix - 1;
-    const uint32_t t = (tb >> (2 * j)) & 3u;
-    const int o = off + esc_count(tb & ((1u << (2 * j)) - 1u));
-    const int hh = j >> 1;
-    uint32_t c[4];
-    extract_codes(hh ? cw[256 + u] : cw[u], cw[512 + u], hh, c);
-    const uint32_t ca = (j & 1) ? c[2] : c[0], cb = (j & 1) ? c[3] : c[1];
-    const uint2 smw = *reinterpret_cast<const uint2*>(img + 32 * u + 8 * j);
-    uint32_t ea, eb;
-    if (t == 1u) {
-      uint32_t ba, bb;
-      if (kind == 0) {
-        const int ch = 32 * (u & 3) + 8 * j;
-        ba = *reinterpret_cast<const uint32_t*>(b4g + ch);
-        bb = *reinterpret_cast<const uint32_t*>(b4g + ch + 4);
-      } else {
-        ba = bb = 0x01010101u * b4g[u >> 1];
-      }
-      const uint2 s = lut[esc[o]];
-      ea = ba + ca + s.x;
-      eb = bb + cb + s.y;
-    } else {
-      uint32_t h0 = 0, h1 = 0;
-#pragma unroll
-      for (int k = 0; k < 5; ++k) {
-        const uint2 s = lut[esc[o + k]];  // bit plane 3+k: spread to bit 3, shifted up by k
-        h0 |= s.x << k;
-        h1 |= s.y << k;
-      }
-      ea = ca | h0;
-      eb = cb | h1;
+  for (int gi = 0; gi < 4; ++gi) {
+    if (((tb >> (2 * gi)) & 3u) == 2u) {
+      const int at = kOffEsc + min(oraw, kEscCap - 8);
+      const uint32_t x0 = load_u32_any(img, at), x1 = load_u32_any(img, at + 4);
+      const uint2 smw = *reinterpret_cast<const uint2*>(img + 32 * u + 8 * gi);
+      join_v2(smw.x, x0, o[4 * gi], o[4 * gi + 1]);
+      join_v2(smw.y, x1, o[4 * gi + 2], o[4 * gi + 3]);
+      oraw += 8;
     }
-    uint32_t w[4];
-    join_v2(smw.x, ea, w[0], w[1]);
-    join_v2(smw.y, eb, w[2], w[3]);
-    *reinterpret_cast<uint4*>(dec + unit_chunk(kind, u, j)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
-// Raw tile (BF16 in storage order) unit u into decoded order.
+// Raw tile (BF16 in storage order) unit u into the decoder's word order.
 __device__ __forceinline__ void raw_unit(const uint8_t* img, int u, uint32_t o[16]) {
   const uint4* src = reinterpret_cast<const uint4*>(img + 64 * u);
 #pragma unroll
@@ -348,349 +241,245 @@ __device__ __forceinline__ void raw_unit(const uint8_t* img, int u, uint32_t o[1
   }
 }
 
-// ------------------------------------------------------------------ decoders
-
-// One decoder warp: eighth e8 (code units [32 e8, 32 e8 + 32)) of every
-// block's K (kind 0) or V (kind 1) tile; lane l owns unit 32 e8 + l.  A K unit
-// is one token's channel block l%4, a V unit one half of channel 16 e8 + l/2,
-// so a lane's window bases never change.  Both kinds run this one code path.
-__device__ __forceinline__ void decoder_warp(const AttnArgs& a, AttSmem& sm, int h, int blk0, int n_my, int len,
-                                             int kind, int e8, int lane) {
-  const uint8_t* b3g = a.base3 + (kind * a.Hkv + h) * kD;
-  const uint8_t* b4g = a.base4 + (kind * a.Hkv + h) * kD;
-  const int u = kDirUnits * e8 + lane;
-  uint32_t b3[8], d43[8];
-  if (kind == 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      b3[i] = *reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 4 * i);
-      d43[i] = *reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 4 * i) - b3[i];
-    }
+// The lane's two units of one tile image (units 64w + lane and 64w + 32 +
+// lane, in eighths 2w and 2w+1), rebuilt into oA / oB; badA / badB: the
+// eighth failed its checks (its words are zero).  Slot bookkeeping: the
+// directory gives each eighth's first 4-bit escape byte and raw group, one
+// warp scan of the four packed counts (at most 4 per unit, 128 per eighth)
+// each unit's.
+__device__ __forceinline__ void tile_units(const AttnArgs& a, const AttSmem& sm, const uint8_t* img, int mode,
+                                           int esc_len, int w, int lane, const uint32_t b3A[8],
+                                           const uint32_t d43A[8], const uint32_t b3B[8], const uint32_t d43B[8],
+                                           uint32_t oA[16], uint32_t oB[16], bool& badA, bool& badB) {
+  const int uA = 64 * w + lane, uB = uA + 32;
+  if (mode == GAAC_MODE_SLOT) {
+    const uint16_t* dir = reinterpret_cast<const uint16_t*>(img + kOffDir);
+    const uint32_t d0 = w ? dir[2 * w - 1] : 0u, dA = dir[2 * w], dB = dir[2 * w + 1], d7 = dir[7];
+    const uint32_t tbA = img[kOffTag + uA], tbB = img[kOffTag + uB];
+    const uint32_t teA = sm.tagl[tbA], teB = sm.tagl[tbB];
+    const uint32_t cnt = ((teA >> 16) & 7u) | (((teB >> 16) & 7u) << 8) | (((teA >> 19) & 7u) << 16) |
+                         (((teB >> 19) & 7u) << 24);
+    const uint32_t incl = warp_incl_scan(cnt, lane);
+    const uint32_t tot = __shfl_sync(kFull, incl, 31), ex = incl - cnt;
+    const int rawbase = static_cast<int>(d7 & 0x1FFu);
+    const int o4A = static_cast<int>((d0 & 0x1FFu) + (ex & 0xFFu));
+    const int o4B = static_cast<int>((dA & 0x1FFu) + ((ex >> 8) & 0xFFu));
+    const int orA = rawbase + 8 * static_cast<int>((d0 >> 9) + ((ex >> 16) & 0xFFu));
+    const int orB = rawbase + 8 * static_cast<int>((dA >> 9) + (ex >> 24));
+    decode_unit(img, uA, tbA, __byte_perm(escape_window(img, o4A), 0u, teA & 0xFFFFu), b3A, d43A, sm.lut, oA);
+    decode_unit(img, uB, tbB, __byte_perm(escape_window(img, o4B), 0u, teB & 0xFFFFu), b3B, d43B, sm.lut, oB);
+    if (teA >> 24) fix_raw(img, uA, tbA, orA, oA);  // raw groups: rare
+    if (teB >> 24) fix_raw(img, uB, tbB, orB, oB);
+    const bool totals = rawbase + 8 * static_cast<int>(d7 >> 9) != esc_len;
+    badA = __any_sync(kFull, (teA >> 22) & 1u) || totals || (d0 & 0x1FFu) + (tot & 0xFFu) != (dA & 0x1FFu) ||
+           (d0 >> 9) + ((tot >> 16) & 0xFFu) != (dA >> 9);
+    badB = __any_sync(kFull, (teB >> 22) & 1u) || totals ||
+           (dA & 0x1FFu) + ((tot >> 8) & 0xFFu) != (dB & 0x1FFu) || (dA >> 9) + (tot >> 24) != (dB >> 9);
+    if ((badA || badB) && lane == 0) report(a.status, GAAC_EFORMAT);
   } else {
-    const uint32_t x3 = 0x01010101u * b3g[u >> 1], x4 = 0x01010101u * b4g[u >> 1];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      b3[i] = x3;
-      d43[i] = x4 - x3;
+    badA = badB = mode != GAAC_MODE_RAW;
+    if (!badA) {
+      raw_unit(img, uA, oA);
+      raw_unit(img, uB, oB);
     }
   }
-  const uint32_t c0 = unit_chunk(kind, u, 0), c1 = unit_chunk(kind, u, 1), c2 = unit_chunk(kind, u, 2),
-                 c3 = unit_chunk(kind, u, 3);
-  uint64_t* dec_full = kind ? sm.dvFull : sm.dkFull;
-  uint64_t* dec_empty = kind ? sm.dvEmpty : sm.dkEmpty;
-  int st = 0, db = 0;
-  uint32_t sph = 0u, dph = 0u;  // parity of the current lap of the staging ring / decoded buffers
-#pragma unroll 1
-  for (int j = 0; j < n_my; ++j) {
-    mbar_wait(&sm.stFull[st], sph, a.status);
-    // the decoded buffer is needed only at the stores: poll it now, wait there if it was not free
-    const bool dfree = j < kDecBufs || mbar_test_wait(&dec_empty[db], dph ^ 1u);
-    const int mode = sm.smeta[st].mode[kind], esc_len = sm.smeta[st].esc[kind];
-    const int nv = min(kBlock, len - (blk0 + j) * kBlock);
-    const uint8_t* img = sm.stage[st][kind];
-    uint8_t* dec = kind ? sm.decV[db] : sm.decK[db];
-    const bool slot = mode == GAAC_MODE_SLOT;
-    // Slot bookkeeping, read without waiting for the mode (the bytes are harmless for other modes):
-    // the escape directory gives the eighth's first escape byte, a warp scan of the units' counts each
-    // unit's (escape bytes are in unit order); the eighth's total must match the directory.
-    const uint16_t* dir = reinterpret_cast<const uint16_t*>(img + kOffDir);
-    const int start = e8 ? dir[e8 - 1] : 0, end = dir[e8];
-    const uint32_t tb = img[kOffTag + u];
-    const uint32_t te = sm.tagl[tb];
-    const int cnt = (te >> 16) & 0xFF;
-    const int incl = warp_incl_scan(cnt, lane);
-    const int off = min(max(start + incl - cnt, 0), kEscCap);  // clamped: reads stay in the image
-    const int total = __shfl_sync(kFull, incl, 31);
-    uint32_t o[16];
-    if (slot) {
-      decode_unit(img, u, tb, __byte_perm(escape_window(img, off), 0u, te & 0xFFFFu), b3, d43, sm.lut, o);
-    } else {
-      raw_unit(img, u, o);
-    }
-    bool bad = !slot && mode != GAAC_MODE_RAW;
-    if (slot) {
-      bad = start > end || end > esc_len || start + total != end;
-      if (bad && lane == 0) report(a.status, GAAC_EFORMAT);
-    }
-    if (bad) {  // no valid data: zeros (K blocks are also masked by the tensor-core warps)
+  if (badA) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = 0u;
-    }
-    if (!dfree) mbar_wait(&dec_empty[db], dph ^ 1u, a.status);
-    store_unit(dec, c0, c1, c2, c3, o);
-    // Every escape offset used below lies inside [start, end) and end <= 496.
-    if (slot && !bad && (te >> 24)) patch_unit(img, kind, u, tb, off, b4g, sm.lut, dec);  // raw groups: rare
-    if (kind == 1 && nv < kBlock) clear_tail(dec, u, nv);
-    if (kind == 0 && lane == 0) {
-      sm.dec_bad[db][e8] = bad ? 1 : 0;
-      if (e8 == 0) sm.dec_nv[db] = nv;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&sm.stEmpty[st]);
-      mbar_arrive(&dec_full[db]);
-    }
-    if (++st == kStages) {
-      st = 0;
-      sph ^= 1u;
-    }
-    if (++db == kDecBufs) {
-      db = 0;
-      dph ^= 1u;
-    }
+    for (int i = 0; i < 16; ++i) oA[i] = 0u;
+  }
+  if (badB) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) oB[i] = 0u;
   }
 }
 
 // ------------------------------------------------------------------ producer
 
-__device__ __forceinline__ void producer_lane(const AttnArgs& a, AttSmem& sm, int b, int h, int blk0, int n_my) {
-  const gaac_entry* tab = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk0) * a.Hkv + h) * 2;
-  const size_t stride = static_cast<size_t>(a.Hkv) * 2;
-  uint2 curK = make_uint2(0u, 0u), curV = make_uint2(0u, 0u);
-  if (n_my > 0) {
-    curK = *reinterpret_cast<const uint2*>(tab);
-    curV = *reinterpret_cast<const uint2*>(tab + 1);
+// Source and byte count of one table entry's tile image (only the bytes a
+// slot uses); nullptr with mode NONE for an entry that fails its checks.
+__device__ __forceinline__ const void* tile_source(const AttnArgs& a, uint2 e, uint32_t& bytes, int& mode, int& esc) {
+  const uint32_t index = e.x, esc_len = e.y & 0xFFFFu, emode = (e.y >> 16) & 0xFFu;
+  if (emode == GAAC_MODE_SLOT && static_cast<int64_t>(index) < a.n_slots && esc_len <= kEscCap) {
+    mode = GAAC_MODE_SLOT;
+    esc = static_cast<int>(esc_len);
+    bytes = (kOffEsc + esc_len + 15u) & ~15u;
+    return a.slot_pool + static_cast<size_t>(index) * kSlot;
   }
-#pragma unroll 1
-  for (int j = 0; j < n_my; ++j) {
-    uint2 nxtK = curK, nxtV = curV;
-    if (j + 1 < n_my) {
-      nxtK = *reinterpret_cast<const uint2*>(tab + (j + 1) * stride);
-      nxtV = *reinterpret_cast<const uint2*>(tab + (j + 1) * stride + 1);
-    }
-    const int st = j % kStages;
-    if (j >= kStages) mbar_wait(&sm.stEmpty[st], ((j / kStages) & 1) ^ 1, a.status);
-    StageMeta m;
-    uint32_t bytes[2];
-    const void* src[2];
-#pragma unroll
-    for (int kv = 0; kv < 2; ++kv) {
-      const uint2 cur = kv ? curV : curK;
-      const uint32_t index = cur.x, esc_len = cur.y & 0xFFFFu, emode = (cur.y >> 16) & 0xFFu;
-      bytes[kv] = 0;
-      src[kv] = nullptr;
-      m.mode[kv] = GAAC_MODE_NONE;
-      m.esc[kv] = 0;
-      if (emode == GAAC_MODE_SLOT && static_cast<int64_t>(index) < a.n_slots && esc_len <= kEscCap) {
-        m.mode[kv] = GAAC_MODE_SLOT;
-        m.esc[kv] = static_cast<int>(esc_len);
-        bytes[kv] = (kOffEsc + esc_len + 15u) & ~15u;
-        src[kv] = a.slot_pool + static_cast<size_t>(index) * kSlot;
-      } else if (emode == GAAC_MODE_RAW && static_cast<int64_t>(index) < a.n_raw) {
-        m.mode[kv] = GAAC_MODE_RAW;
-        bytes[kv] = kRawBytes;
-        src[kv] = a.raw_pool + static_cast<size_t>(index) * kTile;
-      } else {
-        report(a.status, GAAC_EFORMAT);
-      }
-    }
-    sm.smeta[st] = m;
-    mbar_arrive_expect_tx(&sm.stFull[st], bytes[0] + bytes[1]);
-    if (bytes[0]) bulk_g2s(sm.stage[st][0], src[0], bytes[0], &sm.stFull[st]);
-    if (bytes[1]) bulk_g2s(sm.stage[st][1], src[1], bytes[1], &sm.stFull[st]);
-    curK = nxtK;
-    curV = nxtV;
+  esc = 0;
+  if (emode == GAAC_MODE_RAW && static_cast<int64_t>(index) < a.n_raw) {
+    mode = GAAC_MODE_RAW;
+    bytes = kRawBytes;
+    return a.raw_pool + static_cast<size_t>(index) * kTile;
   }
-  // Every issued copy was consumed by the decoders; after a timed-out wait,
-  // wait once more (bounded) so that no copy is still landing at exit.
-#pragma unroll 1
-  for (int i = max(0, n_my - kStages); i < n_my; ++i)
-    mbar_wait(&sm.stFull[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
+  mode = GAAC_MODE_NONE;
+  bytes = 0;
+  return nullptr;
 }
 
-// ------------------------------------------------------------- tensor cores
+// Table entries (K, V) of block j of the split.
+__device__ __forceinline__ void block_entries(const AttnArgs& a, int b, int h, int blk, uint2& eK, uint2& eV) {
+  const gaac_entry* t = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk) * a.Hkv + h) * 2;
+  eK = *reinterpret_cast<const uint2*>(t);
+  eV = *reinterpret_cast<const uint2*>(t + 1);
+}
 
-// A tensor-core group of four warps shares each of its blocks (group gr takes
-// blocks gr, gr+2, ...): warp w scores tokens [16w, 16w+16) (QK^T) and
-// accumulates channels [32w, 32w+32) (PV^T).  The block maximum per head goes
-// through shared memory, so the group's warps keep the same running maximum;
-// the two groups' partials are merged when the split ends.
-__device__ __forceinline__ void tensor_warp(const AttnArgs& a, AttSmem& sm, int n_my, float* part, int gr, int w,
-                                            int lane) {
+// One thread starts the bulk copies of a block's K and V images into stage st
+// (a free stage); stFull[st] completes when both have landed.
+__device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem& sm, int st, uint2 eK, uint2 eV) {
+  StageMeta m;
+  uint32_t bytes[2];
+  const void* src[2];
+  src[0] = tile_source(a, eK, bytes[0], m.mode[0], m.esc[0]);
+  src[1] = tile_source(a, eV, bytes[1], m.mode[1], m.esc[1]);
+  if (!src[0] || !src[1]) report(a.status, GAAC_EFORMAT);
+  sm.smeta[st] = m;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic reads of the stage, then async writes
+  mbar_arrive_expect_tx(&sm.stFull[st], bytes[0] + bytes[1]);
+  if (bytes[0]) bulk_g2s(sm.stage[st][0], src[0], bytes[0], &sm.stFull[st]);
+  if (bytes[1]) bulk_g2s(sm.stage[st][1], src[1], bytes[1], &sm.stFull[st]);
+}
+
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_cta(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.cta.shared::cta.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
+  return old;
+}
+
+// ------------------------------------------------------------ compute warps
+
+// Warp w of group gr: tokens [16w, 16w+16) of blocks gr, gr + kGroups, ...
+// Lane (g, tq) = (lane/4, lane%4).  Returns the warp's (m, l) per head through
+// shared memory and its accumulators in acc (O^T fragments: acc[m][0..3] =
+// channels 16m+g, 16m+g+8 x heads 2tq, 2tq+1).
+__device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int b, int h, int blk0, int n_my, int len,
+                                             int gr, int w, int cw, int lane, float acc[8][4]) {
   const int g = lane >> 2, tq = lane & 3;
-  // ldmatrix row of this lane inside a 16-row tile: matrix m = lane/8 covers rows 8(m%2).., columns 8(m/2)..
-  const int lrow = ((lane >> 3) & 1) * 8 + (lane & 7);
-  const int lcol = lane >> 4;
-  const int tg = quad_perm(g);
-  float acc[2][4];  // channel tiles 2w, 2w+1
+  // K units: channels 32tq..32tq+31 (word i: channels 32tq + 4i..+3)
+  uint32_t kb3[8], kd43[8];
 #pragma unroll
-  for (int ct = 0; ct < 2; ++ct) acc[ct][0] = acc[ct][1] = acc[ct][2] = acc[ct][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2tq, 2tq+1 (log2 domain)
-  // q as the B operand of QK^T: two k-steps per ldmatrix (chunk lane/8 of the head row lane%8)
-  uint32_t qf[16];
-  {
-    const uint32_t qsa = smem_addr(&sm.qs[lane & 7][0]) + 16u * (lane >> 3);
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) ldsm_x4(qsa + 64u * k2, qf[4 * k2], qf[4 * k2 + 1], qf[4 * k2 + 2], qf[4 * k2 + 3]);
+  for (int i = 0; i < 8; ++i) {
+    kb3[i] = *reinterpret_cast<const uint32_t*>(&sm.bases[0][0][32 * tq + 4 * i]);
+    kd43[i] = *reinterpret_cast<const uint32_t*>(&sm.bases[0][1][32 * tq + 4 * i]) - kb3[i];
   }
-  const uint32_t pth = smem_addr(&sm.pt[gr][0][0][0]);
-  // P^T store: matrices (hi rows 0-7, hi rows 8-15, lo rows 0-7, lo rows 8-15) of this warp's 16 positions
-  const uint32_t pst = pth + static_cast<uint32_t>((lane >> 4) * kRPad * kPtStride * 2 + (lane & 7) * kPtStride * 2 +
-                                                   (2 * w + ((lane >> 3) & 1)) * 16);
-  // P^T as B of one k-step: matrices (hi k0-7, hi k8-15, lo k0-7, lo k8-15)
-  const uint32_t pba = pth + static_cast<uint32_t>((lane >> 4) * kRPad * kPtStride * 2 + (lane & 7) * kPtStride * 2 +
-                                                   16 * ((lane >> 3) & 1));
-  uint32_t koff[8], voff[8];  // swizzled ldmatrix offsets: K row 16w + quad_perm(lrow) per k-step; V rows per (k-step, tile)
+  const uint4* qfl = reinterpret_cast<const uint4*>(&sm.qf[g][tq][0]);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) koff[ks] = kswz(16 * w + quad_perm(lrow), 2 * ks + lcol);  // rows follow V's token order
-#pragma unroll
-  for (int kt = 0; kt < 4; ++kt)
-#pragma unroll
-    for (int ct = 0; ct < 2; ++ct) voff[2 * kt + ct] = vswz(32 * w + 16 * ct + lrow, 2 * kt + lcol);
-
+  for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+  float mrun = -INFINITY, lsum = 0.f;  // head g
+  const int tA = 16 * w + 2 * tq, tB = tA + 8;  // tokens of S^T columns 2tq, 2tq+1 of the two octets
 #pragma unroll 1
-  for (int j = gr; j < n_my; j += kMGroups) {
-    const int db = j % kDecBufs;
-    const uint32_t par = (j / kDecBufs) & 1;
-    mbar_wait(&sm.dkFull[db], par, a.status);
-    const int nv = sm.dec_nv[db];
-    const uint2 badw = *reinterpret_cast<const uint2*>(sm.dec_bad[db]);  // one byte per K eighth
-    const bool kbad = (badw.x | badw.y) != 0u;
-    // ---- S = K q^T for tokens 16w..16w+15: 8 k-steps in two accumulation chains
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint32_t kb = smem_addr(sm.decK[db]);
+  for (int j = gr; j < n_my; j += kGroups) {
+    const int st = j % kStages, jn = j + kStages;  // jn: the block this stage takes next
+    uint2 nK = make_uint2(0u, 0u), nV = nK;
+    if (lane == 0 && jn < n_my) block_entries(a, b, h, blk0 + jn, nK, nV);  // used if this warp refills
+    mbar_wait(&sm.stFull[st], static_cast<uint32_t>(j / kStages) & 1u, a.status);
+    const StageMeta meta = sm.smeta[st];
+    const int nv = min(kBlock, len - (blk0 + j) * kBlock);
+    // ---- S^T for tokens 16w..16w+7 (A) and 16w+8..16w+15 (B)
+    float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
+    bool kbadA, kbadB;
+    {
+      uint32_t oA[16], oB[16];
+      tile_units(a, sm, sm.stage[st][0], meta.mode[0], meta.esc[0], w, lane, kb3, kd43, kb3, kd43, oA, oB, kbadA,
+                 kbadB);
+      // q of head g as the A operand of S^T = q K^T (scaled by 2^-4): for k-step m the K lane holds channels
+      // 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no head) are zero
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(kb + koff[ks], a0, a1, a2, a3);
-      mma_bf16(ks & 1 ? sb : sa, a0, a1, a2, a3, qf[2 * ks], qf[2 * ks + 1]);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.dkEmpty[db]);
-    const bool ok0 = !kbad && 16 * w + tg < nv, ok1 = !kbad && 16 * w + 8 + tg < nv;
-    float s0 = ok0 ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;
-    float s1 = ok0 ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;
-    float s2 = ok1 ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;
-    float s3 = ok1 ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;
-    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+      for (int m2 = 0; m2 < 4; ++m2) {
+        const uint4 qv = qfl[m2];  // qa0[2m2], qa0[2m2+1], qa2[2m2], qa2[2m2+1]
 #pragma unroll
-    for (int d = 4; d < 32; d <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, d));
-      x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, d));
-    }
-    if (g == 0) {
-      sm.wmax[gr][2 * tq][w] = x0;
-      sm.wmax[gr][2 * tq + 1][w] = x1;
-    }
-    named_bar_sync(kBarM + gr, kMGroupWarps * 32);  // block maxima of the group's warps written
-    const float4 ma = *reinterpret_cast<const float4*>(&sm.wmax[gr][2 * tq][0]);
-    const float4 mb = *reinterpret_cast<const float4*>(&sm.wmax[gr][2 * tq + 1][0]);
-    const float n0 = fmaxf(m0, fmaxf(fmaxf(ma.x, ma.y), fmaxf(ma.z, ma.w)));
-    const float n1 = fmaxf(m1, fmaxf(fmaxf(mb.x, mb.y), fmaxf(mb.z, mb.w)));
-    if (n0 != m0 || n1 != m1) {  // a running maximum rises: rescale (rare after the first blocks)
-      const float al0 = n0 == -INFINITY ? 1.f : fast_exp2(m0 - n0);
-      const float al1 = n1 == -INFINITY ? 1.f : fast_exp2(m1 - n1);
-      l0 *= al0;
-      l1 *= al1;
-#pragma unroll
-      for (int ct = 0; ct < 2; ++ct) {
-        acc[ct][0] *= al0;
-        acc[ct][1] *= al1;
-        acc[ct][2] *= al0;
-        acc[ct][3] *= al1;
+        for (int i = 0; i < 2; ++i) {
+          const int m = 2 * m2 + i;
+          const uint32_t q0 = i ? qv.y : qv.x, q2 = i ? qv.w : qv.z;
+          mma_bf16(sA, q0, 0u, q2, 0u, oA[2 * m], oA[2 * m + 1]);
+          mma_bf16(sB, q0, 0u, q2, 0u, oB[2 * m], oB[2 * m + 1]);
+        }
       }
-      m0 = n0;
-      m1 = n1;
     }
-    const float p0 = m0 == -INFINITY ? 0.f : fast_exp2(s0 - m0);
-    const float p1 = m1 == -INFINITY ? 0.f : fast_exp2(s1 - m1);
-    const float p2 = m0 == -INFINITY ? 0.f : fast_exp2(s2 - m0);
-    const float p3 = m1 == -INFINITY ? 0.f : fast_exp2(s3 - m1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
+    // ---- online softmax of head g over the warp's 16 tokens
+    const float x0 = (!kbadA && tA < nv) ? sA[0] * a.scale_log2 : -INFINITY;
+    const float x1 = (!kbadA && tA + 1 < nv) ? sA[1] * a.scale_log2 : -INFINITY;
+    const float x2 = (!kbadB && tB < nv) ? sB[0] * a.scale_log2 : -INFINITY;
+    const float x3 = (!kbadB && tB + 1 < nv) ? sB[1] * a.scale_log2 : -INFINITY;
+    float bm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+    const float mnew = fmaxf(mrun, bm);
+    if (__any_sync(kFull, mnew != mrun)) {  // a running maximum rises: rescale (rare after the first blocks)
+      const float al = mrun == -INFINITY ? 0.f : fast_exp2(mrun - mnew);
+      lsum *= al;
+      const float al0 = __shfl_sync(kFull, al, 8 * tq), al1 = __shfl_sync(kFull, al, 8 * tq + 4);  // heads 2tq, 2tq+1
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        acc[m][0] *= al0;
+        acc[m][2] *= al0;
+        acc[m][1] *= al1;
+        acc[m][3] *= al1;
+      }
+      mrun = mnew;
+    }
+    const bool live = mrun != -INFINITY;
+    const float p0 = live ? fast_exp2(x0 - mrun) : 0.f, p1 = live ? fast_exp2(x1 - mrun) : 0.f;
+    const float p2 = live ? fast_exp2(x2 - mrun) : 0.f, p3 = live ? fast_exp2(x3 - mrun) : 0.f;
+    lsum += (p0 + p1) + (p2 + p3);
+    // P^T as the B operand: rows (tokens) 2tq, 2tq+1 from octet A, 2tq+8, 2tq+9 from octet B; column = head g
     const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-    const uint32_t r01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
-    const uint32_t r23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
-    stsm_x4_trans(pst, h01, h23, r01, r23);  // P^T[head][16w + row]
-    named_bar_sync(kBarM + gr, kMGroupWarps * 32);  // P^T of the block complete
-    // ---- acc += V^T P for channels 32w..32w+31: 4 k-steps of 16 tokens
-    mbar_wait(&sm.dvFull[db], par, a.status);
-    const uint32_t vb = smem_addr(sm.decV[db]);
+    const uint32_t l01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
+    const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
+    // ---- O^T += V^T P^T over the 16 tokens, eight 16-channel tiles
+    {
+      uint32_t oA[16], oB[16];
+      bool vbadA, vbadB;
+      uint32_t vb3[2][8], vd43[2][8];  // word 2i and 2i+1 serve group i
 #pragma unroll
-    for (int kt = 0; kt < 4; ++kt) {
-      uint32_t bh0, bh1, bl0, bl1;
-      ldsm_x4(pba + 32u * kt, bh0, bh1, bl0, bl1);
+      for (int hv = 0; hv < 2; ++hv) {
+        const uint4 x3 = *reinterpret_cast<const uint4*>(&sm.vbw[lane][hv][0]);
+        const uint4 x4 = *reinterpret_cast<const uint4*>(&sm.vbw[lane][hv][4]);
+        vb3[hv][0] = vb3[hv][1] = x3.x;
+        vb3[hv][2] = vb3[hv][3] = x3.y;
+        vb3[hv][4] = vb3[hv][5] = x3.z;
+        vb3[hv][6] = vb3[hv][7] = x3.w;
+        vd43[hv][0] = vd43[hv][1] = x4.x;
+        vd43[hv][2] = vd43[hv][3] = x4.y;
+        vd43[hv][4] = vd43[hv][5] = x4.z;
+        vd43[hv][6] = vd43[hv][7] = x4.w;
+      }
+      tile_units(a, sm, sm.stage[st][1], meta.mode[1], meta.esc[1], w, lane, vb3[0], vd43[0], vb3[1], vd43[1], oA,
+                 oB, vbadA, vbadB);
+      // The stage is read: the group's last warp to get here refills it with block jn.
+      __syncwarp();
+      if (lane == 0 && atomic_add_acq_rel_cta(&sm.stDone[st], 1u) == kGroupWarps - 1) {
+        sm.stDone[st] = 0u;
+        if (jn < n_my) issue_block(a, sm, st, nK, nV);
+      }
+      if (nv < kBlock) {  // the open block: values of tokens past the sequence must not meet a zero weight
+        const uint32_t mlo = (tA < nv ? 0x0000FFFFu : 0u) | (tA + 1 < nv ? 0xFFFF0000u : 0u);
+        const uint32_t mhi = (tB < nv ? 0x0000FFFFu : 0u) | (tB + 1 < nv ? 0xFFFF0000u : 0u);
 #pragma unroll
-      for (int ct = 0; ct < 2; ++ct) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(vb + voff[2 * kt + ct], a0, a1, a2, a3);
-        mma_bf16(acc[ct], a0, a1, a2, a3, bh0, bh1);
-        mma_bf16(acc[ct], a0, a1, a2, a3, bl0, bl1);
+        for (int i = 0; i < 4; ++i) {
+          oA[4 * i] &= mlo;
+          oA[4 * i + 1] &= mlo;
+          oA[4 * i + 2] &= mhi;
+          oA[4 * i + 3] &= mhi;
+          oB[4 * i] &= mlo;
+          oB[4 * i + 1] &= mlo;
+          oB[4 * i + 2] &= mhi;
+          oB[4 * i + 3] &= mhi;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mma_bf16(acc[i], oA[4 * i], oA[4 * i + 1], oA[4 * i + 2], oA[4 * i + 3], h01, h23);
+        mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], h01, h23);
+        mma_bf16(acc[i], oA[4 * i], oA[4 * i + 1], oA[4 * i + 2], oA[4 * i + 3], l01, l23);
+        mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], l01, l23);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.dvEmpty[db]);
   }
-  // ---- the split's partial: l summed over lanes and warps; group 1 hands (m, l, acc) to group 0, which
-  // merges the two with a log-sum-exp and writes the partial
-#pragma unroll
-  for (int d = 4; d < 32; d <<= 1) {
-    l0 += __shfl_xor_sync(kFull, l0, d);
-    l1 += __shfl_xor_sync(kFull, l1, d);
-  }
-  if (g == 0) {
-    sm.wl[gr][2 * tq][w] = l0;
-    sm.wl[gr][2 * tq + 1][w] = l1;
-  }
-  if (gr == kMGroups - 1 && gr > 0) {
-    if (w == 0 && g == 0) {
-      sm.xm[2 * tq] = m0;
-      sm.xm[2 * tq + 1] = m1;
-    }
-#pragma unroll
-    for (int ct = 0; ct < 2; ++ct) {
-      const int cA = 32 * w + 16 * ct + g, cB = cA + 8;
-      sm.xacc[2 * tq][cA] = acc[ct][0];
-      sm.xacc[2 * tq + 1][cA] = acc[ct][1];
-      sm.xacc[2 * tq][cB] = acc[ct][2];
-      sm.xacc[2 * tq + 1][cB] = acc[ct][3];
-    }
-  }
-  named_bar_sync(kBarMAll, kMWarps * 32);
-  if (gr != 0) return;
-  float wt[2][2];  // [head 2tq + i][own group, group 1]
-  float mm[2], ll[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float4 la = *reinterpret_cast<const float4*>(&sm.wl[0][2 * tq + i][0]);
-    const float lown = (la.x + la.y) + (la.z + la.w);
-    const float mo = i ? m1 : m0;
-    if (kMGroups > 1) {
-      const float mx = sm.xm[2 * tq + i];
-      const float M = fmaxf(mo, mx);
-      mm[i] = M;
-      wt[i][0] = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
-      wt[i][1] = mx == -INFINITY ? 0.f : fast_exp2(mx - M);
-      const float4 lb = *reinterpret_cast<const float4*>(&sm.wl[kMGroups - 1][2 * tq + i][0]);
-      ll[i] = wt[i][0] * lown + wt[i][1] * ((lb.x + lb.y) + (lb.z + lb.w));
-    } else {
-      mm[i] = mo;
-      wt[i][0] = 1.f;
-      wt[i][1] = 0.f;
-      ll[i] = lown;
-    }
-  }
-  if (w == 0 && g == 0) {
-    part[4 * tq + 0] = mm[0];
-    part[4 * tq + 1] = ll[0];
-    part[4 * tq + 2] = mm[1];
-    part[4 * tq + 3] = ll[1];
-  }
-  float* pa = part + 2 * kRPad;
-#pragma unroll
-  for (int ct = 0; ct < 2; ++ct) {
-    const int cA = 32 * w + 16 * ct + g, cB = cA + 8;
-    if (kMGroups > 1) {
-      pa[(2 * tq) * kD + cA] = wt[0][0] * acc[ct][0] + wt[0][1] * sm.xacc[2 * tq][cA];
-      pa[(2 * tq + 1) * kD + cA] = wt[1][0] * acc[ct][1] + wt[1][1] * sm.xacc[2 * tq + 1][cA];
-      pa[(2 * tq) * kD + cB] = wt[0][0] * acc[ct][2] + wt[0][1] * sm.xacc[2 * tq][cB];
-      pa[(2 * tq + 1) * kD + cB] = wt[1][0] * acc[ct][3] + wt[1][1] * sm.xacc[2 * tq + 1][cB];
-    } else {
-      pa[(2 * tq) * kD + cA] = acc[ct][0];
-      pa[(2 * tq + 1) * kD + cA] = acc[ct][1];
-      pa[(2 * tq) * kD + cB] = acc[ct][2];
-      pa[(2 * tq + 1) * kD + cB] = acc[ct][3];
-    }
+  lsum += __shfl_xor_sync(kFull, lsum, 1);
+  lsum += __shfl_xor_sync(kFull, lsum, 2);
+  if (tq == 0) {
+    sm.wm[cw][g] = mrun;
+    sm.wl[cw][g] = lsum;
   }
 }
 
@@ -809,41 +598,102 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
     sm.tagl[x] = tag_entry(static_cast<uint32_t>(x));
   }
-  // q of the kv-head's query heads, times 2^-4, channels in decoded order (the B operand of QK^T)
-  for (int x = tid; x < kRPad * kD / 2; x += kAttThreads) {
-    const int n = x / (kD / 2), p = 2 * (x % (kD / 2));  // positions p, p+1 hold channels quad_perm(p), quad_perm(p+1)
-    uint32_t w = 0u;
+  for (int x = tid; x < 4 * kD; x += kAttThreads) {  // [K|V][base3|base4][channel]
+    const int kind = x / (2 * kD), which = (x / kD) & 1, c = x % kD;
+    sm.bases[kind][which][c] = (which ? a.base4 : a.base3)[(kind * a.Hkv + h) * kD + c];
+  }
+  // V unit base words: group i of the lane's unit hv holds channels 16m+g and 16m+g+8 (m = 4hv + i, g =
+  // lane/4) in byte lanes 0, 2 and 1, 3 of both of its exponent words
+  for (int x = tid; x < 32 * 2 * 4; x += kAttThreads) {
+    const int ln = x / 8, hv = (x / 4) % 2, i = x % 4;
+    const int cA = 16 * (4 * hv + i) + ln / 4;
+    const uint8_t* v3 = a.base3 + (a.Hkv + h) * kD;
+    const uint8_t* v4 = a.base4 + (a.Hkv + h) * kD;
+    const uint32_t x3 = v3[cA] | (static_cast<uint32_t>(v3[cA + 8]) << 8);
+    const uint32_t x4 = v4[cA] | (static_cast<uint32_t>(v4[cA + 8]) << 8);
+    sm.vbw[ln][hv][i] = x3 | (x3 << 16);
+    sm.vbw[ln][hv][4 + i] = (x4 | (x4 << 16)) - (x3 | (x3 << 16));
+  }
+  // q of the kv-head's query heads, times 2^-4, as A-operand words of S^T = q K^T: for head g and lane tq,
+  // word m (m < 8) = channels 32tq + 4m + {0, 2}, word 8 + m = channels 32tq + 4m + {1, 3}, stored as
+  // [m2][qa0[2m2], qa0[2m2+1], qa2[2m2], qa2[2m2+1]] so that one 16-byte load serves two k-steps
+  for (int x = tid; x < kRPad * 4 * 16; x += kAttThreads) {
+    const int n = x / 64, tq = (x / 16) % 4, k = x % 16, m2 = k / 4, i = k % 4;
+    const int m = 2 * m2 + (i & 1), odd = i >> 1;  // odd: channels {1, 3} of the quad
+    uint32_t v = 0u;
     if (n < a.r) {
-      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + h * a.r + n) * kD;
-      w = bf16x2_div16(static_cast<uint32_t>(qrow[quad_perm(p)]) | (static_cast<uint32_t>(qrow[quad_perm(p + 1)]) << 16));
+      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + h * a.r + n) * kD + 32 * tq + 4 * m + odd;
+      v = bf16x2_div16(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16));
     }
-    *reinterpret_cast<uint32_t*>(&sm.qs[n][p]) = w;
+    sm.qf[n][tq][k] = v;
   }
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.stFull[s], 1);
-      mbar_init(&sm.stEmpty[s], kDWarps);
-    }
-#pragma unroll
-    for (int d = 0; d < kDecBufs; ++d) {
-      mbar_init(&sm.dkFull[d], kDWarps / 2);
-      mbar_init(&sm.dvFull[d], kDWarps / 2);
-      mbar_init(&sm.dkEmpty[d], kMGroupWarps);
-      mbar_init(&sm.dvEmpty[d], kMGroupWarps);
+      sm.stDone[s] = 0u;
     }
     fence_mbar_init();
+    for (int j = 0; j < min(n_my, kStages); ++j) {  // the first blocks; later ones are issued as stages free up
+      uint2 eK, eV;
+      block_entries(a, b, h, blk0 + j, eK, eV);
+      issue_block(a, sm, j, eK, eV);
+    }
   }
   __syncthreads();
 
   const int r = a.r;
   float* part = a.part + ((static_cast<size_t>(b) * a.Hkv + h) * a.n_splits + split) * kPartFloats;
-  if (warp < kDWarps) {
-    decoder_warp(a, sm, h, blk0, n_my, len, warp / (kDWarps / 2), warp % (kDWarps / 2), lane);
-  } else if (warp < kProducerWarp) {
-    tensor_warp(a, sm, n_my, part, (warp - kMWarp0) / kMGroupWarps, (warp - kMWarp0) % kMGroupWarps, lane);
-  } else if (lane == 0) {
-    producer_lane(a, sm, b, h, blk0, n_my);
+  float acc[8][4];
+  compute_warp(a, sm, b, h, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane, acc);
+  if (tid == 0) {
+    // Every issued copy was waited for by its group; after a timed-out wait,
+    // wait once more (bounded) so that no copy is still landing at exit.
+#pragma unroll 1
+    for (int i = max(0, n_my - kStages); i < n_my; ++i)
+      mbar_wait(&sm.stFull[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
+  }
+  __syncthreads();  // every stage consumed: the ring becomes merge scratch
+  // ---- merge of the compute warps' states: weights 2^(m_w - max_w m_w) per head
+  if (tid < kCWarps * kRPad) {
+    const int cw = tid / kRPad, n = tid % kRPad;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kCWarps; ++i) mx = fmaxf(mx, sm.wm[i][n]);
+    const float mw = sm.wm[cw][n];
+    sm.ww[cw][n] = mw == -INFINITY ? 0.f : fast_exp2(mw - mx);
+    if (cw == 0) {
+      float lt = 0.f;
+#pragma unroll
+      for (int i = 0; i < kCWarps; ++i) {
+        const float mi = sm.wm[i][n];
+        lt += (mi == -INFINITY ? 0.f : fast_exp2(mi - mx)) * sm.wl[i][n];
+      }
+      part[2 * n] = mx;
+      part[2 * n + 1] = lt;
+    }
+  }
+  float* xacc = reinterpret_cast<float*>(sm.stage[0][0]);  // [warp][head][channel]
+  {
+    const int g = lane >> 2, tq = lane & 3;
+    float* xw = xacc + warp * kRPad * kD;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int c0 = 16 * m + g;
+      xw[(2 * tq) * kD + c0] = acc[m][0];
+      xw[(2 * tq + 1) * kD + c0] = acc[m][1];
+      xw[(2 * tq) * kD + c0 + 8] = acc[m][2];
+      xw[(2 * tq + 1) * kD + c0 + 8] = acc[m][3];
+    }
+  }
+  __syncthreads();
+  float* pa = part + 2 * kRPad;
+  for (int x = tid; x < kRPad * kD; x += kAttThreads) {
+    const int n = x / kD;
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kCWarps; ++i) s += sm.ww[i][n] * xacc[i * kRPad * kD + x];
+    pa[x] = s;
   }
 
   // ---------------------------------------------------------------- split merge (final reduction)

@@ -1,10 +1,10 @@
-// Device-side building blocks of the GAAC library: tile format v2 constants,
+// Device-side building blocks of the GAAC library: tile format v3 constants,
 // the packed exponent decoder, status reporting, mbarrier and bulk-copy PTX.
 //
 // Method: "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference
 // on Personal Devices", section 3.1 (base-plus-offset exponent codes, 3-bit /
 // 4-bit / raw groups of eight, sign and mantissa verbatim) and Appendix D
-// (3-bit code plane, 2-bit tags, escape bytes).  The bit layout is format v2 as
+// (3-bit code plane, 2-bit tags, escape bytes).  The bit layout is format v3 as
 // declared in gaac.h.
 #pragma once
 
@@ -20,18 +20,37 @@ constexpr int kTile = 8192;
 constexpr int kOffCode = 8192;
 constexpr int kPlaneBytes = 1024;  // one code plane: 256 words
 constexpr int kOffTag = 11264;
-constexpr int kOffDir = 11520;  // escape directory: 8 x u16, entry w = escape bytes of eighths 0..w
-constexpr int kOffEsc = 11536;  // escape bytes
+constexpr int kOffDir = 11520;  // escape directory: 8 x u16, entry w = n4 | nraw << 9 over eighths 0..w
+constexpr int kOffEsc = 11536;  // escape area: 4-bit escape bytes, then 8 exponent bytes per raw group
 constexpr int kEscCap = 496;
 constexpr int kDirUnits = 32;   // units per directory entry: an eighth = 128 groups = 1024 elements
 constexpr int kSlot = 12032;
 constexpr int kRawBytes = 16384;
 
-// Largest escape stream a tile can carry if every group is raw (5 bytes x 1024).
-constexpr int kEscMaxAnyTile = 5120;
-
 __device__ __forceinline__ void report(int32_t* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------ storage order ----
+
+// V tiles (format v3): element (t, c) of the tile sits at storage position
+//   s = 1024 (2 (t/16) + c/64) + 32 (4 (c%8) + (t%8)/2) + 8 ((c/16)%4) + r,
+//   r = (c%16)/8 + 2 (t%2) + 4 ((t%16)/8),
+// so that unit 32 (2w + h) + 4g + q holds, for the 16-channel blocks
+// 4h..4h+3, channels 16m+g and 16m+g+8 at tokens 16w + 2q + {0, 1, 8, 9}: one
+// lane's share of a 16 x 16 (channels x tokens) tensor-core operand tile.  K
+// tiles are token-major (s = t*128 + c).
+__device__ __forceinline__ int v_storage_index(int t, int c) {
+  return 1024 * (2 * (t >> 4) + (c >> 6)) + 32 * (4 * (c & 7) + ((t & 7) >> 1)) + 8 * ((c >> 4) & 3) +
+         ((c >> 3) & 1) + 2 * (t & 1) + 4 * ((t >> 3) & 1);
+}
+__device__ __forceinline__ int v_token_of(int s) {
+  const int u = s >> 5, r = s & 7;
+  return 16 * (u >> 6) + 8 * (r >> 2) + 2 * (u & 3) + ((r >> 1) & 1);
+}
+__device__ __forceinline__ int v_channel_of(int s) {
+  const int u = s >> 5, r = s & 7;
+  return 16 * (4 * ((u >> 5) & 1) + ((s >> 3) & 3)) + 8 * (r & 1) + ((u >> 2) & 7);
 }
 
 // ---------------------------------------------------------------- codec ----
@@ -49,29 +68,40 @@ __device__ __forceinline__ void extract_codes(uint32_t wh, uint32_t w2, int h, u
 // Bit i of a 4-bit value moved to bit 0 of byte lane i.
 __device__ __forceinline__ uint32_t spread4(uint32_t n) { return (n * 0x00204081u) & 0x01010101u; }
 
-// Escape bytes of 16 two-bit group tags (tag 1 -> 1 byte, tag 2 -> 5 bytes, 0 and 3 -> 0).
-__device__ __forceinline__ int esc_count(uint32_t tags) {
-  const uint32_t lo = tags & 0x55555555u, hi = (tags >> 1) & 0x55555555u;
-  return __popc(lo & ~hi) + 5 * __popc(hi & ~lo);
+// Group counts of 16 two-bit tags: 4-bit groups (tag 1), raw groups (tag 2),
+// reserved tags (3).
+__device__ __forceinline__ int n4_of(uint32_t tags) {
+  return __popc(tags & 0x55555555u & ~((tags >> 1) & 0x55555555u));
+}
+__device__ __forceinline__ int nraw_of(uint32_t tags) {
+  return __popc((tags >> 1) & 0x55555555u & ~tags);
+}
+__device__ __forceinline__ bool reserved_in(uint32_t tags) { return (tags & (tags >> 1) & 0x55555555u) != 0u; }
+
+// Table entry x: the escape byte x of a 4-bit group spread over two exponent
+// words, bit j of x becoming bit 3 of byte lane j%4 of word j/4.
+__device__ __forceinline__ uint2 spread_entry(uint32_t x) {
+  return make_uint2(spread4(x & 15u) << 3, spread4(x >> 4) << 3);
 }
 
-// Exponent bytes of one half-unit (two groups).  tagnib: the two groups' tags
-// (bits 0-1 first group).  b3/b4: base bytes of the 16 elements, laid out like
-// the codes.  esc: escape area of the slot; esc_off: escape offset of the first
-// group; esc_len: escape bytes present.  Sets *bad on a reserved tag or an
-// escape read past esc_len.
-__device__ __forceinline__ void half_exponents(uint32_t wh, uint32_t w2, int h, uint32_t tagnib,
-                                               const uint32_t b3[4], const uint32_t b4[4],
-                                               const uint8_t* esc, int esc_off, int esc_len,
-                                               uint32_t e[4], bool* bad) {
+// Four bytes of a slot image at any byte offset `off` (4-byte aligned image);
+// reads no word past the one holding byte off + 3.
+__device__ __forceinline__ uint32_t load_u32_any(const uint8_t* img, int off) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(img + (off & ~3));
+  return (off & 3) ? __funnelshift_r(w[0], w[1], 8 * (off & 3)) : w[0];
+}
+
+// Exponent words of one half-unit (two groups of eight), format v3.  tagnib:
+// the two groups' tags (bits 0-1 first group); b3/b4: base bytes laid out like
+// the codes; img: the slot image; *o4: the 4-bit escape byte of the half's
+// first 4-bit group (advanced past the half's 4-bit groups); *oraw: escape
+// offset of the half's first raw group's exponents (advanced by 8 per raw
+// group).  Sets *bad on a reserved tag or a read past esc_len (reads as 0).
+__device__ __forceinline__ void half_exponents_v3(uint32_t wh, uint32_t w2, int h, uint32_t tagnib,
+                                                  const uint32_t b3[4], const uint32_t b4[4], const uint8_t* img,
+                                                  int* o4, int* oraw, int esc_len, uint32_t e[4], bool* bad) {
   uint32_t c[4];
   extract_codes(wh, w2, h, c);
-  if (tagnib == 0u) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) e[q] = b3[q] + c[q];
-    return;
-  }
-  int off = esc_off;
 #pragma unroll
   for (int gi = 0; gi < 2; ++gi) {
     const uint32_t m = (tagnib >> (2 * gi)) & 3u;
@@ -80,118 +110,20 @@ __device__ __forceinline__ void half_exponents(uint32_t wh, uint32_t w2, int h, 
       e[q0] = b3[q0] + c[q0];
       e[q0 + 1] = b3[q0 + 1] + c[q0 + 1];
     } else if (m == 1u) {
-      const bool in = off + 1 <= esc_len;  // never read past the escape bytes present
+      const bool in = *o4 < esc_len;
       if (!in) *bad = true;
-      const uint32_t x = in ? esc[off] : 0u;
+      const uint32_t x = in ? img[kOffEsc + *o4] : 0u;
       e[q0] = b4[q0] + (c[q0] | (spread4(x & 15u) << 3));
       e[q0 + 1] = b4[q0 + 1] + (c[q0 + 1] | (spread4(x >> 4) << 3));
-      off += 1;
+      *o4 += 1;
     } else {
-      const bool in = off + 5 <= esc_len;
-      if (m == 3u || !in) *bad = true;
-      uint32_t hi0 = 0, hi1 = 0;
-#pragma unroll
-      for (int k = 0; k < 5; ++k) {
-        const uint32_t x = in ? esc[off + k] : 0u;
-        hi0 |= spread4(x & 15u) << (3 + k);
-        hi1 |= spread4(x >> 4) << (3 + k);
-      }
-      e[q0] = c[q0] | hi0;
-      e[q0 + 1] = c[q0 + 1] | hi1;
-      off += 5;
+      const bool in = m == 2u && *oraw + 8 <= esc_len;
+      if (!in) *bad = true;
+      e[q0] = in ? load_u32_any(img, kOffEsc + *oraw) : 0u;
+      e[q0 + 1] = in ? load_u32_any(img, kOffEsc + *oraw + 4) : 0u;
+      *oraw += 8;
     }
   }
-}
-
-// Table entry x: the escape byte x of a 4-bit group spread over two exponent
-// words, bit j of x becoming bit 3 of byte lane j%4 of word j/4.
-__device__ __forceinline__ uint2 spread_entry(uint32_t x) {
-  return make_uint2(spread4(x & 15u) << 3, spread4(x >> 4) << 3);
-}
-
-// Escape bytes of a group with tag m (0: 0, 1: 1, 2: 5; tag 3 counts 6 and is
-// rejected by the caller).
-__device__ __forceinline__ int esc_of_tag(uint32_t m) { return static_cast<int>((m & 1u) + 5u * (m >> 1)); }
-
-// Exponent bytes of one half-unit (two groups of eight), without per-lane
-// branches for the 3-bit and 4-bit modes.  tagnib: the two groups' tags (bits
-// 0-1 first group); b3/b4: base bytes laid out like the codes; esc: escape area
-// of the slot image (esc_len bytes valid); off: escape offset of the first
-// group; lut: 256 spread_entry values.  Raw-mode groups take a rare branch.
-// Sets *bad on a reserved tag or an escape read past esc_len (such bytes read as 0).
-__device__ __forceinline__ void half_exponents_fast(uint32_t wh, uint32_t w2, int h, uint32_t tagnib,
-                                                    const uint32_t b3[4], const uint32_t b4[4],
-                                                    const uint8_t* esc, int off, int esc_len, const uint2* lut,
-                                                    uint32_t e[4], bool* bad) {
-  uint32_t c[4];
-  extract_codes(wh, w2, h, c);
-  const uint32_t m0 = tagnib & 3u, m1 = (tagnib >> 2) & 3u;
-  const int off1 = off + esc_of_tag(m0);
-  const uint32_t x0 = (m0 == 1u && off < esc_len) ? esc[off] : 0u;
-  const uint32_t x1 = (m1 == 1u && off1 < esc_len) ? esc[off1] : 0u;
-  const uint2 s0 = lut[x0], s1 = lut[x1];
-  e[0] = (m0 != 0u ? b4[0] : b3[0]) + c[0] + s0.x;
-  e[1] = (m0 != 0u ? b4[1] : b3[1]) + c[1] + s0.y;
-  e[2] = (m1 != 0u ? b4[2] : b3[2]) + c[2] + s1.x;
-  e[3] = (m1 != 0u ? b4[3] : b3[3]) + c[3] + s1.y;
-  if ((m0 == 1u && off >= esc_len) || (m1 == 1u && off1 >= esc_len)) *bad = true;
-  if (tagnib & 0xAu) {  // a raw-mode (or reserved) group: five escape bit planes
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      const uint32_t m = gi == 0 ? m0 : m1;
-      if (m >= 2u) {
-        const int o = gi == 0 ? off : off1;
-        const bool in = m == 2u && o + 5 <= esc_len;
-        if (!in) *bad = true;
-        uint32_t hi0 = 0, hi1 = 0;
-#pragma unroll
-        for (int k = 0; k < 5; ++k) {
-          const uint32_t x = in ? esc[o + k] : 0u;
-          hi0 |= spread4(x & 15u) << (3 + k);
-          hi1 |= spread4(x >> 4) << (3 + k);
-        }
-        e[2 * gi] = c[2 * gi] | hi0;
-        e[2 * gi + 1] = c[2 * gi + 1] | hi1;
-      }
-    }
-  }
-}
-
-// Exponent bytes of one half-unit when the 4-bit-mode escape bytes of its unit
-// have been gathered in advance: xw holds, in byte j, the escape byte of group j
-// of the unit (0 unless that group is in 4-bit mode).  tb: the unit's tag byte;
-// hh: which half.  Raw-mode groups are left for the caller (their words come out
-// as base4 + code).  The tile must have been validated (no reserved tags).
-__device__ __forceinline__ void half_exponents_gathered(uint32_t wh, uint32_t w2, int hh, uint32_t tb, uint32_t xw,
-                                                        const uint32_t b3[4], const uint32_t b4[4],
-                                                        const uint2* lut, uint32_t e[4]) {
-  uint32_t c[4];
-  extract_codes(wh, w2, hh, c);
-  const uint32_t tagnib = (tb >> (4 * hh)) & 15u;
-  const uint32_t xs = xw >> (16 * hh);
-  const uint2 s0 = lut[xs & 0xFFu], s1 = lut[(xs >> 8) & 0xFFu];
-  const bool w0 = (tagnib & 3u) != 0u, w1 = (tagnib & 12u) != 0u;
-  e[0] = (w0 ? b4[0] : b3[0]) + c[0] + s0.x;
-  e[1] = (w0 ? b4[1] : b3[1]) + c[1] + s0.y;
-  e[2] = (w1 ? b4[2] : b3[2]) + c[2] + s1.x;
-  e[3] = (w1 ? b4[3] : b3[3]) + c[3] + s1.y;
-}
-
-// Raw-mode group gi (0/1) of a half-unit: exponent words from the group's five
-// escape bit planes at `esc` (already offset to the group).
-__device__ __forceinline__ void raw_group_exponents(uint32_t wh, uint32_t w2, int hh, int gi, const uint8_t* esc,
-                                                    uint32_t e[4]) {
-  uint32_t c[4];
-  extract_codes(wh, w2, hh, c);
-  uint32_t hi0 = 0, hi1 = 0;
-#pragma unroll
-  for (int k = 0; k < 5; ++k) {
-    const uint32_t x = esc[k];
-    hi0 |= spread4(x & 15u) << (3 + k);
-    hi1 |= spread4(x >> 4) << (3 + k);
-  }
-  e[2 * gi] = c[2 * gi] | hi0;
-  e[2 * gi + 1] = c[2 * gi + 1] | hi1;
 }
 
 // Four BF16 values from their sign|mantissa bytes and exponent bytes (byte

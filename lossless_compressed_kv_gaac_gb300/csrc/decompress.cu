@@ -32,7 +32,7 @@ struct DecompressArgs {
 // grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
 __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs a) {
   __shared__ alignas(16) uint16_t logical[kBlock * kD];  // [t][c]
-  __shared__ int word_prefix[64];
+  __shared__ int word_prefix[65];
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
   const int blk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, u = tid;
@@ -67,8 +67,9 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
   } else {
     const uint8_t* slot = a.slot_pool + static_cast<size_t>(ent.index) * kSlot;
     const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + kOffTag);
-    if (tid < 32) {  // exclusive prefix of escape bytes over the 64 tag words
-      const int c0 = esc_count(tagw[tid]), c1 = esc_count(tagw[tid + 32]);
+    if (tid < 32) {  // exclusive prefixes of 4-bit and raw group counts over the 64 tag words (packed)
+      const int c0 = n4_of(tagw[tid]) | (nraw_of(tagw[tid]) << 16);
+      const int c1 = n4_of(tagw[tid + 32]) | (nraw_of(tagw[tid + 32]) << 16);
       int i0 = c0, i1 = c1;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -81,21 +82,26 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
       const int tot0 = __shfl_sync(0xFFFFFFFFu, i0, 31);
       word_prefix[tid] = i0 - c0;
       word_prefix[tid + 32] = tot0 + i1 - c1;
+      if (tid == 31) word_prefix[64] = tot0 + i1;  // tile totals
     }
     __syncthreads();
     const uint32_t* cw = reinterpret_cast<const uint32_t*>(slot + kOffCode);
     const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
     const uint32_t tagbyte = slot[kOffTag + u];
     const uint32_t tword = tagw[u >> 2];
-    const int esc_unit = word_prefix[u >> 2] + esc_count(tword & ((1u << (8 * (u & 3))) - 1u));
-    // The escape directory must hold the prefix at each quarter boundary and the total.
+    const uint32_t before = tword & ((1u << (8 * (u & 3))) - 1u);  // tags of the word's earlier units
+    const int pre = word_prefix[u >> 2] + (n4_of(before) | (nraw_of(before) << 16));
+    const int tot = word_prefix[64];
+    const int tot4 = tot & 0xFFFF, totraw = tot >> 16;
+    int o4 = pre & 0xFFFF, oraw = tot4 + 8 * (pre >> 16);
+    // The escape directory must hold the counts at each eighth boundary and the totals.
     const uint16_t* dir = reinterpret_cast<const uint16_t*>(slot + kOffDir);
-    bool bad = false;
-    if ((u & (kDirUnits - 1)) == 0 && u > 0 && dir[u / kDirUnits - 1] != esc_unit) bad = true;
-    if (u == 255) {
-      const int total = esc_unit + esc_count(tagbyte);
-      if (dir[7] != total || total != ent.esc_len) bad = true;
-    }
+    bool bad = reserved_in(tagbyte);
+    if ((u & (kDirUnits - 1)) == 0 && u > 0 &&
+        dir[u / kDirUnits - 1] != (((pre & 0xFFFF) & 0x1FF) | (((pre >> 16) & 0x7F) << 9)))
+      bad = true;
+    if (u == 255 && (dir[7] != ((tot4 & 0x1FF) | ((totraw & 0x7F) << 9)) || tot4 + 8 * totraw != ent.esc_len))
+      bad = true;
     const uint4* smp = reinterpret_cast<const uint4*>(slot + 32 * u);
     const uint4 s0 = smp[0], s1 = smp[1];
     uint32_t smw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
@@ -115,15 +121,19 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
           const int c = 32 * (u & 3) + 16 * hh + 4 * q;
           b3[q] = *reinterpret_cast<const uint32_t*>(b3g + c);
           b4[q] = *reinterpret_cast<const uint32_t*>(b4g + c);
-        } else {  // V: one channel per unit
-          b3[q] = 0x01010101u * b3g[u >> 1];
-          b4[q] = 0x01010101u * b4g[u >> 1];
+        } else {  // V: element 4q+L of half hh is storage element 32u + 16hh + 4q + L
+          b3[q] = b4[q] = 0u;
+#pragma unroll
+          for (int L = 0; L < 4; ++L) {
+            const int c = v_channel_of(32 * u + 16 * hh + 4 * q + L);
+            b3[q] |= static_cast<uint32_t>(b3g[c]) << (8 * L);
+            b4[q] |= static_cast<uint32_t>(b4g[c]) << (8 * L);
+          }
         }
       }
-      const int esc_off = esc_unit + (hh == 0 ? 0 : esc_count(tagbyte & 15u));
       uint32_t e[4];
-      half_exponents(hh == 0 ? W0 : W1, W2, hh, (tagbyte >> (4 * hh)) & 15u, b3, b4, slot + kOffEsc, esc_off,
-                     ent.esc_len, e, &bad);
+      half_exponents_v3(hh == 0 ? W0 : W1, W2, hh, (tagbyte >> (4 * hh)) & 15u, b3, b4, slot, &o4, &oraw,
+                        ent.esc_len, e, &bad);
 #pragma unroll
       for (int q = 0; q < 4; ++q) join_bf16x4(smw[4 * hh + q], e[q], pairs[8 * hh + 2 * q], pairs[8 * hh + 2 * q + 1]);
     }
@@ -135,11 +145,11 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[i] = make_uint4(pairs[4 * i], pairs[4 * i + 1], pairs[4 * i + 2], pairs[4 * i + 3]);
   } else {
-    const int c = u >> 1, t0 = 32 * (u & 1);
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-      logical[(t0 + 2 * m) * kD + c] = static_cast<uint16_t>(pairs[m] & 0xFFFFu);
-      logical[(t0 + 2 * m + 1) * kD + c] = static_cast<uint16_t>(pairs[m] >> 16);
+      const int s0 = 32 * u + 2 * m;
+      logical[v_token_of(s0) * kD + v_channel_of(s0)] = static_cast<uint16_t>(pairs[m] & 0xFFFFu);
+      logical[v_token_of(s0 + 1) * kD + v_channel_of(s0 + 1)] = static_cast<uint16_t>(pairs[m] >> 16);
     }
   }
   __syncthreads();

@@ -12,7 +12,7 @@
 //
 // One CTA of 256 threads encodes one tile; thread u owns the 32-element code
 // unit u (storage elements 32u..32u+31), i.e. exactly one tag byte and one
-// word of each code plane.
+// word of each code plane.  Tile layout: format v3 (gaac.h).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -29,8 +29,8 @@ struct EncShared {
   int ok;
 };
 
-// Channel of storage element s (format v2).
-__device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? (s & 127) : (s >> 6); }
+// Channel of storage element s (format v3).
+__device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? (s & 127) : v_channel_of(s); }
 
 // Encodes the tile in sh->tile into `slot` (global, 16-byte aligned) unless its
 // escape stream exceeds the capacity.  Returns the escape length, or -1 when
@@ -57,12 +57,13 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
 
   uint32_t code[32];
   uint32_t smb[8];  // sign|mantissa bytes, 4 per word
-  uint32_t escw[5] = {0, 0, 0, 0, 0};  // up to 20 escape bytes, little-endian
-  int nesc = 0;
+  uint32_t esc4 = 0;  // the unit's 4-bit escape bytes, little-endian, in group order
+  uint32_t ew[8];     // exponent bytes of the 32 elements, 4 per word
+  int n4 = 0, nraw = 0;
   uint32_t tagbyte = 0;
   int my_counts[3] = {0, 0, 0};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) smb[j] = 0;
+  for (int j = 0; j < 8; ++j) smb[j] = ew[j] = 0;
 
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
@@ -73,6 +74,7 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
       const int el = 8 * gi + j;
       const uint32_t x = (xw[el >> 1] >> (16 * (el & 1))) & 0xFFFFu;
       e[j] = (x >> 7) & 0xFF;
+      ew[el >> 2] |= static_cast<uint32_t>(e[j]) << (8 * (el & 3));
       const uint32_t sm = ((x >> 8) & 0x80u) | (x & 0x7Fu);
       smb[el >> 2] |= sm << (8 * (el & 3));
       const int c = channel_of(kind, 32 * u + el);
@@ -85,38 +87,30 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
     const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
     tagbyte |= mode << (2 * gi);
     my_counts[mode] += 1;
-    uint32_t eb[5] = {0, 0, 0, 0, 0};
+    uint32_t eb = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      uint32_t cd;
+      uint32_t cd = 0;  // raw groups keep code 0: their exponents are escape bytes
       if (mode == 0u) {
         cd = static_cast<uint32_t>(e[j] - b3[j]) & 7u;
       } else if (mode == 1u) {
         const uint32_t off = static_cast<uint32_t>(e[j] - b4[j]) & 0xFFu;
         cd = off & 7u;
-        eb[0] |= ((off >> 3) & 1u) << j;
-      } else {
-        cd = static_cast<uint32_t>(e[j]) & 7u;
-#pragma unroll
-        for (int k = 0; k < 5; ++k) eb[k] |= ((static_cast<uint32_t>(e[j]) >> (3 + k)) & 1u) << j;
+        eb |= ((off >> 3) & 1u) << j;
       }
       code[8 * gi + j] = cd;
     }
-    const int nb = mode == 0u ? 0 : (mode == 1u ? 1 : 5);
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-      if (k < nb) {
-        const int at = nesc + k;  // < 20
-#pragma unroll
-        for (int w = 0; w < 5; ++w)
-          if ((at >> 2) == w) escw[w] |= eb[k] << (8 * (at & 3));
-      }
+    if (mode == 1u) {
+      esc4 |= eb << (8 * n4);
+      n4 += 1;
     }
-    nesc += nb;
+    if (mode == 2u) nraw += 1;
   }
 
-  // Exclusive scan of the escape byte counts over the CTA (unit order = group order).
-  int incl = nesc;
+  // Exclusive scans over the CTA (unit order = group order) of the 4-bit and
+  // raw group counts, packed in one word (each total is at most 1024).
+  const int packed = n4 | (nraw << 16);
+  int incl = packed;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
@@ -131,10 +125,13 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
     if (w < warp) before += s;
     total += s;
   }
-  const int off = before + incl - nesc;
-  if (total > kEscCap || slot == nullptr) return -1;
+  const int excl = before + incl - packed;
+  const int off4 = excl & 0xFFFF, offraw = excl >> 16;
+  const int tot4 = total & 0xFFFF, totraw = total >> 16;
+  const int esc = tot4 + 8 * totraw;
+  if (esc > kEscCap || slot == nullptr) return -1;
 
-  // Code plane words of this unit (format v2 placement).
+  // Code plane words of this unit (format v3 placement, as v1).
   uint32_t W[3] = {0, 0, 0};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -161,16 +158,28 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
   cw[256 + u] = W[1];
   cw[512 + u] = W[2];
   slot[kOffTag + u] = static_cast<uint8_t>(tagbyte);
-  for (int k = 0; k < nesc; ++k) slot[kOffEsc + off + k] = static_cast<uint8_t>(escw[k >> 2] >> (8 * (k & 3)));
+  uint8_t* escp = slot + kOffEsc;
+  for (int k = 0; k < n4; ++k) escp[off4 + k] = static_cast<uint8_t>(esc4 >> (8 * k));
+  if (nraw) {  // raw groups: their eight exponents, after all 4-bit escape bytes of the tile
+    int r = tot4 + 8 * offraw;
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      if (((tagbyte >> (2 * gi)) & 3u) != 2u) continue;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) escp[r + j] = static_cast<uint8_t>(ew[2 * gi + (j >> 2)] >> (8 * (j & 3)));
+      r += 8;
+    }
+  }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int at = 2 * u + i;  // 0..511
-    if (at >= total && at < kEscCap) slot[kOffEsc + at] = 0;
+    if (at >= esc && at < kEscCap) escp[at] = 0;
   }
   if ((u & (kDirUnits - 1)) == kDirUnits - 1) {  // directory entry of eighth u / 32
-    const int w = u / kDirUnits, end = off + nesc;
-    slot[kOffDir + 2 * w] = static_cast<uint8_t>(end & 0xFF);
-    slot[kOffDir + 2 * w + 1] = static_cast<uint8_t>(end >> 8);
+    const int w = u / kDirUnits;
+    const uint32_t entry = ((off4 + n4) & 0x1FF) | (((offraw + nraw) & 0x7F) << 9);
+    slot[kOffDir + 2 * w] = static_cast<uint8_t>(entry & 0xFFu);
+    slot[kOffDir + 2 * w + 1] = static_cast<uint8_t>(entry >> 8);
   }
   if (stats != nullptr) {
 #pragma unroll
@@ -181,11 +190,11 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
 #pragma unroll
       for (int m = 0; m < 3; ++m)
         atomicAdd(&stats->groups[m], static_cast<unsigned long long>(sh->mode_counts[m]));
-      atomicAdd(&stats->escape_bytes, static_cast<unsigned long long>(total));
+      atomicAdd(&stats->escape_bytes, static_cast<unsigned long long>(esc));
       atomicAdd(&stats->slot_tiles, 1ull);
     }
   }
-  return total;
+  return esc;
 }
 
 __device__ __forceinline__ gaac_entry make_entry(uint32_t index, int esc, int mode, int n_tok) {
@@ -271,8 +280,8 @@ __global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int c = 32 * part + 2 * i;
-        sh.tile[c * kBlock + t] = static_cast<uint16_t>(ws[i] & 0xFFFFu);
-        sh.tile[(c + 1) * kBlock + t] = static_cast<uint16_t>(ws[i] >> 16);
+        sh.tile[v_storage_index(t, c)] = static_cast<uint16_t>(ws[i] & 0xFFFFu);
+        sh.tile[v_storage_index(t, c + 1)] = static_cast<uint16_t>(ws[i] >> 16);
       }
     }
   }
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   }
   if (tid < kD) {
     const uint16_t x = (kind == 0 ? a.k_new : a.v_new)[(static_cast<size_t>(b) * a.n_kv_heads + h) * kD + tid];
-    raw[kind == 0 ? pos * kD + tid : tid * kBlock + pos] = x;
+    raw[kind == 0 ? pos * kD + tid : v_storage_index(pos, tid)] = x;
   }
   if (pos + 1 < kBlock) {
     if (tid == 0) *ep = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, pos + 1);

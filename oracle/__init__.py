@@ -108,6 +108,9 @@ def calibrate(x) -> tuple[np.ndarray, np.ndarray]:
     return b3, b4
 
 
+FULL_ESC = 8 * 1024  # every group raw: the largest escape stream a tile can have
+
+
 def encode_tile(tile, kind: int, base3, base4, forced=None, esc_cap: int = ESC_CAP):
     """Encode a [64][128] BF16 tile.  Returns (image uint8 [11536+esc_cap], esc_len);
     esc_len (escape bytes, the directory not counted) is -1 when the escape

@@ -21,13 +21,15 @@
  *     then finalized.
  *   - Appendix D, Table 9 (Storage): 3-bit exponent codes, 2-bit mode tags,
  *     escape bytes, fixed-capacity escape slots.
- * The page gives no bit layout.  This file fixes one, "GAAC tile format v2",
+ * The page gives no bit layout.  This file fixes one, "GAAC tile format v3",
  * summarised below and spelled out rule by rule at the step that follows it.
  *
- * Format v2 in brief (all multi-byte fields little-endian):
+ * Format v3 in brief (all multi-byte fields little-endian):
  *   tile        64 tokens x 128 channels of one (sequence, block, kv-head, K|V)
  *   storage     K tiles: element (t,c) at s = t*128 + c   (token-major)
- *   order       V tiles: element (t,c) at s = c*64  + t   (channel-major)
+ *   order       V tiles: the operand order of storage_index below (a
+ *               32-element unit holds 2 channels x 4 tokens of each of four
+ *               16-channel blocks)
  *   group       8 consecutive elements in storage order, G = s / 8
  *   eighth      128 consecutive groups (1024 elements), w = G / 128
  *   slot image  [0,8192)      mantissa of element s in bits 0-6 of byte s; bit 7
@@ -36,9 +38,13 @@
  *                             inside each aligned group of four)
  *               [8192,11264)  code plane: 3 words per 32-element unit
  *               [11264,11520) tag plane: 2 bits per group
- *               [11520,11536) escape directory: 8 u16, entry w = escape bytes
- *                             of eighths 0..w
- *               [11536,12032) escape bytes, capacity 496, zero filled
+ *               [11520,11536) escape directory: 8 u16; entry w = (4-bit groups
+ *                             of eighths 0..w) | (raw groups of eighths 0..w) << 9
+ *                             (each count modulo its field: 9 and 7 bits; exact
+ *                             whenever the escape area fits 496 bytes)
+ *               [11536,12032) escape area, capacity 496, zero filled: first one
+ *                             byte per 4-bit group, then eight exponent bytes
+ *                             per raw group, each in group order
  *   raw tile    8192 BF16 words in storage order
  */
 #include <math.h>
@@ -68,19 +74,34 @@ static uint16_t bf16_join(unsigned signmant, unsigned exponent) {
     return (uint16_t)(((signmant & 0x80u) << 8) | ((exponent & 0xFFu) << 7) | (signmant & 0x7Fu));
 }
 
-/* ---- sign|mantissa plane (format v2): byte s keeps the mantissa of element s
+/* ---- sign|mantissa plane (format v3, as v2): byte s keeps the mantissa of element s
  * and the sign of element sign_source(s), the previous element of the same
  * aligned group of four, cyclically (byte 4i holds the sign of 4i+3). */
 static int sign_source(int s) { return 4 * (s / 4) + (s + 3) % 4; }
 static int sign_holder(int s) { return 4 * (s / 4) + (s + 1) % 4; }
 
-/* ---- storage order of a tile (format v1) */
+/* ---- storage order of a tile (format v3)
+ * K: token-major, s = t*128 + c.
+ * V: s = 1024*(2*w + h) + 32*(4*g + q) + 8*i + r with
+ *      w = t / 16            (quarter of the block's tokens)
+ *      q = (t % 8) / 2,  r bit 1 = t % 2,  r bit 2 = (t % 16) / 8
+ *      h = c / 64,  i = (c / 16) % 4,  g = c % 8,  r bit 0 = (c % 16) / 8
+ * so that unit 32*(2w+h) + 4g + q holds, for the four 16-channel blocks
+ * 4h..4h+3, channels 16m+g and 16m+g+8 at tokens 16w + 2q + {0,1,8,9}: the
+ * elements one lane of a 16x16 operand tile of a tensor-core product over
+ * (channels x tokens) holds.  A group (r = 0..7) is two channels x four tokens. */
 int gaac_ref_storage_index(int kind, int t, int c) {
-    return kind == ORC_KIND_K ? t * ORC_D + c : c * ORC_BLOCK + t;
+    if (kind == ORC_KIND_K) return t * ORC_D + c;
+    int w = t / 16, q = (t % 8) / 2, h = c / 64, i = (c / 16) % 4, g = c % 8;
+    int r = (c % 16) / 8 + 2 * (t % 2) + 4 * ((t % 16) / 8);
+    return 1024 * (2 * w + h) + 32 * (4 * g + q) + 8 * i + r;
 }
 static void storage_to_tc(int kind, int s, int* t, int* c) {
-    if (kind == ORC_KIND_K) { *t = s / ORC_D; *c = s % ORC_D; }
-    else { *c = s / ORC_BLOCK; *t = s % ORC_BLOCK; }
+    if (kind == ORC_KIND_K) { *t = s / ORC_D; *c = s % ORC_D; return; }
+    int u = s / 32, j = s % 32, eighth = u / 32, lane = u % 32;
+    int w = eighth / 2, h = eighth % 2, g = lane / 4, q = lane % 4, i = j / 8, r = j % 8;
+    *t = 16 * w + 8 * (r >> 2) + 2 * q + ((r >> 1) & 1);
+    *c = 16 * (4 * h + i) + 8 * (r & 1) + g;
 }
 static int channel_of(int kind, int s) { int t, c; storage_to_tc(kind, s, &t, &c); return c; }
 
@@ -115,7 +136,7 @@ void gaac_ref_calibrate(const uint16_t* x, int64_t n_tok, int64_t tok_stride, in
     }
 }
 
-/* ---- code plane location of code bit `bit` (0..2) of element s (format v1).
+/* ---- code plane location of code bit `bit` (0..2) of element s (format v3, as v1).
  * Unit u = s/32 owns words W0(u), W1(u), W2(u), word Wk(u) stored at byte
  * offset 8192 + 4*(k*256 + u).  Within the unit, j = s%32, half h = j/16,
  * jj = j%16, byte lane L = jj%4, quad q = jj/4:
@@ -173,7 +194,7 @@ static unsigned choose_mode(const unsigned* e, const unsigned* b3, const unsigne
     return fits3 ? ORC_M3BIT : (fits4 ? ORC_M4BIT : ORC_MRAW);
 }
 
-static int escape_bytes_of_mode(unsigned mode) { return mode == ORC_M3BIT ? 0 : (mode == ORC_M4BIT ? 1 : 5); }
+static int escape_bytes_of_mode(unsigned mode) { return mode == ORC_M3BIT ? 0 : (mode == ORC_M4BIT ? 1 : 8); }
 int gaac_ref_escape_bytes_of_mode(int mode) { return escape_bytes_of_mode((unsigned)mode); }
 
 /*
@@ -184,6 +205,10 @@ int gaac_ref_escape_bytes_of_mode(int mode) { return escape_bytes_of_mode((unsig
  * Returns the escape length in bytes (escape bytes only, the directory not
  * counted), or -1 if it exceeds img_esc_cap (the image is then incomplete).
  * Unused escape bytes stay zero.
+ *
+ * Codes: 3-bit group: e - base3; 4-bit group: (e - base4) & 7, with bit 3 of
+ * element j's offset in bit j of the group's escape byte; raw group: code 0,
+ * the eight exponents as eight escape bytes in element order.
  */
 int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, const uint8_t* base4,
                          const uint8_t* forced, uint8_t* img, int img_esc_cap) {
@@ -195,7 +220,9 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
     for (int s = 0; s < ORC_TILE; ++s)
         img[s] = (uint8_t)((bf16_signmant(seq[s]) & 0x7Fu) | (bf16_signmant(seq[sign_source(s)]) & 0x80u));
 
-    int esc = 0;
+    /* pass 1: every group's mode; the raw bytes follow all 4-bit bytes */
+    unsigned modes[ORC_GROUPS];
+    int n4 = 0, nraw = 0;
     for (int G = 0; G < ORC_GROUPS; ++G) {
         unsigned e[8], b3[8], b4[8];
         for (int j = 0; j < 8; ++j) {
@@ -204,31 +231,40 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
             b3[j] = base3[channel_of(kind, s)];
             b4[j] = base4[channel_of(kind, s)];
         }
-        unsigned mode = forced ? forced[G] : choose_mode(e, b3, b4);
+        modes[G] = forced ? forced[G] : choose_mode(e, b3, b4);
+        if (modes[G] == ORC_M4BIT) n4 += 1;
+        if (modes[G] == ORC_MRAW) nraw += 1;
+    }
+    int esc = n4 + 8 * nraw;
+    if (esc > img_esc_cap) return -1;
+
+    /* pass 2: tags, codes, escape bytes, directory */
+    int at4 = 0, atraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = modes[G];
         put_tag(img, G, mode);
-        uint8_t escb[5] = {0, 0, 0, 0, 0};
+        uint8_t esc4 = 0;
         for (int j = 0; j < 8; ++j) {
-            unsigned code;
+            int s = 8 * G + j;
+            unsigned e = bf16_exponent(seq[s]), code = 0;
             if (mode == ORC_M3BIT) {
-                code = (e[j] - b3[j]) & 7u;
+                code = (e - base3[channel_of(kind, s)]) & 7u;
             } else if (mode == ORC_M4BIT) {
-                unsigned off = (e[j] - b4[j]) & 0xFFu;
+                unsigned off = (e - base4[channel_of(kind, s)]) & 0xFFu;
                 code = off & 7u;
-                escb[0] |= (uint8_t)(((off >> 3) & 1u) << j);
+                esc4 |= (uint8_t)(((off >> 3) & 1u) << j);
             } else {
-                code = e[j] & 7u;
-                for (int k = 0; k < 5; ++k) escb[k] |= (uint8_t)(((e[j] >> (3 + k)) & 1u) << j);
+                img[ORC_OFF_ESC + n4 + 8 * atraw + j] = (uint8_t)e;
             }
-            put_code(img, 8 * G + j, code);
+            put_code(img, s, code);
         }
-        int nb = escape_bytes_of_mode(mode);
-        if (esc + nb > img_esc_cap) return -1;
-        for (int k = 0; k < nb; ++k) img[ORC_OFF_ESC + esc + k] = escb[k];
-        esc += nb;
-        if ((G + 1) % ORC_DIR_GROUPS == 0) {  /* directory entry: escape bytes so far */
+        if (mode == ORC_M4BIT) img[ORC_OFF_ESC + at4++] = esc4;
+        if (mode == ORC_MRAW) atraw += 1;
+        if ((G + 1) % ORC_DIR_GROUPS == 0) {  /* directory entry: groups so far */
             int w = G / ORC_DIR_GROUPS;
-            img[ORC_OFF_DIR + 2 * w] = (uint8_t)(esc & 0xFF);
-            img[ORC_OFF_DIR + 2 * w + 1] = (uint8_t)(esc >> 8);
+            unsigned entry = ((unsigned)at4 & 0x1FFu) | (((unsigned)atraw & 0x7Fu) << 9);
+            img[ORC_OFF_DIR + 2 * w] = (uint8_t)(entry & 0xFFu);
+            img[ORC_OFF_DIR + 2 * w + 1] = (uint8_t)(entry >> 8);
         }
     }
     return esc;
@@ -236,19 +272,24 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
 
 /*
  * Decode one slot image into the logical tile [64][128].
- * Returns the number of escape bytes consumed, or -1 on a reserved tag (3),
- * -2 if the escape stream would run past esc_limit bytes, or -3 if a
- * directory entry differs from the escape bytes of the eighths it covers.
+ * Returns the number of escape bytes the image uses, or -1 on a reserved tag
+ * (3), -2 if the escape stream would run past esc_limit bytes, or -3 if a
+ * directory entry differs from the group counts of the eighths it covers.
  */
 int gaac_ref_decode_tile(const uint8_t* img, int kind, const uint8_t* base3, const uint8_t* base4,
                          int esc_limit, uint16_t* tile) {
-    int off = 0;
+    int n4 = 0, nraw = 0;
     for (int G = 0; G < ORC_GROUPS; ++G) {
         unsigned mode = get_tag(img, G);
         if (mode == 3u) return -1;
-        int nb = escape_bytes_of_mode(mode);
-        if (off + nb > esc_limit) return -2;
-        const uint8_t* escb = img + ORC_OFF_ESC + off;
+        if (mode == ORC_M4BIT) n4 += 1;
+        if (mode == ORC_MRAW) nraw += 1;
+    }
+    int esc = n4 + 8 * nraw;
+    if (esc > esc_limit) return -2;
+    int at4 = 0, atraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = get_tag(img, G);
         for (int j = 0; j < 8; ++j) {
             int s = 8 * G + j;
             int c = channel_of(kind, s);
@@ -256,25 +297,24 @@ int gaac_ref_decode_tile(const uint8_t* img, int kind, const uint8_t* base3, con
             if (mode == ORC_M3BIT) {
                 e = base3[c] + code;
             } else if (mode == ORC_M4BIT) {
-                e = base4[c] + (code | (((escb[0] >> j) & 1u) << 3));
+                e = base4[c] + (code | (((img[ORC_OFF_ESC + at4] >> j) & 1u) << 3));
             } else {
-                unsigned hi = 0;
-                for (int k = 0; k < 5; ++k) hi |= ((escb[k] >> j) & 1u) << k;
-                e = code | (hi << 3);
+                e = img[ORC_OFF_ESC + n4 + 8 * atraw + j];
             }
             int t, cc;
             storage_to_tc(kind, s, &t, &cc);
             unsigned sm = (img[s] & 0x7Fu) | (img[sign_holder(s)] & 0x80u);
             tile[t * ORC_D + cc] = bf16_join(sm, e);
         }
-        off += nb;
+        if (mode == ORC_M4BIT) at4 += 1;
+        if (mode == ORC_MRAW) atraw += 1;
         if ((G + 1) % ORC_DIR_GROUPS == 0) {
             int w = G / ORC_DIR_GROUPS;
             int dir = img[ORC_OFF_DIR + 2 * w] | (img[ORC_OFF_DIR + 2 * w + 1] << 8);
-            if (dir != off) return -3;
+            if (dir != ((at4 & 0x1FF) | ((atraw & 0x7F) << 9))) return -3;
         }
     }
-    return off;
+    return esc;
 }
 
 /* Per-mode group counts of an encoded tile (diagnostics of section 4.7.1). */

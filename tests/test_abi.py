@@ -34,7 +34,7 @@ def test_host_helpers(lib):
     lib.gaac_strerror.restype = ctypes.c_char_p
     assert lib.gaac_strerror(0) == b"ok"
     assert lib.gaac_strerror(1) == b"invalid argument"
-    assert lib.gaac_format_version() == 2
+    assert lib.gaac_format_version() == 3
     lib.gaac_attention_workspace.restype = ctypes.c_size_t
     # (16 m,l floats + 8 heads x 128 acc floats) x 4 bytes per (sequence, kv-head, split),
     # then one 4-byte merge counter per (sequence, kv-head), rounded up to 16 bytes

@@ -10,7 +10,7 @@ and Appendix D (3-bit codes, 2-bit tags, escape bytes).
   * the byte layout: hand-derived golden images (tests/golden)
   * the mode rule: brute force over every forced mode, validity judged by
     round trip alone; the encoder must pick the cheapest valid mode
-  * the stream size: closed form sum of {0,1,5} bytes per group mode
+  * the stream size: closed form sum of {0,1,8} bytes per group mode
   * the aggregate statistics: the Gaussian prediction of mode shares on the
     synthetic key distribution
 """
@@ -21,7 +21,7 @@ import numpy as np
 import pytest
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-FULL_CAP = 5 * 1024  # every group raw: the largest escape stream a tile can have
+FULL_CAP = 8 * 1024  # every group raw: the largest escape stream a tile can have
 
 
 def _bases(rng, kind):
@@ -47,6 +47,8 @@ def test_exhaustive_roundtrip_all_bf16_patterns(orc, kind):
         for arr in arrangements:
             for i in range(8):
                 tile = arr[i * 8192:(i + 1) * 8192].reshape(64, 128)
+                if kind == 1 and arr is patterns:  # consecutive patterns along the V storage order
+                    tile = orc.unraw_tile(arr[i * 8192:(i + 1) * 8192], kind)
                 img, esc = orc.encode_tile(tile, kind, b3, b4, esc_cap=FULL_CAP)
                 assert esc >= 0
                 dec, st = orc.decode_tile(img, kind, b3, b4, esc_limit=esc)
@@ -64,7 +66,7 @@ def _golden_tile(case):
 
 
 def test_golden_format_examples(orc):
-    cases = json.load(open(os.path.join(HERE, "golden", "format_v2_examples.json")))["cases"]
+    cases = json.load(open(os.path.join(HERE, "golden", "format_v3_examples.json")))["cases"]
     for case in cases:
         tile = _golden_tile(case)
         b3 = np.full(128, case["base3"], np.uint8)
@@ -81,16 +83,59 @@ def test_golden_format_examples(orc):
         np.testing.assert_array_equal(dec, tile)
 
 
+# V operand order (format v3), worked out by hand: (t, c) -> s
+V_ORDER_PINS = [
+    ((0, 0), 0),      # unit 0, element 0
+    ((0, 8), 1),      # channel g+8 of the same 16-channel block: r bit 0
+    ((1, 0), 2),      # the next token of the pair: r bit 1
+    ((8, 0), 4),      # token + 8: r bit 2
+    ((0, 16), 8),     # next 16-channel block: the next group of the unit
+    ((2, 0), 32),     # next token pair: the next unit (lane q)
+    ((0, 1), 128),    # next channel: unit + 4 (lane g)
+    ((0, 64), 1024),  # upper 64 channels: the next eighth
+    ((16, 0), 2048),  # next quarter of the tokens: two eighths on
+    ((5, 3), 450),
+    ((63, 127), 8191),
+]
+
+
+def _v_tc(s):
+    """Inverse of the V operand order, restated from the format rule."""
+    u, j = divmod(s, 32)
+    eighth, lane = divmod(u, 32)
+    w, h = divmod(eighth, 2)
+    g, q = divmod(lane, 4)
+    i, r = divmod(j, 8)
+    return 16 * w + 8 * (r >> 2) + 2 * q + ((r >> 1) & 1), 16 * (4 * h + i) + 8 * (r & 1) + g
+
+
 def test_storage_order_pins(orc):
-    """K tiles are token-major, V tiles channel-major (format v2)."""
+    """K tiles are token-major; V tiles follow the operand order of format v3."""
     assert orc.storage_index(0, 5, 3) == 5 * 128 + 3
-    assert orc.storage_index(1, 5, 3) == 3 * 64 + 5
+    for (t, c), s in V_ORDER_PINS:
+        assert orc.storage_index(1, t, c) == s, (t, c)
+        assert _v_tc(s) == (t, c)
     tile = np.arange(8192, dtype=np.uint16).reshape(64, 128)
-    rk = orc.raw_tile(tile, 0)
+    np.testing.assert_array_equal(orc.raw_tile(tile, 0), tile.reshape(-1))
     rv = orc.raw_tile(tile, 1)
-    np.testing.assert_array_equal(rk, tile.reshape(-1))
-    np.testing.assert_array_equal(rv, tile.T.reshape(-1))
+    expect = np.array([tile[_v_tc(s)] for s in range(8192)], np.uint16)
+    np.testing.assert_array_equal(rv, expect)
+    assert sorted(rv.tolist()) == list(range(8192))  # a permutation
     np.testing.assert_array_equal(orc.unraw_tile(rv, 1), tile)
+
+
+def test_v_units_are_operand_fragments(orc):
+    """Each V unit 32*(2w+h) + 4g + q holds, for the 16-channel blocks 4h..4h+3,
+    channels 16m+g and 16m+g+8 at tokens 16w + 2q + {0, 1, 8, 9}: one lane's
+    share of a 16 x 16 (channels x tokens) operand tile."""
+    for u in range(256):
+        eighth, lane = divmod(u, 32)
+        w, h = divmod(eighth, 2)
+        g, q = divmod(lane, 4)
+        want = {(16 * w + 2 * q + dt, 16 * m + g + dc) for m in range(4 * h, 4 * h + 4) for dt in (0, 1, 8, 9)
+                for dc in (0, 8)}
+        got = {(t, c) for t in range(64) for c in range(128) if orc.storage_index(1, t, c) // 32 == u}
+        assert got == want, u
 
 
 def _near_edge_exponents(rng, b3, b4, n):
@@ -129,7 +174,7 @@ def test_mode_minimality_brute_force(orc, kind):
         for m in range(3):
             forced = np.full(1024, m, np.uint8)
             img, esc = orc.encode_tile(tile, kind, b3, b4, forced=forced, esc_cap=FULL_CAP)
-            assert esc == 1024 * [0, 1, 5][m]
+            assert esc == 1024 * [0, 1, 8][m]
             dec, st = orc.decode_tile(img, kind, b3, b4, esc)
             dseq = np.empty(8192, np.uint16)
             dseq[order.reshape(-1)] = dec.reshape(-1)
@@ -142,7 +187,7 @@ def test_mode_minimality_brute_force(orc, kind):
         assert (np.bincount(cheapest, minlength=3) > 0).all(), "the trial must exercise every mode"
         # closed form of the stream size
         counts = orc.mode_counts(img)
-        assert esc == counts[1] * 1 + counts[2] * 5
+        assert esc == counts[1] * 1 + counts[2] * 8
 
 
 def test_capacity_overflow_reported(orc):
@@ -158,7 +203,8 @@ def test_capacity_overflow_reported(orc):
 
 
 def test_capacity_edge(orc):
-    """496 escape bytes fit, 497 do not: 496 4-bit groups fill the area exactly."""
+    """496 escape bytes fit, 497 do not: 496 4-bit groups fill the area exactly, and so do
+    62 raw groups (8 bytes each); one more 4-bit group next to them overflows."""
     b3 = np.full(128, 124, np.uint8)
     b4 = np.full(128, 120, np.uint8)
     tile = np.full((64, 128), 16256, np.uint16)  # 1.0: exponent 127, 3-bit mode
@@ -168,6 +214,16 @@ def test_capacity_edge(orc):
         t[8 * np.arange(n_wide)] = 135 << 7  # exponent 135: outside [124,131], inside [120,135]
         img, esc = orc.encode_tile(t.reshape(64, 128), 0, b3, b4)
         assert esc == expect
+    for n_wide, expect in ((0, 496), (1, -1)):
+        t = flat.copy()
+        t[8 * np.arange(62)] = 200 << 7  # exponent 200: outside both windows, the group is raw
+        t[8 * (62 + np.arange(n_wide))] = 135 << 7
+        img, esc = orc.encode_tile(t.reshape(64, 128), 0, b3, b4)
+        assert esc == expect
+        if esc > 0:
+            dec, st = orc.decode_tile(img, 0, b3, b4, esc)
+            assert st == esc
+            np.testing.assert_array_equal(dec, t.reshape(64, 128))
 
 
 def _tags(img):
@@ -176,8 +232,8 @@ def _tags(img):
 
 @pytest.mark.parametrize("kind", [0, 1])
 def test_escape_directory_is_the_eighth_prefix(orc, kind):
-    """Directory entry w = escape bytes of groups [0, 128(w+1)), read back from the tag plane
-    with the stream-size rule (0, 1, 5 bytes per mode); the escape bytes start at 11536."""
+    """Directory entry w = (4-bit groups of [0, 128(w+1))) + 512 * (raw groups there), counted
+    from the tag plane; the escape area holds one byte per 4-bit group, then 8 per raw group."""
     rng = np.random.default_rng(77 + kind)
     for trial in range(6):
         b3 = rng.integers(100, 130, 128).astype(np.uint8)
@@ -187,11 +243,12 @@ def test_escape_directory_is_the_eighth_prefix(orc, kind):
         tile = ((rng.integers(0, 2, (64, 128)) << 15) | (e << 7) | rng.integers(0, 128, (64, 128))).astype(np.uint16)
         img, esc = orc.encode_tile(tile, kind, b3, b4, esc_cap=FULL_CAP)
         assert esc >= 0
-        per = np.array([0, 1, 5, 0])[_tags(img)]
-        want = np.cumsum(per.reshape(8, 128).sum(axis=1))
+        tags = _tags(img).reshape(8, 128)
+        n4 = np.cumsum((tags == 1).sum(axis=1))
+        nr = np.cumsum((tags == 2).sum(axis=1))
         got = img[11520:11536].view("<u2")
-        np.testing.assert_array_equal(got, want)
-        assert want[7] == esc
+        np.testing.assert_array_equal(got, (n4 % 512) + 512 * (nr % 128))
+        assert n4[7] + 8 * nr[7] == esc
         dec, st = orc.decode_tile(img, kind, b3, b4, esc_limit=esc)
         assert st == esc
         np.testing.assert_array_equal(dec, tile)
@@ -218,7 +275,7 @@ def test_sign_rotation_pins(orc):
     for kind in (0, 1):
         for s in (0, 1, 2, 3, 4101, 8191):
             tile = np.full((64, 128), 16256, np.uint16)
-            t, c = (s // 128, s % 128) if kind == 0 else (s % 64, s // 64)
+            t, c = (s // 128, s % 128) if kind == 0 else _v_tc(s)
             tile[t, c] = 0xBF80 | 0x2D  # -1.0 with mantissa 0x2D
             img, esc = orc.encode_tile(tile, kind, b, b)
             holder = 4 * (s // 4) + (s + 1) % 4
