@@ -72,8 +72,8 @@ struct AttSmem {
   uint32_t tagl[256];             // tag byte -> gather selector, counts, raw groups (tag_entry)
   alignas(16) uint8_t bases[2][2][kD];  // [K|V][base3|base4][channel] of the CTA's kv-head
   StageMeta smeta[kStages];
-  alignas(16) uint32_t qf[kRPad][4][16];  // q A-operand words per (head g, lane tq): qa0[0..7], qa2[0..7]
-  alignas(16) uint32_t vbw[32][2][8];     // V base words per lane and unit: base3 of groups 0-3, base4 - base3
+  alignas(16) uint4 qf[4][32];           // q A-operand words [k-step pair][lane]: qa0[2p], qa0[2p+1], qa2[2p], qa2[2p+1]
+  alignas(16) uint4 vbw[2][2][32];        // V base words [unit][base3 | base4 - base3][lane], groups 0-3
   unsigned int stDone[kStages];           // warps of the group done reading the stage's current block
   float wm[kCWarps][kRPad];       // per warp and head: running maximum (end of split)
   float wl[kCWarps][kRPad];       // per warp and head: denominator (end of split)
@@ -361,7 +361,6 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
     kb3[i] = *reinterpret_cast<const uint32_t*>(&sm.bases[0][0][32 * tq + 4 * i]);
     kd43[i] = *reinterpret_cast<const uint32_t*>(&sm.bases[0][1][32 * tq + 4 * i]) - kb3[i];
   }
-  const uint4* qfl = reinterpret_cast<const uint4*>(&sm.qf[g][tq][0]);
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
   float mrun = -INFINITY, lsum = 0.f;  // head g
@@ -385,7 +384,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
       // 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no head) are zero
 #pragma unroll
       for (int m2 = 0; m2 < 4; ++m2) {
-        const uint4 qv = qfl[m2];  // qa0[2m2], qa0[2m2+1], qa2[2m2], qa2[2m2+1]
+        const uint4 qv = sm.qf[m2][lane];  // qa0[2m2], qa0[2m2+1], qa2[2m2], qa2[2m2+1]
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int m = 2 * m2 + i;
@@ -432,8 +431,8 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
       uint32_t vb3[2][8], vd43[2][8];  // word 2i and 2i+1 serve group i
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
-        const uint4 x3 = *reinterpret_cast<const uint4*>(&sm.vbw[lane][hv][0]);
-        const uint4 x4 = *reinterpret_cast<const uint4*>(&sm.vbw[lane][hv][4]);
+        const uint4 x3 = sm.vbw[hv][0][lane];
+        const uint4 x4 = sm.vbw[hv][1][lane];
         vb3[hv][0] = vb3[hv][1] = x3.x;
         vb3[hv][2] = vb3[hv][3] = x3.y;
         vb3[hv][4] = vb3[hv][5] = x3.z;
@@ -611,36 +610,33 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     const uint8_t* v4 = a.base4 + (a.Hkv + h) * kD;
     const uint32_t x3 = v3[cA] | (static_cast<uint32_t>(v3[cA + 8]) << 8);
     const uint32_t x4 = v4[cA] | (static_cast<uint32_t>(v4[cA + 8]) << 8);
-    sm.vbw[ln][hv][i] = x3 | (x3 << 16);
-    sm.vbw[ln][hv][4 + i] = (x4 | (x4 << 16)) - (x3 | (x3 << 16));
+    reinterpret_cast<uint32_t*>(&sm.vbw[hv][0][ln])[i] = x3 | (x3 << 16);
+    reinterpret_cast<uint32_t*>(&sm.vbw[hv][1][ln])[i] = (x4 | (x4 << 16)) - (x3 | (x3 << 16));
   }
   // q of the kv-head's query heads, times 2^-4, as A-operand words of S^T = q K^T: for head g and lane tq,
   // word m (m < 8) = channels 32tq + 4m + {0, 2}, word 8 + m = channels 32tq + 4m + {1, 3}, stored as
   // [m2][qa0[2m2], qa0[2m2+1], qa2[2m2], qa2[2m2+1]] so that one 16-byte load serves two k-steps
   for (int x = tid; x < kRPad * 4 * 16; x += kAttThreads) {
-    const int n = x / 64, tq = (x / 16) % 4, k = x % 16, m2 = k / 4, i = k % 4;
+    const int ln = x / 16, n = ln / 4, tq = ln % 4, k = x % 16, m2 = k / 4, i = k % 4;
     const int m = 2 * m2 + (i & 1), odd = i >> 1;  // odd: channels {1, 3} of the quad
     uint32_t v = 0u;
     if (n < a.r) {
       const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + h * a.r + n) * kD + 32 * tq + 4 * m + odd;
       v = bf16x2_div16(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16));
     }
-    sm.qf[n][tq][k] = v;
+    reinterpret_cast<uint32_t*>(&sm.qf[m2][ln])[i] = v;
   }
-  if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.stFull[s], 1);
-      sm.stDone[s] = 0u;
-    }
-    fence_mbar_init();
-    for (int j = 0; j < min(n_my, kStages); ++j) {  // the first blocks; later ones are issued as stages free up
-      uint2 eK, eV;
-      block_entries(a, b, h, blk0 + j, eK, eV);
-      issue_block(a, sm, j, eK, eV);
-    }
+  if (tid < kStages) {
+    mbar_init(&sm.stFull[tid], 1);
+    sm.stDone[tid] = 0u;
   }
+  fence_mbar_init();
   __syncthreads();
+  if (tid < min(n_my, kStages)) {  // the first blocks, one lane each; later ones are issued as stages free up
+    uint2 eK, eV;
+    block_entries(a, b, h, blk0 + tid, eK, eV);
+    issue_block(a, sm, tid, eK, eV);
+  }
 
   const int r = a.r;
   float* part = a.part + ((static_cast<size_t>(b) * a.Hkv + h) * a.n_splits + split) * kPartFloats;
