@@ -34,7 +34,7 @@ CONFIG_ID = 1
 
 # DRAM bytes (read + write) of one attn_split_kernel launch on this workload, from an
 # ncu capture, valid only for the kernel source it was taken on (see profiles/).
-NCU_TRAFFIC = {"kernel_sha": "1e2ca13081823a4b", "bytes_per_launch": 195583488}
+NCU_TRAFFIC = {"kernel_sha": "d850abc773066bcb", "bytes_per_launch": 196250112}
 
 
 def kernel_sha() -> str:

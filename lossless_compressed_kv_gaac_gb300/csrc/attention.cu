@@ -72,7 +72,7 @@ struct AttSmem {
   uint32_t tagl[256];             // tag byte -> gather selector, counts, raw groups (tag_entry)
   alignas(16) uint8_t bases[2][2][kD];  // [K|V][base3|base4][channel] of the CTA's kv-head
   StageMeta smeta[kStages];
-  alignas(16) uint4 qf[4][32];           // q A-operand words [k-step pair][lane]: qa0[2p], qa0[2p+1], qa2[2p], qa2[2p+1]
+  alignas(16) uint4 qf[8][32];           // q A-operand quads [k-step][lane]: (qa0, 0, qa2, 0)
   alignas(16) uint4 vbw[2][2][32];        // V base words [unit][base3 | base4 - base3][lane], groups 0-3
   unsigned int stDone[kStages];           // warps of the group done reading the stage's current block
   float wm[kCWarps][kRPad];       // per warp and head: running maximum (end of split)
@@ -380,18 +380,14 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
       uint32_t oA[16], oB[16];
       tile_units(a, sm, sm.stage[st][0], meta.mode[0], meta.esc[0], w, lane, kb3, kd43, kb3, kd43, oA, oB, kbadA,
                  kbadB);
-      // q of head g as the A operand of S^T = q K^T (scaled by 2^-4): for k-step m the K lane holds channels
-      // 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no head) are zero
+      // q of head g as the A operand of S^T = q K^T (scaled by 2^-4), one 16-byte quad per k-step: for k-step
+      // m the K lane holds channels 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no
+      // head) are zero
 #pragma unroll
-      for (int m2 = 0; m2 < 4; ++m2) {
-        const uint4 qv = sm.qf[m2][lane];  // qa0[2m2], qa0[2m2+1], qa2[2m2], qa2[2m2+1]
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int m = 2 * m2 + i;
-          const uint32_t q0 = i ? qv.y : qv.x, q2 = i ? qv.w : qv.z;
-          mma_bf16(sA, q0, 0u, q2, 0u, oA[2 * m], oA[2 * m + 1]);
-          mma_bf16(sB, q0, 0u, q2, 0u, oB[2 * m], oB[2 * m + 1]);
-        }
+      for (int m = 0; m < 8; ++m) {
+        const uint4 qv = sm.qf[m][lane];
+        mma_bf16(sA, qv.x, qv.y, qv.z, qv.w, oA[2 * m], oA[2 * m + 1]);
+        mma_bf16(sB, qv.x, qv.y, qv.z, qv.w, oB[2 * m], oB[2 * m + 1]);
       }
     }
     // ---- online softmax of head g over the warp's 16 tokens
@@ -613,18 +609,17 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     reinterpret_cast<uint32_t*>(&sm.vbw[hv][0][ln])[i] = x3 | (x3 << 16);
     reinterpret_cast<uint32_t*>(&sm.vbw[hv][1][ln])[i] = (x4 | (x4 << 16)) - (x3 | (x3 << 16));
   }
-  // q of the kv-head's query heads, times 2^-4, as A-operand words of S^T = q K^T: for head g and lane tq,
-  // word m (m < 8) = channels 32tq + 4m + {0, 2}, word 8 + m = channels 32tq + 4m + {1, 3}, stored as
-  // [m2][qa0[2m2], qa0[2m2+1], qa2[2m2], qa2[2m2+1]] so that one 16-byte load serves two k-steps
-  for (int x = tid; x < kRPad * 4 * 16; x += kAttThreads) {
-    const int ln = x / 16, n = ln / 4, tq = ln % 4, k = x % 16, m2 = k / 4, i = k % 4;
-    const int m = 2 * m2 + (i & 1), odd = i >> 1;  // odd: channels {1, 3} of the quad
+  // q of the kv-head's query heads, times 2^-4, as A-operand quads of S^T = q K^T: for lane (g, tq) and
+  // k-step m, (channels 32tq + 4m + {0, 2}, 0, channels 32tq + 4m + {1, 3}, 0) of head g (rows 8-15 zero)
+  for (int x = tid; x < 32 * 8 * 2; x += kAttThreads) {
+    const int ln = x / 16, n = ln / 4, tq = ln % 4, m = (x / 2) % 8, odd = x % 2;
     uint32_t v = 0u;
     if (n < a.r) {
       const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + h * a.r + n) * kD + 32 * tq + 4 * m + odd;
       v = bf16x2_div16(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16));
     }
-    reinterpret_cast<uint32_t*>(&sm.qf[m2][ln])[i] = v;
+    reinterpret_cast<uint32_t*>(&sm.qf[m][ln])[2 * odd] = v;
+    reinterpret_cast<uint32_t*>(&sm.qf[m][ln])[2 * odd + 1] = 0u;
   }
   if (tid < kStages) {
     mbar_init(&sm.stFull[tid], 1);
