@@ -390,6 +390,31 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
         mma_bf16(sB, qv.x, qv.y, qv.z, qv.w, oB[2 * m], oB[2 * m + 1]);
       }
     }
+    // ---- V units of the same tokens (independent of the scores: decoded while the MMAs above run)
+    uint32_t oA[16], oB[16];
+    bool vbadA, vbadB;
+    uint32_t vb3[2][8], vd43[2][8];  // word 2i and 2i+1 serve group i
+#pragma unroll
+    for (int hv = 0; hv < 2; ++hv) {
+      const uint4 x3 = sm.vbw[hv][0][lane];
+      const uint4 x4 = sm.vbw[hv][1][lane];
+      vb3[hv][0] = vb3[hv][1] = x3.x;
+      vb3[hv][2] = vb3[hv][3] = x3.y;
+      vb3[hv][4] = vb3[hv][5] = x3.z;
+      vb3[hv][6] = vb3[hv][7] = x3.w;
+      vd43[hv][0] = vd43[hv][1] = x4.x;
+      vd43[hv][2] = vd43[hv][3] = x4.y;
+      vd43[hv][4] = vd43[hv][5] = x4.z;
+      vd43[hv][6] = vd43[hv][7] = x4.w;
+    }
+    tile_units(a, sm, sm.stage[st][1], meta.mode[1], meta.esc[1], w, lane, vb3[0], vd43[0], vb3[1], vd43[1], oA,
+               oB, vbadA, vbadB);
+    // The stage is read: the group's last warp to get here refills it with block jn.
+    __syncwarp();
+    if (lane == 0 && atomic_add_acq_rel_cta(&sm.stDone[st], 1u) == kGroupWarps - 1) {
+      sm.stDone[st] = 0u;
+      if (jn < n_my) issue_block(a, sm, st, nK, nV);
+    }
     // ---- online softmax of head g over the warp's 16 tokens
     const float x0 = (!kbadA && tA < nv) ? sA[0] * a.scale_log2 : -INFINITY;
     const float x1 = (!kbadA && tA + 1 < nv) ? sA[1] * a.scale_log2 : -INFINITY;
@@ -422,30 +447,6 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
     const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
     // ---- O^T += V^T P^T over the 16 tokens, eight 16-channel tiles
     {
-      uint32_t oA[16], oB[16];
-      bool vbadA, vbadB;
-      uint32_t vb3[2][8], vd43[2][8];  // word 2i and 2i+1 serve group i
-#pragma unroll
-      for (int hv = 0; hv < 2; ++hv) {
-        const uint4 x3 = sm.vbw[hv][0][lane];
-        const uint4 x4 = sm.vbw[hv][1][lane];
-        vb3[hv][0] = vb3[hv][1] = x3.x;
-        vb3[hv][2] = vb3[hv][3] = x3.y;
-        vb3[hv][4] = vb3[hv][5] = x3.z;
-        vb3[hv][6] = vb3[hv][7] = x3.w;
-        vd43[hv][0] = vd43[hv][1] = x4.x;
-        vd43[hv][2] = vd43[hv][3] = x4.y;
-        vd43[hv][4] = vd43[hv][5] = x4.z;
-        vd43[hv][6] = vd43[hv][7] = x4.w;
-      }
-      tile_units(a, sm, sm.stage[st][1], meta.mode[1], meta.esc[1], w, lane, vb3[0], vd43[0], vb3[1], vd43[1], oA,
-                 oB, vbadA, vbadB);
-      // The stage is read: the group's last warp to get here refills it with block jn.
-      __syncwarp();
-      if (lane == 0 && atomic_add_acq_rel_cta(&sm.stDone[st], 1u) == kGroupWarps - 1) {
-        sm.stDone[st] = 0u;
-        if (jn < n_my) issue_block(a, sm, st, nK, nV);
-      }
       if (nv < kBlock) {  // the open block: values of tokens past the sequence must not meet a zero weight
         const uint32_t mlo = (tA < nv ? 0x0000FFFFu : 0u) | (tA + 1 < nv ? 0xFFFF0000u : 0u);
         const uint32_t mhi = (tB < nv ? 0x0000FFFFu : 0u) | (tB + 1 < nv ? 0xFFFF0000u : 0u);
