@@ -34,7 +34,7 @@ CONFIG_ID = 1
 
 # DRAM bytes (read + write) of one attn_split_kernel launch on this workload, from an
 # ncu capture, valid only for the kernel source it was taken on (see profiles/).
-NCU_TRAFFIC = {"kernel_sha": "d850abc773066bcb", "bytes_per_launch": 196250112}
+NCU_TRAFFIC = {"kernel_sha": "be7069b20e274bb0", "bytes_per_launch": 195794944}
 
 
 def kernel_sha() -> str:
