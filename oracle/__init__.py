@@ -70,6 +70,16 @@ def lib() -> ctypes.CDLL:
             L.gaac_ref_escape_bytes_of_mode.restype = i32
             L.gaac_ref_attention.argtypes = [P, P, P, i64, i64, i32, i32, ctypes.c_double, P, P, P]
             L.gaac_ref_attention.restype = None
+            L.gaac_ref_fp8_slot_bytes.argtypes = [i32]
+            L.gaac_ref_fp8_slot_bytes.restype = i32
+            L.gaac_ref_fp8_calibrate.argtypes = [P, i64, i64, i32, i32, P, P]
+            L.gaac_ref_fp8_calibrate.restype = i32
+            L.gaac_ref_fp8_encode_tile.argtypes = [P, i32, i32, P, P, P, P, i32]
+            L.gaac_ref_fp8_encode_tile.restype = i32
+            L.gaac_ref_fp8_decode_tile.argtypes = [P, i32, i32, P, P, i32, P]
+            L.gaac_ref_fp8_decode_tile.restype = i32
+            L.gaac_ref_fp8_mode_counts.argtypes = [P, i32, P]
+            L.gaac_ref_fp8_mode_counts.restype = None
             _lib = L
     return _lib
 
@@ -179,3 +189,54 @@ def attention(q, k, v, scale: float):
     lib().gaac_ref_attention(_ptr(q), _ptr(k), _ptr(v), Hkv * D, T, Hq, Hkv, float(scale), _ptr(out), _ptr(flags),
                              _ptr(scratch))
     return out, flags
+
+
+# ---------------------------------------------------------------- FP8 variant
+FP8_E4M3, FP8_E5M2 = 0, 1
+FP8_OFF_ESC = {FP8_E4M3: 7440, FP8_E5M2: 6416}
+
+
+def fp8_slot_bytes(fmt: int) -> int:
+    return lib().gaac_ref_fp8_slot_bytes(fmt)
+
+
+def fp8_calibrate(x, fmt: int) -> tuple[np.ndarray, np.ndarray]:
+    """x: uint8 [n_tok][n_heads][128] FP8 bits -> (base3, base4) uint8 [n_heads][128]."""
+    x = _u8(x)
+    n_tok, n_heads, d = x.shape
+    assert d == D
+    b3 = np.zeros((n_heads, D), np.uint8)
+    b4 = np.zeros((n_heads, D), np.uint8)
+    assert lib().gaac_ref_fp8_calibrate(_ptr(x), n_tok, n_heads * D, n_heads, fmt, _ptr(b3), _ptr(b4)) == 0
+    return b3, b4
+
+
+def fp8_encode_tile(tile, kind: int, fmt: int, base3, base4, forced=None, esc_cap: int = ESC_CAP):
+    """Encode a [64][128] FP8 tile.  Returns (image uint8 [off_esc + esc_cap], esc_len); esc_len is -1
+    when the escape area would exceed esc_cap."""
+    tile = _u8(tile).reshape(BLOCK, D)
+    b3, b4 = _u8(base3).reshape(D), _u8(base4).reshape(D)
+    img = np.zeros(FP8_OFF_ESC[fmt] + esc_cap, np.uint8)
+    fp = 0
+    if forced is not None:
+        forced = _u8(forced).reshape(1024)
+        fp = _ptr(forced)
+    esc = lib().gaac_ref_fp8_encode_tile(_ptr(tile), kind, fmt, _ptr(b3), _ptr(b4), fp, _ptr(img), esc_cap)
+    return img, esc
+
+
+def fp8_decode_tile(img, kind: int, fmt: int, base3, base4, esc_limit: int | None = None):
+    img = _u8(img)
+    if esc_limit is None:
+        esc_limit = img.size - FP8_OFF_ESC[fmt]
+    b3, b4 = _u8(base3).reshape(D), _u8(base4).reshape(D)
+    out = np.zeros((BLOCK, D), np.uint8)
+    st = lib().gaac_ref_fp8_decode_tile(_ptr(img), kind, fmt, _ptr(b3), _ptr(b4), esc_limit, _ptr(out))
+    return out, st
+
+
+def fp8_mode_counts(img, fmt: int) -> np.ndarray:
+    img = _u8(img)
+    out = np.zeros(4, np.int64)
+    lib().gaac_ref_fp8_mode_counts(_ptr(img), fmt, _ptr(out))
+    return out

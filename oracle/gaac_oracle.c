@@ -108,11 +108,11 @@ static int channel_of(int kind, int s) { int t, c; storage_to_tc(kind, s, &t, &c
 /* ---- calibration (section 3.1 and 4.7.1: windows of 8 and 16 exponents per
  * head-channel, chosen from calibration data).  Window with the largest count;
  * ties go to the smallest base. */
-static int best_window(const uint64_t* hist, int width) {
+static int best_window_n(const uint64_t* hist, int nbins, int width) {
     uint64_t best = 0;
     int arg = 0;
     int have = 0;
-    for (int b = 0; b + width <= 256; ++b) {
+    for (int b = 0; b + width <= nbins; ++b) {
         uint64_t sum = 0;
         for (int i = 0; i < width; ++i) sum += hist[b + i];
         if (!have || sum > best) { best = sum; arg = b; have = 1; }
@@ -120,6 +120,7 @@ static int best_window(const uint64_t* hist, int width) {
     return arg;
 }
 
+static int best_window(const uint64_t* hist, int width) { return best_window_n(hist, 256, width); }
 int gaac_ref_best_window(const uint64_t* hist, int width) { return best_window(hist, width); }
 
 /* x[t*tok_stride + h*128 + c] for t < n_tok; writes base3[h*128+c], base4[h*128+c]. */
@@ -145,7 +146,7 @@ void gaac_ref_calibrate(const uint16_t* x, int64_t n_tok, int64_t tok_stride, in
  *   q=2: code bits 0..2 -> W2, lane L, bits 3h..3h+2
  *   q=3: code bits 0..1 -> Wh, lane L, bits 6..7; code bit 2 -> W2, lane L, bit 6+h
  * Returns the byte offset inside the slot image; *bitpos is the bit inside it. */
-static int code_bit_location(int s, int bit, int* bitpos) {
+static int plane_bit_location(int plane, int s, int bit, int* bitpos) {
     int u = s / 32, j = s % 32, h = j / 16, jj = j % 16, lane = jj % 4, q = jj / 4;
     int word, pos;
     if (q == 0) { word = h; pos = bit; }
@@ -154,7 +155,26 @@ static int code_bit_location(int s, int bit, int* bitpos) {
     else if (bit < 2) { word = h; pos = 6 + bit; }
     else { word = 2; pos = 6 + h; }
     *bitpos = pos;
-    return ORC_OFF_CODE + 4 * (word * ORC_UNITS + u) + lane;
+    return plane + 4 * (word * ORC_UNITS + u) + lane;
+}
+static int code_bit_location(int s, int bit, int* bitpos) { return plane_bit_location(ORC_OFF_CODE, s, bit, bitpos); }
+
+/* A 3-bit field per element at plane offset `plane`, laid out like the code plane. */
+static void put_field3(uint8_t* img, int plane, int s, unsigned v) {
+    for (int b = 0; b < 3; ++b) {
+        int pos;
+        int at = plane_bit_location(plane, s, b, &pos);
+        if ((v >> b) & 1u) img[at] |= (uint8_t)(1u << pos);
+    }
+}
+static unsigned get_field3(const uint8_t* img, int plane, int s) {
+    unsigned v = 0;
+    for (int b = 0; b < 3; ++b) {
+        int pos;
+        int at = plane_bit_location(plane, s, b, &pos);
+        v |= ((img[at] >> pos) & 1u) << b;
+    }
+    return v;
 }
 
 static void put_code(uint8_t* img, int s, unsigned code) {
@@ -331,6 +351,173 @@ void gaac_ref_raw_tile(const uint16_t* tile, int kind, uint16_t* raw) {
 void gaac_ref_unraw_tile(const uint16_t* raw, int kind, uint16_t* tile) {
     for (int t = 0; t < ORC_BLOCK; ++t)
         for (int c = 0; c < ORC_D; ++c) tile[t * ORC_D + c] = raw[gaac_ref_storage_index(kind, t, c)];
+}
+
+/* ======================================================================
+ * FP8 variant (GAAC page, Appendix B "Relation to FP8 KV": the same exponent
+ * coding applied to an FP8 cache, E4M3 and E5M2).  The page prints only the
+ * resulting ratios; this file fixes "GAAC-FP8 tile format v1":
+ *   element     E4M3: sign(1) exponent(4) mantissa(3); E5M2: sign(1)
+ *               exponent(5) mantissa(2); sm = sign << MW | mantissa
+ *   tile, order, groups, modes, codes, tags, directory and escape area as in
+ *               format v3, with the exponent windows inside the format's
+ *               2^EW exponent values (E4M3 has one 16-window, base4 = 0, so
+ *               it never needs the raw mode)
+ *   slot image  E4M3: [0,4096) sm nibbles (element s in byte s/2, low nibble
+ *                     for even s); [4096,7168) codes; [7168,7424) tags;
+ *                     [7424,7440) directory; [7440,7936) escape area
+ *               E5M2: [0,3072) sm, 3 bits per element laid out like the code
+ *                     plane; [3072,6144) codes; [6144,6400) tags;
+ *                     [6400,6416) directory; [6416,6912) escape area
+ * ====================================================================== */
+enum { ORC_FP8_E4M3 = 0, ORC_FP8_E5M2 = 1 };
+
+typedef struct { int ew, mw, off_code, off_tag, off_dir, off_esc, slot; } fp8_layout;
+
+static int fp8_layout_of(int fmt, fp8_layout* L) {
+    if (fmt == ORC_FP8_E4M3) { fp8_layout l = {4, 3, 4096, 7168, 7424, 7440, 7936}; *L = l; return 1; }
+    if (fmt == ORC_FP8_E5M2) { fp8_layout l = {5, 2, 3072, 6144, 6400, 6416, 6912}; *L = l; return 1; }
+    return 0;
+}
+
+int gaac_ref_fp8_slot_bytes(int fmt) { fp8_layout L; return fp8_layout_of(fmt, &L) ? L.slot : 0; }
+
+/* Windows of 8 and 16 exponents among the format's 2^EW values, from
+ * x[t*tok_stride + h*128 + c] (FP8 bytes); ties go to the smallest base. */
+int gaac_ref_fp8_calibrate(const uint8_t* x, int64_t n_tok, int64_t tok_stride, int n_heads, int fmt,
+                           uint8_t* base3, uint8_t* base4) {
+    fp8_layout L;
+    if (!fp8_layout_of(fmt, &L)) return -1;
+    int nb = 1 << L.ew;
+    for (int h = 0; h < n_heads; ++h) {
+        for (int c = 0; c < ORC_D; ++c) {
+            uint64_t hist[32];
+            memset(hist, 0, sizeof hist);
+            for (int64_t t = 0; t < n_tok; ++t) hist[(x[t * tok_stride + h * ORC_D + c] >> L.mw) & (nb - 1)] += 1;
+            base3[h * ORC_D + c] = (uint8_t)best_window_n(hist, nb, 8);
+            base4[h * ORC_D + c] = (uint8_t)best_window_n(hist, nb, 16);
+        }
+    }
+    return 0;
+}
+
+static void fp8_put_sm(uint8_t* img, const fp8_layout* L, int s, unsigned sm) {
+    if (L->ew == 4) img[s / 2] |= (uint8_t)((sm & 15u) << (4 * (s % 2)));
+    else put_field3(img, 0, s, sm);
+}
+static unsigned fp8_get_sm(const uint8_t* img, const fp8_layout* L, int s) {
+    if (L->ew == 4) return (img[s / 2] >> (4 * (s % 2))) & 15u;
+    return get_field3(img, 0, s);
+}
+
+/* Encode one FP8 tile ([64][128] logical order); img must hold
+ * off_esc + img_esc_cap bytes.  Returns the escape length or -1 past
+ * img_esc_cap; -2 on a bad fmt. */
+int gaac_ref_fp8_encode_tile(const uint8_t* tile, int kind, int fmt, const uint8_t* base3, const uint8_t* base4,
+                             const uint8_t* forced, uint8_t* img, int img_esc_cap) {
+    fp8_layout L;
+    if (!fp8_layout_of(fmt, &L)) return -2;
+    memset(img, 0, (size_t)(L.off_esc + img_esc_cap));
+    uint8_t seq[ORC_TILE];
+    for (int t = 0; t < ORC_BLOCK; ++t)
+        for (int c = 0; c < ORC_D; ++c) seq[gaac_ref_storage_index(kind, t, c)] = tile[t * ORC_D + c];
+    unsigned emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
+    for (int s = 0; s < ORC_TILE; ++s) fp8_put_sm(img, &L, s, ((seq[s] >> 7) << L.mw) | (seq[s] & mmask));
+    unsigned modes[ORC_GROUPS];
+    int n4 = 0, nraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned e[8], b3[8], b4[8];
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j;
+            e[j] = (seq[s] >> L.mw) & emask;
+            b3[j] = base3[channel_of(kind, s)];
+            b4[j] = base4[channel_of(kind, s)];
+        }
+        modes[G] = forced ? forced[G] : choose_mode(e, b3, b4);
+        if (modes[G] == ORC_M4BIT) n4 += 1;
+        if (modes[G] == ORC_MRAW) nraw += 1;
+    }
+    int esc = n4 + 8 * nraw;
+    if (esc > img_esc_cap) return -1;
+    int at4 = 0, atraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = modes[G];
+        img[L.off_tag + G / 4] |= (uint8_t)((mode & 3u) << (2 * (G % 4)));
+        uint8_t esc4 = 0;
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j;
+            unsigned e = (seq[s] >> L.mw) & emask, code = 0;
+            if (mode == ORC_M3BIT) {
+                code = (e - base3[channel_of(kind, s)]) & 7u;
+            } else if (mode == ORC_M4BIT) {
+                unsigned off = (e - base4[channel_of(kind, s)]) & 0xFFu;
+                code = off & 7u;
+                esc4 |= (uint8_t)(((off >> 3) & 1u) << j);
+            } else {
+                img[L.off_esc + n4 + 8 * atraw + j] = (uint8_t)e;
+            }
+            put_field3(img, L.off_code, s, code);
+        }
+        if (mode == ORC_M4BIT) img[L.off_esc + at4++] = esc4;
+        if (mode == ORC_MRAW) atraw += 1;
+        if ((G + 1) % ORC_DIR_GROUPS == 0) {
+            int w = G / ORC_DIR_GROUPS;
+            unsigned entry = ((unsigned)at4 & 0x1FFu) | (((unsigned)atraw & 0x7Fu) << 9);
+            img[L.off_dir + 2 * w] = (uint8_t)(entry & 0xFFu);
+            img[L.off_dir + 2 * w + 1] = (uint8_t)(entry >> 8);
+        }
+    }
+    return esc;
+}
+
+/* Decode one FP8 slot image into [64][128].  Returns the escape bytes used,
+ * -1 on a reserved tag, -2 past esc_limit, -3 on a directory mismatch, -4 on
+ * a bad fmt. */
+int gaac_ref_fp8_decode_tile(const uint8_t* img, int kind, int fmt, const uint8_t* base3, const uint8_t* base4,
+                             int esc_limit, uint8_t* tile) {
+    fp8_layout L;
+    if (!fp8_layout_of(fmt, &L)) return -4;
+    int n4 = 0, nraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = (img[L.off_tag + G / 4] >> (2 * (G % 4))) & 3u;
+        if (mode == 3u) return -1;
+        if (mode == ORC_M4BIT) n4 += 1;
+        if (mode == ORC_MRAW) nraw += 1;
+    }
+    int esc = n4 + 8 * nraw;
+    if (esc > esc_limit) return -2;
+    unsigned emask = (1u << L.ew) - 1u;
+    int at4 = 0, atraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = (img[L.off_tag + G / 4] >> (2 * (G % 4))) & 3u;
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j;
+            int c = channel_of(kind, s);
+            unsigned code = get_field3(img, L.off_code, s), e;
+            if (mode == ORC_M3BIT) e = base3[c] + code;
+            else if (mode == ORC_M4BIT) e = base4[c] + (code | (((img[L.off_esc + at4] >> j) & 1u) << 3));
+            else e = img[L.off_esc + n4 + 8 * atraw + j];
+            unsigned sm = fp8_get_sm(img, &L, s);
+            int t, cc;
+            storage_to_tc(kind, s, &t, &cc);
+            tile[t * ORC_D + cc] = (uint8_t)(((sm >> L.mw) << 7) | ((e & emask) << L.mw) | (sm & ((1u << L.mw) - 1u)));
+        }
+        if (mode == ORC_M4BIT) at4 += 1;
+        if (mode == ORC_MRAW) atraw += 1;
+        if ((G + 1) % ORC_DIR_GROUPS == 0) {
+            int w = G / ORC_DIR_GROUPS;
+            int dir = img[L.off_dir + 2 * w] | (img[L.off_dir + 2 * w + 1] << 8);
+            if (dir != ((at4 & 0x1FF) | ((atraw & 0x7F) << 9))) return -3;
+        }
+    }
+    return esc;
+}
+
+void gaac_ref_fp8_mode_counts(const uint8_t* img, int fmt, int64_t* counts4) {
+    fp8_layout L;
+    for (int m = 0; m < 4; ++m) counts4[m] = 0;
+    if (!fp8_layout_of(fmt, &L)) return;
+    for (int G = 0; G < ORC_GROUPS; ++G) counts4[(img[L.off_tag + G / 4] >> (2 * (G % 4))) & 3u] += 1;
 }
 
 /* ---- decode attention in fp64 (section 3.2; grouped-query heads share a
