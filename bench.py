@@ -184,6 +184,53 @@ def time_graph(g, stream, steps: int):
     return start.elapsed_time(end)
 
 
+def fp8_codec(k, v, n_calib: int) -> dict:
+    """FP8 variant of the codec on one layer's K and V cast to FP8 (round to nearest): payload ratio
+    against the FP8 bytes (a tile that does not fit its slot counts as 8 KiB), encode and decode GB/s
+    of FP8 bytes, round trip checked."""
+    import torch
+
+    import lossless_compressed_kv_gaac_gb300 as G
+
+    T, H = k.shape[1], k.shape[2]
+    nb = T // 64
+    out = {}
+    for fmt, name, dt in ((G.FP8_E4M3, "e4m3", torch.float8_e4m3fn), (G.FP8_E5M2, "e5m2", torch.float8_e5m2)):
+        k8, v8 = k[0].float().to(dt).view(torch.uint8), v[0].float().to(dt).view(torch.uint8)
+        b3 = torch.zeros((2 * H, 128), dtype=torch.uint8, device=k.device)
+        b4 = torch.zeros_like(b3)
+        G.fp8_calibrate(k8[:n_calib], fmt, b3[:H], b4[:H])
+        G.fp8_calibrate(v8[:n_calib], fmt, b3[H:], b4[H:])
+        tiles = torch.cat([x[: nb * 64].view(nb, 64, H, 128).permute(2, 0, 1, 3).reshape(-1, 64, 128) for x in (k8, v8)]).contiguous()
+        n = tiles.shape[0]
+        kinds = torch.cat([torch.zeros(H * nb), torch.ones(H * nb)]).to(torch.uint8).to(k.device)
+        rows = torch.cat([torch.arange(H).repeat_interleave(nb), H + torch.arange(H).repeat_interleave(nb)]).int().to(k.device)
+        slots = torch.empty((n, G.fp8_slot_bytes(fmt)), dtype=torch.uint8, device=k.device)
+        esc = torch.empty(n, dtype=torch.int16, device=k.device)
+        back = torch.empty_like(tiles)
+        te, td = [], []
+        for i in range(4):
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record()
+            G.fp8_encode_tiles(tiles, fmt, kinds, rows, b3, b4, slots, esc)
+            e1.record()
+            G.fp8_decompress_tiles(slots, esc, fmt, kinds, rows, b3, b4, back)
+            e2.record()
+            e2.synchronize()
+            if i:
+                te.append(e0.elapsed_time(e1))
+                td.append(e1.elapsed_time(e2))
+        e = esc.view(torch.int16).long() & 0xFFFF
+        fits = e != 0xFFFF
+        assert torch.equal(back[fits], tiles[fits])
+        off_esc = G.fp8_slot_bytes(fmt) - 496
+        payload = int((off_esc + e[fits]).sum().item()) + 8192 * int((~fits).sum().item())
+        out[name] = {"payload_ratio": round(n * 8192 / payload, 4), "resident_ratio": round(8192 / G.fp8_slot_bytes(fmt), 4),
+                     "tiles_kept_fp8": int((~fits).sum().item()), "encode_gbs": round(n * 8192 / (min(te) * 1e-3) / 1e9, 1),
+                     "decode_gbs": round(n * 8192 / (min(td) * 1e-3) / 1e9, 1)}
+    return out
+
+
 def run_gaac(args):
     import torch
 
@@ -233,6 +280,7 @@ def run_gaac(args):
     assert torch.equal(kd.view(torch.int16), k0.view(torch.int16)) and torch.equal(vd.view(torch.int16), v0.view(torch.int16))
     decompress_gbs = raw_bytes_layer / (min(dec_t) * 1e-3) / 1e9
     st = G.stats_dict(c0.stats)
+    fp8 = fp8_codec(k0, v0, wl.n_calib)
     del k0, v0, kd, vd
     alg = [algorithmic_bytes(c) for c in caches]
     alg_step = sum(alg)
@@ -375,6 +423,7 @@ def run_gaac(args):
         "speedup_vs_bf16_cache": round(bf16_ms / ms_per_step, 3) if bf16_ms else None,
         "encode_gbs": round(encode_gbs, 1),
         "decompress_gbs": round(decompress_gbs, 1),
+        "fp8": fp8,
         "ratio": {"payload": round(payload_ratio, 4), "resident": round(resident_ratio, 4),
                   "mode_shares": [round(st[f"groups{m}"] / max(1, 1024 * st["slot_tiles"]), 5) for m in range(3)]},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",

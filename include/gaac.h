@@ -248,6 +248,58 @@ GAAC_API int gaac_decompress(const gaac_entry* table, const int32_t* seq_lens, i
                     uint16_t* v_out, int64_t seq_stride, int64_t tok_stride, int64_t n_tok, int32_t* d_status,
                     void* stream);
 
+/*
+ * FP8 variant of the codec (Appendix B, "Relation to FP8 KV": the same
+ * exponent coding applied to a cache already quantised to FP8; lossless with
+ * respect to the FP8 values).  GAAC-FP8 tile format v1:
+ *  element   E4M3: sign(1) exponent(4) mantissa(3); E5M2: sign(1) exponent(5)
+ *            mantissa(2); sm = sign << mantissa_bits | mantissa
+ *  tile      64 x 128 FP8 bytes; storage order, groups, modes, codes, tags,
+ *            directory and escape area as in format v3, the windows inside the
+ *            format's 16 (E4M3: base4 is 0, no raw groups) or 32 exponents
+ *  slot      E4M3 (7,936 B): [0,4096) sm nibbles (element s in byte s/2, low
+ *            nibble for even s), [4096,7168) codes, [7168,7424) tags,
+ *            [7424,7440) directory, [7440,7936) escape area;
+ *            E5M2 (6,912 B): [0,3072) sm as 3-bit fields laid out like the
+ *            code plane, [3072,6144) codes, [6144,6400) tags, [6400,6416)
+ *            directory, [6416,6912) escape area
+ */
+enum { GAAC_FP8_E4M3 = 0, GAAC_FP8_E5M2 = 1 };
+
+/* Slot bytes of an FP8 format (0 for an unknown format). */
+GAAC_API int gaac_fp8_slot_bytes(int fmt);
+
+/*
+ * Windows of 8 and 16 exponents per (kv-head, channel) from FP8 calibration
+ * data x[t*tok_stride + h*128 + c], t < n_tok: the windows holding the most
+ * values, ties to the smallest base.  1 <= n_tok <= 65535.
+ */
+GAAC_API int gaac_fp8_calibrate(const uint8_t* x, int64_t n_tok, int64_t tok_stride, int n_kv_heads, int fmt,
+                                uint8_t* base3, uint8_t* base4, int32_t* d_status, void* stream);
+
+/*
+ * Encodes n_tiles FP8 tiles tiles[i][64][128] (token-major; 16-byte aligned)
+ * into slots[i][gaac_fp8_slot_bytes(fmt)] (16-byte aligned).  Tile i is K
+ * (tile_kind[i] = 0) or V (1) and uses bases row tile_row[i] of base3 / base4
+ * ([n_rows][128]).  esc_len[i] receives the escape-area length, or 0xFFFF when
+ * the tile does not fit its slot (the caller keeps it as FP8; its slot is not
+ * written).  stats may be NULL.  A bad kind or row sets GAAC_EINVAL in
+ * *d_status and esc_len[i] = 0xFFFF.
+ */
+GAAC_API int gaac_fp8_encode_tiles(const uint8_t* tiles, int64_t n_tiles, int fmt, const uint8_t* tile_kind,
+                                   const int32_t* tile_row, int n_rows, const uint8_t* base3, const uint8_t* base4,
+                                   uint8_t* slots, uint16_t* esc_len, gaac_stats* stats, int32_t* d_status,
+                                   void* stream);
+
+/*
+ * Decodes slot images back to FP8 tiles[i][64][128]; tiles whose esc_len is
+ * 0xFFFF are skipped (not written).  A failed check reports GAAC_EFORMAT.
+ */
+GAAC_API int gaac_fp8_decompress_tiles(const uint8_t* slots, const uint16_t* esc_len, int64_t n_tiles, int fmt,
+                                       const uint8_t* tile_kind, const int32_t* tile_row, int n_rows,
+                                       const uint8_t* base3, const uint8_t* base4, uint8_t* tiles, int32_t* d_status,
+                                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -88,6 +88,14 @@ def lib() -> ctypes.CDLL:
                                                         P, P]
             L.gaac_decode_attention_noalloc.restype = i32
             L.gaac_decompress.restype = i32
+            L.gaac_fp8_slot_bytes.argtypes = [i32]
+            L.gaac_fp8_slot_bytes.restype = i32
+            L.gaac_fp8_calibrate.argtypes = [P, i64, i64, i32, i32, P, P, P, P]
+            L.gaac_fp8_calibrate.restype = i32
+            L.gaac_fp8_encode_tiles.argtypes = [P, i64, i32, P, P, i32, P, P, P, P, P, P, P]
+            L.gaac_fp8_encode_tiles.restype = i32
+            L.gaac_fp8_decompress_tiles.argtypes = [P, P, i64, i32, P, P, i32, P, P, P, P, P]
+            L.gaac_fp8_decompress_tiles.restype = i32
             _lib = L
     return _lib
 
@@ -254,3 +262,41 @@ def decode_attention_noalloc(q, seq_lens, table, pools: Pools, base3, base4, sca
     _check("gaac_decode_attention_noalloc", lib().gaac_decode_attention_noalloc(
         q.data_ptr(), batch, hq, hkv, max_blocks, seq_lens.data_ptr(), table.data_ptr(), ctypes.byref(pc),
         base3.data_ptr(), base4.data_ptr(), float(scale), n_splits, out.data_ptr(), _ptr(status), _stream(stream)))
+
+
+# ---------------------------------------------------------------- FP8 variant of the codec
+FP8_E4M3, FP8_E5M2 = 0, 1
+FP8_NO_SLOT = 0xFFFF  # esc_len of a tile that stays FP8
+
+
+def fp8_slot_bytes(fmt: int) -> int:
+    return lib().gaac_fp8_slot_bytes(fmt)
+
+
+def fp8_calibrate(x: torch.Tensor, fmt: int, base3: torch.Tensor, base4: torch.Tensor, status=None,
+                  stream=None) -> None:
+    """x: uint8 FP8 bits [n_tok, kv_heads, 128] (token stride free); writes uint8 base3/base4 [kv_heads, 128]."""
+    _cuda(x, "x")
+    if x.dtype != torch.uint8 or x.dim() != 3 or x.shape[-1] != HEAD_DIM or x.stride(2) != 1 or x.stride(1) != HEAD_DIM:
+        raise ValueError("x must be uint8 [n_tok, kv_heads, 128] with contiguous heads and channels")
+    _check("gaac_fp8_calibrate", lib().gaac_fp8_calibrate(x.data_ptr(), x.shape[0], x.stride(0), x.shape[1], fmt,
+                                                           base3.data_ptr(), base4.data_ptr(), _ptr(status),
+                                                           _stream(stream)))
+
+
+def fp8_encode_tiles(tiles, fmt: int, tile_kind, tile_row, base3, base4, slots, esc_len, stats=None, status=None,
+                     stream=None) -> None:
+    """tiles: uint8 [n, 64, 128]; tile_kind: uint8 [n] (0 K, 1 V); tile_row: int32 [n] (row of base3/base4
+    [rows, 128]); slots: uint8 [n, fp8_slot_bytes(fmt)]; esc_len: int16 [n] (0xFFFF = stays FP8)."""
+    n = tiles.shape[0]
+    _check("gaac_fp8_encode_tiles", lib().gaac_fp8_encode_tiles(
+        tiles.data_ptr(), n, fmt, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0], base3.data_ptr(),
+        base4.data_ptr(), slots.data_ptr(), esc_len.data_ptr(), _ptr(stats), _ptr(status), _stream(stream)))
+
+
+def fp8_decompress_tiles(slots, esc_len, fmt: int, tile_kind, tile_row, base3, base4, tiles, status=None,
+                         stream=None) -> None:
+    n = tiles.shape[0]
+    _check("gaac_fp8_decompress_tiles", lib().gaac_fp8_decompress_tiles(
+        slots.data_ptr(), esc_len.data_ptr(), n, fmt, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
+        base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status), _stream(stream)))

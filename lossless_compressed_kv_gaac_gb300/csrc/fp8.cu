@@ -1,0 +1,451 @@
+// FP8 variant of the GAAC codec: calibration, tile encoder and decoder for
+// E4M3 and E5M2 KV tiles.
+//
+// "GAAC: Lossless KV Compression for Bandwidth-Efficient LLM Inference on
+// Personal Devices", Appendix B (Relation to FP8 KV): the same exponent coding
+// applied to a cache already quantised to FP8, lossless with respect to the FP8
+// values.  Section 3.1 gives the coding: windows of 8 and 16 exponents per
+// head-channel, groups of eight in 3-bit / 4-bit / raw mode, sign and mantissa
+// verbatim.  Layout: GAAC-FP8 tile format v1 (gaac.h) -- the format v3 storage
+// order, groups, codes, tags, directory and escape area, with the sign and
+// mantissa as 4-bit nibbles (E4M3) or 3-bit fields laid out like the code plane
+// (E5M2), and the exponent windows inside the format's 16 or 32 exponents.
+//
+// One CTA of 256 threads per tile; thread u owns the 32-element code unit u.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gaac {
+
+struct Fp8Layout {
+  int ew, mw, off_code, off_tag, off_dir, off_esc, slot;
+};
+
+__host__ __device__ inline bool fp8_layout(int fmt, Fp8Layout* L) {
+  if (fmt == GAAC_FP8_E4M3) {
+    *L = Fp8Layout{4, 3, 4096, 7168, 7424, 7440, 7936};
+    return true;
+  }
+  if (fmt == GAAC_FP8_E5M2) {
+    *L = Fp8Layout{5, 2, 3072, 6144, 6400, 6416, 6912};
+    return true;
+  }
+  return false;
+}
+
+constexpr int kFp8Threads = 256;
+
+// Calibration: one CTA per row of bases (kv-head), one thread per channel, a
+// histogram of the format's 16 or 32 exponents per channel in shared memory.
+__global__ void __launch_bounds__(kD) fp8_calibrate_kernel(const uint8_t* __restrict__ x, int64_t n_tok,
+                                                           int64_t tok_stride, int ew, int mw,
+                                                           uint8_t* __restrict__ base3, uint8_t* __restrict__ base4) {
+  __shared__ uint32_t hist[32][kD];
+  const int h = blockIdx.x, c = threadIdx.x;
+  const int nb = 1 << ew;
+  for (int b = 0; b < nb; ++b) hist[b][c] = 0u;
+  const uint8_t* p = x + static_cast<int64_t>(h) * kD + c;
+  for (int64_t t = 0; t < n_tok; ++t) hist[(p[t * tok_stride] >> mw) & (nb - 1)][c] += 1u;
+  // strict '>' keeps the smallest base on ties
+  uint32_t best3 = 0, best4 = 0;
+  int arg3 = 0, arg4 = 0;
+  for (int b = 0; b + 8 <= nb; ++b) {
+    uint32_t s = 0;
+    for (int i = 0; i < 8; ++i) s += hist[b + i][c];
+    if (b == 0 || s > best3) {
+      best3 = s;
+      arg3 = b;
+    }
+  }
+  for (int b = 0; b + 16 <= nb; ++b) {
+    uint32_t s = 0;
+    for (int i = 0; i < 16; ++i) s += hist[b + i][c];
+    if (b == 0 || s > best4) {
+      best4 = s;
+      arg4 = b;
+    }
+  }
+  base3[h * kD + c] = static_cast<uint8_t>(arg3);
+  base4[h * kD + c] = static_cast<uint8_t>(arg4);
+}
+
+__device__ __forceinline__ int fp8_channel_of(int kind, int s) { return kind == 0 ? (s & 127) : v_channel_of(s); }
+
+// Three 3-bit-per-element words of a 32-element unit (the code plane's layout):
+// v[j] is element j's field.
+__device__ __forceinline__ void pack_field3(const uint32_t v[32], uint32_t W[3]) {
+  W[0] = W[1] = W[2] = 0u;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int L = 0; L < 4; ++L) {
+      const uint32_t c0 = v[16 * h + L], c1 = v[16 * h + 4 + L], c2 = v[16 * h + 8 + L], c3 = v[16 * h + 12 + L];
+      W[h] |= (c0 | (c1 << 3) | ((c3 & 3u) << 6)) << (8 * L);
+      W[2] |= ((c2 << (3 * h)) | (((c3 >> 2) & 1u) << (6 + h))) << (8 * L);
+    }
+  }
+}
+
+// Element j's 3-bit field from the unit's three words.
+__device__ __forceinline__ uint32_t field3(const uint32_t W[3], int j) {
+  const int h = j >> 4, jj = j & 15, L = jj & 3, q = jj >> 2;
+  const uint32_t wh = (W[h] >> (8 * L)) & 0xFFu, w2 = (W[2] >> (8 * L)) & 0xFFu;
+  if (q == 0) return wh & 7u;
+  if (q == 1) return (wh >> 3) & 7u;
+  if (q == 2) return (w2 >> (3 * h)) & 7u;
+  return ((wh >> 6) & 3u) | (((w2 >> (6 + h)) & 1u) << 2);
+}
+
+struct Fp8Args {
+  const uint8_t* tiles;
+  int64_t n_tiles;
+  Fp8Layout L;
+  const uint8_t* tile_kind;
+  const int32_t* tile_row;
+  int n_rows;
+  const uint8_t* base3;
+  const uint8_t* base4;
+  uint8_t* slots;
+  uint16_t* esc_len;
+  gaac_stats* stats;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
+  __shared__ alignas(16) uint8_t seq[kTile];  // the tile in storage order
+  __shared__ int warp_sums[kFp8Threads / 32];
+  __shared__ int mode_counts[4];
+  const int64_t tile = blockIdx.x;
+  const int u = threadIdx.x, lane = u & 31, warp = u >> 5;
+  const int kind = a.tile_kind[tile], row = a.tile_row[tile];
+  if ((kind != 0 && kind != 1) || row < 0 || row >= a.n_rows) {
+    if (u == 0) {
+      a.esc_len[tile] = 0xFFFFu;
+      report(a.status, GAAC_EINVAL);
+    }
+    return;
+  }
+  const Fp8Layout L = a.L;
+  const uint8_t* src = a.tiles + tile * kTile;
+  {  // stage: 32 bytes per thread, storage order
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + 32 * u);
+    const uint4 x0 = s4[0], x1 = s4[1];
+    if (kind == 0) {
+      uint4* d = reinterpret_cast<uint4*>(seq + 32 * u);
+      d[0] = x0;
+      d[1] = x1;
+    } else {
+      const uint8_t* xb0 = reinterpret_cast<const uint8_t*>(&x0);
+      const uint8_t* xb1 = reinterpret_cast<const uint8_t*>(&x1);
+      const int t = u >> 2, c0 = 32 * (u & 3);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) seq[v_storage_index(t, c0 + i)] = i < 16 ? xb0[i] : xb1[i - 16];
+    }
+  }
+  if (u < 4) mode_counts[u] = 0;
+  __syncthreads();
+  const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
+  const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
+  const uint32_t emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
+  uint32_t code[32], smv[32], ex[32];
+  uint32_t esc4 = 0, tagbyte = 0;
+  int n4 = 0, nraw = 0, my_counts[3] = {0, 0, 0};
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    uint32_t e[8];
+    int b3[8], b4[8];
+    bool fits3 = true, fits4 = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int el = 8 * gi + j;
+      const uint32_t x = seq[32 * u + el];
+      e[j] = (x >> L.mw) & emask;
+      ex[el] = e[j];
+      smv[el] = ((x >> 7) << L.mw) | (x & mmask);
+      const int c = fp8_channel_of(kind, 32 * u + el);
+      b3[j] = b3g[c];
+      b4[j] = b4g[c];
+      const int o3 = static_cast<int>(e[j]) - b3[j], o4 = static_cast<int>(e[j]) - b4[j];
+      fits3 = fits3 && o3 >= 0 && o3 <= 7;
+      fits4 = fits4 && o4 >= 0 && o4 <= 15;
+    }
+    const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
+    tagbyte |= mode << (2 * gi);
+    my_counts[mode] += 1;
+    uint32_t eb = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t cd = 0;  // raw groups keep code 0: their exponents are escape bytes
+      if (mode == 0u) {
+        cd = (e[j] - static_cast<uint32_t>(b3[j])) & 7u;
+      } else if (mode == 1u) {
+        const uint32_t off = (e[j] - static_cast<uint32_t>(b4[j])) & 0xFFu;
+        cd = off & 7u;
+        eb |= ((off >> 3) & 1u) << j;
+      }
+      code[8 * gi + j] = cd;
+    }
+    if (mode == 1u) {
+      esc4 |= eb << (8 * n4);
+      n4 += 1;
+    }
+    if (mode == 2u) nraw += 1;
+  }
+  // exclusive scans of the 4-bit and raw group counts (packed; each total is at most 1024)
+  const int packed = n4 | (nraw << 16);
+  int incl = packed;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kFp8Threads / 32; ++w) {
+    const int s = warp_sums[w];
+    if (w < warp) before += s;
+    total += s;
+  }
+  const int excl = before + incl - packed;
+  const int off4 = excl & 0xFFFF, offraw = excl >> 16, tot4 = total & 0xFFFF, totraw = total >> 16;
+  const int esc = tot4 + 8 * totraw;
+  if (esc > kEscCap) {  // CTA-uniform: the tile stays FP8
+    if (u == 0) {
+      a.esc_len[tile] = 0xFFFFu;
+      if (a.stats != nullptr) atomicAdd(&a.stats->raw_tiles, 1ull);
+    }
+    return;
+  }
+  uint8_t* slot = a.slots + tile * L.slot;
+  // sign|mantissa plane
+  if (L.ew == 4) {  // nibble of element s in byte s/2 (low nibble for even s): 16 bytes per unit
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int el = 0; el < 32; ++el) w[el >> 3] |= smv[el] << (4 * (el & 7));
+    *reinterpret_cast<uint4*>(slot + 16 * u) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {  // 3-bit fields laid out like the code plane, at offset 0
+    uint32_t W[3];
+    pack_field3(smv, W);
+    uint32_t* sw = reinterpret_cast<uint32_t*>(slot);
+    sw[u] = W[0];
+    sw[256 + u] = W[1];
+    sw[512 + u] = W[2];
+  }
+  {
+    uint32_t W[3];
+    pack_field3(code, W);
+    uint32_t* cw = reinterpret_cast<uint32_t*>(slot + L.off_code);
+    cw[u] = W[0];
+    cw[256 + u] = W[1];
+    cw[512 + u] = W[2];
+  }
+  slot[L.off_tag + u] = static_cast<uint8_t>(tagbyte);
+  uint8_t* escp = slot + L.off_esc;
+  for (int k = 0; k < n4; ++k) escp[off4 + k] = static_cast<uint8_t>(esc4 >> (8 * k));
+  if (nraw) {
+    int r = tot4 + 8 * offraw;
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      if (((tagbyte >> (2 * gi)) & 3u) != 2u) continue;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) escp[r + j] = static_cast<uint8_t>(ex[8 * gi + j]);
+      r += 8;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int at = 2 * u + i;
+    if (at >= esc && at < kEscCap) escp[at] = 0;
+  }
+  if ((u & (kDirUnits - 1)) == kDirUnits - 1) {
+    const int w = u / kDirUnits;
+    const uint32_t entry = ((off4 + n4) & 0x1FF) | (((offraw + nraw) & 0x7F) << 9);
+    slot[L.off_dir + 2 * w] = static_cast<uint8_t>(entry & 0xFFu);
+    slot[L.off_dir + 2 * w + 1] = static_cast<uint8_t>(entry >> 8);
+  }
+  if (u == 0) a.esc_len[tile] = static_cast<uint16_t>(esc);
+  if (a.stats != nullptr) {
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+      if (my_counts[m]) atomicAdd(&mode_counts[m], my_counts[m]);
+    __syncthreads();
+    if (u == 0) {
+#pragma unroll
+      for (int m = 0; m < 3; ++m) atomicAdd(&a.stats->groups[m], static_cast<unsigned long long>(mode_counts[m]));
+      atomicAdd(&a.stats->escape_bytes, static_cast<unsigned long long>(esc));
+      atomicAdd(&a.stats->slot_tiles, 1ull);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, uint8_t* __restrict__ out) {
+  __shared__ alignas(16) uint8_t logical[kTile];
+  __shared__ int word_prefix[65];
+  const int64_t tile = blockIdx.x;
+  const int u = threadIdx.x;
+  const int kind = a.tile_kind[tile], row = a.tile_row[tile];
+  const int esc_len = a.esc_len[tile];
+  if (esc_len == 0xFFFF) return;  // kept as FP8 by the caller
+  if ((kind != 0 && kind != 1) || row < 0 || row >= a.n_rows || esc_len > kEscCap) {
+    if (u == 0) report(a.status, GAAC_EINVAL);
+    return;
+  }
+  const Fp8Layout L = a.L;
+  const uint8_t* slot = a.slots + tile * L.slot;
+  const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + L.off_tag);
+  if (u < 32) {  // exclusive prefixes of 4-bit and raw group counts over the 64 tag words (packed)
+    const int c0 = n4_of(tagw[u]) | (nraw_of(tagw[u]) << 16);
+    const int c1 = n4_of(tagw[u + 32]) | (nraw_of(tagw[u + 32]) << 16);
+    int i0 = c0, i1 = c1;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v0 = __shfl_up_sync(0xFFFFFFFFu, i0, d), v1 = __shfl_up_sync(0xFFFFFFFFu, i1, d);
+      if (u >= d) {
+        i0 += v0;
+        i1 += v1;
+      }
+    }
+    const int tot0 = __shfl_sync(0xFFFFFFFFu, i0, 31);
+    word_prefix[u] = i0 - c0;
+    word_prefix[u + 32] = tot0 + i1 - c1;
+    if (u == 31) word_prefix[64] = tot0 + i1;
+  }
+  __syncthreads();
+  const uint32_t tagbyte = slot[L.off_tag + u];
+  const uint32_t before = tagw[u >> 2] & ((1u << (8 * (u & 3))) - 1u);
+  const int pre = word_prefix[u >> 2] + (n4_of(before) | (nraw_of(before) << 16));
+  const int tot = word_prefix[64], tot4 = tot & 0xFFFF, totraw = tot >> 16;
+  int o4 = pre & 0xFFFF, oraw = tot4 + 8 * (pre >> 16);
+  const uint16_t* dir = reinterpret_cast<const uint16_t*>(slot + L.off_dir);
+  bool bad = reserved_in(tagbyte);
+  if ((u & (kDirUnits - 1)) == 0 && u > 0 &&
+      dir[u / kDirUnits - 1] != static_cast<uint16_t>(((pre & 0xFFFF) & 0x1FF) | (((pre >> 16) & 0x7F) << 9)))
+    bad = true;
+  if (u == 255 && (dir[7] != static_cast<uint16_t>((tot4 & 0x1FF) | ((totraw & 0x7F) << 9)) ||
+                   tot4 + 8 * totraw != esc_len))
+    bad = true;
+  uint32_t C[3], S[3] = {0u, 0u, 0u};
+  const uint32_t* cw = reinterpret_cast<const uint32_t*>(slot + L.off_code);
+  C[0] = cw[u];
+  C[1] = cw[256 + u];
+  C[2] = cw[512 + u];
+  uint4 nib = make_uint4(0u, 0u, 0u, 0u);
+  if (L.ew == 4) {
+    nib = *reinterpret_cast<const uint4*>(slot + 16 * u);
+  } else {
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(slot);
+    S[0] = sw[u];
+    S[1] = sw[256 + u];
+    S[2] = sw[512 + u];
+  }
+  const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
+  const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
+  const uint32_t emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
+  const uint32_t nw[4] = {nib.x, nib.y, nib.z, nib.w};
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    const uint32_t mode = (tagbyte >> (2 * gi)) & 3u;
+    uint32_t x4 = 0;
+    if (mode == 1u) {
+      if (o4 < esc_len) x4 = slot[L.off_esc + o4];
+      else bad = true;
+      o4 += 1;
+    }
+    const bool rawok = mode == 2u && oraw + 8 <= esc_len;
+    if (mode == 2u && !rawok) bad = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int el = 8 * gi + j, s = 32 * u + el;
+      const int c = fp8_channel_of(kind, s);
+      const uint32_t cd = field3(C, el);
+      uint32_t e;
+      if (mode == 0u) e = b3g[c] + cd;
+      else if (mode == 1u) e = b4g[c] + (cd | (((x4 >> j) & 1u) << 3));
+      else e = rawok ? slot[L.off_esc + oraw + j] : 0u;
+      const uint32_t sm = L.ew == 4 ? (nw[el >> 3] >> (4 * (el & 7))) & 15u : field3(S, el);
+      const uint8_t x = static_cast<uint8_t>(((sm >> L.mw) << 7) | ((e & emask) << L.mw) | (sm & mmask));
+      const int t = kind == 0 ? (s >> 7) : v_token_of(s);
+      logical[t * kD + c] = x;
+    }
+    if (mode == 2u) oraw += 8;
+  }
+  if (bad) report(a.status, GAAC_EFORMAT);
+  __syncthreads();
+  uint4* d = reinterpret_cast<uint4*>(out + tile * kTile);
+  const uint4* s4 = reinterpret_cast<const uint4*>(logical);
+  d[2 * u] = s4[2 * u];
+  d[2 * u + 1] = s4[2 * u + 1];
+}
+
+}  // namespace gaac
+
+using namespace gaac;
+
+extern "C" int gaac_fp8_slot_bytes(int fmt) {
+  Fp8Layout L;
+  return fp8_layout(fmt, &L) ? L.slot : 0;
+}
+
+extern "C" int gaac_fp8_calibrate(const uint8_t* x, int64_t n_tok, int64_t tok_stride, int n_kv_heads, int fmt,
+                                  uint8_t* base3, uint8_t* base4, int32_t* d_status, void* stream) {
+  (void)d_status;
+  Fp8Layout L;
+  if (x == nullptr || base3 == nullptr || base4 == nullptr || !fp8_layout(fmt, &L)) return GAAC_EINVAL;
+  if (n_tok < 1 || n_tok > 65535 || n_kv_heads <= 0 || n_kv_heads > 65535 || tok_stride < n_kv_heads * kD)
+    return GAAC_EINVAL;
+  fp8_calibrate_kernel<<<n_kv_heads, kD, 0, static_cast<cudaStream_t>(stream)>>>(x, n_tok, tok_stride, L.ew, L.mw,
+                                                                                  base3, base4);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
+
+static int fp8_args(const uint8_t* tiles, int64_t n_tiles, int fmt, const uint8_t* tile_kind, const int32_t* tile_row,
+                    int n_rows, const uint8_t* base3, const uint8_t* base4, uint8_t* slots, uint16_t* esc_len,
+                    gaac_stats* stats, int32_t* d_status, Fp8Args* a) {
+  if (tiles == nullptr || tile_kind == nullptr || tile_row == nullptr || base3 == nullptr || base4 == nullptr ||
+      slots == nullptr || esc_len == nullptr || n_tiles < 0 || n_tiles > 0x7FFFFFFFLL || n_rows <= 0)
+    return GAAC_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(tiles) & 15u) || (reinterpret_cast<uintptr_t>(slots) & 15u)) return GAAC_EINVAL;
+  if (!fp8_layout(fmt, &a->L)) return GAAC_EINVAL;
+  a->tiles = tiles;
+  a->n_tiles = n_tiles;
+  a->tile_kind = tile_kind;
+  a->tile_row = tile_row;
+  a->n_rows = n_rows;
+  a->base3 = base3;
+  a->base4 = base4;
+  a->slots = slots;
+  a->esc_len = esc_len;
+  a->stats = stats;
+  a->status = d_status;
+  return GAAC_OK;
+}
+
+extern "C" int gaac_fp8_encode_tiles(const uint8_t* tiles, int64_t n_tiles, int fmt, const uint8_t* tile_kind,
+                                     const int32_t* tile_row, int n_rows, const uint8_t* base3, const uint8_t* base4,
+                                     uint8_t* slots, uint16_t* esc_len, gaac_stats* stats, int32_t* d_status,
+                                     void* stream) {
+  Fp8Args a;
+  const int st = fp8_args(tiles, n_tiles, fmt, tile_kind, tile_row, n_rows, base3, base4, slots, esc_len, stats,
+                          d_status, &a);
+  if (st != GAAC_OK) return st;
+  if (n_tiles == 0) return GAAC_OK;
+  fp8_encode_kernel<<<static_cast<unsigned>(n_tiles), kFp8Threads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
+
+extern "C" int gaac_fp8_decompress_tiles(const uint8_t* slots, const uint16_t* esc_len, int64_t n_tiles, int fmt,
+                                         const uint8_t* tile_kind, const int32_t* tile_row, int n_rows,
+                                         const uint8_t* base3, const uint8_t* base4, uint8_t* tiles,
+                                         int32_t* d_status, void* stream) {
+  Fp8Args a;
+  const int st = fp8_args(tiles, n_tiles, fmt, tile_kind, tile_row, n_rows, base3, base4,
+                          const_cast<uint8_t*>(slots), const_cast<uint16_t*>(esc_len), nullptr, d_status, &a);
+  if (st != GAAC_OK) return st;
+  if (n_tiles == 0) return GAAC_OK;
+  fp8_decompress_kernel<<<static_cast<unsigned>(n_tiles), kFp8Threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      a, tiles);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
