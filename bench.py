@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--layers", type=int, default=36, help="layers per step (36 = the Qwen3-8B workload)")
     p.add_argument("--cpu-units", type=int, default=48, help="(layer, kv-head) units in the CPU oracle sample")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--study", choices=["rope-drift"], default=None,
+                   help="rope-drift: escape bytes per tile along 32K rotary keys for short and long calibration")
     return p.parse_args()
 
 
@@ -528,8 +530,45 @@ def run_reference(args):
     }), flush=True)
 
 
+def rope_drift_study() -> dict:
+    """The positional-drift study of the GAAC page's Appendix C on synthetic rotary keys: a 32,768-token
+    sequence (8 kv-heads, the Qwen3-8B-shaped workload's channel scales, rotary base 1e6) is encoded with
+    windows calibrated on its first 2K, 8K or all 32K tokens; per 4,096-token segment it reports the mean
+    escape bytes of the K and V tiles kept in slots and the share of tiles that fell back to BF16."""
+    import torch
+
+    import gaac_workloads as W
+    import lossless_compressed_kv_gaac_gb300 as G
+    from lossless_compressed_kv_gaac_gb300.cache import LayerCache
+
+    T, H, seg = 32768, 8, 4096
+    k, v = W.make_kv(CONFIG_ID, 0, 1, T, H, device="cuda", rope_theta=1e6)
+    lens = torch.tensor([T], dtype=torch.int32, device="cuda")
+    out = {"study": "rope-drift", "tokens": T, "kv_heads": H, "segment_tokens": seg, "rope_theta": 1e6, "calibration": {}}
+    for n_cal in (2048, 8192, 32768):
+        c = LayerCache(1, H, T // 64, device="cuda", n_raw=2 * H * (T // 64) + 16)
+        c.calibrate(k[0, :n_cal], v[0, :n_cal])
+        c.encode(k, v, lens)
+        torch.cuda.synchronize()
+        _, esc, mode, _ = G.entry_fields(c.table)
+        esc, mode = esc[0].cpu(), mode[0].cpu()  # [blocks, heads, K|V]
+        row = {}
+        for kv, name in ((0, "k"), (1, "v")):
+            e = esc[:, :, kv].view(T // seg, -1).double()
+            m = mode[:, :, kv].view(T // seg, -1)
+            slot = m == G.MODE_SLOT
+            row[name + "_esc_bytes_per_slot_tile"] = [round(float(e[i][slot[i]].mean()), 1) if slot[i].any() else None
+                                                       for i in range(T // seg)]
+            row[name + "_raw_tile_share"] = [round(float((~slot[i]).double().mean()), 4) for i in range(T // seg)]
+        out["calibration"][str(n_cal)] = row
+    return out
+
+
 def main():
     args = parse()
+    if args.study == "rope-drift":
+        print(json.dumps(rope_drift_study()))
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -14,6 +14,11 @@ Values are drawn in fp32 and rounded to BF16 (round to nearest even).  Channel
 scales are shared by every sequence of a layer.  Every stream has its own seed
 1_000_003*config + 1009*layer + stream so each piece is reproducible alone.
 
+Rotary keys (for the positional-drift study of the GAAC page's Appendix C):
+make_kv(..., rope_theta=1e6) rotates the fp32 keys before rounding, channel
+pairs (c, c+64) by the angle t * theta^(-2c/128) at position t (the half-split
+rotary convention of the Qwen3 family, whose rotary base is 1e6).
+
 Model shapes follow the Qwen3 table of the Transformer-FSQ page (appendix,
 models and memory): 0.6B and 1.7B have 28 layers, 16 query / 8 kv heads;
 8B has 36 layers, 32 query / 8 kv heads; head width 128 throughout.
@@ -85,8 +90,19 @@ def channel_scales(config: int, layer: int, n_kv_heads: int, device="cpu"):
     return sk, sv
 
 
+def rope(k: torch.Tensor, theta: float, first_pos: int = 0) -> torch.Tensor:
+    """Rotary position rotation of fp32 keys [..., n_tok, heads, 128] at positions first_pos + t."""
+    n_tok = k.shape[-3]
+    pos = torch.arange(n_tok, dtype=torch.float64, device=k.device) + first_pos
+    inv = theta ** (-torch.arange(HEAD_DIM // 2, dtype=torch.float64, device=k.device) * 2.0 / HEAD_DIM)
+    ang = pos[:, None] * inv[None, :]
+    cos, sin = torch.cos(ang).float()[:, None, :], torch.sin(ang).float()[:, None, :]
+    x1, x2 = k[..., : HEAD_DIM // 2], k[..., HEAD_DIM // 2:]
+    return torch.cat([x1 * cos - x2 * sin, x2 * cos + x1 * sin], dim=-1)
+
+
 def make_kv(config: int, layer: int, batch: int, n_tok: int, n_kv_heads: int, device="cpu",
-            adversarial: float = 0.0, n_clean: int = 512, token_offset: int = 0):
+            adversarial: float = 0.0, n_clean: int = 512, token_offset: int = 0, rope_theta: float = 0.0):
     """BF16 (K, V), each [batch][n_tok][n_kv_heads][128].
 
     token_offset selects a different seed stream so that appended tokens are
@@ -97,7 +113,10 @@ def make_kv(config: int, layer: int, batch: int, n_tok: int, n_kv_heads: int, de
     sk, sv = channel_scales(config, layer, n_kv_heads, device)
     shape = (batch, n_tok, n_kv_heads, HEAD_DIM)
     ks, vs = (S_K, S_V) if token_offset == 0 else (10_000 + 2 * token_offset, 10_001 + 2 * token_offset)
-    k = (torch.randn(shape, generator=_gen(device, config, layer, ks), device=device) * sk).to(torch.bfloat16)
+    k = torch.randn(shape, generator=_gen(device, config, layer, ks), device=device) * sk
+    if rope_theta > 0.0:
+        k = rope(k, rope_theta, token_offset)
+    k = k.to(torch.bfloat16)
     v = (torch.randn(shape, generator=_gen(device, config, layer, vs), device=device) * sv).to(torch.bfloat16)
     if adversarial > 0.0:
         g = _gen(device, config, layer, S_ADV_MASK)
