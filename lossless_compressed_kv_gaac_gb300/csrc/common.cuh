@@ -18,7 +18,6 @@ constexpr int kD = 128;
 constexpr int kBlock = 64;
 constexpr int kTile = 8192;
 constexpr int kOffCode = 8192;
-constexpr int kPlaneBytes = 1024;  // one code plane: 256 words
 constexpr int kOffTag = 11264;
 constexpr int kOffDir = 11520;  // escape directory: 8 x u16, entry w = n4 | nraw << 9 over eighths 0..w
 constexpr int kOffEsc = 11536;  // escape area: 4-bit escape bytes, then 8 exponent bytes per raw group
@@ -155,10 +154,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // One poll; the thread may sleep up to ~20 us inside it (woken early when the
 // phase completes), so a waiting warp takes few issue slots from working warps.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -167,17 +162,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity), "r"(20000)
-      : "memory");
-  return ok != 0u;
-}
-
-// One non-blocking poll.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return ok != 0u;
 }
@@ -199,10 +183,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // D += A * B, m16n8k16, BF16 inputs, FP32 accumulate.
