@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             L.gaac_ref_escape_bytes_of_mode.restype = i32
             L.gaac_ref_attention.argtypes = [P, P, P, i64, i64, i32, i32, ctypes.c_double, P, P, P]
             L.gaac_ref_attention.restype = None
+            L.gaac_ref_attention_d.argtypes = [P, P, P, i64, i64, i32, i32, i32, ctypes.c_double, P, P, P]
+            L.gaac_ref_attention_d.restype = None
             L.gaac_ref_fp8_slot_bytes.argtypes = [i32]
             L.gaac_ref_fp8_slot_bytes.restype = i32
             L.gaac_ref_fp8_calibrate.argtypes = [P, i64, i64, i32, i32, P, P]
@@ -175,19 +177,19 @@ def escape_bytes_of_mode(mode: int) -> int:
 
 def attention(q, k, v, scale: float):
     """fp64 decode attention of one sequence.
-    q: uint16 [Hq][128]; k, v: uint16 [T][Hkv][128] (BF16 bits).
-    Returns (out float64 [Hq][128], flags int32 [Hq])."""
+    q: uint16 [Hq][d]; k, v: uint16 [T][Hkv][d] (BF16 bits), d = 128 or 256.
+    Returns (out float64 [Hq][d], flags int32 [Hq])."""
     q = _u16(q)
     k = _u16(k)
     v = _u16(v)
-    Hq = q.shape[0]
-    T, Hkv, d = k.shape
-    assert d == D and v.shape == k.shape and Hq % Hkv == 0
-    out = np.zeros((Hq, D), np.float64)
+    Hq, d = q.shape
+    T, Hkv, dk = k.shape
+    assert dk == d and d in (128, 256) and v.shape == k.shape and Hq % Hkv == 0
+    out = np.zeros((Hq, d), np.float64)
     flags = np.zeros(Hq, np.int32)
     scratch = np.zeros(max(T, 1), np.float64)
-    lib().gaac_ref_attention(_ptr(q), _ptr(k), _ptr(v), Hkv * D, T, Hq, Hkv, float(scale), _ptr(out), _ptr(flags),
-                             _ptr(scratch))
+    lib().gaac_ref_attention_d(_ptr(q), _ptr(k), _ptr(v), Hkv * d, T, Hq, Hkv, d, float(scale), _ptr(out),
+                               _ptr(flags), _ptr(scratch))
     return out, flags
 
 

@@ -522,7 +522,10 @@ void gaac_ref_fp8_mode_counts(const uint8_t* img, int fmt, int64_t* counts4) {
 
 /* ---- decode attention in fp64 (section 3.2; grouped-query heads share a
  * kv-head, q head h reads kv-head h / (Hq/Hkv)).
- * q[hq*128 + c]; k, v: element (t, hk, c) at t*tok_stride + hk*128 + c.
+ * q[hq*d + c]; k, v: element (t, hk, c) at t*tok_stride + hk*d + c; d = 128, or 256
+ * for a head the storage splits into two 128-channel half-heads (Appendix D:
+ * a 256-dimensional head is represented as two 128-dimensional half-heads; the
+ * attention still runs over the whole head).
  * out[hq*128 + c] = sum_t softmax_t(scale * q.k_t) v_t[c]; T == 0 gives zeros.
  * flags (may be NULL), per q head: bit 0 set if some token's sum_c |q_c k_tc|
  * reaches 2^130 (a dot product of q/16 and k, or its product with the scale,
@@ -537,20 +540,20 @@ static double bf16_to_double(uint16_t x) {
     return (double)f;
 }
 
-void gaac_ref_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t tok_stride, int64_t T,
-                        int Hq, int Hkv, double scale, double* out, int32_t* flags, double* logits_scratch) {
+void gaac_ref_attention_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t tok_stride, int64_t T,
+                          int Hq, int Hkv, int d, double scale, double* out, int32_t* flags, double* logits_scratch) {
     int r = Hq / Hkv;
     for (int hq = 0; hq < Hq; ++hq) {
         int hk = hq / r;
         int32_t flag = 0;
-        for (int c = 0; c < ORC_D; ++c) out[hq * ORC_D + c] = 0.0;
+        for (int c = 0; c < d; ++c) out[hq * d + c] = 0.0;
         if (T == 0) { if (flags) flags[hq] = 0; continue; }
         double m = -INFINITY;
         for (int64_t t = 0; t < T; ++t) {
             double dot = 0.0, mag = 0.0;
-            for (int c = 0; c < ORC_D; ++c) {
-                double qc = bf16_to_double(q[hq * ORC_D + c]);
-                double kc = bf16_to_double(k[t * tok_stride + hk * ORC_D + c]);
+            for (int c = 0; c < d; ++c) {
+                double qc = bf16_to_double(q[hq * d + c]);
+                double kc = bf16_to_double(k[t * tok_stride + hk * d + c]);
                 dot += qc * kc;
                 mag += fabs(qc * kc);
             }
@@ -564,16 +567,21 @@ void gaac_ref_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
             logits_scratch[t] = w;
             l += w;
         }
-        for (int c = 0; c < ORC_D; ++c) {
+        for (int c = 0; c < d; ++c) {
             double acc = 0.0, mag = 0.0;
             for (int64_t t = 0; t < T; ++t) {
-                double vc = bf16_to_double(v[t * tok_stride + hk * ORC_D + c]);
+                double vc = bf16_to_double(v[t * tok_stride + hk * d + c]);
                 acc += logits_scratch[t] * vc;
                 mag += logits_scratch[t] * fabs(vc);
             }
             if (mag > 3.4028234663852886e38) flag |= 2;
-            out[hq * ORC_D + c] = acc / l;
+            out[hq * d + c] = acc / l;
         }
         if (flags) flags[hq] = flag;
     }
+}
+
+void gaac_ref_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t tok_stride, int64_t T,
+                        int Hq, int Hkv, double scale, double* out, int32_t* flags, double* logits_scratch) {
+    gaac_ref_attention_d(q, k, v, tok_stride, T, Hq, Hkv, ORC_D, scale, out, flags, logits_scratch);
 }

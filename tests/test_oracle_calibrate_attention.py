@@ -167,3 +167,27 @@ def test_attention_on_decoded_cache_equals_original(orc):
     o1, _ = orc.attention(q, kb, vb, 1 / np.sqrt(128))
     o2, _ = orc.attention(q, kd, vd, 1 / np.sqrt(128))
     np.testing.assert_array_equal(o1, o2)
+
+
+def test_attention_256_dim_heads(orc):
+    """A 256-dimensional head (stored as two 128-channel half-heads) attends over the whole head:
+    its output equals float64 numpy, and with the second half of q zero its weights are those of
+    the 128-dimensional attention on the first halves."""
+    rng = np.random.default_rng(256)
+    T, Hq, Hkv = 37, 4, 2
+    q = _f32_to_bf16_bits(rng.normal(size=(Hq, 256)))
+    k = _f32_to_bf16_bits(rng.normal(size=(T, Hkv, 256)))
+    v = _f32_to_bf16_bits(rng.normal(size=(T, Hkv, 256)))
+    out, _ = orc.attention(q, k, v, 1 / 16)
+    qf, kf, vf = _bf16_to_f64(q), _bf16_to_f64(k), _bf16_to_f64(v)
+    for h in range(Hq):
+        s = kf[:, h // 2] @ qf[h] / 16
+        w = np.exp(s - s.max())
+        np.testing.assert_allclose(out[h], (w / w.sum()) @ vf[:, h // 2], rtol=1e-12, atol=1e-12)
+    q0 = q.copy()
+    q0[:, 128:] = 0
+    out0, _ = orc.attention(q0, k, v, 1 / 16)
+    lo, _ = orc.attention(q0[:, :128], k[:, :, :128], v[:, :, :128], 1 / 16)
+    hi, _ = orc.attention(q0[:, :128], k[:, :, :128], v[:, :, 128:], 1 / 16)
+    np.testing.assert_allclose(out0[:, :128], lo, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out0[:, 128:], hi, rtol=1e-12, atol=1e-12)
