@@ -206,6 +206,26 @@ GAAC_API int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, 
                           void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream);
 
 /*
+ * Decode attention for 256-channel heads (Appendix D: a 256-dimensional head is
+ * stored as two 128-dimensional half-heads).  The cache holds 2 * n_kv_heads
+ * half-heads: half-head 2h + j is channels [128 j, 128 j + 128) of kv-head h,
+ * in the table ([batch][max_blocks][2 * n_kv_heads][2]) and in base3 / base4
+ * ([2][2 * n_kv_heads][128]), i.e. the cache of a [batch][T][n_kv_heads][256]
+ * K/V viewed as [batch][T][2 * n_kv_heads][128].  The attention runs over the
+ * whole 256-channel head:
+ *   out[b][hq][c] = sum_t softmax_t(scale * q[b][hq] . k[b][t][hk]) v[b][t][hk][c], c < 256
+ * q: BF16 bits [batch][n_q_heads][256]; out: fp32 [batch][n_q_heads][256].
+ * workspace: at least gaac_attention_workspace(batch, 2 * n_kv_heads, max_blocks,
+ * n_splits) bytes; n_splits = 0 picks gaac_attention_auto_splits(batch,
+ * 2 * n_kv_heads, max_blocks).  Everything else as gaac_decode_attention.
+ */
+GAAC_API int gaac_decode_attention_hd256(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
+                                         const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
+                                         const uint8_t* base3, const uint8_t* base4, float scale, int n_splits,
+                                         float* out, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                         void* stream);
+
+/*
  * Allocation-free decode attention.  The GAAC page has no counterpart; this is a
  * convenience of this library for callers that cannot allocate device memory
  * when they call it, such as a serving loop whose memory plan is fixed after

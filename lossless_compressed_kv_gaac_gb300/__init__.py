@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
             L.gaac_decode_attention.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, ctypes.c_float, i32, P, P, sz,
                                                 P, P]
             L.gaac_decode_attention.restype = i32
+            L.gaac_decode_attention_hd256.argtypes = L.gaac_decode_attention.argtypes
+            L.gaac_decode_attention_hd256.restype = i32
             L.gaac_decompress.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, i64, i64, i64, P, P]
             L.gaac_decode_attention_noalloc.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, ctypes.c_float, i32, P,
                                                         P, P]
@@ -300,3 +302,19 @@ def fp8_decompress_tiles(slots, esc_len, fmt: int, tile_kind, tile_row, base3, b
     _check("gaac_fp8_decompress_tiles", lib().gaac_fp8_decompress_tiles(
         slots.data_ptr(), esc_len.data_ptr(), n, fmt, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
         base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status), _stream(stream)))
+
+
+def decode_attention_hd256(q, seq_lens, table, pools: Pools, base3, base4, scale: float, out, workspace,
+                           n_splits: int = 0, status=None, stream=None) -> None:
+    """Attention over 256-channel heads stored as two 128-channel half-heads: q BF16 [batch, n_q_heads, 256],
+    table [batch, max_blocks, 2 * n_kv_heads, 2], base3/base4 [2, 2 * n_kv_heads, 128], out fp32
+    [batch, n_q_heads, 256]; workspace >= attention_workspace(batch, 2 * n_kv_heads, max_blocks, n_splits)."""
+    B, Hq, d = q.shape
+    if d != 256 or out.shape != (B, Hq, 256):
+        raise ValueError("q and out must be [batch, n_q_heads, 256]")
+    n_kv = table.shape[2] // 2
+    pc = pools.c()
+    _check("gaac_decode_attention_hd256", lib().gaac_decode_attention_hd256(
+        q.data_ptr(), B, Hq, n_kv, table.shape[1], seq_lens.data_ptr(), table.data_ptr(), ctypes.byref(pc),
+        base3.data_ptr(), base4.data_ptr(), float(scale), n_splits, out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))

@@ -54,25 +54,30 @@ constexpr int kGroupWarps = 4;                    // token quarters of a block
 constexpr int kGroups = 3;                        // warp groups, alternate blocks
 constexpr int kCWarps = kGroupWarps * kGroups;    // compute warps
 constexpr int kAttThreads = kCWarps * 32;
-constexpr int kStages = 6;                        // staging ring of K+V tile images (a multiple of kGroups)
+// Staging ring depth: 6 stages of K+V images for 128-channel heads, 4 of K0+K1+V for 256-channel heads
+// (two half-heads); both a multiple of... any depth works, the stage of block j is j % depth.
+template <int NH>
+constexpr int stages_of() { return NH == 1 ? 6 : 4; }
 constexpr int kCtasPerSm = 1;
 constexpr int kRPad = 8;                          // query heads per kv-head in the MMA rows
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
 constexpr uint32_t kJoinMask = 0x807F807Fu;       // sign and mantissa bits of a bf16x2 word
 constexpr uint32_t kFull = 0xFFFFFFFFu;
-static_assert(kStages % kGroups == 0, "a stage must always feed the same group");
 
 struct StageMeta {
-  int mode[2], esc[2];  // [K, V]
+  int mode[3], esc[3];  // [K half 0, (K half 1,) V]
 };
 
+// NH: 128-channel half-heads per attention head (1, or 2 for 256-channel heads).
+template <int NH>
 struct AttSmem {
-  alignas(128) uint8_t stage[kStages][2][kRawBytes];  // K, V tile images
+  static constexpr int kStages = stages_of<NH>();
+  alignas(128) uint8_t stage[kStages][NH + 1][kRawBytes];  // K half-head images, then the V image
   uint2 lut[256];                 // escape byte -> bit 3 spread into the byte lanes of two exponent words
   uint32_t tagl[256];             // tag byte -> gather selector, counts, raw groups (tag_entry)
-  alignas(16) uint8_t bases[2][2][kD];  // [K|V][base3|base4][channel] of the CTA's kv-head
+  alignas(16) uint8_t kbases[NH][2][kD];  // K: [half][base3|base4][channel]
   StageMeta smeta[kStages];
-  alignas(16) uint4 qf[8][32];           // q A-operand quads [k-step][lane]: (qa0, 0, qa2, 0)
+  alignas(16) uint4 qf[NH][8][32];       // q A-operand quads [half][k-step][lane]: (qa0, 0, qa2, 0)
   alignas(16) uint4 vbw[2][2][32];        // V base words [unit][base3 | base4 - base3][lane], groups 0-3
   unsigned int stDone[kStages];           // warps of the group done reading the stage's current block
   float wm[kCWarps][kRPad];       // per warp and head: running maximum (end of split)
@@ -93,9 +98,9 @@ struct AttnArgs {
   const uint8_t* base3;
   const uint8_t* base4;
   float scale_log2;  // scale * 16 * log2(e)
-  int Hq, Hkv, r, max_blocks, n_splits;
+  int Hq, Hkv, r, max_blocks, n_splits;  // Hkv: attention kv-heads (of NH half-heads each)
   float* part;
-  unsigned int* counters;  // [batch][Hkv] splits finished; zero between launches
+  unsigned int* counters;  // [batch][NH * Hkv] splits finished; zero between launches
   float* out;
   int32_t* status;
 };
@@ -247,7 +252,8 @@ __device__ __forceinline__ void raw_unit(const uint8_t* img, int u, uint32_t o[1
 // directory gives each eighth's first 4-bit escape byte and raw group, one
 // warp scan of the four packed counts (at most 4 per unit, 128 per eighth)
 // each unit's.
-__device__ __forceinline__ void tile_units(const AttnArgs& a, const AttSmem& sm, const uint8_t* img, int mode,
+template <class Smem>
+__device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, const uint8_t* img, int mode,
                                            int esc_len, int w, int lane, const uint32_t b3A[8],
                                            const uint32_t d43A[8], const uint32_t b3B[8], const uint32_t d43B[8],
                                            uint32_t oA[16], uint32_t oB[16], bool& badA, bool& badB) {
@@ -316,27 +322,37 @@ __device__ __forceinline__ const void* tile_source(const AttnArgs& a, uint2 e, u
   return nullptr;
 }
 
-// Table entries (K, V) of block j of the split.
-__device__ __forceinline__ void block_entries(const AttnArgs& a, int b, int h, int blk, uint2& eK, uint2& eV) {
-  const gaac_entry* t = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk) * a.Hkv + h) * 2;
-  eK = *reinterpret_cast<const uint2*>(t);
-  eV = *reinterpret_cast<const uint2*>(t + 1);
+// Table entries of block blk for attention head H and output half hf: the K
+// entries of the head's NH half-heads, then the V entry of half-head NH*H + hf.
+template <int NH>
+__device__ __forceinline__ void block_entries(const AttnArgs& a, int b, int H, int hf, int blk, uint2 e[NH + 1]) {
+  const gaac_entry* t = a.table + (static_cast<size_t>(b) * a.max_blocks + blk) * (NH * a.Hkv) * 2;
+#pragma unroll
+  for (int j = 0; j < NH; ++j) e[j] = *reinterpret_cast<const uint2*>(t + (NH * H + j) * 2);
+  e[NH] = *reinterpret_cast<const uint2*>(t + (NH * H + hf) * 2 + 1);
 }
 
-// One thread starts the bulk copies of a block's K and V images into stage st
-// (a free stage); stFull[st] completes when both have landed.
-__device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem& sm, int st, uint2 eK, uint2 eV) {
+// One thread starts the bulk copies of a block's images into stage st (a free
+// stage); stFull[st] completes when all have landed.
+template <int NH>
+__device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem<NH>& sm, int st, const uint2 e[NH + 1]) {
   StageMeta m;
-  uint32_t bytes[2];
-  const void* src[2];
-  src[0] = tile_source(a, eK, bytes[0], m.mode[0], m.esc[0]);
-  src[1] = tile_source(a, eV, bytes[1], m.mode[1], m.esc[1]);
-  if (!src[0] || !src[1]) report(a.status, GAAC_EFORMAT);
+  uint32_t bytes[NH + 1], total = 0;
+  const void* src[NH + 1];
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i <= NH; ++i) {
+    src[i] = tile_source(a, e[i], bytes[i], m.mode[i], m.esc[i]);
+    ok = ok && src[i] != nullptr;
+    total += bytes[i];
+  }
+  if (!ok) report(a.status, GAAC_EFORMAT);
   sm.smeta[st] = m;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic reads of the stage, then async writes
-  mbar_arrive_expect_tx(&sm.stFull[st], bytes[0] + bytes[1]);
-  if (bytes[0]) bulk_g2s(sm.stage[st][0], src[0], bytes[0], &sm.stFull[st]);
-  if (bytes[1]) bulk_g2s(sm.stage[st][1], src[1], bytes[1], &sm.stFull[st]);
+  mbar_arrive_expect_tx(&sm.stFull[st], total);
+#pragma unroll
+  for (int i = 0; i <= NH; ++i)
+    if (bytes[i]) bulk_g2s(sm.stage[st][i], src[i], bytes[i], &sm.stFull[st]);
 }
 
 __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta(unsigned int* p, unsigned int v) {
@@ -351,16 +367,23 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta(unsigned int* p, 
 // Lane (g, tq) = (lane/4, lane%4).  Returns the warp's (m, l) per head through
 // shared memory and its accumulators in acc (O^T fragments: acc[m][0..3] =
 // channels 16m+g, 16m+g+8 x heads 2tq, 2tq+1).
-__device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int b, int h, int blk0, int n_my, int len,
-                                             int gr, int w, int cw, int lane, float acc[8][4]) {
-  const int g = lane >> 2, tq = lane & 3;
-  // K units: channels 32tq..32tq+31 (word i: channels 32tq + 4i..+3)
-  uint32_t kb3[8], kd43[8];
+// K unit base words of half-head `half`: channels 32tq..32tq+31, word i = channels 32tq + 4i..+3.
+template <int NH>
+__device__ __forceinline__ void k_bases(const AttSmem<NH>& sm, int half, int tq, uint32_t kb3[8], uint32_t kd43[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    kb3[i] = *reinterpret_cast<const uint32_t*>(&sm.bases[0][0][32 * tq + 4 * i]);
-    kd43[i] = *reinterpret_cast<const uint32_t*>(&sm.bases[0][1][32 * tq + 4 * i]) - kb3[i];
+    kb3[i] = *reinterpret_cast<const uint32_t*>(&sm.kbases[half][0][32 * tq + 4 * i]);
+    kd43[i] = *reinterpret_cast<const uint32_t*>(&sm.kbases[half][1][32 * tq + 4 * i]) - kb3[i];
   }
+}
+
+template <int NH>
+__device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm, int b, int H, int hf, int blk0,
+                                             int n_my, int len, int gr, int w, int cw, int lane, float acc[8][4]) {
+  constexpr int kStages = AttSmem<NH>::kStages;
+  const int g = lane >> 2, tq = lane & 3;
+  uint32_t kb3[8], kd43[8];  // one half-head: loaded once (NH = 1) or per half and block (NH = 2)
+  if (NH == 1) k_bases(sm, 0, tq, kb3, kd43);
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
   float mrun = -INFINITY, lsum = 0.f;  // head g
@@ -368,24 +391,31 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
 #pragma unroll 1
   for (int j = gr; j < n_my; j += kGroups) {
     const int st = j % kStages, jn = j + kStages;  // jn: the block this stage takes next
-    uint2 nK = make_uint2(0u, 0u), nV = nK;
-    if (lane == 0 && jn < n_my) block_entries(a, b, h, blk0 + jn, nK, nV);  // used if this warp refills
+    uint2 ne[NH + 1];
+#pragma unroll
+    for (int i = 0; i <= NH; ++i) ne[i] = make_uint2(0u, 0u);
+    if (lane == 0 && jn < n_my) block_entries<NH>(a, b, H, hf, blk0 + jn, ne);  // used if this warp refills
     mbar_wait(&sm.stFull[st], static_cast<uint32_t>(j / kStages) & 1u, a.status);
     const StageMeta meta = sm.smeta[st];
     const int nv = min(kBlock, len - (blk0 + j) * kBlock);
-    // ---- S^T for tokens 16w..16w+7 (A) and 16w+8..16w+15 (B)
+    // ---- S^T for tokens 16w..16w+7 (A) and 16w+8..16w+15 (B), summed over the head's half-heads
     float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
-    bool kbadA, kbadB;
-    {
+    bool kbadA = false, kbadB = false;
+#pragma unroll 1
+    for (int half = 0; half < NH; ++half) {
+      if (NH > 1) k_bases(sm, half, tq, kb3, kd43);
       uint32_t oA[16], oB[16];
-      tile_units(a, sm, sm.stage[st][0], meta.mode[0], meta.esc[0], w, lane, kb3, kd43, kb3, kd43, oA, oB, kbadA,
-                 kbadB);
+      bool bA, bB;
+      tile_units(a, sm, sm.stage[st][half], meta.mode[half], meta.esc[half], w, lane, kb3, kd43, kb3, kd43, oA, oB,
+                 bA, bB);
+      kbadA = kbadA || bA;
+      kbadB = kbadB || bB;
       // q of head g as the A operand of S^T = q K^T (scaled by 2^-4), one 16-byte quad per k-step: for k-step
       // m the K lane holds channels 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no
       // head) are zero
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const uint4 qv = sm.qf[m][lane];
+        const uint4 qv = sm.qf[half][m][lane];
         mma_bf16(sA, qv.x, qv.y, qv.z, qv.w, oA[2 * m], oA[2 * m + 1]);
         mma_bf16(sB, qv.x, qv.y, qv.z, qv.w, oB[2 * m], oB[2 * m + 1]);
       }
@@ -407,13 +437,13 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
       vd43[hv][4] = vd43[hv][5] = x4.z;
       vd43[hv][6] = vd43[hv][7] = x4.w;
     }
-    tile_units(a, sm, sm.stage[st][1], meta.mode[1], meta.esc[1], w, lane, vb3[0], vd43[0], vb3[1], vd43[1], oA,
+    tile_units(a, sm, sm.stage[st][NH], meta.mode[NH], meta.esc[NH], w, lane, vb3[0], vd43[0], vb3[1], vd43[1], oA,
                oB, vbadA, vbadB);
     // The stage is read: the group's last warp to get here refills it with block jn.
     __syncwarp();
     if (lane == 0 && atomic_add_acq_rel_cta(&sm.stDone[st], 1u) == kGroupWarps - 1) {
       sm.stDone[st] = 0u;
-      if (jn < n_my) issue_block(a, sm, st, nK, nV);
+      if (jn < n_my) issue_block<NH>(a, sm, st, ne);
     }
     // ---- online softmax of head g over the warp's 16 tokens
     const float x0 = (!kbadA && tA < nv) ? sA[0] * a.scale_log2 : -INFINITY;
@@ -488,7 +518,8 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem& sm, int
 // running maximum; the subsets are then combined the same way in shared
 // memory.  The staging ring is free by then and holds that exchange.
 // base: the first partial of the pair; out: its first output row.
-__device__ __noinline__ void merge_splits(const float* base, int ns, int r, float* out, AttSmem& sm, int tid) {
+template <int NH>
+__device__ __noinline__ void merge_splits(const float* base, int ns, int r, float* out, AttSmem<NH>& sm, int tid) {
   constexpr int kBatch = 10;
   const int o4n = r * (kD / 4);  // float4 columns of the r x 128 output
   const int groups = kAttThreads / o4n;
@@ -564,7 +595,7 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
         den += w * md.y;
       }
     }
-    float* o = out + n * kD + 4 * c4;
+    float* o = out + n * (NH * kD) + 4 * c4;  // rows of NH * 128 channels
     const float inv = den > 0.f ? 1.f / den : 0.f;
     o[0] = acc.x * inv;
     o[1] = acc.y * inv;
@@ -574,10 +605,16 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
 }
 
 
+// Grid (split, NH * Hkv, batch): CTA y serves attention head H = y / NH and
+// output channels [128 hf, 128 hf + 128) of it (hf = y % NH); for NH = 2 it
+// reads the K tiles of both half-heads and the V tile of half-head NH*H + hf.
+template <int NH>
 __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(AttnArgs a) {
+  constexpr int kStages = AttSmem<NH>::kStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  AttSmem& sm = *reinterpret_cast<AttSmem*>(smem_raw);
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  AttSmem<NH>& sm = *reinterpret_cast<AttSmem<NH>*>(smem_raw);
+  const int split = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
+  const int H = y / NH, hf = y % NH, nkv = NH * a.Hkv;  // nkv: half-heads in the table and the bases
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int len = a.seq_lens[b];
   if (len < 0 || len > a.max_blocks * kBlock) {
@@ -594,33 +631,34 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
     sm.tagl[x] = tag_entry(static_cast<uint32_t>(x));
   }
-  for (int x = tid; x < 4 * kD; x += kAttThreads) {  // [K|V][base3|base4][channel]
-    const int kind = x / (2 * kD), which = (x / kD) & 1, c = x % kD;
-    sm.bases[kind][which][c] = (which ? a.base4 : a.base3)[(kind * a.Hkv + h) * kD + c];
+  for (int x = tid; x < NH * 2 * kD; x += kAttThreads) {  // K: [half][base3|base4][channel]
+    const int half = x / (2 * kD), which = (x / kD) & 1, c = x % kD;
+    sm.kbases[half][which][c] = (which ? a.base4 : a.base3)[(NH * H + half) * kD + c];
   }
   // V unit base words: group i of the lane's unit hv holds channels 16m+g and 16m+g+8 (m = 4hv + i, g =
   // lane/4) in byte lanes 0, 2 and 1, 3 of both of its exponent words
   for (int x = tid; x < 32 * 2 * 4; x += kAttThreads) {
     const int ln = x / 8, hv = (x / 4) % 2, i = x % 4;
     const int cA = 16 * (4 * hv + i) + ln / 4;
-    const uint8_t* v3 = a.base3 + (a.Hkv + h) * kD;
-    const uint8_t* v4 = a.base4 + (a.Hkv + h) * kD;
+    const uint8_t* v3 = a.base3 + (nkv + NH * H + hf) * kD;
+    const uint8_t* v4 = a.base4 + (nkv + NH * H + hf) * kD;
     const uint32_t x3 = v3[cA] | (static_cast<uint32_t>(v3[cA + 8]) << 8);
     const uint32_t x4 = v4[cA] | (static_cast<uint32_t>(v4[cA + 8]) << 8);
     reinterpret_cast<uint32_t*>(&sm.vbw[hv][0][ln])[i] = x3 | (x3 << 16);
     reinterpret_cast<uint32_t*>(&sm.vbw[hv][1][ln])[i] = (x4 | (x4 << 16)) - (x3 | (x3 << 16));
   }
-  // q of the kv-head's query heads, times 2^-4, as A-operand quads of S^T = q K^T: for lane (g, tq) and
-  // k-step m, (channels 32tq + 4m + {0, 2}, 0, channels 32tq + 4m + {1, 3}, 0) of head g (rows 8-15 zero)
-  for (int x = tid; x < 32 * 8 * 2; x += kAttThreads) {
-    const int ln = x / 16, n = ln / 4, tq = ln % 4, m = (x / 2) % 8, odd = x % 2;
+  // q of the kv-head's query heads, times 2^-4, as A-operand quads of S^T = q K^T: for half `half`, lane
+  // (g, tq) and k-step m, (channels 128 half + 32tq + 4m + {0, 2}, 0, ... + {1, 3}, 0) of head g (rows 8-15 zero)
+  for (int x = tid; x < NH * 32 * 8 * 2; x += kAttThreads) {
+    const int half = x / 512, ln = (x / 16) % 32, n = ln / 4, tq = ln % 4, m = (x / 2) % 8, odd = x % 2;
     uint32_t v = 0u;
     if (n < a.r) {
-      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + h * a.r + n) * kD + 32 * tq + 4 * m + odd;
+      const uint16_t* qrow =
+          a.q + (static_cast<size_t>(b) * a.Hq + H * a.r + n) * (NH * kD) + kD * half + 32 * tq + 4 * m + odd;
       v = bf16x2_div16(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16));
     }
-    reinterpret_cast<uint32_t*>(&sm.qf[m][ln])[2 * odd] = v;
-    reinterpret_cast<uint32_t*>(&sm.qf[m][ln])[2 * odd + 1] = 0u;
+    reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd] = v;
+    reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd + 1] = 0u;
   }
   if (tid < kStages) {
     mbar_init(&sm.stFull[tid], 1);
@@ -629,15 +667,15 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   fence_mbar_init();
   __syncthreads();
   if (tid < min(n_my, kStages)) {  // the first blocks, one lane each; later ones are issued as stages free up
-    uint2 eK, eV;
-    block_entries(a, b, h, blk0 + tid, eK, eV);
-    issue_block(a, sm, tid, eK, eV);
+    uint2 e[NH + 1];
+    block_entries<NH>(a, b, H, hf, blk0 + tid, e);
+    issue_block<NH>(a, sm, tid, e);
   }
 
   const int r = a.r;
-  float* part = a.part + ((static_cast<size_t>(b) * a.Hkv + h) * a.n_splits + split) * kPartFloats;
+  float* part = a.part + ((static_cast<size_t>(b) * nkv + y) * a.n_splits + split) * kPartFloats;
   float acc[8][4];
-  compute_warp(a, sm, b, h, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane, acc);
+  compute_warp<NH>(a, sm, b, H, hf, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane, acc);
   if (tid == 0) {
     // Every issued copy was waited for by its group; after a timed-out wait,
     // wait once more (bounded) so that no copy is still landing at exit.
@@ -696,12 +734,12 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   // partial stores before thread 0's acq_rel add, and the add orders the other
   // splits' stores before this CTA's loads (the barrier passes that on).
   __syncthreads();
-  unsigned int* counter = a.counters + static_cast<size_t>(b) * a.Hkv + h;
+  unsigned int* counter = a.counters + static_cast<size_t>(b) * nkv + y;
   if (tid == 0) sm.last = atomic_add_acq_rel(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
   __syncthreads();
   if (!sm.last) return;
-  merge_splits(a.part + (static_cast<size_t>(b) * a.Hkv + h) * a.n_splits * kPartFloats, a.n_splits, r,
-               a.out + (static_cast<size_t>(b) * a.Hq + h * r) * kD, sm, tid);
+  merge_splits<NH>(a.part + (static_cast<size_t>(b) * nkv + y) * a.n_splits * kPartFloats, a.n_splits, r,
+                   a.out + (static_cast<size_t>(b) * a.Hq + H * r) * (NH * kD) + kD * hf, sm, tid);
   if (tid == 0) *counter = 0u;
 }
 
@@ -717,13 +755,14 @@ static int device_sms() {
   return cached[dev];
 }
 
+template <int NH>
 static bool prepare_kernel() {
   static bool done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(AttSmem))) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(AttSmem<NH>))) != cudaSuccess)
       return false;
     done[dev] = true;
   }
@@ -754,16 +793,18 @@ extern "C" size_t gaac_attention_workspace(int batch, int n_kv_heads, int max_bl
   return partials_bytes(batch, n_kv_heads, n_splits) + counters;
 }
 
-extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
-                                     const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
-                                     const uint8_t* base3, const uint8_t* base4, float scale, int n_splits,
-                                     float* out, void* workspace, size_t workspace_bytes, int32_t* d_status,
-                                     void* stream) {
+// Checks and launch shared by the 128- and 256-channel entry points; n_kv_heads
+// counts attention kv-heads, each of NH half-heads in the table and the bases.
+template <int NH>
+static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
+                            const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
+                            const uint8_t* base3, const uint8_t* base4, float scale, int n_splits, float* out,
+                            void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
   if (q == nullptr || seq_lens == nullptr || table == nullptr || pools == nullptr || pools->slot_pool == nullptr ||
       pools->raw_pool == nullptr || pools->n_slots < 0 || pools->n_raw < 0 || base3 == nullptr ||
       base4 == nullptr || out == nullptr || workspace == nullptr)
     return GAAC_EINVAL;
-  if (batch <= 0 || batch > 65535 || n_kv_heads <= 0 || n_kv_heads > 65535 || n_q_heads <= 0 ||
+  if (batch <= 0 || batch > 65535 || n_kv_heads <= 0 || NH * n_kv_heads > 65535 || n_q_heads <= 0 ||
       n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > GAAC_MAX_GQA || max_blocks <= 0 ||
       max_blocks > (1 << 24) || !std::isfinite(scale))
     return GAAC_EINVAL;
@@ -772,10 +813,11 @@ extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads
       (reinterpret_cast<uintptr_t>(base4) & 15u) || (reinterpret_cast<uintptr_t>(workspace) & 15u) ||
       (reinterpret_cast<uintptr_t>(out) & 3u))
     return GAAC_EINVAL;
-  if (n_splits <= 0) n_splits = gaac_attention_auto_splits(batch, n_kv_heads, max_blocks);
+  const int nkv = NH * n_kv_heads;  // CTAs per (sequence, split) and half-heads in the table
+  if (n_splits <= 0) n_splits = gaac_attention_auto_splits(batch, nkv, max_blocks);
   if (n_splits > max_blocks) n_splits = max_blocks;
-  if (workspace_bytes < gaac_attention_workspace(batch, n_kv_heads, max_blocks, n_splits)) return GAAC_EINVAL;
-  if (!prepare_kernel()) return GAAC_ECUDA;
+  if (workspace_bytes < gaac_attention_workspace(batch, nkv, max_blocks, n_splits)) return GAAC_EINVAL;
+  if (!prepare_kernel<NH>()) return GAAC_ECUDA;
   AttnArgs a;
   a.q = q;
   a.seq_lens = seq_lens;
@@ -793,12 +835,30 @@ extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads
   a.max_blocks = max_blocks;
   a.n_splits = n_splits;
   a.part = static_cast<float*>(workspace);
-  a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + partials_bytes(batch, n_kv_heads, n_splits));
+  a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + partials_bytes(batch, nkv, n_splits));
   a.out = out;
   a.status = d_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  attn_split_kernel<<<dim3(n_splits, n_kv_heads, batch), kAttThreads, sizeof(AttSmem), st>>>(a);
+  attn_split_kernel<NH><<<dim3(n_splits, nkv, batch), kAttThreads, sizeof(AttSmem<NH>), st>>>(a);
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
+
+extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
+                                     const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
+                                     const uint8_t* base3, const uint8_t* base4, float scale, int n_splits,
+                                     float* out, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                                     void* stream) {
+  return launch_attention<1>(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, base3, base4, scale,
+                             n_splits, out, workspace, workspace_bytes, d_status, stream);
+}
+
+extern "C" int gaac_decode_attention_hd256(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads,
+                                           int max_blocks, const int32_t* seq_lens, const gaac_entry* table,
+                                           const gaac_pools* pools, const uint8_t* base3, const uint8_t* base4,
+                                           float scale, int n_splits, float* out, void* workspace,
+                                           size_t workspace_bytes, int32_t* d_status, void* stream) {
+  return launch_attention<2>(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, base3, base4, scale,
+                             n_splits, out, workspace, workspace_bytes, d_status, stream);
 }
 
 // ------------------------------------------------------------------------

@@ -92,11 +92,11 @@ def rel_err_rows(out: np.ndarray, ref: np.ndarray) -> np.ndarray:
 
 
 def oracle_attention(q, k, v, lens, scale, seqs=None):
-    """fp64 oracle output [B, Hq, 128] and flags [B, Hq] for the listed sequences."""
+    """fp64 oracle output [B, Hq, d] and flags [B, Hq] for the listed sequences (d = 128 or 256)."""
     qn, kn, vn = u16(q), u16(k), u16(v)
     lens_np = lens.cpu().numpy()
     B, Hq = q.shape[0], q.shape[1]
-    ref = np.zeros((B, Hq, 128))
+    ref = np.zeros((B, Hq, q.shape[-1]))
     flags = np.zeros((B, Hq), np.int32)
     for b in (range(B) if seqs is None else seqs):
         L = int(lens_np[b])
