@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
             L.gaac_ref_calibrate.restype = None
             L.gaac_ref_encode_tile.argtypes = [P, i32, P, P, P, P, i32]
             L.gaac_ref_encode_tile.restype = i32
+            L.gaac_ref_encode_open_tile.argtypes = [P, i32, i32, P, P, P, i32]
+            L.gaac_ref_encode_open_tile.restype = i32
             L.gaac_ref_decode_tile.argtypes = [P, i32, P, P, i32, P]
             L.gaac_ref_decode_tile.restype = i32
             L.gaac_ref_mode_counts.argtypes = [P, P]
@@ -135,6 +137,19 @@ def encode_tile(tile, kind: int, base3, base4, forced=None, esc_cap: int = ESC_C
         forced = _u8(forced).reshape(1024)
         fp = _ptr(forced)
     esc = lib().gaac_ref_encode_tile(_ptr(tile), kind, _ptr(b3), _ptr(b4), fp, _ptr(img), esc_cap)
+    return img, esc
+
+
+def encode_open_tile(tile, n_tok: int, kind: int, base3, base4, esc_cap: int = ESC_CAP):
+    """Encode the first n_tok (1..64) tokens of a [64][128] BF16 tile as an open slot image: the
+    tokens past n_tok are absent (no part in a group's mode; all their fields zero).  Returns
+    (image uint8 [11536+esc_cap], esc_len), esc_len -1 when the escape stream exceeds esc_cap."""
+    tile = _u16(tile).reshape(BLOCK, D)
+    b3, b4 = _u8(base3).reshape(D), _u8(base4).reshape(D)
+    img = np.zeros(OFF_ESC + esc_cap, np.uint8)
+    esc = lib().gaac_ref_encode_open_tile(_ptr(tile), int(n_tok), kind, _ptr(b3), _ptr(b4), _ptr(img), esc_cap)
+    if esc == -2:
+        raise ValueError("n_tok must be in [1, 64]")
     return img, esc
 
 

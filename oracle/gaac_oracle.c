@@ -202,10 +202,12 @@ static void put_tag(uint8_t* img, int G, unsigned mode) {
 static unsigned get_tag(const uint8_t* img, int G) { return (img[ORC_OFF_TAG + G / 4] >> (2 * (G % 4))) & 3u; }
 
 /* ---- mode rule (section 3.1): 3-bit if every offset from base3 is in [0,7],
- * else 4-bit if every offset from base4 is in [0,15], else raw. */
-static unsigned choose_mode(const unsigned* e, const unsigned* b3, const unsigned* b4) {
+ * else 4-bit if every offset from base4 is in [0,15], else raw.  Only the
+ * elements with present[j] set count (present NULL: all eight). */
+static unsigned choose_mode(const unsigned* e, const unsigned* b3, const unsigned* b4, const uint8_t* present) {
     int fits3 = 1, fits4 = 1;
     for (int j = 0; j < 8; ++j) {
+        if (present && !present[j]) continue;
         int o3 = (int)e[j] - (int)b3[j];
         int o4 = (int)e[j] - (int)b4[j];
         if (o3 < 0 || o3 > 7) fits3 = 0;
@@ -218,7 +220,8 @@ static int escape_bytes_of_mode(unsigned mode) { return mode == ORC_M3BIT ? 0 : 
 int gaac_ref_escape_bytes_of_mode(int mode) { return escape_bytes_of_mode((unsigned)mode); }
 
 /*
- * Encode one full tile.  `tile` is the tile in logical order [64 tokens][128
+ * Encode the first n_tok tokens of a tile (1 <= n_tok <= 64; 64 = a full,
+ * sealed tile).  `tile` is the tile in logical order [64 tokens][128
  * channels]; b3/b4 are the 128 per-channel bases of this (kv-head, K|V).
  * `forced` (NULL or 1024 modes) overrides the mode rule, for tests only.
  * `img` receives the slot image; it must hold 11536 + img_esc_cap bytes.
@@ -229,29 +232,43 @@ int gaac_ref_escape_bytes_of_mode(int mode) { return escape_bytes_of_mode((unsig
  * Codes: 3-bit group: e - base3; 4-bit group: (e - base4) & 7, with bit 3 of
  * element j's offset in bit j of the group's escape byte; raw group: code 0,
  * the eight exponents as eight escape bytes in element order.
+ *
+ * Open tiles (n_tok < 64; section 3.3 keeps the last block open while decode
+ * tokens arrive, and the open block may be kept in its slot as it fills).  An element of
+ * a token >= n_tok is absent: it takes no part in its group's mode (a group
+ * with no present element is 3-bit), and every field it owns is zero: its
+ * mantissa bits, the sign bit it lends to its neighbour's byte, its code, its
+ * escape bit and, in a raw group, its exponent byte.  With every token present
+ * this is the full tile's encoding, so a tile filled token by token ends in
+ * the bytes of the tile encoded at once.
  */
-int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, const uint8_t* base4,
+static int encode_prefix(const uint16_t* tile, int n_tok, int kind, const uint8_t* base3, const uint8_t* base4,
                          const uint8_t* forced, uint8_t* img, int img_esc_cap) {
     memset(img, 0, (size_t)(ORC_OFF_ESC + img_esc_cap));
     uint16_t seq[ORC_TILE];
+    uint8_t present[ORC_TILE];
     for (int t = 0; t < ORC_BLOCK; ++t)
-        for (int c = 0; c < ORC_D; ++c) seq[gaac_ref_storage_index(kind, t, c)] = tile[t * ORC_D + c];
+        for (int c = 0; c < ORC_D; ++c) {
+            int s = gaac_ref_storage_index(kind, t, c);
+            present[s] = t < n_tok;
+            seq[s] = present[s] ? tile[t * ORC_D + c] : 0;  /* absent: no sign, mantissa or exponent */
+        }
 
     for (int s = 0; s < ORC_TILE; ++s)
         img[s] = (uint8_t)((bf16_signmant(seq[s]) & 0x7Fu) | (bf16_signmant(seq[sign_source(s)]) & 0x80u));
 
-    /* pass 1: every group's mode; the raw bytes follow all 4-bit bytes */
+    /* pass 1: every group's mode over its present elements; the raw bytes follow all 4-bit bytes */
     unsigned modes[ORC_GROUPS];
     int n4 = 0, nraw = 0;
     for (int G = 0; G < ORC_GROUPS; ++G) {
         unsigned e[8], b3[8], b4[8];
         for (int j = 0; j < 8; ++j) {
             int s = 8 * G + j;
-            e[j] = bf16_exponent(seq[s]);
             b3[j] = base3[channel_of(kind, s)];
             b4[j] = base4[channel_of(kind, s)];
+            e[j] = bf16_exponent(seq[s]);
         }
-        modes[G] = forced ? forced[G] : choose_mode(e, b3, b4);
+        modes[G] = forced ? forced[G] : choose_mode(e, b3, b4, present + 8 * G);
         if (modes[G] == ORC_M4BIT) n4 += 1;
         if (modes[G] == ORC_MRAW) nraw += 1;
     }
@@ -267,7 +284,9 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
         for (int j = 0; j < 8; ++j) {
             int s = 8 * G + j;
             unsigned e = bf16_exponent(seq[s]), code = 0;
-            if (mode == ORC_M3BIT) {
+            if (!present[s]) {
+                /* absent: code, escape bit and raw exponent byte stay zero */
+            } else if (mode == ORC_M3BIT) {
                 code = (e - base3[channel_of(kind, s)]) & 7u;
             } else if (mode == ORC_M4BIT) {
                 unsigned off = (e - base4[channel_of(kind, s)]) & 0xFFu;
@@ -288,6 +307,17 @@ int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, c
         }
     }
     return esc;
+}
+
+int gaac_ref_encode_tile(const uint16_t* tile, int kind, const uint8_t* base3, const uint8_t* base4,
+                         const uint8_t* forced, uint8_t* img, int img_esc_cap) {
+    return encode_prefix(tile, ORC_BLOCK, kind, base3, base4, forced, img, img_esc_cap);
+}
+
+int gaac_ref_encode_open_tile(const uint16_t* tile, int n_tok, int kind, const uint8_t* base3,
+                              const uint8_t* base4, uint8_t* img, int img_esc_cap) {
+    if (n_tok < 1 || n_tok > ORC_BLOCK) return -2;
+    return encode_prefix(tile, n_tok, kind, base3, base4, NULL, img, img_esc_cap);
 }
 
 /*
@@ -433,7 +463,7 @@ int gaac_ref_fp8_encode_tile(const uint8_t* tile, int kind, int fmt, const uint8
             b3[j] = base3[channel_of(kind, s)];
             b4[j] = base4[channel_of(kind, s)];
         }
-        modes[G] = forced ? forced[G] : choose_mode(e, b3, b4);
+        modes[G] = forced ? forced[G] : choose_mode(e, b3, b4, NULL);
         if (modes[G] == ORC_M4BIT) n4 += 1;
         if (modes[G] == ORC_MRAW) nraw += 1;
     }
