@@ -80,6 +80,9 @@ enum {
   GAAC_ETIMEOUT = 5  /* a bounded wait inside a kernel gave up (data of that launch invalid) */
 };
 
+/* Flags of gaac_encode_blocks_ex and gaac_append_ex. */
+#define GAAC_OPEN_COMPRESSED 1u /* keep the open (last, partial) block compressed in its slot */
+
 /* Table entry modes. */
 enum { GAAC_MODE_SLOT = 0, GAAC_MODE_RAW = 1, GAAC_MODE_NONE = 255 };
 
@@ -173,6 +176,52 @@ GAAC_API int gaac_append(const uint16_t* k_new, const uint16_t* v_new, int32_t* 
                 int max_blocks, const uint8_t* base3, const uint8_t* base4, gaac_entry* table,
                 const uint32_t* slot_ids, const gaac_pools* pools, gaac_stats* stats, int32_t* d_status,
                 void* stream);
+
+/*
+ * gaac_encode_blocks and gaac_append with flags.  flags = 0 is the plain call.
+ *
+ * GAAC_OPEN_COMPRESSED keeps the open block compressed (section 3.3 keeps the
+ * last block open while decode tokens arrive; here it is stored in its slot
+ * from its first token instead of as a BF16 tile).  The slot of an open block
+ * holding n < 64 tokens is the image of its first n tokens in which the
+ * elements of later tokens are absent: they take no part in their group's
+ * mode, and their sign|mantissa bits (including the sign bit an element lends
+ * to its neighbour's byte), codes, escape bits and raw exponent bytes are zero.
+ * Directory entries and esc_len count the present groups' escapes.  Its table
+ * entry is {slot, esc_len, GAAC_MODE_SLOT, n}.  With all 64 tokens present this
+ * is the sealed encoding, so a block filled token by token ends in the same
+ * bytes as one encoded at once.  Attention and decompression read open slots
+ * like sealed ones (tokens past the sequence length are masked).
+ *  - gaac_encode_blocks_ex: the incomplete last block of each sequence is
+ *    encoded into slot_ids[...] of its block (slot_ids must not be NULL for
+ *    the flag to apply); if its escape stream exceeds GAAC_ESC_CAPACITY, it is
+ *    a raw tile as without the flag.  Open blocks are not counted in stats.
+ *  - gaac_append_ex: a block that opens (position 0) takes slot
+ *    slot_ids[((b*max_blocks+blk)*n_kv_heads+h)*2+kv] and holds the token as a
+ *    one-token open image; a later token is added to the open slot by
+ *    re-encoding its present tokens, writing only the 32-byte sign|mantissa
+ *    rows and code words of the units that hold the new token (4 units for K,
+ *    16 for V) and the tag plane, directory and escape area.  The work is
+ *    bounded by one tile, whatever the sequence length.  If the escape stream
+ *    of the open block outgrows the slot (it never shrinks as tokens arrive, so
+ *    the full block would not fit either), its tokens so far move to a raw tile
+ *    popped from the free list, and the block continues and seals as RAW.  A
+ *    block whose entry is already a raw tail (from gaac_encode_blocks without
+ *    the flag, or handed over by a raw tail that sealed into a slot) continues
+ *    as gaac_append does.  A slot entry whose n_tok differs from seq_lens[b] %
+ *    64, or an open image that fails the format checks, reports GAAC_EFORMAT and
+ *    leaves the block untouched.
+ * Unknown flag bits: GAAC_EINVAL.
+ */
+GAAC_API int gaac_encode_blocks_ex(const uint16_t* k, const uint16_t* v, int64_t seq_stride, int64_t tok_stride,
+                          int64_t n_tok, const int32_t* seq_lens, int batch, int n_kv_heads, int max_blocks,
+                          const uint8_t* base3, const uint8_t* base4, gaac_entry* table, const uint32_t* slot_ids,
+                          const gaac_pools* pools, gaac_stats* stats, unsigned flags, int32_t* d_status,
+                          void* stream);
+GAAC_API int gaac_append_ex(const uint16_t* k_new, const uint16_t* v_new, int32_t* seq_lens, int batch,
+                   int n_kv_heads, int max_blocks, const uint8_t* base3, const uint8_t* base4, gaac_entry* table,
+                   const uint32_t* slot_ids, const gaac_pools* pools, gaac_stats* stats, unsigned flags,
+                   int32_t* d_status, void* stream);
 
 /*
  * Workspace bytes gaac_decode_attention needs for (batch, n_q_heads, n_splits).

@@ -27,6 +27,7 @@ MAX_GQA = 8
 
 OK, EINVAL, EPOOL, EFORMAT, ECUDA, ETIMEOUT = range(6)
 MODE_SLOT, MODE_RAW, MODE_NONE = 0, 1, 255
+OPEN_COMPRESSED = 1  # flag of encode_blocks / append: keep the open block compressed in its slot
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgaac.so")
@@ -76,6 +77,11 @@ def lib() -> ctypes.CDLL:
             L.gaac_encode_blocks.restype = i32
             L.gaac_append.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P]
             L.gaac_append.restype = i32
+            L.gaac_encode_blocks_ex.argtypes = [P, P, i64, i64, i64, P, i32, i32, i32, P, P, P, P, P, P,
+                                                ctypes.c_uint, P, P]
+            L.gaac_encode_blocks_ex.restype = i32
+            L.gaac_append_ex.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P, P, ctypes.c_uint, P, P]
+            L.gaac_append_ex.restype = i32
             L.gaac_attention_workspace.argtypes = [i32, i32, i32, i32]
             L.gaac_attention_workspace.restype = sz
             L.gaac_attention_auto_splits.argtypes = [i32, i32, i32]
@@ -190,32 +196,34 @@ def calibrate(x: torch.Tensor, base3: torch.Tensor, base4: torch.Tensor, status:
 
 
 def encode_blocks(k, v, seq_lens, max_blocks, base3, base4, table, slot_ids, pools: Pools, stats=None, status=None,
-                  stream=None) -> None:
+                  stream=None, open_compressed: bool = False) -> None:
     """Prefill encode of a layer.  k, v: BF16 [batch, tokens, kv_heads, 128]; seq_lens int32 [batch];
     base3/base4 uint8 [2, kv_heads, 128]; table from new_table(); slot_ids int32 shaped like the table,
-    or None to store every block as a raw BF16 tile (the uncompressed baseline)."""
+    or None to store every block as a raw BF16 tile (the uncompressed baseline).  open_compressed keeps
+    each sequence's incomplete last block in its slot (GAAC_OPEN_COMPRESSED)."""
     for t, n in ((k, "k"), (v, "v"), (seq_lens, "seq_lens"), (table, "table")):
         _cuda(t, n)
     ss, ts = _kv_strides(k, "k")
     if _kv_strides(v, "v") != (ss, ts):
         raise ValueError("k and v must share strides")
     pc = pools.c()
-    _check("gaac_encode_blocks", lib().gaac_encode_blocks(
+    _check("gaac_encode_blocks_ex", lib().gaac_encode_blocks_ex(
         k.data_ptr(), v.data_ptr(), ss, ts, min(k.shape[1], v.shape[1]), seq_lens.data_ptr(), k.shape[0], k.shape[2],
         max_blocks,
         base3.data_ptr(), base4.data_ptr(), table.data_ptr(), _ptr(slot_ids), ctypes.byref(pc), _ptr(stats),
-        _ptr(status), _stream(stream)))
+        OPEN_COMPRESSED if open_compressed else 0, _ptr(status), _stream(stream)))
 
 
 def append(k_new, v_new, seq_lens, max_blocks, base3, base4, table, slot_ids, pools: Pools, stats=None,
-           status=None, stream=None) -> None:
+           status=None, stream=None, open_compressed: bool = False) -> None:
     """Append one token per sequence.  k_new, v_new: BF16 [batch, kv_heads, 128]; slot_ids shaped like the
-    table (the slot a block is sealed into); seq_lens is incremented."""
+    table (the slot a block is sealed into, or kept open in with open_compressed); seq_lens is
+    incremented."""
     pc = pools.c()
-    _check("gaac_append", lib().gaac_append(
+    _check("gaac_append_ex", lib().gaac_append_ex(
         k_new.data_ptr(), v_new.data_ptr(), seq_lens.data_ptr(), k_new.shape[0], k_new.shape[1], max_blocks,
         base3.data_ptr(), base4.data_ptr(), table.data_ptr(), slot_ids.data_ptr(), ctypes.byref(pc),
-        _ptr(stats), _ptr(status), _stream(stream)))
+        _ptr(stats), OPEN_COMPRESSED if open_compressed else 0, _ptr(status), _stream(stream)))
 
 
 def attention_workspace(batch: int, n_kv_heads: int, max_blocks: int, n_splits: int = 0) -> int:

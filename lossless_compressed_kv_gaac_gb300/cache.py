@@ -18,11 +18,14 @@ class LayerCache:
     encoded (or sealed) into.  Default: a dense map (one slot per table position).
     n_raw: raw tiles available for tails and fallbacks (default: one per
     (sequence, kv-head, K|V) plus one per table position, i.e. never exhausted).
+    open_compressed: keep each sequence's open block compressed in its slot
+    (prefill and append), instead of as a BF16 tail.
     """
 
     def __init__(self, batch: int, n_kv_heads: int, max_blocks: int, device="cuda", slot_ids=None, n_slots=None,
-                 n_raw=None, raw_free=None):
+                 n_raw=None, raw_free=None, open_compressed: bool = False):
         self.batch, self.n_kv_heads, self.max_blocks = batch, n_kv_heads, max_blocks
+        self.open_compressed = open_compressed
         self.device = torch.device(device)
         positions = batch * max_blocks * n_kv_heads * 2
         if slot_ids is None:
@@ -53,12 +56,13 @@ class LayerCache:
         raw=True stores every block as BF16 (the uncompressed baseline cache)."""
         self.seq_lens.copy_(seq_lens)
         encode_blocks(k, v, self.seq_lens, self.max_blocks, self.base3, self.base4, self.table,
-                      None if raw else self.slot_ids, self.pools, self.stats, self.status, stream)
+                      None if raw else self.slot_ids, self.pools, self.stats, self.status, stream,
+                      open_compressed=self.open_compressed and not raw)
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """Decode step: one token per sequence, k_new/v_new BF16 [batch, kv_heads, 128]."""
         append(k_new, v_new, self.seq_lens, self.max_blocks, self.base3, self.base4, self.table, self.slot_ids,
-               self.pools, self.stats, self.status, stream)
+               self.pools, self.stats, self.status, stream, open_compressed=self.open_compressed)
 
     # -- reading
     def workspace(self, n_splits: int = 0) -> torch.Tensor:

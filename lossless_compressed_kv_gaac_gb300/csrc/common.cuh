@@ -135,6 +135,91 @@ __device__ __forceinline__ void join_bf16x4(uint32_t sm, uint32_t e, uint32_t& p
   p23 = __byte_perm(lo, hi, 0x7362);
 }
 
+// Exclusive prefixes of the 4-bit and raw group counts (packed n4 | nraw << 16)
+// over the 64 tag words of a slot image, into word_prefix[0..63], and the tile
+// totals into word_prefix[64].  Threads 0..31 of the CTA call it (one warp).
+__device__ __forceinline__ void slot_word_prefix(const uint8_t* slot, int lane, int* word_prefix) {
+  const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + kOffTag);
+  const int c0 = n4_of(tagw[lane]) | (nraw_of(tagw[lane]) << 16);
+  const int c1 = n4_of(tagw[lane + 32]) | (nraw_of(tagw[lane + 32]) << 16);
+  int i0 = c0, i1 = c1;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v0 = __shfl_up_sync(0xFFFFFFFFu, i0, d), v1 = __shfl_up_sync(0xFFFFFFFFu, i1, d);
+    if (lane >= d) {
+      i0 += v0;
+      i1 += v1;
+    }
+  }
+  const int tot0 = __shfl_sync(0xFFFFFFFFu, i0, 31);
+  word_prefix[lane] = i0 - c0;
+  word_prefix[lane + 32] = tot0 + i1 - c1;
+  if (lane == 31) word_prefix[64] = tot0 + i1;
+}
+
+// Rebuilds code unit u (storage elements 32u..32u+31) of a slot image into
+// pairs[m] = bf16x2 of storage elements 32u + 2m, 32u + 2m + 1.  word_prefix:
+// slot_word_prefix's output for this image; b3g/b4g: the 128 bases of the
+// tile's (kv-head, K|V).  Returns true when the unit fails a check of the
+// format (a reserved tag, an escape read past esc_len, a directory entry or the
+// totals differing from the tags).
+__device__ __forceinline__ bool decode_slot_unit(const uint8_t* slot, int kind, int u, const uint8_t* b3g,
+                                                 const uint8_t* b4g, int esc_len, const int* word_prefix,
+                                                 uint32_t pairs[16]) {
+  const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + kOffTag);
+  const uint32_t* cw = reinterpret_cast<const uint32_t*>(slot + kOffCode);
+  const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
+  const uint32_t tagbyte = slot[kOffTag + u];
+  const uint32_t tword = tagw[u >> 2];
+  const uint32_t before = tword & ((1u << (8 * (u & 3))) - 1u);  // tags of the word's earlier units
+  const int pre = word_prefix[u >> 2] + (n4_of(before) | (nraw_of(before) << 16));
+  const int tot = word_prefix[64];
+  const int tot4 = tot & 0xFFFF, totraw = tot >> 16;
+  int o4 = pre & 0xFFFF, oraw = tot4 + 8 * (pre >> 16);
+  // The escape directory must hold the counts at each eighth boundary and the totals.
+  const uint16_t* dir = reinterpret_cast<const uint16_t*>(slot + kOffDir);
+  bool bad = reserved_in(tagbyte);
+  if ((u & (kDirUnits - 1)) == 0 && u > 0 &&
+      dir[u / kDirUnits - 1] != (((pre & 0xFFFF) & 0x1FF) | (((pre >> 16) & 0x7F) << 9)))
+    bad = true;
+  if (u == 255 && (dir[7] != ((tot4 & 0x1FF) | ((totraw & 0x7F) << 9)) || tot4 + 8 * totraw != esc_len))
+    bad = true;
+  const uint4* smp = reinterpret_cast<const uint4*>(slot + 32 * u);
+  const uint4 s0 = smp[0], s1 = smp[1];
+  uint32_t smw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {  // signs back to their own bytes (stored one byte up, cyclically)
+    const uint32_t sg = smw[j] & 0x80808080u;
+    smw[j] = (smw[j] & 0x7F7F7F7Fu) | ((sg >> 8) | (sg << 24));
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t b3[4], b4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (kind == 0) {  // K: element 4q+L of half hh is channel 32(u%4) + 16hh + 4q + L
+        const int c = 32 * (u & 3) + 16 * hh + 4 * q;
+        b3[q] = *reinterpret_cast<const uint32_t*>(b3g + c);
+        b4[q] = *reinterpret_cast<const uint32_t*>(b4g + c);
+      } else {  // V: element 4q+L of half hh is storage element 32u + 16hh + 4q + L
+        b3[q] = b4[q] = 0u;
+#pragma unroll
+        for (int L = 0; L < 4; ++L) {
+          const int c = v_channel_of(32 * u + 16 * hh + 4 * q + L);
+          b3[q] |= static_cast<uint32_t>(b3g[c]) << (8 * L);
+          b4[q] |= static_cast<uint32_t>(b4g[c]) << (8 * L);
+        }
+      }
+    }
+    uint32_t e[4];
+    half_exponents_v3(hh == 0 ? W0 : W1, W2, hh, (tagbyte >> (4 * hh)) & 15u, b3, b4, slot, &o4, &oraw, esc_len, e,
+                      &bad);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) join_bf16x4(smw[4 * hh + q], e[q], pairs[8 * hh + 2 * q], pairs[8 * hh + 2 * q + 1]);
+  }
+  return bad;
+}
+
 // ------------------------------------------------------- mbarrier / bulk ----
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

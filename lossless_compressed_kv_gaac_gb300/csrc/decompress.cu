@@ -66,77 +66,10 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
     }
   } else {
     const uint8_t* slot = a.slot_pool + static_cast<size_t>(ent.index) * kSlot;
-    const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + kOffTag);
-    if (tid < 32) {  // exclusive prefixes of 4-bit and raw group counts over the 64 tag words (packed)
-      const int c0 = n4_of(tagw[tid]) | (nraw_of(tagw[tid]) << 16);
-      const int c1 = n4_of(tagw[tid + 32]) | (nraw_of(tagw[tid + 32]) << 16);
-      int i0 = c0, i1 = c1;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int v0 = __shfl_up_sync(0xFFFFFFFFu, i0, d), v1 = __shfl_up_sync(0xFFFFFFFFu, i1, d);
-        if (tid >= d) {
-          i0 += v0;
-          i1 += v1;
-        }
-      }
-      const int tot0 = __shfl_sync(0xFFFFFFFFu, i0, 31);
-      word_prefix[tid] = i0 - c0;
-      word_prefix[tid + 32] = tot0 + i1 - c1;
-      if (tid == 31) word_prefix[64] = tot0 + i1;  // tile totals
-    }
+    if (tid < 32) slot_word_prefix(slot, tid, word_prefix);
     __syncthreads();
-    const uint32_t* cw = reinterpret_cast<const uint32_t*>(slot + kOffCode);
-    const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
-    const uint32_t tagbyte = slot[kOffTag + u];
-    const uint32_t tword = tagw[u >> 2];
-    const uint32_t before = tword & ((1u << (8 * (u & 3))) - 1u);  // tags of the word's earlier units
-    const int pre = word_prefix[u >> 2] + (n4_of(before) | (nraw_of(before) << 16));
-    const int tot = word_prefix[64];
-    const int tot4 = tot & 0xFFFF, totraw = tot >> 16;
-    int o4 = pre & 0xFFFF, oraw = tot4 + 8 * (pre >> 16);
-    // The escape directory must hold the counts at each eighth boundary and the totals.
-    const uint16_t* dir = reinterpret_cast<const uint16_t*>(slot + kOffDir);
-    bool bad = reserved_in(tagbyte);
-    if ((u & (kDirUnits - 1)) == 0 && u > 0 &&
-        dir[u / kDirUnits - 1] != (((pre & 0xFFFF) & 0x1FF) | (((pre >> 16) & 0x7F) << 9)))
-      bad = true;
-    if (u == 255 && (dir[7] != ((tot4 & 0x1FF) | ((totraw & 0x7F) << 9)) || tot4 + 8 * totraw != ent.esc_len))
-      bad = true;
-    const uint4* smp = reinterpret_cast<const uint4*>(slot + 32 * u);
-    const uint4 s0 = smp[0], s1 = smp[1];
-    uint32_t smw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {  // signs back to their own bytes (stored one byte up, cyclically)
-      const uint32_t sg = smw[j] & 0x80808080u;
-      smw[j] = (smw[j] & 0x7F7F7F7Fu) | ((sg >> 8) | (sg << 24));
-    }
-    const uint8_t* b3g = a.base3 + (kind * a.n_kv_heads + h) * kD;
-    const uint8_t* b4g = a.base4 + (kind * a.n_kv_heads + h) * kD;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t b3[4], b4[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (kind == 0) {  // K: element 4q+L of half hh is channel 32(u%4) + 16hh + 4q + L
-          const int c = 32 * (u & 3) + 16 * hh + 4 * q;
-          b3[q] = *reinterpret_cast<const uint32_t*>(b3g + c);
-          b4[q] = *reinterpret_cast<const uint32_t*>(b4g + c);
-        } else {  // V: element 4q+L of half hh is storage element 32u + 16hh + 4q + L
-          b3[q] = b4[q] = 0u;
-#pragma unroll
-          for (int L = 0; L < 4; ++L) {
-            const int c = v_channel_of(32 * u + 16 * hh + 4 * q + L);
-            b3[q] |= static_cast<uint32_t>(b3g[c]) << (8 * L);
-            b4[q] |= static_cast<uint32_t>(b4g[c]) << (8 * L);
-          }
-        }
-      }
-      uint32_t e[4];
-      half_exponents_v3(hh == 0 ? W0 : W1, W2, hh, (tagbyte >> (4 * hh)) & 15u, b3, b4, slot, &o4, &oraw,
-                        ent.esc_len, e, &bad);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) join_bf16x4(smw[4 * hh + q], e[q], pairs[8 * hh + 2 * q], pairs[8 * hh + 2 * q + 1]);
-    }
+    const bool bad = decode_slot_unit(slot, kind, u, a.base3 + (kind * a.n_kv_heads + h) * kD,
+                                      a.base4 + (kind * a.n_kv_heads + h) * kD, ent.esc_len, word_prefix, pairs);
     if (bad) report(a.status, GAAC_EFORMAT);
   }
   // Storage order -> token-major.

@@ -32,13 +32,29 @@ struct EncShared {
 // Channel of storage element s (format v3).
 __device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? (s & 127) : v_channel_of(s); }
 
+// Token of storage element s (format v3).
+__device__ __forceinline__ int token_of(int kind, int s) { return kind == 0 ? (s >> 7) : v_token_of(s); }
+
+// Whether code unit u holds elements of token t: a K unit is a quarter of one
+// token, a V unit unit 32 (2w + h) + 4g + q holds tokens 16w + 2q + {0, 1, 8, 9}.
+__device__ __forceinline__ bool unit_holds_token(int kind, int u, int t) {
+  return kind == 0 ? (u >> 2) == t : ((u >> 6) == (t >> 4) && (u & 3) == ((t & 7) >> 1));
+}
+
 // Encodes the tile in sh->tile into `slot` (global, 16-byte aligned) unless its
 // escape stream exceeds the capacity.  Returns the escape length, or -1 when
 // the tile must stay raw (then nothing is written).  CTA-uniform result; all
 // 256 threads must call it.
+//
+// n_present < 64 encodes an open tile: elements of tokens >= n_present are
+// absent (sh->tile must hold zero there); they take no part in their group's
+// mode, and their codes and escape bits are zero.  only_token >= 0 writes the
+// sign|mantissa and code words of the units holding that token only (the
+// other units' bytes must already be in the slot: appending one token changes
+// no other unit), and the tag plane, directory and escape area in full.
 __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restrict__ b3g,
                                const uint8_t* __restrict__ b4g, uint8_t* __restrict__ slot,
-                               gaac_stats* stats) {
+                               gaac_stats* stats, int n_present = kBlock, int only_token = -1) {
   const int u = threadIdx.x;
   const int lane = u & 31, warp = u >> 5;
   uint32_t xw[16];
@@ -68,10 +84,12 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     int e[8], b3[8], b4[8];
+    bool pres[8];
     bool fits3 = true, fits4 = true;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int el = 8 * gi + j;
+      pres[j] = token_of(kind, 32 * u + el) < n_present;
       const uint32_t x = (xw[el >> 1] >> (16 * (el & 1))) & 0xFFFFu;
       e[j] = (x >> 7) & 0xFF;
       ew[el >> 2] |= static_cast<uint32_t>(e[j]) << (8 * (el & 3));
@@ -81,8 +99,8 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
       b3[j] = b3g[c];
       b4[j] = b4g[c];
       const int o3 = e[j] - b3[j], o4 = e[j] - b4[j];
-      fits3 = fits3 && (o3 >= 0) && (o3 <= 7);
-      fits4 = fits4 && (o4 >= 0) && (o4 <= 15);
+      fits3 = fits3 && (!pres[j] || ((o3 >= 0) && (o3 <= 7)));
+      fits4 = fits4 && (!pres[j] || ((o4 >= 0) && (o4 <= 15)));
     }
     const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
     tagbyte |= mode << (2 * gi);
@@ -91,7 +109,9 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       uint32_t cd = 0;  // raw groups keep code 0: their exponents are escape bytes
-      if (mode == 0u) {
+      if (!pres[j]) {
+        // absent element: code and escape bit zero
+      } else if (mode == 0u) {
         cd = static_cast<uint32_t>(e[j] - b3[j]) & 7u;
       } else if (mode == 1u) {
         const uint32_t off = static_cast<uint32_t>(e[j] - b4[j]) & 0xFFu;
@@ -150,13 +170,15 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
     const uint32_t sg = smb[j] & 0x80808080u;
     smb[j] = (smb[j] & 0x7F7F7F7Fu) | ((sg << 8) | (sg >> 24));
   }
-  uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
-  smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
-  smdst[1] = make_uint4(smb[4], smb[5], smb[6], smb[7]);
-  uint32_t* cw = reinterpret_cast<uint32_t*>(slot + kOffCode);
-  cw[u] = W[0];
-  cw[256 + u] = W[1];
-  cw[512 + u] = W[2];
+  if (only_token < 0 || unit_holds_token(kind, u, only_token)) {
+    uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
+    smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
+    smdst[1] = make_uint4(smb[4], smb[5], smb[6], smb[7]);
+    uint32_t* cw = reinterpret_cast<uint32_t*>(slot + kOffCode);
+    cw[u] = W[0];
+    cw[256 + u] = W[1];
+    cw[512 + u] = W[2];
+  }
   slot[kOffTag + u] = static_cast<uint8_t>(tagbyte);
   uint8_t* escp = slot + kOffEsc;
   for (int k = 0; k < n4; ++k) escp[off4 + k] = static_cast<uint8_t>(esc4 >> (8 * k));
@@ -234,6 +256,7 @@ struct EncodeArgs {
   const uint32_t* slot_ids;
   gaac_pools pools;
   gaac_stats* stats;
+  unsigned flags;
   int32_t* status;
 };
 
@@ -288,7 +311,8 @@ __global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a
   __syncthreads();
   const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
   const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
-  if (nv == kBlock && a.slot_ids != nullptr) {
+  if ((nv == kBlock || (a.flags & GAAC_OPEN_COMPRESSED)) && a.slot_ids != nullptr) {
+    // a full block, or the open last block kept in its slot
     const uint32_t slot_id = a.slot_ids[eidx];
     uint8_t* slot = nullptr;
     if (static_cast<int64_t>(slot_id) < a.pools.n_slots) {
@@ -296,9 +320,9 @@ __global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a
     } else if (tid == 0) {
       report(a.status, GAAC_EPOOL);
     }
-    const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, a.stats);
+    const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, nv == kBlock ? a.stats : nullptr, nv);
     if (esc >= 0) {
-      if (tid == 0) a.table[eidx] = make_entry(slot_id, esc, GAAC_MODE_SLOT, kBlock);
+      if (tid == 0) a.table[eidx] = make_entry(slot_id, esc, GAAC_MODE_SLOT, nv);
       return;
     }
   }
@@ -335,12 +359,18 @@ struct AppendArgs {
   const uint32_t* slot_ids;
   gaac_pools pools;
   gaac_stats* stats;
+  unsigned flags;
   int32_t* status;
 };
+
+// How one append reaches its block.
+enum AppendPath { kFail = 0, kRawTail = 1, kRawFresh = 2, kOpenNew = 3, kOpenSlot = 4 };
 
 // grid (2*n_kv_heads, batch): x = h*2 + kind.
 __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   __shared__ EncShared sh;
+  __shared__ int word_prefix[65];
+  __shared__ int esc_old;
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1, b = blockIdx.y;
   const int tid = threadIdx.x;
   const int len = a.seq_lens[b];
@@ -349,39 +379,120 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
     return;
   }
   const int blk = len / kBlock, pos = len % kBlock;
-  gaac_entry* ep = a.table + ((static_cast<size_t>(b) * a.max_blocks + blk) * a.n_kv_heads + h) * 2 + kind;
+  const size_t eidx = ((static_cast<size_t>(b) * a.max_blocks + blk) * a.n_kv_heads + h) * 2 + kind;
+  gaac_entry* ep = a.table + eidx;
+  const bool open_c = (a.flags & GAAC_OPEN_COMPRESSED) != 0u;
   if (tid == 0) {
-    gaac_entry e = *ep;
-    int ok = 1;
-    if (e.mode != GAAC_MODE_RAW) {
-      if (pos != 0) {
-        report(a.status, GAAC_EFORMAT);
-        ok = 0;
+    const gaac_entry e = *ep;
+    int path = kFail;
+    uint32_t idx = 0;
+    if (e.mode == GAAC_MODE_RAW) {  // a raw tail (from prefill, a hand-over or an overflow)
+      if (e.n_tok == pos && static_cast<int64_t>(e.index) < a.pools.n_raw) {
+        path = kRawTail;
+        idx = e.index;
       } else {
-        uint32_t idx = 0;
-        ok = pop_raw(a.pools, &idx, a.status) ? 2 : 0;  // 2: a fresh tile, cleared below
-        e = make_entry(idx, 0, GAAC_MODE_RAW, 0);
+        report(a.status, GAAC_EFORMAT);
       }
-    } else if (e.n_tok != pos || static_cast<int64_t>(e.index) >= a.pools.n_raw) {
+    } else if (pos == 0) {  // the block opens
+      if (open_c) {
+        idx = a.slot_ids[eidx];
+        if (static_cast<int64_t>(idx) < a.pools.n_slots)
+          path = kOpenNew;
+        else
+          report(a.status, GAAC_EPOOL);
+      } else if (pop_raw(a.pools, &idx, a.status)) {
+        path = kRawFresh;
+      }
+    } else if (open_c && e.mode == GAAC_MODE_SLOT && e.n_tok == pos &&
+               static_cast<int64_t>(e.index) < a.pools.n_slots && e.esc_len <= kEscCap) {
+      path = kOpenSlot;
+      idx = e.index;
+      esc_old = e.esc_len;
+    } else {
       report(a.status, GAAC_EFORMAT);
-      ok = 0;
     }
-    sh.raw_idx = e.index;
-    sh.ok = ok;
+    sh.raw_idx = idx;
+    sh.ok = path;
   }
   __syncthreads();
-  if (!sh.ok) return;
+  const int path = sh.ok;
+  if (path == kFail) return;
+  const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
+  const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
+  const uint16_t x_new =
+      tid < kD ? (kind == 0 ? a.k_new : a.v_new)[(static_cast<size_t>(b) * a.n_kv_heads + h) * kD + tid] : 0;
+  const int s_new = kind == 0 ? pos * kD + tid : v_storage_index(pos, tid & (kD - 1));
+
+  if (path >= kOpenNew) {
+    // The open block lives in its slot: rebuild its tokens so far (absent
+    // elements zero), add the new token and encode the first pos + 1 tokens.
+    // Only the units holding the new token, the tags, the directory and the
+    // escape area change.
+    const uint32_t slot_id = sh.raw_idx;
+    uint8_t* slot = a.pools.slot_pool + static_cast<size_t>(slot_id) * kSlot;
+    bool bad = false;
+    uint4* mine = reinterpret_cast<uint4*>(sh.tile + 32 * tid);
+    if (path == kOpenSlot) {
+      if (tid < 32) slot_word_prefix(slot, tid, word_prefix);
+      __syncthreads();
+      uint32_t pairs[16];
+      bad = decode_slot_unit(slot, kind, tid, b3, b4, esc_old, word_prefix, pairs);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const int s0 = 32 * tid + 2 * m;
+        const uint32_t lo = token_of(kind, s0) < pos ? (pairs[m] & 0xFFFFu) : 0u;
+        const uint32_t hi = token_of(kind, s0 + 1) < pos ? (pairs[m] & 0xFFFF0000u) : 0u;
+        pairs[m] = lo | hi;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mine[i] = make_uint4(pairs[4 * i], pairs[4 * i + 1], pairs[4 * i + 2], pairs[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mine[i] = make_uint4(0, 0, 0, 0);
+    }
+    if (__syncthreads_or(bad)) {
+      if (tid == 0) report(a.status, GAAC_EFORMAT);
+      return;
+    }
+    if (tid < kD) sh.tile[s_new] = x_new;
+    __syncthreads();
+    const bool sealing = pos + 1 == kBlock;
+    const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, sealing ? a.stats : nullptr, pos + 1,
+                                    path == kOpenSlot ? pos : -1);
+    if (esc >= 0) {
+      if (tid == 0) *ep = make_entry(slot_id, esc, GAAC_MODE_SLOT, pos + 1);
+      return;
+    }
+    // The escape stream outgrew the slot (it only grows as tokens arrive, so
+    // the full block would not fit either): the block continues as a raw tile.
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t idx = 0;
+      sh.ok = pop_raw(a.pools, &idx, a.status) ? 1 : 0;
+      sh.raw_idx = idx;
+    }
+    __syncthreads();
+    if (!sh.ok) return;
+    uint4* dst = reinterpret_cast<uint4*>(a.pools.raw_pool + static_cast<size_t>(sh.raw_idx) * kTile);
+    const uint4* src = reinterpret_cast<const uint4*>(sh.tile);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[tid + kEncThreads * i] = src[tid + kEncThreads * i];
+    if (tid == 0) {
+      *ep = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, pos + 1);
+      if (a.stats != nullptr) atomicAdd(sealing ? &a.stats->raw_tiles : &a.stats->tail_tiles, 1ull);
+    }
+    return;
+  }
+
+  // Raw tail: write the token in place; encode the block once when it fills.
   uint16_t* raw = a.pools.raw_pool + static_cast<size_t>(sh.raw_idx) * kTile;
-  if (sh.ok == 2) {
+  if (path == kRawFresh) {
     uint4* d = reinterpret_cast<uint4*>(raw);
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[tid + kEncThreads * i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
   }
-  if (tid < kD) {
-    const uint16_t x = (kind == 0 ? a.k_new : a.v_new)[(static_cast<size_t>(b) * a.n_kv_heads + h) * kD + tid];
-    raw[kind == 0 ? pos * kD + tid : v_storage_index(pos, tid)] = x;
-  }
+  if (tid < kD) raw[s_new] = x_new;
   if (pos + 1 < kBlock) {
     if (tid == 0) *ep = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, pos + 1);
     return;
@@ -389,21 +500,19 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   // The block is full: seal it (encode once; it is never re-encoded).
   __syncthreads();
   {
-    const uint4* s = reinterpret_cast<const uint4*>(raw);
+    const uint4* src = reinterpret_cast<const uint4*>(raw);
     uint4* d = reinterpret_cast<uint4*>(sh.tile);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) d[tid + kEncThreads * i] = s[tid + kEncThreads * i];
+    for (int i = 0; i < 4; ++i) d[tid + kEncThreads * i] = src[tid + kEncThreads * i];
   }
   __syncthreads();
-  const uint32_t slot_id = a.slot_ids[((static_cast<size_t>(b) * a.max_blocks + blk) * a.n_kv_heads + h) * 2 + kind];
+  const uint32_t slot_id = a.slot_ids[eidx];
   uint8_t* slot = nullptr;
   if (static_cast<int64_t>(slot_id) < a.pools.n_slots) {
     slot = a.pools.slot_pool + static_cast<size_t>(slot_id) * kSlot;
   } else if (tid == 0) {
     report(a.status, GAAC_EPOOL);
   }
-  const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
-  const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
   const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, a.stats);
   if (esc >= 0 && blk + 1 < a.max_blocks) {
     // The raw tile becomes the next block's empty tail: clear it so that a tail
@@ -438,13 +547,13 @@ static bool pools_ok(const gaac_pools* p) {
          (reinterpret_cast<uintptr_t>(p->slot_pool) & 15u) == 0 && (reinterpret_cast<uintptr_t>(p->raw_pool) & 15u) == 0;
 }
 
-extern "C" int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t seq_stride, int64_t tok_stride,
-                                  int64_t n_tok, const int32_t* seq_lens, int batch, int n_kv_heads, int max_blocks,
-                                  const uint8_t* base3, const uint8_t* base4, gaac_entry* table,
-                                  const uint32_t* slot_ids, const gaac_pools* pools, gaac_stats* stats,
-                                  int32_t* d_status, void* stream) {
+extern "C" int gaac_encode_blocks_ex(const uint16_t* k, const uint16_t* v, int64_t seq_stride, int64_t tok_stride,
+                                     int64_t n_tok, const int32_t* seq_lens, int batch, int n_kv_heads,
+                                     int max_blocks, const uint8_t* base3, const uint8_t* base4, gaac_entry* table,
+                                     const uint32_t* slot_ids, const gaac_pools* pools, gaac_stats* stats,
+                                     unsigned flags, int32_t* d_status, void* stream) {
   if (k == nullptr || v == nullptr || seq_lens == nullptr || base3 == nullptr || base4 == nullptr ||
-      table == nullptr || !pools_ok(pools))
+      table == nullptr || !pools_ok(pools) || (flags & ~static_cast<unsigned>(GAAC_OPEN_COMPRESSED)))
     return GAAC_EINVAL;
   if (batch <= 0 || n_kv_heads <= 0 || max_blocks <= 0 || max_blocks > 65535 || batch > 65535 ||
       n_kv_heads > 1024)
@@ -454,9 +563,36 @@ extern "C" int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t 
     return GAAC_EINVAL;
   if (n_tok < 0) return GAAC_EINVAL;
   EncodeArgs a{k, v, seq_stride, tok_stride, n_tok, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids,
-               *pools, stats, d_status};
+               *pools, stats, flags, d_status};
   dim3 grid(2 * n_kv_heads, max_blocks, batch);
   encode_blocks_kernel<<<grid, kEncThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
+
+extern "C" int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t seq_stride, int64_t tok_stride,
+                                  int64_t n_tok, const int32_t* seq_lens, int batch, int n_kv_heads, int max_blocks,
+                                  const uint8_t* base3, const uint8_t* base4, gaac_entry* table,
+                                  const uint32_t* slot_ids, const gaac_pools* pools, gaac_stats* stats,
+                                  int32_t* d_status, void* stream) {
+  return gaac_encode_blocks_ex(k, v, seq_stride, tok_stride, n_tok, seq_lens, batch, n_kv_heads, max_blocks, base3,
+                               base4, table, slot_ids, pools, stats, 0u, d_status, stream);
+}
+
+extern "C" int gaac_append_ex(const uint16_t* k_new, const uint16_t* v_new, int32_t* seq_lens, int batch,
+                              int n_kv_heads, int max_blocks, const uint8_t* base3, const uint8_t* base4,
+                              gaac_entry* table, const uint32_t* slot_ids, const gaac_pools* pools,
+                              gaac_stats* stats, unsigned flags, int32_t* d_status, void* stream) {
+  if (k_new == nullptr || v_new == nullptr || seq_lens == nullptr || base3 == nullptr || base4 == nullptr ||
+      table == nullptr || slot_ids == nullptr || !pools_ok(pools) ||
+      (flags & ~static_cast<unsigned>(GAAC_OPEN_COMPRESSED)))
+    return GAAC_EINVAL;
+  if (batch <= 0 || batch > 65535 || n_kv_heads <= 0 || n_kv_heads > 1024 || max_blocks <= 0) return GAAC_EINVAL;
+  AppendArgs a{k_new, v_new, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids, *pools,
+               stats, flags, d_status};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  append_kernel<<<dim3(2 * n_kv_heads, batch), kEncThreads, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return GAAC_ECUDA;
+  bump_lens_kernel<<<(batch + 255) / 256, 256, 0, st>>>(seq_lens, batch);
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
 
@@ -464,15 +600,6 @@ extern "C" int gaac_append(const uint16_t* k_new, const uint16_t* v_new, int32_t
                            int n_kv_heads, int max_blocks, const uint8_t* base3, const uint8_t* base4,
                            gaac_entry* table, const uint32_t* slot_ids, const gaac_pools* pools,
                            gaac_stats* stats, int32_t* d_status, void* stream) {
-  if (k_new == nullptr || v_new == nullptr || seq_lens == nullptr || base3 == nullptr || base4 == nullptr ||
-      table == nullptr || slot_ids == nullptr || !pools_ok(pools))
-    return GAAC_EINVAL;
-  if (batch <= 0 || batch > 65535 || n_kv_heads <= 0 || n_kv_heads > 1024 || max_blocks <= 0) return GAAC_EINVAL;
-  AppendArgs a{k_new, v_new, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids, *pools,
-               stats, d_status};
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  append_kernel<<<dim3(2 * n_kv_heads, batch), kEncThreads, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return GAAC_ECUDA;
-  bump_lens_kernel<<<(batch + 255) / 256, 256, 0, st>>>(seq_lens, batch);
-  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+  return gaac_append_ex(k_new, v_new, seq_lens, batch, n_kv_heads, max_blocks, base3, base4, table, slot_ids, pools,
+                        stats, 0u, d_status, stream);
 }

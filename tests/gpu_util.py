@@ -44,9 +44,10 @@ def logical_tile(x_np, b, blk, h, nv):
     return tile
 
 
-def check_tiles(c: LayerCache, k, v, lens, tiles=None, b3=None, b4=None, raw_all=False):
+def check_tiles(c: LayerCache, k, v, lens, tiles=None, b3=None, b4=None, raw_all=False, open_compressed=False):
     """Every (or the listed) tile of the cache equals the oracle's encoding of the input bits.
-    tiles: iterable of (b, blk, h, kind).  Returns counts of slot / raw tiles checked."""
+    tiles: iterable of (b, blk, h, kind).  open_compressed: open blocks are expected in their slots
+    (the oracle's open-tile image) unless that overflows.  Returns counts of slot / raw tiles checked."""
     kn, vn = u16(k), u16(v)
     lens_np = lens.cpu().numpy()
     if b3 is None:
@@ -66,11 +67,11 @@ def check_tiles(c: LayerCache, k, v, lens, tiles=None, b3=None, b4=None, raw_all
             n["none"] += 1
             continue
         tile = logical_tile(kn if kind == 0 else vn, b, blk, h, nv)
-        if nv == 64 and not raw_all:
-            img, e = O.encode_tile(tile, kind, b3[kind, h], b4[kind, h])
+        if (nv == 64 or open_compressed) and not raw_all:
+            img, e = O.encode_open_tile(tile, nv, kind, b3[kind, h], b4[kind, h])
             if e >= 0:
                 assert m == MODE_SLOT, (b, blk, h, kind, m)
-                assert esc[b, blk, h, kind] == e and ntok[b, blk, h, kind] == 64
+                assert esc[b, blk, h, kind] == e and ntok[b, blk, h, kind] == nv
                 got = slots[idx[b, blk, h, kind]]
                 if not np.array_equal(got, img):
                     bad = np.nonzero(got != img)[0]
