@@ -34,7 +34,7 @@ CONFIG_ID = 1
 
 # DRAM bytes (read + write) of one attn_split_kernel launch on this workload, from an
 # ncu capture, valid only for the kernel source it was taken on (see profiles/).
-NCU_TRAFFIC = {"kernel_sha": "be7069b20e274bb0", "bytes_per_launch": 195794944}
+NCU_TRAFFIC = {"kernel_sha": "6d6cc2b2a39e75e5", "bytes_per_launch": 195849472}
 
 
 def kernel_sha() -> str:
@@ -233,6 +233,43 @@ def fp8_codec(k, v, n_calib: int) -> dict:
     return out
 
 
+def append_cost(k, v, n_calib: int) -> dict:
+    """Device time of one decode-token append (all kv-heads, K and V, one layer, batch 1) with the
+    open block as a BF16 raw tail and with it kept compressed in its slot.  64 consecutive appends (a
+    block opening, 62 in-block tokens and a seal) are captured in a CUDA graph and replayed; the
+    time per append is the replay's CUDA-event time / 64."""
+    import torch
+
+    from lossless_compressed_kv_gaac_gb300.cache import LayerCache
+
+    H = k.shape[2]
+    T0, reps = 1024, 4
+    out = {"unit": "us per append", "tokens_per_replay": 64}
+    stream = torch.cuda.Stream(k.device)
+    kn = k[0, T0:T0 + 64].unsqueeze(1).contiguous()  # [64, 1, H, 128]
+    vn = v[0, T0:T0 + 64].unsqueeze(1).contiguous()
+    for name, open_c in (("raw_tail", False), ("open_compressed", True)):
+        c = LayerCache(1, H, T0 // 64 + 64 * (reps + 2) // 64, device=k.device, open_compressed=open_c)
+        c.calibrate(k[0, :n_calib], v[0, :n_calib])
+        c.encode(k[:, :T0], v[:, :T0], torch.tensor([T0], dtype=torch.int32, device=k.device))
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(64):
+                    c.append(kn[i], vn[i], stream=stream)
+        torch.cuda.synchronize()
+        times = []
+        for r in range(reps):
+            t = time_graph(g, stream, 1)
+            if r:
+                times.append(t)
+        assert int(c.status.item()) == 0, "append reported an error"
+        assert int(c.seq_lens.item()) == T0 + 64 * reps
+        out[name] = round(min(times) * 1e3 / 64, 2)
+    return out
+
+
 def run_gaac(args):
     import torch
 
@@ -283,6 +320,7 @@ def run_gaac(args):
     decompress_gbs = raw_bytes_layer / (min(dec_t) * 1e-3) / 1e9
     st = G.stats_dict(c0.stats)
     fp8 = fp8_codec(k0, v0, wl.n_calib)
+    app = append_cost(k0, v0, wl.n_calib)
     del k0, v0, kd, vd
     alg = [algorithmic_bytes(c) for c in caches]
     alg_step = sum(alg)
@@ -426,6 +464,7 @@ def run_gaac(args):
         "encode_gbs": round(encode_gbs, 1),
         "decompress_gbs": round(decompress_gbs, 1),
         "fp8": fp8,
+        "append": app,
         "ratio": {"payload": round(payload_ratio, 4), "resident": round(resident_ratio, 4),
                   "mode_shares": [round(st[f"groups{m}"] / max(1, 1024 * st["slot_tiles"]), 5) for m in range(3)]},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",

@@ -52,6 +52,9 @@ __device__ __forceinline__ bool unit_holds_token(int kind, int u, int t) {
 // sign|mantissa and code words of the units holding that token only (the
 // other units' bytes must already be in the slot: appending one token changes
 // no other unit), and the tag plane, directory and escape area in full.
+// kOpen = false compiles the sealed-tile encoder (n_present and only_token
+// are then ignored: every token present, every unit written).
+template <bool kOpen>
 __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restrict__ b3g,
                                const uint8_t* __restrict__ b4g, uint8_t* __restrict__ slot,
                                gaac_stats* stats, int n_present = kBlock, int only_token = -1) {
@@ -89,7 +92,7 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int el = 8 * gi + j;
-      pres[j] = token_of(kind, 32 * u + el) < n_present;
+      pres[j] = !kOpen || token_of(kind, 32 * u + el) < n_present;
       const uint32_t x = (xw[el >> 1] >> (16 * (el & 1))) & 0xFFFFu;
       e[j] = (x >> 7) & 0xFF;
       ew[el >> 2] |= static_cast<uint32_t>(e[j]) << (8 * (el & 3));
@@ -170,7 +173,7 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
     const uint32_t sg = smb[j] & 0x80808080u;
     smb[j] = (smb[j] & 0x7F7F7F7Fu) | ((sg << 8) | (sg >> 24));
   }
-  if (only_token < 0 || unit_holds_token(kind, u, only_token)) {
+  if (!kOpen || only_token < 0 || unit_holds_token(kind, u, only_token)) {
     uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
     smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
     smdst[1] = make_uint4(smb[4], smb[5], smb[6], smb[7]);
@@ -320,7 +323,8 @@ __global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a
     } else if (tid == 0) {
       report(a.status, GAAC_EPOOL);
     }
-    const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, nv == kBlock ? a.stats : nullptr, nv);
+    const int esc = nv == kBlock ? encode_tile_cta<false>(&sh, kind, b3, b4, slot, a.stats)
+                                 : encode_tile_cta<true>(&sh, kind, b3, b4, slot, nullptr, nv);
     if (esc >= 0) {
       if (tid == 0) a.table[eidx] = make_entry(slot_id, esc, GAAC_MODE_SLOT, nv);
       return;
@@ -457,8 +461,8 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
     if (tid < kD) sh.tile[s_new] = x_new;
     __syncthreads();
     const bool sealing = pos + 1 == kBlock;
-    const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, sealing ? a.stats : nullptr, pos + 1,
-                                    path == kOpenSlot ? pos : -1);
+    const int esc = encode_tile_cta<true>(&sh, kind, b3, b4, slot, sealing ? a.stats : nullptr, pos + 1,
+                                          path == kOpenSlot ? pos : -1);
     if (esc >= 0) {
       if (tid == 0) *ep = make_entry(slot_id, esc, GAAC_MODE_SLOT, pos + 1);
       return;
@@ -513,7 +517,7 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   } else if (tid == 0) {
     report(a.status, GAAC_EPOOL);
   }
-  const int esc = encode_tile_cta(&sh, kind, b3, b4, slot, a.stats);
+  const int esc = encode_tile_cta<false>(&sh, kind, b3, b4, slot, a.stats);
   if (esc >= 0 && blk + 1 < a.max_blocks) {
     // The raw tile becomes the next block's empty tail: clear it so that a tail
     // always holds zeros past its last token.
