@@ -60,6 +60,14 @@ def lib() -> ctypes.CDLL:
             L.gaac_ref_encode_tile.restype = i32
             L.gaac_ref_encode_open_tile.argtypes = [P, i32, i32, P, P, P, i32]
             L.gaac_ref_encode_open_tile.restype = i32
+            L.gaac_ref_nested_slot_bytes.argtypes = []
+            L.gaac_ref_nested_slot_bytes.restype = i32
+            L.gaac_ref_nested_calibrate.argtypes = [P, i64, i64, i32, P]
+            L.gaac_ref_nested_calibrate.restype = None
+            L.gaac_ref_nested_encode_tile.argtypes = [P, i32, P, P, P, P, P]
+            L.gaac_ref_nested_encode_tile.restype = i32
+            L.gaac_ref_nested_decode_tile.argtypes = [P, i32, P, P, P, P]
+            L.gaac_ref_nested_decode_tile.restype = i32
             L.gaac_ref_decode_tile.argtypes = [P, i32, P, P, i32, P]
             L.gaac_ref_decode_tile.restype = i32
             L.gaac_ref_mode_counts.argtypes = [P, P]
@@ -257,3 +265,41 @@ def fp8_mode_counts(img, fmt: int) -> np.ndarray:
     out = np.zeros(4, np.int64)
     lib().gaac_ref_fp8_mode_counts(_ptr(img), fmt, _ptr(out))
     return out
+
+
+# ---- nested 2-bit mode: the ablation format of the GAAC page's section 4.7.2 (Table 4)
+NESTED_OFF_ESC = 11552
+
+
+def nested_slot_bytes() -> int:
+    return lib().gaac_ref_nested_slot_bytes()
+
+
+def nested_calibrate(x) -> np.ndarray:
+    """x: uint16 [n_tok][n_heads][128] BF16 bits -> base2 uint8 [n_heads][128] (best 4-window)."""
+    x = _u16(x)
+    n_tok, n_heads, d = x.shape
+    assert d == D
+    b2 = np.zeros((n_heads, D), np.uint8)
+    lib().gaac_ref_nested_calibrate(_ptr(x), n_tok, n_heads * D, n_heads, _ptr(b2))
+    return b2
+
+
+def nested_encode_tile(tile, kind: int, base2, base3, base4):
+    """[64][128] BF16 tile -> (image uint8 [nested_slot_bytes()], esc_len, code_bits); esc_len -1 when
+    the escape stream exceeds 496 bytes."""
+    tile = _u16(tile).reshape(BLOCK, D)
+    b2, b3, b4 = (_u8(b).reshape(D) for b in (base2, base3, base4))
+    img = np.zeros(nested_slot_bytes(), np.uint8)
+    bits = ctypes.c_int(0)
+    esc = lib().gaac_ref_nested_encode_tile(_ptr(tile), kind, _ptr(b2), _ptr(b3), _ptr(b4), _ptr(img),
+                                            ctypes.addressof(bits))
+    return img, esc, bits.value
+
+
+def nested_decode_tile(img, kind: int, base2, base3, base4):
+    img = _u8(img)
+    b2, b3, b4 = (_u8(b).reshape(D) for b in (base2, base3, base4))
+    out = np.zeros((BLOCK, D), np.uint16)
+    st = lib().gaac_ref_nested_decode_tile(_ptr(img), kind, _ptr(b2), _ptr(b3), _ptr(b4), _ptr(out))
+    return out, st

@@ -615,3 +615,168 @@ void gaac_ref_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         int Hq, int Hkv, double scale, double* out, int32_t* flags, double* logits_scratch) {
     gaac_ref_attention_d(q, k, v, tok_stride, T, Hq, Hkv, ORC_D, scale, out, flags, logits_scratch);
 }
+
+/* ==== Nested 2-bit mode: the ablation format of section 4.7.2 (Table 4) ====
+ *
+ * The page measures a fourth, 2-bit mode nested inside the 3-bit one: a group
+ * whose offsets from a per-channel base2 all fit [0,3] keeps 2 code bits per
+ * element.  The saving only exists if the code width varies per group, so this
+ * ablation format (not used by the cache) replaces format v3's fixed 3-bit
+ * code planes with a code stream:
+ *   [0,8192)       sign|mantissa plane, as format v3
+ *   [8192,11264)   code stream: groups in group order; a 2-bit group takes 16
+ *                  bits, a 3-bit or 4-bit group 24 (the 4-bit group's low
+ *                  three offset bits), a raw group none; element j of a group
+ *                  at bit (group start + j * width); bit b of the stream is bit
+ *                  b % 8 of byte b / 8; zero past its end
+ *   [11264,11520)  tags, 2 bits per group: 0 3-bit, 1 4-bit, 2 raw, 3 2-bit
+ *   [11520,11552)  directory: 8 u32, entry w = 4-bit groups | raw groups << 9
+ *                  | code-stream bits << 16, each over groups [0, 128(w+1))
+ *   [11552,12048)  escape area, capacity 496: one byte per 4-bit group, then
+ *                  eight exponent bytes per raw group, each in group order
+ * The mode rule tries the windows from the narrowest: 2-bit if every offset
+ * from base2 is in [0,3], else 3-bit, else 4-bit, else raw.
+ */
+#define NST_OFF_CODE 8192
+#define NST_OFF_TAG 11264
+#define NST_OFF_DIR 11520
+#define NST_OFF_ESC 11552
+#define NST_SLOT (NST_OFF_ESC + ORC_ESC_CAP)
+enum { NST_M2BIT = 3 };
+
+int gaac_ref_nested_slot_bytes(void) { return NST_SLOT; }
+
+/* base2 of every (head, channel): the 4-exponent window holding the most
+ * calibration values (ties to the smallest base), as base3 and base4. */
+void gaac_ref_nested_calibrate(const uint16_t* x, int64_t n_tok, int64_t tok_stride, int n_heads, uint8_t* base2) {
+    for (int h = 0; h < n_heads; ++h) {
+        for (int c = 0; c < ORC_D; ++c) {
+            uint64_t hist[256];
+            memset(hist, 0, sizeof hist);
+            for (int64_t t = 0; t < n_tok; ++t) hist[bf16_exponent(x[t * tok_stride + h * ORC_D + c])] += 1;
+            base2[h * ORC_D + c] = (uint8_t)best_window(hist, 4);
+        }
+    }
+}
+
+static int nested_width(unsigned mode) { return mode == NST_M2BIT ? 2 : (mode == ORC_MRAW ? 0 : 3); }
+
+static void put_bits(uint8_t* img, int bit, unsigned v, int n) {
+    for (int i = 0; i < n; ++i)
+        if ((v >> i) & 1u) img[NST_OFF_CODE + (bit + i) / 8] |= (uint8_t)(1u << ((bit + i) % 8));
+}
+static unsigned get_bits(const uint8_t* img, int bit, int n) {
+    unsigned v = 0;
+    for (int i = 0; i < n; ++i) v |= ((img[NST_OFF_CODE + (bit + i) / 8] >> ((bit + i) % 8)) & 1u) << i;
+    return v;
+}
+
+/* Encode one full tile ([64][128], logical order).  Returns the escape length,
+ * or -1 if the escape stream exceeds 496 bytes; *code_bits receives the length
+ * of the code stream in bits.  img must hold NST_SLOT bytes. */
+int gaac_ref_nested_encode_tile(const uint16_t* tile, int kind, const uint8_t* base2, const uint8_t* base3,
+                                const uint8_t* base4, uint8_t* img, int* code_bits) {
+    memset(img, 0, NST_SLOT);
+    uint16_t seq[ORC_TILE];
+    for (int t = 0; t < ORC_BLOCK; ++t)
+        for (int c = 0; c < ORC_D; ++c) seq[gaac_ref_storage_index(kind, t, c)] = tile[t * ORC_D + c];
+    for (int s = 0; s < ORC_TILE; ++s)
+        img[s] = (uint8_t)((bf16_signmant(seq[s]) & 0x7Fu) | (bf16_signmant(seq[sign_source(s)]) & 0x80u));
+    unsigned modes[ORC_GROUPS];
+    int n4 = 0, nraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned e[8], b3[8], b4[8];
+        int fits2 = 1;
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j, c = channel_of(kind, s);
+            e[j] = bf16_exponent(seq[s]);
+            b3[j] = base3[c];
+            b4[j] = base4[c];
+            int o2 = (int)e[j] - (int)base2[c];
+            if (o2 < 0 || o2 > 3) fits2 = 0;
+        }
+        modes[G] = fits2 ? NST_M2BIT : choose_mode(e, b3, b4, NULL);
+        if (modes[G] == ORC_M4BIT) n4 += 1;
+        if (modes[G] == ORC_MRAW) nraw += 1;
+    }
+    int esc = n4 + 8 * nraw;
+    if (esc > ORC_ESC_CAP) return -1;
+    int bit = 0, at4 = 0, atraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = modes[G];
+        int w = nested_width(mode);
+        img[NST_OFF_TAG + G / 4] |= (uint8_t)(mode << (2 * (G % 4)));
+        uint8_t esc4 = 0;
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j, c = channel_of(kind, s);
+            unsigned e = bf16_exponent(seq[s]);
+            if (mode == NST_M2BIT) {
+                put_bits(img, bit + 2 * j, e - base2[c], 2);
+            } else if (mode == ORC_M3BIT) {
+                put_bits(img, bit + 3 * j, e - base3[c], 3);
+            } else if (mode == ORC_M4BIT) {
+                unsigned off = (e - base4[c]) & 0xFFu;
+                put_bits(img, bit + 3 * j, off & 7u, 3);
+                esc4 |= (uint8_t)(((off >> 3) & 1u) << j);
+            } else {
+                img[NST_OFF_ESC + n4 + 8 * atraw + j] = (uint8_t)e;
+            }
+        }
+        bit += 8 * w;
+        if (mode == ORC_M4BIT) img[NST_OFF_ESC + at4++] = esc4;
+        if (mode == ORC_MRAW) atraw += 1;
+        if ((G + 1) % ORC_DIR_GROUPS == 0) {
+            uint32_t entry = ((uint32_t)at4 & 0x1FFu) | (((uint32_t)atraw & 0x7Fu) << 9) | ((uint32_t)bit << 16);
+            memcpy(img + NST_OFF_DIR + 4 * (G / ORC_DIR_GROUPS), &entry, 4);  /* little-endian host assumed */
+        }
+    }
+    if (code_bits) *code_bits = bit;
+    return esc;
+}
+
+/* Decode a nested-format image into the logical tile.  Returns the escape
+ * length, -2 if the escape stream exceeds 496 bytes, or -3 if a directory
+ * entry differs from the counts of the groups it covers. */
+int gaac_ref_nested_decode_tile(const uint8_t* img, int kind, const uint8_t* base2, const uint8_t* base3,
+                                const uint8_t* base4, uint16_t* tile) {
+    int n4 = 0, nraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = (img[NST_OFF_TAG + G / 4] >> (2 * (G % 4))) & 3u;
+        if (mode == ORC_M4BIT) n4 += 1;
+        if (mode == ORC_MRAW) nraw += 1;
+    }
+    int esc = n4 + 8 * nraw;
+    if (esc > ORC_ESC_CAP) return -2;
+    int bit = 0, at4 = 0, atraw = 0;
+    for (int G = 0; G < ORC_GROUPS; ++G) {
+        unsigned mode = (img[NST_OFF_TAG + G / 4] >> (2 * (G % 4))) & 3u;
+        int w = nested_width(mode);
+        for (int j = 0; j < 8; ++j) {
+            int s = 8 * G + j, c = channel_of(kind, s);
+            unsigned e;
+            if (mode == NST_M2BIT) {
+                e = base2[c] + get_bits(img, bit + 2 * j, 2);
+            } else if (mode == ORC_M3BIT) {
+                e = base3[c] + get_bits(img, bit + 3 * j, 3);
+            } else if (mode == ORC_M4BIT) {
+                e = base4[c] + (get_bits(img, bit + 3 * j, 3) | (((img[NST_OFF_ESC + at4] >> j) & 1u) << 3));
+            } else {
+                e = img[NST_OFF_ESC + n4 + 8 * atraw + j];
+            }
+            int t, cc;
+            storage_to_tc(kind, s, &t, &cc);
+            unsigned sm = (img[s] & 0x7Fu) | (img[sign_holder(s)] & 0x80u);
+            tile[t * ORC_D + cc] = bf16_join(sm, e & 0xFFu);
+        }
+        bit += 8 * w;
+        if (mode == ORC_M4BIT) at4 += 1;
+        if (mode == ORC_MRAW) atraw += 1;
+        if ((G + 1) % ORC_DIR_GROUPS == 0) {
+            uint32_t entry;
+            memcpy(&entry, img + NST_OFF_DIR + 4 * (G / ORC_DIR_GROUPS), 4);
+            if (entry != (((uint32_t)at4 & 0x1FFu) | (((uint32_t)atraw & 0x7Fu) << 9) | ((uint32_t)bit << 16)))
+                return -3;
+        }
+    }
+    return esc;
+}
