@@ -233,6 +233,64 @@ def fp8_codec(k, v, n_calib: int) -> dict:
     return out
 
 
+def mode_ablation(k, v, n_calib: int) -> dict:
+    """The GAAC page's nested 2-bit-mode ablation on one layer's tiles: format v3 and the nested format
+    (a 2-bit mode and a variable-width code stream) encode the same K and V tiles; payload ratio of
+    each (BF16 bytes / bytes a read of the tile needs) and the decode time of each tile-batch decoder
+    (same launch shape: one CTA per tile, one thread per 32-element unit), round trips checked."""
+    import torch
+
+    import lossless_compressed_kv_gaac_gb300 as G
+
+    T, H = k.shape[1], k.shape[2]
+    nb = T // 64
+    tiles = torch.cat([x[0, : nb * 64].view(nb, 64, H, 128).permute(2, 0, 1, 3).reshape(-1, 64, 128)
+                       for x in (k, v)]).contiguous()
+    n = tiles.shape[0]
+    dev = k.device
+    kinds = torch.cat([torch.zeros(H * nb), torch.ones(H * nb)]).to(torch.uint8).to(dev)
+    rows = torch.cat([torch.arange(H).repeat_interleave(nb), H + torch.arange(H).repeat_interleave(nb)]).int().to(dev)
+    b2, b3, b4 = (torch.zeros((2 * H, 128), dtype=torch.uint8, device=dev) for _ in range(3))
+    for x, lo in ((k, 0), (v, H)):
+        G.calibrate(x[0, :n_calib], b3[lo:lo + H], b4[lo:lo + H])
+        G.nested_calibrate(x[0, :n_calib], b2[lo:lo + H])
+    s3 = torch.empty((n, G.SLOT_BYTES), dtype=torch.uint8, device=dev)
+    sn = torch.empty((n, G.NESTED_SLOT_BYTES), dtype=torch.uint8, device=dev)
+    e3 = torch.empty(n, dtype=torch.int16, device=dev)
+    en = torch.empty(n, dtype=torch.int16, device=dev)
+    G.encode_tiles(tiles, kinds, rows, b3, b4, s3, e3)
+    G.nested_encode_tiles(tiles, kinds, rows, b2, b3, b4, sn, en)
+    back = torch.empty_like(tiles)
+    t3, tn = [], []
+    for i in range(5):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record()
+        G.decode_tiles(s3, e3, kinds, rows, b3, b4, back)
+        ev[1].record()
+        G.nested_decode_tiles(sn, en, kinds, rows, b2, b3, b4, back)
+        ev[2].record()
+        ev[2].synchronize()
+        if i:
+            t3.append(ev[0].elapsed_time(ev[1]))
+            tn.append(ev[1].elapsed_time(ev[2]))
+    assert torch.equal(back.view(torch.int16), tiles.view(torch.int16))
+    G.decode_tiles(s3, e3, kinds, rows, b3, b4, back)
+    torch.cuda.synchronize()
+    assert torch.equal(back.view(torch.int16), tiles.view(torch.int16))
+    e3l, enl = e3.long() & 0xFFFF, en.long() & 0xFFFF
+    assert bool((e3l != 0xFFFF).all()) and bool((enl != 0xFFFF).all()), "a tile overflowed its escape area"
+    d7 = sn[:, 11548:11552].long()
+    bits = (d7[:, 0] | (d7[:, 1] << 8) | (d7[:, 2] << 16) | (d7[:, 3] << 24)) >> 16
+    pay3 = int((11536 + e3l).sum().item())
+    payn = int((8192 + (bits + 7) // 8 + 256 + 32 + enl).sum().item())
+    raw = n * 16384
+    d3, dn = min(t3), min(tn)
+    return {"tiles": n, "payload_ratio_v3": round(raw / pay3, 4), "payload_ratio_nested": round(raw / payn, 4),
+            "ratio_gain_pct": round(100 * (pay3 / payn - 1), 2),
+            "decode_us_v3": round(d3 * 1e3, 1), "decode_us_nested": round(dn * 1e3, 1),
+            "decode_time_ratio": round(dn / d3, 3)}
+
+
 def append_cost(k, v, n_calib: int) -> dict:
     """Device time of one decode-token append (all kv-heads, K and V, one layer, batch 1) with the
     open block as a BF16 raw tail and with it kept compressed in its slot.  64 consecutive appends (a
@@ -321,6 +379,7 @@ def run_gaac(args):
     st = G.stats_dict(c0.stats)
     fp8 = fp8_codec(k0, v0, wl.n_calib)
     app = append_cost(k0, v0, wl.n_calib)
+    abl = mode_ablation(k0, v0, wl.n_calib)
     del k0, v0, kd, vd
     alg = [algorithmic_bytes(c) for c in caches]
     alg_step = sum(alg)
@@ -465,6 +524,7 @@ def run_gaac(args):
         "decompress_gbs": round(decompress_gbs, 1),
         "fp8": fp8,
         "append": app,
+        "mode_ablation": abl,
         "ratio": {"payload": round(payload_ratio, 4), "resident": round(resident_ratio, 4),
                   "mode_shares": [round(st[f"groups{m}"] / max(1, 1024 * st["slot_tiles"]), 5) for m in range(3)]},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",

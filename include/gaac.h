@@ -369,6 +369,58 @@ GAAC_API int gaac_fp8_decompress_tiles(const uint8_t* slots, const uint16_t* esc
                                        const uint8_t* base3, const uint8_t* base4, uint8_t* tiles, int32_t* d_status,
                                        void* stream);
 
+/*
+ * Tile-batch codec, format v3 (the block encoder and decoder of the cache,
+ * without the table): tiles[i][64][128] BF16 token-major, tile_kind[i] 0 = K,
+ * 1 = V, tile_row[i] < n_rows selects the 128 bases base3/base4[row*128..].
+ * gaac_encode_tiles writes slot image i at slots + i*GAAC_SLOT_BYTES and
+ * esc_len[i], or esc_len[i] = 0xFFFF (slot untouched) when the escape stream
+ * exceeds GAAC_ESC_CAPACITY; gaac_decode_tiles rebuilds tiles[i] from every
+ * slot whose esc_len is not 0xFFFF.  tiles and slots 16-byte aligned, bases
+ * 4-byte aligned.  A bad kind or row: GAAC_EINVAL in *d_status (esc_len 0xFFFF
+ * on encode); a slot failing the format checks: GAAC_EFORMAT.
+ */
+GAAC_API int gaac_encode_tiles(const uint16_t* tiles, int64_t n_tiles, const uint8_t* tile_kind,
+                               const int32_t* tile_row, int n_rows, const uint8_t* base3, const uint8_t* base4,
+                               uint8_t* slots, uint16_t* esc_len, gaac_stats* stats, int32_t* d_status, void* stream);
+GAAC_API int gaac_decode_tiles(const uint8_t* slots, const uint16_t* esc_len, int64_t n_tiles,
+                               const uint8_t* tile_kind, const int32_t* tile_row, int n_rows, const uint8_t* base3,
+                               const uint8_t* base4, uint16_t* tiles, int32_t* d_status, void* stream);
+
+/*
+ * Nested 2-bit-mode ablation format (section 4.7.2, Table 4: a 2-bit mode
+ * nested inside the 3-bit one).  Not used by the cache; it measures the
+ * ratio / decode-time trade of a variable code width.  Slot image of
+ * GAAC_NESTED_SLOT_BYTES:
+ *   [0,8192)      sign|mantissa plane, as format v3
+ *   [8192,11264)  code stream: groups in group order; a 2-bit group takes 16
+ *                 bits, a 3-bit or 4-bit group 24 (the 4-bit group's low three
+ *                 offset bits), a raw group none; element j of a group at bit
+ *                 (group start + j*width); bit b of the stream is bit b%8 of
+ *                 byte b/8; zero past its end
+ *   [11264,11520) tags, 2 bits per group: 0 3-bit, 1 4-bit, 2 raw, 3 2-bit
+ *   [11520,11552) directory: 8 u32, entry w = 4-bit groups (mod 512) | raw
+ *                 groups (mod 128) << 9 | code-stream bits << 16, each over
+ *                 groups [0, 128(w+1))
+ *   [11552,12048) escape area as format v3 (4-bit bytes, then raw exponents)
+ * Mode rule: 2-bit if every offset from base2 is in [0,3], else format v3's.
+ * gaac_nested_calibrate: base2[h*128+c] = the 4-exponent window holding the
+ * most values of x[t*tok_stride + h*128 + c], t < n_tok, ties to the smallest
+ * base.  The encode and decode calls follow gaac_encode_tiles and
+ * gaac_decode_tiles (bases base2/base3/base4 [n_rows][128]).
+ */
+#define GAAC_NESTED_SLOT_BYTES 12048
+GAAC_API int gaac_nested_calibrate(const uint16_t* x, int64_t n_tok, int64_t tok_stride, int n_kv_heads,
+                                   uint8_t* base2, int32_t* d_status, void* stream);
+GAAC_API int gaac_nested_encode_tiles(const uint16_t* tiles, int64_t n_tiles, const uint8_t* tile_kind,
+                                      const int32_t* tile_row, int n_rows, const uint8_t* base2, const uint8_t* base3,
+                                      const uint8_t* base4, uint8_t* slots, uint16_t* esc_len, int32_t* d_status,
+                                      void* stream);
+GAAC_API int gaac_nested_decode_tiles(const uint8_t* slots, const uint16_t* esc_len, int64_t n_tiles,
+                                      const uint8_t* tile_kind, const int32_t* tile_row, int n_rows,
+                                      const uint8_t* base2, const uint8_t* base3, const uint8_t* base4,
+                                      uint16_t* tiles, int32_t* d_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

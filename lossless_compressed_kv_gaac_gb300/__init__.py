@@ -96,6 +96,16 @@ def lib() -> ctypes.CDLL:
                                                         P, P]
             L.gaac_decode_attention_noalloc.restype = i32
             L.gaac_decompress.restype = i32
+            L.gaac_encode_tiles.argtypes = [P, i64, P, P, i32, P, P, P, P, P, P, P]
+            L.gaac_encode_tiles.restype = i32
+            L.gaac_decode_tiles.argtypes = [P, P, i64, P, P, i32, P, P, P, P, P]
+            L.gaac_decode_tiles.restype = i32
+            L.gaac_nested_calibrate.argtypes = [P, i64, i64, i32, P, P, P]
+            L.gaac_nested_calibrate.restype = i32
+            L.gaac_nested_encode_tiles.argtypes = [P, i64, P, P, i32, P, P, P, P, P, P, P]
+            L.gaac_nested_encode_tiles.restype = i32
+            L.gaac_nested_decode_tiles.argtypes = [P, P, i64, P, P, i32, P, P, P, P, P, P]
+            L.gaac_nested_decode_tiles.restype = i32
             L.gaac_fp8_slot_bytes.argtypes = [i32]
             L.gaac_fp8_slot_bytes.restype = i32
             L.gaac_fp8_calibrate.argtypes = [P, i64, i64, i32, i32, P, P, P, P]
@@ -310,6 +320,52 @@ def fp8_decompress_tiles(slots, esc_len, fmt: int, tile_kind, tile_row, base3, b
     _check("gaac_fp8_decompress_tiles", lib().gaac_fp8_decompress_tiles(
         slots.data_ptr(), esc_len.data_ptr(), n, fmt, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
         base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status), _stream(stream)))
+
+
+def encode_tiles(tiles, tile_kind, tile_row, base3, base4, slots, esc_len, stats=None, status=None,
+                 stream=None) -> None:
+    """Format v3 tile batch.  tiles: BF16 [n, 64, 128] token-major; tile_kind: uint8 [n] (0 K, 1 V);
+    tile_row: int32 [n] (row of base3/base4 [rows, 128]); slots: uint8 [n, SLOT_BYTES]; esc_len: int16 [n]
+    (0xFFFF: does not fit, slot untouched)."""
+    _check("gaac_encode_tiles", lib().gaac_encode_tiles(
+        tiles.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
+        base3.data_ptr(), base4.data_ptr(), slots.data_ptr(), esc_len.data_ptr(), _ptr(stats), _ptr(status),
+        _stream(stream)))
+
+
+def decode_tiles(slots, esc_len, tile_kind, tile_row, base3, base4, tiles, status=None, stream=None) -> None:
+    _check("gaac_decode_tiles", lib().gaac_decode_tiles(
+        slots.data_ptr(), esc_len.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(),
+        base3.shape[0], base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status), _stream(stream)))
+
+
+NESTED_SLOT_BYTES = 12048
+
+
+def nested_calibrate(x: torch.Tensor, base2: torch.Tensor, status=None, stream=None) -> None:
+    """x: BF16 [n_tok, kv_heads, 128] -> base2 uint8 [kv_heads, 128] (best 4-exponent window)."""
+    _cuda(x, "x")
+    if x.dim() != 3 or x.shape[-1] != HEAD_DIM or x.stride(2) != 1 or x.stride(1) != HEAD_DIM:
+        raise ValueError("x must be [n_tok, kv_heads, 128] with contiguous heads and channels")
+    _check("gaac_nested_calibrate", lib().gaac_nested_calibrate(x.data_ptr(), x.shape[0], x.stride(0), x.shape[1],
+                                                                 base2.data_ptr(), _ptr(status), _stream(stream)))
+
+
+def nested_encode_tiles(tiles, tile_kind, tile_row, base2, base3, base4, slots, esc_len, status=None,
+                        stream=None) -> None:
+    """Nested 2-bit-mode ablation format; arguments as encode_tiles, slots [n, NESTED_SLOT_BYTES]."""
+    _check("gaac_nested_encode_tiles", lib().gaac_nested_encode_tiles(
+        tiles.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
+        base2.data_ptr(), base3.data_ptr(), base4.data_ptr(), slots.data_ptr(), esc_len.data_ptr(), _ptr(status),
+        _stream(stream)))
+
+
+def nested_decode_tiles(slots, esc_len, tile_kind, tile_row, base2, base3, base4, tiles, status=None,
+                        stream=None) -> None:
+    _check("gaac_nested_decode_tiles", lib().gaac_nested_decode_tiles(
+        slots.data_ptr(), esc_len.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(),
+        base3.shape[0], base2.data_ptr(), base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status),
+        _stream(stream)))
 
 
 def decode_attention_hd256(q, seq_lens, table, pools: Pools, base3, base4, scale: float, out, workspace,

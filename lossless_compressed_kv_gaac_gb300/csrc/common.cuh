@@ -135,6 +135,69 @@ __device__ __forceinline__ void join_bf16x4(uint32_t sm, uint32_t e, uint32_t& p
   p23 = __byte_perm(lo, hi, 0x7362);
 }
 
+// Stages tokens [0, nv) of a tile (token t's 128 channels at src + t *
+// tok_stride, 16-byte aligned) into `tile` in storage order; tokens past nv
+// are zero.  Thread tid of 256 moves a quarter of token tid / 4.
+__device__ __forceinline__ void stage_tile(uint16_t* tile, const uint16_t* src, int64_t tok_stride, int nv, int kind,
+                                           int tid) {
+  const int t = tid >> 2, part = tid & 3;
+  uint4 w[4];
+  if (t < nv) {
+    const uint4* p = reinterpret_cast<const uint4*>(src + t * tok_stride + 32 * part);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = p[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (kind == 0) {
+    uint4* d = reinterpret_cast<uint4*>(tile + t * kD + 32 * part);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = w[i];
+  } else {
+    const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c = 32 * part + 2 * i;
+      tile[v_storage_index(t, c)] = static_cast<uint16_t>(ws[i] & 0xFFFFu);
+      tile[v_storage_index(t, c + 1)] = static_cast<uint16_t>(ws[i] >> 16);
+    }
+  }
+}
+
+// Unit u's rebuilt values (pairs[m] = bf16x2 of storage elements 32u + 2m, +1)
+// into a token-major [64][128] tile in shared memory.
+__device__ __forceinline__ void unit_to_logical(uint16_t* logical, int kind, int u, const uint32_t pairs[16]) {
+  if (kind == 0) {
+    uint4* d = reinterpret_cast<uint4*>(logical + 32 * u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(pairs[4 * i], pairs[4 * i + 1], pairs[4 * i + 2], pairs[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const int s0 = 32 * u + 2 * m;
+      logical[v_token_of(s0) * kD + v_channel_of(s0)] = static_cast<uint16_t>(pairs[m] & 0xFFFFu);
+      logical[v_token_of(s0 + 1) * kD + v_channel_of(s0 + 1)] = static_cast<uint16_t>(pairs[m] >> 16);
+    }
+  }
+}
+
+// Base bytes of unit u's 32 elements, four per word (word k = elements
+// 4k..4k+3 of the unit), from a row of 128 per-channel bases.
+__device__ __forceinline__ void unit_base_words(int kind, int u, const uint8_t* bg, uint32_t out[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (kind == 0) {  // K: element 4k+L of unit u is channel 32(u%4) + 4k + L
+      out[k] = *reinterpret_cast<const uint32_t*>(bg + 32 * (u & 3) + 4 * k);
+    } else {
+      uint32_t w = 0u;
+#pragma unroll
+      for (int L = 0; L < 4; ++L) w |= static_cast<uint32_t>(bg[v_channel_of(32 * u + 4 * k + L)]) << (8 * L);
+      out[k] = w;
+    }
+  }
+}
+
 // Exclusive prefixes of the 4-bit and raw group counts (packed n4 | nraw << 16)
 // over the 64 tag words of a slot image, into word_prefix[0..63], and the tile
 // totals into word_prefix[64].  Threads 0..31 of the CTA call it (one warp).

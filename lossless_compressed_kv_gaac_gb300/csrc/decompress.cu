@@ -72,19 +72,7 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
                                       a.base4 + (kind * a.n_kv_heads + h) * kD, ent.esc_len, word_prefix, pairs);
     if (bad) report(a.status, GAAC_EFORMAT);
   }
-  // Storage order -> token-major.
-  if (kind == 0) {
-    uint4* d = reinterpret_cast<uint4*>(logical + 32 * u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_uint4(pairs[4 * i], pairs[4 * i + 1], pairs[4 * i + 2], pairs[4 * i + 3]);
-  } else {
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const int s0 = 32 * u + 2 * m;
-      logical[v_token_of(s0) * kD + v_channel_of(s0)] = static_cast<uint16_t>(pairs[m] & 0xFFFFu);
-      logical[v_token_of(s0 + 1) * kD + v_channel_of(s0 + 1)] = static_cast<uint16_t>(pairs[m] >> 16);
-    }
-  }
+  unit_to_logical(logical, kind, u, pairs);  // storage order -> token-major
   __syncthreads();
   uint16_t* dst = (kind == 0 ? a.k_out : a.v_out) + static_cast<int64_t>(b) * a.seq_stride +
                   static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD;
@@ -95,6 +83,46 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[i] = s[i];
   }
+}
+
+struct DecodeTilesArgs {
+  const uint8_t* slots;
+  const uint16_t* esc_len;
+  const uint8_t* kind;
+  const int32_t* row;
+  int n_rows;
+  const uint8_t* base3;
+  const uint8_t* base4;
+  uint16_t* tiles;
+  int32_t* status;
+};
+
+// grid (n_tiles): one CTA rebuilds one slot image of the batch into its
+// token-major tile (tiles whose esc_len is 0xFFFF are skipped).
+__global__ void __launch_bounds__(kDecThreads) decode_tiles_kernel(DecodeTilesArgs a) {
+  __shared__ alignas(16) uint16_t logical[kBlock * kD];
+  __shared__ int word_prefix[65];
+  const int64_t i = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int esc = a.esc_len[i];
+  if (esc == 0xFFFF) return;
+  const int kind = a.kind[i], r = a.row[i];
+  if (kind > 1 || r < 0 || r >= a.n_rows || esc > kEscCap) {
+    if (tid == 0) report(a.status, GAAC_EINVAL);
+    return;
+  }
+  const uint8_t* slot = a.slots + i * kSlot;
+  if (tid < 32) slot_word_prefix(slot, tid, word_prefix);
+  __syncthreads();
+  uint32_t pairs[16];
+  if (decode_slot_unit(slot, kind, tid, a.base3 + r * kD, a.base4 + r * kD, esc, word_prefix, pairs))
+    report(a.status, GAAC_EFORMAT);
+  unit_to_logical(logical, kind, tid, pairs);
+  __syncthreads();
+  const uint4* s = reinterpret_cast<const uint4*>(logical);
+  uint4* d = reinterpret_cast<uint4*>(a.tiles + i * kTile);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) d[tid + kDecThreads * k] = s[tid + kDecThreads * k];
 }
 
 }  // namespace gaac
@@ -122,5 +150,21 @@ extern "C" int gaac_decompress(const gaac_entry* table, const int32_t* seq_lens,
   DecompressArgs a{table, seq_lens, n_kv_heads, max_blocks, slot_pool, pools->n_slots, raw_pool, pools->n_raw,
                    base3, base4, k_out, v_out, seq_stride, tok_stride, n_tok, d_status};
   decompress_kernel<<<dim3(2 * n_kv_heads, max_blocks, batch), kDecThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
+
+extern "C" int gaac_decode_tiles(const uint8_t* slots, const uint16_t* esc_len, int64_t n_tiles,
+                                 const uint8_t* tile_kind, const int32_t* tile_row, int n_rows, const uint8_t* base3,
+                                 const uint8_t* base4, uint16_t* tiles, int32_t* d_status, void* stream) {
+  if (slots == nullptr || esc_len == nullptr || tile_kind == nullptr || tile_row == nullptr || base3 == nullptr ||
+      base4 == nullptr || tiles == nullptr || n_rows <= 0)
+    return GAAC_EINVAL;
+  if (n_tiles < 0 || n_tiles > 0x7FFFFFFF || (reinterpret_cast<uintptr_t>(tiles) & 15u) ||
+      (reinterpret_cast<uintptr_t>(slots) & 15u) || (reinterpret_cast<uintptr_t>(base3) & 3u) ||
+      (reinterpret_cast<uintptr_t>(base4) & 3u))
+    return GAAC_EINVAL;
+  if (n_tiles == 0) return GAAC_OK;
+  DecodeTilesArgs a{slots, esc_len, tile_kind, tile_row, n_rows, base3, base4, tiles, d_status};
+  decode_tiles_kernel<<<static_cast<unsigned>(n_tiles), kDecThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }

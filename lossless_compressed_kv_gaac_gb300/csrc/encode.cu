@@ -284,33 +284,9 @@ __global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a
   }
   const int nv = min(kBlock, len - blk * kBlock);
   // Stage the tile in storage order; tokens past the sequence are zero.
-  {
-    const uint16_t* src = (kind == 0 ? a.k : a.v) + static_cast<int64_t>(b) * a.seq_stride +
-                          static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD;
-    const int t = tid >> 2, part = tid & 3;
-    uint4 w[4];
-    if (t < nv) {
-      const uint4* p = reinterpret_cast<const uint4*>(src + t * a.tok_stride + 32 * part);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = p[i];
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = make_uint4(0, 0, 0, 0);
-    }
-    if (kind == 0) {
-      uint4* d = reinterpret_cast<uint4*>(sh.tile + t * kD + 32 * part);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) d[i] = w[i];
-    } else {
-      const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int c = 32 * part + 2 * i;
-        sh.tile[v_storage_index(t, c)] = static_cast<uint16_t>(ws[i] & 0xFFFFu);
-        sh.tile[v_storage_index(t, c + 1)] = static_cast<uint16_t>(ws[i] >> 16);
-      }
-    }
-  }
+  stage_tile(sh.tile, (kind == 0 ? a.k : a.v) + static_cast<int64_t>(b) * a.seq_stride +
+                          static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD,
+             a.tok_stride, nv, kind, tid);
   __syncthreads();
   const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
   const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
@@ -536,6 +512,38 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   }
 }
 
+struct EncodeTilesArgs {
+  const uint16_t* tiles;  // [n][64][128] BF16, token-major
+  const uint8_t* kind;
+  const int32_t* row;
+  int n_rows;
+  const uint8_t* base3;
+  const uint8_t* base4;
+  uint8_t* slots;
+  uint16_t* esc_len;
+  gaac_stats* stats;
+  int32_t* status;
+};
+
+// grid (n_tiles): one CTA encodes one tile of the batch.
+__global__ void __launch_bounds__(kEncThreads) encode_tiles_kernel(EncodeTilesArgs a) {
+  __shared__ EncShared sh;
+  const int64_t i = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int kind = a.kind[i], r = a.row[i];
+  if (kind > 1 || r < 0 || r >= a.n_rows) {
+    if (tid == 0) {
+      a.esc_len[i] = 0xFFFFu;
+      report(a.status, GAAC_EINVAL);
+    }
+    return;
+  }
+  stage_tile(sh.tile, a.tiles + i * kTile, kD, kBlock, kind, tid);
+  __syncthreads();
+  const int esc = encode_tile_cta<false>(&sh, kind, a.base3 + r * kD, a.base4 + r * kD, a.slots + i * kSlot, a.stats);
+  if (tid == 0) a.esc_len[i] = esc >= 0 ? static_cast<uint16_t>(esc) : 0xFFFFu;
+}
+
 __global__ void bump_lens_kernel(int32_t* lens, int batch) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < batch) lens[i] += 1;
@@ -606,4 +614,21 @@ extern "C" int gaac_append(const uint16_t* k_new, const uint16_t* v_new, int32_t
                            gaac_stats* stats, int32_t* d_status, void* stream) {
   return gaac_append_ex(k_new, v_new, seq_lens, batch, n_kv_heads, max_blocks, base3, base4, table, slot_ids, pools,
                         stats, 0u, d_status, stream);
+}
+
+extern "C" int gaac_encode_tiles(const uint16_t* tiles, int64_t n_tiles, const uint8_t* tile_kind,
+                                 const int32_t* tile_row, int n_rows, const uint8_t* base3, const uint8_t* base4,
+                                 uint8_t* slots, uint16_t* esc_len, gaac_stats* stats, int32_t* d_status,
+                                 void* stream) {
+  if (tiles == nullptr || tile_kind == nullptr || tile_row == nullptr || base3 == nullptr || base4 == nullptr ||
+      slots == nullptr || esc_len == nullptr || n_rows <= 0)
+    return GAAC_EINVAL;
+  if (n_tiles < 0 || n_tiles > 0x7FFFFFFF || (reinterpret_cast<uintptr_t>(tiles) & 15u) ||
+      (reinterpret_cast<uintptr_t>(slots) & 15u) || (reinterpret_cast<uintptr_t>(base3) & 3u) ||
+      (reinterpret_cast<uintptr_t>(base4) & 3u))
+    return GAAC_EINVAL;
+  if (n_tiles == 0) return GAAC_OK;
+  EncodeTilesArgs a{tiles, tile_kind, tile_row, n_rows, base3, base4, slots, esc_len, stats, d_status};
+  encode_tiles_kernel<<<static_cast<unsigned>(n_tiles), kEncThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
