@@ -7,11 +7,13 @@
 // softmax.  Section 3.3: the block table says per block whether it is a slot
 // or a raw tile.
 //
-// GB300 design: one CTA of 416 threads per SM, grid (split, kv-head, sequence).
-//  * Warp 12 (producer): one lane streams each 64-token block's K and V tile
-//    images (only the bytes a slot uses) into a 6-stage shared-memory ring
-//    with 1-D bulk copies tracked by mbarriers.
-//  * Warps 0-11 form three groups of four; group gr takes blocks gr, gr+3, ...
+// GB300 design: one CTA of 384 threads per SM, grid (split, kv-head, sequence).
+//  * The CTA streams its split's 64-token blocks through a ring of shared-
+//    memory stages: each block's K and V tile images (only the bytes a slot
+//    uses) arrive by 1-D bulk copies tracked by an mbarrier per stage.  There
+//    is no copy warp: the last warp to finish reading a stage issues its
+//    refill with the next block for it.
+//  * Twelve warps form three groups of four; group gr takes blocks gr, gr+3, ...
 //    of the split, and warp w of a group takes tokens [16w, 16w+16) of each.
 //    Each warp keeps its own online-softmax state (m, l, acc) over its tokens;
 //    the twelve states are merged with a log-sum-exp when the split ends.
@@ -55,7 +57,7 @@ constexpr int kGroups = 3;                        // warp groups, alternate bloc
 constexpr int kCWarps = kGroupWarps * kGroups;    // compute warps
 constexpr int kAttThreads = kCWarps * 32;
 // Staging ring depth: 6 stages of K+V images for 128-channel heads, 4 of K0+K1+V for 256-channel heads
-// (two half-heads); both a multiple of... any depth works, the stage of block j is j % depth.
+// (two half-heads).  Block j of a split uses stage j % depth.
 template <int NH>
 constexpr int stages_of() { return NH == 1 ? 6 : 4; }
 constexpr int kCtasPerSm = 1;
