@@ -80,7 +80,7 @@ struct AttSmem {
   alignas(16) uint8_t kbases[NH][2][kD];  // K: [half][base3|base4][channel]
   StageMeta smeta[kStages];
   alignas(16) uint4 qf[NH][8][32];       // q A-operand quads [half][k-step][lane]: (qa0, 0, qa2, 0)
-  alignas(16) uint4 vbw[2][2][32];        // V base words [unit][base3 | base4 - base3][lane], groups 0-3
+  alignas(16) uint4 vbw[2][2][32];        // V base words [unit][base3 | base4][lane], groups 0-3
   unsigned int stDone[kStages];           // warps of the group done reading the stage's current block
   float wm[kCWarps][kRPad];       // per warp and head: running maximum (end of split)
   float wl[kCWarps][kRPad];       // per warp and head: denominator (end of split)
@@ -189,11 +189,11 @@ __device__ __forceinline__ uint32_t escape_window(const uint8_t* img, int off) {
 
 // Rebuilds 32-element unit u of a slot image into 16 bf16x2 words: word 2m+i
 // holds elements 4m + {0,2} (i=0) / {1,3} (i=1).  x: the unit's gathered 4-bit
-// escape bytes (byte j = group j); b3/d43: the unit's base3 words and base4 -
+// escape bytes (byte j = group j); b3/b4: the unit's base3 and base4 words
 // base3 (32-bit, modular: e stays exact), word 2i and 2i+1 covering group i.
 // Raw groups come out wrong and are re-joined by fix_raw.
 __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t tb, uint32_t x, const uint32_t b3[8],
-                                            const uint32_t d43[8], const uint2* lut, uint32_t o[16]) {
+                                            const uint32_t b4[8], const uint2* lut, uint32_t o[16]) {
   const uint32_t* cw = reinterpret_cast<const uint32_t*>(img + kOffCode);
   const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
   const uint4 s0 = *reinterpret_cast<const uint4*>(img + 32 * u);
@@ -209,7 +209,7 @@ __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t 
     for (int q = 0; q < 4; ++q) {
       const uint32_t f = q < 2 ? fa : fb;
       const uint32_t sp = q == 0 ? sa.x : (q == 1 ? sa.y : (q == 2 ? sb.x : sb.y));
-      e[q] = (f ? b3[4 * hh + q] + d43[4 * hh + q] : b3[4 * hh + q]) + c[q] + sp;  // base4 = base3 + d43
+      e[q] = (f ? b4[4 * hh + q] : b3[4 * hh + q]) + c[q] + sp;
     }
     const uint4 sm = hh ? s1 : s0;
     join_v2(sm.x, e[0], o[8 * hh + 0], o[8 * hh + 1]);
@@ -257,7 +257,7 @@ __device__ __forceinline__ void raw_unit(const uint8_t* img, int u, uint32_t o[1
 template <class Smem>
 __device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, const uint8_t* img, int mode,
                                            int esc_len, int w, int lane, const uint32_t b3A[8],
-                                           const uint32_t d43A[8], const uint32_t b3B[8], const uint32_t d43B[8],
+                                           const uint32_t b4A[8], const uint32_t b3B[8], const uint32_t b4B[8],
                                            uint32_t oA[16], uint32_t oB[16], bool& badA, bool& badB) {
   const int uA = 64 * w + lane, uB = uA + 32;
   if (mode == GAAC_MODE_SLOT) {
@@ -274,8 +274,8 @@ __device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, co
     const int o4B = static_cast<int>((dA & 0x1FFu) + ((ex >> 8) & 0xFFu));
     const int orA = rawbase + 8 * static_cast<int>((d0 >> 9) + ((ex >> 16) & 0xFFu));
     const int orB = rawbase + 8 * static_cast<int>((dA >> 9) + (ex >> 24));
-    decode_unit(img, uA, tbA, __byte_perm(escape_window(img, o4A), 0u, teA & 0xFFFFu), b3A, d43A, sm.lut, oA);
-    decode_unit(img, uB, tbB, __byte_perm(escape_window(img, o4B), 0u, teB & 0xFFFFu), b3B, d43B, sm.lut, oB);
+    decode_unit(img, uA, tbA, __byte_perm(escape_window(img, o4A), 0u, teA & 0xFFFFu), b3A, b4A, sm.lut, oA);
+    decode_unit(img, uB, tbB, __byte_perm(escape_window(img, o4B), 0u, teB & 0xFFFFu), b3B, b4B, sm.lut, oB);
     if (teA >> 24) fix_raw(img, uA, tbA, orA, oA);  // raw groups: rare
     if (teB >> 24) fix_raw(img, uB, tbB, orB, oB);
     const bool totals = rawbase + 8 * static_cast<int>(d7 >> 9) != esc_len;
@@ -371,11 +371,11 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta(unsigned int* p, 
 // channels 16m+g, 16m+g+8 x heads 2tq, 2tq+1).
 // K unit base words of half-head `half`: channels 32tq..32tq+31, word i = channels 32tq + 4i..+3.
 template <int NH>
-__device__ __forceinline__ void k_bases(const AttSmem<NH>& sm, int half, int tq, uint32_t kb3[8], uint32_t kd43[8]) {
+__device__ __forceinline__ void k_bases(const AttSmem<NH>& sm, int half, int tq, uint32_t kb3[8], uint32_t kb4[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     kb3[i] = *reinterpret_cast<const uint32_t*>(&sm.kbases[half][0][32 * tq + 4 * i]);
-    kd43[i] = *reinterpret_cast<const uint32_t*>(&sm.kbases[half][1][32 * tq + 4 * i]) - kb3[i];
+    kb4[i] = *reinterpret_cast<const uint32_t*>(&sm.kbases[half][1][32 * tq + 4 * i]);
   }
 }
 
@@ -384,8 +384,8 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
                                              int n_my, int len, int gr, int w, int cw, int lane, float acc[8][4]) {
   constexpr int kStages = AttSmem<NH>::kStages;
   const int g = lane >> 2, tq = lane & 3;
-  uint32_t kb3[8], kd43[8];  // one half-head: loaded once (NH = 1) or per half and block (NH = 2)
-  if (NH == 1) k_bases(sm, 0, tq, kb3, kd43);
+  uint32_t kb3[8], kb4[8];  // one half-head: loaded once (NH = 1) or per half and block (NH = 2)
+  if (NH == 1) k_bases(sm, 0, tq, kb3, kb4);
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
   float mrun = -INFINITY, lsum = 0.f;  // head g
@@ -405,10 +405,10 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
     bool kbadA = false, kbadB = false;
 #pragma unroll 1
     for (int half = 0; half < NH; ++half) {
-      if (NH > 1) k_bases(sm, half, tq, kb3, kd43);
+      if (NH > 1) k_bases(sm, half, tq, kb3, kb4);
       uint32_t oA[16], oB[16];
       bool bA, bB;
-      tile_units(a, sm, sm.stage[st][half], meta.mode[half], meta.esc[half], w, lane, kb3, kd43, kb3, kd43, oA, oB,
+      tile_units(a, sm, sm.stage[st][half], meta.mode[half], meta.esc[half], w, lane, kb3, kb4, kb3, kb4, oA, oB,
                  bA, bB);
       kbadA = kbadA || bA;
       kbadB = kbadB || bB;
@@ -425,7 +425,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
     // ---- V units of the same tokens (independent of the scores: decoded while the MMAs above run)
     uint32_t oA[16], oB[16];
     bool vbadA, vbadB;
-    uint32_t vb3[2][8], vd43[2][8];  // word 2i and 2i+1 serve group i
+    uint32_t vb3[2][8], vb4[2][8];  // word 2i and 2i+1 serve group i
 #pragma unroll
     for (int hv = 0; hv < 2; ++hv) {
       const uint4 x3 = sm.vbw[hv][0][lane];
@@ -434,12 +434,12 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
       vb3[hv][2] = vb3[hv][3] = x3.y;
       vb3[hv][4] = vb3[hv][5] = x3.z;
       vb3[hv][6] = vb3[hv][7] = x3.w;
-      vd43[hv][0] = vd43[hv][1] = x4.x;
-      vd43[hv][2] = vd43[hv][3] = x4.y;
-      vd43[hv][4] = vd43[hv][5] = x4.z;
-      vd43[hv][6] = vd43[hv][7] = x4.w;
+      vb4[hv][0] = vb4[hv][1] = x4.x;
+      vb4[hv][2] = vb4[hv][3] = x4.y;
+      vb4[hv][4] = vb4[hv][5] = x4.z;
+      vb4[hv][6] = vb4[hv][7] = x4.w;
     }
-    tile_units(a, sm, sm.stage[st][NH], meta.mode[NH], meta.esc[NH], w, lane, vb3[0], vd43[0], vb3[1], vd43[1], oA,
+    tile_units(a, sm, sm.stage[st][NH], meta.mode[NH], meta.esc[NH], w, lane, vb3[0], vb4[0], vb3[1], vb4[1], oA,
                oB, vbadA, vbadB);
     // The stage is read: the group's last warp to get here refills it with block jn.
     __syncwarp();
@@ -647,7 +647,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     const uint32_t x3 = v3[cA] | (static_cast<uint32_t>(v3[cA + 8]) << 8);
     const uint32_t x4 = v4[cA] | (static_cast<uint32_t>(v4[cA + 8]) << 8);
     reinterpret_cast<uint32_t*>(&sm.vbw[hv][0][ln])[i] = x3 | (x3 << 16);
-    reinterpret_cast<uint32_t*>(&sm.vbw[hv][1][ln])[i] = (x4 | (x4 << 16)) - (x3 | (x3 << 16));
+    reinterpret_cast<uint32_t*>(&sm.vbw[hv][1][ln])[i] = x4 | (x4 << 16);
   }
   // q of the kv-head's query heads, times 2^-4, as A-operand quads of S^T = q K^T: for half `half`, lane
   // (g, tq) and k-step m, (channels 128 half + 32tq + 4m + {0, 2}, 0, ... + {1, 3}, 0) of head g (rows 8-15 zero)
