@@ -303,6 +303,46 @@ def mode_ablation(k, v, n_calib: int) -> dict:
             "decode_time_ratio": round(dn / d3, 3)}
 
 
+def hd256_attention(device, n_calib: int) -> dict:
+    """Decode attention over 256-channel heads (stored as two 128-channel half-heads): one layer of a
+    Qwen3-family shape with head_dim 256, 16 q / 4 kv heads, T = 65,536, batch 1, the same synthetic
+    value recipe; CUDA-event time per launch (10 launches after warm-up) and algorithmic GB/s."""
+    import torch
+
+    import gaac_workloads as W
+    import lossless_compressed_kv_gaac_gb300 as G
+    from lossless_compressed_kv_gaac_gb300.cache import LayerCache
+
+    T, Hkv, Hq = 65536, 4, 16
+    k, v = W.make_kv(CONFIG_ID, 0, 1, T, 2 * Hkv, device=device)  # 8 half-heads of 128 channels
+    c = LayerCache(1, 2 * Hkv, T // 64, device=device, n_raw=256)
+    c.calibrate(k[0, :n_calib], v[0, :n_calib])
+    c.encode(k, v, torch.tensor([T], dtype=torch.int32, device=device))
+    del k, v
+    g = torch.Generator(device=device)
+    g.manual_seed(256)
+    q = torch.randn(1, Hq, 256, generator=g, device=device).to(torch.bfloat16)
+    out = torch.empty((1, Hq, 256), dtype=torch.float32, device=device)
+    ws = torch.zeros(G.attention_workspace(1, 2 * Hkv, c.max_blocks), dtype=torch.uint8, device=device)
+
+    def launch():
+        G.decode_attention_hd256(q, c.seq_lens, c.table, c.pools, c.base3, c.base4, 1 / 16, out, ws, status=c.status)
+
+    for _ in range(3):
+        launch()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        launch()
+    e1.record()
+    e1.synchronize()
+    assert int(c.status.item()) == 0, "hd256 attention reported an error"
+    us = e0.elapsed_time(e1) * 1e3 / 10
+    alg = algorithmic_bytes(c)
+    return {"workload": "one layer, head_dim 256 (two 128-channel half-heads), 16 q / 4 kv heads, T=65536, batch 1",
+            "us_per_layer": round(us, 2), "algorithmic_bytes": alg, "compressed_gbs": round(alg / (us * 1e-6) / 1e9, 1)}
+
+
 def append_cost(k, v, n_calib: int) -> dict:
     """Device time of one decode-token append (all kv-heads, K and V, one layer, batch 1) with the
     open block as a BF16 raw tail and with it kept compressed in its slot.  64 consecutive appends (a
@@ -393,6 +433,7 @@ def run_gaac(args):
     app = append_cost(k0, v0, wl.n_calib)
     abl = mode_ablation(k0, v0, wl.n_calib)
     del k0, v0, kd, vd
+    hd256 = hd256_attention(device, wl.n_calib)
     alg = [algorithmic_bytes(c) for c in caches]
     alg_step = sum(alg)
     raw_step = raw_bytes_layer * L
@@ -537,6 +578,7 @@ def run_gaac(args):
         "fp8": fp8,
         "append": app,
         "mode_ablation": abl,
+        "hd256": hd256,
         "ratio": {"payload": round(payload_ratio, 4), "resident": round(resident_ratio, 4),
                   "mode_shares": [round(st[f"groups{m}"] / max(1, 1024 * st["slot_tiles"]), 5) for m in range(3)]},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",

@@ -328,6 +328,276 @@ __global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a
   }
 }
 
+// ------------------------------------------------ open block, one token --
+//
+// Adding token `pos` to an open slot changes only the groups that hold it:
+// the 16 groups of that token (K: an eighth of the tile holds 8 tokens), or
+// 64 groups of the V operand order, all inside the two eighths of the token's
+// 16-token quarter.  One thread per group of the affected eighths rebuilds its
+// group's present elements from the slot, adds the token's elements, and
+// re-encodes the group; groups that do not hold the token keep their mode and
+// move their escape bytes.  Earlier eighths keep their 4-bit escape bytes in
+// place and their raw bytes shift with the new number of 4-bit bytes; later
+// eighths hold no token yet (no escapes).  The result is the open image of
+// the first pos + 1 tokens, byte for byte.
+
+struct OpenShared {
+  uint8_t esc_old[kEscCap + 16];
+  uint8_t esc_new[kEscCap + 16];
+  uint16_t tok[kD];  // the new token's 128 values
+  int warp_old[kEncThreads / 32];
+  int warp_new[kEncThreads / 32];
+  int bad;
+};
+
+// Tokens of the 8 elements of group G (storage 8G..8G+7).
+__device__ __forceinline__ int group_token(int kind, int G, int j) { return token_of(kind, 8 * G + j); }
+
+// Base bytes of group G's 8 elements as two byte-lane words.
+__device__ __forceinline__ void group_bases(int kind, int G, const uint8_t* bg, uint32_t& w0, uint32_t& w1) {
+  if (kind == 0) {  // K: channels 8 (G % 16) .. + 7
+    const uint2 v = *reinterpret_cast<const uint2*>(bg + 8 * (G & 15));
+    w0 = v.x;
+    w1 = v.y;
+  } else {
+    w0 = w1 = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      w0 |= static_cast<uint32_t>(bg[v_channel_of(8 * G + j)]) << (8 * j);
+      w1 |= static_cast<uint32_t>(bg[v_channel_of(8 * G + 4 + j)]) << (8 * j);
+    }
+  }
+}
+
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int x = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += x;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kEncThreads / 32; ++w) {
+    const int x = warp_sums[w];
+    if (w < warp) before += x;
+    total += x;
+  }
+  return before + incl - v;
+}
+
+// Returns the new escape length (the slot updated), -1 if the escape stream
+// would outgrow the slot (nothing written), or -2 if the open image fails its
+// checks (nothing written).  All kEncThreads threads call it; os->tok holds
+// the token.  esc_old: the entry's escape length.
+__device__ int open_append_groups(OpenShared* os, uint8_t* slot, int kind, int pos, int esc_old,
+                                  const uint8_t* __restrict__ b3g, const uint8_t* __restrict__ b4g, gaac_stats* stats) {
+  const int tid = threadIdx.x;
+  const int nA = kind == 0 ? 128 : 256;                 // groups of the affected eighths
+  const int A0 = kind == 0 ? (pos >> 3) : 2 * (pos >> 4);  // first affected eighth
+  const int A1 = A0 + (kind == 0 ? 0 : 1);
+  const uint16_t* dir = reinterpret_cast<const uint16_t*>(slot + kOffDir);
+  const uint32_t d7 = dir[7], dprev = A0 ? dir[A0 - 1] : 0u;
+  const int n4_old = d7 & 0x1FF, nraw_old = d7 >> 9;
+  const int p4 = dprev & 0x1FF, praw = dprev >> 9;  // counts of the eighths before A0
+  if (tid == 0) os->bad = 0;
+  __syncthreads();
+  if (tid == 0 && n4_old + 8 * nraw_old != esc_old) os->bad = 1;
+  for (int b = tid; b < kEscCap + 16; b += kEncThreads) {
+    os->esc_old[b] = b < esc_old ? slot[kOffEsc + b] : 0;
+    os->esc_new[b] = 0;
+  }
+  const bool act = tid < nA;
+  const int G = 128 * A0 + tid, u = G >> 2, gi = G & 3;
+  uint32_t m_old = 0u;
+  if (act) m_old = (slot[kOffTag + u] >> (2 * gi)) & 3u;
+  if (act && m_old == 3u) os->bad = 1;
+  __syncthreads();
+  // old escape offsets of the affected groups
+  int tot_old;
+  const int ex_old = block_excl_scan(act ? ((m_old == 1u) | ((m_old == 2u) << 16)) : 0, os->warp_old, tot_old);
+  const int o4_old = p4 + (ex_old & 0xFFFF);
+  const int oraw_old = n4_old + 8 * (praw + (ex_old >> 16));
+  // the group's tokens: does it hold token pos?
+  bool touched = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) touched = touched || (act && group_token(kind, G, j) == pos);
+  uint32_t m_new = m_old;
+  uint32_t smw[2] = {0u, 0u}, C[2] = {0u, 0u}, ew[2] = {0u, 0u}, esc4 = 0u;
+  if (act && m_old == 1u) esc4 = o4_old < kEscCap ? os->esc_old[o4_old] : 0u;
+  if (act && m_old == 2u) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      ew[j >> 2] |= static_cast<uint32_t>(oraw_old + j < kEscCap ? os->esc_old[oraw_old + j] : 0u) << (8 * (j & 3));
+  }
+  if (touched) {
+    uint32_t b3w[2], b4w[2];
+    group_bases(kind, G, b3g, b3w[0], b3w[1]);
+    group_bases(kind, G, b4g, b4w[0], b4w[1]);
+    // old codes: words 2(gi & 1) and 2(gi & 1) + 1 of the half's extraction
+    const uint32_t* cw = reinterpret_cast<const uint32_t*>(slot + kOffCode);
+    const int h = gi >> 1;
+    uint32_t c[4];
+    extract_codes(h ? cw[256 + u] : cw[u], cw[512 + u], h, c);
+    const uint32_t c0 = c[2 * (gi & 1)], c1 = c[2 * (gi & 1) + 1];
+    // old exponents (valid where an element was present)
+    uint32_t eo[2];
+    if (m_old == 0u) {
+      eo[0] = b3w[0] + c0;
+      eo[1] = b3w[1] + c1;
+    } else if (m_old == 1u) {
+      eo[0] = b4w[0] + (c0 | (spread4(esc4 & 15u) << 3));
+      eo[1] = b4w[1] + (c1 | (spread4(esc4 >> 4) << 3));
+    } else {
+      eo[0] = ew[0];
+      eo[1] = ew[1];
+    }
+    // old sign|mantissa bytes, signs back in their own bytes
+    const uint2 sraw = *reinterpret_cast<const uint2*>(slot + 8 * G);
+    uint32_t so[2] = {sraw.x, sraw.y};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t sg = so[q] & 0x80808080u;
+      so[q] = (so[q] & 0x7F7F7F7Fu) | ((sg >> 8) | (sg << 24));
+    }
+    // present elements after the append: old ones and the token's
+    uint32_t e[2] = {0u, 0u}, sm[2] = {0u, 0u};
+    bool f3 = true, f4 = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = group_token(kind, G, j), q = j >> 2, sh8 = 8 * (j & 3);
+      uint32_t ej = 0u, sj = 0u;
+      if (t < pos) {
+        ej = (eo[q] >> sh8) & 0xFFu;
+        sj = (so[q] >> sh8) & 0xFFu;
+      } else if (t == pos) {
+        const int ch = kind == 0 ? ((8 * G + j) & (kD - 1)) : v_channel_of(8 * G + j);
+        const uint32_t x = os->tok[ch];
+        ej = (x >> 7) & 0xFFu;
+        sj = ((x >> 8) & 0x80u) | (x & 0x7Fu);
+      }
+      e[q] |= ej << sh8;
+      sm[q] |= sj << sh8;
+      if (t <= pos) {
+        const int o3 = static_cast<int>(ej) - static_cast<int>((b3w[q] >> sh8) & 0xFFu);
+        const int o4 = static_cast<int>(ej) - static_cast<int>((b4w[q] >> sh8) & 0xFFu);
+        f3 = f3 && o3 >= 0 && o3 <= 7;
+        f4 = f4 && o4 >= 0 && o4 <= 15;
+      }
+    }
+    m_new = f3 ? 0u : (f4 ? 1u : 2u);
+    // codes (byte lanes: C[0] elements 0-3, C[1] elements 4-7), escape byte, raw exponents
+    esc4 = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = group_token(kind, G, j), q = j >> 2, sh8 = 8 * (j & 3);
+      if (t > pos) continue;  // absent: code and escape bit zero
+      const uint32_t ej = (e[q] >> sh8) & 0xFFu;
+      uint32_t cd = 0u;
+      if (m_new == 0u) {
+        cd = (ej - ((b3w[q] >> sh8) & 0xFFu)) & 7u;
+      } else if (m_new == 1u) {
+        const uint32_t off = (ej - ((b4w[q] >> sh8) & 0xFFu)) & 0xFFu;
+        cd = off & 7u;
+        esc4 |= ((off >> 3) & 1u) << j;
+      }
+      C[q] |= cd << sh8;
+    }
+    ew[0] = m_new == 2u ? e[0] : 0u;
+    ew[1] = m_new == 2u ? e[1] : 0u;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {  // signs rotated one byte within each aligned group of four
+      const uint32_t sg = sm[q] & 0x80808080u;
+      smw[q] = (sm[q] & 0x7F7F7F7Fu) | ((sg << 8) | (sg >> 24));
+    }
+  }
+  // new escape offsets
+  int tot_new;
+  const int ex_new = block_excl_scan(act ? ((m_new == 1u) | ((m_new == 2u) << 16)) : 0, os->warp_new, tot_new);
+  const int n4_new = p4 + (tot_new & 0xFFFF);  // no 4-bit groups after the affected eighths
+  const int nraw_new = praw + (tot_new >> 16);
+  const int esc_new = n4_new + 8 * nraw_new;
+  if (os->bad) return -2;
+  if (esc_new > kEscCap) return -1;
+  // the new escape area in shared memory: earlier 4-bit bytes in place, earlier raw bytes shifted, then
+  // the affected groups' bytes at their new offsets
+  for (int b = tid; b < kEscCap; b += kEncThreads) {
+    if (b < p4)
+      os->esc_new[b] = os->esc_old[b];
+    else if (b >= n4_new && b < n4_new + 8 * praw)
+      os->esc_new[b] = os->esc_old[b - n4_new + n4_old];
+  }
+  if (act && m_new == 1u) os->esc_new[p4 + (ex_new & 0xFFFF)] = static_cast<uint8_t>(esc4);
+  if (act && m_new == 2u) {
+    const int at = n4_new + 8 * (praw + (ex_new >> 16));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) os->esc_new[at + j] = static_cast<uint8_t>(ew[j >> 2] >> (8 * (j & 3)));
+  }
+  // touched groups: sign|mantissa bytes; touched units (all four groups touched): code words, tag byte
+  if (touched) *reinterpret_cast<uint2*>(slot + 8 * G) = make_uint2(smw[0], smw[1]);
+  const int h = gi >> 1;
+  uint32_t wH = 0u, w2 = 0u;
+  if (touched) {
+    if ((gi & 1) == 0) {
+      wH = C[0] | (C[1] << 3);
+    } else {
+      wH = (C[1] & 0x03030303u) << 6;
+      w2 = (C[0] << (3 * h)) | (((C[1] >> 2) & 0x01010101u) << (6 + h));
+    }
+  }
+  uint32_t tagbits = touched ? (m_new << (2 * gi)) : 0u;
+  wH |= __shfl_xor_sync(0xFFFFFFFFu, wH, 1);  // groups 0+1 -> W0, groups 2+3 -> W1
+  w2 |= __shfl_xor_sync(0xFFFFFFFFu, w2, 1);
+  w2 |= __shfl_xor_sync(0xFFFFFFFFu, w2, 2);
+  tagbits |= __shfl_xor_sync(0xFFFFFFFFu, tagbits, 1);
+  tagbits |= __shfl_xor_sync(0xFFFFFFFFu, tagbits, 2);
+  if (touched) {
+    uint32_t* cw = reinterpret_cast<uint32_t*>(slot + kOffCode);
+    if (gi == 0) {
+      cw[u] = wH;
+      cw[512 + u] = w2;
+      slot[kOffTag + u] = static_cast<uint8_t>(tagbits);
+    } else if (gi == 2) {
+      cw[256 + u] = wH;
+    }
+  }
+  // directory: the affected eighths' entries from the scan, later entries the totals
+  if (act && (tid & 127) == 127) {
+    const int w = A0 + (tid >> 7);
+    const int incl = ex_new + ((m_new == 1u) | ((m_new == 2u) << 16));
+    const uint32_t entry = static_cast<uint32_t>((p4 + (incl & 0xFFFF)) & 0x1FF) |
+                           (static_cast<uint32_t>((praw + (incl >> 16)) & 0x7F) << 9);
+    *reinterpret_cast<uint16_t*>(slot + kOffDir + 2 * w) = static_cast<uint16_t>(entry);
+  }
+  if (tid > A1 && tid < 8) {
+    const uint32_t entry = static_cast<uint32_t>(n4_new & 0x1FF) | (static_cast<uint32_t>(nraw_new & 0x7F) << 9);
+    *reinterpret_cast<uint16_t*>(slot + kOffDir + 2 * tid) = static_cast<uint16_t>(entry);
+  }
+  __syncthreads();
+  for (int b = tid; b < kEscCap / 4; b += kEncThreads)
+    reinterpret_cast<uint32_t*>(slot + kOffEsc)[b] = reinterpret_cast<const uint32_t*>(os->esc_new)[b];
+  if (stats != nullptr) {  // the block seals: count its groups' modes
+    __syncthreads();
+    const uint32_t tb = slot[kOffTag + tid];
+    const int c4 = n4_of(tb), cr = nraw_of(tb);
+    int t4;
+    block_excl_scan(c4 | (cr << 16), os->warp_old, t4);
+    if (tid == 0) {
+      const int n4 = t4 & 0xFFFF, nr = t4 >> 16;
+      atomicAdd(&stats->groups[0], static_cast<unsigned long long>(1024 - n4 - nr));
+      atomicAdd(&stats->groups[1], static_cast<unsigned long long>(n4));
+      atomicAdd(&stats->groups[2], static_cast<unsigned long long>(nr));
+      atomicAdd(&stats->escape_bytes, static_cast<unsigned long long>(esc_new));
+      atomicAdd(&stats->slot_tiles, 1ull);
+    }
+  }
+  return esc_new;
+}
+
 struct AppendArgs {
   const uint16_t* k_new;
   const uint16_t* v_new;
@@ -349,6 +619,7 @@ enum AppendPath { kFail = 0, kRawTail = 1, kRawFresh = 2, kOpenNew = 3, kOpenSlo
 // grid (2*n_kv_heads, batch): x = h*2 + kind.
 __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   __shared__ EncShared sh;
+  __shared__ OpenShared os;
   __shared__ int word_prefix[65];
   __shared__ int esc_old;
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1, b = blockIdx.y;
@@ -404,12 +675,30 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   const int s_new = kind == 0 ? pos * kD + tid : v_storage_index(pos, tid & (kD - 1));
 
   if (path >= kOpenNew) {
-    // The open block lives in its slot: rebuild its tokens so far (absent
-    // elements zero), add the new token and encode the first pos + 1 tokens.
-    // Only the units holding the new token, the tags, the directory and the
-    // escape area change.
+    // The open block lives in its slot: only the groups holding the new token
+    // are rebuilt and re-encoded (open_append_groups).
     const uint32_t slot_id = sh.raw_idx;
     uint8_t* slot = a.pools.slot_pool + static_cast<size_t>(slot_id) * kSlot;
+    if (tid < kD) os.tok[tid] = x_new;
+    if (path == kOpenNew) {  // a fresh slot: every byte of the empty image is zero
+      uint4* z = reinterpret_cast<uint4*>(slot);
+      for (int i = tid; i < kSlot / 16; i += kEncThreads) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    const bool sealing = pos + 1 == kBlock;
+    const int esc = open_append_groups(&os, slot, kind, pos, path == kOpenSlot ? esc_old : 0, b3, b4,
+                                       sealing ? a.stats : nullptr);
+    if (esc == -2) {
+      if (tid == 0) report(a.status, GAAC_EFORMAT);
+      return;
+    }
+    if (esc >= 0) {
+      if (tid == 0) *ep = make_entry(slot_id, esc, GAAC_MODE_SLOT, pos + 1);
+      return;
+    }
+    // The escape stream would outgrow the slot (it only grows as tokens
+    // arrive, so the full block would not fit either; the slot is untouched):
+    // the block continues as a raw tile holding its tokens so far.
     bool bad = false;
     uint4* mine = reinterpret_cast<uint4*>(sh.tile + 32 * tid);
     if (path == kOpenSlot) {
@@ -435,17 +724,6 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
       return;
     }
     if (tid < kD) sh.tile[s_new] = x_new;
-    __syncthreads();
-    const bool sealing = pos + 1 == kBlock;
-    const int esc = encode_tile_cta<true>(&sh, kind, b3, b4, slot, sealing ? a.stats : nullptr, pos + 1,
-                                          path == kOpenSlot ? pos : -1);
-    if (esc >= 0) {
-      if (tid == 0) *ep = make_entry(slot_id, esc, GAAC_MODE_SLOT, pos + 1);
-      return;
-    }
-    // The escape stream outgrew the slot (it only grows as tokens arrive, so
-    // the full block would not fit either): the block continues as a raw tile.
-    __syncthreads();
     if (tid == 0) {
       uint32_t idx = 0;
       sh.ok = pop_raw(a.pools, &idx, a.status) ? 1 : 0;
