@@ -17,6 +17,10 @@
 //    of the split, and warp w of a group takes tokens [16w, 16w+16) of each.
 //    Each warp keeps its own online-softmax state (m, l, acc) over its tokens;
 //    the twelve states are merged with a log-sum-exp when the split ends.
+//  * 256-channel heads (two 128-channel half-heads): the two CTAs of a head
+//    form a cluster; each decodes its own half-head's K and V tiles, and the
+//    warps exchange partial scores with st.async stores into the peer's shared
+//    memory (completed on the peer's mbarrier) before the softmax.
 //  * Per block a lane rebuilds two K units and two V units (32 elements each)
 //    straight into tensor-core operand registers, with no shared-memory copy
 //    of the decoded tile:
@@ -58,8 +62,8 @@ constexpr int kCWarps = kGroupWarps * kGroups;    // compute warps
 constexpr int kAttThreads = kCWarps * 32;
 // Staging ring depth: 6 stages of K+V images for 128-channel heads, 4 of K0+K1+V for 256-channel heads
 // (two half-heads).  Block j of a split uses stage j % depth.
-template <int NH>
-constexpr int stages_of() { return NH == 1 ? 6 : 4; }
+template <int KH>
+constexpr int stages_of() { return KH == 1 ? 6 : 4; }
 constexpr int kCtasPerSm = 1;
 constexpr int kRPad = 8;                          // query heads per kv-head in the MMA rows
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
@@ -71,21 +75,28 @@ struct StageMeta {
 };
 
 // NH: 128-channel half-heads per attention head (1, or 2 for 256-channel heads).
-template <int NH>
+// KH: K half-head images a CTA decodes per block: NH, or 1 when the two CTAs
+// of a 256-channel head form a cluster and exchange their partial scores.
+template <int NH, int KH>
 struct AttSmem {
-  static constexpr int kStages = stages_of<NH>();
-  alignas(128) uint8_t stage[kStages][NH + 1][kRawBytes];  // K half-head images, then the V image
+  static constexpr int kStages = stages_of<KH>();
+  static constexpr int kPairs = NH > KH ? kCWarps : 1;  // score mailboxes (cluster pairs only)
+  alignas(128) uint8_t stage[kStages][KH + 1][kRawBytes];  // K half-head images, then the V image
   uint2 lut[256];                 // escape byte -> bit 3 spread into the byte lanes of two exponent words
   uint32_t tagl[256];             // tag byte -> gather selector, counts, raw groups (tag_entry)
-  alignas(16) uint8_t kbases[NH][2][kD];  // K: [half][base3|base4][channel]
+  alignas(16) uint8_t kbases[KH][2][kD];  // K: [image][base3|base4][channel]
   StageMeta smeta[kStages];
-  alignas(16) uint4 qf[NH][8][32];       // q A-operand quads [half][k-step][lane]: (qa0, 0, qa2, 0)
+  alignas(16) uint4 qf[KH][8][32];       // q A-operand quads [image][k-step][lane]: (qa0, 0, qa2, 0)
   alignas(16) uint4 vbw[2][2][32];        // V base words [unit][base3 | base4][lane], groups 0-3
   unsigned int stDone[kStages];           // warps of the group done reading the stage's current block
   float wm[kCWarps][kRPad];       // per warp and head: running maximum (end of split)
   float wl[kCWarps][kRPad];       // per warp and head: denominator (end of split)
   float ww[kCWarps][kRPad];       // per warp and head: merge weight (end of split)
   uint64_t stFull[kStages];
+  alignas(16) float4 mail[kPairs][2][32];  // [warp][buffer][lane]: the peer CTA's partial scores of a block
+  uint64_t mFull[kPairs][2];               // the peer's 512 bytes landed in mail[warp][buffer]
+  uint64_t mEmpty[kPairs][2];              // the peer's warp has read this warp's partials from its mailbox
+  alignas(16) float4 ack[kPairs][2];       // landing slots of the peer's acknowledgements (16 bytes each)
   int last;
 };
 
@@ -326,24 +337,24 @@ __device__ __forceinline__ const void* tile_source(const AttnArgs& a, uint2 e, u
 
 // Table entries of block blk for attention head H and output half hf: the K
 // entries of the head's NH half-heads, then the V entry of half-head NH*H + hf.
-template <int NH>
-__device__ __forceinline__ void block_entries(const AttnArgs& a, int b, int H, int hf, int blk, uint2 e[NH + 1]) {
+template <int NH, int KH>
+__device__ __forceinline__ void block_entries(const AttnArgs& a, int b, int H, int hf, int blk, uint2 e[KH + 1]) {
   const gaac_entry* t = a.table + (static_cast<size_t>(b) * a.max_blocks + blk) * (NH * a.Hkv) * 2;
 #pragma unroll
-  for (int j = 0; j < NH; ++j) e[j] = *reinterpret_cast<const uint2*>(t + (NH * H + j) * 2);
-  e[NH] = *reinterpret_cast<const uint2*>(t + (NH * H + hf) * 2 + 1);
+  for (int j = 0; j < KH; ++j) e[j] = *reinterpret_cast<const uint2*>(t + (NH * H + (KH == NH ? j : hf)) * 2);
+  e[KH] = *reinterpret_cast<const uint2*>(t + (NH * H + hf) * 2 + 1);
 }
 
 // One thread starts the bulk copies of a block's images into stage st (a free
 // stage); stFull[st] completes when all have landed.
-template <int NH>
-__device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem<NH>& sm, int st, const uint2 e[NH + 1]) {
+template <int NH, int KH>
+__device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem<NH, KH>& sm, int st, const uint2 e[KH + 1]) {
   StageMeta m;
-  uint32_t bytes[NH + 1], total = 0;
-  const void* src[NH + 1];
+  uint32_t bytes[KH + 1], total = 0;
+  const void* src[KH + 1];
   bool ok = true;
 #pragma unroll
-  for (int i = 0; i <= NH; ++i) {
+  for (int i = 0; i <= KH; ++i) {
     src[i] = tile_source(a, e[i], bytes[i], m.mode[i], m.esc[i]);
     ok = ok && src[i] != nullptr;
     total += bytes[i];
@@ -353,7 +364,7 @@ __device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem<NH>& sm, 
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic reads of the stage, then async writes
   mbar_arrive_expect_tx(&sm.stFull[st], total);
 #pragma unroll
-  for (int i = 0; i <= NH; ++i)
+  for (int i = 0; i <= KH; ++i)
     if (bytes[i]) bulk_g2s(sm.stage[st][i], src[i], bytes[i], &sm.stFull[st]);
 }
 
@@ -363,6 +374,34 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta(unsigned int* p, 
   return old;
 }
 
+// ------------------------------------------------------ cluster pair (DSMEM)
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of this CTA's shared variable p in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory that completes its bytes on that CTA's
+// mbarrier `bar` (which expects them with arrive.expect_tx).
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float x, float y, float z, float w, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(x), "f"(y), "f"(z), "f"(w), "r"(bar)
+               : "memory");
+}
+
+// All threads of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------ compute warps
 
 // Warp w of group gr: tokens [16w, 16w+16) of blocks gr, gr + kGroups, ...
@@ -370,8 +409,8 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel_cta(unsigned int* p, 
 // shared memory and its accumulators in acc (O^T fragments: acc[m][0..3] =
 // channels 16m+g, 16m+g+8 x heads 2tq, 2tq+1).
 // K unit base words of half-head `half`: channels 32tq..32tq+31, word i = channels 32tq + 4i..+3.
-template <int NH>
-__device__ __forceinline__ void k_bases(const AttSmem<NH>& sm, int half, int tq, uint32_t kb3[8], uint32_t kb4[8]) {
+template <int NH, int KH>
+__device__ __forceinline__ void k_bases(const AttSmem<NH, KH>& sm, int half, int tq, uint32_t kb3[8], uint32_t kb4[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     kb3[i] = *reinterpret_cast<const uint32_t*>(&sm.kbases[half][0][32 * tq + 4 * i]);
@@ -379,33 +418,42 @@ __device__ __forceinline__ void k_bases(const AttSmem<NH>& sm, int half, int tq,
   }
 }
 
-template <int NH>
-__device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm, int b, int H, int hf, int blk0,
+template <int NH, int KH>
+__device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>& sm, int b, int H, int hf, int blk0,
                                              int n_my, int len, int gr, int w, int cw, int lane, float acc[8][4]) {
-  constexpr int kStages = AttSmem<NH>::kStages;
+  constexpr int kStages = AttSmem<NH, KH>::kStages;
   const int g = lane >> 2, tq = lane & 3;
   uint32_t kb3[8], kb4[8];  // one half-head: loaded once (NH = 1) or per half and block (NH = 2)
-  if (NH == 1) k_bases(sm, 0, tq, kb3, kb4);
+  if (KH == 1) k_bases(sm, 0, tq, kb3, kb4);
+  [[maybe_unused]] uint32_t peer_mail = 0u, peer_full = 0u, peer_empty = 0u, peer_ack = 0u;  // the peer's mailbox
+  if constexpr (NH > KH) {
+    const uint32_t peer = cluster_rank() ^ 1u;
+    peer_mail = peer_addr(&sm.mail[cw][0][lane], peer);
+    peer_full = peer_addr(&sm.mFull[cw][0], peer);
+    peer_empty = peer_addr(&sm.mEmpty[cw][0], peer);
+    peer_ack = peer_addr(&sm.ack[cw][0], peer);
+  }
+  int it = 0;  // this warp's block count
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
   float mrun = -INFINITY, lsum = 0.f;  // head g
   const int tA = 16 * w + 2 * tq, tB = tA + 8;  // tokens of S^T columns 2tq, 2tq+1 of the two octets
 #pragma unroll 1
-  for (int j = gr; j < n_my; j += kGroups) {
+  for (int j = gr; j < n_my; j += kGroups, ++it) {
     const int st = j % kStages, jn = j + kStages;  // jn: the block this stage takes next
-    uint2 ne[NH + 1];
+    uint2 ne[KH + 1];
 #pragma unroll
-    for (int i = 0; i <= NH; ++i) ne[i] = make_uint2(0u, 0u);
-    if (lane == 0 && jn < n_my) block_entries<NH>(a, b, H, hf, blk0 + jn, ne);  // used if this warp refills
+    for (int i = 0; i <= KH; ++i) ne[i] = make_uint2(0u, 0u);
+    if (lane == 0 && jn < n_my) block_entries<NH, KH>(a, b, H, hf, blk0 + jn, ne);  // used if this warp refills
     mbar_wait(&sm.stFull[st], static_cast<uint32_t>(j / kStages) & 1u, a.status);
     const StageMeta meta = sm.smeta[st];
     const int nv = min(kBlock, len - (blk0 + j) * kBlock);
-    // ---- S^T for tokens 16w..16w+7 (A) and 16w+8..16w+15 (B), summed over the head's half-heads
+    // ---- S^T for tokens 16w..16w+7 (A) and 16w+8..16w+15 (B), summed over this CTA's K images
     float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
     bool kbadA = false, kbadB = false;
 #pragma unroll 1
-    for (int half = 0; half < NH; ++half) {
-      if (NH > 1) k_bases(sm, half, tq, kb3, kb4);
+    for (int half = 0; half < KH; ++half) {
+      if (KH > 1) k_bases(sm, half, tq, kb3, kb4);
       uint32_t oA[16], oB[16];
       bool bA, bB;
       tile_units(a, sm, sm.stage[st][half], meta.mode[half], meta.esc[half], w, lane, kb3, kb4, kb3, kb4, oA, oB,
@@ -421,6 +469,19 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
         mma_bf16(sA, qv.x, qv.y, qv.z, qv.w, oA[2 * m], oA[2 * m + 1]);
         mma_bf16(sB, qv.x, qv.y, qv.z, qv.w, oB[2 * m], oB[2 * m + 1]);
       }
+    }
+    if constexpr (NH > KH) {
+      // 256-channel heads as a cluster pair: the scores are this CTA's half-head partial plus the peer's.
+      // Each lane posts its partials (NaN for a unit that failed its checks) into the peer's mailbox now,
+      // as asynchronous stores that complete on the peer's barrier, and takes the peer's after the V
+      // decode; both CTAs add S0 + S1 (exact-commutative), so their softmax weights are identical.
+      const int bb = it & 1;
+      if (it >= 2) {  // the peer has read this buffer's previous use: its 16-byte acknowledgement landed
+        if (lane == 0) mbar_arrive_expect_tx(&sm.mEmpty[cw][bb], sizeof(float4));
+        mbar_wait(&sm.mEmpty[cw][bb], static_cast<uint32_t>((it >> 1) + 1) & 1u, a.status);
+      }
+      st_async_f4(peer_mail + bb * 32 * sizeof(float4), kbadA ? NAN : sA[0], kbadA ? NAN : sA[1],
+                  kbadB ? NAN : sB[0], kbadB ? NAN : sB[1], peer_full + bb * sizeof(uint64_t));
     }
     // ---- V units of the same tokens (independent of the scores: decoded while the MMAs above run)
     uint32_t oA[16], oB[16];
@@ -439,13 +500,37 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
       vb4[hv][4] = vb4[hv][5] = x4.z;
       vb4[hv][6] = vb4[hv][7] = x4.w;
     }
-    tile_units(a, sm, sm.stage[st][NH], meta.mode[NH], meta.esc[NH], w, lane, vb3[0], vb4[0], vb3[1], vb4[1], oA,
+    tile_units(a, sm, sm.stage[st][KH], meta.mode[KH], meta.esc[KH], w, lane, vb3[0], vb4[0], vb3[1], vb4[1], oA,
                oB, vbadA, vbadB);
     // The stage is read: the group's last warp to get here refills it with block jn.
     __syncwarp();
     if (lane == 0 && atomic_add_acq_rel_cta(&sm.stDone[st], 1u) == kGroupWarps - 1) {
       sm.stDone[st] = 0u;
-      if (jn < n_my) issue_block<NH>(a, sm, st, ne);
+      if (jn < n_my) issue_block<NH, KH>(a, sm, st, ne);
+    }
+    if constexpr (NH > KH) {  // take the peer's partial scores of this block (posted above)
+      const int bb = it & 1;
+      if (lane == 0) mbar_arrive_expect_tx(&sm.mFull[cw][bb], 32 * sizeof(float4));
+      mbar_wait(&sm.mFull[cw][bb], static_cast<uint32_t>(it >> 1) & 1u, a.status);
+      const float4 X = sm.mail[cw][bb][lane];
+      // Acknowledge with an asynchronous store into the peer's ack slot that completes on its mEmpty; its
+      // payload is the sum of the loaded scores, so it cannot issue before every lane's load has returned.
+      {
+        float ackv = (X.x + X.y) + (X.z + X.w);
+        ackv += __shfl_xor_sync(kFull, ackv, 16);
+        ackv += __shfl_xor_sync(kFull, ackv, 8);
+        ackv += __shfl_xor_sync(kFull, ackv, 4);
+        ackv += __shfl_xor_sync(kFull, ackv, 2);
+        ackv += __shfl_xor_sync(kFull, ackv, 1);
+        if (lane == 0)
+          st_async_f4(peer_ack + bb * sizeof(float4), ackv, 0.f, 0.f, 0.f, peer_empty + bb * sizeof(uint64_t));
+      }
+      sA[0] = (kbadA ? NAN : sA[0]) + X.x;
+      sA[1] = (kbadA ? NAN : sA[1]) + X.y;
+      sB[0] = (kbadB ? NAN : sB[0]) + X.z;
+      sB[1] = (kbadB ? NAN : sB[1]) + X.w;
+      kbadA = __any_sync(kFull, isnan(sA[0]) || isnan(sA[1]));
+      kbadB = __any_sync(kFull, isnan(sB[0]) || isnan(sB[1]));
     }
     // ---- online softmax of head g over the warp's 16 tokens
     const float x0 = (!kbadA && tA < nv) ? sA[0] * a.scale_log2 : -INFINITY;
@@ -503,6 +588,16 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
       }
     }
   }
+  if constexpr (NH > KH) {
+    // The acknowledgements of this warp's last posts (one per buffer used) are still owed: take them, so that
+    // no asynchronous store is on its way to this CTA when it exits.
+#pragma unroll 1
+    for (int u = max(0, it - 2); u < it; ++u) {
+      const int bb = u & 1;
+      if (lane == 0) mbar_arrive_expect_tx(&sm.mEmpty[cw][bb], sizeof(float4));
+      mbar_wait(&sm.mEmpty[cw][bb], static_cast<uint32_t>(u >> 1) & 1u, a.status);
+    }
+  }
   lsum += __shfl_xor_sync(kFull, lsum, 1);
   lsum += __shfl_xor_sync(kFull, lsum, 2);
   if (tq == 0) {
@@ -520,8 +615,8 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH>& sm,
 // running maximum; the subsets are then combined the same way in shared
 // memory.  The staging ring is free by then and holds that exchange.
 // base: the first partial of the pair; out: its first output row.
-template <int NH>
-__device__ __noinline__ void merge_splits(const float* base, int ns, int r, float* out, AttSmem<NH>& sm, int tid) {
+template <int NH, class Smem>
+__device__ __noinline__ void merge_splits(const float* base, int ns, int r, float* out, Smem& sm, int tid) {
   constexpr int kBatch = 10;
   const int o4n = r * (kD / 4);  // float4 columns of the r x 128 output
   const int groups = kAttThreads / o4n;
@@ -608,13 +703,16 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
 
 
 // Grid (split, NH * Hkv, batch): CTA y serves attention head H = y / NH and
-// output channels [128 hf, 128 hf + 128) of it (hf = y % NH); for NH = 2 it
-// reads the K tiles of both half-heads and the V tile of half-head NH*H + hf.
-template <int NH>
+// output channels [128 hf, 128 hf + 128) of it (hf = y % NH), reading the V
+// tile of half-head NH*H + hf.  KH = NH: the CTA also reads the K tiles of all
+// NH half-heads.  KH = 1 < NH: the NH CTAs of a head form a cluster; each
+// reads the K tile of its own half-head and the pair exchanges partial scores
+// through distributed shared memory, so every K tile is decoded once.
+template <int NH, int KH>
 __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(AttnArgs a) {
-  constexpr int kStages = AttSmem<NH>::kStages;
+  constexpr int kStages = AttSmem<NH, KH>::kStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  AttSmem<NH>& sm = *reinterpret_cast<AttSmem<NH>*>(smem_raw);
+  AttSmem<NH, KH>& sm = *reinterpret_cast<AttSmem<NH, KH>*>(smem_raw);
   const int split = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
   const int H = y / NH, hf = y % NH, nkv = NH * a.Hkv;  // nkv: half-heads in the table and the bases
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -633,9 +731,9 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
     sm.tagl[x] = tag_entry(static_cast<uint32_t>(x));
   }
-  for (int x = tid; x < NH * 2 * kD; x += kAttThreads) {  // K: [half][base3|base4][channel]
+  for (int x = tid; x < KH * 2 * kD; x += kAttThreads) {  // K: [image][base3|base4][channel]
     const int half = x / (2 * kD), which = (x / kD) & 1, c = x % kD;
-    sm.kbases[half][which][c] = (which ? a.base4 : a.base3)[(NH * H + half) * kD + c];
+    sm.kbases[half][which][c] = (which ? a.base4 : a.base3)[(NH * H + (KH == NH ? half : hf)) * kD + c];
   }
   // V unit base words: group i of the lane's unit hv holds channels 16m+g and 16m+g+8 (m = 4hv + i, g =
   // lane/4) in byte lanes 0, 2 and 1, 3 of both of its exponent words
@@ -651,12 +749,12 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   }
   // q of the kv-head's query heads, times 2^-4, as A-operand quads of S^T = q K^T: for half `half`, lane
   // (g, tq) and k-step m, (channels 128 half + 32tq + 4m + {0, 2}, 0, ... + {1, 3}, 0) of head g (rows 8-15 zero)
-  for (int x = tid; x < NH * 32 * 8 * 2; x += kAttThreads) {
+  for (int x = tid; x < KH * 32 * 8 * 2; x += kAttThreads) {
     const int half = x / 512, ln = (x / 16) % 32, n = ln / 4, tq = ln % 4, m = (x / 2) % 8, odd = x % 2;
     uint32_t v = 0u;
     if (n < a.r) {
-      const uint16_t* qrow =
-          a.q + (static_cast<size_t>(b) * a.Hq + H * a.r + n) * (NH * kD) + kD * half + 32 * tq + 4 * m + odd;
+      const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + H * a.r + n) * (NH * kD) +
+                             kD * (KH == NH ? half : hf) + 32 * tq + 4 * m + odd;
       v = bf16x2_div16(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16));
     }
     reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd] = v;
@@ -666,18 +764,23 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     mbar_init(&sm.stFull[tid], 1);
     sm.stDone[tid] = 0u;
   }
+  if (NH > KH && tid < 2 * AttSmem<NH, KH>::kPairs) {
+    mbar_init(&sm.mFull[tid / 2][tid % 2], 1);   // lane 0's expect_tx; the peer's bytes complete it
+    mbar_init(&sm.mEmpty[tid / 2][tid % 2], 1);  // lane 0 of the peer's warp, after reading
+  }
   fence_mbar_init();
   __syncthreads();
+  if constexpr (NH > KH) cluster_sync();  // the peer's mailbox barriers exist before any remote arrival
   if (tid < min(n_my, kStages)) {  // the first blocks, one lane each; later ones are issued as stages free up
-    uint2 e[NH + 1];
-    block_entries<NH>(a, b, H, hf, blk0 + tid, e);
-    issue_block<NH>(a, sm, tid, e);
+    uint2 e[KH + 1];
+    block_entries<NH, KH>(a, b, H, hf, blk0 + tid, e);
+    issue_block<NH, KH>(a, sm, tid, e);
   }
 
   const int r = a.r;
   float* part = a.part + ((static_cast<size_t>(b) * nkv + y) * a.n_splits + split) * kPartFloats;
   float acc[8][4];
-  compute_warp<NH>(a, sm, b, H, hf, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane, acc);
+  compute_warp<NH, KH>(a, sm, b, H, hf, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane, acc);
   if (tid == 0) {
     // Every issued copy was waited for by its group; after a timed-out wait,
     // wait once more (bounded) so that no copy is still landing at exit.
@@ -736,6 +839,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   // partial stores before thread 0's acq_rel add, and the add orders the other
   // splits' stores before this CTA's loads (the barrier passes that on).
   __syncthreads();
+  if constexpr (NH > KH) cluster_sync();  // no remote arrival is still on its way to this CTA
   unsigned int* counter = a.counters + static_cast<size_t>(b) * nkv + y;
   if (tid == 0) sm.last = atomic_add_acq_rel(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
   __syncthreads();
@@ -757,18 +861,54 @@ static int device_sms() {
   return cached[dev];
 }
 
-template <int NH>
+template <int NH, int KH>
 static bool prepare_kernel() {
   static bool done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(attn_split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(AttSmem<NH>))) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_split_kernel<NH, KH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(AttSmem<NH, KH>))) != cudaSuccess)
       return false;
     done[dev] = true;
   }
   return true;
+}
+
+// Launch configuration of the cluster-pair kernel for 256-channel heads: clusters of the NH CTAs of a head.
+template <int NH, int KH>
+static cudaLaunchConfig_t pair_config(dim3 grid, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAttThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(AttSmem<NH, KH>);
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = NH;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Clusters of the pair kernel that can be resident at once (0 if unknown), cached per device.
+template <int NH, int KH>
+static int pair_max_clusters() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config<NH, KH>(dim3(1, NH, 1), nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_split_kernel<NH, KH>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = -1;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev] > 0 ? cached[dev] : 0;
 }
 
 }  // namespace gaac
@@ -815,11 +955,19 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
       (reinterpret_cast<uintptr_t>(base4) & 15u) || (reinterpret_cast<uintptr_t>(workspace) & 15u) ||
       (reinterpret_cast<uintptr_t>(out) & 3u))
     return GAAC_EINVAL;
+  constexpr int KH = 1;  // 256-channel heads: the two CTAs of a head form a cluster and share the scores
   const int nkv = NH * n_kv_heads;  // CTAs per (sequence, split) and half-heads in the table
-  if (n_splits <= 0) n_splits = gaac_attention_auto_splits(batch, nkv, max_blocks);
+  if (!prepare_kernel<NH, KH>()) return GAAC_ECUDA;
+  if (n_splits <= 0) {
+    n_splits = gaac_attention_auto_splits(batch, nkv, max_blocks);
+    if (NH > KH) {  // one wave of resident clusters
+      const long long per_split = static_cast<long long>(batch) * n_kv_heads;
+      const int mc = pair_max_clusters<NH, KH>();
+      if (mc > 0 && per_split * n_splits > mc) n_splits = static_cast<int>(max(1ll, mc / per_split));
+    }
+  }
   if (n_splits > max_blocks) n_splits = max_blocks;
   if (workspace_bytes < gaac_attention_workspace(batch, nkv, max_blocks, n_splits)) return GAAC_EINVAL;
-  if (!prepare_kernel<NH>()) return GAAC_ECUDA;
   AttnArgs a;
   a.q = q;
   a.seq_lens = seq_lens;
@@ -841,7 +989,13 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
   a.out = out;
   a.status = d_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  attn_split_kernel<NH><<<dim3(n_splits, nkv, batch), kAttThreads, sizeof(AttSmem<NH>), st>>>(a);
+  if (NH > KH) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config<NH, KH>(dim3(n_splits, nkv, batch), st, attr);
+    if (cudaLaunchKernelEx(&cfg, attn_split_kernel<NH, KH>, a) != cudaSuccess) return GAAC_ECUDA;
+  } else {
+    attn_split_kernel<NH, KH><<<dim3(n_splits, nkv, batch), kAttThreads, sizeof(AttSmem<NH, KH>), st>>>(a);
+  }
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
 
