@@ -514,16 +514,14 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
       mbar_wait(&sm.mFull[cw][bb], static_cast<uint32_t>(it >> 1) & 1u, a.status);
       const float4 X = sm.mail[cw][bb][lane];
       // Acknowledge with an asynchronous store into the peer's ack slot that completes on its mEmpty; its
-      // payload is the sum of the loaded scores, so it cannot issue before every lane's load has returned.
+      // payload is an OR over the warp of the loaded scores' bits, so it cannot issue before every lane's
+      // load has returned.
       {
-        float ackv = (X.x + X.y) + (X.z + X.w);
-        ackv += __shfl_xor_sync(kFull, ackv, 16);
-        ackv += __shfl_xor_sync(kFull, ackv, 8);
-        ackv += __shfl_xor_sync(kFull, ackv, 4);
-        ackv += __shfl_xor_sync(kFull, ackv, 2);
-        ackv += __shfl_xor_sync(kFull, ackv, 1);
+        const uint32_t dep = __reduce_or_sync(kFull, __float_as_uint(X.x) | __float_as_uint(X.y) |
+                                                         __float_as_uint(X.z) | __float_as_uint(X.w));
         if (lane == 0)
-          st_async_f4(peer_ack + bb * sizeof(float4), ackv, 0.f, 0.f, 0.f, peer_empty + bb * sizeof(uint64_t));
+          st_async_f4(peer_ack + bb * sizeof(float4), __uint_as_float(dep), 0.f, 0.f, 0.f,
+                      peer_empty + bb * sizeof(uint64_t));
       }
       sA[0] = (kbadA ? NAN : sA[0]) + X.x;
       sA[1] = (kbadA ? NAN : sA[1]) + X.y;
