@@ -51,3 +51,25 @@ def test_attention_hd256_rejects_bad_shapes():
     ws = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(ValueError):
         G.decode_attention_hd256(q, c.seq_lens, c.table, c.pools, c.base3, c.base4, 1 / 16, out, ws)
+
+
+def test_attention_hd256_long_splits_reuse_mailboxes():
+    """Few splits over a long sequence: each CTA of a cluster pair takes 64 blocks (about 21 per warp),
+    so every warp reuses both of its score mailboxes many times; the result must still match the fp64
+    oracle, and an open BF16 tail must be read too."""
+    B, Hkv, Hq = 1, 2, 8
+    T = 8192 + 37
+    k, v = W.make_kv(0, 8, B, T, 2 * Hkv, device="cuda")
+    lens = U.lens_tensor([T])
+    c = U.build(k, v, lens)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(257)
+    q = torch.randn(B, Hq, 256, generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.empty((B, Hq, 256), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(G.attention_workspace(B, 2 * Hkv, c.max_blocks, 2), dtype=torch.uint8, device="cuda")
+    G.decode_attention_hd256(q, c.seq_lens, c.table, c.pools, c.base3, c.base4, 1 / 16, out, ws, n_splits=2,
+                             status=c.status)
+    torch.cuda.synchronize()
+    assert int(c.status.item()) == 0
+    worst, flagged = U.check_attention(out, q, k.view(B, T, Hkv, 256), v.view(B, T, Hkv, 256), lens, 1 / 16)
+    assert flagged == 0
