@@ -8,7 +8,9 @@
 //    mantissa are stored unchanged;
 //  - section 3.3 / Figure 3: complete blocks are encoded once into
 //    fixed-capacity slots, oversized blocks stay BF16, the incomplete tail is a
-//    BF16 block that is encoded when it fills ("fill-then-finalize").
+//    BF16 block that is encoded when it fills ("fill-then-finalize").  With
+//    GAAC_OPEN_COMPRESSED the open block is kept in its slot instead, and an
+//    append re-encodes only the groups that gain the new token.
 //
 // One CTA of 256 threads encodes one tile; thread u owns the 32-element code
 // unit u (storage elements 32u..32u+31), i.e. exactly one tag byte and one
@@ -35,29 +37,20 @@ __device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? 
 // Token of storage element s (format v3).
 __device__ __forceinline__ int token_of(int kind, int s) { return kind == 0 ? (s >> 7) : v_token_of(s); }
 
-// Whether code unit u holds elements of token t: a K unit is a quarter of one
-// token, a V unit unit 32 (2w + h) + 4g + q holds tokens 16w + 2q + {0, 1, 8, 9}.
-__device__ __forceinline__ bool unit_holds_token(int kind, int u, int t) {
-  return kind == 0 ? (u >> 2) == t : ((u >> 6) == (t >> 4) && (u & 3) == ((t & 7) >> 1));
-}
-
 // Encodes the tile in sh->tile into `slot` (global, 16-byte aligned) unless its
 // escape stream exceeds the capacity.  Returns the escape length, or -1 when
 // the tile must stay raw (then nothing is written).  CTA-uniform result; all
 // 256 threads must call it.
 //
-// n_present < 64 encodes an open tile: elements of tokens >= n_present are
-// absent (sh->tile must hold zero there); they take no part in their group's
-// mode, and their codes and escape bits are zero.  only_token >= 0 writes the
-// sign|mantissa and code words of the units holding that token only (the
-// other units' bytes must already be in the slot: appending one token changes
-// no other unit), and the tag plane, directory and escape area in full.
-// kOpen = false compiles the sealed-tile encoder (n_present and only_token
-// are then ignored: every token present, every unit written).
+// n_present < 64 encodes an open tile (the incomplete last block of a
+// prefill): elements of tokens >= n_present are absent (sh->tile must hold
+// zero there); they take no part in their group's mode, and their codes and
+// escape bits are zero.  kOpen = false compiles the sealed-tile encoder
+// (n_present is then ignored: every token present).
 template <bool kOpen>
 __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restrict__ b3g,
                                const uint8_t* __restrict__ b4g, uint8_t* __restrict__ slot,
-                               gaac_stats* stats, int n_present = kBlock, int only_token = -1) {
+                               gaac_stats* stats, int n_present = kBlock) {
   const int u = threadIdx.x;
   const int lane = u & 31, warp = u >> 5;
   uint32_t xw[16];
@@ -173,15 +166,13 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
     const uint32_t sg = smb[j] & 0x80808080u;
     smb[j] = (smb[j] & 0x7F7F7F7Fu) | ((sg << 8) | (sg >> 24));
   }
-  if (!kOpen || only_token < 0 || unit_holds_token(kind, u, only_token)) {
-    uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
-    smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
-    smdst[1] = make_uint4(smb[4], smb[5], smb[6], smb[7]);
-    uint32_t* cw = reinterpret_cast<uint32_t*>(slot + kOffCode);
-    cw[u] = W[0];
-    cw[256 + u] = W[1];
-    cw[512 + u] = W[2];
-  }
+  uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
+  smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
+  smdst[1] = make_uint4(smb[4], smb[5], smb[6], smb[7]);
+  uint32_t* cw = reinterpret_cast<uint32_t*>(slot + kOffCode);
+  cw[u] = W[0];
+  cw[256 + u] = W[1];
+  cw[512 + u] = W[2];
   slot[kOffTag + u] = static_cast<uint8_t>(tagbyte);
   uint8_t* escp = slot + kOffEsc;
   for (int k = 0; k < n4; ++k) escp[off4 + k] = static_cast<uint8_t>(esc4 >> (8 * k));
