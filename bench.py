@@ -735,19 +735,40 @@ def cpu_baseline(units: int, n_layers: int) -> dict:
                       f"{n_layers * H} units over {cores} cores; {wall:.0f} s wall including the untimed encode"}
 
 
+_WORKER_SAMPLE = None
+
+
+def _init_reference_worker(counter, n_units: int):
+    """Pool initializer: this worker's own (layer, kv-head) unit, encoded once (untimed)."""
+    global _WORKER_SAMPLE
+    with counter.get_lock():
+        uid = counter.value
+        counter.value += 1
+    _WORKER_SAMPLE = OracleSample([uid % n_units])
+
+
+def _time_reference_worker(_) -> float:
+    return _WORKER_SAMPLE.run(0)
+
+
 def run_reference(args):
-    """The oracle arm: each step runs one (layer, kv-head) unit per host core at once, scaled to a full step."""
+    """The oracle arm: one process per host core, each holding one (layer, kv-head) unit of the workload
+    built once; a step runs every core's unit at once, scaled to a full step."""
+    import multiprocessing as mp
+
     rank, world, _ = dist_env()
     if rank != 0:
         return
     cores = host_cores()
     H = 8
-    for _ in range(args.warmup):
-        oracle_pool_times([[c] for c in range(cores)])
+    ctx = mp.get_context("spawn")
+    counter = ctx.Value("i", 0)
     steps_us = []
-    for s in range(args.steps):
-        times = oracle_pool_times([[(s * cores + c) % (args.layers * H)] for c in range(cores)])
-        steps_us.append(statistics.mean(times) * args.layers * H / cores * 1e6)
+    with ctx.Pool(cores, initializer=_init_reference_worker, initargs=(counter, args.layers * H)) as pool:
+        for i in range(args.warmup + args.steps):
+            times = pool.map(_time_reference_worker, range(cores), chunksize=1)
+            if i >= args.warmup:
+                steps_us.append(statistics.mean(times) * args.layers * H / cores * 1e6)
     v = statistics.median(steps_us)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": world,
