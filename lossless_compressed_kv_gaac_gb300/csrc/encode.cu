@@ -48,7 +48,7 @@ __device__ __forceinline__ int token_of(int kind, int s) { return kind == 0 ? (s
 // escape bits are zero.  kOpen = false compiles the sealed-tile encoder
 // (n_present is then ignored: every token present).
 template <bool kOpen>
-__device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restrict__ b3g,
+__device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restrict__ b3g,
                                const uint8_t* __restrict__ b4g, uint8_t* __restrict__ slot,
                                gaac_stats* stats, int n_present = kBlock) {
   const int u = threadIdx.x;
@@ -67,15 +67,14 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
   }
   if (u < 4) sh->mode_counts[u] = 0;
 
-  uint32_t code[32];
+  uint32_t W[3] = {0, 0, 0};  // the unit's code-plane words, filled code by code
   uint32_t smb[8];  // sign|mantissa bytes, 4 per word
   uint32_t esc4 = 0;  // the unit's 4-bit escape bytes, little-endian, in group order
-  uint32_t ew[8];     // exponent bytes of the 32 elements, 4 per word
   int n4 = 0, nraw = 0;
   uint32_t tagbyte = 0;
   int my_counts[3] = {0, 0, 0};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) smb[j] = ew[j] = 0;
+  for (int j = 0; j < 8; ++j) smb[j] = 0;
 
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
@@ -88,7 +87,6 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
       pres[j] = !kOpen || token_of(kind, 32 * u + el) < n_present;
       const uint32_t x = (xw[el >> 1] >> (16 * (el & 1))) & 0xFFFFu;
       e[j] = (x >> 7) & 0xFF;
-      ew[el >> 2] |= static_cast<uint32_t>(e[j]) << (8 * (el & 3));
       const uint32_t sm = ((x >> 8) & 0x80u) | (x & 0x7Fu);
       smb[el >> 2] |= sm << (8 * (el & 3));
       const int c = channel_of(kind, 32 * u + el);
@@ -114,7 +112,16 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
         cd = off & 7u;
         eb |= ((off >> 3) & 1u) << j;
       }
-      code[8 * gi + j] = cd;
+      // format v3 placement: element 16h + 4q + L of the unit goes to byte lane L of W[h] (q = 0: bits
+      // 0-2, q = 1: bits 3-5, q = 3: bits 6-7 with its third bit in W[2] bit 6+h) or of W[2] (q = 2: bits 3h..)
+      const int h = gi >> 1, q = (8 * (gi & 1) + j) >> 2, L = j & 3;
+      if (q == 0) W[h] |= cd << (8 * L);
+      if (q == 1) W[h] |= cd << (8 * L + 3);
+      if (q == 2) W[2] |= cd << (8 * L + 3 * h);
+      if (q == 3) {
+        W[h] |= (cd & 3u) << (8 * L + 6);
+        W[2] |= ((cd >> 2) & 1u) << (8 * L + 6 + h);
+      }
     }
     if (mode == 1u) {
       esc4 |= eb << (8 * n4);
@@ -147,18 +154,6 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
   const int esc = tot4 + 8 * totraw;
   if (esc > kEscCap || slot == nullptr) return -1;
 
-  // Code plane words of this unit (format v3 placement, as v1).
-  uint32_t W[3] = {0, 0, 0};
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-#pragma unroll
-    for (int L = 0; L < 4; ++L) {
-      const uint32_t c0 = code[16 * h + L], c1 = code[16 * h + 4 + L], c2 = code[16 * h + 8 + L],
-                     c3 = code[16 * h + 12 + L];
-      W[h] |= (c0 | (c1 << 3) | ((c3 & 3u) << 6)) << (8 * L);
-      W[2] |= ((c2 << (3 * h)) | (((c3 >> 2) & 1u) << (6 + h))) << (8 * L);
-    }
-  }
   // Sign|mantissa plane: each byte keeps its mantissa and takes the sign of the
   // previous element of its aligned group of four (cyclically).
 #pragma unroll
@@ -182,7 +177,10 @@ __device__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restric
     for (int gi = 0; gi < 4; ++gi) {
       if (((tagbyte >> (2 * gi)) & 3u) != 2u) continue;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) escp[r + j] = static_cast<uint8_t>(ew[2 * gi + (j >> 2)] >> (8 * (j & 3)));
+      for (int j = 0; j < 8; ++j) {  // the exponent of element 8gi + j (zero where absent)
+        const int el = 8 * gi + j;
+        escp[r + j] = static_cast<uint8_t>(xw[el >> 1] >> (16 * (el & 1) + 7));
+      }
       r += 8;
     }
   }
@@ -255,7 +253,7 @@ struct EncodeArgs {
 };
 
 // grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
-__global__ void __launch_bounds__(kEncThreads) encode_blocks_kernel(EncodeArgs a) {
+__global__ void __launch_bounds__(kEncThreads, 3) encode_blocks_kernel(EncodeArgs a) {
   __shared__ EncShared sh;
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
   const int blk = blockIdx.y, b = blockIdx.z;
