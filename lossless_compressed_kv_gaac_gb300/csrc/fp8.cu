@@ -72,18 +72,17 @@ __global__ void __launch_bounds__(kD) fp8_calibrate_kernel(const uint8_t* __rest
 
 __device__ __forceinline__ int fp8_channel_of(int kind, int s) { return kind == 0 ? (s & 127) : v_channel_of(s); }
 
-// Three 3-bit-per-element words of a 32-element unit (the code plane's layout):
-// v[j] is element j's field.
-__device__ __forceinline__ void pack_field3(const uint32_t v[32], uint32_t W[3]) {
-  W[0] = W[1] = W[2] = 0u;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-#pragma unroll
-    for (int L = 0; L < 4; ++L) {
-      const uint32_t c0 = v[16 * h + L], c1 = v[16 * h + 4 + L], c2 = v[16 * h + 8 + L], c3 = v[16 * h + 12 + L];
-      W[h] |= (c0 | (c1 << 3) | ((c3 & 3u) << 6)) << (8 * L);
-      W[2] |= ((c2 << (3 * h)) | (((c3 >> 2) & 1u) << (6 + h))) << (8 * L);
-    }
+// Adds element j's 3-bit field v to the unit's three words (format v3's code-plane placement: element
+// 16h + 4q + L in byte lane L of W[h] at bits 0-2 (q = 0) or 3-5 (q = 1), of W[2] at bits 3h.. (q = 2), or
+// split as bits 6-7 of W[h] and bit 6+h of W[2] (q = 3)).
+__device__ __forceinline__ void put_field3(uint32_t W[3], int j, uint32_t v) {
+  const int h = j >> 4, jj = j & 15, L = jj & 3, q = jj >> 2;
+  if (q == 0) W[h] |= v << (8 * L);
+  if (q == 1) W[h] |= v << (8 * L + 3);
+  if (q == 2) W[2] |= v << (8 * L + 3 * h);
+  if (q == 3) {
+    W[h] |= (v & 3u) << (8 * L + 6);
+    W[2] |= ((v >> 2) & 1u) << (8 * L + 6 + h);
   }
 }
 
@@ -148,7 +147,8 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
   const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
   const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
   const uint32_t emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
-  uint32_t code[32], smv[32], ex[32];
+  uint32_t CW[3] = {0u, 0u, 0u};  // code-plane words, filled field by field
+  uint32_t SW[4] = {0u, 0u, 0u, 0u};  // sign|mantissa: nibbles (E4M3) or 3-bit fields in SW[0..2] (E5M2)
   uint32_t esc4 = 0, tagbyte = 0;
   int n4 = 0, nraw = 0, my_counts[3] = {0, 0, 0};
 #pragma unroll
@@ -161,8 +161,11 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
       const int el = 8 * gi + j;
       const uint32_t x = seq[32 * u + el];
       e[j] = (x >> L.mw) & emask;
-      ex[el] = e[j];
-      smv[el] = ((x >> 7) << L.mw) | (x & mmask);
+      const uint32_t smv = ((x >> 7) << L.mw) | (x & mmask);
+      if (L.ew == 4)
+        SW[el >> 3] |= smv << (4 * (el & 7));
+      else
+        put_field3(SW, el, smv);
       const int c = fp8_channel_of(kind, 32 * u + el);
       b3[j] = b3g[c];
       b4[j] = b4g[c];
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
         cd = off & 7u;
         eb |= ((off >> 3) & 1u) << j;
       }
-      code[8 * gi + j] = cd;
+      put_field3(CW, 8 * gi + j, cd);
     }
     if (mode == 1u) {
       esc4 |= eb << (8 * n4);
@@ -222,25 +225,18 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
   uint8_t* slot = a.slots + tile * L.slot;
   // sign|mantissa plane
   if (L.ew == 4) {  // nibble of element s in byte s/2 (low nibble for even s): 16 bytes per unit
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int el = 0; el < 32; ++el) w[el >> 3] |= smv[el] << (4 * (el & 7));
-    *reinterpret_cast<uint4*>(slot + 16 * u) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(slot + 16 * u) = make_uint4(SW[0], SW[1], SW[2], SW[3]);
   } else {  // 3-bit fields laid out like the code plane, at offset 0
-    uint32_t W[3];
-    pack_field3(smv, W);
     uint32_t* sw = reinterpret_cast<uint32_t*>(slot);
-    sw[u] = W[0];
-    sw[256 + u] = W[1];
-    sw[512 + u] = W[2];
+    sw[u] = SW[0];
+    sw[256 + u] = SW[1];
+    sw[512 + u] = SW[2];
   }
   {
-    uint32_t W[3];
-    pack_field3(code, W);
     uint32_t* cw = reinterpret_cast<uint32_t*>(slot + L.off_code);
-    cw[u] = W[0];
-    cw[256 + u] = W[1];
-    cw[512 + u] = W[2];
+    cw[u] = CW[0];
+    cw[256 + u] = CW[1];
+    cw[512 + u] = CW[2];
   }
   slot[L.off_tag + u] = static_cast<uint8_t>(tagbyte);
   uint8_t* escp = slot + L.off_esc;
@@ -251,7 +247,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
     for (int gi = 0; gi < 4; ++gi) {
       if (((tagbyte >> (2 * gi)) & 3u) != 2u) continue;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) escp[r + j] = static_cast<uint8_t>(ex[8 * gi + j]);
+      for (int j = 0; j < 8; ++j) escp[r + j] = static_cast<uint8_t>((seq[32 * u + 8 * gi + j] >> L.mw) & emask);
       r += 8;
     }
   }
