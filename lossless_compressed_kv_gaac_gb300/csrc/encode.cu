@@ -53,42 +53,28 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
                                gaac_stats* stats, int n_present = kBlock) {
   const int u = threadIdx.x;
   const int lane = u & 31, warp = u >> 5;
-  uint32_t xw[16];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(sh->tile + 32 * u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 w = src[i];
-      xw[4 * i + 0] = w.x;
-      xw[4 * i + 1] = w.y;
-      xw[4 * i + 2] = w.z;
-      xw[4 * i + 3] = w.w;
-    }
-  }
+  const uint4* src = reinterpret_cast<const uint4*>(sh->tile + 32 * u);  // the unit's 32 values, 4 quads of 8
   if (u < 4) sh->mode_counts[u] = 0;
 
   uint32_t W[3] = {0, 0, 0};  // the unit's code-plane words, filled code by code
-  uint32_t smb[8];  // sign|mantissa bytes, 4 per word
   uint32_t esc4 = 0;  // the unit's 4-bit escape bytes, little-endian, in group order
   int n4 = 0, nraw = 0;
   uint32_t tagbyte = 0;
   int my_counts[3] = {0, 0, 0};
-#pragma unroll
-  for (int j = 0; j < 8; ++j) smb[j] = 0;
 
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     int e[8], b3[8], b4[8];
     bool pres[8];
     bool fits3 = true, fits4 = true;
+    const uint4 gq = src[gi];  // the group's 8 values
+    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int el = 8 * gi + j;
       pres[j] = !kOpen || token_of(kind, 32 * u + el) < n_present;
-      const uint32_t x = (xw[el >> 1] >> (16 * (el & 1))) & 0xFFFFu;
+      const uint32_t x = (gw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
       e[j] = (x >> 7) & 0xFF;
-      const uint32_t sm = ((x >> 8) & 0x80u) | (x & 0x7Fu);
-      smb[el >> 2] |= sm << (8 * (el & 3));
       const int c = channel_of(kind, 32 * u + el);
       b3[j] = b3g[c];
       b4[j] = b4g[c];
@@ -156,8 +142,15 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
 
   // Sign|mantissa plane: each byte keeps its mantissa and takes the sign of the
   // previous element of its aligned group of four (cyclically).
+  uint32_t smb[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < 8; ++j) {  // word j: elements 4j..4j+3 from two staged words
+    const uint4 gq = src[j >> 1];
+    const uint32_t w0 = (j & 1) ? gq.z : gq.x, w1 = (j & 1) ? gq.w : gq.y;
+    // sign|mantissa byte of a BF16 value x: sign (bit 15) to bit 7, mantissa bits 0-6
+    const uint32_t b0 = ((w0 >> 8) & 0x80u) | (w0 & 0x7Fu), b1 = ((w0 >> 24) & 0x80u) | ((w0 >> 16) & 0x7Fu);
+    const uint32_t b2 = ((w1 >> 8) & 0x80u) | (w1 & 0x7Fu), b3 = ((w1 >> 24) & 0x80u) | ((w1 >> 16) & 0x7Fu);
+    smb[j] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
     const uint32_t sg = smb[j] & 0x80808080u;
     smb[j] = (smb[j] & 0x7F7F7F7Fu) | ((sg << 8) | (sg >> 24));
   }
@@ -177,10 +170,8 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
     for (int gi = 0; gi < 4; ++gi) {
       if (((tagbyte >> (2 * gi)) & 3u) != 2u) continue;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {  // the exponent of element 8gi + j (zero where absent)
-        const int el = 8 * gi + j;
-        escp[r + j] = static_cast<uint8_t>(xw[el >> 1] >> (16 * (el & 1) + 7));
-      }
+      for (int j = 0; j < 8; ++j)  // the exponent of element 8gi + j (zero where absent)
+        escp[r + j] = static_cast<uint8_t>(sh->tile[32 * u + 8 * gi + j] >> 7);
       r += 8;
     }
   }
@@ -253,7 +244,7 @@ struct EncodeArgs {
 };
 
 // grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
-__global__ void __launch_bounds__(kEncThreads, 3) encode_blocks_kernel(EncodeArgs a) {
+__global__ void __launch_bounds__(kEncThreads, 4) encode_blocks_kernel(EncodeArgs a) {
   __shared__ EncShared sh;
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
   const int blk = blockIdx.y, b = blockIdx.z;
