@@ -165,20 +165,40 @@ __device__ __forceinline__ void stage_tile(uint16_t* tile, const uint16_t* src, 
   }
 }
 
+// Row stride (elements) of a token-major tile staged in shared memory: 8
+// elements of padding put consecutive tokens 4 banks apart, so the scattered
+// stores of V units (channels 16m+g, 16m+g+8 of four tokens per lane) spread
+// over the banks.
+constexpr int kLogicalStride = kD + 8;
+constexpr int kLogicalElems = kBlock * kLogicalStride;
+
 // Unit u's rebuilt values (pairs[m] = bf16x2 of storage elements 32u + 2m, +1)
-// into a token-major [64][128] tile in shared memory.
+// into a token-major [64][kLogicalStride] tile in shared memory.
 __device__ __forceinline__ void unit_to_logical(uint16_t* logical, int kind, int u, const uint32_t pairs[16]) {
-  if (kind == 0) {
-    uint4* d = reinterpret_cast<uint4*>(logical + 32 * u);
+  if (kind == 0) {  // token u/4, channels 32(u%4)..+31
+    uint4* d = reinterpret_cast<uint4*>(logical + (u >> 2) * kLogicalStride + 32 * (u & 3));
 #pragma unroll
     for (int i = 0; i < 4; ++i) d[i] = make_uint4(pairs[4 * i], pairs[4 * i + 1], pairs[4 * i + 2], pairs[4 * i + 3]);
   } else {
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
       const int s0 = 32 * u + 2 * m;
-      logical[v_token_of(s0) * kD + v_channel_of(s0)] = static_cast<uint16_t>(pairs[m] & 0xFFFFu);
-      logical[v_token_of(s0 + 1) * kD + v_channel_of(s0 + 1)] = static_cast<uint16_t>(pairs[m] >> 16);
+      logical[v_token_of(s0) * kLogicalStride + v_channel_of(s0)] = static_cast<uint16_t>(pairs[m] & 0xFFFFu);
+      logical[v_token_of(s0 + 1) * kLogicalStride + v_channel_of(s0 + 1)] = static_cast<uint16_t>(pairs[m] >> 16);
     }
+  }
+}
+
+// Copies the staged tile's 64 rows to dst (row t at dst + t * dst_stride elements, 16-byte aligned), rows
+// t < nv only; 256 threads, each store instruction of a warp covering two whole 256-byte rows.
+__device__ __forceinline__ void logical_to_global(const uint16_t* logical, uint16_t* dst, int64_t dst_stride, int nv,
+                                                  int tid) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int idx = tid + 256 * k, t = idx >> 4, c8 = 8 * (idx & 15);
+    if (t < nv)
+      *reinterpret_cast<uint4*>(dst + t * dst_stride + c8) =
+          *reinterpret_cast<const uint4*>(logical + t * kLogicalStride + c8);
   }
 }
 

@@ -31,7 +31,7 @@ struct DecompressArgs {
 
 // grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
 __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs a) {
-  __shared__ alignas(16) uint16_t logical[kBlock * kD];  // [t][c]
+  __shared__ alignas(16) uint16_t logical[kLogicalElems];  // [t][c], padded rows
   __shared__ int word_prefix[65];
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
   const int blk = blockIdx.y, b = blockIdx.z;
@@ -76,13 +76,7 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
   __syncthreads();
   uint16_t* dst = (kind == 0 ? a.k_out : a.v_out) + static_cast<int64_t>(b) * a.seq_stride +
                   static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD;
-  const int t = tid >> 2, part = tid & 3;
-  if (t < nv) {
-    uint4* d = reinterpret_cast<uint4*>(dst + t * a.tok_stride + 32 * part);
-    const uint4* s = reinterpret_cast<const uint4*>(logical + t * kD + 32 * part);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = s[i];
-  }
+  logical_to_global(logical, dst, a.tok_stride, nv, tid);
 }
 
 struct DecodeTilesArgs {
@@ -100,7 +94,7 @@ struct DecodeTilesArgs {
 // grid (n_tiles): one CTA rebuilds one slot image of the batch into its
 // token-major tile (tiles whose esc_len is 0xFFFF are skipped).
 __global__ void __launch_bounds__(kDecThreads) decode_tiles_kernel(DecodeTilesArgs a) {
-  __shared__ alignas(16) uint16_t logical[kBlock * kD];
+  __shared__ alignas(16) uint16_t logical[kLogicalElems];
   __shared__ int word_prefix[65];
   const int64_t i = blockIdx.x;
   const int tid = threadIdx.x;
@@ -119,10 +113,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_tiles_kernel(DecodeTilesAr
     report(a.status, GAAC_EFORMAT);
   unit_to_logical(logical, kind, tid, pairs);
   __syncthreads();
-  const uint4* s = reinterpret_cast<const uint4*>(logical);
-  uint4* d = reinterpret_cast<uint4*>(a.tiles + i * kTile);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) d[tid + kDecThreads * k] = s[tid + kDecThreads * k];
+  logical_to_global(logical, a.tiles + i * kTile, kD, kBlock, tid);
 }
 
 }  // namespace gaac

@@ -267,7 +267,7 @@ __device__ __forceinline__ uint32_t fields_to_bytes(uint32_t g, int w) {
 }
 
 __global__ void __launch_bounds__(kNThreads) nested_decode_kernel(NestedArgs a) {
-  __shared__ alignas(16) uint16_t logical[kBlock * kD];
+  __shared__ alignas(16) uint16_t logical[kLogicalElems];
   const int64_t i = blockIdx.x;
   const int u = threadIdx.x, lane = u & 31, warp = u >> 5;
   const int esc = a.esc_in[i];
@@ -370,10 +370,7 @@ __global__ void __launch_bounds__(kNThreads) nested_decode_kernel(NestedArgs a) 
   if (bad) report(a.status, GAAC_EFORMAT);
   unit_to_logical(logical, kind, u, pairs);
   __syncthreads();
-  const uint4* s = reinterpret_cast<const uint4*>(logical);
-  uint4* d = reinterpret_cast<uint4*>(a.tiles_out + i * kTile);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) d[u + kNThreads * k] = s[u + kNThreads * k];
+  logical_to_global(logical, a.tiles_out + i * kTile, kD, kBlock, u);
 }
 
 }  // namespace gaac
