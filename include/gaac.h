@@ -350,7 +350,7 @@ GAAC_API int gaac_fp8_calibrate(const uint8_t* x, int64_t n_tok, int64_t tok_str
  * Encodes n_tiles FP8 tiles tiles[i][64][128] (token-major; 16-byte aligned)
  * into slots[i][gaac_fp8_slot_bytes(fmt)] (16-byte aligned).  Tile i is K
  * (tile_kind[i] = 0) or V (1) and uses bases row tile_row[i] of base3 / base4
- * ([n_rows][128]).  esc_len[i] receives the escape-area length, or 0xFFFF when
+ * ([n_rows][128], 4-byte aligned).  esc_len[i] receives the escape-area length, or 0xFFFF when
  * the tile does not fit its slot (the caller keeps it as FP8; its slot is not
  * written).  stats may be NULL.  A bad kind or row sets GAAC_EINVAL in
  * *d_status and esc_len[i] = 0xFFFF.

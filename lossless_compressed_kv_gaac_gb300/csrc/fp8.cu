@@ -35,6 +35,7 @@ __host__ __device__ inline bool fp8_layout(int fmt, Fp8Layout* L) {
 }
 
 constexpr int kFp8Threads = 256;
+constexpr int kFp8Stride = kD + 16;  // padded row of a staged FP8 tile: consecutive tokens 4 banks apart
 
 // Calibration: one CTA per row of bases (kv-head), one thread per channel, a
 // histogram of the format's 16 or 32 exponents per channel in shared memory.
@@ -84,16 +85,6 @@ __device__ __forceinline__ void put_field3(uint32_t W[3], int j, uint32_t v) {
     W[h] |= (v & 3u) << (8 * L + 6);
     W[2] |= ((v >> 2) & 1u) << (8 * L + 6 + h);
   }
-}
-
-// Element j's 3-bit field from the unit's three words.
-__device__ __forceinline__ uint32_t field3(const uint32_t W[3], int j) {
-  const int h = j >> 4, jj = j & 15, L = jj & 3, q = jj >> 2;
-  const uint32_t wh = (W[h] >> (8 * L)) & 0xFFu, w2 = (W[2] >> (8 * L)) & 0xFFu;
-  if (q == 0) return wh & 7u;
-  if (q == 1) return (wh >> 3) & 7u;
-  if (q == 2) return (w2 >> (3 * h)) & 7u;
-  return ((wh >> 6) & 3u) | (((w2 >> (6 + h)) & 1u) << 2);
 }
 
 struct Fp8Args {
@@ -278,7 +269,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
 }
 
 __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, uint8_t* __restrict__ out) {
-  __shared__ alignas(16) uint8_t logical[kTile];
+  __shared__ alignas(16) uint8_t logical[kBlock * kFp8Stride];  // token-major, padded rows
   __shared__ int word_prefix[65];
   const int64_t tile = blockIdx.x;
   const int u = threadIdx.x;
@@ -337,43 +328,75 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, 
     S[1] = sw[256 + u];
     S[2] = sw[512 + u];
   }
-  const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
-  const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
-  const uint32_t emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
-  const uint32_t nw[4] = {nib.x, nib.y, nib.z, nib.w};
+  // Four elements per 32-bit word (byte lane L = element 4k + L of the unit), as in the BF16 decoder:
+  // codes and E5M2 sign|mantissa fields come out of their three-word units by byte lanes, E4M3 nibbles by
+  // two masks and a byte permute.
+  uint32_t cq[8], sq[8];
+  extract_codes(C[0], C[2], 0, &cq[0]);
+  extract_codes(C[1], C[2], 1, &cq[4]);
+  if (L.ew == 4) {
+    const uint32_t nw[4] = {nib.x, nib.y, nib.z, nib.w};  // word i: elements 8i..8i+7, low nibble first
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = nw[i] & 0x0F0F0F0Fu, hi = (nw[i] >> 4) & 0x0F0F0F0Fu;
+      sq[2 * i] = __byte_perm(lo, hi, 0x5140);
+      sq[2 * i + 1] = __byte_perm(lo, hi, 0x7362);
+    }
+  } else {
+    extract_codes(S[0], S[2], 0, &sq[0]);
+    extract_codes(S[1], S[2], 1, &sq[4]);
+  }
+  uint32_t b3w[8], b4w[8];
+  unit_base_words(kind, u, a.base3 + static_cast<size_t>(row) * kD, b3w);
+  unit_base_words(kind, u, a.base4 + static_cast<size_t>(row) * kD, b4w);
+  const uint32_t emask_w = ((1u << L.ew) - 1u) * 0x01010101u, mmask_w = ((1u << L.mw) - 1u) * 0x01010101u;
+  uint32_t xw[8];
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     const uint32_t mode = (tagbyte >> (2 * gi)) & 3u;
-    uint32_t x4 = 0;
-    if (mode == 1u) {
+    uint32_t e[2];
+    if (mode == 0u) {
+      e[0] = b3w[2 * gi] + cq[2 * gi];
+      e[1] = b3w[2 * gi + 1] + cq[2 * gi + 1];
+    } else if (mode == 1u) {
+      uint32_t x4 = 0;
       if (o4 < esc_len) x4 = slot[L.off_esc + o4];
       else bad = true;
       o4 += 1;
+      e[0] = b4w[2 * gi] + (cq[2 * gi] | (spread4(x4 & 15u) << 3));
+      e[1] = b4w[2 * gi + 1] + (cq[2 * gi + 1] | (spread4(x4 >> 4) << 3));
+    } else {
+      const bool rawok = mode == 2u && oraw + 8 <= esc_len;
+      if (!rawok) bad = true;
+      e[0] = rawok ? load_u32_any(slot, L.off_esc + oraw) : 0u;
+      e[1] = rawok ? load_u32_any(slot, L.off_esc + oraw + 4) : 0u;
+      oraw += 8;
     }
-    const bool rawok = mode == 2u && oraw + 8 <= esc_len;
-    if (mode == 2u && !rawok) bad = true;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int el = 8 * gi + j, s = 32 * u + el;
-      const int c = fp8_channel_of(kind, s);
-      const uint32_t cd = field3(C, el);
-      uint32_t e;
-      if (mode == 0u) e = b3g[c] + cd;
-      else if (mode == 1u) e = b4g[c] + (cd | (((x4 >> j) & 1u) << 3));
-      else e = rawok ? slot[L.off_esc + oraw + j] : 0u;
-      const uint32_t sm = L.ew == 4 ? (nw[el >> 3] >> (4 * (el & 7))) & 15u : field3(S, el);
-      const uint8_t x = static_cast<uint8_t>(((sm >> L.mw) << 7) | ((e & emask) << L.mw) | (sm & mmask));
-      const int t = kind == 0 ? (s >> 7) : v_token_of(s);
-      logical[t * kD + c] = x;
+    for (int q = 0; q < 2; ++q) {  // FP8 byte: sign (bit mw of sm) to bit 7, exponent, mantissa
+      const uint32_t sm = sq[2 * gi + q];
+      xw[2 * gi + q] = (((sm >> L.mw) & 0x01010101u) << 7) | ((e[q] & emask_w) << L.mw) | (sm & mmask_w);
     }
-    if (mode == 2u) oraw += 8;
   }
   if (bad) report(a.status, GAAC_EFORMAT);
+  if (kind == 0) {  // token u/4, channels 32(u%4)..+31
+    uint4* d = reinterpret_cast<uint4*>(logical + (u >> 2) * kFp8Stride + 32 * (u & 3));
+    d[0] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+    d[1] = make_uint4(xw[4], xw[5], xw[6], xw[7]);
+  } else {
+#pragma unroll
+    for (int el = 0; el < 32; ++el) {
+      const int s = 32 * u + el;
+      logical[v_token_of(s) * kFp8Stride + v_channel_of(s)] = static_cast<uint8_t>(xw[el >> 2] >> (8 * (el & 3)));
+    }
+  }
   __syncthreads();
-  uint4* d = reinterpret_cast<uint4*>(out + tile * kTile);
-  const uint4* s4 = reinterpret_cast<const uint4*>(logical);
-  d[2 * u] = s4[2 * u];
-  d[2 * u + 1] = s4[2 * u + 1];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {  // 64 rows of 128 bytes, a whole row per 8 threads
+    const int idx = u + kFp8Threads * k, t = idx >> 3, c16 = 16 * (idx & 7);
+    *reinterpret_cast<uint4*>(out + tile * kTile + t * kD + c16) =
+        *reinterpret_cast<const uint4*>(logical + t * kFp8Stride + c16);
+  }
 }
 
 }  // namespace gaac
@@ -403,7 +426,9 @@ static int fp8_args(const uint8_t* tiles, int64_t n_tiles, int fmt, const uint8_
   if (tiles == nullptr || tile_kind == nullptr || tile_row == nullptr || base3 == nullptr || base4 == nullptr ||
       slots == nullptr || esc_len == nullptr || n_tiles < 0 || n_tiles > 0x7FFFFFFFLL || n_rows <= 0)
     return GAAC_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(tiles) & 15u) || (reinterpret_cast<uintptr_t>(slots) & 15u)) return GAAC_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(tiles) & 15u) || (reinterpret_cast<uintptr_t>(slots) & 15u) ||
+      (reinterpret_cast<uintptr_t>(base3) & 3u) || (reinterpret_cast<uintptr_t>(base4) & 3u))
+    return GAAC_EINVAL;
   if (!fp8_layout(fmt, &a->L)) return GAAC_EINVAL;
   a->tiles = tiles;
   a->n_tiles = n_tiles;
