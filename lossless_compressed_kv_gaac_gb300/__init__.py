@@ -304,11 +304,33 @@ def fp8_calibrate(x: torch.Tensor, fmt: int, base3: torch.Tensor, base4: torch.T
                                                            _stream(stream)))
 
 
+def _tile_batch(tiles, slots, esc_len, tile_kind, tile_row, bases, elem_bytes: int, slot_bytes: int) -> int:
+    """Checks a tile batch's tensors (device, contiguity, shapes, element sizes) and returns n."""
+    n = tiles.shape[0] if tiles.dim() == 3 else -1
+    for t, name in ((tiles, "tiles"), (slots, "slots"), (esc_len, "esc_len"), (tile_kind, "tile_kind"),
+                    (tile_row, "tile_row"), *((b, "base") for b in bases)):
+        _cuda(t, name)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if tiles.dim() != 3 or tuple(tiles.shape[1:]) != (BLOCK, HEAD_DIM) or tiles.element_size() != elem_bytes:
+        raise ValueError(f"tiles must be [n, {BLOCK}, {HEAD_DIM}] of {elem_bytes}-byte elements")
+    if tuple(slots.shape) != (n, slot_bytes) or slots.element_size() != 1:
+        raise ValueError(f"slots must be uint8 [n, {slot_bytes}]")
+    if esc_len.numel() != n or esc_len.element_size() != 2:
+        raise ValueError("esc_len must hold n 16-bit values")
+    if tile_kind.numel() != n or tile_kind.element_size() != 1 or tile_row.numel() != n or tile_row.dtype != torch.int32:
+        raise ValueError("tile_kind must be uint8 [n] and tile_row int32 [n]")
+    for b in bases:
+        if b.dim() != 2 or b.shape[1] != HEAD_DIM or b.element_size() != 1 or b.shape[0] != bases[0].shape[0]:
+            raise ValueError("bases must be uint8 [rows, 128], all with the same rows")
+    return n
+
+
 def fp8_encode_tiles(tiles, fmt: int, tile_kind, tile_row, base3, base4, slots, esc_len, stats=None, status=None,
                      stream=None) -> None:
     """tiles: uint8 [n, 64, 128]; tile_kind: uint8 [n] (0 K, 1 V); tile_row: int32 [n] (row of base3/base4
     [rows, 128]); slots: uint8 [n, fp8_slot_bytes(fmt)]; esc_len: int16 [n] (0xFFFF = stays FP8)."""
-    n = tiles.shape[0]
+    n = _tile_batch(tiles, slots, esc_len, tile_kind, tile_row, (base3, base4), 1, fp8_slot_bytes(fmt))
     _check("gaac_fp8_encode_tiles", lib().gaac_fp8_encode_tiles(
         tiles.data_ptr(), n, fmt, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0], base3.data_ptr(),
         base4.data_ptr(), slots.data_ptr(), esc_len.data_ptr(), _ptr(stats), _ptr(status), _stream(stream)))
@@ -316,7 +338,7 @@ def fp8_encode_tiles(tiles, fmt: int, tile_kind, tile_row, base3, base4, slots, 
 
 def fp8_decompress_tiles(slots, esc_len, fmt: int, tile_kind, tile_row, base3, base4, tiles, status=None,
                          stream=None) -> None:
-    n = tiles.shape[0]
+    n = _tile_batch(tiles, slots, esc_len, tile_kind, tile_row, (base3, base4), 1, fp8_slot_bytes(fmt))
     _check("gaac_fp8_decompress_tiles", lib().gaac_fp8_decompress_tiles(
         slots.data_ptr(), esc_len.data_ptr(), n, fmt, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
         base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status), _stream(stream)))
@@ -327,15 +349,17 @@ def encode_tiles(tiles, tile_kind, tile_row, base3, base4, slots, esc_len, stats
     """Format v3 tile batch.  tiles: BF16 [n, 64, 128] token-major; tile_kind: uint8 [n] (0 K, 1 V);
     tile_row: int32 [n] (row of base3/base4 [rows, 128]); slots: uint8 [n, SLOT_BYTES]; esc_len: int16 [n]
     (0xFFFF: does not fit, slot untouched)."""
+    n = _tile_batch(tiles, slots, esc_len, tile_kind, tile_row, (base3, base4), 2, SLOT_BYTES)
     _check("gaac_encode_tiles", lib().gaac_encode_tiles(
-        tiles.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
+        tiles.data_ptr(), n, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
         base3.data_ptr(), base4.data_ptr(), slots.data_ptr(), esc_len.data_ptr(), _ptr(stats), _ptr(status),
         _stream(stream)))
 
 
 def decode_tiles(slots, esc_len, tile_kind, tile_row, base3, base4, tiles, status=None, stream=None) -> None:
+    n = _tile_batch(tiles, slots, esc_len, tile_kind, tile_row, (base3, base4), 2, SLOT_BYTES)
     _check("gaac_decode_tiles", lib().gaac_decode_tiles(
-        slots.data_ptr(), esc_len.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(),
+        slots.data_ptr(), esc_len.data_ptr(), n, tile_kind.data_ptr(), tile_row.data_ptr(),
         base3.shape[0], base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status), _stream(stream)))
 
 
@@ -354,16 +378,18 @@ def nested_calibrate(x: torch.Tensor, base2: torch.Tensor, status=None, stream=N
 def nested_encode_tiles(tiles, tile_kind, tile_row, base2, base3, base4, slots, esc_len, status=None,
                         stream=None) -> None:
     """Nested 2-bit-mode ablation format; arguments as encode_tiles, slots [n, NESTED_SLOT_BYTES]."""
+    n = _tile_batch(tiles, slots, esc_len, tile_kind, tile_row, (base2, base3, base4), 2, NESTED_SLOT_BYTES)
     _check("gaac_nested_encode_tiles", lib().gaac_nested_encode_tiles(
-        tiles.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
+        tiles.data_ptr(), n, tile_kind.data_ptr(), tile_row.data_ptr(), base3.shape[0],
         base2.data_ptr(), base3.data_ptr(), base4.data_ptr(), slots.data_ptr(), esc_len.data_ptr(), _ptr(status),
         _stream(stream)))
 
 
 def nested_decode_tiles(slots, esc_len, tile_kind, tile_row, base2, base3, base4, tiles, status=None,
                         stream=None) -> None:
+    n = _tile_batch(tiles, slots, esc_len, tile_kind, tile_row, (base2, base3, base4), 2, NESTED_SLOT_BYTES)
     _check("gaac_nested_decode_tiles", lib().gaac_nested_decode_tiles(
-        slots.data_ptr(), esc_len.data_ptr(), tiles.shape[0], tile_kind.data_ptr(), tile_row.data_ptr(),
+        slots.data_ptr(), esc_len.data_ptr(), n, tile_kind.data_ptr(), tile_row.data_ptr(),
         base3.shape[0], base2.data_ptr(), base3.data_ptr(), base4.data_ptr(), tiles.data_ptr(), _ptr(status),
         _stream(stream)))
 
