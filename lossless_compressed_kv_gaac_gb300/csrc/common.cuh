@@ -242,13 +242,13 @@ __device__ __forceinline__ void slot_word_prefix(const uint8_t* slot, int lane, 
 
 // Rebuilds code unit u (storage elements 32u..32u+31) of a slot image into
 // pairs[m] = bf16x2 of storage elements 32u + 2m, 32u + 2m + 1.  word_prefix:
-// slot_word_prefix's output for this image; b3g/b4g: the 128 bases of the
-// tile's (kv-head, K|V).  Returns true when the unit fails a check of the
-// format (a reserved tag, an escape read past esc_len, a directory entry or the
-// totals differing from the tags).
-__device__ __forceinline__ bool decode_slot_unit(const uint8_t* slot, int kind, int u, const uint8_t* b3g,
-                                                 const uint8_t* b4g, int esc_len, const int* word_prefix,
-                                                 uint32_t pairs[16]) {
+// slot_word_prefix's output for this image; b3w/b4w: the unit's base words
+// (word k = elements 4k..4k+3, unit_base_words' layout).  Returns true when the
+// unit fails a check of the format (a reserved tag, an escape read past
+// esc_len, a directory entry or the totals differing from the tags).
+__device__ __forceinline__ bool decode_slot_unit_w(const uint8_t* slot, int u, const uint32_t b3w[8],
+                                                   const uint32_t b4w[8], int esc_len, const int* word_prefix,
+                                                   uint32_t pairs[16]) {
   const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + kOffTag);
   const uint32_t* cw = reinterpret_cast<const uint32_t*>(slot + kOffCode);
   const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
@@ -277,23 +277,8 @@ __device__ __forceinline__ bool decode_slot_unit(const uint8_t* slot, int kind, 
   }
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
-    uint32_t b3[4], b4[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (kind == 0) {  // K: element 4q+L of half hh is channel 32(u%4) + 16hh + 4q + L
-        const int c = 32 * (u & 3) + 16 * hh + 4 * q;
-        b3[q] = *reinterpret_cast<const uint32_t*>(b3g + c);
-        b4[q] = *reinterpret_cast<const uint32_t*>(b4g + c);
-      } else {  // V: element 4q+L of half hh is storage element 32u + 16hh + 4q + L
-        b3[q] = b4[q] = 0u;
-#pragma unroll
-        for (int L = 0; L < 4; ++L) {
-          const int c = v_channel_of(32 * u + 16 * hh + 4 * q + L);
-          b3[q] |= static_cast<uint32_t>(b3g[c]) << (8 * L);
-          b4[q] |= static_cast<uint32_t>(b4g[c]) << (8 * L);
-        }
-      }
-    }
+    const uint32_t b3[4] = {b3w[4 * hh], b3w[4 * hh + 1], b3w[4 * hh + 2], b3w[4 * hh + 3]};
+    const uint32_t b4[4] = {b4w[4 * hh], b4w[4 * hh + 1], b4w[4 * hh + 2], b4w[4 * hh + 3]};
     uint32_t e[4];
     half_exponents_v3(hh == 0 ? W0 : W1, W2, hh, (tagbyte >> (4 * hh)) & 15u, b3, b4, slot, &o4, &oraw, esc_len, e,
                       &bad);
@@ -301,6 +286,34 @@ __device__ __forceinline__ bool decode_slot_unit(const uint8_t* slot, int kind, 
     for (int q = 0; q < 4; ++q) join_bf16x4(smw[4 * hh + q], e[q], pairs[8 * hh + 2 * q], pairs[8 * hh + 2 * q + 1]);
   }
   return bad;
+}
+
+// As decode_slot_unit_w, with the unit's base words read from the tile's 128
+// bases b3g/b4g (K: word loads; V: byte gathers).
+__device__ __forceinline__ bool decode_slot_unit(const uint8_t* slot, int kind, int u, const uint8_t* b3g,
+                                                 const uint8_t* b4g, int esc_len, const int* word_prefix,
+                                                 uint32_t pairs[16]) {
+  uint32_t b3w[8], b4w[8];
+  unit_base_words(kind, u, b3g, b3w);
+  unit_base_words(kind, u, b4g, b4w);
+  return decode_slot_unit_w(slot, u, b3w, b4w, esc_len, word_prefix, pairs);
+}
+
+// A V unit u's element 4k+L has channel v_channel_of(32u + 4k + L), which
+// depends on u only through h = (u >> 5) & 1 and g = (u >> 2) & 7: 16 classes.
+__device__ __forceinline__ int v_unit_class(int u) { return 8 * ((u >> 5) & 1) + ((u >> 2) & 7); }
+
+// Base words of the 16 V unit classes, table[0 base3 | 1 base4][class][k]; one
+// word per thread of 256.
+__device__ __forceinline__ void fill_v_base_table(uint32_t (*table)[16][8], const uint8_t* b3g, const uint8_t* b4g,
+                                                  int tid) {
+  const int which = tid >> 7, cls = (tid >> 3) & 15, k = tid & 7;
+  const int urep = 32 * (cls >> 3) + 4 * (cls & 7);  // a unit of the class
+  const uint8_t* bg = which ? b4g : b3g;
+  uint32_t w = 0u;
+#pragma unroll
+  for (int L = 0; L < 4; ++L) w |= static_cast<uint32_t>(bg[v_channel_of(32 * urep + 4 * k + L)]) << (8 * L);
+  table[which][cls][k] = w;
 }
 
 // ------------------------------------------------------- mbarrier / bulk ----

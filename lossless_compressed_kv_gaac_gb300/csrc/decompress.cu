@@ -33,6 +33,7 @@ struct DecompressArgs {
 __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs a) {
   __shared__ alignas(16) uint16_t logical[kLogicalElems];  // [t][c], padded rows
   __shared__ int word_prefix[65];
+  __shared__ uint32_t vbt[2][16][8];  // V: base words of the unit classes
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
   const int blk = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, u = tid;
@@ -66,10 +67,14 @@ __global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs 
     }
   } else {
     const uint8_t* slot = a.slot_pool + static_cast<size_t>(ent.index) * kSlot;
+    const uint8_t* b3g = a.base3 + (kind * a.n_kv_heads + h) * kD;
+    const uint8_t* b4g = a.base4 + (kind * a.n_kv_heads + h) * kD;
     if (tid < 32) slot_word_prefix(slot, tid, word_prefix);
+    if (kind == 1) fill_v_base_table(vbt, b3g, b4g, tid);
     __syncthreads();
-    const bool bad = decode_slot_unit(slot, kind, u, a.base3 + (kind * a.n_kv_heads + h) * kD,
-                                      a.base4 + (kind * a.n_kv_heads + h) * kD, ent.esc_len, word_prefix, pairs);
+    const int cls = v_unit_class(u);
+    const bool bad = kind == 0 ? decode_slot_unit(slot, 0, u, b3g, b4g, ent.esc_len, word_prefix, pairs)
+                               : decode_slot_unit_w(slot, u, vbt[0][cls], vbt[1][cls], ent.esc_len, word_prefix, pairs);
     if (bad) report(a.status, GAAC_EFORMAT);
   }
   unit_to_logical(logical, kind, u, pairs);  // storage order -> token-major
@@ -96,6 +101,7 @@ struct DecodeTilesArgs {
 __global__ void __launch_bounds__(kDecThreads) decode_tiles_kernel(DecodeTilesArgs a) {
   __shared__ alignas(16) uint16_t logical[kLogicalElems];
   __shared__ int word_prefix[65];
+  __shared__ uint32_t vbt[2][16][8];  // V: base words of the unit classes
   const int64_t i = blockIdx.x;
   const int tid = threadIdx.x;
   const int esc = a.esc_len[i];
@@ -107,10 +113,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_tiles_kernel(DecodeTilesAr
   }
   const uint8_t* slot = a.slots + i * kSlot;
   if (tid < 32) slot_word_prefix(slot, tid, word_prefix);
+  if (kind == 1) fill_v_base_table(vbt, a.base3 + r * kD, a.base4 + r * kD, tid);
   __syncthreads();
   uint32_t pairs[16];
-  if (decode_slot_unit(slot, kind, tid, a.base3 + r * kD, a.base4 + r * kD, esc, word_prefix, pairs))
-    report(a.status, GAAC_EFORMAT);
+  const int cls = v_unit_class(tid);
+  const bool bad = kind == 0 ? decode_slot_unit(slot, 0, tid, a.base3 + r * kD, a.base4 + r * kD, esc, word_prefix, pairs)
+                             : decode_slot_unit_w(slot, tid, vbt[0][cls], vbt[1][cls], esc, word_prefix, pairs);
+  if (bad) report(a.status, GAAC_EFORMAT);
   unit_to_logical(logical, kind, tid, pairs);
   __syncthreads();
   logical_to_global(logical, a.tiles + i * kTile, kD, kBlock, tid);

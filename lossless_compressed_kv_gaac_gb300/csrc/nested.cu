@@ -268,6 +268,8 @@ __device__ __forceinline__ uint32_t fields_to_bytes(uint32_t g, int w) {
 
 __global__ void __launch_bounds__(kNThreads) nested_decode_kernel(NestedArgs a) {
   __shared__ alignas(16) uint16_t logical[kLogicalElems];
+  __shared__ uint32_t vbt[2][16][8];  // V: base3 / base4 words of the unit classes
+  __shared__ uint32_t vbt2[16][8];    // V: base2 words
   const int64_t i = blockIdx.x;
   const int u = threadIdx.x, lane = u & 31, warp = u >> 5;
   const int esc = a.esc_in[i];
@@ -278,6 +280,16 @@ __global__ void __launch_bounds__(kNThreads) nested_decode_kernel(NestedArgs a) 
     return;
   }
   const uint8_t* slot = a.slots_in + i * kNSlot;
+  if (kind == 1) {  // V base words of the 16 unit classes (base3, base4, then base2)
+    fill_v_base_table(vbt, a.base3 + r * kD, a.base4 + r * kD, u);
+    if (u < 128) {
+      const int cls = (u >> 3) & 15, k = u & 7, urep = 32 * (cls >> 3) + 4 * (cls & 7);
+      uint32_t w = 0u;
+#pragma unroll
+      for (int L = 0; L < 4; ++L) w |= static_cast<uint32_t>(a.base2[r * kD + v_channel_of(32 * urep + 4 * k + L)]) << (8 * L);
+      vbt2[cls][k] = w;
+    }
+  }
   const uint32_t* dir = reinterpret_cast<const uint32_t*>(slot + kNOffDir);
   const uint32_t tagbyte = slot[kNOffTag + u];
   int bits_u = 0, n4 = 0, nraw = 0;
@@ -321,9 +333,20 @@ __global__ void __launch_bounds__(kNThreads) nested_decode_kernel(NestedArgs a) 
   }
   const uint64_t lo = static_cast<uint64_t>(x0) | (static_cast<uint64_t>(x1) << 32);
   uint32_t b2w[8], b3w[8], b4w[8];
-  unit_base_words(kind, u, a.base2 + r * kD, b2w);
-  unit_base_words(kind, u, a.base3 + r * kD, b3w);
-  unit_base_words(kind, u, a.base4 + r * kD, b4w);
+  if (kind == 0) {
+    unit_base_words(0, u, a.base2 + r * kD, b2w);
+    unit_base_words(0, u, a.base3 + r * kD, b3w);
+    unit_base_words(0, u, a.base4 + r * kD, b4w);
+  } else {  // V: from the table of the 16 unit classes, as the format-v3 decoder
+    __syncthreads();
+    const int cls = v_unit_class(u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      b2w[k] = vbt2[cls][k];
+      b3w[k] = vbt[0][cls][k];
+      b4w[k] = vbt[1][cls][k];
+    }
+  }
   const uint4* smp = reinterpret_cast<const uint4*>(slot + 32 * u);
   const uint4 s0 = smp[0], s1 = smp[1];
   uint32_t smw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
