@@ -149,7 +149,8 @@ GAAC_API int gaac_calibrate(const uint16_t* x, int64_t n_tok, int64_t tok_stride
  * kernel; used as the uncompressed baseline).
  * k, v: BF16 bits, element (b, t, h, c) at b*seq_stride + t*tok_stride + h*128 + c.
  * base3/base4: [2][n_kv_heads][128] bytes (index 0 = K, 1 = V), 16-byte aligned.
- * k and v must be 16-byte aligned and both strides multiples of 8 elements.
+ * k and v must be 16-byte aligned and both strides multiples of 8 elements
+ * (a misaligned pointer or stride returns GAAC_EINVAL).
  * n_tok: tokens present per sequence in k and v.  Each seq_lens[b] must be
  * <= min(n_tok, max_blocks*64); otherwise GAAC_EINVAL goes to *d_status and the
  * sequence is left out (its entries become GAAC_MODE_NONE).
@@ -171,6 +172,7 @@ GAAC_API int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t se
  * handed to block blk+1 as its tail; if not, the block stays RAW.  Finally
  * seq_lens[b] += 1 (a second small kernel on the same stream).
  * seq_lens[b] must be < max_blocks*64 (else GAAC_EINVAL in *d_status).
+ * base3/base4 as for gaac_encode_blocks (16-byte aligned, else GAAC_EINVAL).
  */
 GAAC_API int gaac_append(const uint16_t* k_new, const uint16_t* v_new, int32_t* seq_lens, int batch, int n_kv_heads,
                 int max_blocks, const uint8_t* base3, const uint8_t* base4, gaac_entry* table,

@@ -25,6 +25,7 @@ constexpr int kEncThreads = 256;
 
 struct EncShared {
   alignas(16) uint16_t tile[kTile];  // tile in storage order
+  uint32_t vtab[2][16][8];           // V: base3 / base4 words of the 16 unit classes
   int warp_sums[kEncThreads / 32];
   int mode_counts[4];
   uint32_t raw_idx;
@@ -55,6 +56,11 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
   const int lane = u & 31, warp = u >> 5;
   const uint4* src = reinterpret_cast<const uint4*>(sh->tile + 32 * u);  // the unit's 32 values, 4 quads of 8
   if (u < 4) sh->mode_counts[u] = 0;
+  if (kind == 1) {  // V bases by unit class (kind is the same for the whole CTA)
+    fill_v_base_table(sh->vtab, b3g, b4g, u);
+    __syncthreads();
+  }
+  const int cls = v_unit_class(u);
 
   uint32_t W[3] = {0, 0, 0};  // the unit's code-plane words, filled code by code
   uint32_t esc4 = 0;  // the unit's 4-bit escape bytes, little-endian, in group order
@@ -69,15 +75,28 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
     bool fits3 = true, fits4 = true;
     const uint4 gq = src[gi];  // the group's 8 values
     const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+    uint32_t b3q[2], b4q[2];  // the group's bases, four per word
+    if (kind == 0) {  // K: channels 32(u%4) + 8gi .. + 7 (bases are 4-byte aligned)
+      const uint32_t* w3 = reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 8 * gi);
+      const uint32_t* w4 = reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 8 * gi);
+      b3q[0] = w3[0];
+      b3q[1] = w3[1];
+      b4q[0] = w4[0];
+      b4q[1] = w4[1];
+    } else {
+      b3q[0] = sh->vtab[0][cls][2 * gi];
+      b3q[1] = sh->vtab[0][cls][2 * gi + 1];
+      b4q[0] = sh->vtab[1][cls][2 * gi];
+      b4q[1] = sh->vtab[1][cls][2 * gi + 1];
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int el = 8 * gi + j;
       pres[j] = !kOpen || token_of(kind, 32 * u + el) < n_present;
       const uint32_t x = (gw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
       e[j] = (x >> 7) & 0xFF;
-      const int c = channel_of(kind, 32 * u + el);
-      b3[j] = b3g[c];
-      b4[j] = b4g[c];
+      b3[j] = (b3q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      b4[j] = (b4q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
       const int o3 = e[j] - b3[j], o4 = e[j] - b4[j];
       fits3 = fits3 && (!pres[j] || ((o3 >= 0) && (o3 <= 7)));
       fits4 = fits4 && (!pres[j] || ((o4 >= 0) && (o4 <= 15)));
@@ -829,7 +848,8 @@ extern "C" int gaac_encode_blocks_ex(const uint16_t* k, const uint16_t* v, int64
       n_kv_heads > 1024)
     return GAAC_EINVAL;
   if (tok_stride < static_cast<int64_t>(n_kv_heads) * kD || (tok_stride & 7) || (seq_stride & 7) ||
-      (reinterpret_cast<uintptr_t>(k) & 15u) || (reinterpret_cast<uintptr_t>(v) & 15u))
+      (reinterpret_cast<uintptr_t>(k) & 15u) || (reinterpret_cast<uintptr_t>(v) & 15u) ||
+      (reinterpret_cast<uintptr_t>(base3) & 15u) || (reinterpret_cast<uintptr_t>(base4) & 15u))
     return GAAC_EINVAL;
   if (n_tok < 0) return GAAC_EINVAL;
   EncodeArgs a{k, v, seq_stride, tok_stride, n_tok, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids,
@@ -857,6 +877,7 @@ extern "C" int gaac_append_ex(const uint16_t* k_new, const uint16_t* v_new, int3
       (flags & ~static_cast<unsigned>(GAAC_OPEN_COMPRESSED)))
     return GAAC_EINVAL;
   if (batch <= 0 || batch > 65535 || n_kv_heads <= 0 || n_kv_heads > 1024 || max_blocks <= 0) return GAAC_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(base3) & 15u) || (reinterpret_cast<uintptr_t>(base4) & 15u)) return GAAC_EINVAL;
   AppendArgs a{k_new, v_new, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids, *pools,
                stats, flags, d_status};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
