@@ -71,8 +71,6 @@ __global__ void __launch_bounds__(kD) fp8_calibrate_kernel(const uint8_t* __rest
   base4[h * kD + c] = static_cast<uint8_t>(arg4);
 }
 
-__device__ __forceinline__ int fp8_channel_of(int kind, int s) { return kind == 0 ? (s & 127) : v_channel_of(s); }
-
 // Adds element j's 3-bit field v to the unit's three words (format v3's code-plane placement: element
 // 16h + 4q + L in byte lane L of W[h] at bits 0-2 (q = 0) or 3-5 (q = 1), of W[2] at bits 3h.. (q = 2), or
 // split as bits 6-7 of W[h] and bit 6+h of W[2] (q = 3)).
@@ -104,6 +102,7 @@ struct Fp8Args {
 
 __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
   __shared__ alignas(16) uint8_t seq[kTile];  // the tile in storage order
+  __shared__ uint32_t vtab[2][16][8];         // V: base3 / base4 words of the 16 unit classes
   __shared__ int warp_sums[kFp8Threads / 32];
   __shared__ int mode_counts[4];
   const int64_t tile = blockIdx.x;
@@ -133,10 +132,12 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
       for (int i = 0; i < 32; ++i) seq[v_storage_index(t, c0 + i)] = i < 16 ? xb0[i] : xb1[i - 16];
     }
   }
-  if (u < 4) mode_counts[u] = 0;
-  __syncthreads();
   const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
   const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
+  if (kind == 1) fill_v_base_table(vtab, b3g, b4g, u);
+  if (u < 4) mode_counts[u] = 0;
+  __syncthreads();
+  const int cls = v_unit_class(u);
   const uint32_t emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
   uint32_t CW[3] = {0u, 0u, 0u};  // code-plane words, filled field by field
   uint32_t SW[4] = {0u, 0u, 0u, 0u};  // sign|mantissa: nibbles (E4M3) or 3-bit fields in SW[0..2] (E5M2)
@@ -147,6 +148,20 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
     uint32_t e[8];
     int b3[8], b4[8];
     bool fits3 = true, fits4 = true;
+    uint32_t b3q[2], b4q[2];  // the group's bases, four per word
+    if (kind == 0) {  // K: channels 32(u%4) + 8gi .. + 7 (bases are 4-byte aligned)
+      const uint32_t* w3 = reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 8 * gi);
+      const uint32_t* w4 = reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 8 * gi);
+      b3q[0] = w3[0];
+      b3q[1] = w3[1];
+      b4q[0] = w4[0];
+      b4q[1] = w4[1];
+    } else {
+      b3q[0] = vtab[0][cls][2 * gi];
+      b3q[1] = vtab[0][cls][2 * gi + 1];
+      b4q[0] = vtab[1][cls][2 * gi];
+      b4q[1] = vtab[1][cls][2 * gi + 1];
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int el = 8 * gi + j;
@@ -157,9 +172,8 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
         SW[el >> 3] |= smv << (4 * (el & 7));
       else
         put_field3(SW, el, smv);
-      const int c = fp8_channel_of(kind, 32 * u + el);
-      b3[j] = b3g[c];
-      b4[j] = b4g[c];
+      b3[j] = (b3q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      b4[j] = (b4q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
       const int o3 = static_cast<int>(e[j]) - b3[j], o4 = static_cast<int>(e[j]) - b4[j];
       fits3 = fits3 && o3 >= 0 && o3 <= 7;
       fits4 = fits4 && o4 >= 0 && o4 <= 15;
@@ -270,6 +284,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
 
 __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, uint8_t* __restrict__ out) {
   __shared__ alignas(16) uint8_t logical[kBlock * kFp8Stride];  // token-major, padded rows
+  __shared__ uint32_t vtab[2][16][8];  // V: base3 / base4 words of the 16 unit classes
   __shared__ int word_prefix[65];
   const int64_t tile = blockIdx.x;
   const int u = threadIdx.x;
@@ -283,6 +298,9 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, 
   const Fp8Layout L = a.L;
   const uint8_t* slot = a.slots + tile * L.slot;
   const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + L.off_tag);
+  const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
+  const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
+  if (kind == 1) fill_v_base_table(vtab, b3g, b4g, u);
   if (u < 32) {  // exclusive prefixes of 4-bit and raw group counts over the 64 tag words (packed)
     const int c0 = n4_of(tagw[u]) | (nraw_of(tagw[u]) << 16);
     const int c1 = n4_of(tagw[u + 32]) | (nraw_of(tagw[u + 32]) << 16);
@@ -347,8 +365,17 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, 
     extract_codes(S[1], S[2], 1, &sq[4]);
   }
   uint32_t b3w[8], b4w[8];
-  unit_base_words(kind, u, a.base3 + static_cast<size_t>(row) * kD, b3w);
-  unit_base_words(kind, u, a.base4 + static_cast<size_t>(row) * kD, b4w);
+  if (kind == 0) {
+    unit_base_words(0, u, b3g, b3w);
+    unit_base_words(0, u, b4g, b4w);
+  } else {
+    const int cls = v_unit_class(u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      b3w[k] = vtab[0][cls][k];
+      b4w[k] = vtab[1][cls][k];
+    }
+  }
   const uint32_t emask_w = ((1u << L.ew) - 1u) * 0x01010101u, mmask_w = ((1u << L.mw) - 1u) * 0x01010101u;
   uint32_t xw[8];
 #pragma unroll
