@@ -55,3 +55,27 @@ def test_null_arguments_rejected_on_host(lib):
                                   None) == EINVAL
     lib.gaac_calibrate.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P, P, P]
     assert lib.gaac_calibrate(None, 10, 1024, 8, None, None, None, None) == EINVAL
+
+
+class _Pools(ctypes.Structure):
+    _fields_ = [("slot_pool", ctypes.c_void_p), ("n_slots", ctypes.c_int64), ("raw_pool", ctypes.c_void_p),
+                ("n_raw", ctypes.c_int64), ("raw_free", ctypes.c_void_p), ("n_raw_free", ctypes.c_int64),
+                ("raw_cursor", ctypes.c_void_p)]
+
+
+def test_misaligned_bases_rejected_on_host(lib):
+    # The block encoder and the append read a K group's bases as words, so both
+    # require 16-byte aligned base rows (gaac.h) and refuse others before any
+    # launch; the pointers below are never dereferenced.
+    P = ctypes.c_void_p
+    EINVAL = 1
+    good, odd = 0x10000, 0x10004
+    pools = _Pools(good, 4, good, 4, None, 4, good)
+    lib.gaac_encode_blocks.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P]
+    lib.gaac_append.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P, P]
+    for b3, b4 in ((odd, good), (good, odd)):
+        assert lib.gaac_encode_blocks(good, good, 1024, 1024, 64, good, 1, 8, 1, b3, b4, good, good,
+                                      ctypes.byref(pools), None, good, None) == EINVAL
+        assert lib.gaac_append(good, good, good, 1, 8, 1, b3, b4, good, good, ctypes.byref(pools), None, good,
+                               None) == EINVAL
