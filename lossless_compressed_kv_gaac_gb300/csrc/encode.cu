@@ -38,6 +38,64 @@ __device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? 
 // Token of storage element s (format v3).
 __device__ __forceinline__ int token_of(int kind, int s) { return kind == 0 ? (s >> 7) : v_token_of(s); }
 
+// Stages tokens [0, nv) of a tile (token t's 128 channels at src + t * tok_stride,
+// 16-byte aligned) into `tile` in storage order; tokens past nv are zero.
+//  K (token-major storage): 16-byte chunk q = tid + 256i is token q / 16,
+//    channels 8(q % 16) .. +7, so a warp's loads and stores are contiguous.
+//  V: storage elements 2m and 2m+1 are channels c and c+8 of one token, so a
+//    thread takes token t, channels 32p .. 32p+31 and stores each such pair as
+//    one word; the thread -> (t, p) assignment puts a warp's 32 stores of an
+//    instruction in 16 distinct banks.
+__device__ __forceinline__ void stage_tile_enc(uint16_t* tile, const uint16_t* src, int64_t tok_stride, int nv,
+                                               int kind, int tid) {
+  if (kind == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int q = tid + kEncThreads * i, t = q >> 4, col = 8 * (q & 15);
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (t < nv) x = *reinterpret_cast<const uint4*>(src + t * tok_stride + col);
+      *reinterpret_cast<uint4*>(tile + t * kD + col) = x;
+    }
+    return;
+  }
+  const int l = tid & 31, w = tid >> 5;
+  const int t = (l & 1) | (((l >> 3) & 1) << 1) | (((l >> 4) & 1) << 2) | (((l >> 1) & 1) << 3) | ((w & 3) << 4);
+  const int p = ((l >> 2) & 1) | (((w >> 2) & 1) << 1);
+  uint4 x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = make_uint4(0, 0, 0, 0);
+  if (t < nv) {
+    const uint4* g = reinterpret_cast<const uint4*>(src + t * tok_stride + 32 * p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = g[i];
+  }
+  // word index of storage element v_storage_index(t, 32p + 16m + j) / 2 = base + 64j + 4m (j < 8)
+  const int base = 1024 * (t >> 4) + 512 * (p >> 1) + 16 * ((t >> 1) & 3) + 8 * (p & 1) + (t & 1) + 2 * ((t >> 3) & 1);
+  uint32_t* tw = reinterpret_cast<uint32_t*>(tile);
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const uint32_t aw[4] = {x[2 * m].x, x[2 * m].y, x[2 * m].z, x[2 * m].w};          // channels c
+    const uint32_t bw[4] = {x[2 * m + 1].x, x[2 * m + 1].y, x[2 * m + 1].z, x[2 * m + 1].w};  // c + 8
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      tw[base + 64 * (2 * i) + 4 * m] = __byte_perm(aw[i], bw[i], 0x5410);
+      tw[base + 64 * (2 * i + 1) + 4 * m] = __byte_perm(aw[i], bw[i], 0x7632);
+    }
+  }
+}
+
+// Exponent bytes of four BF16 values (w0 = elements 0, 1; w1 = elements 2, 3):
+// byte L = exponent of element L.
+__device__ __forceinline__ uint32_t exponent_word(uint32_t w0, uint32_t w1) {
+  const uint32_t lo = __byte_perm(w0, w1, 0x6420), hi = __byte_perm(w0, w1, 0x7531);
+  return ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
+}
+
+// The 4-bit escape nibble of a word of 4-bit offsets: bit L = bit 3 of byte L.
+__device__ __forceinline__ uint32_t escape_nibble(uint32_t d4) {
+  return (((d4 >> 3) & 0x01010101u) * 0x01020408u) >> 24;
+}
+
 // Encodes the tile in sh->tile into `slot` (global, 16-byte aligned) unless its
 // escape stream exceeds the capacity.  Returns the escape length, or -1 when
 // the tile must stay raw (then nothing is written).  CTA-uniform result; all
@@ -56,10 +114,18 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
   const int lane = u & 31, warp = u >> 5;
   const uint4* src = reinterpret_cast<const uint4*>(sh->tile + 32 * u);  // the unit's 32 values, 4 quads of 8
   if (u < 4) sh->mode_counts[u] = 0;
-  if (kind == 1) {  // V bases by unit class (kind is the same for the whole CTA)
-    fill_v_base_table(sh->vtab, b3g, b4g, u);
-    __syncthreads();
+  if (kind == 1) fill_v_base_table(sh->vtab, b3g, b4g, u);  // V bases by unit class (kind is CTA-uniform)
+  // Calibrated bases lie in [0, 248] (base3) and [0, 240] (base4); for those a
+  // word subtraction decides a group's fit exactly (below).  Other bases take
+  // the element-by-element path.
+  bool odd_base = false;
+  if (u < kD / 4) {
+    const uint32_t w3 = reinterpret_cast<const uint32_t*>(b3g)[u], w4 = reinterpret_cast<const uint32_t*>(b4g)[u];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) odd_base = odd_base || ((w3 >> (8 * L)) & 0xFFu) > 248u || ((w4 >> (8 * L)) & 0xFFu) > 240u;
   }
+  const bool any_odd = __syncthreads_or(odd_base) != 0;  // also orders the V table's writes before its reads
+  const bool word_fit = !kOpen && !any_odd;
   const int cls = v_unit_class(u);
 
   uint32_t W[3] = {0, 0, 0};  // the unit's code-plane words, filled code by code
@@ -68,6 +134,56 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
   uint32_t tagbyte = 0;
   int my_counts[3] = {0, 0, 0};
 
+  if (word_fit) {
+    // Four elements per word: E = exponent bytes, D = E - base.  With every
+    // base3 <= 248, a group fits the 3-bit mode iff no byte of E - base3 (either
+    // word) has a bit above bit 2: when all bytes are in [0, 7] nothing
+    // borrows, and the lowest byte that is out of range is exact modulo 256 and
+    // lies in [8, 255] (a negative offset is at least -248).  Likewise 4 bits
+    // with base4 <= 240.  In a group that fits, D holds the offsets themselves.
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      const uint4 gq = src[gi];  // the group's 8 values
+      uint32_t b3q[2], b4q[2];
+      if (kind == 0) {  // K: channels 32(u%4) + 8gi .. + 7 (bases are 4-byte aligned)
+        const uint32_t* w3 = reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 8 * gi);
+        const uint32_t* w4 = reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 8 * gi);
+        b3q[0] = w3[0];
+        b3q[1] = w3[1];
+        b4q[0] = w4[0];
+        b4q[1] = w4[1];
+      } else {
+        b3q[0] = sh->vtab[0][cls][2 * gi];
+        b3q[1] = sh->vtab[0][cls][2 * gi + 1];
+        b4q[0] = sh->vtab[1][cls][2 * gi];
+        b4q[1] = sh->vtab[1][cls][2 * gi + 1];
+      }
+      const uint32_t E0 = exponent_word(gq.x, gq.y), E1 = exponent_word(gq.z, gq.w);
+      const uint32_t d3a = E0 - b3q[0], d3b = E1 - b3q[1], d4a = E0 - b4q[0], d4b = E1 - b4q[1];
+      const bool fits3 = ((d3a | d3b) & 0xF8F8F8F8u) == 0u, fits4 = ((d4a | d4b) & 0xF0F0F0F0u) == 0u;
+      const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
+      tagbyte |= mode << (2 * gi);
+      my_counts[mode] += 1;
+      // codes: the offsets (3-bit), their low three bits (4-bit), zero (raw)
+      const uint32_t c0 = fits3 ? d3a : (fits4 ? (d4a & 0x07070707u) : 0u);
+      const uint32_t c1 = fits3 ? d3b : (fits4 ? (d4b & 0x07070707u) : 0u);
+      // format v3 placement (word k = 2gi, 2gi+1 is q = k % 4 of half h = gi / 2): q = 0 in bits 0-2 and
+      // q = 1 in bits 3-5 of W[h]; q = 2 in bits 3h.. of W[2]; q = 3 in bits 6-7 of W[h], third bit in W[2]
+      // bit 6+h (every byte lane L the element 4q+L of the half)
+      const int h = gi >> 1;
+      if ((gi & 1) == 0) {
+        W[h] |= c0 | (c1 << 3);
+      } else {
+        W[2] |= (c0 << (3 * h)) | ((c1 & 0x04040404u) << (4 + h));
+        W[h] |= (c1 & 0x03030303u) << 6;
+      }
+      if (mode == 1u) {
+        esc4 |= (escape_nibble(d4a) | (escape_nibble(d4b) << 4)) << (8 * n4);
+        n4 += 1;
+      }
+      if (mode == 2u) nraw += 1;
+    }
+  } else {
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     int e[8], b3[8], b4[8];
@@ -134,6 +250,7 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
     }
     if (mode == 2u) nraw += 1;
   }
+  }
 
   // Exclusive scans over the CTA (unit order = group order) of the 4-bit and
   // raw group counts, packed in one word (each total is at most 1024).
@@ -166,12 +283,9 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
   for (int j = 0; j < 8; ++j) {  // word j: elements 4j..4j+3 from two staged words
     const uint4 gq = src[j >> 1];
     const uint32_t w0 = (j & 1) ? gq.z : gq.x, w1 = (j & 1) ? gq.w : gq.y;
-    // sign|mantissa byte of a BF16 value x: sign (bit 15) to bit 7, mantissa bits 0-6
-    const uint32_t b0 = ((w0 >> 8) & 0x80u) | (w0 & 0x7Fu), b1 = ((w0 >> 24) & 0x80u) | ((w0 >> 16) & 0x7Fu);
-    const uint32_t b2 = ((w1 >> 8) & 0x80u) | (w1 & 0x7Fu), b3 = ((w1 >> 24) & 0x80u) | ((w1 >> 16) & 0x7Fu);
-    smb[j] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    const uint32_t sg = smb[j] & 0x80808080u;
-    smb[j] = (smb[j] & 0x7F7F7F7Fu) | ((sg << 8) | (sg >> 24));
+    // byte L: the mantissa (low byte, bits 0-6) of element L and the sign (high byte, bit 7) of element (L+3)%4
+    const uint32_t lo = __byte_perm(w0, w1, 0x6420), hi = __byte_perm(w0, w1, 0x7531);
+    smb[j] = (lo & 0x7F7F7F7Fu) | (__byte_perm(hi, hi, 0x2103) & 0x80808080u);
   }
   uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
   smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
@@ -283,9 +397,9 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_blocks_kernel(EncodeArg
   }
   const int nv = min(kBlock, len - blk * kBlock);
   // Stage the tile in storage order; tokens past the sequence are zero.
-  stage_tile(sh.tile, (kind == 0 ? a.k : a.v) + static_cast<int64_t>(b) * a.seq_stride +
-                          static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD,
-             a.tok_stride, nv, kind, tid);
+  stage_tile_enc(sh.tile, (kind == 0 ? a.k : a.v) + static_cast<int64_t>(b) * a.seq_stride +
+                              static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD,
+                 a.tok_stride, nv, kind, tid);
   __syncthreads();
   const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
   const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
@@ -815,7 +929,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_tiles_kernel(EncodeTilesAr
     }
     return;
   }
-  stage_tile(sh.tile, a.tiles + i * kTile, kD, kBlock, kind, tid);
+  stage_tile_enc(sh.tile, a.tiles + i * kTile, kD, kBlock, kind, tid);
   __syncthreads();
   const int esc = encode_tile_cta<false>(&sh, kind, a.base3 + r * kD, a.base4 + r * kD, a.slots + i * kSlot, a.stats);
   if (tid == 0) a.esc_len[i] = esc >= 0 ? static_cast<uint16_t>(esc) : 0xFFFFu;

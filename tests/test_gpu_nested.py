@@ -127,3 +127,54 @@ def test_tile_batch_bad_row_reported():
         assert int(status.item()) == G.EINVAL
         assert ((esc.cpu().numpy().astype(np.int64) & 0xFFFF) == 0xFFFF).all()
         assert not slots.any().item()
+
+
+def _wild_base_batch():
+    """Base rows: all out of the calibrated ranges, random over [0, 255], random inside them, at their
+    limits.  base4 lies 3-8 below base3, so a 4-bit window holds the 3-bit one and the three exponents
+    below it.  Exponents are base3 plus an offset: in [0, 7] for 97.7% of elements, one or three below it
+    (4-bit groups) for 2.1%, 40 away (raw groups) for 0.2%; sign and mantissa are random."""
+    rng = np.random.default_rng(11)
+    b3 = np.stack([rng.integers(249, 256, 128), rng.integers(0, 256, 128), rng.integers(8, 249, 128),
+                   np.full(128, 248)])
+    b4 = np.clip(b3 - rng.integers(3, 9, (4, 128)), 0, 255)
+    b4[2] = np.minimum(b4[2], 240)
+    b4[3] = 240
+    tiles, kinds, rows = [], [], []
+    for r in range(4):
+        for kind in (0, 1):
+            for _ in range(2):
+                off = rng.choice([0, 1, 2, 3, 4, 5, 6, 7, -1, -3, 40, -40], (64, 128),
+                                 p=[.2, .2, .15, .12, .1, .08, .072, .055, .012, .009, .001, .001])
+                e = np.clip(b3[r][None, :] + off, 0, 255)
+                x = (rng.integers(0, 2, (64, 128)) << 15) | (e << 7) | rng.integers(0, 128, (64, 128))
+                tiles.append(x.astype(np.uint16))
+                kinds.append(kind)
+                rows.append(r)
+    return np.stack(tiles), kinds, rows, b3.astype(np.uint8), b4.astype(np.uint8)
+
+
+def test_v3_tile_batch_any_bases_match_oracle():
+    """Bases anywhere in [0, 255] (calibration gives base3 <= 248 and base4 <= 240; the encoder decides a
+    group's fit a word at a time only for those, element by element otherwise)."""
+    tn, kinds, rows, b3, b4 = _wild_base_batch()
+    n = tn.shape[0]
+    t_dev = torch.from_numpy(tn.view(np.int16)).view(torch.bfloat16).cuda()
+    k_dev = torch.tensor(kinds, dtype=torch.uint8, device="cuda")
+    r_dev = torch.tensor(rows, dtype=torch.int32, device="cuda")
+    b3d, b4d = torch.from_numpy(b3).cuda(), torch.from_numpy(b4).cuda()
+    slots = torch.zeros((n, G.SLOT_BYTES), dtype=torch.uint8, device="cuda")
+    esc = torch.zeros(n, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    G.encode_tiles(t_dev, k_dev, r_dev, b3d, b4d, slots, esc, status=status)
+    back = torch.zeros_like(t_dev)
+    G.decode_tiles(slots, esc, k_dev, r_dev, b3d, b4d, back, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sn, en, bn = slots.cpu().numpy(), esc.cpu().numpy().astype(np.int64) & 0xFFFF, _u16(back)
+    for i in range(n):
+        img, e = O.encode_tile(tn[i], kinds[i], b3[rows[i]], b4[rows[i]])
+        assert e >= 0, i  # the batch is built to fit
+        assert en[i] == e, i
+        np.testing.assert_array_equal(sn[i], img, err_msg=f"tile {i}")
+        np.testing.assert_array_equal(bn[i], tn[i])
