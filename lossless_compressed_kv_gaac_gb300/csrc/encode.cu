@@ -23,13 +23,25 @@ namespace gaac {
 
 constexpr int kEncThreads = 256;
 
-struct EncShared {
-  alignas(16) uint16_t tile[kTile];  // tile in storage order
-  uint32_t vtab[2][16][8];           // V: base3 / base4 words of the 16 unit classes
+// Shared state of one tile's encode (every encoder kernel).
+struct EncCommon {
+  uint32_t vtab[2][16][8];  // base3 / base4 words of the unit classes (V: 16, K: 4)
   int warp_sums[kEncThreads / 32];
   int mode_counts[4];
   uint32_t raw_idx;
   int ok;
+};
+
+// One tile staged in storage order (the appender and the tile-batch encoder).
+struct EncShared : EncCommon {
+  alignas(16) uint16_t tile[kTile];
+};
+
+// The block encoder: the tile token-major with padded rows (filled by
+// asynchronous copies), and V rearranged into storage order.
+struct EncBlockShared : EncCommon {
+  alignas(16) uint16_t raw[kLogicalElems];
+  alignas(16) uint16_t vtile[kTile];
 };
 
 // Channel of storage element s (format v3).
@@ -38,14 +50,38 @@ __device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? 
 // Token of storage element s (format v3).
 __device__ __forceinline__ int token_of(int kind, int s) { return kind == 0 ? (s >> 7) : v_token_of(s); }
 
+// V staging: thread tid takes token t, channels 32p .. 32p+31.  Storage
+// elements 2m and 2m+1 are channels c and c+8 of one token, so the thread
+// stores each such pair as one word; this assignment puts a warp's 32 stores
+// of an instruction in 16 distinct banks.
+__device__ __forceinline__ void v_pair_slice(int tid, int& t, int& p) {
+  const int l = tid & 31, w = tid >> 5;
+  t = (l & 1) | (((l >> 3) & 1) << 1) | (((l >> 4) & 1) << 2) | (((l >> 1) & 1) << 3) | ((w & 3) << 4);
+  p = ((l >> 2) & 1) | (((w >> 2) & 1) << 1);
+}
+
+// Stores channels 32p .. 32p+31 of token t (x[i] = channels 32p + 8i .. + 7) into a V tile in storage order.
+__device__ __forceinline__ void store_v_pairs(uint16_t* tile, int t, int p, const uint4 x[4]) {
+  // word index of storage element v_storage_index(t, 32p + 16m + j) / 2 = base + 64j + 4m (j < 8)
+  const int base = 1024 * (t >> 4) + 512 * (p >> 1) + 16 * ((t >> 1) & 3) + 8 * (p & 1) + (t & 1) + 2 * ((t >> 3) & 1);
+  uint32_t* tw = reinterpret_cast<uint32_t*>(tile);
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const uint32_t aw[4] = {x[2 * m].x, x[2 * m].y, x[2 * m].z, x[2 * m].w};                  // channels c
+    const uint32_t bw[4] = {x[2 * m + 1].x, x[2 * m + 1].y, x[2 * m + 1].z, x[2 * m + 1].w};  // c + 8
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      tw[base + 64 * (2 * i) + 4 * m] = __byte_perm(aw[i], bw[i], 0x5410);
+      tw[base + 64 * (2 * i + 1) + 4 * m] = __byte_perm(aw[i], bw[i], 0x7632);
+    }
+  }
+}
+
 // Stages tokens [0, nv) of a tile (token t's 128 channels at src + t * tok_stride,
 // 16-byte aligned) into `tile` in storage order; tokens past nv are zero.
 //  K (token-major storage): 16-byte chunk q = tid + 256i is token q / 16,
 //    channels 8(q % 16) .. +7, so a warp's loads and stores are contiguous.
-//  V: storage elements 2m and 2m+1 are channels c and c+8 of one token, so a
-//    thread takes token t, channels 32p .. 32p+31 and stores each such pair as
-//    one word; the thread -> (t, p) assignment puts a warp's 32 stores of an
-//    instruction in 16 distinct banks.
+//  V: v_pair_slice / store_v_pairs.
 __device__ __forceinline__ void stage_tile_enc(uint16_t* tile, const uint16_t* src, int64_t tok_stride, int nv,
                                                int kind, int tid) {
   if (kind == 0) {
@@ -58,9 +94,8 @@ __device__ __forceinline__ void stage_tile_enc(uint16_t* tile, const uint16_t* s
     }
     return;
   }
-  const int l = tid & 31, w = tid >> 5;
-  const int t = (l & 1) | (((l >> 3) & 1) << 1) | (((l >> 4) & 1) << 2) | (((l >> 1) & 1) << 3) | ((w & 3) << 4);
-  const int p = ((l >> 2) & 1) | (((w >> 2) & 1) << 1);
+  int t, p;
+  v_pair_slice(tid, t, p);
   uint4 x[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) x[i] = make_uint4(0, 0, 0, 0);
@@ -69,19 +104,7 @@ __device__ __forceinline__ void stage_tile_enc(uint16_t* tile, const uint16_t* s
 #pragma unroll
     for (int i = 0; i < 4; ++i) x[i] = g[i];
   }
-  // word index of storage element v_storage_index(t, 32p + 16m + j) / 2 = base + 64j + 4m (j < 8)
-  const int base = 1024 * (t >> 4) + 512 * (p >> 1) + 16 * ((t >> 1) & 3) + 8 * (p & 1) + (t & 1) + 2 * ((t >> 3) & 1);
-  uint32_t* tw = reinterpret_cast<uint32_t*>(tile);
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const uint32_t aw[4] = {x[2 * m].x, x[2 * m].y, x[2 * m].z, x[2 * m].w};          // channels c
-    const uint32_t bw[4] = {x[2 * m + 1].x, x[2 * m + 1].y, x[2 * m + 1].z, x[2 * m + 1].w};  // c + 8
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      tw[base + 64 * (2 * i) + 4 * m] = __byte_perm(aw[i], bw[i], 0x5410);
-      tw[base + 64 * (2 * i + 1) + 4 * m] = __byte_perm(aw[i], bw[i], 0x7632);
-    }
-  }
+  store_v_pairs(tile, t, p, x);
 }
 
 // Exponent bytes of four BF16 values (w0 = elements 0, 1; w1 = elements 2, 3):
@@ -96,25 +119,33 @@ __device__ __forceinline__ uint32_t escape_nibble(uint32_t d4) {
   return (((d4 >> 3) & 0x01010101u) * 0x01020408u) >> 24;
 }
 
-// Encodes the tile in sh->tile into `slot` (global, 16-byte aligned) unless its
-// escape stream exceeds the capacity.  Returns the escape length, or -1 when
+// Encodes a staged tile into `slot` (global, 16-byte aligned) unless its
+// escape stream exceeds the capacity.  `unit`: this thread's 32 values (code
+// unit u = threadIdx.x, storage elements 32u .. 32u+31; 16-byte aligned).  Returns the escape length, or -1 when
 // the tile must stay raw (then nothing is written).  CTA-uniform result; all
 // 256 threads must call it.
 //
 // n_present < 64 encodes an open tile (the incomplete last block of a
-// prefill): elements of tokens >= n_present are absent (sh->tile must hold
-// zero there); they take no part in their group's mode, and their codes and
+// prefill): elements of tokens >= n_present are absent (the staged tile must
+// hold zero there); they take no part in their group's mode, and their codes and
 // escape bits are zero.  kOpen = false compiles the sealed-tile encoder
 // (n_present is then ignored: every token present).
 template <bool kOpen>
-__device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8_t* __restrict__ b3g,
-                               const uint8_t* __restrict__ b4g, uint8_t* __restrict__ slot,
-                               gaac_stats* stats, int n_present = kBlock) {
+__device__ __noinline__ int encode_tile_cta(EncCommon* sh, const uint16_t* unit, int kind,
+                                           const uint8_t* __restrict__ b3g, const uint8_t* __restrict__ b4g,
+                                           uint8_t* __restrict__ slot, gaac_stats* stats, int n_present = kBlock) {
   const int u = threadIdx.x;
   const int lane = u & 31, warp = u >> 5;
-  const uint4* src = reinterpret_cast<const uint4*>(sh->tile + 32 * u);  // the unit's 32 values, 4 quads of 8
-  if (u < 4) sh->mode_counts[u] = 0;
-  if (kind == 1) fill_v_base_table(sh->vtab, b3g, b4g, u);  // V bases by unit class (kind is CTA-uniform)
+  const uint4* src = reinterpret_cast<const uint4*>(unit);  // the unit's 32 values, 4 quads of 8
+  if (u == 0) sh->mode_counts[0] = 0;
+  // Base words by unit class: V, the 16 classes of v_unit_class; K, class u % 4
+  // (element 4k+L of unit u is channel 32(u%4) + 4k + L).  kind is CTA-uniform.
+  if (kind == 1) {
+    fill_v_base_table(sh->vtab, b3g, b4g, u);
+  } else if (u < 64) {
+    const int which = u >> 5, c = (u >> 3) & 3, k = u & 7;
+    sh->vtab[which][c][k] = *reinterpret_cast<const uint32_t*>((which ? b4g : b3g) + 32 * c + 4 * k);
+  }
   // Calibrated bases lie in [0, 248] (base3) and [0, 240] (base4); for those a
   // word subtraction decides a group's fit exactly (below).  Other bases take
   // the element-by-element path.
@@ -126,13 +157,13 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
   }
   const bool any_odd = __syncthreads_or(odd_base) != 0;  // also orders the V table's writes before its reads
   const bool word_fit = !kOpen && !any_odd;
-  const int cls = v_unit_class(u);
+  const int cls = kind == 0 ? (u & 3) : v_unit_class(u);
 
   uint32_t W[3] = {0, 0, 0};  // the unit's code-plane words, filled code by code
   uint32_t esc4 = 0;  // the unit's 4-bit escape bytes, little-endian, in group order
   int n4 = 0, nraw = 0;
   uint32_t tagbyte = 0;
-  int my_counts[3] = {0, 0, 0};
+  uint32_t counts = 0;  // 3-bit groups | 4-bit groups << 16 (raw: the rest of the tile's 1024)
 
   if (word_fit) {
     // Four elements per word: E = exponent bytes, D = E - base.  With every
@@ -144,26 +175,14 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
 #pragma unroll
     for (int gi = 0; gi < 4; ++gi) {
       const uint4 gq = src[gi];  // the group's 8 values
-      uint32_t b3q[2], b4q[2];
-      if (kind == 0) {  // K: channels 32(u%4) + 8gi .. + 7 (bases are 4-byte aligned)
-        const uint32_t* w3 = reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 8 * gi);
-        const uint32_t* w4 = reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 8 * gi);
-        b3q[0] = w3[0];
-        b3q[1] = w3[1];
-        b4q[0] = w4[0];
-        b4q[1] = w4[1];
-      } else {
-        b3q[0] = sh->vtab[0][cls][2 * gi];
-        b3q[1] = sh->vtab[0][cls][2 * gi + 1];
-        b4q[0] = sh->vtab[1][cls][2 * gi];
-        b4q[1] = sh->vtab[1][cls][2 * gi + 1];
-      }
+      const uint32_t b3q[2] = {sh->vtab[0][cls][2 * gi], sh->vtab[0][cls][2 * gi + 1]};
+      const uint32_t b4q[2] = {sh->vtab[1][cls][2 * gi], sh->vtab[1][cls][2 * gi + 1]};
       const uint32_t E0 = exponent_word(gq.x, gq.y), E1 = exponent_word(gq.z, gq.w);
       const uint32_t d3a = E0 - b3q[0], d3b = E1 - b3q[1], d4a = E0 - b4q[0], d4b = E1 - b4q[1];
       const bool fits3 = ((d3a | d3b) & 0xF8F8F8F8u) == 0u, fits4 = ((d4a | d4b) & 0xF0F0F0F0u) == 0u;
       const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
       tagbyte |= mode << (2 * gi);
-      my_counts[mode] += 1;
+      counts += mode == 0u ? 1u : (mode == 1u ? 0x10000u : 0u);
       // codes: the offsets (3-bit), their low three bits (4-bit), zero (raw)
       const uint32_t c0 = fits3 ? d3a : (fits4 ? (d4a & 0x07070707u) : 0u);
       const uint32_t c1 = fits3 ? d3b : (fits4 ? (d4b & 0x07070707u) : 0u);
@@ -191,20 +210,8 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
     bool fits3 = true, fits4 = true;
     const uint4 gq = src[gi];  // the group's 8 values
     const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-    uint32_t b3q[2], b4q[2];  // the group's bases, four per word
-    if (kind == 0) {  // K: channels 32(u%4) + 8gi .. + 7 (bases are 4-byte aligned)
-      const uint32_t* w3 = reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 8 * gi);
-      const uint32_t* w4 = reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 8 * gi);
-      b3q[0] = w3[0];
-      b3q[1] = w3[1];
-      b4q[0] = w4[0];
-      b4q[1] = w4[1];
-    } else {
-      b3q[0] = sh->vtab[0][cls][2 * gi];
-      b3q[1] = sh->vtab[0][cls][2 * gi + 1];
-      b4q[0] = sh->vtab[1][cls][2 * gi];
-      b4q[1] = sh->vtab[1][cls][2 * gi + 1];
-    }
+    const uint32_t b3q[2] = {sh->vtab[0][cls][2 * gi], sh->vtab[0][cls][2 * gi + 1]};  // four bases per word
+    const uint32_t b4q[2] = {sh->vtab[1][cls][2 * gi], sh->vtab[1][cls][2 * gi + 1]};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int el = 8 * gi + j;
@@ -219,7 +226,7 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
     }
     const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
     tagbyte |= mode << (2 * gi);
-    my_counts[mode] += 1;
+    counts += mode == 0u ? 1u : (mode == 1u ? 0x10000u : 0u);
     uint32_t eb = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -304,7 +311,7 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
       if (((tagbyte >> (2 * gi)) & 3u) != 2u) continue;
 #pragma unroll
       for (int j = 0; j < 8; ++j)  // the exponent of element 8gi + j (zero where absent)
-        escp[r + j] = static_cast<uint8_t>(sh->tile[32 * u + 8 * gi + j] >> 7);
+        escp[r + j] = static_cast<uint8_t>(unit[8 * gi + j] >> 7);
       r += 8;
     }
   }
@@ -319,15 +326,16 @@ __device__ __noinline__ int encode_tile_cta(EncShared* sh, int kind, const uint8
     slot[kOffDir + 2 * w] = static_cast<uint8_t>(entry & 0xFFu);
     slot[kOffDir + 2 * w + 1] = static_cast<uint8_t>(entry >> 8);
   }
-  if (stats != nullptr) {
-#pragma unroll
-    for (int m = 0; m < 3; ++m)
-      if (my_counts[m]) atomicAdd(&sh->mode_counts[m], my_counts[m]);
+  if (stats != nullptr) {  // a sealed tile: all 1024 groups counted
+    const uint32_t warp_counts = __reduce_add_sync(0xFFFFFFFFu, counts);
+    if (lane == 0) atomicAdd(reinterpret_cast<unsigned int*>(&sh->mode_counts[0]), warp_counts);
     __syncthreads();
     if (u == 0) {
-#pragma unroll
-      for (int m = 0; m < 3; ++m)
-        atomicAdd(&stats->groups[m], static_cast<unsigned long long>(sh->mode_counts[m]));
+      const uint32_t c = static_cast<uint32_t>(sh->mode_counts[0]);
+      const unsigned long long n3 = c & 0xFFFFu, n4g = c >> 16;
+      atomicAdd(&stats->groups[0], n3);
+      atomicAdd(&stats->groups[1], n4g);
+      atomicAdd(&stats->groups[2], 1024ull - n3 - n4g);
       atomicAdd(&stats->escape_bytes, static_cast<unsigned long long>(esc));
       atomicAdd(&stats->slot_tiles, 1ull);
     }
@@ -376,31 +384,93 @@ struct EncodeArgs {
   int32_t* status;
 };
 
-// grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
-__global__ void __launch_bounds__(kEncThreads, 4) encode_blocks_kernel(EncodeArgs a) {
-  __shared__ EncShared sh;
-  const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
-  const int blk = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
-  const size_t eidx = ((static_cast<size_t>(b) * a.max_blocks + blk) * a.n_kv_heads + h) * 2 + kind;
-  const int len = a.seq_lens[b];
-  if (len < 0 || len > a.max_blocks * kBlock || len > a.n_tok) {
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Work item i of the block encoder: x = i % (2 n_kv_heads) = h*2 + kind, then
+// block, then sequence.  nv = tokens of the block present (0: the block is past
+// the sequence; -1: the sequence length is invalid).
+struct BlockItem {
+  int b, blk, h, kind, nv;
+};
+
+__device__ __forceinline__ BlockItem block_item(const EncodeArgs& a, int64_t i) {
+  BlockItem it;
+  const uint32_t two_h = 2u * static_cast<uint32_t>(a.n_kv_heads), mb = static_cast<uint32_t>(a.max_blocks);
+  uint32_t x, blk, b;
+  if (i <= 0xFFFFFFFFll) {  // 32-bit division (every realistic cache)
+    const uint32_t i32 = static_cast<uint32_t>(i), r = i32 / two_h;
+    x = i32 - r * two_h;
+    b = r / mb;
+    blk = r - b * mb;
+  } else {
+    const int64_t r = i / two_h;
+    x = static_cast<uint32_t>(i - r * two_h);
+    b = static_cast<uint32_t>(r / mb);
+    blk = static_cast<uint32_t>(r - static_cast<int64_t>(b) * mb);
+  }
+  it.h = static_cast<int>(x >> 1);
+  it.kind = static_cast<int>(x & 1u);
+  it.blk = static_cast<int>(blk);
+  it.b = static_cast<int>(b);
+  const int len = a.seq_lens[it.b];
+  if (len < 0 || len > a.max_blocks * kBlock || len > a.n_tok)
+    it.nv = -1;
+  else
+    it.nv = max(0, min(kBlock, len - it.blk * kBlock));
+  return it;
+}
+
+// Starts the copies of an item's tile into a token-major buffer with padded rows
+// (tokens past the sequence are filled with zeros) as one commit group.
+__device__ __forceinline__ void prefetch_block(const EncodeArgs& a, const BlockItem& it, uint16_t* buf, int tid) {
+  if (it.nv > 0) {
+    const uint16_t* src = (it.kind == 0 ? a.k : a.v) + static_cast<int64_t>(it.b) * a.seq_stride +
+                          static_cast<int64_t>(it.blk) * kBlock * a.tok_stride + it.h * kD;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = tid + kEncThreads * j, t = q >> 4, col = 8 * (q & 15);
+      const bool in = t < it.nv;
+      cp_async16(buf + t * kLogicalStride + col, in ? src + t * a.tok_stride + col : src, in ? 16u : 0u);
+    }
+  }
+  cp_async_commit();
+}
+
+// Encodes an item, staged in `buf`; all threads call it.
+__device__ __forceinline__ void encode_block_item(const EncodeArgs& a, const BlockItem& it, EncBlockShared& sh,
+                                                  const uint16_t* buf, int tid) {
+  const size_t eidx = ((static_cast<size_t>(it.b) * a.max_blocks + it.blk) * a.n_kv_heads + it.h) * 2 + it.kind;
+  if (it.nv <= 0) {
     if (tid == 0) {
       a.table[eidx] = make_entry(0, 0, GAAC_MODE_NONE, 0);
-      report(a.status, GAAC_EINVAL);
+      if (it.nv < 0) report(a.status, GAAC_EINVAL);
     }
     return;
   }
-  if (blk * kBlock >= len) {
-    if (tid == 0) a.table[eidx] = make_entry(0, 0, GAAC_MODE_NONE, 0);
-    return;
+  const int kind = it.kind, h = it.h, nv = it.nv;
+  const uint16_t* unit;
+  if (kind == 1) {  // V: rearrange the token-major tile into storage order
+    int t, p;
+    v_pair_slice(tid, t, p);
+    uint4 x[4];
+    const uint4* row = reinterpret_cast<const uint4*>(buf + t * kLogicalStride + 32 * p);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = row[j];
+    store_v_pairs(sh.vtile, t, p, x);
+    __syncthreads();
+    unit = sh.vtile + 32 * tid;
+  } else {  // K: storage order is token-major; unit u = token u/4, channels 32(u%4) .. +31
+    unit = buf + (tid >> 2) * kLogicalStride + 32 * (tid & 3);
   }
-  const int nv = min(kBlock, len - blk * kBlock);
-  // Stage the tile in storage order; tokens past the sequence are zero.
-  stage_tile_enc(sh.tile, (kind == 0 ? a.k : a.v) + static_cast<int64_t>(b) * a.seq_stride +
-                              static_cast<int64_t>(blk) * kBlock * a.tok_stride + h * kD,
-                 a.tok_stride, nv, kind, tid);
-  __syncthreads();
   const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
   const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
   if ((nv == kBlock || (a.flags & GAAC_OPEN_COMPRESSED)) && a.slot_ids != nullptr) {
@@ -412,14 +482,14 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_blocks_kernel(EncodeArg
     } else if (tid == 0) {
       report(a.status, GAAC_EPOOL);
     }
-    const int esc = nv == kBlock ? encode_tile_cta<false>(&sh, kind, b3, b4, slot, a.stats)
-                                 : encode_tile_cta<true>(&sh, kind, b3, b4, slot, nullptr, nv);
+    const int esc = nv == kBlock ? encode_tile_cta<false>(&sh, unit, kind, b3, b4, slot, a.stats)
+                                 : encode_tile_cta<true>(&sh, unit, kind, b3, b4, slot, nullptr, nv);
     if (esc >= 0) {
       if (tid == 0) a.table[eidx] = make_entry(slot_id, esc, GAAC_MODE_SLOT, nv);
       return;
     }
   }
-  // Raw tile: overflow fallback of a full block, or the open tail.
+  // Raw tile (storage order): overflow fallback of a full block, or the open tail.
   if (tid == 0) {
     uint32_t idx = 0;
     sh.ok = pop_raw(a.pools, &idx, a.status) ? 1 : 0;
@@ -431,14 +501,33 @@ __global__ void __launch_bounds__(kEncThreads, 4) encode_blocks_kernel(EncodeArg
     return;
   }
   uint4* dst = reinterpret_cast<uint4*>(a.pools.raw_pool + static_cast<size_t>(sh.raw_idx) * kTile);
-  const uint4* s = reinterpret_cast<const uint4*>(sh.tile);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) dst[tid + kEncThreads * i] = s[tid + kEncThreads * i];
+  for (int j = 0; j < 4; ++j) {
+    const int q = tid + kEncThreads * j;  // 16-byte chunk q: storage elements 8q .. 8q+7
+    const uint16_t* from = kind == 1 ? sh.vtile + 8 * q : buf + (q >> 4) * kLogicalStride + 8 * (q & 15);
+    dst[q] = *reinterpret_cast<const uint4*>(from);
+  }
   if (tid == 0) {
     a.table[eidx] = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, nv);
     if (a.stats != nullptr && a.slot_ids != nullptr)
       atomicAdd(nv == kBlock ? &a.stats->raw_tiles : &a.stats->tail_tiles, 1ull);
   }
+}
+
+// One CTA per item.  (A persistent variant that copied the next item's tile
+// while encoding the current one was slower: the scheduler already overlaps
+// the copies of some CTAs with the encoding of others.)
+__global__ void __launch_bounds__(kEncThreads, 5) encode_blocks_kernel(EncodeArgs a, int64_t n_items) {
+  extern __shared__ __align__(16) uint8_t enc_smem[];
+  EncBlockShared& sh = *reinterpret_cast<EncBlockShared*>(enc_smem);
+  const int tid = threadIdx.x;
+  const int64_t i = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+  if (i >= n_items) return;
+  const BlockItem it = block_item(a, i);
+  prefetch_block(a, it, sh.raw, tid);
+  cp_async_wait<0>();
+  __syncthreads();
+  encode_block_item(a, it, sh, sh.raw, tid);
 }
 
 // ------------------------------------------------ open block, one token --
@@ -884,7 +973,7 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   } else if (tid == 0) {
     report(a.status, GAAC_EPOOL);
   }
-  const int esc = encode_tile_cta<false>(&sh, kind, b3, b4, slot, a.stats);
+  const int esc = encode_tile_cta<false>(&sh, sh.tile + 32 * tid, kind, b3, b4, slot, a.stats);
   if (esc >= 0 && blk + 1 < a.max_blocks) {
     // The raw tile becomes the next block's empty tail: clear it so that a tail
     // always holds zeros past its last token.
@@ -931,7 +1020,8 @@ __global__ void __launch_bounds__(kEncThreads) encode_tiles_kernel(EncodeTilesAr
   }
   stage_tile_enc(sh.tile, a.tiles + i * kTile, kD, kBlock, kind, tid);
   __syncthreads();
-  const int esc = encode_tile_cta<false>(&sh, kind, a.base3 + r * kD, a.base4 + r * kD, a.slots + i * kSlot, a.stats);
+  const int esc = encode_tile_cta<false>(&sh, sh.tile + 32 * tid, kind, a.base3 + r * kD, a.base4 + r * kD,
+                                         a.slots + i * kSlot, a.stats);
   if (tid == 0) a.esc_len[i] = esc >= 0 ? static_cast<uint16_t>(esc) : 0xFFFFu;
 }
 
@@ -943,6 +1033,20 @@ __global__ void bump_lens_kernel(int32_t* lens, int batch) {
 }  // namespace gaac
 
 using namespace gaac;
+
+// Sets the block encoder's dynamic shared-memory size on the current device (once).
+static bool prepare_encode_blocks() {
+  static bool done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(encode_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(EncBlockShared))) != cudaSuccess)
+      return false;
+    done[dev] = true;
+  }
+  return true;
+}
 
 static bool pools_ok(const gaac_pools* p) {
   return p != nullptr && p->slot_pool != nullptr && p->raw_pool != nullptr && p->raw_cursor != nullptr &&
@@ -968,8 +1072,11 @@ extern "C" int gaac_encode_blocks_ex(const uint16_t* k, const uint16_t* v, int64
   if (n_tok < 0) return GAAC_EINVAL;
   EncodeArgs a{k, v, seq_stride, tok_stride, n_tok, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids,
                *pools, stats, flags, d_status};
-  dim3 grid(2 * n_kv_heads, max_blocks, batch);
-  encode_blocks_kernel<<<grid, kEncThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (!prepare_encode_blocks()) return GAAC_ECUDA;
+  const int64_t n_items = static_cast<int64_t>(2 * n_kv_heads) * max_blocks * batch;
+  const int64_t gx = n_items < 0x7FFFFFFF ? n_items : 0x7FFFFFFF;  // then ceil(n_items / gx) <= 4096 rows
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>((n_items + gx - 1) / gx));
+  encode_blocks_kernel<<<grid, kEncThreads, sizeof(EncBlockShared), static_cast<cudaStream_t>(stream)>>>(a, n_items);
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
 
