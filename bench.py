@@ -183,6 +183,25 @@ def algorithmic_bytes(cache) -> int:
     return n
 
 
+def time_calls(fn, reps: int = 5, rounds: int = 3) -> float:
+    """Device time of one call of fn (ms): `reps` back-to-back calls between two CUDA events on the
+    current stream, min over rounds.  One more call is queued before the first event, so the device is
+    busy while the host enqueues the timed calls and their launch overhead is not in the time."""
+    import torch
+
+    best = float("inf")
+    for _ in range(rounds):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) / reps)
+    return best
+
+
 def time_graph(g, stream, steps: int):
     """Replays the graph `steps` times on `stream`; CUDA-event time on that stream (ms)."""
     import torch
@@ -222,26 +241,17 @@ def fp8_codec(k, v, n_calib: int) -> dict:
         slots = torch.empty((n, G.fp8_slot_bytes(fmt)), dtype=torch.uint8, device=k.device)
         esc = torch.empty(n, dtype=torch.int16, device=k.device)
         back = torch.empty_like(tiles)
-        te, td = [], []
-        for i in range(4):
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            e0.record()
-            G.fp8_encode_tiles(tiles, fmt, kinds, rows, b3, b4, slots, esc)
-            e1.record()
-            G.fp8_decompress_tiles(slots, esc, fmt, kinds, rows, b3, b4, back)
-            e2.record()
-            e2.synchronize()
-            if i:
-                te.append(e0.elapsed_time(e1))
-                td.append(e1.elapsed_time(e2))
+        te = time_calls(lambda: G.fp8_encode_tiles(tiles, fmt, kinds, rows, b3, b4, slots, esc))
+        td = time_calls(lambda: G.fp8_decompress_tiles(slots, esc, fmt, kinds, rows, b3, b4, back))
+        torch.cuda.synchronize()
         e = esc.view(torch.int16).long() & 0xFFFF
         fits = e != 0xFFFF
         assert torch.equal(back[fits], tiles[fits])
         off_esc = G.fp8_slot_bytes(fmt) - 496
         payload = int((off_esc + e[fits]).sum().item()) + 8192 * int((~fits).sum().item())
         out[name] = {"payload_ratio": round(n * 8192 / payload, 4), "resident_ratio": round(8192 / G.fp8_slot_bytes(fmt), 4),
-                     "tiles_kept_fp8": int((~fits).sum().item()), "encode_gbs": round(n * 8192 / (min(te) * 1e-3) / 1e9, 1),
-                     "decode_gbs": round(n * 8192 / (min(td) * 1e-3) / 1e9, 1)}
+                     "tiles_kept_fp8": int((~fits).sum().item()), "encode_gbs": round(n * 8192 / (te * 1e-3) / 1e9, 1),
+                     "decode_gbs": round(n * 8192 / (td * 1e-3) / 1e9, 1)}
     return out
 
 
@@ -273,18 +283,9 @@ def mode_ablation(k, v, n_calib: int) -> dict:
     G.encode_tiles(tiles, kinds, rows, b3, b4, s3, e3)
     G.nested_encode_tiles(tiles, kinds, rows, b2, b3, b4, sn, en)
     back = torch.empty_like(tiles)
-    t3, tn = [], []
-    for i in range(5):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        ev[0].record()
-        G.decode_tiles(s3, e3, kinds, rows, b3, b4, back)
-        ev[1].record()
-        G.nested_decode_tiles(sn, en, kinds, rows, b2, b3, b4, back)
-        ev[2].record()
-        ev[2].synchronize()
-        if i:
-            t3.append(ev[0].elapsed_time(ev[1]))
-            tn.append(ev[1].elapsed_time(ev[2]))
+    d3 = time_calls(lambda: G.decode_tiles(s3, e3, kinds, rows, b3, b4, back))
+    dn = time_calls(lambda: G.nested_decode_tiles(sn, en, kinds, rows, b2, b3, b4, back))
+    torch.cuda.synchronize()
     assert torch.equal(back.view(torch.int16), tiles.view(torch.int16))
     G.decode_tiles(s3, e3, kinds, rows, b3, b4, back)
     torch.cuda.synchronize()
@@ -296,7 +297,6 @@ def mode_ablation(k, v, n_calib: int) -> dict:
     pay3 = int((11536 + e3l).sum().item())
     payn = int((8192 + (bits + 7) // 8 + 256 + 32 + enl).sum().item())
     raw = n * 16384
-    d3, dn = min(t3), min(tn)
     return {"tiles": n, "payload_ratio_v3": round(raw / pay3, 4), "payload_ratio_nested": round(raw / payn, 4),
             "ratio_gain_pct": round(100 * (pay3 / payn - 1), 2),
             "decode_us_v3": round(d3 * 1e3, 1), "decode_us_nested": round(dn * 1e3, 1),
@@ -445,30 +445,15 @@ def run_gaac(args):
     c0 = caches[0]
     k0, v0 = W.make_kv(CONFIG_ID, 0, 1, wl.seq_len, wl.n_kv_heads, device=device)
     lens = torch.tensor([wl.seq_len], dtype=torch.int32, device=device)
-    enc_t = []
-    for i in range(4):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        c0.encode(k0, v0, lens)
-        e1.record()
-        e1.synchronize()
-        if i:
-            enc_t.append(e0.elapsed_time(e1))
+    enc_ms = time_calls(lambda: c0.encode(k0, v0, lens))
     raw_bytes_layer = 2 * wl.seq_len * wl.n_kv_heads * 128 * 2
-    encode_gbs = raw_bytes_layer / (min(enc_t) * 1e-3) / 1e9
-    dec_t = []
+    encode_gbs = raw_bytes_layer / (enc_ms * 1e-3) / 1e9
     kd = torch.empty_like(k0)
     vd = torch.empty_like(v0)
-    for i in range(4):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        G.decompress(c0.table, c0.seq_lens, c0.pools, c0.base3, c0.base4, kd, vd)
-        e1.record()
-        e1.synchronize()
-        if i:
-            dec_t.append(e0.elapsed_time(e1))
+    dec_ms = time_calls(lambda: G.decompress(c0.table, c0.seq_lens, c0.pools, c0.base3, c0.base4, kd, vd))
+    torch.cuda.synchronize()
     assert torch.equal(kd.view(torch.int16), k0.view(torch.int16)) and torch.equal(vd.view(torch.int16), v0.view(torch.int16))
-    decompress_gbs = raw_bytes_layer / (min(dec_t) * 1e-3) / 1e9
+    decompress_gbs = raw_bytes_layer / (dec_ms * 1e-3) / 1e9
     st = G.stats_dict(c0.stats)
     fp8 = fp8_codec(k0, v0, wl.n_calib)
     app = append_cost(k0, v0, wl.n_calib)
