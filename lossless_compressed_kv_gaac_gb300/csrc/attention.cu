@@ -714,6 +714,10 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   const int split = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
   const int H = y / NH, hf = y % NH, nkv = NH * a.Hkv;  // nkv: half-heads in the table and the bases
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Launched as a programmatic dependent of the previous kernel on the stream,
+  // the CTA may already be resident while that kernel finishes: wait for it
+  // (and its memory) before reading anything.  A no-op for an ordinary launch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int len = a.seq_lens[b];
   if (len < 0 || len > a.max_blocks * kBlock) {
     if (tid == 0) report(a.status, GAAC_EINVAL);
@@ -724,6 +728,24 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   const int per = (nblk + a.n_splits - 1) / a.n_splits;
   const int blk0 = split * per;
   const int n_my = max(0, min(nblk, blk0 + per) - blk0);
+
+  // The first blocks' copies start before anything else: lane st initialises
+  // stage st's barrier and issues block st into it (later blocks are issued as
+  // stages free up), so the tables below are built while the copies land.
+  if (tid < kStages) {
+    mbar_init(&sm.stFull[tid], 1);
+    sm.stDone[tid] = 0u;
+  }
+  if (NH > KH && tid < 2 * AttSmem<NH, KH>::kPairs) {
+    mbar_init(&sm.mFull[tid / 2][tid % 2], 1);   // lane 0's expect_tx; the peer's bytes complete it
+    mbar_init(&sm.mEmpty[tid / 2][tid % 2], 1);  // lane 0 of the peer's warp, after reading
+  }
+  fence_mbar_init();
+  if (tid < min(n_my, kStages)) {
+    uint2 e[KH + 1];
+    block_entries<NH, KH>(a, b, H, hf, blk0 + tid, e);
+    issue_block<NH, KH>(a, sm, tid, e);
+  }
 
   for (int x = tid; x < 256; x += kAttThreads) {
     sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
@@ -758,27 +780,15 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd] = v;
     reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd + 1] = 0u;
   }
-  if (tid < kStages) {
-    mbar_init(&sm.stFull[tid], 1);
-    sm.stDone[tid] = 0u;
-  }
-  if (NH > KH && tid < 2 * AttSmem<NH, KH>::kPairs) {
-    mbar_init(&sm.mFull[tid / 2][tid % 2], 1);   // lane 0's expect_tx; the peer's bytes complete it
-    mbar_init(&sm.mEmpty[tid / 2][tid % 2], 1);  // lane 0 of the peer's warp, after reading
-  }
-  fence_mbar_init();
-  __syncthreads();
+  __syncthreads();  // barriers initialised, tables built
   if constexpr (NH > KH) cluster_sync();  // the peer's mailbox barriers exist before any remote arrival
-  if (tid < min(n_my, kStages)) {  // the first blocks, one lane each; later ones are issued as stages free up
-    uint2 e[KH + 1];
-    block_entries<NH, KH>(a, b, H, hf, blk0 + tid, e);
-    issue_block<NH, KH>(a, sm, tid, e);
-  }
 
   const int r = a.r;
   float* part = a.part + ((static_cast<size_t>(b) * nkv + y) * a.n_splits + split) * kPartFloats;
   float acc[8][4];
   compute_warp<NH, KH>(a, sm, b, H, hf, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane, acc);
+  // The next kernel on the stream may be scheduled now (it waits for this one before its first read).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     // Every issued copy was waited for by its group; after a timed-out wait,
     // wait once more (bounded) so that no copy is still landing at exit.
@@ -992,7 +1002,18 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
     const cudaLaunchConfig_t cfg = pair_config<NH, KH>(dim3(n_splits, nkv, batch), st, attr);
     if (cudaLaunchKernelEx(&cfg, attn_split_kernel<NH, KH>, a) != cudaSuccess) return GAAC_ECUDA;
   } else {
-    attn_split_kernel<NH, KH><<<dim3(n_splits, nkv, batch), kAttThreads, sizeof(AttSmem<NH, KH>), st>>>(a);
+    // Programmatic dependent launch: the grid is set up while the previous kernel on the stream drains.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_splits, nkv, batch);
+    cfg.blockDim = dim3(kAttThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(AttSmem<NH, KH>);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn_split_kernel<NH, KH>, a) != cudaSuccess) return GAAC_ECUDA;
   }
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
