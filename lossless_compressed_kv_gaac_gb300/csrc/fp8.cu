@@ -85,6 +85,19 @@ __device__ __forceinline__ void put_field3(uint32_t W[3], int j, uint32_t v) {
   }
 }
 
+// Adds the 3-bit fields of group gi (f0: elements 8gi..8gi+3, f1: 8gi+4..8gi+7, one field per byte lane)
+// to the unit's three words in put_field3's placement: words 2gi and 2gi+1 are q = 2(gi%2) and q+1 of
+// half gi/2.
+__device__ __forceinline__ void place_fields3(uint32_t W[3], int gi, uint32_t f0, uint32_t f1) {
+  const int h = gi >> 1;
+  if ((gi & 1) == 0) {
+    W[h] |= f0 | (f1 << 3);
+  } else {
+    W[2] |= (f0 << (3 * h)) | ((f1 & 0x04040404u) << (4 + h));
+    W[h] |= (f1 & 0x03030303u) << 6;
+  }
+}
+
 struct Fp8Args {
   const uint8_t* tiles;
   int64_t n_tiles;
@@ -134,34 +147,75 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
   }
   const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
   const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
-  if (kind == 1) fill_v_base_table(vtab, b3g, b4g, u);
+  // Base words by unit class: V, the 16 classes of v_unit_class; K, class u % 4.
+  if (kind == 1) {
+    fill_v_base_table(vtab, b3g, b4g, u);
+  } else if (u < 64) {
+    const int which = u >> 5, c = (u >> 3) & 3, k = u & 7;
+    vtab[which][c][k] = *reinterpret_cast<const uint32_t*>((which ? b4g : b3g) + 32 * c + 4 * k);
+  }
   if (u < 4) mode_counts[u] = 0;
-  __syncthreads();
-  const int cls = v_unit_class(u);
+  // Bases above 248 (base3) or 240 (base4) take the element-by-element path (the word test below is exact
+  // only up to those).
+  bool odd_base = false;
+  if (u < kD / 4) {
+    const uint32_t w3 = reinterpret_cast<const uint32_t*>(b3g)[u], w4 = reinterpret_cast<const uint32_t*>(b4g)[u];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) odd_base = odd_base || ((w3 >> (8 * q)) & 0xFFu) > 248u || ((w4 >> (8 * q)) & 0xFFu) > 240u;
+  }
+  const bool word_fit = __syncthreads_or(odd_base) == 0;
+  const int cls = kind == 0 ? (u & 3) : v_unit_class(u);
   const uint32_t emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
   uint32_t CW[3] = {0u, 0u, 0u};  // code-plane words, filled field by field
   uint32_t SW[4] = {0u, 0u, 0u, 0u};  // sign|mantissa: nibbles (E4M3) or 3-bit fields in SW[0..2] (E5M2)
   uint32_t esc4 = 0, tagbyte = 0;
   int n4 = 0, nraw = 0, my_counts[3] = {0, 0, 0};
+  if (word_fit) {
+    // Four elements per word (word k = elements 4k..4k+3 of the unit): exponent bytes E, offsets
+    // D = E - base in one subtraction; a group fits the 3-bit (4-bit) mode iff no byte of D has a bit
+    // above bit 2 (bit 3), exact for base3 <= 248 (base4 <= 240) as in the BF16 encoder.
+    const uint4* s4 = reinterpret_cast<const uint4*>(seq + 32 * u);
+    const uint4 q0 = s4[0], q1 = s4[1];
+    const uint32_t x[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t emw = emask * 0x01010101u, mmw = mmask * 0x01010101u, sgw = 0x01010101u << L.mw;
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      const uint32_t w0 = x[2 * gi], w1 = x[2 * gi + 1];
+      const uint32_t E0 = (w0 >> L.mw) & emw, E1 = (w1 >> L.mw) & emw;
+      // sign|mantissa fields: the sign (bit 7) to bit mw above the mantissa
+      const uint32_t s0 = ((w0 >> (7 - L.mw)) & sgw) | (w0 & mmw), s1 = ((w1 >> (7 - L.mw)) & sgw) | (w1 & mmw);
+      const uint32_t d3a = E0 - vtab[0][cls][2 * gi], d3b = E1 - vtab[0][cls][2 * gi + 1];
+      const uint32_t d4a = E0 - vtab[1][cls][2 * gi], d4b = E1 - vtab[1][cls][2 * gi + 1];
+      const bool fits3 = ((d3a | d3b) & 0xF8F8F8F8u) == 0u, fits4 = ((d4a | d4b) & 0xF0F0F0F0u) == 0u;
+      const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
+      tagbyte |= mode << (2 * gi);
+      my_counts[mode] += 1;
+      const uint32_t c0 = fits3 ? d3a : (fits4 ? (d4a & 0x07070707u) : 0u);
+      const uint32_t c1 = fits3 ? d3b : (fits4 ? (d4b & 0x07070707u) : 0u);
+      place_fields3(CW, gi, c0, c1);
+      if (L.ew == 4) {  // nibbles, element 8gi + j in nibble j of SW[gi]
+        const uint32_t n0 = (s0 & 0x000F000Fu) | ((s0 >> 4) & 0x00F000F0u);
+        const uint32_t n1 = (s1 & 0x000F000Fu) | ((s1 >> 4) & 0x00F000F0u);
+        SW[gi] = __byte_perm(n0, n1, 0x6420);
+      } else {
+        place_fields3(SW, gi, s0, s1);
+      }
+      if (mode == 1u) {
+        const uint32_t eb = ((((d4a >> 3) & 0x01010101u) * 0x01020408u) >> 24) |
+                            (((((d4b >> 3) & 0x01010101u) * 0x01020408u) >> 24) << 4);
+        esc4 |= eb << (8 * n4);
+        n4 += 1;
+      }
+      if (mode == 2u) nraw += 1;
+    }
+  } else {
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     uint32_t e[8];
     int b3[8], b4[8];
     bool fits3 = true, fits4 = true;
-    uint32_t b3q[2], b4q[2];  // the group's bases, four per word
-    if (kind == 0) {  // K: channels 32(u%4) + 8gi .. + 7 (bases are 4-byte aligned)
-      const uint32_t* w3 = reinterpret_cast<const uint32_t*>(b3g + 32 * (u & 3) + 8 * gi);
-      const uint32_t* w4 = reinterpret_cast<const uint32_t*>(b4g + 32 * (u & 3) + 8 * gi);
-      b3q[0] = w3[0];
-      b3q[1] = w3[1];
-      b4q[0] = w4[0];
-      b4q[1] = w4[1];
-    } else {
-      b3q[0] = vtab[0][cls][2 * gi];
-      b3q[1] = vtab[0][cls][2 * gi + 1];
-      b4q[0] = vtab[1][cls][2 * gi];
-      b4q[1] = vtab[1][cls][2 * gi + 1];
-    }
+    const uint32_t b3q[2] = {vtab[0][cls][2 * gi], vtab[0][cls][2 * gi + 1]};  // four bases per word
+    const uint32_t b4q[2] = {vtab[1][cls][2 * gi], vtab[1][cls][2 * gi + 1]};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int el = 8 * gi + j;
@@ -199,6 +253,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
       n4 += 1;
     }
     if (mode == 2u) nraw += 1;
+  }
   }
   // exclusive scans of the 4-bit and raw group counts (packed; each total is at most 1024)
   const int packed = n4 | (nraw << 16);
