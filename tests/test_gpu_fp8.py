@@ -114,3 +114,34 @@ def test_fp8_random_bytes_overflow_and_edges(fmt):
     torch.cuda.synchronize()
     assert int(status.item()) == G.EINVAL
     assert ((e2.cpu().numpy().astype(np.int64) & 0xFFFF) == 0xFFFF).all()
+
+
+@pytest.mark.parametrize("fmt", [G.FP8_E4M3, G.FP8_E5M2])
+def test_fp8_out_of_range_bases_match_oracle(fmt):
+    """A row with a base3 above 248 or a base4 above 240 (calibration never gives one) is encoded
+    element by element; every tile, of those rows and of the others, must equal the oracle's."""
+    T, H = 256, 4
+    k, v = W.make_kv(0, 1, 1, T, H, device="cuda")
+    k8, v8 = _fp8(k[0], fmt), _fp8(v[0], fmt)
+    b3 = torch.zeros((2 * H, 128), dtype=torch.uint8, device="cuda")
+    b4 = torch.zeros_like(b3)
+    G.fp8_calibrate(k8, fmt, b3[:H], b4[:H])
+    G.fp8_calibrate(v8, fmt, b3[H:], b4[H:])
+    b3[0, 5] = 250  # K row 0
+    b4[H + 1, 77] = 245  # V row 1
+    tiles = torch.cat([_tiles(k8), _tiles(v8)])
+    nb = T // 64
+    kinds = torch.cat([torch.zeros(H * nb, dtype=torch.uint8), torch.ones(H * nb, dtype=torch.uint8)]).cuda()
+    rows = torch.cat([torch.arange(H).repeat_interleave(nb), H + torch.arange(H).repeat_interleave(nb)]).int().cuda()
+    slots, esc, back, status, _ = _run(tiles, kinds, rows, b3, b4, fmt)
+    assert status == 0
+    tn, sn, bn = tiles.cpu().numpy(), slots.cpu().numpy(), back.cpu().numpy()
+    kn, rn, b3n, b4n = kinds.cpu().numpy(), rows.cpu().numpy(), b3.cpu().numpy(), b4.cpu().numpy()
+    for i in range(tn.shape[0]):
+        img, oesc = O.fp8_encode_tile(tn[i], int(kn[i]), fmt, b3n[rn[i]], b4n[rn[i]])
+        if oesc < 0:
+            assert esc[i] == 0xFFFF, i
+            continue
+        assert esc[i] == oesc, i
+        np.testing.assert_array_equal(sn[i], img, err_msg=f"tile {i}")
+        np.testing.assert_array_equal(bn[i], tn[i])
