@@ -30,7 +30,7 @@ struct DecompressArgs {
 };
 
 // grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
-__global__ void __launch_bounds__(kDecThreads) decompress_kernel(DecompressArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 8) decompress_kernel(DecompressArgs a) {
   __shared__ alignas(16) uint16_t logical[kLogicalElems];  // [t][c], padded rows
   __shared__ int word_prefix[65];
   __shared__ uint32_t vbt[2][16][8];  // V: base words of the unit classes
@@ -98,7 +98,7 @@ struct DecodeTilesArgs {
 
 // grid (n_tiles): one CTA rebuilds one slot image of the batch into its
 // token-major tile (tiles whose esc_len is 0xFFFF are skipped).
-__global__ void __launch_bounds__(kDecThreads) decode_tiles_kernel(DecodeTilesArgs a) {
+__global__ void __launch_bounds__(kDecThreads, 8) decode_tiles_kernel(DecodeTilesArgs a) {
   __shared__ alignas(16) uint16_t logical[kLogicalElems];
   __shared__ int word_prefix[65];
   __shared__ uint32_t vbt[2][16][8];  // V: base words of the unit classes

@@ -266,7 +266,7 @@ __device__ __forceinline__ uint32_t fields_to_bytes(uint32_t g, int w) {
   return (g & m) | (((g >> w) & m) << 8) | (((g >> (2 * w)) & m) << 16) | (((g >> (3 * w)) & m) << 24);
 }
 
-__global__ void __launch_bounds__(kNThreads) nested_decode_kernel(NestedArgs a) {
+__global__ void __launch_bounds__(kNThreads, 6) nested_decode_kernel(NestedArgs a) {
   __shared__ alignas(16) uint16_t logical[kLogicalElems];
   __shared__ uint32_t vbt[2][16][8];  // V: base3 / base4 words of the unit classes
   __shared__ uint32_t vbt2[16][8];    // V: base2 words
