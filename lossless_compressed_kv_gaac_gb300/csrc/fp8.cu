@@ -113,7 +113,7 @@ struct Fp8Args {
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(kFp8Threads) fp8_encode_kernel(Fp8Args a) {
+__global__ void __launch_bounds__(kFp8Threads, 6) fp8_encode_kernel(Fp8Args a) {
   __shared__ alignas(16) uint8_t seq[kTile];  // the tile in storage order
   __shared__ uint32_t vtab[2][16][8];         // V: base3 / base4 words of the 16 unit classes
   __shared__ int warp_sums[kFp8Threads / 32];
