@@ -44,9 +44,6 @@ struct EncBlockShared : EncCommon {
   alignas(16) uint16_t vtile[kTile];
 };
 
-// Channel of storage element s (format v3).
-__device__ __forceinline__ int channel_of(int kind, int s) { return kind == 0 ? (s & 127) : v_channel_of(s); }
-
 // Token of storage element s (format v3).
 __device__ __forceinline__ int token_of(int kind, int s) { return kind == 0 ? (s >> 7) : v_token_of(s); }
 
