@@ -823,6 +823,10 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   __shared__ int esc_old;
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1, b = blockIdx.y;
   const int tid = threadIdx.x;
+  // Launched as a programmatic dependent: wait for the previous kernel on the stream (and its memory)
+  // before the first read, then let the length bump that follows be scheduled.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int len = a.seq_lens[b];
   if (len < 0 || len >= a.max_blocks * kBlock) {
     if (tid == 0) report(a.status, GAAC_EINVAL);
@@ -1023,6 +1027,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_tiles_kernel(EncodeTilesAr
 }
 
 __global__ void bump_lens_kernel(int32_t* lens, int batch) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the append kernel has read every length
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < batch) lens[i] += 1;
 }
@@ -1099,9 +1104,21 @@ extern "C" int gaac_append_ex(const uint16_t* k_new, const uint16_t* v_new, int3
   AppendArgs a{k_new, v_new, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids, *pools,
                stats, flags, d_status};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  append_kernel<<<dim3(2 * n_kv_heads, batch), kEncThreads, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return GAAC_ECUDA;
-  bump_lens_kernel<<<(batch + 255) / 256, 256, 0, st>>>(seq_lens, batch);
+  // Both kernels are programmatic dependents of their predecessor on the stream (each waits for it before
+  // any read): a launch is set up while the previous kernel runs.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * n_kv_heads, batch);
+  cfg.blockDim = dim3(kEncThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, append_kernel, a) != cudaSuccess) return GAAC_ECUDA;
+  cfg.gridDim = dim3((batch + 255) / 256);
+  cfg.blockDim = dim3(256);
+  if (cudaLaunchKernelEx(&cfg, bump_lens_kernel, seq_lens, batch) != cudaSuccess) return GAAC_ECUDA;
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
 
