@@ -116,6 +116,85 @@ __device__ __forceinline__ uint32_t escape_nibble(uint32_t d4) {
   return (((d4 >> 3) & 0x01010101u) * 0x01020408u) >> 24;
 }
 
+// The group loop element by element (open tiles, whose absent elements take no
+// part; bases outside the calibrated ranges).  Rare, so kept out of line: the
+// word-wide loop then gets the registers.
+struct UnitCodes {
+  uint32_t W[3], esc4, tagbyte, counts;
+  int n4, nraw;
+};
+
+template <bool kOpen>
+__device__ __noinline__ void encode_groups_elementwise(const uint16_t* unit, int kind, int u, const EncCommon* sh,
+                                                       int cls, int n_present, UnitCodes* out) {
+  const uint4* src = reinterpret_cast<const uint4*>(unit);
+  uint32_t W[3] = {0, 0, 0};
+  uint32_t esc4 = 0, tagbyte = 0, counts = 0;
+  int n4 = 0, nraw = 0;
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    int e[8], b3[8], b4[8];
+    bool pres[8];
+    bool fits3 = true, fits4 = true;
+    const uint4 gq = src[gi];  // the group's 8 values
+    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+    const uint32_t b3q[2] = {sh->vtab[0][cls][2 * gi], sh->vtab[0][cls][2 * gi + 1]};  // four bases per word
+    const uint32_t b4q[2] = {sh->vtab[1][cls][2 * gi], sh->vtab[1][cls][2 * gi + 1]};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int el = 8 * gi + j;
+      pres[j] = !kOpen || token_of(kind, 32 * u + el) < n_present;
+      const uint32_t x = (gw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+      e[j] = (x >> 7) & 0xFF;
+      b3[j] = (b3q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      b4[j] = (b4q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      const int o3 = e[j] - b3[j], o4 = e[j] - b4[j];
+      fits3 = fits3 && (!pres[j] || ((o3 >= 0) && (o3 <= 7)));
+      fits4 = fits4 && (!pres[j] || ((o4 >= 0) && (o4 <= 15)));
+    }
+    const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
+    tagbyte |= mode << (2 * gi);
+    counts += mode == 0u ? 1u : (mode == 1u ? 0x10000u : 0u);
+    uint32_t eb = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t cd = 0;  // raw groups keep code 0: their exponents are escape bytes
+      if (!pres[j]) {
+        // absent element: code and escape bit zero
+      } else if (mode == 0u) {
+        cd = static_cast<uint32_t>(e[j] - b3[j]) & 7u;
+      } else if (mode == 1u) {
+        const uint32_t off = static_cast<uint32_t>(e[j] - b4[j]) & 0xFFu;
+        cd = off & 7u;
+        eb |= ((off >> 3) & 1u) << j;
+      }
+      // format v3 placement: element 16h + 4q + L of the unit goes to byte lane L of W[h] (q = 0: bits
+      // 0-2, q = 1: bits 3-5, q = 3: bits 6-7 with its third bit in W[2] bit 6+h) or of W[2] (q = 2: bits 3h..)
+      const int h = gi >> 1, q = (8 * (gi & 1) + j) >> 2, L = j & 3;
+      if (q == 0) W[h] |= cd << (8 * L);
+      if (q == 1) W[h] |= cd << (8 * L + 3);
+      if (q == 2) W[2] |= cd << (8 * L + 3 * h);
+      if (q == 3) {
+        W[h] |= (cd & 3u) << (8 * L + 6);
+        W[2] |= ((cd >> 2) & 1u) << (8 * L + 6 + h);
+      }
+    }
+    if (mode == 1u) {
+      esc4 |= eb << (8 * n4);
+      n4 += 1;
+    }
+    if (mode == 2u) nraw += 1;
+  }
+  out->W[0] = W[0];
+  out->W[1] = W[1];
+  out->W[2] = W[2];
+  out->esc4 = esc4;
+  out->tagbyte = tagbyte;
+  out->counts = counts;
+  out->n4 = n4;
+  out->nraw = nraw;
+}
+
 // Encodes a staged tile into `slot` (global, 16-byte aligned) unless its
 // escape stream exceeds the capacity.  `unit`: this thread's 32 values (code
 // unit u = threadIdx.x, storage elements 32u .. 32u+31; 16-byte aligned).  Returns the escape length, or -1 when
@@ -200,60 +279,16 @@ __device__ __noinline__ int encode_tile_cta(EncCommon* sh, const uint16_t* unit,
       if (mode == 2u) nraw += 1;
     }
   } else {
-#pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    int e[8], b3[8], b4[8];
-    bool pres[8];
-    bool fits3 = true, fits4 = true;
-    const uint4 gq = src[gi];  // the group's 8 values
-    const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
-    const uint32_t b3q[2] = {sh->vtab[0][cls][2 * gi], sh->vtab[0][cls][2 * gi + 1]};  // four bases per word
-    const uint32_t b4q[2] = {sh->vtab[1][cls][2 * gi], sh->vtab[1][cls][2 * gi + 1]};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int el = 8 * gi + j;
-      pres[j] = !kOpen || token_of(kind, 32 * u + el) < n_present;
-      const uint32_t x = (gw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-      e[j] = (x >> 7) & 0xFF;
-      b3[j] = (b3q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      b4[j] = (b4q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      const int o3 = e[j] - b3[j], o4 = e[j] - b4[j];
-      fits3 = fits3 && (!pres[j] || ((o3 >= 0) && (o3 <= 7)));
-      fits4 = fits4 && (!pres[j] || ((o4 >= 0) && (o4 <= 15)));
-    }
-    const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
-    tagbyte |= mode << (2 * gi);
-    counts += mode == 0u ? 1u : (mode == 1u ? 0x10000u : 0u);
-    uint32_t eb = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t cd = 0;  // raw groups keep code 0: their exponents are escape bytes
-      if (!pres[j]) {
-        // absent element: code and escape bit zero
-      } else if (mode == 0u) {
-        cd = static_cast<uint32_t>(e[j] - b3[j]) & 7u;
-      } else if (mode == 1u) {
-        const uint32_t off = static_cast<uint32_t>(e[j] - b4[j]) & 0xFFu;
-        cd = off & 7u;
-        eb |= ((off >> 3) & 1u) << j;
-      }
-      // format v3 placement: element 16h + 4q + L of the unit goes to byte lane L of W[h] (q = 0: bits
-      // 0-2, q = 1: bits 3-5, q = 3: bits 6-7 with its third bit in W[2] bit 6+h) or of W[2] (q = 2: bits 3h..)
-      const int h = gi >> 1, q = (8 * (gi & 1) + j) >> 2, L = j & 3;
-      if (q == 0) W[h] |= cd << (8 * L);
-      if (q == 1) W[h] |= cd << (8 * L + 3);
-      if (q == 2) W[2] |= cd << (8 * L + 3 * h);
-      if (q == 3) {
-        W[h] |= (cd & 3u) << (8 * L + 6);
-        W[2] |= ((cd >> 2) & 1u) << (8 * L + 6 + h);
-      }
-    }
-    if (mode == 1u) {
-      esc4 |= eb << (8 * n4);
-      n4 += 1;
-    }
-    if (mode == 2u) nraw += 1;
-  }
+    UnitCodes uc;
+    encode_groups_elementwise<kOpen>(unit, kind, u, sh, cls, n_present, &uc);
+    W[0] = uc.W[0];
+    W[1] = uc.W[1];
+    W[2] = uc.W[2];
+    esc4 = uc.esc4;
+    tagbyte = uc.tagbyte;
+    counts = uc.counts;
+    n4 = uc.n4;
+    nraw = uc.nraw;
   }
 
   // Exclusive scans over the CTA (unit order = group order) of the 4-bit and
@@ -514,7 +549,7 @@ __device__ __forceinline__ void encode_block_item(const EncodeArgs& a, const Blo
 // One CTA per item.  (A persistent variant that copied the next item's tile
 // while encoding the current one was slower: the scheduler already overlaps
 // the copies of some CTAs with the encoding of others.)
-__global__ void __launch_bounds__(kEncThreads, 5) encode_blocks_kernel(EncodeArgs a, int64_t n_items) {
+__global__ void __launch_bounds__(kEncThreads, 6) encode_blocks_kernel(EncodeArgs a, int64_t n_items) {
   extern __shared__ __align__(16) uint8_t enc_smem[];
   EncBlockShared& sh = *reinterpret_cast<EncBlockShared*>(enc_smem);
   const int tid = threadIdx.x;
