@@ -113,6 +113,77 @@ struct Fp8Args {
   int32_t* status;
 };
 
+// The group loop element by element (bases outside the calibrated ranges).  Rare, so kept out of line:
+// the word-wide loop then gets the registers.
+struct Fp8UnitCodes {
+  uint32_t CW[3], SW[4], esc4, tagbyte;
+  int n4, nraw, my_counts[3];
+};
+
+__device__ __noinline__ void fp8_groups_elementwise(const uint8_t* seq, int u, const Fp8Layout& L,
+                                                    const uint32_t (*vtab)[16][8], int cls, Fp8UnitCodes* out) {
+  const uint32_t emask = (1u << L.ew) - 1u, mmask = (1u << L.mw) - 1u;
+  uint32_t CW[3] = {0u, 0u, 0u};
+  uint32_t SW[4] = {0u, 0u, 0u, 0u};
+  uint32_t esc4 = 0, tagbyte = 0;
+  int n4 = 0, nraw = 0, my_counts[3] = {0, 0, 0};
+#pragma unroll
+  for (int gi = 0; gi < 4; ++gi) {
+    uint32_t e[8];
+    int b3[8], b4[8];
+    bool fits3 = true, fits4 = true;
+    const uint32_t b3q[2] = {vtab[0][cls][2 * gi], vtab[0][cls][2 * gi + 1]};  // four bases per word
+    const uint32_t b4q[2] = {vtab[1][cls][2 * gi], vtab[1][cls][2 * gi + 1]};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int el = 8 * gi + j;
+      const uint32_t x = seq[32 * u + el];
+      e[j] = (x >> L.mw) & emask;
+      const uint32_t smv = ((x >> 7) << L.mw) | (x & mmask);
+      if (L.ew == 4)
+        SW[el >> 3] |= smv << (4 * (el & 7));
+      else
+        put_field3(SW, el, smv);
+      b3[j] = (b3q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      b4[j] = (b4q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      const int o3 = static_cast<int>(e[j]) - b3[j], o4 = static_cast<int>(e[j]) - b4[j];
+      fits3 = fits3 && o3 >= 0 && o3 <= 7;
+      fits4 = fits4 && o4 >= 0 && o4 <= 15;
+    }
+    const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
+    tagbyte |= mode << (2 * gi);
+    my_counts[mode] += 1;
+    uint32_t eb = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t cd = 0;  // raw groups keep code 0: their exponents are escape bytes
+      if (mode == 0u) {
+        cd = (e[j] - static_cast<uint32_t>(b3[j])) & 7u;
+      } else if (mode == 1u) {
+        const uint32_t off = (e[j] - static_cast<uint32_t>(b4[j])) & 0xFFu;
+        cd = off & 7u;
+        eb |= ((off >> 3) & 1u) << j;
+      }
+      put_field3(CW, 8 * gi + j, cd);
+    }
+    if (mode == 1u) {
+      esc4 |= eb << (8 * n4);
+      n4 += 1;
+    }
+    if (mode == 2u) nraw += 1;
+  }
+#pragma unroll
+  for (int i = 0; i < 3; ++i) out->CW[i] = CW[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out->SW[i] = SW[i];
+  out->esc4 = esc4;
+  out->tagbyte = tagbyte;
+  out->n4 = n4;
+  out->nraw = nraw;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) out->my_counts[i] = my_counts[i];
+}
+
 __global__ void __launch_bounds__(kFp8Threads, 6) fp8_encode_kernel(Fp8Args a) {
   __shared__ alignas(16) uint8_t seq[kTile];  // the tile in storage order
   __shared__ uint32_t vtab[2][16][8];         // V: base3 / base4 words of the 16 unit classes
@@ -209,51 +280,18 @@ __global__ void __launch_bounds__(kFp8Threads, 6) fp8_encode_kernel(Fp8Args a) {
       if (mode == 2u) nraw += 1;
     }
   } else {
+    Fp8UnitCodes uc;
+    fp8_groups_elementwise(seq, u, L, vtab, cls, &uc);
 #pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    uint32_t e[8];
-    int b3[8], b4[8];
-    bool fits3 = true, fits4 = true;
-    const uint32_t b3q[2] = {vtab[0][cls][2 * gi], vtab[0][cls][2 * gi + 1]};  // four bases per word
-    const uint32_t b4q[2] = {vtab[1][cls][2 * gi], vtab[1][cls][2 * gi + 1]};
+    for (int i = 0; i < 3; ++i) CW[i] = uc.CW[i];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int el = 8 * gi + j;
-      const uint32_t x = seq[32 * u + el];
-      e[j] = (x >> L.mw) & emask;
-      const uint32_t smv = ((x >> 7) << L.mw) | (x & mmask);
-      if (L.ew == 4)
-        SW[el >> 3] |= smv << (4 * (el & 7));
-      else
-        put_field3(SW, el, smv);
-      b3[j] = (b3q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      b4[j] = (b4q[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      const int o3 = static_cast<int>(e[j]) - b3[j], o4 = static_cast<int>(e[j]) - b4[j];
-      fits3 = fits3 && o3 >= 0 && o3 <= 7;
-      fits4 = fits4 && o4 >= 0 && o4 <= 15;
-    }
-    const uint32_t mode = fits3 ? 0u : (fits4 ? 1u : 2u);
-    tagbyte |= mode << (2 * gi);
-    my_counts[mode] += 1;
-    uint32_t eb = 0;
+    for (int i = 0; i < 4; ++i) SW[i] = uc.SW[i];
+    esc4 = uc.esc4;
+    tagbyte = uc.tagbyte;
+    n4 = uc.n4;
+    nraw = uc.nraw;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t cd = 0;  // raw groups keep code 0: their exponents are escape bytes
-      if (mode == 0u) {
-        cd = (e[j] - static_cast<uint32_t>(b3[j])) & 7u;
-      } else if (mode == 1u) {
-        const uint32_t off = (e[j] - static_cast<uint32_t>(b4[j])) & 0xFFu;
-        cd = off & 7u;
-        eb |= ((off >> 3) & 1u) << j;
-      }
-      put_field3(CW, 8 * gi + j, cd);
-    }
-    if (mode == 1u) {
-      esc4 |= eb << (8 * n4);
-      n4 += 1;
-    }
-    if (mode == 2u) nraw += 1;
-  }
+    for (int i = 0; i < 3; ++i) my_counts[i] = uc.my_counts[i];
   }
   // exclusive scans of the 4-bit and raw group counts (packed; each total is at most 1024)
   const int packed = n4 | (nraw << 16);
