@@ -282,6 +282,8 @@ def mode_ablation(k, v, n_calib: int) -> dict:
     en = torch.empty(n, dtype=torch.int16, device=dev)
     G.encode_tiles(tiles, kinds, rows, b3, b4, s3, e3)
     G.nested_encode_tiles(tiles, kinds, rows, b2, b3, b4, sn, en)
+    c3 = time_calls(lambda: G.encode_tiles(tiles, kinds, rows, b3, b4, s3, e3))
+    cn = time_calls(lambda: G.nested_encode_tiles(tiles, kinds, rows, b2, b3, b4, sn, en))
     back = torch.empty_like(tiles)
     d3 = time_calls(lambda: G.decode_tiles(s3, e3, kinds, rows, b3, b4, back))
     dn = time_calls(lambda: G.nested_decode_tiles(sn, en, kinds, rows, b2, b3, b4, back))
@@ -300,7 +302,8 @@ def mode_ablation(k, v, n_calib: int) -> dict:
     return {"tiles": n, "payload_ratio_v3": round(raw / pay3, 4), "payload_ratio_nested": round(raw / payn, 4),
             "ratio_gain_pct": round(100 * (pay3 / payn - 1), 2),
             "decode_us_v3": round(d3 * 1e3, 1), "decode_us_nested": round(dn * 1e3, 1),
-            "decode_time_ratio": round(dn / d3, 3)}
+            "decode_time_ratio": round(dn / d3, 3),
+            "encode_us_v3": round(c3 * 1e3, 1), "encode_us_nested": round(cn * 1e3, 1)}
 
 
 def hd256_attention(device, n_calib: int) -> dict:

@@ -1042,7 +1042,7 @@ struct EncodeTilesArgs {
 };
 
 // grid (n_tiles): one CTA encodes one tile of the batch.
-__global__ void __launch_bounds__(kEncThreads) encode_tiles_kernel(EncodeTilesArgs a) {
+__global__ void __launch_bounds__(kEncThreads, 6) encode_tiles_kernel(EncodeTilesArgs a) {
   __shared__ EncShared sh;
   const int64_t i = blockIdx.x;
   const int tid = threadIdx.x;
