@@ -92,7 +92,7 @@ __device__ __forceinline__ void put_field(uint64_t& lo, uint32_t& hi, uint32_t v
   }
 }
 
-__global__ void __launch_bounds__(kNThreads) nested_encode_kernel(NestedArgs a) {
+__global__ void __launch_bounds__(kNThreads, 4) nested_encode_kernel(NestedArgs a) {
   __shared__ NestedEncShared sh;
   const int64_t i = blockIdx.x;
   const int u = threadIdx.x, lane = u & 31, warp = u >> 5;
