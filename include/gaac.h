@@ -241,7 +241,11 @@ GAAC_API int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_block
  *   out[b][hq][c] = sum_{t < seq_lens[b]} softmax_t(scale * q[b][hq] . k[b][t][hk]) v[b][t][hk][c]
  * with hk = hq / (n_q_heads / n_kv_heads), in fp32 (0 for an empty sequence).
  * q: BF16 bits [batch][n_q_heads][128]; out: fp32 [batch][n_q_heads][128].
- * n_q_heads / n_kv_heads must be an integer <= GAAC_MAX_GQA.
+ * n_q_heads / n_kv_heads must be an integer <= GAAC_MAX_GQA.  scale: any finite
+ * value (negative and zero included).  Every row whose logits scale * q . k_t are
+ * fp32 numbers with |scale| * sum_c |q_c k_tc| below the largest fp32 value is
+ * computed without overflow: the kernel subtracts each score's running maximum
+ * before it applies the scale.
  * workspace: at least gaac_attention_workspace(...) bytes, 16-byte aligned.  It holds
  * the split partials and, at its end, one counter per (sequence, kv-head) that
  * must be zero before the first call; every call leaves them at zero again.
@@ -292,7 +296,10 @@ GAAC_API int gaac_decode_attention_hd256(const uint16_t* q, int batch, int n_q_h
  * enqueues nothing.  It calls no allocator (no cudaMalloc, no cudaFree).
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
- *    stream capture.
+ *    stream capture.  Under CUDA's lazy module loading (the default) that
+ *    first call may also be what loads the library's device code on the
+ *    device, which reserves the array's 4 MiB there: a caller with a fixed
+ *    memory plan makes the first call during start-up.
  *  - Every call shares the one array.  Calls whose kernels overlap on the GPU
  *    (other streams, other threads) race on it and give wrong results; issue
  *    them in one stream or order them.  The array keeps the last call's

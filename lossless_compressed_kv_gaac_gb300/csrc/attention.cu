@@ -43,8 +43,13 @@
 //    re-joined by the lanes that own them.
 //  * Softmax in the log2 domain; rescales only when a running maximum rises;
 //    P goes to the tensor cores as a bf16 hi + lo pair (rounding near 2^-17).
-//  * q is pre-scaled by 2^-4 (exact for normal values) to keep q.k inside the
-//    fp32 range for extreme keys; the factor is folded into the softmax scale.
+//  * q is pre-scaled by +-2^-4 (exact for normal values; the sign is that of
+//    the softmax scale) so that q.k stays inside the fp32 range for extreme
+//    keys.  Running maxima are kept on these raw scores and only a score's
+//    difference from its maximum is multiplied by |scale| * 16 * log2(e), so
+//    no unshifted scaled logit is ever formed: a score whose logit is within
+//    the fp32 range never overflows, and a difference that does is a weight
+//    of exactly zero.
 //  * Partials (m, l, acc) per split go to the workspace; the last CTA of each
 //    (sequence, kv-head) to finish, found with a device counter, merges them
 //    with a log-sum-exp (the final split reduction) and resets the counter.
@@ -110,7 +115,8 @@ struct AttnArgs {
   int64_t n_raw;
   const uint8_t* base3;
   const uint8_t* base4;
-  float scale_log2;  // scale * 16 * log2(e)
+  float qmul;       // q multiplier: 2^-4 times the sign of the softmax scale (0 for a zero scale)
+  float c_log2;     // |scale| * 16 * log2(e): raw-score differences to log2 weights (1 for a zero scale)
   int Hq, Hkv, r, max_blocks, n_splits;  // Hkv: attention kv-heads (of NH half-heads each)
   float* part;
   unsigned int* counters;  // [batch][NH * Hkv] splits finished; zero between launches
@@ -120,10 +126,10 @@ struct AttnArgs {
 
 // ------------------------------------------------------------------ helpers
 
-// bf16x2 times 2^-4; exact whenever the result is a normal number.
-__device__ __forceinline__ uint32_t bf16x2_div16(uint32_t w) {
-  const float lo = __uint_as_float(w << 16) * 0.0625f;
-  const float hi = __uint_as_float(w & 0xFFFF0000u) * 0.0625f;
+// bf16x2 times f (+-2^-4 or 0); exact whenever the result is a normal number or zero.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t w, float f) {
+  const float lo = __uint_as_float(w << 16) * f;
+  const float hi = __uint_as_float(w & 0xFFFF0000u) * f;
   return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
 }
 
@@ -530,17 +536,18 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
       kbadA = __any_sync(kFull, isnan(sA[0]) || isnan(sA[1]));
       kbadB = __any_sync(kFull, isnan(sB[0]) || isnan(sB[1]));
     }
-    // ---- online softmax of head g over the warp's 16 tokens
-    const float x0 = (!kbadA && tA < nv) ? sA[0] * a.scale_log2 : -INFINITY;
-    const float x1 = (!kbadA && tA + 1 < nv) ? sA[1] * a.scale_log2 : -INFINITY;
-    const float x2 = (!kbadB && tB < nv) ? sB[0] * a.scale_log2 : -INFINITY;
-    const float x3 = (!kbadB && tB + 1 < nv) ? sB[1] * a.scale_log2 : -INFINITY;
+    // ---- online softmax of head g over the warp's 16 tokens, on raw scores (q/16).k: only the
+    // differences from the running maximum are scaled to the log2 domain
+    const float x0 = (!kbadA && tA < nv) ? sA[0] : -INFINITY;
+    const float x1 = (!kbadA && tA + 1 < nv) ? sA[1] : -INFINITY;
+    const float x2 = (!kbadB && tB < nv) ? sB[0] : -INFINITY;
+    const float x3 = (!kbadB && tB + 1 < nv) ? sB[1] : -INFINITY;
     float bm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
     bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
     const float mnew = fmaxf(mrun, bm);
     if (__any_sync(kFull, mnew != mrun)) {  // a running maximum rises: rescale (rare after the first blocks)
-      const float al = mrun == -INFINITY ? 0.f : fast_exp2(mrun - mnew);
+      const float al = mrun == -INFINITY ? 0.f : fast_exp2((mrun - mnew) * a.c_log2);
       lsum *= al;
       const float al0 = __shfl_sync(kFull, al, 8 * tq), al1 = __shfl_sync(kFull, al, 8 * tq + 4);  // heads 2tq, 2tq+1
 #pragma unroll
@@ -553,8 +560,9 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
       mrun = mnew;
     }
     const bool live = mrun != -INFINITY;
-    const float p0 = live ? fast_exp2(x0 - mrun) : 0.f, p1 = live ? fast_exp2(x1 - mrun) : 0.f;
-    const float p2 = live ? fast_exp2(x2 - mrun) : 0.f, p3 = live ? fast_exp2(x3 - mrun) : 0.f;
+    const float cl = a.c_log2;
+    const float p0 = live ? fast_exp2((x0 - mrun) * cl) : 0.f, p1 = live ? fast_exp2((x1 - mrun) * cl) : 0.f;
+    const float p2 = live ? fast_exp2((x2 - mrun) * cl) : 0.f, p3 = live ? fast_exp2((x3 - mrun) * cl) : 0.f;
     lsum += (p0 + p1) + (p2 + p3);
     // P^T as the B operand: rows (tokens) 2tq, 2tq+1 from octet A, 2tq+8, 2tq+9 from octet B; column = head g
     const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
@@ -606,7 +614,8 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
 
 // Log-sum-exp merge of the n_splits partials (m, l, acc) of one (sequence,
 // kv-head) into out[b, h*r + n, :] = sum_s w_s acc_s / sum_s w_s l_s with
-// w_s = 2^(m_s - max_s m_s) per head n (the final split reduction).  Runs on
+// w_s = 2^((m_s - max_s m_s) cl) per head n (the final split reduction; m_s are
+// raw-score maxima, cl converts their differences to the log2 domain).  Runs on
 // the CTA that finished last, so it is a tail on the critical path: each
 // thread owns one float4 column of the output and a subset of the splits,
 // issues that subset's loads ten at a time and folds them in with its own
@@ -614,7 +623,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
 // memory.  The staging ring is free by then and holds that exchange.
 // base: the first partial of the pair; out: its first output row.
 template <int NH, class Smem>
-__device__ __noinline__ void merge_splits(const float* base, int ns, int r, float* out, Smem& sm, int tid) {
+__device__ __noinline__ void merge_splits(const float* base, int ns, int r, float cl, float* out, Smem& sm, int tid) {
   constexpr int kBatch = 10;
   const int o4n = r * (kD / 4);  // float4 columns of the r x 128 output
   const int groups = kAttThreads / o4n;
@@ -642,7 +651,7 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, ml[u].x);
       if (mb != -INFINITY) {
-        const float al = mt == -INFINITY ? 0.f : fast_exp2(mt - mb);
+        const float al = mt == -INFINITY ? 0.f : fast_exp2((mt - mb) * cl);
         acc.x *= al;
         acc.y *= al;
         acc.z *= al;
@@ -650,7 +659,7 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
         den *= al;
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-          const float w = ml[u].x == -INFINITY ? 0.f : fast_exp2(ml[u].x - mb);
+          const float w = ml[u].x == -INFINITY ? 0.f : fast_exp2((ml[u].x - mb) * cl);
           acc.x += w * v[u].x;
           acc.y += w * v[u].y;
           acc.z += w * v[u].z;
@@ -672,7 +681,7 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
     float mx = mt;
     for (int gi = 1; gi < groups; ++gi) mx = fmaxf(mx, xm[gi * o4n + o4].x);
     if (mx != -INFINITY) {
-      const float al = mt == -INFINITY ? 0.f : fast_exp2(mt - mx);
+      const float al = mt == -INFINITY ? 0.f : fast_exp2((mt - mx) * cl);
       acc.x *= al;
       acc.y *= al;
       acc.z *= al;
@@ -681,7 +690,7 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
       for (int gi = 1; gi < groups; ++gi) {
         const float2 md = xm[gi * o4n + o4];
         if (md.x == -INFINITY) continue;
-        const float w = fast_exp2(md.x - mx);
+        const float w = fast_exp2((md.x - mx) * cl);
         const float4 x = xa[gi * o4n + o4];
         acc.x += w * x.x;
         acc.y += w * x.y;
@@ -775,7 +784,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     if (n < a.r) {
       const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + H * a.r + n) * (NH * kD) +
                              kD * (KH == NH ? half : hf) + 32 * tq + 4 * m + odd;
-      v = bf16x2_div16(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16));
+      v = bf16x2_mul(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16), a.qmul);
     }
     reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd] = v;
     reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd + 1] = 0u;
@@ -804,13 +813,13 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
 #pragma unroll
     for (int i = 0; i < kCWarps; ++i) mx = fmaxf(mx, sm.wm[i][n]);
     const float mw = sm.wm[cw][n];
-    sm.ww[cw][n] = mw == -INFINITY ? 0.f : fast_exp2(mw - mx);
+    sm.ww[cw][n] = mw == -INFINITY ? 0.f : fast_exp2((mw - mx) * a.c_log2);
     if (cw == 0) {
       float lt = 0.f;
 #pragma unroll
       for (int i = 0; i < kCWarps; ++i) {
         const float mi = sm.wm[i][n];
-        lt += (mi == -INFINITY ? 0.f : fast_exp2(mi - mx)) * sm.wl[i][n];
+        lt += (mi == -INFINITY ? 0.f : fast_exp2((mi - mx) * a.c_log2)) * sm.wl[i][n];
       }
       part[2 * n] = mx;
       part[2 * n + 1] = lt;
@@ -852,7 +861,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   if (tid == 0) sm.last = atomic_add_acq_rel(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
   __syncthreads();
   if (!sm.last) return;
-  merge_splits<NH>(a.part + (static_cast<size_t>(b) * nkv + y) * a.n_splits * kPartFloats, a.n_splits, r,
+  merge_splits<NH>(a.part + (static_cast<size_t>(b) * nkv + y) * a.n_splits * kPartFloats, a.n_splits, r, a.c_log2,
                    a.out + (static_cast<size_t>(b) * a.Hq + H * r) * (NH * kD) + kD * hf, sm, tid);
   if (tid == 0) *counter = 0u;
 }
@@ -945,11 +954,14 @@ extern "C" size_t gaac_attention_workspace(int batch, int n_kv_heads, int max_bl
 
 // Checks and launch shared by the 128- and 256-channel entry points; n_kv_heads
 // counts attention kv-heads, each of NH half-heads in the table and the bases.
+// clear_counters: zero the workspace's merge counters on the stream once every
+// check has passed (a call that fails a check enqueues nothing).
 template <int NH>
 static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
                             const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
                             const uint8_t* base3, const uint8_t* base4, float scale, int n_splits, float* out,
-                            void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
+                            void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream,
+                            bool clear_counters = false) {
   if (q == nullptr || seq_lens == nullptr || table == nullptr || pools == nullptr || pools->slot_pool == nullptr ||
       pools->raw_pool == nullptr || pools->n_slots < 0 || pools->n_raw < 0 || base3 == nullptr ||
       base4 == nullptr || out == nullptr || workspace == nullptr)
@@ -986,7 +998,10 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
   a.n_raw = pools->n_raw;
   a.base3 = base3;
   a.base4 = base4;
-  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 16.0 * 1.4426950408889634);
+  // Scores are (q * qmul) . k; weights 2^((s - m) * c_log2) = e^(scale (q.k - max q.k)).  The sign of
+  // the scale goes into q (exactly), so the running maxima are maxima of the logits for either sign.
+  a.qmul = scale > 0.f ? 0.0625f : (scale < 0.f ? -0.0625f : 0.f);
+  a.c_log2 = scale != 0.f ? static_cast<float>(std::fabs(static_cast<double>(scale)) * 16.0 * 1.4426950408889634) : 1.f;
   a.Hq = n_q_heads;
   a.Hkv = n_kv_heads;
   a.r = n_q_heads / n_kv_heads;
@@ -997,6 +1012,9 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
   a.out = out;
   a.status = d_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (clear_counters &&
+      cudaMemsetAsync(a.counters, 0, static_cast<size_t>(batch) * nkv * sizeof(unsigned int), st) != cudaSuccess)
+    return GAAC_ECUDA;
   if (NH > KH) {
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pair_config<NH, KH>(dim3(n_splits, nkv, batch), st, attr);
@@ -1071,12 +1089,8 @@ extern "C" int gaac_decode_attention_noalloc(const uint16_t* q, int batch, int n
   if (gaac_attention_workspace(batch, n_kv_heads, max_blocks, ns) > kStaticScratchBytes) return GAAC_EINVAL;
   void* scratch = static_scratch_address();
   if (scratch == nullptr) return GAAC_ECUDA;
-  // The merge counters must start at zero; clear them on every call so that a
-  // call never depends on how an earlier one ended.
-  const size_t cbytes = static_cast<size_t>(batch) * n_kv_heads * sizeof(unsigned int);
-  if (cudaMemsetAsync(static_cast<char*>(scratch) + partials_bytes(batch, n_kv_heads, ns), 0, cbytes,
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return GAAC_ECUDA;
-  return gaac_decode_attention(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, base3, base4,
-                               scale, ns, out, scratch, kStaticScratchBytes, d_status, stream);
+  // The merge counters must start at zero: every call clears the ones it uses (after its argument
+  // checks, so a rejected call leaves the array untouched) and never depends on how an earlier call ended.
+  return launch_attention<1>(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, base3, base4,
+                             scale, ns, out, scratch, kStaticScratchBytes, d_status, stream, true);
 }

@@ -557,12 +557,17 @@ void gaac_ref_fp8_mode_counts(const uint8_t* img, int fmt, int64_t* counts4) {
  * a 256-dimensional head is represented as two 128-dimensional half-heads; the
  * attention still runs over the whole head).
  * out[hq*128 + c] = sum_t softmax_t(scale * q.k_t) v_t[c]; T == 0 gives zeros.
- * flags (may be NULL), per q head: bit 0 set if some token's sum_c |q_c k_tc|
- * reaches 2^130 (a dot product of q/16 and k, or its product with the scale,
- * may then leave the fp32 range); bit 1 set if some channel's sum_t w_t |v_tc|
- * (w_t = the unnormalised softmax weight, at most 1) exceeds the largest fp32
- * value (an fp32 accumulator may then overflow).  Such rows are not
- * comparable with an fp32 kernel and are reported apart. */
+ * flags (may be NULL), per q head, mark rows whose quantities leave the fp32
+ * range, so that no fp32 evaluation of them can be held to a tolerance:
+ *   bit 0: for some token, |scale| * sum_c |q_c k_tc| exceeds the largest
+ *          finite fp32 value.  That sum bounds the logit scale * q.k_t and
+ *          every partial sum of its terms scale * q_c * k_tc, so below it the
+ *          logit has an fp32 value reachable in any order of summation.
+ *   bit 1: for some channel, sum_t w_t |v_tc| exceeds the largest finite fp32
+ *          value, w_t = exp(logit_t - max logit) being the unnormalised
+ *          softmax weight (at most 1): the numerator of the softmax-weighted
+ *          sum then has no fp32 value.
+ * Such rows are reported apart from the ones compared with a tolerance. */
 static double bf16_to_double(uint16_t x) {
     uint32_t u = (uint32_t)x << 16;
     float f;
@@ -587,7 +592,7 @@ void gaac_ref_attention_d(const uint16_t* q, const uint16_t* k, const uint16_t* 
                 dot += qc * kc;
                 mag += fabs(qc * kc);
             }
-            if (mag >= ldexp(1.0, 130)) flag |= 1;
+            if (fabs(scale) * mag > 3.4028234663852886e38) flag |= 1;
             logits_scratch[t] = scale * dot;
             if (logits_scratch[t] > m) m = logits_scratch[t];
         }

@@ -144,6 +144,28 @@ def test_attention_range_flags(orc):
     assert (flags == 2).all()
 
 
+def test_attention_range_flag_boundary(orc):
+    """Bit 0 marks a row once |scale| * sum_c |q_c k_c| of some token passes the largest fp32 value, and
+    not before: with q = 1 and one token's 128 keys at 2^124, the sum is 2^131 and the logit at scale
+    2^-3.5 is 2^127.5 (representable, unflagged); at 2^125 the bound is 2^128.5 (flagged).  A negative
+    scale has the same magnitudes.  The unflagged extreme row's output is that token's value row: its
+    weight is 1 and every other weight underflows to 0 in fp64."""
+    Hq, Hkv, T = 2, 1, 5
+    q = np.full((Hq, 128), 0x3F80, np.uint16)  # 1.0
+    k = np.full((T, Hkv, 128), 0x3F80, np.uint16)
+    v = _f32_to_bf16_bits(np.arange(T * 128, dtype=np.float64).reshape(T, Hkv, 128) / 64.0)
+    scale = 2.0 ** -3.5
+    for s_ in (scale, -scale):
+        k[3, 0, :] = 0x7D80  # 2^124
+        out, flags = orc.attention(q, k, v, s_)
+        assert (flags == 0).all()
+        if s_ > 0:
+            np.testing.assert_array_equal(out, np.broadcast_to(_bf16_to_f64(v[3, 0]), out.shape))
+        k[3, 0, :] = 0x7E00  # 2^125
+        _, flags = orc.attention(q, k, v, s_)
+        assert (flags == 1).all()
+
+
 def test_attention_on_decoded_cache_equals_original(orc):
     """Attention reads the decoded cache; by losslessness it must equal attention
     on the original cache exactly (this pins the codec-to-attention plumbing)."""
