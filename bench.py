@@ -69,6 +69,9 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--study", choices=["rope-drift"], default=None,
                    help="rope-drift: escape bytes per tile along 32K rotary keys for short and long calibration")
+    p.add_argument("--timeline", action="store_true",
+                   help="build the instrumented library and print the per-CTA timeline of one attention launch over "
+                        "one layer of the workload (compressed, then BF16), instead of the benchmark")
     return p.parse_args()
 
 
@@ -521,23 +524,33 @@ def run_gaac(args):
     region_launch_ms = ms_per_step / L  # average launch duration inside the timed graph replays
     achieved_gbs = alg_launch / (region_launch_ms * 1e-3) / 1e9
 
-    # ---- uncompressed BF16 baseline: the same kernel over an all-raw cache
-    bf16_ms = None
+    # ---- uncompressed BF16 baseline: the BF16 kernel (the attention kernel specialised to raw tiles, no
+    # decode path) over an all-raw cache of the same layers; also the compressed kernel's own raw path
+    bf16_ms = raw_path_ms = None
     try:
         raw_caches, _ = build_layers(L, device, raw=True)
 
-        def step_raw():
+        def step_raw(bf16):
             for c, q, o in zip(raw_caches, qs, outs):
-                c.attention(q, scale, out=o)
+                c.attention(q, scale, out=o, bf16=bf16)
 
-        with torch.cuda.stream(stream):
-            step_raw()
-        torch.cuda.synchronize()
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            step_raw()
-        bf16_ms = time_graph(g2, stream, args.steps) / args.steps
-        del raw_caches, g2
+        times = {}
+        for bf16 in (True, False):
+            with torch.cuda.stream(stream):
+                step_raw(bf16)
+            torch.cuda.synchronize()
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2, stream=stream):
+                step_raw(bf16)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g2.replay()
+            times[bf16] = time_graph(g2, stream, args.steps) / args.steps
+            del g2
+        for c in raw_caches:
+            assert int(c.status.item()) == 0, "BF16 attention reported an error"
+        bf16_ms, raw_path_ms = times[True], times[False]
+        del raw_caches
     except torch.cuda.OutOfMemoryError:
         bf16_ms = None
     torch.cuda.empty_cache()
@@ -581,6 +594,8 @@ def run_gaac(args):
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["kernel_sha"] == kernel_sha() else None
+    # BF16 kernel: per layer 16,384 raw tiles of 16 KiB plus 8 B per table entry
+    bf16_bytes = L * (raw_bytes_layer + 2 * (wl.seq_len // 64) * wl.n_kv_heads * 8)
 
     result = {
         "metric": METRIC,
@@ -603,6 +618,13 @@ def run_gaac(args):
         "equiv_uncompressed_gbs": round(raw_step / (ms_per_step * 1e-3) / 1e9, 1),
         "bf16_cache_us_per_step": round(bf16_ms * 1e3, 2) if bf16_ms else None,
         "speedup_vs_bf16_cache": round(bf16_ms / ms_per_step, 3) if bf16_ms else None,
+        "bf16_kernel": ({"us_per_step": round(bf16_ms * 1e3, 2), "gbs": round(bf16_bytes / (bf16_ms * 1e-3) / 1e9, 1),
+                         "frac": round(bf16_bytes / (bf16_ms * 1e-3) / 1e9 / peak, 4),
+                         "bytes_per_step": bf16_bytes,
+                         "kernel": "attn_split_kernel<1, 1, true>: the attention kernel specialised to raw tiles "
+                                   "(no decode path), all-raw BF16 cache of the same layers",
+                         "raw_cache_through_compressed_kernel_us_per_step": round(raw_path_ms * 1e3, 2)}
+                        if bf16_ms else None),
         "bf16_sdpa": sdpa,
         "encode_gbs": round(encode_gbs, 1),
         "decompress_gbs": round(decompress_gbs, 1),
@@ -805,8 +827,77 @@ def rope_drift_study() -> dict:
     return out
 
 
+def timeline_summary(raw, n_ctas: int, n_blocks: int, grid) -> dict:
+    """Per-CTA timeline records (u64 ns: start, split_end, exit, merged, then issue/arrive/land/release per
+    block) of one launch with grid (splits, kv-heads, batch), summarised in microseconds."""
+    import numpy as np
+
+    X, Y, Z = grid
+    n = X * Y * Z
+    rec = raw.reshape(n_ctas, -1)[:n].astype(np.float64)
+    start, split_end, exit_, merged = rec[:, 0], rec[:, 1], rec[:, 2], rec[:, 3]
+    issue, arrive, land, release = (rec[:, 4 + i * n_blocks: 4 + (i + 1) * n_blocks] for i in range(4))
+    t0 = start.min()
+    end = np.maximum(exit_, merged)
+    used = land > 0
+    q = lambda x, p: round(float(np.percentile(x, p)) / 1e3, 3) if x.size else None
+    inflight = (land - issue)[used]
+    waited = (land - arrive)[used]
+    return {"ctas": n, "span_us": round((end.max() - t0) / 1e3, 2),
+            "start_spread_us": round((start.max() - t0) / 1e3, 2),
+            "split_work_us": {"min": round((split_end - start).min() / 1e3, 2),
+                              "mean": round((split_end - start).mean() / 1e3, 2),
+                              "max": round((split_end - start).max() / 1e3, 2)},
+            "split_end_spread_us": round((split_end.max() - split_end.min()) / 1e3, 2),
+            "merge_us": {"mean": round(float((merged - exit_)[merged > 0].mean()) / 1e3, 2),
+                         "max": round(float((merged - exit_)[merged > 0].max()) / 1e3, 2)},
+            "copy_issue_to_land_us": {"p10": q(inflight, 10), "p50": q(inflight, 50), "p90": q(inflight, 90)},
+            "group_wait_for_data_us": {"p10": q(waited, 10), "p50": q(waited, 50), "p90": q(waited, 90)},
+            "blocks_per_cta": round(float(used.sum(axis=1).mean()), 1)}
+
+
+def run_timeline() -> None:
+    """One Qwen3-8B-shaped layer (T = 65,536) through the instrumented library: the per-CTA timeline of the
+    third attention launch over the compressed cache and over the all-raw cache with the BF16 kernel."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import gaac_workloads as W
+    import lossless_compressed_kv_gaac_gb300 as G
+    from lossless_compressed_kv_gaac_gb300 import build as B
+
+    G.LIB_PATH = B.build(timeline=True)
+    L = G.lib()
+    L.gaac_timeline_fetch.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p]
+    cb, nc, nb = ctypes.c_size_t(), ctypes.c_int(), ctypes.c_int()
+    L.gaac_timeline_fetch(None, 0, ctypes.byref(cb), ctypes.byref(nc), ctypes.byref(nb))
+    dev = torch.device("cuda", 0)
+    wl = W.WORKLOADS[CONFIG_ID]
+    out = {"timeline": "one layer, T=65536, 32q/8kv, batch 1 (third launch)"}
+    for name, raw in (("compressed", False), ("bf16", True)):
+        caches, qs = build_layers(1, dev, raw=raw)
+        c, q = caches[0], qs[0]
+        for _ in range(3):
+            o = c.attention(q, wl.scale, bf16=raw)
+        torch.cuda.synchronize()
+        assert int(c.status.item()) == 0
+        buf = np.zeros(nc.value * cb.value // 8, np.uint64)
+        G._check("gaac_timeline_fetch", L.gaac_timeline_fetch(buf.ctypes.data, buf.nbytes, None, None, None))
+        ns = G.lib().gaac_attention_auto_splits(1, wl.n_kv_heads, c.max_blocks)
+        out[name] = timeline_summary(buf, nc.value, nb.value, (ns, wl.n_kv_heads, 1))
+        del caches, o
+        torch.cuda.empty_cache()
+    print(json.dumps(out))
+
+
 def main():
     args = parse()
+    if args.timeline:
+        run_timeline()
+        return
     if args.study == "rope-drift":
         print(json.dumps(rope_drift_study()))
         return

@@ -246,9 +246,11 @@ GAAC_API int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_block
  * fp32 numbers with |scale| * sum_c |q_c k_tc| below the largest fp32 value is
  * computed without overflow: the kernel subtracts each score's running maximum
  * before it applies the scale.
- * workspace: at least gaac_attention_workspace(...) bytes, 16-byte aligned.  It holds
- * the split partials and, at its end, one counter per (sequence, kv-head) that
- * must be zero before the first call; every call leaves them at zero again.
+ * workspace: at least gaac_attention_workspace(...) bytes, 16-byte aligned.  It opens
+ * with one counter per (sequence, kv-head) (u32, the block rounded up to 16 bytes)
+ * that must be zero before the first call; every call leaves them at zero again,
+ * whatever its split count, so one workspace serves calls with different counts.
+ * The split partials follow the counters.
  * After a call that reported an error, zero the workspace before reusing it.
  * pools: only slot_pool, n_slots, raw_pool and n_raw are read; both pools must be
  * 16-byte aligned (tiles are fetched with bulk copies).  A table entry that is
@@ -259,6 +261,24 @@ GAAC_API int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads, 
                           const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
                           const uint8_t* base3, const uint8_t* base4, float scale, int n_splits, float* out,
                           void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream);
+
+/*
+ * Decode attention over an uncompressed BF16 cache: the same kernel as
+ * gaac_decode_attention (grid, staging ring, tensor-core QK^T and PV^T, online
+ * softmax, split merge) specialised to raw tiles, with no decode path.  Every
+ * table entry of a block below seq_lens must be a raw tile (mode GAAC_MODE_RAW,
+ * 16 KiB of BF16 in the format's storage order in pools->raw_pool), as
+ * gaac_encode_blocks writes them when slot_ids is NULL.  An entry of any other
+ * mode reports GAAC_EFORMAT and its block contributes nothing.  It is the
+ * uncompressed path the compressed cache is measured against: the GAAC page's
+ * section 3.2 and Table 5 weigh the reads a compressed cache saves against the
+ * reconstruction it adds.  Arguments, result, workspace and errors as
+ * gaac_decode_attention, without bases; pools->slot_pool may be NULL.
+ */
+GAAC_API int gaac_decode_attention_bf16(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
+                                        const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
+                                        float scale, int n_splits, float* out, void* workspace, size_t workspace_bytes,
+                                        int32_t* d_status, void* stream);
 
 /*
  * Decode attention for 256-channel heads (Appendix D: a 256-dimensional head is

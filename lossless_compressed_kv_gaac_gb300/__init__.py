@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
             L.gaac_decode_attention.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, ctypes.c_float, i32, P, P, sz,
                                                 P, P]
             L.gaac_decode_attention.restype = i32
+            L.gaac_decode_attention_bf16.argtypes = [P, i32, i32, i32, i32, P, P, P, ctypes.c_float, i32, P, P, sz,
+                                                     P, P]
+            L.gaac_decode_attention_bf16.restype = i32
             L.gaac_decode_attention_hd256.argtypes = L.gaac_decode_attention.argtypes
             L.gaac_decode_attention_hd256.restype = i32
             L.gaac_decompress.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, i64, i64, i64, P, P]
@@ -254,6 +257,19 @@ def decode_attention(q, seq_lens, table, pools: Pools, base3, base4, scale: floa
         q.data_ptr(), batch, hq, hkv, max_blocks, seq_lens.data_ptr(), table.data_ptr(), ctypes.byref(pc),
         base3.data_ptr(), base4.data_ptr(), float(scale), n_splits, out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream)))
+
+
+def decode_attention_bf16(q, seq_lens, table, pools: Pools, scale: float, out, workspace, n_splits: int = 0,
+                          status=None, stream=None) -> None:
+    """decode_attention over an uncompressed BF16 cache (every entry a raw tile): the same kernel specialised
+    to raw tiles, with no decode path."""
+    batch, hq = q.shape[0], q.shape[1]
+    max_blocks, hkv = table.shape[1], table.shape[2]
+    pc = pools.c()
+    _check("gaac_decode_attention_bf16", lib().gaac_decode_attention_bf16(
+        q.data_ptr(), batch, hq, hkv, max_blocks, seq_lens.data_ptr(), table.data_ptr(), ctypes.byref(pc),
+        float(scale), n_splits, out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
 
 
 def decompress(table, seq_lens, pools: Pools, base3, base4, k_out, v_out, status=None, stream=None) -> None:

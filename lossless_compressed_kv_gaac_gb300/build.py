@@ -36,25 +36,32 @@ def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+TIMELINE_LIB_PATH = os.path.join(PKG, "libgaac_timeline.so")
+
+
+def _stale(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB_PATH
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    """Builds libgaac.so; timeline=True builds the instrumented libgaac_timeline.so instead (the attention
+    kernel with its per-CTA timeline, include/gaac_timeline.h)."""
+    lib = TIMELINE_LIB_PATH if timeline else LIB_PATH
+    obj_dir = OBJ_DIR + ("_timeline" if timeline else "")
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(OBJ_DIR, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, os.path.basename(src).replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *NVCC_FLAGS, *(["-DGAAC_TIMELINE"] if timeline else []), "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -66,12 +73,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     subprocess.check_call([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-cudart", "static",
                            *objs, "-o", tmp])
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, timeline="--timeline" in sys.argv))

@@ -7,8 +7,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (BLOCK, HEAD_DIM, Pools, append, attention_workspace, calibrate, decode_attention, decompress,
-               encode_blocks, entry_fields, new_stats, new_table)
+from . import (BLOCK, HEAD_DIM, Pools, append, attention_workspace, calibrate, decode_attention,
+               decode_attention_bf16, decompress, encode_blocks, entry_fields, new_stats, new_table)
 
 
 class LayerCache:
@@ -72,12 +72,17 @@ class LayerCache:
         return self._ws
 
     def attention(self, q: torch.Tensor, scale: float, out: torch.Tensor | None = None, n_splits: int = 0,
-                  stream=None) -> torch.Tensor:
-        """q: BF16 [batch, q_heads, 128] -> fp32 [batch, q_heads, 128]."""
+                  stream=None, bf16: bool = False) -> torch.Tensor:
+        """q: BF16 [batch, q_heads, 128] -> fp32 [batch, q_heads, 128].  bf16=True: the uncompressed BF16
+        kernel (the cache must have been encoded with raw=True)."""
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-        decode_attention(q, self.seq_lens, self.table, self.pools, self.base3, self.base4, scale, out,
-                         self.workspace(n_splits), n_splits, self.status, stream)
+        if bf16:
+            decode_attention_bf16(q, self.seq_lens, self.table, self.pools, scale, out, self.workspace(n_splits),
+                                  n_splits, self.status, stream)
+        else:
+            decode_attention(q, self.seq_lens, self.table, self.pools, self.base3, self.base4, scale, out,
+                             self.workspace(n_splits), n_splits, self.status, stream)
         return out
 
     def decompress(self, n_tok: int | None = None, stream=None):

@@ -124,6 +124,40 @@ struct AttnArgs {
   int32_t* status;
 };
 
+// ------------------------------------------------------------- timeline
+// Opt-in per-CTA timeline (built only with -DGAAC_TIMELINE; the default
+// library has none of it): %globaltimer stamps of each CTA's start (after the
+// dependent-launch wait), of every block's copy issue, landing (the first warp
+// of its group through the stage wait, after it began waiting at arrive) and
+// release (the group's last warp done
+// with the stage), of the end of the split's blocks and of the CTA's exit
+// (after the merge, for the CTA that merges).  Read with gaac_timeline_fetch.
+#ifdef GAAC_TIMELINE
+constexpr int kTlCtas = 1024, kTlBlocks = 256;
+struct TlCta {
+  unsigned long long start, split_end, exit, merged;
+  unsigned long long issue[kTlBlocks], arrive[kTlBlocks], land[kTlBlocks], release[kTlBlocks];
+};
+__device__ TlCta g_timeline[kTlCtas];
+__device__ __forceinline__ unsigned long long tl_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ TlCta* tl_cta() {
+  const unsigned id = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  return id < kTlCtas ? &g_timeline[id] : nullptr;
+}
+#define GAAC_TL(...) \
+  do {               \
+    __VA_ARGS__;     \
+  } while (0)
+#else
+#define GAAC_TL(...) \
+  do {               \
+  } while (0)
+#endif
+
 // ------------------------------------------------------------------ helpers
 
 // bf16x2 times f (+-2^-4 or 0); exact whenever the result is a normal number or zero.
@@ -354,7 +388,9 @@ __device__ __forceinline__ void block_entries(const AttnArgs& a, int b, int H, i
 // One thread starts the bulk copies of a block's images into stage st (a free
 // stage); stFull[st] completes when all have landed.
 template <int NH, int KH>
-__device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem<NH, KH>& sm, int st, const uint2 e[KH + 1]) {
+__device__ __forceinline__ void issue_block(const AttnArgs& a, AttSmem<NH, KH>& sm, int st, const uint2 e[KH + 1],
+                                            [[maybe_unused]] int j) {
+  GAAC_TL(if (TlCta* c = tl_cta()) if (j < kTlBlocks) c->issue[j] = tl_now());
   StageMeta m;
   uint32_t bytes[KH + 1], total = 0;
   const void* src[KH + 1];
@@ -424,13 +460,27 @@ __device__ __forceinline__ void k_bases(const AttSmem<NH, KH>& sm, int half, int
   }
 }
 
+// The group's last warp to finish reading stage st refills it with block jn (entries ne, read by lane 0).
 template <int NH, int KH>
+__device__ __forceinline__ void release_stage(const AttnArgs& a, AttSmem<NH, KH>& sm, int st, int jn, int n_my,
+                                              int lane, const uint2 ne[KH + 1]) {
+  __syncwarp();
+  if (lane == 0 && atomic_add_acq_rel_cta(&sm.stDone[st], 1u) == kGroupWarps - 1) {
+    sm.stDone[st] = 0u;
+    GAAC_TL(if (TlCta* c = tl_cta()) if (jn - AttSmem<NH, KH>::kStages < kTlBlocks) c->release[jn - AttSmem<NH, KH>::kStages] = tl_now());
+    if (jn < n_my) issue_block<NH, KH>(a, sm, st, ne, jn);
+  }
+}
+
+// RAW: the uncompressed BF16 path (every tile a raw tile): the warp loads its K and V units straight
+// into operand registers, releases the stage before any MMA, and has no decode.
+template <int NH, int KH, bool RAW>
 __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>& sm, int b, int H, int hf, int blk0,
                                              int n_my, int len, int gr, int w, int cw, int lane, float acc[8][4]) {
   constexpr int kStages = AttSmem<NH, KH>::kStages;
   const int g = lane >> 2, tq = lane & 3;
   uint32_t kb3[8], kb4[8];  // one half-head: loaded once (NH = 1) or per half and block (NH = 2)
-  if (KH == 1) k_bases(sm, 0, tq, kb3, kb4);
+  if (KH == 1 && !RAW) k_bases(sm, 0, tq, kb3, kb4);
   [[maybe_unused]] uint32_t peer_mail = 0u, peer_full = 0u, peer_empty = 0u, peer_ack = 0u;  // the peer's mailbox
   if constexpr (NH > KH) {
     const uint32_t peer = cluster_rank() ^ 1u;
@@ -444,76 +494,119 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
   float mrun = -INFINITY, lsum = 0.f;  // head g
   const int tA = 16 * w + 2 * tq, tB = tA + 8;  // tokens of S^T columns 2tq, 2tq+1 of the two octets
+  // BF16 path: q's A-operand registers (rows 0-7; rows 8-15 are zero) stay in registers across blocks
+  [[maybe_unused]] uint32_t qa0[8], qa2[8];
+  if constexpr (RAW) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const uint4 qv = sm.qf[0][m][lane];
+      qa0[m] = qv.x;
+      qa2[m] = qv.z;
+    }
+  }
+  // Table entries of the block each stage takes next, read one iteration of the group ahead so that a
+  // refill never waits for them: ne serves this iteration's refill (block j + kStages), nn the next one's.
+  uint2 ne[KH + 1], nn[KH + 1];
+#pragma unroll
+  for (int i = 0; i <= KH; ++i) ne[i] = nn[i] = make_uint2(0u, 0u);
+  if (lane == 0 && gr + kStages < n_my) block_entries<NH, KH>(a, b, H, hf, blk0 + gr + kStages, ne);
 #pragma unroll 1
   for (int j = gr; j < n_my; j += kGroups, ++it) {
     const int st = j % kStages, jn = j + kStages;  // jn: the block this stage takes next
-    uint2 ne[KH + 1];
-#pragma unroll
-    for (int i = 0; i <= KH; ++i) ne[i] = make_uint2(0u, 0u);
-    if (lane == 0 && jn < n_my) block_entries<NH, KH>(a, b, H, hf, blk0 + jn, ne);  // used if this warp refills
+    if (lane == 0 && jn + kGroups < n_my) block_entries<NH, KH>(a, b, H, hf, blk0 + jn + kGroups, nn);
+    GAAC_TL(if (w == 0 && lane == 0) if (TlCta* c = tl_cta()) if (j < kTlBlocks) c->arrive[j] = tl_now());
     mbar_wait(&sm.stFull[st], static_cast<uint32_t>(j / kStages) & 1u, a.status);
+    GAAC_TL(if (w == 0 && lane == 0) if (TlCta* c = tl_cta()) if (j < kTlBlocks) c->land[j] = tl_now());
     const StageMeta meta = sm.smeta[st];
     const int nv = min(kBlock, len - (blk0 + j) * kBlock);
     // ---- S^T for tokens 16w..16w+7 (A) and 16w+8..16w+15 (B), summed over this CTA's K images
     float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
     bool kbadA = false, kbadB = false;
+    uint32_t oA[16], oB[16];  // the V operands of this warp's 16 tokens
+    if constexpr (RAW) {
+      static_assert(NH == 1 && KH == 1, "the BF16 path serves 128-channel heads");
+      const int uA = 64 * w + lane, uB = uA + 32;
+      uint32_t kA[16], kB[16];
+      raw_unit(sm.stage[st][0], uA, kA);
+      raw_unit(sm.stage[st][0], uB, kB);
+      raw_unit(sm.stage[st][1], uA, oA);
+      raw_unit(sm.stage[st][1], uB, oB);
+      release_stage<NH, KH>(a, sm, st, jn, n_my, lane, ne);
+      kbadA = kbadB = meta.mode[0] != GAAC_MODE_RAW;
+      const bool vbad = meta.mode[1] != GAAC_MODE_RAW;
+      if ((kbadA || vbad) && lane == 0) report(a.status, GAAC_EFORMAT);
+      if (vbad) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) oA[i] = oB[i] = 0u;
+      }
+      // two accumulators per octet (even and odd k-steps) halve the dependent MMA chain
+      float tA2[4] = {0.f, 0.f, 0.f, 0.f}, tB2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int m = 0; m < 8; m += 2) {
+        mma_bf16(sA, qa0[m], 0u, qa2[m], 0u, kA[2 * m], kA[2 * m + 1]);
+        mma_bf16(sB, qa0[m], 0u, qa2[m], 0u, kB[2 * m], kB[2 * m + 1]);
+        mma_bf16(tA2, qa0[m + 1], 0u, qa2[m + 1], 0u, kA[2 * m + 2], kA[2 * m + 3]);
+        mma_bf16(tB2, qa0[m + 1], 0u, qa2[m + 1], 0u, kB[2 * m + 2], kB[2 * m + 3]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sA[i] += tA2[i];
+        sB[i] += tB2[i];
+      }
+    } else {
 #pragma unroll 1
-    for (int half = 0; half < KH; ++half) {
-      if (KH > 1) k_bases(sm, half, tq, kb3, kb4);
-      uint32_t oA[16], oB[16];
-      bool bA, bB;
-      tile_units(a, sm, sm.stage[st][half], meta.mode[half], meta.esc[half], w, lane, kb3, kb4, kb3, kb4, oA, oB,
-                 bA, bB);
-      kbadA = kbadA || bA;
-      kbadB = kbadB || bB;
-      // q of head g as the A operand of S^T = q K^T (scaled by 2^-4), one 16-byte quad per k-step: for k-step
-      // m the K lane holds channels 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no
-      // head) are zero
+      for (int half = 0; half < KH; ++half) {
+        if (KH > 1) k_bases(sm, half, tq, kb3, kb4);
+        uint32_t oA[16], oB[16];
+        bool bA, bB;
+        tile_units(a, sm, sm.stage[st][half], meta.mode[half], meta.esc[half], w, lane, kb3, kb4, kb3, kb4, oA, oB,
+                   bA, bB);
+        kbadA = kbadA || bA;
+        kbadB = kbadB || bB;
+        // q of head g as the A operand of S^T = q K^T (scaled by 2^-4), one 16-byte quad per k-step: for k-step
+        // m the K lane holds channels 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no
+        // head) are zero
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const uint4 qv = sm.qf[half][m][lane];
-        mma_bf16(sA, qv.x, qv.y, qv.z, qv.w, oA[2 * m], oA[2 * m + 1]);
-        mma_bf16(sB, qv.x, qv.y, qv.z, qv.w, oB[2 * m], oB[2 * m + 1]);
+        for (int m = 0; m < 8; ++m) {
+          const uint4 qv = sm.qf[half][m][lane];
+          mma_bf16(sA, qv.x, qv.y, qv.z, qv.w, oA[2 * m], oA[2 * m + 1]);
+          mma_bf16(sB, qv.x, qv.y, qv.z, qv.w, oB[2 * m], oB[2 * m + 1]);
+        }
       }
-    }
-    if constexpr (NH > KH) {
-      // 256-channel heads as a cluster pair: the scores are this CTA's half-head partial plus the peer's.
-      // Each lane posts its partials (NaN for a unit that failed its checks) into the peer's mailbox now,
-      // as asynchronous stores that complete on the peer's barrier, and takes the peer's after the V
-      // decode; both CTAs add S0 + S1 (exact-commutative), so their softmax weights are identical.
-      const int bb = it & 1;
-      if (it >= 2) {  // the peer has read this buffer's previous use: its 16-byte acknowledgement landed
-        if (lane == 0) mbar_arrive_expect_tx(&sm.mEmpty[cw][bb], sizeof(float4));
-        mbar_wait(&sm.mEmpty[cw][bb], static_cast<uint32_t>((it >> 1) + 1) & 1u, a.status);
+      if constexpr (NH > KH) {
+        // 256-channel heads as a cluster pair: the scores are this CTA's half-head partial plus the peer's.
+        // Each lane posts its partials (NaN for a unit that failed its checks) into the peer's mailbox now,
+        // as asynchronous stores that complete on the peer's barrier, and takes the peer's after the V
+        // decode; both CTAs add S0 + S1 (exact-commutative), so their softmax weights are identical.
+        const int bb = it & 1;
+        if (it >= 2) {  // the peer has read this buffer's previous use: its 16-byte acknowledgement landed
+          if (lane == 0) mbar_arrive_expect_tx(&sm.mEmpty[cw][bb], sizeof(float4));
+          mbar_wait(&sm.mEmpty[cw][bb], static_cast<uint32_t>((it >> 1) + 1) & 1u, a.status);
+        }
+        st_async_f4(peer_mail + bb * 32 * sizeof(float4), kbadA ? NAN : sA[0], kbadA ? NAN : sA[1],
+                    kbadB ? NAN : sB[0], kbadB ? NAN : sB[1], peer_full + bb * sizeof(uint64_t));
       }
-      st_async_f4(peer_mail + bb * 32 * sizeof(float4), kbadA ? NAN : sA[0], kbadA ? NAN : sA[1],
-                  kbadB ? NAN : sB[0], kbadB ? NAN : sB[1], peer_full + bb * sizeof(uint64_t));
-    }
-    // ---- V units of the same tokens (independent of the scores: decoded while the MMAs above run)
-    uint32_t oA[16], oB[16];
-    bool vbadA, vbadB;
-    uint32_t vb3[2][8], vb4[2][8];  // word 2i and 2i+1 serve group i
+      // ---- V units of the same tokens (independent of the scores: decoded while the MMAs above run)
+      bool vbadA, vbadB;
+      uint32_t vb3[2][8], vb4[2][8];  // word 2i and 2i+1 serve group i
 #pragma unroll
-    for (int hv = 0; hv < 2; ++hv) {
-      const uint4 x3 = sm.vbw[hv][0][lane];
-      const uint4 x4 = sm.vbw[hv][1][lane];
-      vb3[hv][0] = vb3[hv][1] = x3.x;
-      vb3[hv][2] = vb3[hv][3] = x3.y;
-      vb3[hv][4] = vb3[hv][5] = x3.z;
-      vb3[hv][6] = vb3[hv][7] = x3.w;
-      vb4[hv][0] = vb4[hv][1] = x4.x;
-      vb4[hv][2] = vb4[hv][3] = x4.y;
-      vb4[hv][4] = vb4[hv][5] = x4.z;
-      vb4[hv][6] = vb4[hv][7] = x4.w;
-    }
-    tile_units(a, sm, sm.stage[st][KH], meta.mode[KH], meta.esc[KH], w, lane, vb3[0], vb4[0], vb3[1], vb4[1], oA,
-               oB, vbadA, vbadB);
-    // The stage is read: the group's last warp to get here refills it with block jn.
-    __syncwarp();
-    if (lane == 0 && atomic_add_acq_rel_cta(&sm.stDone[st], 1u) == kGroupWarps - 1) {
-      sm.stDone[st] = 0u;
-      if (jn < n_my) issue_block<NH, KH>(a, sm, st, ne);
-    }
+      for (int hv = 0; hv < 2; ++hv) {
+        const uint4 x3 = sm.vbw[hv][0][lane];
+        const uint4 x4 = sm.vbw[hv][1][lane];
+        vb3[hv][0] = vb3[hv][1] = x3.x;
+        vb3[hv][2] = vb3[hv][3] = x3.y;
+        vb3[hv][4] = vb3[hv][5] = x3.z;
+        vb3[hv][6] = vb3[hv][7] = x3.w;
+        vb4[hv][0] = vb4[hv][1] = x4.x;
+        vb4[hv][2] = vb4[hv][3] = x4.y;
+        vb4[hv][4] = vb4[hv][5] = x4.z;
+        vb4[hv][6] = vb4[hv][7] = x4.w;
+      }
+      tile_units(a, sm, sm.stage[st][KH], meta.mode[KH], meta.esc[KH], w, lane, vb3[0], vb4[0], vb3[1], vb4[1], oA,
+                 oB, vbadA, vbadB);
+      // The stage is read: the group's last warp to get here refills it with block jn.
+      release_stage<NH, KH>(a, sm, st, jn, n_my, lane, ne);
+    }  // compressed path
     if constexpr (NH > KH) {  // take the peer's partial scores of this block (posted above)
       const int bb = it & 1;
       if (lane == 0) mbar_arrive_expect_tx(&sm.mFull[cw][bb], 32 * sizeof(float4));
@@ -593,6 +686,8 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
         mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], l01, l23);
       }
     }
+#pragma unroll
+    for (int i = 0; i <= KH; ++i) ne[i] = nn[i];
   }
   if constexpr (NH > KH) {
     // The acknowledgements of this warp's last posts (one per buffer used) are still owed: take them, so that
@@ -715,7 +810,7 @@ __device__ __noinline__ void merge_splits(const float* base, int ns, int r, floa
 // NH half-heads.  KH = 1 < NH: the NH CTAs of a head form a cluster; each
 // reads the K tile of its own half-head and the pair exchanges partial scores
 // through distributed shared memory, so every K tile is decoded once.
-template <int NH, int KH>
+template <int NH, int KH, bool RAW>
 __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(AttnArgs a) {
   constexpr int kStages = AttSmem<NH, KH>::kStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -727,6 +822,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   // the CTA may already be resident while that kernel finishes: wait for it
   // (and its memory) before reading anything.  A no-op for an ordinary launch.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  GAAC_TL(if (tid == 0) if (TlCta* c = tl_cta()) { c->start = tl_now(); c->merged = 0ull; });
   int len = a.seq_lens[b];
   if (len < 0 || len > a.max_blocks * kBlock) {
     if (tid == 0) report(a.status, GAAC_EINVAL);
@@ -753,20 +849,20 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   if (tid < min(n_my, kStages)) {
     uint2 e[KH + 1];
     block_entries<NH, KH>(a, b, H, hf, blk0 + tid, e);
-    issue_block<NH, KH>(a, sm, tid, e);
+    issue_block<NH, KH>(a, sm, tid, e, tid);
   }
 
-  for (int x = tid; x < 256; x += kAttThreads) {
+  for (int x = tid; x < (RAW ? 0 : 256); x += kAttThreads) {  // decode tables (compressed path only)
     sm.lut[x] = spread_entry(static_cast<uint32_t>(x));
     sm.tagl[x] = tag_entry(static_cast<uint32_t>(x));
   }
-  for (int x = tid; x < KH * 2 * kD; x += kAttThreads) {  // K: [image][base3|base4][channel]
+  for (int x = tid; x < (RAW ? 0 : KH * 2 * kD); x += kAttThreads) {  // K: [image][base3|base4][channel]
     const int half = x / (2 * kD), which = (x / kD) & 1, c = x % kD;
     sm.kbases[half][which][c] = (which ? a.base4 : a.base3)[(NH * H + (KH == NH ? half : hf)) * kD + c];
   }
   // V unit base words: group i of the lane's unit hv holds channels 16m+g and 16m+g+8 (m = 4hv + i, g =
   // lane/4) in byte lanes 0, 2 and 1, 3 of both of its exponent words
-  for (int x = tid; x < 32 * 2 * 4; x += kAttThreads) {
+  for (int x = tid; x < (RAW ? 0 : 32 * 2 * 4); x += kAttThreads) {
     const int ln = x / 8, hv = (x / 4) % 2, i = x % 4;
     const int cA = 16 * (4 * hv + i) + ln / 4;
     const uint8_t* v3 = a.base3 + (nkv + NH * H + hf) * kD;
@@ -795,7 +891,8 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   const int r = a.r;
   float* part = a.part + ((static_cast<size_t>(b) * nkv + y) * a.n_splits + split) * kPartFloats;
   float acc[8][4];
-  compute_warp<NH, KH>(a, sm, b, H, hf, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane, acc);
+  compute_warp<NH, KH, RAW>(a, sm, b, H, hf, blk0, n_my, len, warp / kGroupWarps, warp % kGroupWarps, warp, lane,
+                            acc);
   // The next kernel on the stream may be scheduled now (it waits for this one before its first read).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
@@ -806,6 +903,7 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
       mbar_wait(&sm.stFull[i % kStages], (i / kStages) & 1, a.status, 1u << 10);
   }
   __syncthreads();  // every stage consumed: the ring becomes merge scratch
+  GAAC_TL(if (tid == 0) if (TlCta* c = tl_cta()) c->split_end = tl_now());
   // ---- merge of the compute warps' states: weights 2^(m_w - max_w m_w) per head
   if (tid < kCWarps * kRPad) {
     const int cw = tid / kRPad, n = tid % kRPad;
@@ -860,10 +958,12 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   unsigned int* counter = a.counters + static_cast<size_t>(b) * nkv + y;
   if (tid == 0) sm.last = atomic_add_acq_rel(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
   __syncthreads();
+  GAAC_TL(if (tid == 0) if (TlCta* c = tl_cta()) c->exit = tl_now());
   if (!sm.last) return;
   merge_splits<NH>(a.part + (static_cast<size_t>(b) * nkv + y) * a.n_splits * kPartFloats, a.n_splits, r, a.c_log2,
                    a.out + (static_cast<size_t>(b) * a.Hq + H * r) * (NH * kD) + kD * hf, sm, tid);
   if (tid == 0) *counter = 0u;
+  GAAC_TL(if (tid == 0) if (TlCta* c = tl_cta()) c->merged = tl_now());
 }
 
 static int device_sms() {
@@ -878,13 +978,13 @@ static int device_sms() {
   return cached[dev];
 }
 
-template <int NH, int KH>
+template <int NH, int KH, bool RAW>
 static bool prepare_kernel() {
   static bool done[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(attn_split_kernel<NH, KH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_split_kernel<NH, KH, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(AttSmem<NH, KH>))) != cudaSuccess)
       return false;
     done[dev] = true;
@@ -919,7 +1019,7 @@ static int pair_max_clusters() {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pair_config<NH, KH>(dim3(1, NH, 1), nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_split_kernel<NH, KH>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, attn_split_kernel<NH, KH, false>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = -1;
     }
@@ -945,24 +1045,31 @@ static size_t partials_bytes(int batch, int n_kv_heads, int n_splits) {
   return static_cast<size_t>(batch) * n_kv_heads * n_splits * kPartFloats * sizeof(float);
 }
 
+// The merge counters open the workspace (one u32 per (sequence, kv-head), rounded up to 16 bytes), so
+// their place does not depend on the split count and a workspace reused with another count still
+// finds them at zero; the split partials follow.
+static size_t counters_bytes(int batch, int n_kv_heads) {
+  return (static_cast<size_t>(batch) * n_kv_heads * sizeof(unsigned int) + 15) & ~static_cast<size_t>(15);
+}
+
 extern "C" size_t gaac_attention_workspace(int batch, int n_kv_heads, int max_blocks, int n_splits) {
   if (n_splits <= 0) n_splits = gaac_attention_auto_splits(batch, n_kv_heads, max_blocks);
   if (batch <= 0 || n_kv_heads <= 0) return 0;
-  const size_t counters = (static_cast<size_t>(batch) * n_kv_heads * sizeof(unsigned int) + 15) & ~static_cast<size_t>(15);
-  return partials_bytes(batch, n_kv_heads, n_splits) + counters;
+  return counters_bytes(batch, n_kv_heads) + partials_bytes(batch, n_kv_heads, n_splits);
 }
 
 // Checks and launch shared by the 128- and 256-channel entry points; n_kv_heads
 // counts attention kv-heads, each of NH half-heads in the table and the bases.
 // clear_counters: zero the workspace's merge counters on the stream once every
-// check has passed (a call that fails a check enqueues nothing).
-template <int NH>
+// check has passed (a call that fails a check enqueues nothing).  RAW: the
+// uncompressed BF16 kernel (128-channel heads only).
+template <int NH, bool RAW = false>
 static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads, int max_blocks,
                             const int32_t* seq_lens, const gaac_entry* table, const gaac_pools* pools,
                             const uint8_t* base3, const uint8_t* base4, float scale, int n_splits, float* out,
                             void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream,
                             bool clear_counters = false) {
-  if (q == nullptr || seq_lens == nullptr || table == nullptr || pools == nullptr || pools->slot_pool == nullptr ||
+  if (q == nullptr || seq_lens == nullptr || table == nullptr || pools == nullptr || (!RAW && pools->slot_pool == nullptr) ||
       pools->raw_pool == nullptr || pools->n_slots < 0 || pools->n_raw < 0 || base3 == nullptr ||
       base4 == nullptr || out == nullptr || workspace == nullptr)
     return GAAC_EINVAL;
@@ -970,14 +1077,15 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
       n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > GAAC_MAX_GQA || max_blocks <= 0 ||
       max_blocks > (1 << 24) || !std::isfinite(scale))
     return GAAC_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(pools->slot_pool) & 15u) ||
+  if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(pools->slot_pool) & 15u) ||  // null passes
       (reinterpret_cast<uintptr_t>(pools->raw_pool) & 15u) || (reinterpret_cast<uintptr_t>(base3) & 15u) ||
       (reinterpret_cast<uintptr_t>(base4) & 15u) || (reinterpret_cast<uintptr_t>(workspace) & 15u) ||
       (reinterpret_cast<uintptr_t>(out) & 3u))
     return GAAC_EINVAL;
   constexpr int KH = 1;  // 256-channel heads: the two CTAs of a head form a cluster and share the scores
   const int nkv = NH * n_kv_heads;  // CTAs per (sequence, split) and half-heads in the table
-  if (!prepare_kernel<NH, KH>()) return GAAC_ECUDA;
+  static_assert(!RAW || NH == 1, "the BF16 kernel serves 128-channel heads");
+  if (!prepare_kernel<NH, KH, RAW>()) return GAAC_ECUDA;
   if (n_splits <= 0) {
     n_splits = gaac_attention_auto_splits(batch, nkv, max_blocks);
     if (NH > KH) {  // one wave of resident clusters
@@ -1007,8 +1115,8 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
   a.r = n_q_heads / n_kv_heads;
   a.max_blocks = max_blocks;
   a.n_splits = n_splits;
-  a.part = static_cast<float*>(workspace);
-  a.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + partials_bytes(batch, nkv, n_splits));
+  a.counters = static_cast<unsigned int*>(workspace);
+  a.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + counters_bytes(batch, nkv));
   a.out = out;
   a.status = d_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1018,7 +1126,7 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
   if (NH > KH) {
     cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = pair_config<NH, KH>(dim3(n_splits, nkv, batch), st, attr);
-    if (cudaLaunchKernelEx(&cfg, attn_split_kernel<NH, KH>, a) != cudaSuccess) return GAAC_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, attn_split_kernel<NH, KH, false>, a) != cudaSuccess) return GAAC_ECUDA;
   } else {
     // Programmatic dependent launch: the grid is set up while the previous kernel on the stream drains.
     cudaLaunchConfig_t cfg = {};
@@ -1031,7 +1139,7 @@ static int launch_attention(const uint16_t* q, int batch, int n_q_heads, int n_k
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, attn_split_kernel<NH, KH>, a) != cudaSuccess) return GAAC_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, attn_split_kernel<NH, KH, RAW>, a) != cudaSuccess) return GAAC_ECUDA;
   }
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
@@ -1045,6 +1153,16 @@ extern "C" int gaac_decode_attention(const uint16_t* q, int batch, int n_q_heads
                              n_splits, out, workspace, workspace_bytes, d_status, stream);
 }
 
+extern "C" int gaac_decode_attention_bf16(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads,
+                                          int max_blocks, const int32_t* seq_lens, const gaac_entry* table,
+                                          const gaac_pools* pools, float scale, int n_splits, float* out,
+                                          void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
+  // The BF16 kernel reads no bases; any aligned non-null pointer satisfies the shared checks.
+  const uint8_t* unused = reinterpret_cast<const uint8_t*>(pools ? pools->raw_pool : nullptr);
+  return launch_attention<1, true>(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, unused,
+                                   unused, scale, n_splits, out, workspace, workspace_bytes, d_status, stream);
+}
+
 extern "C" int gaac_decode_attention_hd256(const uint16_t* q, int batch, int n_q_heads, int n_kv_heads,
                                            int max_blocks, const int32_t* seq_lens, const gaac_entry* table,
                                            const gaac_pools* pools, const uint8_t* base3, const uint8_t* base4,
@@ -1053,6 +1171,19 @@ extern "C" int gaac_decode_attention_hd256(const uint16_t* q, int batch, int n_q
   return launch_attention<2>(q, batch, n_q_heads, n_kv_heads, max_blocks, seq_lens, table, pools, base3, base4, scale,
                              n_splits, out, workspace, workspace_bytes, d_status, stream);
 }
+
+#ifdef GAAC_TIMELINE
+// Copies the per-CTA timeline of the last attention launch (CTA id = x + X (y + Y z)) to host memory.
+extern "C" GAAC_API int gaac_timeline_fetch(void* host_dst, size_t bytes, size_t* cta_bytes, int* n_ctas,
+                                            int* n_blocks) {
+  if (cta_bytes) *cta_bytes = sizeof(TlCta);
+  if (n_ctas) *n_ctas = kTlCtas;
+  if (n_blocks) *n_blocks = kTlBlocks;
+  if (host_dst == nullptr) return GAAC_OK;
+  if (bytes > sizeof(g_timeline)) bytes = sizeof(g_timeline);
+  return cudaMemcpyFromSymbol(host_dst, g_timeline, bytes) == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+}
+#endif
 
 // ------------------------------------------------------------------------
 // Allocation-free variant.  Some callers cannot hand the library a workspace

@@ -87,7 +87,7 @@ def test_ragged_lengths_and_gqa(hq, hkv):
         assert torch.equal(kd[b, :L].view(torch.int16), k[b, :L].view(torch.int16))
         assert torch.equal(vd[b, :L].view(torch.int16), v[b, :L].view(torch.int16))
     q = W.make_q(0, 1, B, hq, device="cuda")
-    for n_splits in (1, 3, 0):
+    for n_splits in (1, 3, 0, 2):  # the last call reuses a workspace sized for more splits
         out = c.attention(q, 1 / np.sqrt(128), n_splits=n_splits)
         assert _status(c) == 0
         assert U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128)).compared == B * hq
@@ -95,7 +95,9 @@ def test_ragged_lengths_and_gqa(hq, hkv):
 
 
 def test_all_raw_baseline_same_outputs():
-    """The uncompressed baseline: every block stored raw, read by the same kernel."""
+    """The uncompressed baseline: every block stored raw, read by the compressed kernel's raw path and by
+    the BF16 kernel (the same kernel without a decode path); both against the oracle, and the BF16 kernel
+    on a compressed cache reports a format error."""
     k, v = U.kv(0, 2, 2, 2048, 8)
     lens = U.lens_tensor([2048, 1500])
     c = U.build(k, v, lens, raw=True)
@@ -104,11 +106,35 @@ def test_all_raw_baseline_same_outputs():
     assert n["slot"] == 0
     q = W.make_q(0, 2, 2, 32, device="cuda")
     out = c.attention(q, 1 / np.sqrt(128))
-    U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128))
+    assert U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128)).compared == 2 * 32
     cz = U.build(k, v, lens)
     outz = cz.attention(q, 1 / np.sqrt(128))
     torch.cuda.synchronize()
     assert (out - outz).abs().max().item() < 1e-5
+    for n_splits in (1, 5, 0):
+        ob = c.attention(q, 1 / np.sqrt(128), n_splits=n_splits, bf16=True)
+        assert _status(c) == 0
+        assert U.check_attention(ob, q, k, v, lens, 1 / np.sqrt(128)).compared == 2 * 32
+    assert (ob - out).abs().max().item() < 1e-5  # the same values through the compressed kernel's raw path
+    cz.attention(q, 1 / np.sqrt(128), bf16=True)
+    assert _status(cz) == G.EFORMAT
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (64, 8)])
+def test_bf16_kernel_ragged_lengths(hq, hkv):
+    """The BF16 kernel over ragged lengths (empty, one token, block edges, open tails) and GQA ratios."""
+    lens_v = [0, 1, 63, 64, 65, 700, 1024, 333]
+    B, T = len(lens_v), 1024
+    k, v = U.kv(0, 9, B, T, hkv)
+    lens = U.lens_tensor(lens_v)
+    c = U.build(k, v, lens, raw=True)
+    assert _status(c) == 0
+    q = W.make_q(0, 9, B, hq, device="cuda")
+    for n_splits in (1, 3, 0):
+        out = c.attention(q, 1 / np.sqrt(128), n_splits=n_splits, bf16=True)
+        assert _status(c) == 0
+        assert U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128)).compared == B * hq
+    assert out[0].abs().max().item() == 0.0
 
 
 def test_incremental_append_equals_one_shot():
