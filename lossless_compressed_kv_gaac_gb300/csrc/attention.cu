@@ -91,7 +91,7 @@ struct AttSmem {
   uint32_t tagl[256];             // tag byte -> gather selector, counts, raw groups (tag_entry)
   alignas(16) uint8_t kbases[KH][2][kD];  // K: [image][base3|base4][channel]
   StageMeta smeta[kStages];
-  alignas(16) uint4 qf[KH][8][32];       // q A-operand quads [image][k-step][lane]: (qa0, 0, qa2, 0)
+  alignas(16) uint2 qf[KH][8][32];       // q^T B-operand pairs [image][k-step][lane] of S = K q^T
   alignas(16) uint4 vbw[2][2][32];        // V base words [unit][base3 | base4][lane], groups 0-3
   unsigned int stDone[kStages];           // warps of the group done reading the stage's current block
   float wm[kCWarps][kRPad];       // per warp and head: running maximum (end of split)
@@ -170,6 +170,14 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t w, float f) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Transpose of an 8 x 8 matrix of 16-bit values held one row pair per lane (lane (g, tq): row g, columns
+// 2tq, 2tq+1): the result holds row g, columns 2tq, 2tq+1 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
   return r;
 }
 
@@ -492,16 +500,22 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
   int it = 0;  // this warp's block count
 #pragma unroll
   for (int m = 0; m < 8; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
-  float mrun = -INFINITY, lsum = 0.f;  // head g
-  const int tA = 16 * w + 2 * tq, tB = tA + 8;  // tokens of S^T columns 2tq, 2tq+1 of the two octets
-  // BF16 path: q's A-operand registers (rows 0-7; rows 8-15 are zero) stay in registers across blocks
-  [[maybe_unused]] uint32_t qa0[8], qa2[8];
+  // Scores S = K q^T of the warp's 16 tokens: rows g and g+8 (tokens tA, tB of the two octets), columns
+  // 2tq, 2tq+1.  A column is a query head; with r <= 4 query heads per kv-head, columns 4-7 repeat
+  // heads 0-3 (`packed`): their lanes run the same softmax and feed the low parts of P to the same PV MMA
+  // in which columns 0-3 take the high parts.  Running maxima m0, m1 and sums l0, l1 per column.
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int tA = 16 * w + g, tB = tA + 8;        // tokens of S rows g, g+8
+  const int vA = 16 * w + 2 * tq, vB = vA + 8;   // tokens of the V operand's columns 2tq, 2tq+1
+  const bool packed = a.r <= 4;
+  // BF16 path: q's B-operand registers stay in registers across blocks
+  [[maybe_unused]] uint32_t qb0[8], qb1[8];
   if constexpr (RAW) {
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const uint4 qv = sm.qf[0][m][lane];
-      qa0[m] = qv.x;
-      qa2[m] = qv.z;
+      const uint2 qv = sm.qf[0][m][lane];
+      qb0[m] = qv.x;
+      qb1[m] = qv.y;
     }
   }
   // Table entries of the block each stage takes next, read one iteration of the group ahead so that a
@@ -519,8 +533,10 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
     GAAC_TL(if (w == 0 && lane == 0) if (TlCta* c = tl_cta()) if (j < kTlBlocks) c->land[j] = tl_now());
     const StageMeta meta = sm.smeta[st];
     const int nv = min(kBlock, len - (blk0 + j) * kBlock);
-    // ---- S^T for tokens 16w..16w+7 (A) and 16w+8..16w+15 (B), summed over this CTA's K images
-    float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S = K q^T for tokens tA (row g) and tB (row g+8), summed over this CTA's K images: the K units
+    // of the two tokens are the A operand (k-step m: a0, a2 = token tA, a1, a3 = token tB), q^T the B
+    // operand; even and odd k-steps go to two accumulators (a chain of four MMAs each)
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
     bool kbadA = false, kbadB = false;
     uint32_t oA[16], oB[16];  // the V operands of this warp's 16 tokens
     if constexpr (RAW) {
@@ -539,19 +555,10 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
 #pragma unroll
         for (int i = 0; i < 16; ++i) oA[i] = oB[i] = 0u;
       }
-      // two accumulators per octet (even and odd k-steps) halve the dependent MMA chain
-      float tA2[4] = {0.f, 0.f, 0.f, 0.f}, tB2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int m = 0; m < 8; m += 2) {
-        mma_bf16(sA, qa0[m], 0u, qa2[m], 0u, kA[2 * m], kA[2 * m + 1]);
-        mma_bf16(sB, qa0[m], 0u, qa2[m], 0u, kB[2 * m], kB[2 * m + 1]);
-        mma_bf16(tA2, qa0[m + 1], 0u, qa2[m + 1], 0u, kA[2 * m + 2], kA[2 * m + 3]);
-        mma_bf16(tB2, qa0[m + 1], 0u, qa2[m + 1], 0u, kB[2 * m + 2], kB[2 * m + 3]);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sA[i] += tA2[i];
-        sB[i] += tB2[i];
+        mma_bf16(sc, kA[2 * m], kB[2 * m], kA[2 * m + 1], kB[2 * m + 1], qb0[m], qb1[m]);
+        mma_bf16(s1, kA[2 * m + 2], kB[2 * m + 2], kA[2 * m + 3], kB[2 * m + 3], qb0[m + 1], qb1[m + 1]);
       }
     } else {
 #pragma unroll 1
@@ -563,14 +570,14 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
                    bA, bB);
         kbadA = kbadA || bA;
         kbadB = kbadB || bB;
-        // q of head g as the A operand of S^T = q K^T (scaled by 2^-4), one 16-byte quad per k-step: for k-step
-        // m the K lane holds channels 32tq + 4m + {0,2} (first register) and {1,3} (second); rows 8-15 (no
-        // head) are zero
+        // q^T (scaled by 2^-4) as the B operand: for k-step m the lane's K registers hold channels
+        // 32tq + 4m + {0,2} (first) and {1,3} (second) of its two tokens, and its q pair the same channels
+        // of column g
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const uint4 qv = sm.qf[half][m][lane];
-          mma_bf16(sA, qv.x, qv.y, qv.z, qv.w, oA[2 * m], oA[2 * m + 1]);
-          mma_bf16(sB, qv.x, qv.y, qv.z, qv.w, oB[2 * m], oB[2 * m + 1]);
+        for (int m = 0; m < 8; m += 2) {
+          const uint2 q0 = sm.qf[half][m][lane], q1 = sm.qf[half][m + 1][lane];
+          mma_bf16(sc, oA[2 * m], oB[2 * m], oA[2 * m + 1], oB[2 * m + 1], q0.x, q0.y);
+          mma_bf16(s1, oA[2 * m + 2], oB[2 * m + 2], oA[2 * m + 3], oB[2 * m + 3], q1.x, q1.y);
         }
       }
       if constexpr (NH > KH) {
@@ -583,8 +590,9 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
           if (lane == 0) mbar_arrive_expect_tx(&sm.mEmpty[cw][bb], sizeof(float4));
           mbar_wait(&sm.mEmpty[cw][bb], static_cast<uint32_t>((it >> 1) + 1) & 1u, a.status);
         }
-        st_async_f4(peer_mail + bb * 32 * sizeof(float4), kbadA ? NAN : sA[0], kbadA ? NAN : sA[1],
-                    kbadB ? NAN : sB[0], kbadB ? NAN : sB[1], peer_full + bb * sizeof(uint64_t));
+        st_async_f4(peer_mail + bb * 32 * sizeof(float4), kbadA ? NAN : sc[0] + s1[0],
+                    kbadA ? NAN : sc[1] + s1[1], kbadB ? NAN : sc[2] + s1[2], kbadB ? NAN : sc[3] + s1[3],
+                    peer_full + bb * sizeof(uint64_t));
       }
       // ---- V units of the same tokens (independent of the scores: decoded while the MMAs above run)
       bool vbadA, vbadB;
@@ -622,27 +630,33 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
           st_async_f4(peer_ack + bb * sizeof(float4), __uint_as_float(dep), 0.f, 0.f, 0.f,
                       peer_empty + bb * sizeof(uint64_t));
       }
-      sA[0] = (kbadA ? NAN : sA[0]) + X.x;
-      sA[1] = (kbadA ? NAN : sA[1]) + X.y;
-      sB[0] = (kbadB ? NAN : sB[0]) + X.z;
-      sB[1] = (kbadB ? NAN : sB[1]) + X.w;
-      kbadA = __any_sync(kFull, isnan(sA[0]) || isnan(sA[1]));
-      kbadB = __any_sync(kFull, isnan(sB[0]) || isnan(sB[1]));
+      sc[0] = (kbadA ? NAN : sc[0] + s1[0]) + X.x;
+      sc[1] = (kbadA ? NAN : sc[1] + s1[1]) + X.y;
+      sc[2] = (kbadB ? NAN : sc[2] + s1[2]) + X.z;
+      sc[3] = (kbadB ? NAN : sc[3] + s1[3]) + X.w;
+      s1[0] = s1[1] = s1[2] = s1[3] = 0.f;
+      kbadA = __any_sync(kFull, isnan(sc[0]) || isnan(sc[1]));
+      kbadB = __any_sync(kFull, isnan(sc[2]) || isnan(sc[3]));
     }
-    // ---- online softmax of head g over the warp's 16 tokens, on raw scores (q/16).k: only the
-    // differences from the running maximum are scaled to the log2 domain
-    const float x0 = (!kbadA && tA < nv) ? sA[0] : -INFINITY;
-    const float x1 = (!kbadA && tA + 1 < nv) ? sA[1] : -INFINITY;
-    const float x2 = (!kbadB && tB < nv) ? sB[0] : -INFINITY;
-    const float x3 = (!kbadB && tB + 1 < nv) ? sB[1] : -INFINITY;
-    float bm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
-    const float mnew = fmaxf(mrun, bm);
-    if (__any_sync(kFull, mnew != mrun)) {  // a running maximum rises: rescale (rare after the first blocks)
-      const float al = mrun == -INFINITY ? 0.f : fast_exp2((mrun - mnew) * a.c_log2);
-      lsum *= al;
-      const float al0 = __shfl_sync(kFull, al, 8 * tq), al1 = __shfl_sync(kFull, al, 8 * tq + 4);  // heads 2tq, 2tq+1
+    // ---- online softmax of columns 2tq, 2tq+1 over the warp's 16 tokens, on raw scores (q/16).k: only the
+    // differences from the running maxima are scaled to the log2 domain
+    const float x0 = (!kbadA && tA < nv) ? sc[0] + s1[0] : -INFINITY;  // token tA, column 2tq
+    const float x1 = (!kbadA && tA < nv) ? sc[1] + s1[1] : -INFINITY;  // token tA, column 2tq+1
+    const float x2 = (!kbadB && tB < nv) ? sc[2] + s1[2] : -INFINITY;  // token tB
+    const float x3 = (!kbadB && tB < nv) ? sc[3] + s1[3] : -INFINITY;
+    float b0 = fmaxf(x0, x2), b1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int d = 4; d < 32; d <<= 1) {  // over the eight lanes g of each column pair
+      b0 = fmaxf(b0, __shfl_xor_sync(kFull, b0, d));
+      b1 = fmaxf(b1, __shfl_xor_sync(kFull, b1, d));
+    }
+    const float n0 = fmaxf(m0, b0), n1 = fmaxf(m1, b1);
+    const float cl = a.c_log2;
+    if (__any_sync(kFull, n0 != m0 || n1 != m1)) {  // a running maximum rises: rescale (rare after the first blocks)
+      const float al0 = m0 == -INFINITY ? 0.f : fast_exp2((m0 - n0) * cl);
+      const float al1 = m1 == -INFINITY ? 0.f : fast_exp2((m1 - n1) * cl);
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
         acc[m][0] *= al0;
@@ -650,40 +664,52 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
         acc[m][1] *= al1;
         acc[m][3] *= al1;
       }
-      mrun = mnew;
+      m0 = n0;
+      m1 = n1;
     }
-    const bool live = mrun != -INFINITY;
-    const float cl = a.c_log2;
-    const float p0 = live ? fast_exp2((x0 - mrun) * cl) : 0.f, p1 = live ? fast_exp2((x1 - mrun) * cl) : 0.f;
-    const float p2 = live ? fast_exp2((x2 - mrun) * cl) : 0.f, p3 = live ? fast_exp2((x3 - mrun) * cl) : 0.f;
-    lsum += (p0 + p1) + (p2 + p3);
-    // P^T as the B operand: rows (tokens) 2tq, 2tq+1 from octet A, 2tq+8, 2tq+9 from octet B; column = head g
+    const float p0 = m0 != -INFINITY ? fast_exp2((x0 - m0) * cl) : 0.f;
+    const float p2 = m0 != -INFINITY ? fast_exp2((x2 - m0) * cl) : 0.f;
+    const float p1 = m1 != -INFINITY ? fast_exp2((x1 - m1) * cl) : 0.f;
+    const float p3 = m1 != -INFINITY ? fast_exp2((x3 - m1) * cl) : 0.f;
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    // P as bf16 high and low parts (rows = tokens, columns 2tq, 2tq+1), then transposed per octet into the
+    // B operand P^T of O^T += V^T P^T (lane (g, tq): tokens 2tq, 2tq+1 of the octet, column g)
     const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
     const uint32_t l01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
     const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
     // ---- O^T += V^T P^T over the 16 tokens, eight 16-channel tiles
-    {
-      if (nv < kBlock) {  // the open block: values of tokens past the sequence must not meet a zero weight
-        const uint32_t mlo = (tA < nv ? 0x0000FFFFu : 0u) | (tA + 1 < nv ? 0xFFFF0000u : 0u);
-        const uint32_t mhi = (tB < nv ? 0x0000FFFFu : 0u) | (tB + 1 < nv ? 0xFFFF0000u : 0u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          oA[4 * i] &= mlo;
-          oA[4 * i + 1] &= mlo;
-          oA[4 * i + 2] &= mhi;
-          oA[4 * i + 3] &= mhi;
-          oB[4 * i] &= mlo;
-          oB[4 * i + 1] &= mlo;
-          oB[4 * i + 2] &= mhi;
-          oB[4 * i + 3] &= mhi;
-        }
-      }
+    if (nv < kBlock) {  // the open block: values of tokens past the sequence must not meet a zero weight
+      const uint32_t mlo = (vA < nv ? 0x0000FFFFu : 0u) | (vA + 1 < nv ? 0xFFFF0000u : 0u);
+      const uint32_t mhi = (vB < nv ? 0x0000FFFFu : 0u) | (vB + 1 < nv ? 0xFFFF0000u : 0u);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        mma_bf16(acc[i], oA[4 * i], oA[4 * i + 1], oA[4 * i + 2], oA[4 * i + 3], h01, h23);
-        mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], h01, h23);
-        mma_bf16(acc[i], oA[4 * i], oA[4 * i + 1], oA[4 * i + 2], oA[4 * i + 3], l01, l23);
-        mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], l01, l23);
+        oA[4 * i] &= mlo;
+        oA[4 * i + 1] &= mlo;
+        oA[4 * i + 2] &= mhi;
+        oA[4 * i + 3] &= mhi;
+        oB[4 * i] &= mlo;
+        oB[4 * i + 1] &= mlo;
+        oB[4 * i + 2] &= mhi;
+        oB[4 * i + 3] &= mhi;
+      }
+    }
+    if (packed) {  // columns 0-3: high parts, columns 4-7: low parts of the same heads
+      const uint32_t pA = movmatrix_trans(tq < 2 ? h01 : l01), pB = movmatrix_trans(tq < 2 ? h23 : l23);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mma_bf16(acc[i], oA[4 * i], oA[4 * i + 1], oA[4 * i + 2], oA[4 * i + 3], pA, pB);
+        mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], pA, pB);
+      }
+    } else {
+      const uint32_t hA = movmatrix_trans(h01), hB = movmatrix_trans(h23);
+      const uint32_t lA = movmatrix_trans(l01), lB = movmatrix_trans(l23);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mma_bf16(acc[i], oA[4 * i], oA[4 * i + 1], oA[4 * i + 2], oA[4 * i + 3], hA, hB);
+        mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], hA, hB);
+        mma_bf16(acc[i], oA[4 * i], oA[4 * i + 1], oA[4 * i + 2], oA[4 * i + 3], lA, lB);
+        mma_bf16(acc[4 + i], oB[4 * i], oB[4 * i + 1], oB[4 * i + 2], oB[4 * i + 3], lA, lB);
       }
     }
 #pragma unroll
@@ -699,11 +725,23 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
       mbar_wait(&sm.mEmpty[cw][bb], static_cast<uint32_t>(u >> 1) & 1u, a.status);
     }
   }
-  lsum += __shfl_xor_sync(kFull, lsum, 1);
-  lsum += __shfl_xor_sync(kFull, lsum, 2);
-  if (tq == 0) {
-    sm.wm[cw][g] = mrun;
-    sm.wl[cw][g] = lsum;
+#pragma unroll
+  for (int d = 4; d < 32; d <<= 1) {
+    l0 += __shfl_xor_sync(kFull, l0, d);
+    l1 += __shfl_xor_sync(kFull, l1, d);
+  }
+  if (packed) {  // fold the low-part columns 4-7 into the high-part columns 0-3 of the same heads
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[m][k] += __shfl_xor_sync(kFull, acc[m][k], 2);
+  }
+  if (g == 0) {  // columns 4-7 of a packed warp hold no head of their own
+    const bool own = !packed || tq < 2;
+    sm.wm[cw][2 * tq] = own ? m0 : -INFINITY;
+    sm.wm[cw][2 * tq + 1] = own ? m1 : -INFINITY;
+    sm.wl[cw][2 * tq] = own ? l0 : 0.f;
+    sm.wl[cw][2 * tq + 1] = own ? l1 : 0.f;
   }
 }
 
@@ -872,18 +910,20 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     reinterpret_cast<uint32_t*>(&sm.vbw[hv][0][ln])[i] = x3 | (x3 << 16);
     reinterpret_cast<uint32_t*>(&sm.vbw[hv][1][ln])[i] = x4 | (x4 << 16);
   }
-  // q of the kv-head's query heads, times 2^-4, as A-operand quads of S^T = q K^T: for half `half`, lane
-  // (g, tq) and k-step m, (channels 128 half + 32tq + 4m + {0, 2}, 0, ... + {1, 3}, 0) of head g (rows 8-15 zero)
+  // q of the kv-head's query heads, times 2^-4 (and the sign of the scale), as B-operand pairs of
+  // S = K q^T: for half `half`, lane (g, tq) and k-step m, (channels 128 half + 32tq + 4m + {0, 2},
+  // ... + {1, 3}) of column g's head: head g, or g % 4 when the kv-head has at most 4 query heads
+  // (columns 4-7 repeat heads 0-3); columns without a head are zero
   for (int x = tid; x < KH * 32 * 8 * 2; x += kAttThreads) {
-    const int half = x / 512, ln = (x / 16) % 32, n = ln / 4, tq = ln % 4, m = (x / 2) % 8, odd = x % 2;
+    const int half = x / 512, ln = (x / 16) % 32, tq = ln % 4, m = (x / 2) % 8, odd = x % 2;
+    const int n = a.r <= 4 ? (ln / 4) & 3 : ln / 4;
     uint32_t v = 0u;
     if (n < a.r) {
       const uint16_t* qrow = a.q + (static_cast<size_t>(b) * a.Hq + H * a.r + n) * (NH * kD) +
                              kD * (KH == NH ? half : hf) + 32 * tq + 4 * m + odd;
       v = bf16x2_mul(static_cast<uint32_t>(qrow[0]) | (static_cast<uint32_t>(qrow[2]) << 16), a.qmul);
     }
-    reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd] = v;
-    reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[2 * odd + 1] = 0u;
+    reinterpret_cast<uint32_t*>(&sm.qf[half][m][ln])[odd] = v;
   }
   __syncthreads();  // barriers initialised, tables built
   if constexpr (NH > KH) cluster_sync();  // the peer's mailbox barriers exist before any remote arrival
