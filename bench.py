@@ -67,6 +67,7 @@ def parse():
     p.add_argument("--layers", type=int, default=36, help="layers per step (36 = the Qwen3-8B workload)")
     p.add_argument("--cpu-units", type=int, default=48, help="(layer, kv-head) units in the CPU oracle sample")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-side", action="store_true", help="skip the side workloads (configs 0, 2, 3, 4)")
     p.add_argument("--study", choices=["rope-drift"], default=None,
                    help="rope-drift: escape bytes per tile along 32K rotary keys for short and long calibration")
     p.add_argument("--timeline", action="store_true",
@@ -349,6 +350,182 @@ def hd256_attention(device, n_calib: int) -> dict:
             "us_per_layer": round(us, 2), "algorithmic_bytes": alg, "compressed_gbs": round(alg / (us * 1e-6) / 1e9, 1)}
 
 
+def graph_of(fn, stream):
+    """fn() run once eagerly (kernel attributes set outside the capture), then captured in a CUDA graph.
+    Synchronises first: the caches were built on the default stream, which `stream` does not wait for."""
+    import torch
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def config_entry(name, launches, us_compressed, us_bf16, alg_bytes, raw_bytes, peak, **extra) -> dict:
+    """One side config's figures: per-step times of both kernels and the compressed kernel's GB/s and
+    roofline fraction (algorithmic bytes of the step / its time)."""
+    d = {"workload": name, "launches_per_step": launches, "us_per_step": round(us_compressed, 2),
+         "bf16_cache_us_per_step": round(us_bf16, 2), "speedup_vs_bf16_cache": round(us_bf16 / us_compressed, 3),
+         "algorithmic_bytes_per_step": int(alg_bytes), "raw_bytes_per_step": int(raw_bytes),
+         "hbm_gbs_compressed": round(alg_bytes / (us_compressed * 1e-6) / 1e9, 1),
+         "equiv_uncompressed_gbs": round(raw_bytes / (us_compressed * 1e-6) / 1e9, 1),
+         "frac": round(alg_bytes / (us_compressed * 1e-6) / 1e9 / peak, 4),
+         "bf16_frac": round(raw_bytes / (us_bf16 * 1e-6) / 1e9 / peak, 4)}
+    d.update(extra)
+    return d
+
+
+def raw_cache_bytes(cache) -> int:
+    """Bytes the BF16 kernel reads for one launch: 16,384 per raw tile and 8 per table entry."""
+    _, _, mode, _ = cache.fields()
+    return int((mode == 1).sum().item()) * (16384 + 8)
+
+
+def side_configs(device, stream, steps: int, peak: float) -> dict:
+    """The other workloads, each with the compressed kernel and the BF16 kernel over an all-raw twin cache of
+    the same data (CUDA graphs, CUDA-event time, caches larger than L2 except config 0):
+      config 0: one layer, T = 4096 (L2-resident: launch latency only);
+      config 2: paged batch 32, lengths uniform in [4096, 32768], slots scattered by a seeded permutation,
+                28 launches per step cycling 4 distinct layers (1.7 GB compressed each);
+      config 3: batch 8 after a 32,768-token prefill, 28 layers, each of 256 decode steps appends one token
+                per sequence and layer and then attends (every step timed, seals included);
+      config 4: batch 4, T = 131,072, 10% random-bit tokens (one layer, 8 launches per timing)."""
+    import torch
+
+    import gaac_workloads as W
+    from lossless_compressed_kv_gaac_gb300.cache import LayerCache
+
+    out = {}
+    scale = W.WORKLOADS[0].scale
+
+    def pair_caches(cfg, layer, B, T, H, lens, adversarial=0.0, paged=False, max_blocks=None):
+        k, v = W.make_kv(cfg, layer, B, T, H, device=device, adversarial=adversarial)
+        mb = max_blocks or (T + 63) // 64
+        positions = B * mb * H * 2
+        ids = W.slot_permutation(cfg, layer, positions, device=device).to(torch.int32).view(B, mb, H, 2) if paged else None
+        c = LayerCache(B, H, mb, device=device, slot_ids=ids, n_slots=positions,
+                       n_raw=(positions if adversarial > 0 else 4096) + B * H * 2)
+        c.calibrate(k[0, :512], v[0, :512])
+        c.encode(k, v, lens)
+        r = LayerCache(B, H, mb, device=device, n_slots=0, n_raw=positions + B * H * 2)
+        r.encode(k, v, lens, raw=True)
+        del k, v
+        return c, r
+
+    def time_pair(cs, rs, qs, launches, reps):
+        outs = [torch.empty(q.shape, dtype=torch.float32, device=device) for q in qs]
+        res = []
+        for caches, bf in ((cs, False), (rs, True)):
+            def step():
+                for i in range(launches):
+                    caches[i % len(caches)].attention(qs[i % len(qs)], scale, out=outs[i % len(qs)], bf16=bf)
+            g = graph_of(step, stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+            res.append(time_graph(g, stream, reps) / reps * 1e3)
+            for c in caches:
+                assert int(c.status.item()) == 0, "attention reported an error"
+        return res
+
+    # ---- config 0: L2-resident single layer
+    wl = W.WORKLOADS[0]
+    lens = torch.tensor([wl.seq_len], dtype=torch.int32, device=device)
+    c, r = pair_caches(0, 0, 1, wl.seq_len, wl.n_kv_heads, lens)
+    q = W.make_q(0, 0, 1, wl.n_q_heads, device=device)
+    uc, ub = time_pair([c], [r], [q], 1, max(steps, 20))
+    out["config0"] = {"workload": wl.name, "us_per_launch": round(uc, 2), "bf16_cache_us_per_launch": round(ub, 2),
+                      "note": "16.8 MB of raw K/V: L2-resident, so a latency figure, not a bandwidth one"}
+    del c, r
+
+    # ---- config 2: paged batch 32, 28 layers (4 distinct layers cycled)
+    wl = W.WORKLOADS[2]
+    lens = W.make_lengths(2, wl.batch, wl.min_len, wl.seq_len, device=device)
+    cs, rs, qs = [], [], []
+    for layer in range(4):
+        c, r = pair_caches(2, layer, wl.batch, wl.seq_len, wl.n_kv_heads, lens, paged=True)
+        cs.append(c)
+        rs.append(r)
+        qs.append(W.make_q(2, layer, wl.batch, wl.n_q_heads, device=device))
+    uc, ub = time_pair(cs, rs, qs, wl.n_layers, steps)
+    alg = sum(algorithmic_bytes(c) for c in cs) / 4 * wl.n_layers
+    rawb = sum(raw_cache_bytes(r) for r in rs) / 4 * wl.n_layers
+    out["config2"] = config_entry(wl.name, wl.n_layers, uc, ub, alg, rawb, peak,
+                                  tokens=int(lens.sum().item()), distinct_layers=4,
+                                  splits=cs[0].auto_splits())
+    del cs, rs, qs
+    torch.cuda.empty_cache()
+
+    # ---- config 4: adversarial, one layer
+    wl = W.WORKLOADS[4]
+    lens = torch.tensor([wl.seq_len] * wl.batch, dtype=torch.int32, device=device)
+    c, r = pair_caches(4, 0, wl.batch, wl.seq_len, wl.n_kv_heads, lens, adversarial=wl.adversarial)
+    q = W.make_q(4, 0, wl.batch, wl.n_q_heads, device=device)
+    uc, ub = time_pair([c], [r], [q], 8, steps)
+    _, _, mode, _ = c.fields()
+    raw_share = float((mode == 1).double().mean().item())
+    out["config4"] = config_entry(wl.name, 1, uc / 8, ub / 8, algorithmic_bytes(c), raw_cache_bytes(r), peak,
+                                  raw_tile_share=round(raw_share, 4), splits=c.auto_splits())
+    del c, r
+    torch.cuda.empty_cache()
+
+    # ---- config 3: prefill 32768, then 256 steps of append + attention over 28 layers
+    wl = W.WORKLOADS[3]
+    B, H, T0, n_app = wl.batch, wl.n_kv_heads, wl.seq_len, wl.appends
+    mb = (T0 + n_app + 63) // 64
+    lens0 = torch.tensor([T0] * B, dtype=torch.int32, device=device)
+    cs, rs, qs, news = [], [], [], []
+    for layer in range(wl.n_layers):
+        c, r = pair_caches(3, layer, B, T0, H, lens0, max_blocks=mb)
+        cs.append(c)
+        rs.append(r)
+        qs.append(W.make_q(3, layer, B, wl.n_q_heads, device=device))
+        kn, vn = W.make_kv(3, layer, B, n_app, H, device=device, token_offset=T0)
+        news.append((kn, vn))
+    stage_k = [torch.empty((B, H, 128), dtype=torch.bfloat16, device=device) for _ in range(wl.n_layers)]
+    stage_v = [torch.empty_like(x) for x in stage_k]
+    outs = [torch.empty((B, wl.n_q_heads, 128), dtype=torch.float32, device=device) for _ in range(wl.n_layers)]
+    res = []
+    for caches, bf in ((cs, False), (rs, True)):
+        def step():
+            for i, c in enumerate(caches):
+                c.append(stage_k[i], stage_v[i])
+                c.attention(qs[i], scale, out=outs[i], bf16=bf)
+        g = graph_of(step, stream)  # the capture's eager run is step 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for i in range(wl.n_layers):
+                stage_k[i].copy_(news[i][0][:, 0])
+                stage_v[i].copy_(news[i][1][:, 0])
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for s_ in range(1, n_app):
+                for i in range(wl.n_layers):  # the step's new tokens (from the projections in a model)
+                    stage_k[i].copy_(news[i][0][:, s_])
+                    stage_v[i].copy_(news[i][1][:, s_])
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        res.append(e0.elapsed_time(e1) * 1e3 / (n_app - 1))
+        for c in caches:
+            stv = int(c.status.item())
+            assert stv == 0, f"config 3 ({'BF16' if bf else 'compressed'} cache): status {stv}"
+            assert c.seq_lens.tolist() == [T0 + n_app] * B, f"config 3 lengths {c.seq_lens.tolist()}"
+        del g
+    alg = sum(algorithmic_bytes(c) for c in cs)  # at the end of the run (33,024 tokens)
+    rawb = sum(raw_cache_bytes(r) for r in rs)
+    out["config3"] = config_entry(wl.name + " (append + attention per step)", 2 * wl.n_layers, res[0], res[1], alg,
+                                  rawb, peak, steps_timed=n_app - 1, splits=cs[0].auto_splits(),
+                                  note="bytes and GB/s at the final length, 33,024 tokens")
+    del cs, rs, qs, news
+    torch.cuda.empty_cache()
+    return out
+
+
 def bf16_sdpa_step(n_layers: int, device, stream, steps: int) -> dict:
     """Context for the uncompressed path: torch's scaled_dot_product_attention (a library kernel) over a
     contiguous BF16 cache of the same workload (32 q / 8 kv heads with GQA, T = 65,536, batch 1), one call per
@@ -394,7 +571,8 @@ def append_cost(k, v, n_calib: int) -> dict:
     """Device time of one decode-token append (all kv-heads, K and V, one layer, batch 1) with the
     open block as a BF16 raw tail and with it kept compressed in its slot.  64 consecutive appends (a
     block opening, 62 in-block tokens and a seal) are captured in a CUDA graph and replayed; the
-    time per append is the replay's CUDA-event time / 64."""
+    time per append is the replay's CUDA-event time / 64.  Each append is one launch (the length
+    advance is folded in)."""
     import torch
 
     from lossless_compressed_kv_gaac_gb300.cache import LayerCache
@@ -405,6 +583,14 @@ def append_cost(k, v, n_calib: int) -> dict:
     stream = torch.cuda.Stream(k.device)
     kn = k[0, T0:T0 + 64].unsqueeze(1).contiguous()  # [64, 1, H, 128]
     vn = v[0, T0:T0 + 64].unsqueeze(1).contiguous()
+    # one eager append on a throwaway cache first: the library settles its launch form (one launch, the
+    # sequence's CTAs as a cluster) outside a capture, as a serving loop's first decode step would
+    warm = LayerCache(1, H, T0 // 64 + 2, device=k.device)
+    warm.calibrate(k[0, :n_calib], v[0, :n_calib])
+    warm.encode(k[:, :T0], v[:, :T0], torch.tensor([T0], dtype=torch.int32, device=k.device))
+    warm.append(kn[0], vn[0])
+    torch.cuda.synchronize()
+    del warm
     for name, open_c in (("raw_tail", False), ("open_compressed", True)):
         c = LayerCache(1, H, T0 // 64 + 64 * (reps + 2) // 64, device=k.device, open_compressed=open_c)
         c.calibrate(k[0, :n_calib], v[0, :n_calib])
@@ -590,6 +776,14 @@ def run_gaac(args):
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except (OSError, ValueError):
         pass
+    side = None
+    if not args.no_side:
+        del g, g3
+        side = side_configs(device, stream, args.steps, peaks.get("hbm_gbs") or 6800.0)
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
@@ -632,6 +826,7 @@ def run_gaac(args):
         "append": app,
         "mode_ablation": abl,
         "hd256": hd256,
+        "configs": side,
         "ratio": {"payload": round(payload_ratio, 4), "resident": round(resident_ratio, 4),
                   "mode_shares": [round(st[f"groups{m}"] / max(1, 1024 * st["slot_tiles"]), 5) for m in range(3)]},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",

@@ -169,8 +169,12 @@ GAAC_API int gaac_encode_blocks(const uint16_t* k, const uint16_t* v, int64_t se
  * has none yet; a new tail tile is cleared to zero first).  When the tile becomes full it is encoded into slot
  * slot_ids[((b*max_blocks+blk)*n_kv_heads+h)*2+kv] (same layout as for
  * gaac_encode_blocks); if it fits, the entry becomes SLOT and the raw tile is
- * handed to block blk+1 as its tail; if not, the block stays RAW.  Finally
- * seq_lens[b] += 1 (a second small kernel on the same stream).
+ * handed to block blk+1 as its tail; if not, the block stays RAW.  slot_ids may be
+ * NULL (a cache of raw tiles only, as gaac_encode_blocks writes with NULL): a full
+ * tail then stays a RAW tile.  Finally seq_lens[b] += 1: with 2 * n_kv_heads <= 16
+ * the CTAs of a sequence run as one thread-block cluster (one launch) and the
+ * first advances the length once all have read it; with more kv-heads a second
+ * small kernel on the same stream does it.
  * seq_lens[b] must be < max_blocks*64 (else GAAC_EINVAL in *d_status).
  * base3/base4 as for gaac_encode_blocks (16-byte aligned, else GAAC_EINVAL).
  */
@@ -231,7 +235,15 @@ GAAC_API int gaac_append_ex(const uint16_t* k_new, const uint16_t* v_new, int32_
  */
 GAAC_API size_t gaac_attention_workspace(int batch, int n_kv_heads, int max_blocks, int n_splits);
 
-/* Number of splits gaac_decode_attention uses for n_splits = 0. */
+/*
+ * Number of splits gaac_decode_attention uses for n_splits = 0.  A launch with
+ * n_splits splits cuts every (sequence, kv-head) into chunks of
+ * ceil(max_blocks / n_splits) blocks, one CTA each (one CTA per SM); a sequence
+ * of nblk blocks uses max(1, ceil(nblk / chunk)) of them, so sequences of mixed
+ * lengths give CTAs of equal work.  The automatic count minimises, for full
+ * sequences, the number of waves of CTAs times (chunk + a CTA's fixed cost of
+ * about 4 blocks).
+ */
 GAAC_API int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_blocks);
 
 /*

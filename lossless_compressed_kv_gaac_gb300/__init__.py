@@ -230,12 +230,12 @@ def encode_blocks(k, v, seq_lens, max_blocks, base3, base4, table, slot_ids, poo
 def append(k_new, v_new, seq_lens, max_blocks, base3, base4, table, slot_ids, pools: Pools, stats=None,
            status=None, stream=None, open_compressed: bool = False) -> None:
     """Append one token per sequence.  k_new, v_new: BF16 [batch, kv_heads, 128]; slot_ids shaped like the
-    table (the slot a block is sealed into, or kept open in with open_compressed); seq_lens is
-    incremented."""
+    table (the slot a block is sealed into, or kept open in with open_compressed), or None for a cache of
+    raw tiles only (full tails stay raw); seq_lens is incremented."""
     pc = pools.c()
     _check("gaac_append_ex", lib().gaac_append_ex(
         k_new.data_ptr(), v_new.data_ptr(), seq_lens.data_ptr(), k_new.shape[0], k_new.shape[1], max_blocks,
-        base3.data_ptr(), base4.data_ptr(), table.data_ptr(), slot_ids.data_ptr(), ctypes.byref(pc),
+        base3.data_ptr(), base4.data_ptr(), table.data_ptr(), _ptr(slot_ids), ctypes.byref(pc),
         _ptr(stats), OPEN_COMPRESSED if open_compressed else 0, _ptr(status), _stream(stream)))
 
 

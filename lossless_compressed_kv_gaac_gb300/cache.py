@@ -44,6 +44,7 @@ class LayerCache:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.seq_lens = torch.zeros(batch, dtype=torch.int32, device=device)
         self._ws = None
+        self.all_raw = False  # encoded with raw=True: every block a raw tile, appends keep it so
 
     # -- building
     def calibrate(self, k_cal: torch.Tensor, v_cal: torch.Tensor, stream=None):
@@ -55,16 +56,23 @@ class LayerCache:
         """Prefill: k, v BF16 [batch, tokens, kv_heads, 128]; seq_lens int32 [batch].
         raw=True stores every block as BF16 (the uncompressed baseline cache)."""
         self.seq_lens.copy_(seq_lens)
+        self.all_raw = raw
         encode_blocks(k, v, self.seq_lens, self.max_blocks, self.base3, self.base4, self.table,
                       None if raw else self.slot_ids, self.pools, self.stats, self.status, stream,
                       open_compressed=self.open_compressed and not raw)
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """Decode step: one token per sequence, k_new/v_new BF16 [batch, kv_heads, 128]."""
-        append(k_new, v_new, self.seq_lens, self.max_blocks, self.base3, self.base4, self.table, self.slot_ids,
-               self.pools, self.stats, self.status, stream, open_compressed=self.open_compressed)
+        append(k_new, v_new, self.seq_lens, self.max_blocks, self.base3, self.base4, self.table,
+               None if self.all_raw else self.slot_ids, self.pools, self.stats, self.status, stream,
+               open_compressed=self.open_compressed)
 
     # -- reading
+    def auto_splits(self) -> int:
+        from . import auto_splits
+
+        return auto_splits(self.batch, self.n_kv_heads, self.max_blocks)
+
     def workspace(self, n_splits: int = 0) -> torch.Tensor:
         need = attention_workspace(self.batch, self.n_kv_heads, self.max_blocks, n_splits)
         if self._ws is None or self._ws.numel() < need:

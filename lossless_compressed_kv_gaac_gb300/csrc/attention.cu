@@ -55,6 +55,7 @@
 //    with a log-sum-exp (the final split reduction) and resets the counter.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -866,9 +867,12 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
     if (tid == 0) report(a.status, GAAC_EINVAL);
     len = 0;
   }
-  // This split's blocks of the sequence: an even share of its blocks.
+  // This split's blocks of the sequence: chunks of `per` blocks, the same for every sequence of the
+  // launch, so a shorter sequence uses fewer splits (at least one) and the others leave at once.
   const int nblk = (len + kBlock - 1) / kBlock;
-  const int per = (nblk + a.n_splits - 1) / a.n_splits;
+  const int per = (a.max_blocks + a.n_splits - 1) / a.n_splits;
+  const int n_used = max(1, (nblk + per - 1) / per);  // splits of this sequence, and partials its merge takes
+  if (split >= n_used) return;
   const int blk0 = split * per;
   const int n_my = max(0, min(nblk, blk0 + per) - blk0);
 
@@ -996,11 +1000,11 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   __syncthreads();
   if constexpr (NH > KH) cluster_sync();  // no remote arrival is still on its way to this CTA
   unsigned int* counter = a.counters + static_cast<size_t>(b) * nkv + y;
-  if (tid == 0) sm.last = atomic_add_acq_rel(counter, 1u) == static_cast<unsigned int>(a.n_splits - 1);
+  if (tid == 0) sm.last = atomic_add_acq_rel(counter, 1u) == static_cast<unsigned int>(n_used - 1);
   __syncthreads();
   GAAC_TL(if (tid == 0) if (TlCta* c = tl_cta()) c->exit = tl_now());
   if (!sm.last) return;
-  merge_splits<NH>(a.part + (static_cast<size_t>(b) * nkv + y) * a.n_splits * kPartFloats, a.n_splits, r, a.c_log2,
+  merge_splits<NH>(a.part + (static_cast<size_t>(b) * nkv + y) * a.n_splits * kPartFloats, n_used, r, a.c_log2,
                    a.out + (static_cast<size_t>(b) * a.Hq + H * r) * (NH * kD) + kD * hf, sm, tid);
   if (tid == 0) *counter = 0u;
   GAAC_TL(if (tid == 0) if (TlCta* c = tl_cta()) c->merged = tl_now());
@@ -1072,13 +1076,28 @@ static int pair_max_clusters() {
 
 using namespace gaac;
 
+// Split count for sequences of up to max_blocks blocks: each (sequence, kv-head) is cut into chunks of
+// ceil(max_blocks / s) blocks, one CTA per chunk, one resident CTA per SM.  The count minimises the
+// launch's length for full sequences, waves x (chunk + a CTA's fixed cost), the fixed cost (ramp-up of
+// its first copies, partial and merge) being worth about kCtaCostBlocks blocks; ties go to fewer splits.
+constexpr int kCtaCostBlocks = 4;
 extern "C" int gaac_attention_auto_splits(int batch, int n_kv_heads, int max_blocks) {
   if (batch <= 0 || n_kv_heads <= 0 || max_blocks <= 0) return 1;
-  const long long target = static_cast<long long>(kCtasPerSm) * device_sms();  // one wave of resident CTAs
+  const long long slots = static_cast<long long>(kCtasPerSm) * device_sms();
   const long long pairs = static_cast<long long>(batch) * n_kv_heads;
-  long long s = (target + pairs - 1) / pairs;
-  if (s > max_blocks) s = max_blocks;
-  return static_cast<int>(s < 1 ? 1 : s);
+  long long best = 1, best_cost = -1;
+  const long long smax = std::min<long long>(max_blocks, std::max<long long>(1, 64 * slots / pairs));
+  for (long long s = 1; s <= smax; ++s) {
+    const long long chunk = (max_blocks + s - 1) / s;
+    if (s > 1 && (max_blocks + chunk - 1) / chunk < s) continue;  // the same chunks as a smaller count
+    const long long waves = (pairs * s + slots - 1) / slots;
+    const long long cost = waves * (chunk + kCtaCostBlocks);
+    if (best_cost < 0 || cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return static_cast<int>(best);
 }
 
 static size_t partials_bytes(int batch, int n_kv_heads, int n_splits) {

@@ -835,7 +835,7 @@ __device__ int open_append_groups(OpenShared* os, uint8_t* slot, int kind, int p
 struct AppendArgs {
   const uint16_t* k_new;
   const uint16_t* v_new;
-  const int32_t* seq_lens;
+  int32_t* seq_lens;
   int n_kv_heads, max_blocks;
   const uint8_t* base3;
   const uint8_t* base4;
@@ -845,6 +845,7 @@ struct AppendArgs {
   gaac_stats* stats;
   unsigned flags;
   int32_t* status;
+  int bump;  // 1: the CTAs of a sequence form one cluster and its first CTA advances the length
 };
 
 // How one append reaches its block.
@@ -863,6 +864,11 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int len = a.seq_lens[b];
+  if (a.bump) {
+    // Every CTA of the sequence (one cluster) has read the length before the first one advances it.
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (blockIdx.x == 0 && tid == 0) a.seq_lens[b] = len + 1;
+  }
   if (len < 0 || len >= a.max_blocks * kBlock) {
     if (tid == 0) report(a.status, GAAC_EINVAL);
     return;
@@ -1002,6 +1008,13 @@ __global__ void __launch_bounds__(kEncThreads) append_kernel(AppendArgs a) {
     for (int i = 0; i < 4; ++i) d[tid + kEncThreads * i] = src[tid + kEncThreads * i];
   }
   __syncthreads();
+  if (a.slot_ids == nullptr) {  // an all-raw cache: the full tail stays a raw tile
+    if (tid == 0) {
+      *ep = make_entry(sh.raw_idx, 0, GAAC_MODE_RAW, kBlock);
+      if (a.stats != nullptr) atomicAdd(&a.stats->raw_tiles, 1ull);
+    }
+    return;
+  }
   const uint32_t slot_id = a.slot_ids[eidx];
   uint8_t* slot = nullptr;
   if (static_cast<int64_t>(slot_id) < a.pools.n_slots) {
@@ -1065,6 +1078,42 @@ __global__ void bump_lens_kernel(int32_t* lens, int batch) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the append kernel has read every length
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < batch) lens[i] += 1;
+}
+
+// Whether clusters of n append CTAs (one sequence's tiles) can be launched on this device, cached per
+// device and size; sizes above 8 need the non-portable cluster attribute.  The first question is not
+// answered while `st` is being captured into a graph (the two-kernel form serves that call).
+static bool append_cluster_ok(int n, cudaStream_t st) {
+  if (n < 1 || n > 16) return false;
+  static signed char cached[64][17] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (cached[dev][n] == 0) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return false;
+    }
+    bool ok = n <= 8 || cudaFuncSetAttribute(append_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                            cudaSuccess;
+    if (ok) {
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = n;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(n, 1);
+      cfg.blockDim = dim3(kEncThreads);
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      ok = cudaOccupancyMaxActiveClusters(&clusters, append_kernel, &cfg) == cudaSuccess && clusters > 0;
+    }
+    cudaGetLastError();
+    cached[dev][n] = ok ? 1 : -1;
+  }
+  return cached[dev][n] > 0;
 }
 
 }  // namespace gaac
@@ -1131,17 +1180,17 @@ extern "C" int gaac_append_ex(const uint16_t* k_new, const uint16_t* v_new, int3
                               gaac_entry* table, const uint32_t* slot_ids, const gaac_pools* pools,
                               gaac_stats* stats, unsigned flags, int32_t* d_status, void* stream) {
   if (k_new == nullptr || v_new == nullptr || seq_lens == nullptr || base3 == nullptr || base4 == nullptr ||
-      table == nullptr || slot_ids == nullptr || !pools_ok(pools) ||
-      (flags & ~static_cast<unsigned>(GAAC_OPEN_COMPRESSED)))
+      table == nullptr || !pools_ok(pools) || (flags & ~static_cast<unsigned>(GAAC_OPEN_COMPRESSED)) ||
+      (slot_ids == nullptr && (flags & GAAC_OPEN_COMPRESSED)))
     return GAAC_EINVAL;
   if (batch <= 0 || batch > 65535 || n_kv_heads <= 0 || n_kv_heads > 1024 || max_blocks <= 0) return GAAC_EINVAL;
   if ((reinterpret_cast<uintptr_t>(base3) & 15u) || (reinterpret_cast<uintptr_t>(base4) & 15u)) return GAAC_EINVAL;
   AppendArgs a{k_new, v_new, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids, *pools,
-               stats, flags, d_status};
+               stats, flags, d_status, 0};
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Both kernels are programmatic dependents of their predecessor on the stream (each waits for it before
-  // any read): a launch is set up while the previous kernel runs.
-  cudaLaunchAttribute attr[1];
+  // Programmatic dependents of their predecessor on the stream (each waits for it before any read): a
+  // launch is set up while the previous kernel runs.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
@@ -1150,6 +1199,19 @@ extern "C" int gaac_append_ex(const uint16_t* k_new, const uint16_t* v_new, int3
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // One launch: the 2 * n_kv_heads CTAs of a sequence as one thread-block cluster, whose first CTA
+  // advances the length once all have read it.  Otherwise (more than 16 CTAs per sequence, or clusters of
+  // that size not schedulable) a second small kernel advances the lengths.
+  if (append_cluster_ok(2 * n_kv_heads, st)) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2 * n_kv_heads;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    a.bump = 1;
+    if (cudaLaunchKernelEx(&cfg, append_kernel, a) != cudaSuccess) return GAAC_ECUDA;
+    return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
+  }
   if (cudaLaunchKernelEx(&cfg, append_kernel, a) != cudaSuccess) return GAAC_ECUDA;
   cfg.gridDim = dim3((batch + 255) / 256);
   cfg.blockDim = dim3(256);

@@ -368,3 +368,26 @@ def test_extreme_logits_and_scale_signs(scale):
     assert U.check_attention(out, q, k, v, lens, scale).compared == B * Hq
     if scale > 0:
         assert torch.equal(out[0], v[0, 700].float().repeat_interleave(Hq // H, dim=0))
+
+
+@pytest.mark.parametrize("H", [8, 12])
+def test_raw_cache_appends_stay_raw(H):
+    """A cache of raw tiles only (the BF16 baseline) grows by appends whose full tails stay raw tiles; the
+    BF16 kernel reads it.  H = 8 runs the single-launch append (a sequence's 16 CTAs as one cluster),
+    H = 12 the two-kernel form (24 CTAs per sequence)."""
+    B, T0, steps = 3, 200, 130
+    T = T0 + steps
+    k, v = U.kv(3, 1, B, T, H)
+    c = LayerCache(B, H, (T + 63) // 64 + 1)
+    c.calibrate(k[0, :T0], v[0, :T0])
+    c.encode(k[:, :T0], v[:, :T0], U.lens_tensor([T0] * B), raw=True)
+    q = W.make_q(3, 1, B, 2 * H, device="cuda")
+    for s in range(steps):
+        c.append(k[:, T0 + s].contiguous(), v[:, T0 + s].contiguous())
+    assert _status(c) == 0
+    assert c.seq_lens.tolist() == [T] * B
+    n = U.check_tiles(c, k, v, c.seq_lens, raw_all=True)
+    assert n["slot"] == 0 and n["raw"] == B * ((T + 63) // 64) * H * 2
+    out = c.attention(q, 1 / np.sqrt(128), bf16=True)
+    assert _status(c) == 0
+    assert U.check_attention(out, q, k, v, c.seq_lens, 1 / np.sqrt(128)).compared == B * 2 * H
