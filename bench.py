@@ -923,6 +923,45 @@ def oracle_pool_times(unit_lists) -> list:
         return [t for ts in pool.map(_oracle_units, unit_lists) for t in ts]
 
 
+def cpu_config0_single_thread() -> dict:
+    """The oracle on one host thread over the whole config-0 workload (one layer, batch 1, 8 kv-heads,
+    T = 4096, 16 query heads; seeded inputs drawn on the CPU): calibration, encode of its 1,024 tiles,
+    decode of them, and fp64 attention over the decoded cache, each timed."""
+    import numpy as np
+
+    import gaac_workloads as W
+    import oracle as O
+
+    wl = W.WORKLOADS[0]
+    T, H = wl.seq_len, wl.n_kv_heads
+    k, v = W.make_kv(0, 0, 1, T, H)
+    kn, vn = (W.bits(x).numpy().view(np.uint16)[0] for x in (k, v))
+    q = W.bits(W.make_q(0, 0, 1, wl.n_q_heads)).numpy().view(np.uint16)[0]
+    t0 = time.perf_counter()
+    bases = (O.calibrate(kn[:wl.n_calib]), O.calibrate(vn[:wl.n_calib]))
+    t1 = time.perf_counter()
+    imgs = []
+    for blk in range(T // 64):
+        for h in range(H):
+            for kind, x in ((0, kn), (1, vn)):
+                b3, b4 = bases[kind]
+                img, e = O.encode_tile(x[blk * 64:(blk + 1) * 64, h], kind, b3[h], b4[h])
+                imgs.append((blk, h, kind, img, e))
+    t2 = time.perf_counter()
+    kd, vd = np.zeros_like(kn), np.zeros_like(vn)
+    for blk, h, kind, img, e in imgs:
+        b3, b4 = bases[kind]
+        tile, _ = O.decode_tile(img, kind, b3[h], b4[h], e)
+        (kd if kind == 0 else vd)[blk * 64:(blk + 1) * 64, h] = tile
+    t3 = time.perf_counter()
+    O.attention(q, kd, vd, wl.scale)
+    t4 = time.perf_counter()
+    assert np.array_equal(kd, kn) and np.array_equal(vd, vn)
+    return {"workload": wl.name, "threads": 1, "calibrate_s": round(t1 - t0, 4), "encode_s": round(t2 - t1, 3),
+            "decode_s": round(t3 - t2, 3), "attention_s": round(t4 - t3, 3),
+            "decode_attention_us_per_step": round((t4 - t2) * 1e6, 1)}
+
+
 def cpu_baseline(units: int, n_layers: int) -> dict:
     """Oracle throughput on the host cores: `units` (layer, kv-head) units spread over one process per core,
     all cores busy at once; a step is n_layers x 8 units shared by those cores."""
@@ -934,10 +973,14 @@ def cpu_baseline(units: int, n_layers: int) -> dict:
     H = 8
     step_us = statistics.mean(times) * n_layers * H / cores * 1e6
     return {"value": round(step_us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{units} (layer, kv-head) units of the workload, {cores} processes at once: per unit the oracle "
-                      f"decodes 2x1024 tiles and runs fp64 attention for 4 query heads over 65536 tokens "
-                      f"(mean {statistics.mean(times):.3f} s per unit with every core busy); a step is "
-                      f"{n_layers * H} units over {cores} cores; {wall:.0f} s wall including the untimed encode"}
+            "extrapolated": {"units_timed": units, "units_per_step": n_layers * H,
+                             "mean_s_per_unit_all_cores_busy": round(statistics.mean(times), 4)},
+            "sample": f"sampled extrapolation: {units} (layer, kv-head) units of the workload timed, {cores} processes "
+                      f"at once: per unit the oracle decodes 2x1024 tiles and runs fp64 attention for 4 query heads "
+                      f"over 65536 tokens (mean {statistics.mean(times):.3f} s per unit with every core busy); the "
+                      f"value is that mean x {n_layers * H} units per step / {cores} cores; {wall:.0f} s wall "
+                      f"including the untimed encode",
+            "config0_single_thread": cpu_config0_single_thread()}
 
 
 _WORKER_SAMPLE = None
@@ -968,11 +1011,13 @@ def run_reference(args):
     H = 8
     ctx = mp.get_context("spawn")
     counter = ctx.Value("i", 0)
-    steps_us = []
+    steps_us, walls = [], []
     with ctx.Pool(cores, initializer=_init_reference_worker, initargs=(counter, args.layers * H)) as pool:
         for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
             times = pool.map(_time_reference_worker, range(cores), chunksize=1)
             if i >= args.warmup:
+                walls.append(time.perf_counter() - t0)
                 steps_us.append(statistics.mean(times) * args.layers * H / cores * 1e6)
     v = statistics.median(steps_us)
     print(json.dumps({
@@ -981,9 +1026,13 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "layers": args.layers},
         "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"per step {cores} (layer, kv-head) units at once, one process per core (decode "
-                                   "2x1024 tiles + fp64 attention, 4 heads x 65536 tokens), scaled to "
-                                   f"{args.layers} layers x {H} kv-heads over {cores} cores"},
+                         "extrapolated": {"units_timed_per_step": cores, "units_per_step": args.layers * H,
+                                          "wall_s_per_timed_step": round(statistics.median(walls), 3)},
+                         "sample": f"sampled extrapolation: per step {cores} (layer, kv-head) units run at once, one "
+                                   "process per core (decode 2x1024 tiles + fp64 attention, 4 heads x 65536 tokens); "
+                                   f"the value is their mean time x {args.layers} layers x {H} kv-heads / {cores} "
+                                   f"cores, so a timed step takes {statistics.median(walls):.2f} s of wall time and "
+                                   "stands for the whole step"},
         "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
