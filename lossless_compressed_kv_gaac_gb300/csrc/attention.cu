@@ -221,22 +221,21 @@ __device__ __forceinline__ void join_v2(uint32_t w, uint32_t e, uint32_t& p02, u
 //  bits 0-15: byte permute selector that gathers the unit's 4-bit escape
 //    bytes from the four escape bytes at the unit's offset (byte j = group j's
 //    escape byte if group j is 4-bit, else a zero byte);
-//  bits 16-18: 4-bit groups; bits 19-21: raw groups; bit 22: a reserved tag;
-//  bits 24-27: which groups are raw.
+//  byte 2: the 4-bit groups, plus 32 per reserved tag, so that a reserved tag
+//    breaks its eighth's check against the escape directory;
+//  byte 3: the raw groups.
+// Bytes 2 and 3 of two units' entries are the packed counts of the warp scan.
 __device__ __forceinline__ uint32_t tag_entry(uint32_t tb) {
-  uint32_t sel = 0, n4 = 0, nr = 0, rsv = 0, raw = 0;
+  uint32_t sel = 0, n4 = 0, nr = 0, rsv = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t t = (tb >> (2 * j)) & 3u;
     sel |= (t == 1u ? n4 : 4u) << (4 * j);  // 4: a zero byte of the second operand
     if (t == 1u) ++n4;
-    if (t == 2u) {
-      ++nr;
-      raw |= 1u << j;
-    }
-    if (t == 3u) rsv = 1u;
+    if (t == 2u) ++nr;
+    if (t == 3u) ++rsv;
   }
-  return sel | (n4 << 16) | (nr << 19) | (rsv << 22) | (raw << 24);
+  return sel | ((n4 + 32u * rsv) << 16) | (nr << 24);
 }
 
 // The four escape bytes starting at escape offset `off` (clamped into the escape area).
@@ -310,7 +309,7 @@ __device__ __forceinline__ void raw_unit(const uint8_t* img, int u, uint32_t o[1
 
 // The lane's two units of one tile image (units 64w + lane and 64w + 32 +
 // lane, in eighths 2w and 2w+1), rebuilt into oA / oB; badA / badB: the
-// eighth failed its checks (its words are zero).  Slot bookkeeping: the
+// eighth failed its checks (its words are then meaningless).  Slot bookkeeping: the
 // directory gives each eighth's first 4-bit escape byte and raw group, one
 // warp scan of the four packed counts (at most 4 per unit, 128 per eighth)
 // each unit's.
@@ -325,8 +324,7 @@ __device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, co
     const uint32_t d0 = w ? dir[2 * w - 1] : 0u, dA = dir[2 * w], dB = dir[2 * w + 1], d7 = dir[7];
     const uint32_t tbA = img[kOffTag + uA], tbB = img[kOffTag + uB];
     const uint32_t teA = sm.tagl[tbA], teB = sm.tagl[tbB];
-    const uint32_t cnt = ((teA >> 16) & 7u) | (((teB >> 16) & 7u) << 8) | (((teA >> 19) & 7u) << 16) |
-                         (((teB >> 19) & 7u) << 24);
+    const uint32_t cnt = __byte_perm(teA, teB, 0x7362);  // 4-bit A, 4-bit B, raw A, raw B
     const uint32_t incl = warp_incl_scan(cnt, lane);
     const uint32_t tot = __shfl_sync(kFull, incl, 31), ex = incl - cnt;
     const int rawbase = static_cast<int>(d7 & 0x1FFu);
@@ -338,12 +336,12 @@ __device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, co
     decode_unit(img, uB, tbB, __byte_perm(escape_window(img, o4B), 0u, teB & 0xFFFFu), b3B, b4B, sm.lut, oB);
     if (teA >> 24) fix_raw(img, uA, tbA, orA, oA);  // raw groups: rare
     if (teB >> 24) fix_raw(img, uB, tbB, orB, oB);
+    // Checks of the format, on warp-uniform values (no vote): the directory entry after each eighth must be
+    // the one before it plus the eighth's counts from the tags (exact arithmetic: the counts of a valid image
+    // never fill their fields), and the totals must give esc_len.  A reserved tag counts 32 four-bit groups.
     const bool totals = rawbase + 8 * static_cast<int>(d7 >> 9) != esc_len;
-    badA = __any_sync(kFull, (teA >> 22) & 1u) || totals || (d0 & 0x1FFu) + (tot & 0xFFu) != (dA & 0x1FFu) ||
-           (d0 >> 9) + ((tot >> 16) & 0xFFu) != (dA >> 9);
-    badB = __any_sync(kFull, (teB >> 22) & 1u) || totals ||
-           (dA & 0x1FFu) + ((tot >> 8) & 0xFFu) != (dB & 0x1FFu) || (dA >> 9) + (tot >> 24) != (dB >> 9);
-    if ((badA || badB) && lane == 0) report(a.status, GAAC_EFORMAT);
+    badA = totals || ((d0 + (tot & 0xFFu) + (((tot >> 16) & 0xFFu) << 9)) & 0xFFFFu) != dA;
+    badB = totals || ((dA + ((tot >> 8) & 0xFFu) + ((tot >> 24) << 9)) & 0xFFFFu) != dB;
   } else {
     badA = badB = mode != GAAC_MODE_RAW;
     if (!badA) {
@@ -351,14 +349,9 @@ __device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, co
       raw_unit(img, uB, oB);
     }
   }
-  if (badA) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) oA[i] = 0u;
-  }
-  if (badB) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) oB[i] = 0u;
-  }
+  // The words of a unit that failed its checks are left as they are (no branch here, between the decode
+  // and the MMAs): a bad K eighth's scores are masked in the softmax and a bad V eighth's operands are
+  // cleared just before the PV MMAs.
 }
 
 // ------------------------------------------------------------------ producer
@@ -489,7 +482,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
   constexpr int kStages = AttSmem<NH, KH>::kStages;
   const int g = lane >> 2, tq = lane & 3;
   uint32_t kb3[8], kb4[8];  // one half-head: loaded once (NH = 1) or per half and block (NH = 2)
-  if (KH == 1 && !RAW) k_bases(sm, 0, tq, kb3, kb4);
+  // K base words are reloaded from shared memory per block (registers are scarce at 12 warps per SM)
   [[maybe_unused]] uint32_t peer_mail = 0u, peer_full = 0u, peer_empty = 0u, peer_ack = 0u;  // the peer's mailbox
   if constexpr (NH > KH) {
     const uint32_t peer = cluster_rank() ^ 1u;
@@ -509,6 +502,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
   const int tA = 16 * w + g, tB = tA + 8;        // tokens of S rows g, g+8
   const int vA = 16 * w + 2 * tq, vB = vA + 8;   // tokens of the V operand's columns 2tq, 2tq+1
   const bool packed = a.r <= 4;
+  bool fmt_bad = false;  // a tile this warp read failed the format checks (reported once, at the end)
   // BF16 path: q's B-operand registers stay in registers across blocks
   [[maybe_unused]] uint32_t qb0[8], qb1[8];
   if constexpr (RAW) {
@@ -538,7 +532,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
     // of the two tokens are the A operand (k-step m: a0, a2 = token tA, a1, a3 = token tB), q^T the B
     // operand; even and odd k-steps go to two accumulators (a chain of four MMAs each)
     float sc[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-    bool kbadA = false, kbadB = false;
+    bool kbadA = false, kbadB = false, vbadA = false, vbadB = false;
     uint32_t oA[16], oB[16];  // the V operands of this warp's 16 tokens
     if constexpr (RAW) {
       static_assert(NH == 1 && KH == 1, "the BF16 path serves 128-channel heads");
@@ -550,12 +544,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
       raw_unit(sm.stage[st][1], uB, oB);
       release_stage<NH, KH>(a, sm, st, jn, n_my, lane, ne);
       kbadA = kbadB = meta.mode[0] != GAAC_MODE_RAW;
-      const bool vbad = meta.mode[1] != GAAC_MODE_RAW;
-      if ((kbadA || vbad) && lane == 0) report(a.status, GAAC_EFORMAT);
-      if (vbad) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) oA[i] = oB[i] = 0u;
-      }
+      vbadA = vbadB = meta.mode[1] != GAAC_MODE_RAW;
 #pragma unroll
       for (int m = 0; m < 8; m += 2) {
         mma_bf16(sc, kA[2 * m], kB[2 * m], kA[2 * m + 1], kB[2 * m + 1], qb0[m], qb1[m]);
@@ -564,7 +553,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
     } else {
 #pragma unroll 1
       for (int half = 0; half < KH; ++half) {
-        if (KH > 1) k_bases(sm, half, tq, kb3, kb4);
+        k_bases(sm, half, tq, kb3, kb4);
         uint32_t oA[16], oB[16];
         bool bA, bB;
         tile_units(a, sm, sm.stage[st][half], meta.mode[half], meta.esc[half], w, lane, kb3, kb4, kb3, kb4, oA, oB,
@@ -596,7 +585,6 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
                     peer_full + bb * sizeof(uint64_t));
       }
       // ---- V units of the same tokens (independent of the scores: decoded while the MMAs above run)
-      bool vbadA, vbadB;
       uint32_t vb3[2][8], vb4[2][8];  // word 2i and 2i+1 serve group i
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
@@ -641,6 +629,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
     }
     // ---- online softmax of columns 2tq, 2tq+1 over the warp's 16 tokens, on raw scores (q/16).k: only the
     // differences from the running maxima are scaled to the log2 domain
+    fmt_bad = fmt_bad || kbadA || kbadB || vbadA || vbadB;
     const float x0 = (!kbadA && tA < nv) ? sc[0] + s1[0] : -INFINITY;  // token tA, column 2tq
     const float x1 = (!kbadA && tA < nv) ? sc[1] + s1[1] : -INFINITY;  // token tA, column 2tq+1
     const float x2 = (!kbadB && tB < nv) ? sc[2] + s1[2] : -INFINITY;  // token tB
@@ -680,19 +669,22 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
     const uint32_t l01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
     const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
     // ---- O^T += V^T P^T over the 16 tokens, eight 16-channel tiles
-    if (nv < kBlock) {  // the open block: values of tokens past the sequence must not meet a zero weight
+    if (nv < kBlock || vbadA || vbadB) {
+      // the open block: values of tokens past the sequence must not meet a zero weight; a V eighth that
+      // failed its checks contributes nothing
       const uint32_t mlo = (vA < nv ? 0x0000FFFFu : 0u) | (vA + 1 < nv ? 0xFFFF0000u : 0u);
       const uint32_t mhi = (vB < nv ? 0x0000FFFFu : 0u) | (vB + 1 < nv ? 0xFFFF0000u : 0u);
+      const uint32_t kA = vbadA ? 0u : 0xFFFFFFFFu, kB = vbadB ? 0u : 0xFFFFFFFFu;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        oA[4 * i] &= mlo;
-        oA[4 * i + 1] &= mlo;
-        oA[4 * i + 2] &= mhi;
-        oA[4 * i + 3] &= mhi;
-        oB[4 * i] &= mlo;
-        oB[4 * i + 1] &= mlo;
-        oB[4 * i + 2] &= mhi;
-        oB[4 * i + 3] &= mhi;
+        oA[4 * i] &= mlo & kA;
+        oA[4 * i + 1] &= mlo & kA;
+        oA[4 * i + 2] &= mhi & kA;
+        oA[4 * i + 3] &= mhi & kA;
+        oB[4 * i] &= mlo & kB;
+        oB[4 * i + 1] &= mlo & kB;
+        oB[4 * i + 2] &= mhi & kB;
+        oB[4 * i + 3] &= mhi & kB;
       }
     }
     if (packed) {  // columns 0-3: high parts, columns 4-7: low parts of the same heads
@@ -726,6 +718,7 @@ __device__ __forceinline__ void compute_warp(const AttnArgs& a, AttSmem<NH, KH>&
       mbar_wait(&sm.mEmpty[cw][bb], static_cast<uint32_t>(u >> 1) & 1u, a.status);
     }
   }
+  if (fmt_bad && lane == 0) report(a.status, GAAC_EFORMAT);
 #pragma unroll
   for (int d = 4; d < 32; d <<= 1) {
     l0 += __shfl_xor_sync(kFull, l0, d);

@@ -391,3 +391,28 @@ def test_raw_cache_appends_stay_raw(H):
     out = c.attention(q, 1 / np.sqrt(128), bf16=True)
     assert _status(c) == 0
     assert U.check_attention(out, q, k, v, c.seq_lens, 1 / np.sqrt(128)).compared == B * 2 * H
+
+
+def test_corrupted_slot_images_are_reported():
+    """Slot images that break the format are reported as GAAC_EFORMAT by the attention kernel, without a
+    fault, and only the kv-head they belong to is affected: a reserved tag (tag 3) in a K tile, then an
+    escape-directory entry that disagrees with the tags in a V tile."""
+    k, v = U.kv(0, 4, 1, 512, 8)
+    lens = U.lens_tensor([512])
+    c = U.build(k, v, lens)
+    q = W.make_q(0, 4, 1, 16, device="cuda")
+    good = c.attention(q, 1 / np.sqrt(128)).clone()
+    assert _status(c) == 0
+    idx = c.fields()[0]
+    pool = c.pools.slot_pool
+    for (blk, h, kind, off, val) in ((2, 1, 0, 11264 + 40, 0x03), (5, 5, 1, 11520 + 2 * 3, 0x7F)):
+        s = int(idx[0, blk, h, kind])
+        saved = pool[s].clone()
+        pool[s, off] = pool[s, off] | val
+        c.status.zero_()
+        out = c.attention(q, 1 / np.sqrt(128))
+        assert _status(c) == G.EFORMAT
+        assert torch.isfinite(out).all()
+        others = [hq for hq in range(16) if hq // 2 != h]
+        assert torch.equal(out[0, others], good[0, others])
+        pool[s] = saved
