@@ -250,7 +250,7 @@ __device__ __forceinline__ uint32_t escape_window(const uint8_t* img, int off) {
 // holds elements 4m + {0,2} (i=0) / {1,3} (i=1).  x: the unit's gathered 4-bit
 // escape bytes (byte j = group j); b3/b4: the unit's base3 and base4 words
 // base3 (32-bit, modular: e stays exact), word 2i and 2i+1 covering group i.
-// Raw groups come out wrong and are re-joined by fix_raw.
+// A raw group comes out right when its base3 words hold its exponents (raw_bases).
 __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t tb, uint32_t x, const uint32_t b3[8],
                                             const uint32_t b4[8], const uint2* lut, uint32_t o[16]) {
   const uint32_t* cw = reinterpret_cast<const uint32_t*>(img + kOffCode);
@@ -278,17 +278,17 @@ __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t 
   }
 }
 
-// Re-joins the raw groups of unit u: their exponents are eight escape bytes
-// each, the unit's first at escape offset `oraw` (clamped into the area).
-__device__ __forceinline__ void fix_raw(const uint8_t* img, int u, uint32_t tb, int oraw, uint32_t o[16]) {
+// Raw groups of a unit take their exponents as base words: a raw group's codes are zero and its escape
+// selector byte is zero, so decode_unit's exponent sum is the base word itself.  The eight exponent bytes of
+// each raw group start at escape offset `oraw` (clamped into the area); b3: the unit's base3 words, those of
+// its raw groups replaced.
+__device__ __forceinline__ void raw_bases(const uint8_t* img, uint32_t tb, int oraw, uint32_t b3[8]) {
 #pragma unroll
   for (int gi = 0; gi < 4; ++gi) {
     if (((tb >> (2 * gi)) & 3u) == 2u) {
       const int at = kOffEsc + min(oraw, kEscCap - 8);
-      const uint32_t x0 = load_u32_any(img, at), x1 = load_u32_any(img, at + 4);
-      const uint2 smw = *reinterpret_cast<const uint2*>(img + 32 * u + 8 * gi);
-      join_v2(smw.x, x0, o[4 * gi], o[4 * gi + 1]);
-      join_v2(smw.y, x1, o[4 * gi + 2], o[4 * gi + 3]);
+      b3[2 * gi] = load_u32_any(img, at);
+      b3[2 * gi + 1] = load_u32_any(img, at + 4);
       oraw += 8;
     }
   }
@@ -332,10 +332,16 @@ __device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, co
     const int o4B = static_cast<int>((dA & 0x1FFu) + ((ex >> 8) & 0xFFu));
     const int orA = rawbase + 8 * static_cast<int>((d0 >> 9) + ((ex >> 16) & 0xFFu));
     const int orB = rawbase + 8 * static_cast<int>((dA >> 9) + (ex >> 24));
-    decode_unit(img, uA, tbA, __byte_perm(escape_window(img, o4A), 0u, teA & 0xFFFFu), b3A, b4A, sm.lut, oA);
-    decode_unit(img, uB, tbB, __byte_perm(escape_window(img, o4B), 0u, teB & 0xFFFFu), b3B, b4B, sm.lut, oB);
-    if (teA >> 24) fix_raw(img, uA, tbA, orA, oA);  // raw groups: rare
-    if (teB >> 24) fix_raw(img, uB, tbB, orB, oB);
+    uint32_t eA[8], eB[8];  // base3 words, raw groups' exponents in their place (raw groups: rare)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      eA[i] = b3A[i];
+      eB[i] = b3B[i];
+    }
+    if (teA >> 24) raw_bases(img, tbA, orA, eA);
+    if (teB >> 24) raw_bases(img, tbB, orB, eB);
+    decode_unit(img, uA, tbA, __byte_perm(escape_window(img, o4A), 0u, teA & 0xFFFFu), eA, b4A, sm.lut, oA);
+    decode_unit(img, uB, tbB, __byte_perm(escape_window(img, o4B), 0u, teB & 0xFFFFu), eB, b4B, sm.lut, oB);
     // Checks of the format, on warp-uniform values (no vote): the directory entry after each eighth must be
     // the one before it plus the eighth's counts from the tags (exact arithmetic: the counts of a valid image
     // never fill their fields), and the totals must give esc_len.  A reserved tag counts 32 four-bit groups.
@@ -850,9 +856,30 @@ __global__ void __launch_bounds__(kAttThreads, kCtasPerSm) attn_split_kernel(Att
   const int split = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
   const int H = y / NH, hf = y % NH, nkv = NH * a.Hkv;  // nkv: half-heads in the table and the bases
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Launched as a programmatic dependent of the previous kernel on the stream,
-  // the CTA may already be resident while that kernel finishes: wait for it
-  // (and its memory) before reading anything.  A no-op for an ordinary launch.
+  // Launched as a programmatic dependent of the previous kernel on the stream, the CTA may already be
+  // resident while that kernel finishes.  Meanwhile its first blocks' images are prefetched into L2 from a
+  // guess of the length and table (the previous kernel may still write them: a stale or torn guess only
+  // wastes a prefetch, and every address is checked against the pools), then the CTA waits for that
+  // kernel (and its memory) before any read it relies on.  A no-op wait for an ordinary launch.
+  if (tid < kStages) {
+    const int glen = *reinterpret_cast<const volatile int32_t*>(a.seq_lens + b);
+    if (glen > 0 && glen <= a.max_blocks * kBlock) {
+      const int gper = (a.max_blocks + a.n_splits - 1) / a.n_splits;
+      const int gblk = split * gper + tid;
+      if (tid < gper && gblk * kBlock < glen) {
+        uint2 e[KH + 1];
+        block_entries<NH, KH>(a, b, H, hf, gblk, e);
+#pragma unroll
+        for (int i = 0; i <= KH; ++i) {
+          uint32_t bytes;
+          int mode, esc;
+          const void* src = tile_source(a, e[i], bytes, mode, esc);
+          if (src != nullptr)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+        }
+      }
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   GAAC_TL(if (tid == 0) if (TlCta* c = tl_cta()) { c->start = tl_now(); c->merged = 0ull; });
   int len = a.seq_lens[b];
