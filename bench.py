@@ -1097,7 +1097,13 @@ def timeline_summary(raw, n_ctas: int, n_blocks: int, grid) -> dict:
                          "max": round(float((merged - exit_)[merged > 0].max()) / 1e3, 2)},
             "copy_issue_to_land_us": {"p10": q(inflight, 10), "p50": q(inflight, 50), "p90": q(inflight, 90)},
             "group_wait_for_data_us": {"p10": q(waited, 10), "p50": q(waited, 50), "p90": q(waited, 90)},
-            "blocks_per_cta": round(float(used.sum(axis=1).mean()), 1)}
+            "blocks_per_cta": round(float(used.sum(axis=1).mean()), 1),
+            # split work per kv-head: the spread within a head (per-SM speed) against the spread of the
+            # heads' means (per-head data)
+            "split_work_by_head_us": {"head_means_min": round(float(((split_end - start).reshape(Z * Y, X).mean(1)).min()) / 1e3, 2),
+                                      "head_means_max": round(float(((split_end - start).reshape(Z * Y, X).mean(1)).max()) / 1e3, 2),
+                                      "within_head_spread_mean": round(float(np.ptp((split_end - start).reshape(Z * Y, X), axis=1).mean()) / 1e3, 2)},
+            "smid_note": "CTA order x fastest: split, kv-head, sequence"}
 
 
 def run_timeline() -> None:

@@ -238,11 +238,32 @@ __device__ __forceinline__ uint32_t tag_entry(uint32_t tb) {
   return sel | ((n4 + 32u * rsv) << 16) | (nr << 24);
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
 // The four escape bytes starting at escape offset `off` (clamped into the escape area).
 __device__ __forceinline__ uint32_t escape_window(const uint8_t* img, int off) {
   off = min(off, kEscCap);
-  const uint32_t* ew = reinterpret_cast<const uint32_t*>(img + kOffEsc);
-  const uint32_t w0 = ew[off >> 2], w1 = ew[(off >> 2) + 1];
+  const uint32_t a = smem_addr(img) + kOffEsc + 4 * (off >> 2);
+  const uint32_t w0 = lds32(a), w1 = lds32(a + 4);
   return __funnelshift_r(w0, w1, 8 * (off & 3));
 }
 
@@ -253,15 +274,16 @@ __device__ __forceinline__ uint32_t escape_window(const uint8_t* img, int off) {
 // A raw group comes out right when its base3 words hold its exponents (raw_bases).
 __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t tb, uint32_t x, const uint32_t b3[8],
                                             const uint32_t b4[8], const uint2* lut, uint32_t o[16]) {
-  const uint32_t* cw = reinterpret_cast<const uint32_t*>(img + kOffCode);
-  const uint32_t W0 = cw[u], W1 = cw[256 + u], W2 = cw[512 + u];
-  const uint4 s0 = *reinterpret_cast<const uint4*>(img + 32 * u);
-  const uint4 s1 = *reinterpret_cast<const uint4*>(img + 32 * u + 16);
+  const uint32_t ib = smem_addr(img);
+  const uint32_t W0 = lds32(ib + kOffCode + 4 * u), W1 = lds32(ib + kOffCode + 1024 + 4 * u);
+  const uint32_t W2 = lds32(ib + kOffCode + 2048 + 4 * u);
+  const uint4 s0 = lds128(ib + 32 * u), s1 = lds128(ib + 32 * u + 16);
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     uint32_t c[4];
     extract_codes(hh ? W1 : W0, W2, hh, c);
-    const uint2 sa = lut[(x >> (16 * hh)) & 0xFFu], sb = lut[(x >> (16 * hh + 8)) & 0xFFu];
+    const uint32_t lb = smem_addr(lut);
+    const uint2 sa = lds64(lb + 8 * ((x >> (16 * hh)) & 0xFFu)), sb = lds64(lb + 8 * ((x >> (16 * hh + 8)) & 0xFFu));
     const uint32_t fa = (tb >> (4 * hh)) & 1u, fb = (tb >> (4 * hh + 2)) & 1u;  // 4-bit flags of the two groups
     uint32_t e[4];
 #pragma unroll
@@ -283,14 +305,24 @@ __device__ __forceinline__ void decode_unit(const uint8_t* img, int u, uint32_t 
 // each raw group start at escape offset `oraw` (clamped into the area); b3: the unit's base3 words, those of
 // its raw groups replaced.
 __device__ __forceinline__ void raw_bases(const uint8_t* img, uint32_t tb, int oraw, uint32_t b3[8]) {
+  // one pass per raw group of this lane (bit 2gi of m set for raw group gi), not per group position
+  uint32_t m = (tb >> 1) & ~tb & 0x55u;
+#pragma unroll 1
+  while (m != 0u) {
+    const int bit = __ffs(m) - 1;
+    m &= m - 1u;
+    const int at = kOffEsc + min(oraw, kEscCap - 8);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(img + (at & ~3));
+    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], sh = 8u * static_cast<uint32_t>(at & 3);
+    const uint32_t x0 = __funnelshift_r(w0, w1, sh), x1 = __funnelshift_r(w1, w2, sh);
 #pragma unroll
-  for (int gi = 0; gi < 4; ++gi) {
-    if (((tb >> (2 * gi)) & 3u) == 2u) {
-      const int at = kOffEsc + min(oraw, kEscCap - 8);
-      b3[2 * gi] = load_u32_any(img, at);
-      b3[2 * gi + 1] = load_u32_any(img, at + 4);
-      oraw += 8;
+    for (int g = 0; g < 4; ++g) {
+      if (bit == 2 * g) {
+        b3[2 * g] = x0;
+        b3[2 * g + 1] = x1;
+      }
     }
+    oraw += 8;
   }
 }
 
@@ -322,8 +354,9 @@ __device__ __forceinline__ void tile_units(const AttnArgs& a, const Smem& sm, co
   if (mode == GAAC_MODE_SLOT) {
     const uint16_t* dir = reinterpret_cast<const uint16_t*>(img + kOffDir);
     const uint32_t d0 = w ? dir[2 * w - 1] : 0u, dA = dir[2 * w], dB = dir[2 * w + 1], d7 = dir[7];
-    const uint32_t tbA = img[kOffTag + uA], tbB = img[kOffTag + uB];
-    const uint32_t teA = sm.tagl[tbA], teB = sm.tagl[tbB];
+    const uint32_t ib = smem_addr(img), tl = smem_addr(sm.tagl);
+    const uint32_t tbA = lds8(ib + kOffTag + uA), tbB = lds8(ib + kOffTag + uB);
+    const uint32_t teA = lds32(tl + 4 * tbA), teB = lds32(tl + 4 * tbB);
     const uint32_t cnt = __byte_perm(teA, teB, 0x7362);  // 4-bit A, 4-bit B, raw A, raw B
     const uint32_t incl = warp_incl_scan(cnt, lane);
     const uint32_t tot = __shfl_sync(kFull, incl, 31), ex = incl - cnt;
