@@ -70,6 +70,7 @@ constexpr int kAttThreads = kCWarps * 32;
 // (two half-heads).  Block j of a split uses stage j % depth.
 template <int KH>
 constexpr int stages_of() { return KH == 1 ? 6 : 4; }
+
 constexpr int kCtasPerSm = 1;
 constexpr int kRPad = 8;                          // query heads per kv-head in the MMA rows
 constexpr int kPartFloats = 2 * kRPad + kRPad * kD;
@@ -86,6 +87,10 @@ struct StageMeta {
 template <int NH, int KH>
 struct AttSmem {
   static constexpr int kStages = stages_of<KH>();
+  // Block j uses stage j % kStages and is read by group j % kGroups.  The depth must be a multiple of the
+  // group count, so that one group reads every block of a stage, in order: a group then never waits on a
+  // stage whose previous phase has not completed (a parity wait would take that phase for done).
+  static_assert(kStages % kGroups == 0, "each stage must belong to one warp group");
   static constexpr int kPairs = NH > KH ? kCWarps : 1;  // score mailboxes (cluster pairs only)
   alignas(128) uint8_t stage[kStages][KH + 1][kRawBytes];  // K half-head images, then the V image
   uint2 lut[256];                 // escape byte -> bit 3 spread into the byte lanes of two exponent words
