@@ -30,6 +30,21 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_timeline_only_in_the_instrumented_build(lib):
+    """gaac_timeline_fetch (include/gaac_timeline.h) exists only in the library built with the timeline; the
+    default library carries no instrumentation.  With a NULL destination it reports the record sizes without
+    touching a device."""
+    from lossless_compressed_kv_gaac_gb300 import build
+
+    assert not hasattr(lib, "gaac_timeline_fetch")
+    tl = ctypes.CDLL(build.build(timeline=True))
+    tl.gaac_timeline_fetch.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p]
+    cb, nc, nb = ctypes.c_size_t(), ctypes.c_int(), ctypes.c_int()
+    assert tl.gaac_timeline_fetch(None, 0, ctypes.byref(cb), ctypes.byref(nc), ctypes.byref(nb)) == 0
+    assert cb.value == 8 * (4 + 4 * nb.value) and nc.value >= 152
+
+
 def test_host_helpers(lib):
     lib.gaac_strerror.restype = ctypes.c_char_p
     assert lib.gaac_strerror(0) == b"ok"
