@@ -38,10 +38,9 @@ struct EncShared : EncCommon {
 };
 
 // The block encoder: the tile token-major with padded rows (filled by
-// asynchronous copies), and V rearranged into storage order.
+// asynchronous copies); a V tile is then rearranged into storage order in place.
 struct EncBlockShared : EncCommon {
   alignas(16) uint16_t raw[kLogicalElems];
-  alignas(16) uint16_t vtile[kTile];
 };
 
 // Token of storage element s (format v3).
@@ -57,7 +56,21 @@ __device__ __forceinline__ void v_pair_slice(int tid, int& t, int& p) {
   p = ((l >> 2) & 1) | (((w >> 2) & 1) << 1);
 }
 
-// Stores channels 32p .. 32p+31 of token t (x[i] = channels 32p + 8i .. + 7) into a V tile in storage order.
+// 16-byte chunk positions of the block encoder's staged tile.  A unit's four
+// chunks are read by one thread, a warp's 8 threads of one shared-memory
+// phase taking 8 consecutive units; XOR-ing each unit's chunk index with a
+// function of the unit puts those 8 reads in 8 distinct bank groups.
+//  V (storage order, 64-byte units): chunk j of unit u lies at j ^ ((u >> 1) & 3).
+//  K (token-major rows of kLogicalStride): chunk c of a row (channels 8c ..
+//    8c+7) lies at c ^ ((c >> 2) & 2), i.e. unit u's chunk j at j ^ (u & 2).
+//    (A V tile's token-major rows, read once by the rearrangement, stay plain.)
+__device__ __forceinline__ int v_chunk_swz(int u) { return (u >> 1) & 3; }
+__device__ __forceinline__ int k_chunk_swz(int u) { return u & 2; }
+__device__ __forceinline__ int k_row_chunk(int c) { return c ^ ((c >> 2) & 2); }
+
+// Stores channels 32p .. 32p+31 of token t (x[i] = channels 32p + 8i .. + 7) into a V tile in storage order
+// (kSwz: with the block encoder's chunk swizzle).
+template <bool kSwz = false>
 __device__ __forceinline__ void store_v_pairs(uint16_t* tile, int t, int p, const uint4 x[4]) {
   // word index of storage element v_storage_index(t, 32p + 16m + j) / 2 = base + 64j + 4m (j < 8)
   const int base = 1024 * (t >> 4) + 512 * (p >> 1) + 16 * ((t >> 1) & 3) + 8 * (p & 1) + (t & 1) + 2 * ((t >> 3) & 1);
@@ -68,8 +81,13 @@ __device__ __forceinline__ void store_v_pairs(uint16_t* tile, int t, int p, cons
     const uint32_t bw[4] = {x[2 * m + 1].x, x[2 * m + 1].y, x[2 * m + 1].z, x[2 * m + 1].w};  // c + 8
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      tw[base + 64 * (2 * i) + 4 * m] = __byte_perm(aw[i], bw[i], 0x5410);
-      tw[base + 64 * (2 * i + 1) + 4 * m] = __byte_perm(aw[i], bw[i], 0x7632);
+      int w0 = base + 64 * (2 * i) + 4 * m, w1 = base + 64 * (2 * i + 1) + 4 * m;
+      if (kSwz) {  // word w: unit w >> 4, chunk (w >> 2) & 3
+        w0 ^= v_chunk_swz(w0 >> 4) << 2;
+        w1 ^= v_chunk_swz(w1 >> 4) << 2;
+      }
+      tw[w0] = __byte_perm(aw[i], bw[i], 0x5410);
+      tw[w1] = __byte_perm(aw[i], bw[i], 0x7632);
     }
   }
 }
@@ -105,15 +123,18 @@ __device__ __forceinline__ void stage_tile_enc(uint16_t* tile, const uint16_t* s
 }
 
 // Exponent bytes of four BF16 values (w0 = elements 0, 1; w1 = elements 2, 3):
-// byte L = exponent of element L.
+// byte L = exponent of element L.  Shifting a word of two BF16 values right by
+// 7 puts their exponents in bytes 0 and 2.
 __device__ __forceinline__ uint32_t exponent_word(uint32_t w0, uint32_t w1) {
-  const uint32_t lo = __byte_perm(w0, w1, 0x6420), hi = __byte_perm(w0, w1, 0x7531);
-  return ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
+  return __byte_perm(w0 >> 7, w1 >> 7, 0x6420);
 }
 
-// The 4-bit escape nibble of a word of 4-bit offsets: bit L = bit 3 of byte L.
-__device__ __forceinline__ uint32_t escape_nibble(uint32_t d4) {
-  return (((d4 >> 3) & 0x01010101u) * 0x01020408u) >> 24;
+// The escape byte of a 4-bit group from its two words of 4-bit offsets: bit L
+// (bit 4 + L) = bit 3 of byte L of d4a (d4b).  Multiplying the four masked bits
+// 3 + 8L by 2^25 + 2^18 + 2^11 + 2^4 lands bit L at 28 + L; every other product
+// term stays below bit 24 or leaves the word, so nothing carries into 24..31.
+__device__ __forceinline__ uint32_t escape_byte(uint32_t d4a, uint32_t d4b) {
+  return (((d4a & 0x08080808u) * 0x02040810u) >> 28) | (((d4b & 0x08080808u) * 0x02040810u) >> 24);
 }
 
 // The group loop element by element (open tiles, whose absent elements take no
@@ -126,7 +147,7 @@ struct UnitCodes {
 
 template <bool kOpen>
 __device__ __noinline__ void encode_groups_elementwise(const uint16_t* unit, int kind, int u, const EncCommon* sh,
-                                                       int cls, int n_present, UnitCodes* out) {
+                                                       int cls, int n_present, int sw, UnitCodes* out) {
   const uint4* src = reinterpret_cast<const uint4*>(unit);
   uint32_t W[3] = {0, 0, 0};
   uint32_t esc4 = 0, tagbyte = 0, counts = 0;
@@ -136,7 +157,7 @@ __device__ __noinline__ void encode_groups_elementwise(const uint16_t* unit, int
     int e[8], b3[8], b4[8];
     bool pres[8];
     bool fits3 = true, fits4 = true;
-    const uint4 gq = src[gi];  // the group's 8 values
+    const uint4 gq = src[gi ^ sw];  // the group's 8 values
     const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
     const uint32_t b3q[2] = {sh->vtab[0][cls][2 * gi], sh->vtab[0][cls][2 * gi + 1]};  // four bases per word
     const uint32_t b4q[2] = {sh->vtab[1][cls][2 * gi], sh->vtab[1][cls][2 * gi + 1]};
@@ -195,6 +216,31 @@ __device__ __noinline__ void encode_groups_elementwise(const uint16_t* unit, int
   out->nraw = nraw;
 }
 
+// The per-CTA tables of encode_tile_cta: the base words of the unit classes
+// (V: the 16 classes of v_unit_class; K: class u % 4, element 4k+L of unit u
+// being channel 32(u%4) + 4k + L) and the statistics counter.  Returns whether
+// one of this thread's bases lies outside the calibrated ranges (base3 <= 248,
+// base4 <= 240), for which a word subtraction decides a group's fit exactly
+// (the tile then takes the element-by-element path).  A barrier must follow
+// before the tables are read.
+__device__ __forceinline__ bool base_tables(EncCommon* sh, int kind, const uint8_t* __restrict__ b3g,
+                                            const uint8_t* __restrict__ b4g, int u) {
+  if (u == 0) sh->mode_counts[0] = 0;
+  if (kind == 1) {
+    fill_v_base_table(sh->vtab, b3g, b4g, u);
+  } else if (u < 64) {
+    const int which = u >> 5, c = (u >> 3) & 3, k = u & 7;
+    sh->vtab[which][c][k] = *reinterpret_cast<const uint32_t*>((which ? b4g : b3g) + 32 * c + 4 * k);
+  }
+  bool odd_base = false;
+  if (u < kD / 4) {
+    const uint32_t w3 = reinterpret_cast<const uint32_t*>(b3g)[u], w4 = reinterpret_cast<const uint32_t*>(b4g)[u];
+#pragma unroll
+    for (int L = 0; L < 4; ++L) odd_base = odd_base || ((w3 >> (8 * L)) & 0xFFu) > 248u || ((w4 >> (8 * L)) & 0xFFu) > 240u;
+  }
+  return odd_base;
+}
+
 // Encodes a staged tile into `slot` (global, 16-byte aligned) unless its
 // escape stream exceeds the capacity.  `unit`: this thread's 32 values (code
 // unit u = threadIdx.x, storage elements 32u .. 32u+31; 16-byte aligned).  Returns the escape length, or -1 when
@@ -206,32 +252,19 @@ __device__ __noinline__ void encode_groups_elementwise(const uint16_t* unit, int
 // hold zero there); they take no part in their group's mode, and their codes and
 // escape bits are zero.  kOpen = false compiles the sealed-tile encoder
 // (n_present is then ignored: every token present).
+//
+// odd < 0: the routine builds the base tables itself (base_tables); odd = 0 or
+// 1: the caller built them (and put a barrier after) and passes whether any
+// base lies outside the calibrated ranges.
 template <bool kOpen>
 __device__ __noinline__ int encode_tile_cta(EncCommon* sh, const uint16_t* unit, int kind,
                                            const uint8_t* __restrict__ b3g, const uint8_t* __restrict__ b4g,
-                                           uint8_t* __restrict__ slot, gaac_stats* stats, int n_present = kBlock) {
+                                           uint8_t* __restrict__ slot, gaac_stats* stats, int n_present = kBlock,
+                                           int odd = -1, int sw = 0) {
   const int u = threadIdx.x;
   const int lane = u & 31, warp = u >> 5;
   const uint4* src = reinterpret_cast<const uint4*>(unit);  // the unit's 32 values, 4 quads of 8
-  if (u == 0) sh->mode_counts[0] = 0;
-  // Base words by unit class: V, the 16 classes of v_unit_class; K, class u % 4
-  // (element 4k+L of unit u is channel 32(u%4) + 4k + L).  kind is CTA-uniform.
-  if (kind == 1) {
-    fill_v_base_table(sh->vtab, b3g, b4g, u);
-  } else if (u < 64) {
-    const int which = u >> 5, c = (u >> 3) & 3, k = u & 7;
-    sh->vtab[which][c][k] = *reinterpret_cast<const uint32_t*>((which ? b4g : b3g) + 32 * c + 4 * k);
-  }
-  // Calibrated bases lie in [0, 248] (base3) and [0, 240] (base4); for those a
-  // word subtraction decides a group's fit exactly (below).  Other bases take
-  // the element-by-element path.
-  bool odd_base = false;
-  if (u < kD / 4) {
-    const uint32_t w3 = reinterpret_cast<const uint32_t*>(b3g)[u], w4 = reinterpret_cast<const uint32_t*>(b4g)[u];
-#pragma unroll
-    for (int L = 0; L < 4; ++L) odd_base = odd_base || ((w3 >> (8 * L)) & 0xFFu) > 248u || ((w4 >> (8 * L)) & 0xFFu) > 240u;
-  }
-  const bool any_odd = __syncthreads_or(odd_base) != 0;  // also orders the V table's writes before its reads
+  const bool any_odd = odd >= 0 ? odd != 0 : __syncthreads_or(base_tables(sh, kind, b3g, b4g, u)) != 0;
   const bool word_fit = !kOpen && !any_odd;
   const int cls = kind == 0 ? (u & 3) : v_unit_class(u);
 
@@ -250,7 +283,7 @@ __device__ __noinline__ int encode_tile_cta(EncCommon* sh, const uint16_t* unit,
     // with base4 <= 240.  In a group that fits, D holds the offsets themselves.
 #pragma unroll
     for (int gi = 0; gi < 4; ++gi) {
-      const uint4 gq = src[gi];  // the group's 8 values
+      const uint4 gq = src[gi ^ sw];  // the group's 8 values
       const uint32_t b3q[2] = {sh->vtab[0][cls][2 * gi], sh->vtab[0][cls][2 * gi + 1]};
       const uint32_t b4q[2] = {sh->vtab[1][cls][2 * gi], sh->vtab[1][cls][2 * gi + 1]};
       const uint32_t E0 = exponent_word(gq.x, gq.y), E1 = exponent_word(gq.z, gq.w);
@@ -273,14 +306,14 @@ __device__ __noinline__ int encode_tile_cta(EncCommon* sh, const uint16_t* unit,
         W[h] |= (c1 & 0x03030303u) << 6;
       }
       if (mode == 1u) {
-        esc4 |= (escape_nibble(d4a) | (escape_nibble(d4b) << 4)) << (8 * n4);
+        esc4 |= escape_byte(d4a, d4b) << (8 * n4);
         n4 += 1;
       }
       if (mode == 2u) nraw += 1;
     }
   } else {
     UnitCodes uc;
-    encode_groups_elementwise<kOpen>(unit, kind, u, sh, cls, n_present, &uc);
+    encode_groups_elementwise<kOpen>(unit, kind, u, sh, cls, n_present, sw, &uc);
     W[0] = uc.W[0];
     W[1] = uc.W[1];
     W[2] = uc.W[2];
@@ -320,11 +353,12 @@ __device__ __noinline__ int encode_tile_cta(EncCommon* sh, const uint16_t* unit,
   uint32_t smb[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {  // word j: elements 4j..4j+3 from two staged words
-    const uint4 gq = src[j >> 1];
+    const uint4 gq = src[(j >> 1) ^ sw];
     const uint32_t w0 = (j & 1) ? gq.z : gq.x, w1 = (j & 1) ? gq.w : gq.y;
     // byte L: the mantissa (low byte, bits 0-6) of element L and the sign (high byte, bit 7) of element (L+3)%4
-    const uint32_t lo = __byte_perm(w0, w1, 0x6420), hi = __byte_perm(w0, w1, 0x7531);
-    smb[j] = (lo & 0x7F7F7F7Fu) | (__byte_perm(hi, hi, 0x2103) & 0x80808080u);
+    // mantissas from the low bytes of the four values (bytes 0, 2 of each word); the sign bytes (high bytes
+    // 1, 3) of elements 3, 0, 1, 2 into bytes 0-3
+    smb[j] = (__byte_perm(w0, w1, 0x6420) & 0x7F7F7F7Fu) | (__byte_perm(w0, w1, 0x5317) & 0x80808080u);
   }
   uint4* smdst = reinterpret_cast<uint4*>(slot + 32 * u);
   smdst[0] = make_uint4(smb[0], smb[1], smb[2], smb[3]);
@@ -343,7 +377,7 @@ __device__ __noinline__ int encode_tile_cta(EncCommon* sh, const uint16_t* unit,
       if (((tagbyte >> (2 * gi)) & 3u) != 2u) continue;
 #pragma unroll
       for (int j = 0; j < 8; ++j)  // the exponent of element 8gi + j (zero where absent)
-        escp[r + j] = static_cast<uint8_t>(unit[8 * gi + j] >> 7);
+        escp[r + j] = static_cast<uint8_t>(unit[8 * (gi ^ sw) + j] >> 7);
       r += 8;
     }
   }
@@ -427,28 +461,15 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Work item i of the block encoder: x = i % (2 n_kv_heads) = h*2 + kind, then
-// block, then sequence.  nv = tokens of the block present (0: the block is past
-// the sequence; -1: the sequence length is invalid).
+// Work item (x, blk, b) of the block encoder, the CTA's grid coordinates: x =
+// h*2 + kind, block blk of sequence b.  nv = tokens of the block present (0:
+// the block is past the sequence; -1: the sequence length is invalid).
 struct BlockItem {
   int b, blk, h, kind, nv;
 };
 
-__device__ __forceinline__ BlockItem block_item(const EncodeArgs& a, int64_t i) {
+__device__ __forceinline__ BlockItem block_item(const EncodeArgs& a, uint32_t x, uint32_t blk, uint32_t b) {
   BlockItem it;
-  const uint32_t two_h = 2u * static_cast<uint32_t>(a.n_kv_heads), mb = static_cast<uint32_t>(a.max_blocks);
-  uint32_t x, blk, b;
-  if (i <= 0xFFFFFFFFll) {  // 32-bit division (every realistic cache)
-    const uint32_t i32 = static_cast<uint32_t>(i), r = i32 / two_h;
-    x = i32 - r * two_h;
-    b = r / mb;
-    blk = r - b * mb;
-  } else {
-    const int64_t r = i / two_h;
-    x = static_cast<uint32_t>(i - r * two_h);
-    b = static_cast<uint32_t>(r / mb);
-    blk = static_cast<uint32_t>(r - static_cast<int64_t>(b) * mb);
-  }
   it.h = static_cast<int>(x >> 1);
   it.kind = static_cast<int>(x & 1u);
   it.blk = static_cast<int>(blk);
@@ -471,16 +492,29 @@ __device__ __forceinline__ void prefetch_block(const EncodeArgs& a, const BlockI
     for (int j = 0; j < 4; ++j) {
       const int q = tid + kEncThreads * j, t = q >> 4, col = 8 * (q & 15);
       const bool in = t < it.nv;
-      cp_async16(buf + t * kLogicalStride + col, in ? src + t * a.tok_stride + col : src, in ? 16u : 0u);
+      const int at = it.kind == 0 ? k_row_chunk(q & 15) : (q & 15);  // K rows swizzled, V rows plain
+      cp_async16(buf + t * kLogicalStride + 8 * at, in ? src + t * a.tok_stride + col : src, in ? 16u : 0u);
     }
   }
   cp_async_commit();
 }
 
-// Encodes an item, staged in `buf`; all threads call it.
+// Table entry of an item.
+__device__ __forceinline__ size_t item_entry(const EncodeArgs& a, const BlockItem& it) {
+  return ((static_cast<size_t>(it.b) * a.max_blocks + it.blk) * a.n_kv_heads + it.h) * 2 + it.kind;
+}
+
+// Whether an item is encoded into its slot (a full block, or the open last block kept in its slot).
+__device__ __forceinline__ bool item_to_slot(const EncodeArgs& a, const BlockItem& it) {
+  return it.nv > 0 && (it.nv == kBlock || (a.flags & GAAC_OPEN_COMPRESSED)) && a.slot_ids != nullptr;
+}
+
+// Encodes an item, staged in `buf`; all threads call it.  The base tables are
+// built (any_odd: a base outside the calibrated ranges) and, for an item going
+// to a slot, slot_id is its slot.
 __device__ __forceinline__ void encode_block_item(const EncodeArgs& a, const BlockItem& it, EncBlockShared& sh,
-                                                  const uint16_t* buf, int tid) {
-  const size_t eidx = ((static_cast<size_t>(it.b) * a.max_blocks + it.blk) * a.n_kv_heads + it.h) * 2 + it.kind;
+                                                  const uint16_t* buf, int tid, size_t eidx, uint32_t slot_id,
+                                                  bool any_odd) {
   if (it.nv <= 0) {
     if (tid == 0) {
       a.table[eidx] = make_entry(0, 0, GAAC_MODE_NONE, 0);
@@ -490,6 +524,7 @@ __device__ __forceinline__ void encode_block_item(const EncodeArgs& a, const Blo
   }
   const int kind = it.kind, h = it.h, nv = it.nv;
   const uint16_t* unit;
+  int sw;  // the unit's chunk swizzle
   if (kind == 1) {  // V: rearrange the token-major tile into storage order
     int t, p;
     v_pair_slice(tid, t, p);
@@ -497,25 +532,26 @@ __device__ __forceinline__ void encode_block_item(const EncodeArgs& a, const Blo
     const uint4* row = reinterpret_cast<const uint4*>(buf + t * kLogicalStride + 32 * p);
 #pragma unroll
     for (int j = 0; j < 4; ++j) x[j] = row[j];
-    store_v_pairs(sh.vtile, t, p, x);
+    __syncthreads();  // every thread holds its slice: the buffer takes storage order in place
+    store_v_pairs<true>(sh.raw, t, p, x);
     __syncthreads();
-    unit = sh.vtile + 32 * tid;
+    unit = sh.raw + 32 * tid;
+    sw = v_chunk_swz(tid);
   } else {  // K: storage order is token-major; unit u = token u/4, channels 32(u%4) .. +31
     unit = buf + (tid >> 2) * kLogicalStride + 32 * (tid & 3);
+    sw = k_chunk_swz(tid);
   }
   const uint8_t* b3 = a.base3 + (kind * a.n_kv_heads + h) * kD;
   const uint8_t* b4 = a.base4 + (kind * a.n_kv_heads + h) * kD;
-  if ((nv == kBlock || (a.flags & GAAC_OPEN_COMPRESSED)) && a.slot_ids != nullptr) {
-    // a full block, or the open last block kept in its slot
-    const uint32_t slot_id = a.slot_ids[eidx];
+  if (item_to_slot(a, it)) {
     uint8_t* slot = nullptr;
     if (static_cast<int64_t>(slot_id) < a.pools.n_slots) {
       slot = a.pools.slot_pool + static_cast<size_t>(slot_id) * kSlot;
     } else if (tid == 0) {
       report(a.status, GAAC_EPOOL);
     }
-    const int esc = nv == kBlock ? encode_tile_cta<false>(&sh, unit, kind, b3, b4, slot, a.stats)
-                                 : encode_tile_cta<true>(&sh, unit, kind, b3, b4, slot, nullptr, nv);
+    const int esc = nv == kBlock ? encode_tile_cta<false>(&sh, unit, kind, b3, b4, slot, a.stats, kBlock, any_odd, sw)
+                                 : encode_tile_cta<true>(&sh, unit, kind, b3, b4, slot, nullptr, nv, any_odd, sw);
     if (esc >= 0) {
       if (tid == 0) a.table[eidx] = make_entry(slot_id, esc, GAAC_MODE_SLOT, nv);
       return;
@@ -536,7 +572,8 @@ __device__ __forceinline__ void encode_block_item(const EncodeArgs& a, const Blo
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int q = tid + kEncThreads * j;  // 16-byte chunk q: storage elements 8q .. 8q+7
-    const uint16_t* from = kind == 1 ? sh.vtile + 8 * q : buf + (q >> 4) * kLogicalStride + 8 * (q & 15);
+    const uint16_t* from = kind == 1 ? buf + 8 * (q ^ v_chunk_swz(q >> 2))
+                                     : buf + (q >> 4) * kLogicalStride + 8 * k_row_chunk(q & 15);
     dst[q] = *reinterpret_cast<const uint4*>(from);
   }
   if (tid == 0) {
@@ -549,17 +586,20 @@ __device__ __forceinline__ void encode_block_item(const EncodeArgs& a, const Blo
 // One CTA per item.  (A persistent variant that copied the next item's tile
 // while encoding the current one was slower: the scheduler already overlaps
 // the copies of some CTAs with the encoding of others.)
-__global__ void __launch_bounds__(kEncThreads, 6) encode_blocks_kernel(EncodeArgs a, int64_t n_items) {
+__global__ void __launch_bounds__(kEncThreads, 7) encode_blocks_kernel(EncodeArgs a) {
   extern __shared__ __align__(16) uint8_t enc_smem[];
   EncBlockShared& sh = *reinterpret_cast<EncBlockShared*>(enc_smem);
   const int tid = threadIdx.x;
-  const int64_t i = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-  if (i >= n_items) return;
-  const BlockItem it = block_item(a, i);
+  const BlockItem it = block_item(a, blockIdx.x, blockIdx.y, blockIdx.z);
   prefetch_block(a, it, sh.raw, tid);
+  // while the copies land: the item's slot and the base tables of its (kind, head)
+  const size_t eidx = item_entry(a, it);
+  const uint32_t slot_id = item_to_slot(a, it) ? a.slot_ids[eidx] : 0u;
+  const int row = (it.kind * a.n_kv_heads + it.h) * kD;
+  const bool odd = base_tables(&sh, it.kind, a.base3 + row, a.base4 + row, tid);
   cp_async_wait<0>();
-  __syncthreads();
-  encode_block_item(a, it, sh, sh.raw, tid);
+  const bool any_odd = __syncthreads_or(odd) != 0;
+  encode_block_item(a, it, sh, sh.raw, tid, eidx, slot_id, any_odd);
 }
 
 // ------------------------------------------------ open block, one token --
@@ -1159,10 +1199,9 @@ extern "C" int gaac_encode_blocks_ex(const uint16_t* k, const uint16_t* v, int64
   EncodeArgs a{k, v, seq_stride, tok_stride, n_tok, seq_lens, n_kv_heads, max_blocks, base3, base4, table, slot_ids,
                *pools, stats, flags, d_status};
   if (!prepare_encode_blocks()) return GAAC_ECUDA;
-  const int64_t n_items = static_cast<int64_t>(2 * n_kv_heads) * max_blocks * batch;
-  const int64_t gx = n_items < 0x7FFFFFFF ? n_items : 0x7FFFFFFF;  // then ceil(n_items / gx) <= 4096 rows
-  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>((n_items + gx - 1) / gx));
-  encode_blocks_kernel<<<grid, kEncThreads, sizeof(EncBlockShared), static_cast<cudaStream_t>(stream)>>>(a, n_items);
+  // one CTA per (h*2 + kind, block, sequence): the argument checks above keep every dimension in range
+  const dim3 grid(static_cast<unsigned>(2 * n_kv_heads), static_cast<unsigned>(max_blocks), static_cast<unsigned>(batch));
+  encode_blocks_kernel<<<grid, kEncThreads, sizeof(EncBlockShared), static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? GAAC_OK : GAAC_ECUDA;
 }
 
