@@ -74,6 +74,11 @@ template <bool kSwz = false>
 __device__ __forceinline__ void store_v_pairs(uint16_t* tile, int t, int p, const uint4 x[4]) {
   // word index of storage element v_storage_index(t, 32p + 16m + j) / 2 = base + 64j + 4m (j < 8)
   const int base = 1024 * (t >> 4) + 512 * (p >> 1) + 16 * ((t >> 1) & 3) + 8 * (p & 1) + (t & 1) + 2 * ((t >> 3) & 1);
+  // Bit 2 of base is clear and base + 4m stays below the next multiple of 32, so base + 4m = base ^ 4m; the
+  // offsets 128i leave bits 0-6 alone.  The swizzle reads unit bits 5-6, the same for every m and i, so it
+  // is one XOR on base (words 64j, j even) and one on base + 64 (j odd).
+  const int e0 = kSwz ? base ^ (v_chunk_swz(base >> 4) << 2) : base;
+  const int e1 = kSwz ? (base + 64) ^ (v_chunk_swz((base + 64) >> 4) << 2) : base + 64;
   uint32_t* tw = reinterpret_cast<uint32_t*>(tile);
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
@@ -81,13 +86,8 @@ __device__ __forceinline__ void store_v_pairs(uint16_t* tile, int t, int p, cons
     const uint32_t bw[4] = {x[2 * m + 1].x, x[2 * m + 1].y, x[2 * m + 1].z, x[2 * m + 1].w};  // c + 8
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      int w0 = base + 64 * (2 * i) + 4 * m, w1 = base + 64 * (2 * i + 1) + 4 * m;
-      if (kSwz) {  // word w: unit w >> 4, chunk (w >> 2) & 3
-        w0 ^= v_chunk_swz(w0 >> 4) << 2;
-        w1 ^= v_chunk_swz(w1 >> 4) << 2;
-      }
-      tw[w0] = __byte_perm(aw[i], bw[i], 0x5410);
-      tw[w1] = __byte_perm(aw[i], bw[i], 0x7632);
+      tw[(e0 ^ (4 * m)) + 128 * i] = __byte_perm(aw[i], bw[i], 0x5410);
+      tw[(e1 ^ (4 * m)) + 128 * i] = __byte_perm(aw[i], bw[i], 0x7632);
     }
   }
 }
