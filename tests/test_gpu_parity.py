@@ -73,6 +73,35 @@ def test_config0_encode_decompress_attention():
     assert st["groups0"] + st["groups1"] + st["groups2"] == 1024 * st["slot_tiles"]
 
 
+def test_block_encoder_out_of_range_bases():
+    """Bases above the calibrated ranges (base3 > 248 or base4 > 240; calibration never gives one) send a
+    head's tiles down the block encoder's element-by-element fit: every tile of those heads and of the others
+    must still equal the oracle's image, and the cache must decode and attend exactly as with calibrated
+    bases.  Ragged lengths put open tails (raw) beside sealed tiles."""
+    lens_v = [1024, 700, 65]
+    B, T, H = len(lens_v), 1024, 4
+    k, v = U.kv(0, 3, B, T, H)
+    lens = U.lens_tensor(lens_v)
+    c = LayerCache(B, H, T // 64, device=k.device)
+    c.calibrate(k[0, :512], v[0, :512])
+    c.base3[0, 0, 5] = 250  # K of head 0
+    c.base4[1, 1, 77] = 245  # V of head 1
+    c.base3[1, 3, 0] = 255  # V of head 3
+    c.encode(k, v, lens)
+    assert _status(c) == 0
+    b3, b4 = c.base3.cpu().numpy(), c.base4.cpu().numpy()
+    n = U.check_tiles(c, k, v, lens, b3=b3, b4=b4)
+    assert n["slot"] > 0 and n["raw"] >= 2 * H * 2  # the two ragged sequences' open tails
+    kd, vd = c.decompress(T)
+    for b, L in enumerate(lens_v):
+        assert torch.equal(kd[b, :L].view(torch.int16), k[b, :L].view(torch.int16))
+        assert torch.equal(vd[b, :L].view(torch.int16), v[b, :L].view(torch.int16))
+    q = W.make_q(0, 3, B, 16, device="cuda")
+    out = c.attention(q, 1 / np.sqrt(128))
+    assert _status(c) == 0
+    assert U.check_attention(out, q, k, v, lens, 1 / np.sqrt(128)).compared == B * 16
+
+
 @pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 8), (64, 8), (12, 4)])
 def test_ragged_lengths_and_gqa(hq, hkv):
     lens_v = [0, 1, 63, 64, 65, 700, 1024, 333]
