@@ -2,9 +2,11 @@
 // latency the GAAC page's section 4.3 / Figure 4 reports; used here for
 // bit-exact checks and the decode-bandwidth measurement).
 //
-// One CTA of 256 threads per tile; thread u decodes code unit u (32 storage
-// elements) with the same packed decoder the attention kernel uses, the tile
-// is assembled token-major in shared memory and written out row by row.
+// One CTA of 256 threads per tile.  The slot image's used bytes are staged in
+// shared memory with 16-byte asynchronous copies; thread u decodes code unit u
+// (32 storage elements) from it with the same packed decoder the attention
+// kernel uses; the tile is then assembled token-major in the same buffer and
+// written out row by row.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -29,9 +31,16 @@ struct DecompressArgs {
   int32_t* status;
 };
 
+// 16-byte asynchronous global -> shared copy.
+__device__ __forceinline__ void cp_async16_dec(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 // grid (2*n_kv_heads, max_blocks, batch): x = h*2 + kind.
 __global__ void __launch_bounds__(kDecThreads, 8) decompress_kernel(DecompressArgs a) {
-  __shared__ alignas(16) uint16_t logical[kLogicalElems];  // [t][c], padded rows
+  // the slot image's used bytes, then (after a barrier) the token-major tile [t][c] with padded rows
+  __shared__ alignas(16) uint16_t logical[kLogicalElems];
+  uint8_t* simg = reinterpret_cast<uint8_t*>(logical);
   __shared__ int word_prefix[65];
   __shared__ uint32_t vbt[2][16][8];  // V: base words of the unit classes
   const int h = blockIdx.x >> 1, kind = blockIdx.x & 1;
@@ -69,13 +78,20 @@ __global__ void __launch_bounds__(kDecThreads, 8) decompress_kernel(DecompressAr
     const uint8_t* slot = a.slot_pool + static_cast<size_t>(ent.index) * kSlot;
     const uint8_t* b3g = a.base3 + (kind * a.n_kv_heads + h) * kD;
     const uint8_t* b4g = a.base4 + (kind * a.n_kv_heads + h) * kD;
+    // The image's used bytes move to shared memory as 16-byte asynchronous copies while the tag prefix and
+    // the base table are built from global memory; the units then read the staged image.
+    const int n16 = (kOffEsc + ent.esc_len + 15) >> 4;
+    for (int q = tid; q < n16; q += kDecThreads) cp_async16_dec(simg + 16 * q, slot + 16 * q);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid < 32) slot_word_prefix(slot, tid, word_prefix);
     if (kind == 1) fill_v_base_table(vbt, b3g, b4g, tid);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
     const int cls = v_unit_class(u);
-    const bool bad = kind == 0 ? decode_slot_unit(slot, 0, u, b3g, b4g, ent.esc_len, word_prefix, pairs)
-                               : decode_slot_unit_w(slot, u, vbt[0][cls], vbt[1][cls], ent.esc_len, word_prefix, pairs);
+    const bool bad = kind == 0 ? decode_slot_unit(simg, 0, u, b3g, b4g, ent.esc_len, word_prefix, pairs)
+                               : decode_slot_unit_w(simg, u, vbt[0][cls], vbt[1][cls], ent.esc_len, word_prefix, pairs);
     if (bad) report(a.status, GAAC_EFORMAT);
+    __syncthreads();  // every unit has read the staged image
   }
   unit_to_logical(logical, kind, u, pairs);  // storage order -> token-major
   __syncthreads();
