@@ -376,7 +376,9 @@ __global__ void __launch_bounds__(kFp8Threads, 6) fp8_encode_kernel(Fp8Args a) {
 }
 
 __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, uint8_t* __restrict__ out) {
-  __shared__ alignas(16) uint8_t logical[kBlock * kFp8Stride];  // token-major, padded rows
+  // the staged slot image, then (after a barrier) the token-major tile with padded rows
+  __shared__ alignas(16) uint8_t logical[kBlock * kFp8Stride];
+  static_assert(kBlock * kFp8Stride >= 7936, "the buffer holds the larger FP8 slot image");
   __shared__ uint32_t vtab[2][16][8];  // V: base3 / base4 words of the 16 unit classes
   __shared__ int word_prefix[65];
   const int64_t tile = blockIdx.x;
@@ -389,8 +391,15 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, 
     return;
   }
   const Fp8Layout L = a.L;
-  const uint8_t* slot = a.slots + tile * L.slot;
-  const uint32_t* tagw = reinterpret_cast<const uint32_t*>(slot + L.off_tag);
+  const uint8_t* gslot = a.slots + tile * L.slot;
+  // The image's used bytes move to shared memory as 16-byte asynchronous copies, into the buffer that takes
+  // the token-major tile later; the tag prefix and the V base table are built from global memory meanwhile.
+  const int n16 = (L.off_esc + esc_len + 15) >> 4;
+  for (int q = u; q < n16; q += kFp8Threads)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(logical + 16 * q)), "l"(gslot + 16 * q)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  const uint32_t* tagw = reinterpret_cast<const uint32_t*>(gslot + L.off_tag);
   const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
   const uint8_t* b4g = a.base4 + static_cast<size_t>(row) * kD;
   if (kind == 1) fill_v_base_table(vtab, b3g, b4g, u);
@@ -411,9 +420,11 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, 
     word_prefix[u + 32] = tot0 + i1 - c1;
     if (u == 31) word_prefix[64] = tot0 + i1;
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
+  const uint8_t* slot = logical;  // the staged image
   const uint32_t tagbyte = slot[L.off_tag + u];
-  const uint32_t before = tagw[u >> 2] & ((1u << (8 * (u & 3))) - 1u);
+  const uint32_t before = reinterpret_cast<const uint32_t*>(slot + L.off_tag)[u >> 2] & ((1u << (8 * (u & 3))) - 1u);
   const int pre = word_prefix[u >> 2] + (n4_of(before) | (nraw_of(before) << 16));
   const int tot = word_prefix[64], tot4 = tot & 0xFFFF, totraw = tot >> 16;
   int o4 = pre & 0xFFFF, oraw = tot4 + 8 * (pre >> 16);
@@ -499,6 +510,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_decompress_kernel(Fp8Args a, 
     }
   }
   if (bad) report(a.status, GAAC_EFORMAT);
+  __syncthreads();  // every unit has read the staged image
   if (kind == 0) {  // token u/4, channels 32(u%4)..+31
     uint4* d = reinterpret_cast<uint4*>(logical + (u >> 2) * kFp8Stride + 32 * (u & 3));
     d[0] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
