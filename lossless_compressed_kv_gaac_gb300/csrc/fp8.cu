@@ -209,11 +209,19 @@ __global__ void __launch_bounds__(kFp8Threads, 6) fp8_encode_kernel(Fp8Args a) {
       d[0] = x0;
       d[1] = x1;
     } else {
-      const uint8_t* xb0 = reinterpret_cast<const uint8_t*>(&x0);
-      const uint8_t* xb1 = reinterpret_cast<const uint8_t*>(&x1);
-      const int t = u >> 2, c0 = 32 * (u & 3);
+      // Storage elements 2m' and 2m'+1 are channels c and c+8 of one token, so the thread's 32 channels
+      // 32p .. 32p+31 of token t form 16 byte pairs: channels 32p + 16m + j and + 8 (j < 8) at pair index
+      // v_storage_index(t, 32p + 16m + j) / 2 = base + 64j + 4m.
+      const int t = u >> 2, p = u & 3;
+      const int base = 1024 * (t >> 4) + 512 * (p >> 1) + 16 * ((t >> 1) & 3) + 8 * (p & 1) + (t & 1) + 2 * ((t >> 3) & 1);
+      uint16_t* sp = reinterpret_cast<uint16_t*>(seq) + base;
+      const uint32_t lo[2][2] = {{x0.x, x0.y}, {x1.x, x1.y}};  // [m][j / 4]: channels 16m + j
+      const uint32_t hi[2][2] = {{x0.z, x0.w}, {x1.z, x1.w}};  // the same + 8
 #pragma unroll
-      for (int i = 0; i < 32; ++i) seq[v_storage_index(t, c0 + i)] = i < 16 ? xb0[i] : xb1[i - 16];
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          sp[64 * j + 4 * m] = static_cast<uint16_t>(__byte_perm(lo[m][j >> 2], hi[m][j >> 2], 0x40 | (j & 3) | ((j & 3) << 4)));
     }
   }
   const uint8_t* b3g = a.base3 + static_cast<size_t>(row) * kD;
